@@ -1,0 +1,265 @@
+"""Pins for the CPU oracle: brute force, closed forms, invariants and the
+figures the pages print.  None of these compares the oracle with itself.
+
+Sources (web pages on multi-LoRA serving):
+  [Guide]    "Multi-LoRA batching and adapter paging"
+  [Concepts] "Serving Many LoRA Adapters"
+  [Handbook] "Serving multiple LoRAs: segmented matrix multiplies and adapter scheduling"
+  [Blog]     "Serving many LoRA adapters" (blog.ecitis.org)
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+from oracle import lora_ref as O
+from lora_serving_device_gb300 import workloads as W
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _gold(name):
+    with open(os.path.join(GOLD, name)) as f:
+        return json.load(f)
+
+
+# ----------------------------------------------------------------------------
+# brute force: the layer's definition with explicit scalar loops, tiny shapes
+# ----------------------------------------------------------------------------
+
+def brute_force_y(x, W0, A, B, scale, ids):
+    T, d_in = x.shape
+    d_out = W0.shape[1]
+    n_slots, _, r = A.shape
+    y = [[0.0] * d_out for _ in range(T)]
+    for t in range(T):
+        a = int(ids[t])
+        v = [0.0] * r
+        if 0 <= a < n_slots:
+            for q in range(r):
+                acc = 0.0
+                for k in range(d_in):
+                    acc += float(x[t, k]) * float(A[a, k, q])
+                v[q] = float(scale[a]) * acc
+        for n in range(d_out):
+            acc = 0.0
+            for k in range(d_in):
+                acc += float(x[t, k]) * float(W0[k, n])
+            if 0 <= a < n_slots:
+                for q in range(r):
+                    acc += v[q] * float(B[a, q, n])
+            y[t][n] = acc
+    return np.array(y)
+
+
+def _tiny(seed, T=7, d_in=12, d_out=10, r=3, n_slots=4, invalid=True):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((T, d_in))
+    W0 = rng.standard_normal((d_in, d_out))
+    A = rng.standard_normal((n_slots, d_in, r))
+    B = rng.standard_normal((n_slots, r, d_out))
+    scale = rng.uniform(0.5, 3.0, n_slots)
+    ids = rng.integers(-1, n_slots, T)
+    if invalid:
+        ids[0] = n_slots          # out of range -> base only
+        ids[-1] = -3              # below -1 -> base only
+    return x, W0, A, B, scale, ids
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_brute_force_tiny(seed):
+    x, W0, A, B, s, ids = _tiny(seed, T=1 + seed, d_in=4 + 2 * seed, d_out=3 + seed,
+                                r=1 + seed % 4, n_slots=1 + seed % 5)
+    ref = brute_force_y(x, W0, A, B, s, ids)
+    for fn in (O.lora_linear, O.lora_linear_gathered, O.lora_linear_segmented):
+        np.testing.assert_allclose(fn(x, W0, A, B, s, ids), ref, rtol=1e-12, atol=1e-12)
+
+
+def test_shrink_expand_brute_force():
+    x, W0, A, B, s, ids = _tiny(11)
+    v = O.shrink(x, A, s, ids)
+    for t in range(x.shape[0]):
+        a = ids[t]
+        for q in range(A.shape[2]):
+            want = 0.0
+            if 0 <= a < A.shape[0]:
+                want = s[a] * sum(x[t, k] * A[a, k, q] for k in range(x.shape[1]))
+            assert abs(v[t, q] - want) <= 1e-12 * (1 + abs(want))
+    d = O.expand(v, B, ids)
+    base = brute_force_y(x, W0, A, B, s, np.full_like(ids, -1))
+    full = brute_force_y(x, W0, A, B, s, ids)
+    np.testing.assert_allclose(d, full - base, rtol=1e-10, atol=1e-10)
+
+
+def test_brute_force_catches_planted_mistakes():
+    """The brute-force pin separates the oracle from plausible mistakes: a
+    dropped or doubled scale, A/B of the wrong adapter, -1 read as the last
+    adapter (negative indexing), the base term dropped."""
+    x, W0, A, B, s, ids = _tiny(3, T=8, invalid=False)
+    ids[2] = -1
+    ref = brute_force_y(x, W0, A, B, s, ids)
+    good = O.lora_linear(x, W0, A, B, s, ids)
+    np.testing.assert_allclose(good, ref, rtol=1e-12, atol=1e-12)
+    mutants = {
+        "scale dropped": O.lora_linear(x, W0, A, B, np.ones_like(s), ids),
+        "scale doubled": O.lora_linear(x, W0, A, B, 2 * s, ids),
+        "adapter off by one": O.lora_linear(x, W0, np.roll(A, 1, 0), np.roll(B, 1, 0), np.roll(s, 1), ids),
+        "-1 read as last adapter": O.lora_linear(x, W0, A, B, s, np.where(ids < 0, A.shape[0] - 1, ids)),
+        "base dropped": O.lora_linear(x, 0 * W0, A, B, s, ids),
+    }
+    for name, y in mutants.items():
+        assert not np.allclose(y, ref, rtol=1e-6, atol=1e-6), name
+
+
+# ----------------------------------------------------------------------------
+# closed forms and invariants the pages state
+# ----------------------------------------------------------------------------
+
+def test_merge_equivalence():
+    """[Blog, "Merge or keep separate"]: W' = W0 + (alpha/r) B A gives the same
+    output as the unmerged path; in row-vector form x (W0 + s A B)."""
+    x, W0, A, B, s, _ = _tiny(5, T=9, d_in=20, d_out=14, r=4, n_slots=3, invalid=False)
+    for a in range(3):
+        ids = np.full(x.shape[0], a)
+        Wm = O.merge(W0, A[a], B[a], s[a])
+        np.testing.assert_allclose(O.lora_linear(x, W0, A, B, s, ids), x @ Wm, rtol=1e-12, atol=1e-12)
+
+
+def test_base_only_rows_and_zero_B():
+    """Id -1 rows ([Blog, "Replay": "req C -> base only"]) and adapters with
+    B = 0 both give exactly x W0 ([Blog, "Low-rank structure and additivity"]:
+    the base output does not depend on the adapter)."""
+    x, W0, A, B, s, ids = _tiny(6, invalid=False)
+    base = x @ W0
+    y = O.lora_linear(x, W0, A, B, s, np.full_like(ids, -1))
+    np.testing.assert_array_equal(y, base)
+    y0 = O.lora_linear(x, W0, A, np.zeros_like(B), s, ids)
+    np.testing.assert_allclose(y0, base, rtol=0, atol=1e-13)
+
+
+def test_permutation_invariance():
+    """Additivity ([Blog, "Low-rank structure and additivity"]): each row's
+    output depends only on its own input and adapter, so shuffling the batch
+    (rows with their ids) shuffles the output identically."""
+    x, W0, A, B, s, ids = _tiny(7, T=16)
+    y = O.lora_linear(x, W0, A, B, s, ids)
+    p = np.random.default_rng(1).permutation(x.shape[0])
+    np.testing.assert_allclose(O.lora_linear(x[p], W0, A, B, s, ids[p]), y[p], rtol=1e-13, atol=1e-13)
+
+
+def test_one_hot_rows_closed_form():
+    """x_t = e_k picks row k: y_t = W0[k] + s A[a][k] B[a]."""
+    _, W0, A, B, s, _ = _tiny(8, invalid=False)
+    d_in = W0.shape[0]
+    x = np.eye(d_in)
+    for a in (-1, 0, 2):
+        y = O.lora_linear(x, W0, A, B, s, np.full(d_in, a))
+        want = W0 + (s[a] * (A[a] @ B[a]) if a >= 0 else 0.0)
+        np.testing.assert_allclose(y, want, rtol=1e-13, atol=1e-13)
+
+
+def test_rank_padding_exact():
+    """Zero-padding an adapter to the pool rank leaves the result unchanged
+    ([Concepts, "When It Falls Down"]; [Handbook, Exercise 2])."""
+    rng = np.random.default_rng(9)
+    x = rng.standard_normal((5, 24))
+    W0 = rng.standard_normal((24, 18))
+    A = rng.standard_normal((24, 8))
+    B = rng.standard_normal((8, 18))
+    Ap, Bp = O.pad_rank(A, B, 64)
+    ids = np.zeros(5, int)
+    y8 = O.lora_linear(x, W0, A[None], B[None], [2.0], ids)
+    y64 = O.lora_linear(x, W0, Ap[None], Bp[None], [2.0], ids)
+    np.testing.assert_allclose(y64, y8, rtol=1e-13, atol=1e-13)
+    # the padded pass does r_pad/r times the adapter arithmetic: rank 4 in a
+    # rank-64 batch pays 16x ([Concepts, "When It Falls Down"])
+    f = _gold("printed_figures.json")["rank_padding_penalty"]
+    assert f["r_max"] // f["r_small"] == f["penalty"]
+
+
+# ----------------------------------------------------------------------------
+# the pages' printed figures
+# ----------------------------------------------------------------------------
+
+def test_toy_counts_and_segments_golden():
+    """[Handbook] toy batch: 53 rows, 6 requests, 4 segments; perm / seg_off
+    hand-derived (tests/golden/toy_segments.json)."""
+    g = _gold("toy_segments.json")
+    w = W.toy_mixed_batch()
+    assert w.T == g["rows"] == 53
+    assert len(w.req_lengths) == g["requests"] == 6
+    seg = O.build_segments(w.slot_ids, w.n_slots)
+    assert seg["n_seg"] == g["segments"] == 4
+    assert seg["seg_slot"].tolist() == g["seg_slot"]
+    assert seg["seg_off"].tolist() == g["seg_off"]
+    assert np.diff(seg["seg_off"]).tolist() == g["seg_counts"]
+    assert seg["perm"].tolist() == g["perm"]
+
+
+def test_toy_three_forms_agree():
+    """[Handbook]: BGMV and SGMV both match the per-request computation (the
+    toy checks this in fp32 at atol 1e-5; in fp64 they agree to rounding)."""
+    w = W.toy_mixed_batch()
+    ref = O.lora_linear_per_request(w.x, w.W0, w.A_pool, w.B_pool, w.scale, w.req_lengths, w.req_slots)
+    for fn in (O.lora_linear, O.lora_linear_gathered, O.lora_linear_segmented):
+        np.testing.assert_allclose(fn(w.x, w.W0, w.A_pool, w.B_pool, w.scale, w.slot_ids), ref,
+                                   rtol=0, atol=1e-12)
+
+
+def _segments_by_definition(ids, n_slots):
+    """Counting-sort definition in plain Python: for each bin in ascending order
+    (base-only bin first), the token indices holding it, in index order."""
+    ids = [int(i) if 0 <= i < n_slots else -1 for i in ids]
+    perm, seg_slot, seg_off = [], [], []
+    for b in [-1] + list(range(n_slots)):
+        members = [t for t, a in enumerate(ids) if a == b]
+        if b >= 0 and members:
+            seg_slot.append(b)
+            seg_off.append(len(perm))
+        perm.extend(members)
+    seg_off.append(len(ids))
+    return perm, seg_slot, seg_off
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_segments_by_definition(seed):
+    rng = np.random.default_rng(100 + seed)
+    n_slots = int(rng.integers(1, 12))
+    T = int(rng.integers(0, 40))
+    ids = rng.integers(-3, n_slots + 3, T)
+    seg = O.build_segments(ids, n_slots)
+    perm, seg_slot, seg_off = _segments_by_definition(ids, n_slots)
+    assert seg["perm"].tolist() == perm
+    assert seg["seg_slot"].tolist() == seg_slot
+    assert seg["seg_off"].tolist() == seg_off
+    assert seg["n_seg"] == len(seg_slot)
+
+
+def test_param_count_figure():
+    """[Blog, "Low-rank structure and additivity"]: d = k = 4096, r = 16 gives
+    131k adapter parameters against 16.8M, about 0.8%."""
+    f = _gold("printed_figures.json")["param_count"]
+    n = O.lora_param_count(f["d"], f["k"], f["r"])
+    assert n == 131072
+    assert round(n / 1000) == round(f["lora_params_approx"] / 1000)
+    dense = f["d"] * f["k"]
+    assert round(dense / 1e5) == round(f["dense_params_approx"] / 1e5)
+    assert abs(n / dense - f["fraction_approx"]) < 0.0005
+
+
+def test_adapter_size_figures():
+    """[Handbook] ~80 MB per adapter for an 8B base at rank 16 over the 7
+    projections (8 GB keeps ~100); [Guide] 40 MB per hot adapter (10 GB keeps
+    ~250), which is the same model at rank 8."""
+    f = _gold("printed_figures.json")
+    proj = [tuple(p) for p in f["decoder_8b_shape"]["projections"]]
+    layers = f["decoder_8b_shape"]["layers"]
+    b16 = O.adapter_bytes(proj, 16, layers)
+    b8 = O.adapter_bytes(proj, 8, layers)
+    assert b16 == 80 * 2 ** 20 and b8 == 40 * 2 ** 20
+    assert abs(b16 / 1e6 - f["adapter_size_r16"]["approx_mb"]) / 80 < 0.06
+    assert round(f["adapter_size_r16"]["budget_gb"] * 1e9 / (b16 * 1.0) / 10) * 10 == 100 or \
+        abs(f["adapter_size_r16"]["budget_gb"] * 1e9 / b16 - 100) < 5
+    assert abs(f["adapter_size_hot"]["budget_gb"] * 1e9 / (f["adapter_size_hot"]["approx_mb"] * 1e6)
+               - f["adapter_size_hot"]["resident_approx"]) < 1e-9
