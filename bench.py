@@ -1,0 +1,648 @@
+#!/usr/bin/env python
+"""Throughput of the multi-LoRA batched linear layer on GB300.
+
+One step = one pass of the whole layer over one batch: segment build, the
+segment-grouped shrink, and the tcgen05 base GEMM with the expand folded into
+its accumulator (lora_linear_fused), on the decode workload: one 4096->4096
+layer, rank 16, 256 resident adapters, 64 one-token requests with Zipf(1.1)
+adapter ids and 8 base-only rows.  Inputs are seeded and synthetic; weights
+and activations are resident in HBM before timing.
+
+Reported on one JSON line (rank 0):
+  value     tokens/s over K steps (CUDA-graph replays; 4 rotating buffer sets
+            whose total is > 2x L2, so every step reads HBM)
+  e2e       the same metric through the public call with host buffers: each
+            step copies x and the ids from pinned memory, runs the layer and
+            copies y back
+  roofline  the dominant kernel (base GEMM + expand), timed with CUDA events
+            around each of its launches, against the measured HBM copy peak
+  sweep     tokens/s and achieved GB/s over distinct adapters per batch
+            (4096->4096, rank 16, 1024-slot pool; T = 32 and 256)
+  configs   the prefill workload (and the 8B-shaped stack with --stack)
+  cpu_baseline  the fp64 CPU oracle on the host cores (a bounded sample)
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "LoRA-layer tokens/s and achieved HBM GB/s vs roofline, swept over distinct adapters/batch"
+UNIT = "tokens/s"
+NSETS = 4
+GRAPH_STEPS = 500
+
+DECODE_DESC = ("decode_bgmv: one 4096->4096 layer, rank 16, 256 resident adapters, 64 one-token "
+               "requests, ids Zipf(1.1) over the pool, 8 rows base-only")
+
+
+# ----------------------------------------------------------------- helpers
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=100000)
+    p.add_argument("--warmup", type=int, default=5000)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-sweep", action="store_true")
+    p.add_argument("--no-prefill", action="store_true")
+    p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--stack", action="store_true", help="also time the 224-layer 8B-shaped stack")
+    a = p.parse_args(argv)
+    if a.warmup < 3:
+        p.error("--warmup must be >= 3")
+    if a.steps < 1:
+        p.error("--steps must be >= 1")
+    return a
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def dist_setup(backend):
+    import torch.distributed as dist
+    rank, world, _ = dist_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return rank, world
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def reduce_max(x: float, device=None) -> float:
+    """Max of a host float over all ranks (the slowest rank sets the time)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64,
+                     device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        return {"hbm_gbs": float(m["hbm_gbs"]), "bf16_tflops": float(m["bf16_tflops"]),
+                "bf16_tflops_sustained": float(m.get("bf16_tflops_sustained", m["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+def kernel_src_sha():
+    h = hashlib.sha256()
+    for f in ("k_fused_tc.cu", "ptx.cuh", "common.cuh"):
+        with open(os.path.join(ROOT, "lora_serving_device_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def dram_traffic_per_launch():
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, or None when the kernel source changed since it was taken."""
+    p = os.path.join(ROOT, "profiles", "fused_tc_decode_traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if d.get("src_sha") != kernel_src_sha():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: str):
+        self.proc = None
+        self.lines = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", gpu_index], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        return parse_clocks(self.lines)
+
+
+def parse_clocks(lines):
+    sm, mx, reasons = [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for ln in lines:
+        parts = [p.strip() for p in ln.split(",")]
+        if len(parts) < 10:
+            continue
+        try:
+            s, m = float(parts[2]), float(parts[3])
+        except ValueError:
+            continue
+        sm.append(s)
+        mx.append(m)
+        for n, v in zip(names, parts[6:10]):
+            if v.lower() in ("active", "1", "yes"):
+                reasons.add(n)
+    if not sm:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+    busy = [s for s in sm if s >= 0.5 * max(sm)] or sm
+    return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+            "samples": len(sm)}
+
+
+def fused_ksplit(T, d_in, n_slots, num_sms=152):
+    """The shrink split the fused path uses (mirrors the library's choice;
+    tests/test_bench_host.py checks it against lora_workspace_bytes)."""
+    cap = min(T, n_slots)
+    est = (T + 63) // 64 + (cap + 1) // 2
+    ks = -(-2 * num_sms // max(est, 1))
+    return max(1, min(ks, 16, max(d_in // 128, 1)))
+
+
+def layer_bytes(T, d_in, d_out, r, D, elem=2):
+    """Algorithmic HBM bytes of one fused layer: W0 once, each distinct
+    adapter's A and B once, x read, y written, the ids."""
+    return (d_in * d_out + D * r * (d_in + d_out) + T * d_in + T * d_out) * elem + T * 4
+
+
+def gemm_bytes(T, d_in, d_out, r, D, elem=2):
+    """Algorithmic bytes of the base-GEMM + expand kernel: W0, the distinct
+    adapters' B, x, the fp32 shrink output v, y written, the ids."""
+    return (d_in * d_out + D * r * d_out + T * d_in + T * d_out) * elem + T * r * 4 + T * 4
+
+
+# ------------------------------------------------------------ reference arm
+def run_reference(args):
+    """The CPU fp64 oracle as it stands, timed on the host cores.  One step is
+    a bounded sample of the decode workload: one token's output on one
+    64-column block of the layer (1/64 of a token's work)."""
+    import numpy as np
+    from lora_serving_device_gb300 import workloads as W
+    from oracle import lora_ref as O
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    w = W.decode_bgmv()
+    nblk = w.d_out // 64
+
+    def step(j):
+        t = j % w.T
+        c0 = ((j // w.T) % nblk) * 64
+        O.lora_linear(w.x[t:t + 1], w.W0[:, c0:c0 + 64], w.A_pool, w.B_pool[:, :, c0:c0 + 64],
+                      w.scale, w.slot_ids[t:t + 1])
+
+    for j in range(args.warmup):
+        step(j)
+    t0 = time.perf_counter()
+    for j in range(args.steps):
+        step(args.warmup + j)
+    dt = time.perf_counter() - t0
+    tokens = args.steps * (64 / w.d_out)
+    value = tokens / dt
+    cores = len(os.sched_getaffinity(0))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded)",
+            "config": {"workload": DECODE_DESC, "T": w.T, "d_in": w.d_in, "d_out": w.d_out,
+                       "r": w.r, "n_slots": w.n_slots, "parallelism": "host"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": "per step: one token x one 64-column block of the "
+                                       "4096x4096 layer (1/64 token)"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------- our arm
+def _up(a, dev):
+    import numpy as np
+    import torch
+    from lora_serving_device_gb300 import workloads as W
+    return torch.from_numpy(W.bf16_bits(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+
+class LayerSet:
+    """Device tensors of one layer instance (one of the rotating sets)."""
+
+    def __init__(self, x, W0, A, B, ids, scale, y):
+        self.x, self.W0, self.A, self.B, self.ids, self.scale, self.y = x, W0, A, B, ids, scale, y
+
+    def clone(self):
+        return LayerSet(self.x.clone(), self.W0.clone(), self.A.clone(), self.B.clone(),
+                        self.ids.clone(), self.scale.clone(), self.y.clone())
+
+
+def capture(fn, n_steps, stream):
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n_steps):
+                fn(i)
+    return g
+
+
+def timed_graph_steps(fn, K, W, stream):
+    """Run W warm-up steps then time exactly K steps of `fn(i)` from CUDA
+    graphs; returns (elapsed ms of the K steps, launches per replay)."""
+    import torch
+    G = min(K, GRAPH_STEPS)
+    with torch.cuda.stream(stream):
+        for i in range(2):          # eager warm-up before capture
+            fn(i)
+    stream.synchronize()
+    g_full = capture(fn, G, stream)
+    rem = K % G
+    g_rem = capture(fn, rem, stream) if rem else None
+    gw = W % G
+    g_wrem = capture(fn, gw, stream) if gw else None
+    with torch.cuda.stream(stream):
+        for _ in range(W // G):
+            g_full.replay()
+        if g_wrem is not None:
+            g_wrem.replay()
+    stream.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    wall0 = time.time()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(K // G):
+            g_full.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        e1.record(stream)
+    stream.synchronize()
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    barrier()
+    return e0.elapsed_time(e1), (wall0, wall1)
+
+
+def per_kernel_times(sets, L, T, d_in, d_out, r, n_slots, n_steps, stream):
+    """Each step as three public calls with CUDA events around each kernel:
+    segment build, shrink, base GEMM + expand.  Returns mean ms per kernel."""
+    import torch
+    ks = fused_ksplit(T, d_in, n_slots)
+    dev = sets[0].x.device
+    cap = max(1, min(T, n_slots))
+    perm = torch.empty(T, dtype=torch.int32, device=dev)
+    seg_slot = torch.empty(cap, dtype=torch.int32, device=dev)
+    seg_off = torch.empty(cap + 1, dtype=torch.int32, device=dev)
+    n_seg = torch.empty(1, dtype=torch.int32, device=dev)
+    vpart = torch.empty((ks, T, r), dtype=torch.float32, device=dev)
+    ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    segs = (perm, seg_slot, seg_off, n_seg)
+    try:
+        evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
+               for _ in range(n_steps)]
+    except TypeError:
+        return None
+
+    def step(i, rec=True):
+        s = sets[i % len(sets)]
+        if rec:
+            evs[i][0].record(stream)
+        L.check(L.lora_build_segments(s.ids.data_ptr(), T, n_slots, perm.data_ptr(),
+                                      seg_slot.data_ptr(), seg_off.data_ptr(), n_seg.data_ptr(),
+                                      ws.data_ptr(), ws.numel(), stream.cuda_stream), "segments")
+        if rec:
+            evs[i][1].record(stream)
+        L.sgmv_shrink_t(s.x, s.A, segs, s.scale, ks, ws, v_partial=vpart, stream=stream)
+        if rec:
+            evs[i][2].record(stream)
+        L.base_gemm_expand_t(s.x, s.W0, s.B, s.ids, vpart, ws, y=s.y, stream=stream)
+        if rec:
+            evs[i][3].record(stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            step(i, rec=False)
+    stream.synchronize()
+    g = capture(step, n_steps, stream)
+    with torch.cuda.stream(stream):
+        g.replay()
+    stream.synchronize()
+    seg = [evs[i][0].elapsed_time(evs[i][1]) for i in range(n_steps)]
+    shr = [evs[i][1].elapsed_time(evs[i][2]) for i in range(n_steps)]
+    gem = [evs[i][2].elapsed_time(evs[i][3]) for i in range(n_steps)]
+    return {"segments_ms": statistics.mean(seg), "shrink_ms": statistics.mean(shr),
+            "gemm_ms": statistics.mean(gem), "gemm_ms_median": statistics.median(gem),
+            "n": n_steps}
+
+
+def e2e_steps(s0, L, T, d_in, d_out, r, n_slots, n_steps, stream):
+    """The public call with host buffers: H2D of x and ids from pinned memory,
+    the layer, D2H of y -- every step inside the timed region."""
+    import torch
+    x_h = s0.x.cpu().pin_memory()
+    ids_h = s0.ids.cpu().pin_memory()
+    y_h = torch.empty((T, d_out), dtype=s0.y.dtype).pin_memory()
+    x_d = torch.empty_like(s0.x)
+    ids_d = torch.empty_like(s0.ids)
+    y_d = torch.empty_like(s0.y)
+    ws = L.workspace(L.OP_LINEAR_FUSED, T, d_in, d_out, r, n_slots)
+
+    def step():
+        x_d.copy_(x_h, non_blocking=True)
+        ids_d.copy_(ids_h, non_blocking=True)
+        L.linear_fused_t(x_d, s0.W0, s0.A, s0.B, ids_d, s0.scale, ws, y=y_d, stream=stream)
+        y_h.copy_(y_d, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(20):
+            step()
+    stream.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(n_steps):
+            step()
+        e1.record(stream)
+    stream.synchronize()
+    ms = e0.elapsed_time(e1)
+    return ms, x_h.numel() * x_h.element_size() + ids_h.numel() * 4, y_h.numel() * y_h.element_size()
+
+
+def cpu_baseline(w, budget_s=12.0):
+    from oracle import lora_ref as O
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        O.lora_linear(w.x, w.W0, w.A_pool, w.B_pool, w.scale, w.slot_ids)
+        n += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": n * w.T / dt, "unit": UNIT, "cores": len(os.sched_getaffinity(0)),
+            "kind": "oracle",
+            "sample": f"the full 64-token decode batch, {n} pass(es) ({dt:.1f} s), numpy fp64 "
+                      f"per-request loop, BLAS threads = all cores"}
+
+
+def device_normal(shape, std, seed, dev):
+    import torch
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    t = torch.empty(shape, dtype=torch.float32, device=dev)
+    t.normal_(0.0, std, generator=g)
+    return t.to(torch.bfloat16)
+
+
+def sweep(L, stream, pk, dev, steps=2000, warm=300):
+    """Distinct adapters per batch: tokens/s and achieved GB/s of the fused
+    layer over the diversity workload (weights drawn on the device)."""
+    import numpy as np
+    import torch
+    from lora_serving_device_gb300 import workloads as W
+    d_in = d_out = 4096
+    r, n_slots = 16, 1024
+    bases = []
+    for s in range(NSETS):
+        W0 = device_normal((d_in, d_out), W.W0_STD, 40400 + s, dev)
+        A = device_normal((n_slots, d_in, r), W.A_STD, 40410 + s, dev)
+        B = device_normal((n_slots, r, d_out), W.B_STD, 40420 + s, dev)
+        bases.append((W0, A, B))
+    scale = torch.full((n_slots,), W.SCALE, dtype=torch.float32, device=dev)
+    out = []
+    for T, k in W.SWEEP_POINTS:
+        ids = torch.from_numpy(W.sweep_ids(T, k)).to(dev)
+        x = device_normal((T, d_in), 1.0, 40430 + T, dev)
+        sets = [LayerSet(x, b[0], b[1], b[2], ids, scale,
+                         torch.empty((T, d_out), dtype=torch.bfloat16, device=dev)) for b in bases]
+        ws = L.workspace(L.OP_LINEAR_FUSED, T, d_in, d_out, r, n_slots)
+
+        def fn(i):
+            s = sets[i % NSETS]
+            L.linear_fused_t(s.x, s.W0, s.A, s.B, s.ids, s.scale, ws, y=s.y, stream=stream)
+
+        ms, _ = timed_graph_steps(fn, steps, warm, stream)
+        t_step = ms / 1e3 / steps
+        nbytes = layer_bytes(T, d_in, d_out, r, k)
+        gbs = nbytes / t_step / 1e9
+        roof_s = nbytes / (pk["hbm_gbs"] * 1e9)
+        out.append({"T": T, "distinct": k, "us_per_step": t_step * 1e6,
+                    "tokens_per_s": T / t_step, "gbs": gbs, "frac": gbs / pk["hbm_gbs"],
+                    "roofline_us": roof_s * 1e6, "latency_floored": roof_s < 5e-6})
+    del bases
+    torch.cuda.empty_cache()
+    return out
+
+
+def prefill_point(L, stream, pk, dev, steps=30, warm=5):
+    import numpy as np
+    import torch
+    from lora_serving_device_gb300 import workloads as W
+    lengths, slots = W.prefill_ids()
+    ids_np = np.repeat(np.array(slots, np.int32), np.array(lengths))
+    T = int(ids_np.size)
+    d_in, d_out, r, n_slots = 4096, 14336, 64, 64
+    x = device_normal((T, d_in), 1.0, 30301, dev)
+    W0 = device_normal((d_in, d_out), W.W0_STD, 30302, dev)
+    A = device_normal((n_slots, d_in, r), W.A_STD, 30303, dev)
+    B = device_normal((n_slots, r, d_out), W.B_STD, 30304, dev)
+    ids = torch.from_numpy(ids_np).to(dev)
+    scale = torch.full((n_slots,), W.SCALE, dtype=torch.float32, device=dev)
+    y = torch.empty((T, d_out), dtype=torch.bfloat16, device=dev)
+    ws = L.workspace(L.OP_LINEAR_FUSED, T, d_in, d_out, r, n_slots)
+
+    def fn(i):
+        L.linear_fused_t(x, W0, A, B, ids, scale, ws, y=y, stream=stream)
+
+    ms, _ = timed_graph_steps(fn, steps, warm, stream)
+    t = ms / 1e3 / steps
+    D = int(np.unique(ids_np).size)
+    flops = 2.0 * T * d_in * d_out + 2.0 * T * r * (d_in + d_out)
+    nbytes = layer_bytes(T, d_in, d_out, r, D)
+    tf = flops / t / 1e12
+    res = {"workload": "prefill_sgmv: 4096->14336, rank 64, 64 slots, 16 prefill requests "
+                       "(U[64,1024] tokens) + 48 decode tokens",
+           "T": T, "distinct": D, "ms_per_step": t * 1e3, "tokens_per_s": T / t,
+           "tflops": tf, "gbs": nbytes / t / 1e9,
+           "roofline": {"bound": "tensor", "achieved": tf, "peak": pk["bf16_tflops_sustained"],
+                        "unit": "TFLOP/s", "frac": tf / pk["bf16_tflops_sustained"]}}
+    del x, W0, A, B
+    torch.cuda.empty_cache()
+    return res
+
+
+def stack_point(L, stream, pk, dev, steps=5, warm=3):
+    """The 8B-shaped stack: 32 layers x 7 projections, one fused call each."""
+    import numpy as np
+    import torch
+    from lora_serving_device_gb300 import workloads as W
+    ranks = W.stack_ranks()
+    ids_np = W.stack_ids()
+    ids = torch.from_numpy(ids_np).to(dev)
+    scale = torch.full((250,), W.SCALE, dtype=torch.float32, device=dev)
+    layers = []
+    for layer in range(W.STACK_LAYERS):
+        for p in range(7):
+            t = W.stack_layer_device(layer, p, device=dev, ranks=ranks)
+            _, d_in, d_out = W.STACK_PROJECTIONS[p]
+            ws = L.workspace(L.OP_LINEAR_FUSED, 256, d_in, d_out, 64, 250)
+            y = torch.empty((256, d_out), dtype=torch.bfloat16, device=dev)
+            layers.append((t, ws, y))
+
+    def fn(i):
+        for t, ws, y in layers:
+            L.linear_fused_t(t["x"], t["W0"], t["A_pool"], t["B_pool"], ids, scale, ws, y=y,
+                             stream=stream)
+
+    ms, _ = timed_graph_steps(fn, steps, warm, stream)
+    t = ms / 1e3 / steps
+    D = int(np.unique(ids_np[ids_np >= 0]).size)
+    nbytes = sum(layer_bytes(256, di, do, 64, D) for _, di, do in W.STACK_PROJECTIONS) * W.STACK_LAYERS
+    res = {"workload": "stack_8b: 32 layers x 7 projections, 250 slots (ranks 8/16/64 padded "
+                       "to 64), T=256", "distinct": D, "ms_per_step": t * 1e3,
+           "tokens_per_s": 256 / t, "gbs": nbytes / t / 1e9, "frac": nbytes / t / 1e9 / pk["hbm_gbs"]}
+    del layers
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    from lora_serving_device_gb300 import build as B
+    from lora_serving_device_gb300 import lora as L
+    from lora_serving_device_gb300 import workloads as W
+
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist_setup("nccl")
+    if rank == 0 and not os.path.exists(L.LIB_PATH):
+        B.build()
+    barrier()
+    L.load()
+    pk = peaks()
+    stream = torch.cuda.Stream(device=dev)
+
+    w = W.decode_bgmv()
+    T, d_in, d_out, r, n_slots = w.T, w.d_in, w.d_out, w.r, w.n_slots
+    D = w.distinct
+    s0 = LayerSet(_up(w.x, dev), _up(w.W0, dev), _up(w.A_pool, dev), _up(w.B_pool, dev),
+                  torch.from_numpy(w.slot_ids).to(dev), torch.from_numpy(w.scale).to(dev),
+                  torch.empty((T, d_out), dtype=torch.bfloat16, device=dev))
+    sets = [s0] + [s0.clone() for _ in range(NSETS - 1)]
+    ws = L.workspace(L.OP_LINEAR_FUSED, T, d_in, d_out, r, n_slots, device=dev)
+
+    def step(i):
+        s = sets[i % NSETS]
+        L.linear_fused_t(s.x, s.W0, s.A, s.B, s.ids, s.scale, ws, y=s.y, stream=stream)
+
+    gpu_index = os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0] or str(local)
+    clk = ClockSampler(gpu_index if world == 1 else str(local))
+    ms, _ = timed_graph_steps(step, args.steps, args.warmup, stream)
+    clk.stop()
+    ms_max = reduce_max(ms, device=dev)
+    err = L.get_error_t(ws, stream=stream)
+    if err:
+        raise SystemExit(f"device error word {err:#x}")
+    value = world * T * args.steps / (ms_max / 1e3)
+
+    kt = per_kernel_times(sets, L, T, d_in, d_out, r, n_slots, 400, stream)
+    e2e_ms, h2d, d2h = e2e_steps(s0, L, T, d_in, d_out, r, n_slots, 2000, stream)
+    e2e_ms = reduce_max(e2e_ms, device=dev)
+    if rank != 0:
+        barrier()
+        return 0
+
+    step_s = ms_max / 1e3 / args.steps
+    gb = gemm_bytes(T, d_in, d_out, r, D)
+    roof = None
+    if kt is not None:
+        ach = gb / (kt["gemm_ms"] / 1e3) / 1e9
+        traffic = dram_traffic_per_launch()
+        roof = {"bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": ach / pk["hbm_gbs"], "traffic": traffic,
+                "kernel": "fused_tc_kernel (base GEMM + expand, tcgen05)",
+                "algorithmic_bytes_per_launch": gb, "launch_us": kt["gemm_ms"] * 1e3,
+                "peak_source": pk["source"], "frac_vs_8tbs": ach / 8000.0}
+    lb = layer_bytes(T, d_in, d_out, r, D)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded)",
+        "config": {"workload": DECODE_DESC, "T": T, "d_in": d_in, "d_out": d_out, "r": r,
+                   "n_slots": n_slots, "distinct": D,
+                   "l2": f"{NSETS} rotating buffer sets (>2x L2)", "parallelism": "replicas",
+                   "graph": f"CUDA graphs of {min(args.steps, GRAPH_STEPS)} steps"},
+        "layer_gbs": lb / step_s / 1e9, "layer_frac": lb / step_s / 1e9 / pk["hbm_gbs"],
+        "gpu_launches": 3 * args.steps,
+        "e2e": {"value": world * T * 2000 / (e2e_ms / 1e3), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms / 2000},
+        "roofline": roof,
+        "kernels_ms": kt,
+        "clocks": clk.summary(),
+    }
+    if not args.no_sweep:
+        line["sweep"] = sweep(L, stream, pk, dev)
+    cfgs = {}
+    if not args.no_prefill:
+        cfgs["prefill_sgmv"] = prefill_point(L, stream, pk, dev)
+    if args.stack:
+        cfgs["stack_8b"] = stack_point(L, stream, pk, dev)
+    if cfgs:
+        line["configs"] = cfgs
+    if world == 1 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(w)
+    print(json.dumps(line), flush=True)
+    barrier()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

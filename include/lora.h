@@ -1,0 +1,213 @@
+/*
+ * lora.h -- C ABI of liblora.so, the multi-LoRA batched linear layer for
+ * GB300 (sm_103a).
+ *
+ * The layer (row-vector form, as in "Serving multiple LoRAs: segmented matrix
+ * multiplies and adapter scheduling", section "Not merging the weights,
+ * computing in batches"):
+ *
+ *     y[t,:] = x[t,:] W0 + s[a_t] * (x[t,:] A[a_t]) B[a_t]
+ *
+ * for a batch of T tokens that may each use a different adapter a_t, or none
+ * (a_t = -1: base only, as in the "Replay" figure of "Serving many LoRA
+ * adapters", blog.ecitis.org: "req C -> base only").  The base product runs
+ * once for the whole batch; the adapter term is gathered per token (BGMV) or
+ * per segment of tokens sorted by adapter (SGMV), first shrinking to rank r
+ * and then expanding back ("Serving multiple LoRAs ...", the paragraph after
+ * the toy script: shrink x -> xA, then expand and add into the base output).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Arrays are caller-owned DEVICE pointers to dense row-major storage.  Data
+ *    pointers must be 16-byte aligned.  x and y must not alias.
+ *  - Layouts (element type = dt for x, W0, A_pool, B_pool, y):
+ *        x       [T, d_in]
+ *        W0      [d_in, d_out]
+ *        A_pool  [n_slots, d_in, r]     adapter a's A is A_pool[a]
+ *        B_pool  [n_slots, r, d_out]    adapter a's B is B_pool[a]
+ *        scale   [n_slots] float32      s[a] = alpha/r of adapter a; it
+ *                travels with the adapter ("Serving many LoRA adapters",
+ *                section "Correctness across tenants").  NULL means 1.0.
+ *        slot_ids[T] int32              -1 = base only.  Any id outside
+ *                [-1, n_slots) is treated as base only and sets
+ *                LORA_DEVERR_BAD_SLOT in the workspace error word.
+ *        v_partial [ksplit, T, r] float32: shrink output split over d_in into
+ *                ksplit contiguous ranges; v = sum over the first index.  The
+ *                scale is already applied (v = s * x A).
+ *  - Shapes: T >= 0; d_in, d_out >= 8 and multiples of 8; r in {8,16,32,64,
+ *    128}; 1 <= n_slots <= LORA_MAX_SLOTS; T <= LORA_MAX_TOKENS; 1 <= ksplit
+ *    <= LORA_MAX_KSPLIT.  T = 0 is a valid empty batch (nothing is launched).
+ *  - Workspace: every call takes a caller-owned device workspace `ws` of at
+ *    least lora_workspace_bytes(op, ...) bytes.  Its first 16 bytes hold the
+ *    sticky device error word; zero-fill the workspace once before first use.
+ *    One workspace must not be used by two calls that run concurrently.
+ *  - Streams: every call only enqueues work on `stream` (a cudaStream_t;
+ *    NULL = the legacy default stream) and returns; nothing synchronises
+ *    except lora_get_error.  The library allocates no memory and keeps no
+ *    per-call global state.  Calls can be captured into CUDA graphs.
+ *  - Errors: host-side validation failures return a status != LORA_OK and
+ *    launch nothing.  LORA_ERR_CUDA reports a launch failure.  Data-dependent
+ *    problems found on the device never trap: they set bits in the workspace
+ *    error word, read back by lora_get_error.
+ *  - dt: LORA_DTYPE_BF16 (bf16 storage, fp32 accumulation, tensor cores for
+ *    the base product) or LORA_DTYPE_F32 (fp32 storage and arithmetic on CUDA
+ *    cores; meant for small checks).
+ */
+#ifndef LORA_H_
+#define LORA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  LORA_OK = 0,
+  LORA_ERR_INVALID_ARG = 1, /* null pointer, misaligned pointer, negative size */
+  LORA_ERR_SHAPE = 2,       /* unsupported dimension (see conventions)          */
+  LORA_ERR_DTYPE = 3,       /* unknown dtype                                     */
+  LORA_ERR_WORKSPACE = 4,   /* ws NULL or smaller than lora_workspace_bytes      */
+  LORA_ERR_CUDA = 5,        /* a CUDA runtime call or launch failed              */
+  LORA_ERR_DEVICE = 6       /* current device is not a GB300-class sm_103 GPU    */
+} lora_status_t;
+
+typedef enum { LORA_DTYPE_BF16 = 0, LORA_DTYPE_F32 = 1 } lora_dtype_t;
+
+/* operation codes for lora_workspace_bytes */
+typedef enum {
+  LORA_OP_BUILD_SEGMENTS = 0,
+  LORA_OP_BGMV_SHRINK = 1,
+  LORA_OP_BGMV_EXPAND = 2,
+  LORA_OP_SGMV_SHRINK = 3,
+  LORA_OP_SGMV_EXPAND = 4,
+  LORA_OP_LINEAR_FUSED = 5,
+  LORA_OP_BASE_GEMM_EXPAND = 6
+} lora_op_t;
+
+/* device error word bits */
+#define LORA_DEVERR_BAD_SLOT 0x1u /* a slot id outside [-1, n_slots) was read   */
+#define LORA_DEVERR_TIMEOUT 0x2u  /* a bounded on-chip wait gave up (no hang)   */
+
+#define LORA_MAX_SLOTS 16384
+#define LORA_MAX_TOKENS (1 << 20)
+#define LORA_MAX_KSPLIT 64
+
+/* Bytes of workspace `op` needs for these sizes (>= 16; the error word). */
+size_t lora_workspace_bytes(int32_t op, int32_t T, int32_t d_in, int32_t d_out, int32_t r,
+                            int32_t n_slots);
+
+/*
+ * Segment builder (SGMV's sort step: "Serving multiple LoRAs ...", SGMV
+ * bullet -- tokens of one adapter are placed together -- and its toy script,
+ * which groups by a stable sort of the ids).
+ *   perm     [T]   out: token indices, stably sorted by slot id; base-only
+ *                  (and invalid) tokens come first.
+ *   seg_slot [min(T, n_slots)] out: ids >= 0 present in the batch, ascending;
+ *                  entries past n_seg are left untouched.
+ *   seg_off  [min(T, n_slots) + 1] out: segment j is perm[seg_off[j] ..
+ *                  seg_off[j+1]); seg_off[n_seg] = T; seg_off[0] is the count
+ *                  of base-only tokens.
+ *   n_seg    [1]   out: number of segments (device int; no host sync).
+ * Bit-exact: equals a stable argsort of the ids followed by run-length
+ * grouping.  One CTA; latency-bound.
+ */
+lora_status_t lora_build_segments(const int32_t* slot_ids, int32_t T, int32_t n_slots,
+                                  int32_t* perm, int32_t* seg_slot, int32_t* seg_off,
+                                  int32_t* n_seg, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * BGMV shrink ("Serving multiple LoRAs ...", BGMV bullet: each token gathers
+ * its adapter's A by index): for every token t with a valid id,
+ *   v_partial[s, t, :] = s[a_t] * x[t, K_s] A[a_t][K_s, :]
+ * over the s-th of ksplit contiguous, 8-aligned ranges K_s of d_in.  Rows of
+ * base-only tokens are written as zeros.  Overwrites v_partial.
+ */
+lora_status_t lora_bgmv_shrink(const void* x, const void* A_pool, const int32_t* slot_ids,
+                               const float* scale, float* v_partial, int32_t T, int32_t d_in,
+                               int32_t r, int32_t n_slots, int32_t ksplit, lora_dtype_t dt,
+                               void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * BGMV expand: y[t, :] += (sum_s v_partial[s, t, :]) B[a_t] for tokens with a
+ * valid id (fp32 arithmetic, one rounding to dt per element).  Base-only rows
+ * of y are not touched.  Accumulates into y.
+ */
+lora_status_t lora_bgmv_expand(const float* v_partial, int32_t ksplit, const void* B_pool,
+                               const int32_t* slot_ids, void* y, int32_t T, int32_t r,
+                               int32_t d_out, int32_t n_slots, lora_dtype_t dt, void* ws,
+                               size_t ws_bytes, void* stream);
+
+/*
+ * SGMV shrink ("Serving Many LoRA Adapters", section "Punica: The Segmented
+ * Gather-Scatter Kernel"; "Serving multiple LoRAs ...", SGMV bullet): the
+ * shrink done segment by segment, each segment reading its adapter's A once.
+ * Takes the outputs of lora_build_segments (device arrays; n_seg is read on
+ * the device).  Same output contract as lora_bgmv_shrink: v_partial rows of
+ * every token are written (zeros for base-only tokens).
+ */
+lora_status_t lora_sgmv_shrink(const void* x, const void* A_pool, const int32_t* perm,
+                               const int32_t* seg_slot, const int32_t* seg_off,
+                               const int32_t* n_seg, const float* scale, float* v_partial,
+                               int32_t T, int32_t d_in, int32_t r, int32_t n_slots,
+                               int32_t ksplit, lora_dtype_t dt, void* ws, size_t ws_bytes,
+                               void* stream);
+
+/*
+ * SGMV expand: per segment, y[t, :] += (sum_s v_partial[s, t, :]) B[a] for
+ * the segment's tokens, reading B[a] once per segment.  Accumulates into y;
+ * base-only rows untouched.
+ */
+lora_status_t lora_sgmv_expand(const float* v_partial, int32_t ksplit, const void* B_pool,
+                               const int32_t* perm, const int32_t* seg_slot,
+                               const int32_t* seg_off, const int32_t* n_seg, void* y, int32_t T,
+                               int32_t r, int32_t d_out, int32_t n_slots, lora_dtype_t dt,
+                               void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * The whole layer: y = x W0 + s (x A) B, y OVERWRITTEN and written once
+ * ("Multi-LoRA batching and adapter paging", section "Walking through a
+ * batch": the base product once for all rows, then each row's adapter term;
+ * "Serving many LoRA adapters", "Replay" figure: segmented gather, grouped
+ * GEMM, scatter add, one fused output).  Enqueues the segment builder, the
+ * segment-grouped shrink and one base-GEMM kernel whose accumulator also
+ * takes the expand term (bf16: tcgen05 tensor cores, accumulator in tensor
+ * memory), so y is stored once.
+ */
+lora_status_t lora_linear_fused(const void* x, const void* W0, const void* A_pool,
+                                const void* B_pool, const int32_t* slot_ids, const float* scale,
+                                void* y, int32_t T, int32_t d_in, int32_t d_out, int32_t r,
+                                int32_t n_slots, lora_dtype_t dt, void* ws, size_t ws_bytes,
+                                void* stream);
+
+/*
+ * The last kernel of lora_linear_fused on its own: the shared base product
+ * with the expand folded into the same accumulator, given the shrink output.
+ *   y[t, :] = x[t, :] W0 + (sum_s v_partial[s, t, :]) B[a_t]   (a_t valid)
+ *   y[t, :] = x[t, :] W0                                       (base only)
+ * y is OVERWRITTEN and written once.  v_partial is any shrink output
+ * (lora_bgmv_shrink or lora_sgmv_shrink, scale applied).  bf16: tcgen05
+ * tensor cores with the accumulator in tensor memory; fp32: CUDA cores.
+ * Workspace: the 16-byte error word only.
+ */
+lora_status_t lora_base_gemm_expand(const void* x, const void* W0, const void* B_pool,
+                                    const int32_t* slot_ids, const float* v_partial,
+                                    int32_t ksplit, void* y, int32_t T, int32_t d_in,
+                                    int32_t d_out, int32_t r, int32_t n_slots, lora_dtype_t dt,
+                                    void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Synchronises `stream`, copies the workspace error word to *device_err and
+ * clears it.  Returns LORA_ERR_CUDA if the stream reports an error.
+ */
+lora_status_t lora_get_error(void* ws, void* stream, int32_t* device_err);
+
+/* Static, human-readable name of a status code. */
+const char* lora_status_string(lora_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LORA_H_ */

@@ -1,0 +1,65 @@
+// Internal launcher interface between the C-ABI entry points (lora_api.cu)
+// and the kernel translation units.  Launchers assume validated arguments.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+#include "lora.h"
+
+namespace lora {
+
+// Per-device facts the launchers need (cached after the first query).
+struct DeviceInfo {
+  int device = -1;
+  int num_sms = 0;
+  int cc_major = 0, cc_minor = 0;
+  size_t max_smem_optin = 0;
+};
+cudaError_t device_info(DeviceInfo* out);
+
+// Segment builder: one CTA, see k_segments.cu.
+cudaError_t launch_build_segments(const int32_t* ids, int T, int n_slots, int32_t* perm,
+                                  int32_t* seg_slot, int32_t* seg_off, int32_t* n_seg,
+                                  uint32_t* err, cudaStream_t st);
+
+// Gather kernels (CUDA cores), see k_gather.cu.
+cudaError_t launch_bgmv_shrink(const void* x, const void* A, const int32_t* ids,
+                               const float* scale, float* vpart, int T, int d_in, int r,
+                               int n_slots, int ksplit, lora_dtype_t dt, uint32_t* err,
+                               cudaStream_t st);
+cudaError_t launch_bgmv_expand(const float* vpart, int ksplit, const void* B, const int32_t* ids,
+                               void* y, int T, int r, int d_out, int n_slots, lora_dtype_t dt,
+                               uint32_t* err, cudaStream_t st);
+// `pdl` launches the shrink as a programmatic dependent of the previous
+// kernel on the stream (used inside lora_linear_fused).
+cudaError_t launch_sgmv_shrink(const void* x, const void* A, const int32_t* perm,
+                               const int32_t* seg_slot, const int32_t* seg_off,
+                               const int32_t* n_seg, const float* scale, float* vpart, int T,
+                               int d_in, int r, int n_slots, int ksplit, lora_dtype_t dt,
+                               uint32_t* err, cudaStream_t st, bool pdl);
+cudaError_t launch_sgmv_expand(const float* vpart, int ksplit, const void* B, const int32_t* perm,
+                               const int32_t* seg_slot, const int32_t* seg_off,
+                               const int32_t* n_seg, void* y, int T, int r, int d_out,
+                               int n_slots, lora_dtype_t dt, uint32_t* err, cudaStream_t st);
+
+// Upper bound on SGMV work items (segment x token-chunk pairs) for a batch.
+int sgmv_max_items(int T, int n_slots);
+// ksplit the fused path uses for its shrink.
+int fused_shrink_ksplit(int T, int d_in, int n_slots, int num_sms);
+
+// Base GEMM + expand-in-accumulator kernel, bf16 (tcgen05), see k_fused_tc.cu.
+cudaError_t launch_fused_tc(const void* x, const void* W0, const void* B, const int32_t* ids,
+                            const float* vpart, int v_ksplit, void* y, int T, int d_in, int d_out,
+                            int r, int n_slots, uint32_t* err, cudaStream_t st,
+                            const DeviceInfo& dev);
+// Same contract for fp32 storage on CUDA cores, see k_fused_simt.cu.
+cudaError_t launch_fused_f32(const float* x, const float* W0, const float* B, const int32_t* ids,
+                             const float* vpart, int v_ksplit, float* y, int T, int d_in,
+                             int d_out, int r, int n_slots, uint32_t* err, cudaStream_t st);
+
+// Whether cuTensorMapEncodeTiled could be resolved (needed for bf16 fused).
+bool tensor_map_available();
+
+}  // namespace lora

@@ -1,0 +1,529 @@
+// The base product of the multi-LoRA layer on tcgen05 tensor cores, with the
+// adapter expand folded into the same accumulator so y is written once.
+//
+// What it computes, for one output tile (a d_out range x a token range):
+//
+//   acc  = x[tokens, :] W0[:, cols]                       (base K-blocks)
+//   acc += sum over the distinct adapters a in the tile of
+//          V_a[tokens, :] B_a[:, cols]                    (LoRA K-blocks)
+//   y    = bf16(acc)
+//
+// where V_a holds the (scaled) shrink output v of the tile's tokens that use
+// adapter a and zeros in every other row.  This is the additivity of the
+// adapter term ("Serving many LoRA adapters", blog.ecitis.org, section
+// "Low-rank structure and additivity"): the base output does not depend on
+// the adapter, so one shared GEMM serves every row, and each row's low-rank
+// correction is extra accumulation on top ("Multi-LoRA batching and adapter
+// paging", section "Walking through a batch"; the expand is "added directly
+// to the base output", "Serving multiple LoRAs ...", after its toy script).
+// Concatenating the adapters along K, [x | V_a1 | V_a2 ...] x [W0 ; B_a1 ;
+// B_a2 ...], turns the gathered expand into ordinary K-blocks of the same
+// MMA pipeline: one 64-row K-block holds 64 / r adapters (r <= 64).
+//
+// Two tile shapes:
+//  * decode (T <= 256), "swap": MMA M = 128 d_out columns (A operand = W0^T,
+//    MN-major), N = the token tile (B operand = x^T, K-major).  d_in is split
+//    over a cluster of S CTAs (split-K); the S fp32 partial tiles are summed
+//    through distributed shared memory, so W0 is streamed by ~all SMs.
+//  * prefill: MMA M = 128 tokens (A = x, K-major), N = 256 d_out columns
+//    (B = W0, MN-major).
+// Both operands arrive by TMA with 128-byte swizzle; the accumulator lives in
+// tensor memory; one thread issues the MMAs.  Warp roles: warp 0 = TMA
+// producer (also builds the masked V operand of the LoRA K-blocks), warp 1 =
+// MMA issuer (and TMEM allocator), warps 2-5 = epilogue (load v during the
+// main loop, then TMEM -> shared -> global).  Every on-chip wait is bounded
+// in time; on timeout the kernel raises LORA_DEVERR_TIMEOUT and returns.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace lora {
+namespace {
+
+constexpr int kBK = 64;           // K elements per stage: one 128-byte swizzle row of bf16
+constexpr int kThreads = 192;     // 6 warps
+constexpr int kEpiThreads = 128;  // warps 2..5
+constexpr int kRedPad = 4;        // fp32 padding per staged accumulator row
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s; the longest legitimate wait is ~ms
+
+struct TcParams {
+  int T, d_in, d_out, r, n_slots;
+  int n_kblk;    // ceil(d_in / 64)
+  int stages;
+  int box_rows;  // rows of one B_pool TMA box: min(r, 64)
+  int v_ksplit;
+  const int32_t* ids;
+  const float* vpart;
+  bf16* y;
+  uint32_t* err;
+};
+
+struct SmemLayout {
+  uint32_t x_bytes, stage_bytes, stages_total;
+  uint32_t vt, tok, uniq, bitmap, bars, misc, total;
+};
+
+// Offsets from a 1024-byte aligned base (the 128-byte swizzle repeats every
+// 8 rows = 1024 bytes, and TMA / MMA agree on it only from such a base).
+template <int BT, int BN>
+__host__ __device__ inline SmemLayout smem_layout(int stages, int r, int n_slots) {
+  SmemLayout L;
+  L.x_bytes = BT * 128;
+  L.stage_bytes = L.x_bytes + (BN / 64) * 8192;
+  L.stages_total = static_cast<uint32_t>(stages) * L.stage_bytes;
+  uint32_t o = L.stages_total;
+  L.vt = o;
+  o += BT * r * 2;
+  o = (o + 15u) & ~15u;
+  L.tok = o;
+  o += BT * 4;
+  L.uniq = o;
+  o += BT * 4;
+  L.bitmap = o;
+  o += ((n_slots + 31) / 32) * 4;
+  o = (o + 7u) & ~7u;
+  L.bars = o;
+  o += (2 * stages + 2) * 8;
+  L.misc = o;
+  o += 16;
+  L.total = o;
+  return L;
+}
+
+// One elected lane waits; the result is broadcast so the warp stays converged.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  int ok = 0;
+  if ((threadIdx.x & 31) == 0) ok = ptx::mbar_wait_bounded(bar, parity, abort, kWaitLimitNs) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+template <bool SWAP, int BT, int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    fused_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+                    const __grid_constant__ CUtensorMap tm_b, const TcParams p) {
+  constexpr int kUmmaM = 128;
+  constexpr int kUmmaN = SWAP ? BT : BN;
+  constexpr int kTmemCols = kUmmaN < 32 ? 32 : kUmmaN;
+  constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kUmmaM, kUmmaN, SWAP, !SWAP);
+  constexpr int kRedLd = BN + kRedPad;   // staged accumulator: [token][d_out column]
+  constexpr int kWBoxes = BN / 64;
+  static_assert((SWAP ? BN : BT) == 128, "MMA M is 128");
+  static_assert(kUmmaN % 16 == 0 && kUmmaN >= 16 && kUmmaN <= 256, "MMA N");
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const SmemLayout L = smem_layout<BT, BN>(p.stages, p.r, p.n_slots);
+  bf16* vt = reinterpret_cast<bf16*>(smem + L.vt);
+  int* tok = reinterpret_cast<int*>(smem + L.tok);
+  int* uniq = reinterpret_cast<int*>(smem + L.uniq);
+  uint32_t* bitmap = reinterpret_cast<uint32_t*>(smem + L.bitmap);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
+  uint64_t* empty = full + p.stages;
+  uint64_t* accum_full = empty + p.stages;
+  uint64_t* vt_ready = accum_full + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc);
+  int* n_uniq_s = reinterpret_cast<int*>(smem + L.misc + 4);
+  volatile int* abort_f = reinterpret_cast<volatile int*>(smem + L.misc + 8);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n0 = blockIdx.x * BN, t0 = blockIdx.y * BT;
+  const int S = static_cast<int>(gridDim.z), z = static_cast<int>(blockIdx.z);
+  const int n_words = (p.n_slots + 31) >> 5;
+
+  // ---- prologue: barriers, the tile's slot ids, TMEM --------------------
+  if (tid == 0) {
+    for (int i = 0; i < p.stages; ++i) {
+      ptx::mbar_init(&full[i], 1);
+      ptx::mbar_init(&empty[i], 1);
+    }
+    ptx::mbar_init(accum_full, 1);
+    ptx::mbar_init(vt_ready, kEpiThreads);
+    *abort_f = 0;
+    ptx::fence_mbar_init();
+  }
+  if (tid == 32) {
+    ptx::prefetch_tmap(&tm_x);
+    ptx::prefetch_tmap(&tm_w);
+    ptx::prefetch_tmap(&tm_b);
+  }
+  bool bad = false;
+  for (int i = tid; i < BT; i += kThreads) {
+    const int t = t0 + i;
+    int s = -1;
+    if (t < p.T) {
+      const int id = p.ids[t];
+      if (slot_valid(id, p.n_slots)) s = id;
+      else if (id != -1) bad = true;
+    }
+    tok[i] = s;
+  }
+  for (int w = tid; w < n_words; w += kThreads) bitmap[w] = 0u;
+  if (bad && blockIdx.x == 0 && z == 0) flag_error(p.err, LORA_DEVERR_BAD_SLOT);
+  if (warp == 1) {
+    ptx::tmem_alloc(tmem_slot, kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  __syncthreads();
+  for (int i = tid; i < BT; i += kThreads) {
+    const int s = tok[i];
+    if (s >= 0) atomicOr(&bitmap[s >> 5], 1u << (s & 31));
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == 0) {  // distinct adapters of the tile, ascending slot order
+    const int per = (n_words + 31) / 32;
+    const int w0 = min(n_words, lane * per), w1 = min(n_words, w0 + per);
+    int c = 0;
+    for (int w = w0; w < w1; ++w) c += __popc(bitmap[w]);
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int off = incl - c;
+    for (int w = w0; w < w1; ++w) {
+      uint32_t m = bitmap[w];
+      while (m) {
+        const int b = __ffs(m) - 1;
+        m &= m - 1;
+        uniq[off++] = w * 32 + b;
+      }
+    }
+    if (lane == 31) *n_uniq_s = incl;
+  }
+  __syncthreads();
+
+  const uint32_t tmem = *tmem_slot;
+  const int n_uniq = *n_uniq_s;
+  const int upa = p.r / p.box_rows;   // TMA boxes per adapter (2 when r = 128)
+  const int G = kBK / p.box_rows;     // boxes per LoRA K-block
+  const int U = n_uniq * upa;
+  const int n_groups = (U + G - 1) / G;
+  const int my_groups = (z < n_groups) ? (n_groups - z + S - 1) / S : 0;
+  const int kb0 = static_cast<int>(static_cast<long long>(z) * p.n_kblk / S);
+  const int kb1 = static_cast<int>(static_cast<long long>(z + 1) * p.n_kblk / S);
+  const int nbase = kb1 - kb0;
+  const int n_iter = nbase + my_groups;
+
+  if (warp == 0) {
+    // ---------------- producer -------------------------------------------
+    bool vt_ok = false;
+    for (int it = 0; it < n_iter; ++it) {
+      const int st = it % p.stages;
+      const uint32_t ph = static_cast<uint32_t>(it / p.stages) & 1u;
+      if (!warp_wait(&empty[st], ph ^ 1u, abort_f)) break;
+      uint8_t* X = smem + static_cast<size_t>(st) * L.stage_bytes;
+      uint8_t* Wr = X + L.x_bytes;
+      if (it < nbase) {
+        if (lane == 0) {
+          const int kb = kb0 + it;
+          ptx::mbar_arrive_expect_tx(&full[st], L.stage_bytes);
+          ptx::tma_load_2d(X, &tm_x, &full[st], kb * kBK, t0);
+#pragma unroll
+          for (int h = 0; h < kWBoxes; ++h)
+            ptx::tma_load_2d(Wr + h * 8192, &tm_w, &full[st], n0 + 64 * h, kb * kBK);
+        }
+        __syncwarp();
+      } else {
+        if (!vt_ok) {
+          if (!warp_wait(vt_ready, 0, abort_f)) break;
+          vt_ok = true;
+        }
+        const int g = z + (it - nbase) * S;
+        const int u_first = g * G;
+        const int n_units = min(G, U - u_first);
+        // masked V operand (K-major, 128-byte swizzle written by hand):
+        // row i, K index kk -> v[token i][q] if token i uses this K-block's
+        // adapter, else 0
+        for (int e = lane; e < BT * 8; e += 32) {
+          const int i = e >> 3, c = e & 7;
+          const int kk = c * 8;
+          const int wu = kk / p.box_rows;
+          uint4 val = make_uint4(0u, 0u, 0u, 0u);
+          if (wu < n_units) {
+            const int w = u_first + wu;
+            const int u = w / upa;
+            const int q0 = (w % upa) * p.box_rows + (kk % p.box_rows);
+            if (tok[i] == uniq[u]) val = *reinterpret_cast<const uint4*>(vt + i * p.r + q0);
+          }
+          *reinterpret_cast<uint4*>(X + i * 128 + ((c ^ (i & 7)) << 4)) = val;
+        }
+        // K rows of the W side that no adapter fills this time are zeroed
+        const int used = n_units * p.box_rows;
+        if (used < kBK) {
+          const int per_box = (kBK - used) * 8;
+          for (int e = lane; e < per_box * kWBoxes; e += 32) {
+            const int h = e / per_box, rem = e % per_box;
+            *reinterpret_cast<uint4*>(Wr + h * 8192 + (used + rem / 8) * 128 + (rem % 8) * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          ptx::mbar_arrive_expect_tx(&full[st],
+                                     static_cast<uint32_t>(n_units * p.box_rows * 128 * kWBoxes));
+          for (int wu = 0; wu < n_units; ++wu) {
+            const int w = u_first + wu;
+            const int a = uniq[w / upa];
+            const int qb = (w % upa) * p.box_rows;
+#pragma unroll
+            for (int h = 0; h < kWBoxes; ++h)
+              ptx::tma_load_2d(Wr + h * 8192 + wu * p.box_rows * 128, &tm_b, &full[st],
+                               n0 + 64 * h, a * p.r + qb);
+          }
+        }
+        __syncwarp();
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer -----------------------------------------
+    if (lane == 0) {
+      for (int it = 0; it < n_iter; ++it) {
+        const int st = it % p.stages;
+        const uint32_t ph = static_cast<uint32_t>(it / p.stages) & 1u;
+        if (!ptx::mbar_wait_bounded(&full[st], ph, abort_f, kWaitLimitNs)) break;
+        ptx::tc_fence_after();
+        const uint32_t xa = ptx::smem_u32(smem + static_cast<size_t>(st) * L.stage_bytes);
+        const uint32_t wa = xa + L.x_bytes;
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk) {
+          // K-major x / V: advance 16 elements = 32 bytes inside the swizzle row
+          const uint64_t xd = ptx::sdesc_sw128(xa + kk * 32, 16, 1024);
+          // MN-major W0 / B: advance 16 K-rows = 2048 bytes; 64-column boxes
+          // are 8 KiB apart (LBO), 8-row groups 1 KiB apart (SBO)
+          const uint64_t wd = ptx::sdesc_sw128(wa + kk * 2048, 8192, 1024);
+          const uint32_t accum = (it > 0 || kk > 0) ? 1u : 0u;
+          if (SWAP) ptx::mma_bf16(tmem, wd, xd, kIdesc, accum);
+          else ptx::mma_bf16(tmem, xd, wd, kIdesc, accum);
+        }
+        ptx::mma_commit(&empty[st]);
+      }
+      ptx::mma_commit(accum_full);
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue warps -------------------------------------
+    const int etid = tid - 64;
+    pdl_wait();  // v is written by the shrink kernel launched just before
+    if (n_uniq > 0) {
+      const int qcn = p.r / 8;
+      for (int e = etid; e < BT * qcn; e += kEpiThreads) {
+        const int i = e / qcn, qc = e % qcn;
+        float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (tok[i] >= 0) {
+          const int t = t0 + i;
+          for (int s = 0; s < p.v_ksplit; ++s) {
+            float g[8];
+            load8(p.vpart + (static_cast<size_t>(s) * p.T + t) * p.r + qc * 8, g);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) f[c] += g[c];
+          }
+        }
+        *reinterpret_cast<uint4*>(vt + i * p.r + qc * 8) = pack8_bf16(f);
+      }
+    }
+    ptx::mbar_arrive(vt_ready);
+    if (warp_wait(accum_full, 0, abort_f)) {
+      ptx::tc_fence_after();
+      const int q = warp & 3;  // TMEM lanes 32q..32q+31 belong to this warp
+      float* red = reinterpret_cast<float*>(smem);
+      const uint32_t tq = tmem + (static_cast<uint32_t>(q * 32) << 16);
+#pragma unroll 1
+      for (int c0 = 0; c0 < kUmmaN; c0 += 16) {
+        uint32_t v[16];
+        ptx::tmem_ld16(tq + c0, v);
+        ptx::tmem_ld_wait();
+        if (SWAP) {
+          const int n = q * 32 + lane;  // TMEM lane = d_out column, column = token
+#pragma unroll
+          for (int j = 0; j < 16; ++j) red[(c0 + j) * kRedLd + n] = __uint_as_float(v[j]);
+        } else {
+          const int i = q * 32 + lane;  // TMEM lane = token, column = d_out column
+          float4* dst = reinterpret_cast<float4*>(red + i * kRedLd + c0);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                 __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+        }
+      }
+    }
+  }
+
+  // ---- split-K reduction through distributed shared memory, store y ------
+  if (S > 1) ptx::cluster_sync();
+  else __syncthreads();
+  if (!*abort_f) {
+    const int rows = min(BT, p.T - t0);
+    const int rb0 = static_cast<int>(static_cast<long long>(z) * rows / S);
+    const int rb1 = static_cast<int>(static_cast<long long>(z + 1) * rows / S);
+    constexpr int kChunks = BN / 8;
+    const uint32_t red_s = ptx::smem_u32(smem);
+    for (int e = tid; e < (rb1 - rb0) * kChunks; e += kThreads) {
+      const int i = rb0 + e / kChunks, c8 = (e % kChunks) * 8;
+      const int n = n0 + c8;
+      if (n >= p.d_out) continue;
+      const uint32_t off = static_cast<uint32_t>((i * kRedLd + c8) * 4);
+      float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      for (int rk = 0; rk < S; ++rk) {
+        float4 a, b;
+        if (S > 1) {
+          const uint32_t ra = ptx::mapa_shared(red_s + off, static_cast<uint32_t>(rk));
+          a = ptx::ld_dsmem_f4(ra);
+          b = ptx::ld_dsmem_f4(ra + 16);
+        } else {
+          a = *reinterpret_cast<const float4*>(smem + off);
+          b = *reinterpret_cast<const float4*>(smem + off + 16);
+        }
+        f[0] += a.x; f[1] += a.y; f[2] += a.z; f[3] += a.w;
+        f[4] += b.x; f[5] += b.y; f[6] += b.z; f[7] += b.w;
+      }
+      store8(p.y + static_cast<size_t>(t0 + i) * p.d_out + n, f);
+    }
+  }
+  if (S > 1) ptx::cluster_sync();
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+  if (tid == 0 && *abort_f) flag_error(p.err, LORA_DEVERR_TIMEOUT);
+}
+
+// ------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+void resolve_encode() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+}
+
+// 2-D bf16 tensor map: `inner` contiguous elements per row, `outer` rows,
+// rows `row_elems` apart; box = box_inner x box_outer, 128-byte swizzle,
+// out-of-range elements read as zero.
+bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_elems,
+              uint32_t box_inner, uint32_t box_outer) {
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_elems * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool SWAP, int BT, int BN>
+cudaError_t launch_variant(const void* x, const void* W0, const void* B, TcParams prm,
+                           int tiles_n, int tiles_t, int S, cudaStream_t st,
+                           const DeviceInfo& dev) {
+  // deepest pipeline that fits next to the v tile and bookkeeping, and that
+  // can hold the staged fp32 accumulator afterwards
+  const size_t cap = dev.max_smem_optin;
+  const size_t red_bytes = static_cast<size_t>(BT) * (BN + kRedPad) * 4;
+  int stages = 0;
+  for (int s = 8; s >= 2; --s) {
+    const SmemLayout L = smem_layout<BT, BN>(s, prm.r, prm.n_slots);
+    if (L.total + 1024 <= cap && L.stages_total >= red_bytes) {
+      stages = s;
+      break;
+    }
+  }
+  if (stages == 0) return cudaErrorInvalidConfiguration;
+  prm.stages = stages;
+  const SmemLayout L = smem_layout<BT, BN>(stages, prm.r, prm.n_slots);
+  const size_t smem = L.total + 1024;
+
+  CUtensorMap tm_x, tm_w, tm_b;
+  if (!make_map(&tm_x, x, prm.d_in, prm.T, prm.d_in, kBK, BT) ||
+      !make_map(&tm_w, W0, prm.d_out, prm.d_in, prm.d_out, 64, kBK) ||
+      !make_map(&tm_b, B, prm.d_out, static_cast<uint64_t>(prm.n_slots) * prm.r, prm.d_out, 64,
+                prm.box_rows))
+    return cudaErrorInvalidValue;
+
+  auto kern = fused_tc_kernel<SWAP, BT, BN>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(tiles_n, tiles_t, S);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = S;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, tm_x, tm_w, tm_b, prm);
+}
+
+}  // namespace
+
+bool tensor_map_available() {
+  resolve_encode();
+  return g_encode != nullptr;
+}
+
+cudaError_t launch_fused_tc(const void* x, const void* W0, const void* B, const int32_t* ids,
+                            const float* vpart, int v_ksplit, void* y, int T, int d_in, int d_out,
+                            int r, int n_slots, uint32_t* err, cudaStream_t st,
+                            const DeviceInfo& dev) {
+  resolve_encode();
+  if (g_encode == nullptr) return cudaErrorNotSupported;
+  TcParams prm;
+  prm.T = T;
+  prm.d_in = d_in;
+  prm.d_out = d_out;
+  prm.r = r;
+  prm.n_slots = n_slots;
+  prm.n_kblk = (d_in + kBK - 1) / kBK;
+  prm.stages = 0;
+  prm.box_rows = r < 64 ? r : 64;
+  prm.v_ksplit = v_ksplit;
+  prm.ids = ids;
+  prm.vpart = vpart;
+  prm.y = static_cast<bf16*>(y);
+  prm.err = err;
+
+  auto pick_split = [&](int tiles) {
+    int S = dev.num_sms / (tiles > 0 ? tiles : 1);
+    if (S > 8) S = 8;
+    if (S > prm.n_kblk) S = prm.n_kblk;
+    if (S < 1) S = 1;
+    return S;
+  };
+  if (T <= 256) {
+    const int tiles_n = (d_out + 127) / 128;
+    const int S = pick_split(tiles_n);
+    if (T <= 32) return launch_variant<true, 32, 128>(x, W0, B, prm, tiles_n, 1, S, st, dev);
+    if (T <= 64) return launch_variant<true, 64, 128>(x, W0, B, prm, tiles_n, 1, S, st, dev);
+    if (T <= 128) return launch_variant<true, 128, 128>(x, W0, B, prm, tiles_n, 1, S, st, dev);
+    return launch_variant<true, 256, 128>(x, W0, B, prm, tiles_n, 1, S, st, dev);
+  }
+  const int tiles_n = (d_out + 255) / 256;
+  const int tiles_t = (T + 127) / 128;
+  const int S = pick_split(tiles_n * tiles_t);
+  return launch_variant<false, 128, 256>(x, W0, B, prm, tiles_n, tiles_t, S, st, dev);
+}
+
+}  // namespace lora

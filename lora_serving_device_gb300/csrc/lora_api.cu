@@ -1,0 +1,333 @@
+// C-ABI entry points of liblora.so (declared in include/lora.h): argument
+// validation, workspace carving and kernel enqueueing.  Nothing here
+// allocates device memory or synchronises, except lora_get_error.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "internal.h"
+#include "lora.h"
+
+namespace lora {
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int32_t kMaxDim = 1 << 20;
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool rank_ok(int32_t r) { return r == 8 || r == 16 || r == 32 || r == 64 || r == 128; }
+bool dim_ok(int32_t d) { return d >= 8 && d % 8 == 0 && d <= kMaxDim; }
+bool tokens_ok(int32_t T) { return T <= LORA_MAX_TOKENS; }
+bool slots_ok(int32_t n) { return n >= 1 && n <= LORA_MAX_SLOTS; }
+bool dtype_ok(lora_dtype_t dt) { return dt == LORA_DTYPE_BF16 || dt == LORA_DTYPE_F32; }
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+constexpr size_t kErrBytes = 16;
+
+struct FusedWs {
+  uint32_t* err;
+  int32_t* perm;
+  int32_t* seg_slot;
+  int32_t* seg_off;
+  int32_t* n_seg;
+  float* vpart;
+  int ksplit;
+  size_t bytes;
+};
+
+// Workspace of lora_linear_fused: error word, segment arrays, shrink partials.
+FusedWs fused_ws_layout(void* ws, int32_t T, int32_t d_in, int32_t r, int32_t n_slots) {
+  FusedWs w;
+  const size_t cap = static_cast<size_t>(T < n_slots ? T : n_slots);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  size_t o = kErrBytes;
+  const size_t o_perm = o;
+  o += static_cast<size_t>(T) * 4;
+  const size_t o_slot = o;
+  o += cap * 4;
+  const size_t o_off = o;
+  o += (cap + 1) * 4;
+  const size_t o_nseg = o;
+  o += 4;
+  o = round_up(o, 256);
+  const size_t o_v = o;
+  w.ksplit = fused_shrink_ksplit(T, d_in, n_slots, 152);
+  o += static_cast<size_t>(w.ksplit) * T * r * 4;
+  w.bytes = round_up(o, 256);
+  w.err = reinterpret_cast<uint32_t*>(base);
+  w.perm = reinterpret_cast<int32_t*>(base + o_perm);
+  w.seg_slot = reinterpret_cast<int32_t*>(base + o_slot);
+  w.seg_off = reinterpret_cast<int32_t*>(base + o_off);
+  w.n_seg = reinterpret_cast<int32_t*>(base + o_nseg);
+  w.vpart = reinterpret_cast<float*>(base + o_v);
+  return w;
+}
+
+lora_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? LORA_OK : LORA_ERR_CUDA; }
+
+// The library is built for sm_103a only.
+lora_status_t check_device(DeviceInfo* out) {
+  return device_info(out) == cudaSuccess
+             ? ((out->cc_major == 10 && out->cc_minor == 3) ? LORA_OK : LORA_ERR_DEVICE)
+             : LORA_ERR_CUDA;
+}
+
+lora_status_t check_ws(const void* ws, size_t ws_bytes, size_t need) {
+  if (ws == nullptr || !aligned16(ws) || ws_bytes < need) return LORA_ERR_WORKSPACE;
+  return LORA_OK;
+}
+
+}  // namespace
+
+cudaError_t device_info(DeviceInfo* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (d.device != dev) {
+    DeviceInfo n;
+    n.device = dev;
+    int v = 0;
+    if ((e = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    n.num_sms = v;
+    if ((e = cudaDeviceGetAttribute(&v, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess) return e;
+    n.cc_major = v;
+    if ((e = cudaDeviceGetAttribute(&v, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess) return e;
+    n.cc_minor = v;
+    if ((e = cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess) return e;
+    n.max_smem_optin = static_cast<size_t>(v);
+    d = n;
+  }
+  *out = d;
+  return cudaSuccess;
+}
+
+}  // namespace lora
+
+using namespace lora;
+
+extern "C" {
+
+size_t lora_workspace_bytes(int32_t op, int32_t T, int32_t d_in, int32_t d_out, int32_t r,
+                            int32_t n_slots) {
+  (void)d_out;
+  if (op == LORA_OP_LINEAR_FUSED) {
+    if (T < 0 || !rank_ok(r) || !slots_ok(n_slots) || d_in < 8) return kErrBytes;
+    return fused_ws_layout(nullptr, T, d_in, r, n_slots).bytes;
+  }
+  return kErrBytes;
+}
+
+const char* lora_status_string(lora_status_t s) {
+  switch (s) {
+    case LORA_OK: return "LORA_OK";
+    case LORA_ERR_INVALID_ARG: return "LORA_ERR_INVALID_ARG: null or misaligned pointer, or negative size";
+    case LORA_ERR_SHAPE: return "LORA_ERR_SHAPE: unsupported dimension";
+    case LORA_ERR_DTYPE: return "LORA_ERR_DTYPE: unknown dtype";
+    case LORA_ERR_WORKSPACE: return "LORA_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    case LORA_ERR_CUDA: return "LORA_ERR_CUDA: a CUDA call or kernel launch failed";
+    case LORA_ERR_DEVICE: return "LORA_ERR_DEVICE: current device is not sm_103";
+  }
+  return "LORA_ERR_UNKNOWN";
+}
+
+lora_status_t lora_build_segments(const int32_t* slot_ids, int32_t T, int32_t n_slots,
+                                  int32_t* perm, int32_t* seg_slot, int32_t* seg_off,
+                                  int32_t* n_seg, void* ws, size_t ws_bytes, void* stream) {
+  if (T < 0) return LORA_ERR_INVALID_ARG;
+  if (!tokens_ok(T) || !slots_ok(n_slots)) return LORA_ERR_SHAPE;
+  if ((T > 0 && (slot_ids == nullptr || perm == nullptr || seg_slot == nullptr)) ||
+      seg_off == nullptr || n_seg == nullptr)
+    return LORA_ERR_INVALID_ARG;
+  lora_status_t s = check_ws(ws, ws_bytes, kErrBytes);
+  if (s != LORA_OK) return s;
+  DeviceInfo dev;
+  if ((s = check_device(&dev)) != LORA_OK) return s;
+  return from_cuda(launch_build_segments(slot_ids, T, n_slots, perm, seg_slot, seg_off, n_seg,
+                                         static_cast<uint32_t*>(ws),
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+lora_status_t lora_bgmv_shrink(const void* x, const void* A_pool, const int32_t* slot_ids,
+                               const float* scale, float* v_partial, int32_t T, int32_t d_in,
+                               int32_t r, int32_t n_slots, int32_t ksplit, lora_dtype_t dt,
+                               void* ws, size_t ws_bytes, void* stream) {
+  if (T < 0) return LORA_ERR_INVALID_ARG;
+  if (!dtype_ok(dt)) return LORA_ERR_DTYPE;
+  if (!tokens_ok(T) || !dim_ok(d_in) || !rank_ok(r) || !slots_ok(n_slots) || ksplit < 1 ||
+      ksplit > LORA_MAX_KSPLIT)
+    return LORA_ERR_SHAPE;
+  if (x == nullptr || A_pool == nullptr || slot_ids == nullptr || v_partial == nullptr ||
+      !aligned16(x) || !aligned16(A_pool) || !aligned16(v_partial))
+    return LORA_ERR_INVALID_ARG;
+  lora_status_t s = check_ws(ws, ws_bytes, kErrBytes);
+  if (s != LORA_OK) return s;
+  if (T == 0) return LORA_OK;
+  DeviceInfo dev;
+  if ((s = check_device(&dev)) != LORA_OK) return s;
+  return from_cuda(launch_bgmv_shrink(x, A_pool, slot_ids, scale, v_partial, T, d_in, r, n_slots,
+                                      ksplit, dt, static_cast<uint32_t*>(ws),
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+lora_status_t lora_bgmv_expand(const float* v_partial, int32_t ksplit, const void* B_pool,
+                               const int32_t* slot_ids, void* y, int32_t T, int32_t r,
+                               int32_t d_out, int32_t n_slots, lora_dtype_t dt, void* ws,
+                               size_t ws_bytes, void* stream) {
+  if (T < 0) return LORA_ERR_INVALID_ARG;
+  if (!dtype_ok(dt)) return LORA_ERR_DTYPE;
+  if (!tokens_ok(T) || !dim_ok(d_out) || !rank_ok(r) || !slots_ok(n_slots) || ksplit < 1 ||
+      ksplit > LORA_MAX_KSPLIT)
+    return LORA_ERR_SHAPE;
+  if (v_partial == nullptr || B_pool == nullptr || slot_ids == nullptr || y == nullptr ||
+      !aligned16(v_partial) || !aligned16(B_pool) || !aligned16(y))
+    return LORA_ERR_INVALID_ARG;
+  lora_status_t s = check_ws(ws, ws_bytes, kErrBytes);
+  if (s != LORA_OK) return s;
+  if (T == 0) return LORA_OK;
+  DeviceInfo dev;
+  if ((s = check_device(&dev)) != LORA_OK) return s;
+  return from_cuda(launch_bgmv_expand(v_partial, ksplit, B_pool, slot_ids, y, T, r, d_out,
+                                      n_slots, dt, static_cast<uint32_t*>(ws),
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+lora_status_t lora_sgmv_shrink(const void* x, const void* A_pool, const int32_t* perm,
+                               const int32_t* seg_slot, const int32_t* seg_off,
+                               const int32_t* n_seg, const float* scale, float* v_partial,
+                               int32_t T, int32_t d_in, int32_t r, int32_t n_slots,
+                               int32_t ksplit, lora_dtype_t dt, void* ws, size_t ws_bytes,
+                               void* stream) {
+  if (T < 0) return LORA_ERR_INVALID_ARG;
+  if (!dtype_ok(dt)) return LORA_ERR_DTYPE;
+  if (!tokens_ok(T) || !dim_ok(d_in) || !rank_ok(r) || !slots_ok(n_slots) || ksplit < 1 ||
+      ksplit > LORA_MAX_KSPLIT)
+    return LORA_ERR_SHAPE;
+  if (x == nullptr || A_pool == nullptr || perm == nullptr || seg_slot == nullptr ||
+      seg_off == nullptr || n_seg == nullptr || v_partial == nullptr || !aligned16(x) ||
+      !aligned16(A_pool) || !aligned16(v_partial))
+    return LORA_ERR_INVALID_ARG;
+  lora_status_t s = check_ws(ws, ws_bytes, kErrBytes);
+  if (s != LORA_OK) return s;
+  if (T == 0) return LORA_OK;
+  DeviceInfo dev;
+  if ((s = check_device(&dev)) != LORA_OK) return s;
+  return from_cuda(launch_sgmv_shrink(x, A_pool, perm, seg_slot, seg_off, n_seg, scale, v_partial,
+                                      T, d_in, r, n_slots, ksplit, dt, static_cast<uint32_t*>(ws),
+                                      static_cast<cudaStream_t>(stream), false));
+}
+
+lora_status_t lora_sgmv_expand(const float* v_partial, int32_t ksplit, const void* B_pool,
+                               const int32_t* perm, const int32_t* seg_slot,
+                               const int32_t* seg_off, const int32_t* n_seg, void* y, int32_t T,
+                               int32_t r, int32_t d_out, int32_t n_slots, lora_dtype_t dt,
+                               void* ws, size_t ws_bytes, void* stream) {
+  if (T < 0) return LORA_ERR_INVALID_ARG;
+  if (!dtype_ok(dt)) return LORA_ERR_DTYPE;
+  if (!tokens_ok(T) || !dim_ok(d_out) || !rank_ok(r) || !slots_ok(n_slots) || ksplit < 1 ||
+      ksplit > LORA_MAX_KSPLIT)
+    return LORA_ERR_SHAPE;
+  if (v_partial == nullptr || B_pool == nullptr || perm == nullptr || seg_slot == nullptr ||
+      seg_off == nullptr || n_seg == nullptr || y == nullptr || !aligned16(v_partial) ||
+      !aligned16(B_pool) || !aligned16(y))
+    return LORA_ERR_INVALID_ARG;
+  lora_status_t s = check_ws(ws, ws_bytes, kErrBytes);
+  if (s != LORA_OK) return s;
+  if (T == 0) return LORA_OK;
+  DeviceInfo dev;
+  if ((s = check_device(&dev)) != LORA_OK) return s;
+  return from_cuda(launch_sgmv_expand(v_partial, ksplit, B_pool, perm, seg_slot, seg_off, n_seg, y,
+                                      T, r, d_out, n_slots, dt, static_cast<uint32_t*>(ws),
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+lora_status_t lora_linear_fused(const void* x, const void* W0, const void* A_pool,
+                                const void* B_pool, const int32_t* slot_ids, const float* scale,
+                                void* y, int32_t T, int32_t d_in, int32_t d_out, int32_t r,
+                                int32_t n_slots, lora_dtype_t dt, void* ws, size_t ws_bytes,
+                                void* stream) {
+  if (T < 0) return LORA_ERR_INVALID_ARG;
+  if (!dtype_ok(dt)) return LORA_ERR_DTYPE;
+  if (!tokens_ok(T) || !dim_ok(d_in) || !dim_ok(d_out) || !rank_ok(r) || !slots_ok(n_slots))
+    return LORA_ERR_SHAPE;
+  if (x == nullptr || W0 == nullptr || A_pool == nullptr || B_pool == nullptr ||
+      slot_ids == nullptr || y == nullptr || !aligned16(x) || !aligned16(W0) ||
+      !aligned16(A_pool) || !aligned16(B_pool) || !aligned16(y))
+    return LORA_ERR_INVALID_ARG;
+  if (x == y) return LORA_ERR_INVALID_ARG;
+  const FusedWs w = fused_ws_layout(ws, T, d_in, r, n_slots);
+  lora_status_t s = check_ws(ws, ws_bytes, w.bytes);
+  if (s != LORA_OK) return s;
+  if (T == 0) return LORA_OK;
+  DeviceInfo dev;
+  if ((s = check_device(&dev)) != LORA_OK) return s;
+  if (dt == LORA_DTYPE_BF16 && !tensor_map_available()) return LORA_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_build_segments(slot_ids, T, n_slots, w.perm, w.seg_slot, w.seg_off,
+                                        w.n_seg, w.err, st);
+  if (e != cudaSuccess) return LORA_ERR_CUDA;
+  e = launch_sgmv_shrink(x, A_pool, w.perm, w.seg_slot, w.seg_off, w.n_seg, scale, w.vpart, T,
+                         d_in, r, n_slots, w.ksplit, dt, w.err, st, true);
+  if (e != cudaSuccess) return LORA_ERR_CUDA;
+  if (dt == LORA_DTYPE_BF16)
+    e = launch_fused_tc(x, W0, B_pool, slot_ids, w.vpart, w.ksplit, y, T, d_in, d_out, r, n_slots,
+                        w.err, st, dev);
+  else
+    e = launch_fused_f32(static_cast<const float*>(x), static_cast<const float*>(W0),
+                         static_cast<const float*>(B_pool), slot_ids, w.vpart, w.ksplit,
+                         static_cast<float*>(y), T, d_in, d_out, r, n_slots, w.err, st);
+  return from_cuda(e);
+}
+
+lora_status_t lora_base_gemm_expand(const void* x, const void* W0, const void* B_pool,
+                                    const int32_t* slot_ids, const float* v_partial,
+                                    int32_t ksplit, void* y, int32_t T, int32_t d_in,
+                                    int32_t d_out, int32_t r, int32_t n_slots, lora_dtype_t dt,
+                                    void* ws, size_t ws_bytes, void* stream) {
+  if (T < 0) return LORA_ERR_INVALID_ARG;
+  if (!dtype_ok(dt)) return LORA_ERR_DTYPE;
+  if (!tokens_ok(T) || !dim_ok(d_in) || !dim_ok(d_out) || !rank_ok(r) || !slots_ok(n_slots) ||
+      ksplit < 1 || ksplit > LORA_MAX_KSPLIT)
+    return LORA_ERR_SHAPE;
+  if (x == nullptr || W0 == nullptr || B_pool == nullptr || slot_ids == nullptr ||
+      v_partial == nullptr || y == nullptr || !aligned16(x) || !aligned16(W0) ||
+      !aligned16(B_pool) || !aligned16(v_partial) || !aligned16(y) || x == y)
+    return LORA_ERR_INVALID_ARG;
+  lora_status_t s = check_ws(ws, ws_bytes, kErrBytes);
+  if (s != LORA_OK) return s;
+  if (T == 0) return LORA_OK;
+  DeviceInfo dev;
+  if ((s = check_device(&dev)) != LORA_OK) return s;
+  if (dt == LORA_DTYPE_BF16 && !tensor_map_available()) return LORA_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t* err = static_cast<uint32_t*>(ws);
+  cudaError_t e;
+  if (dt == LORA_DTYPE_BF16)
+    e = launch_fused_tc(x, W0, B_pool, slot_ids, v_partial, ksplit, y, T, d_in, d_out, r, n_slots,
+                        err, st, dev);
+  else
+    e = launch_fused_f32(static_cast<const float*>(x), static_cast<const float*>(W0),
+                         static_cast<const float*>(B_pool), slot_ids, v_partial, ksplit,
+                         static_cast<float*>(y), T, d_in, d_out, r, n_slots, err, st);
+  return from_cuda(e);
+}
+
+lora_status_t lora_get_error(void* ws, void* stream, int32_t* device_err) {
+  if (ws == nullptr || device_err == nullptr || !aligned16(ws)) return LORA_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t host = 0;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return LORA_ERR_CUDA;
+  if (cudaMemcpyAsync(&host, ws, sizeof(host), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return LORA_ERR_CUDA;
+  if (cudaMemsetAsync(ws, 0, sizeof(host), st) != cudaSuccess) return LORA_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return LORA_ERR_CUDA;
+  *device_err = static_cast<int32_t>(host);
+  return LORA_OK;
+}
+
+}  // extern "C"

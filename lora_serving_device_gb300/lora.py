@@ -1,0 +1,255 @@
+"""ctypes binding of liblora.so (C ABI in include/lora.h).
+
+Argument marshalling only: every step of the layer runs in the library's CUDA
+kernels.  The raw functions keep the C names and take integer device
+pointers; the ``*_t`` helpers take torch tensors (device memory and streams
+come from PyTorch) and raise ``LoraError`` on a non-OK status.  There is no
+fallback: if the library is missing or the device is not sm_103, calls fail.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "liblora.so")
+
+# status codes / enums mirrored from include/lora.h
+LORA_OK = 0
+STATUS_NAMES = {0: "LORA_OK", 1: "LORA_ERR_INVALID_ARG", 2: "LORA_ERR_SHAPE", 3: "LORA_ERR_DTYPE",
+                4: "LORA_ERR_WORKSPACE", 5: "LORA_ERR_CUDA", 6: "LORA_ERR_DEVICE"}
+DTYPE_BF16, DTYPE_F32 = 0, 1
+OP_BUILD_SEGMENTS, OP_BGMV_SHRINK, OP_BGMV_EXPAND = 0, 1, 2
+OP_SGMV_SHRINK, OP_SGMV_EXPAND, OP_LINEAR_FUSED, OP_BASE_GEMM_EXPAND = 3, 4, 5, 6
+DEVERR_BAD_SLOT, DEVERR_TIMEOUT = 0x1, 0x2
+MAX_SLOTS, MAX_TOKENS, MAX_KSPLIT = 16384, 1 << 20, 64
+
+EXPORTS = ("lora_workspace_bytes", "lora_build_segments", "lora_bgmv_shrink", "lora_bgmv_expand",
+           "lora_sgmv_shrink", "lora_sgmv_expand", "lora_linear_fused", "lora_base_gemm_expand",
+           "lora_get_error",
+           "lora_status_string")
+
+
+class LoraError(RuntimeError):
+    def __init__(self, status, what=""):
+        self.status = status
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)}")
+
+
+_lib = None
+_P = ctypes.c_void_p
+_I = ctypes.c_int32
+_Z = ctypes.c_size_t
+
+_SIGS = {
+    "lora_workspace_bytes": (_Z, [_I, _I, _I, _I, _I, _I]),
+    "lora_build_segments": (_I, [_P, _I, _I, _P, _P, _P, _P, _P, _Z, _P]),
+    "lora_bgmv_shrink": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _Z, _P]),
+    "lora_bgmv_expand": (_I, [_P, _I, _P, _P, _P, _I, _I, _I, _I, _I, _P, _Z, _P]),
+    "lora_sgmv_shrink": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _Z, _P]),
+    "lora_sgmv_expand": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _Z, _P]),
+    "lora_linear_fused": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _Z, _P]),
+    "lora_base_gemm_expand": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _Z, _P]),
+    "lora_get_error": (_I, [_P, _P, ctypes.POINTER(ctypes.c_int32)]),
+    "lora_status_string": (ctypes.c_char_p, [_I]),
+}
+
+
+def load(path: str = LIB_PATH):
+    """Load liblora.so (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with "
+                               "`python -m lora_serving_device_gb300.build`")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(lib, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _call(name, *args):
+    return getattr(load(), name)(*args)
+
+
+# ----------------------------------------------------------------- raw C names
+def lora_workspace_bytes(op, T, d_in, d_out, r, n_slots):
+    return _call("lora_workspace_bytes", op, T, d_in, d_out, r, n_slots)
+
+
+def lora_build_segments(slot_ids, T, n_slots, perm, seg_slot, seg_off, n_seg, ws, ws_bytes, stream):
+    return _call("lora_build_segments", slot_ids, T, n_slots, perm, seg_slot, seg_off, n_seg, ws,
+                 ws_bytes, stream)
+
+
+def lora_bgmv_shrink(x, A_pool, slot_ids, scale, v_partial, T, d_in, r, n_slots, ksplit, dt, ws,
+                     ws_bytes, stream):
+    return _call("lora_bgmv_shrink", x, A_pool, slot_ids, scale, v_partial, T, d_in, r, n_slots,
+                 ksplit, dt, ws, ws_bytes, stream)
+
+
+def lora_bgmv_expand(v_partial, ksplit, B_pool, slot_ids, y, T, r, d_out, n_slots, dt, ws,
+                     ws_bytes, stream):
+    return _call("lora_bgmv_expand", v_partial, ksplit, B_pool, slot_ids, y, T, r, d_out, n_slots,
+                 dt, ws, ws_bytes, stream)
+
+
+def lora_sgmv_shrink(x, A_pool, perm, seg_slot, seg_off, n_seg, scale, v_partial, T, d_in, r,
+                     n_slots, ksplit, dt, ws, ws_bytes, stream):
+    return _call("lora_sgmv_shrink", x, A_pool, perm, seg_slot, seg_off, n_seg, scale, v_partial,
+                 T, d_in, r, n_slots, ksplit, dt, ws, ws_bytes, stream)
+
+
+def lora_sgmv_expand(v_partial, ksplit, B_pool, perm, seg_slot, seg_off, n_seg, y, T, r, d_out,
+                     n_slots, dt, ws, ws_bytes, stream):
+    return _call("lora_sgmv_expand", v_partial, ksplit, B_pool, perm, seg_slot, seg_off, n_seg, y,
+                 T, r, d_out, n_slots, dt, ws, ws_bytes, stream)
+
+
+def lora_linear_fused(x, W0, A_pool, B_pool, slot_ids, scale, y, T, d_in, d_out, r, n_slots, dt,
+                      ws, ws_bytes, stream):
+    return _call("lora_linear_fused", x, W0, A_pool, B_pool, slot_ids, scale, y, T, d_in, d_out, r,
+                 n_slots, dt, ws, ws_bytes, stream)
+
+
+def lora_base_gemm_expand(x, W0, B_pool, slot_ids, v_partial, ksplit, y, T, d_in, d_out, r,
+                          n_slots, dt, ws, ws_bytes, stream):
+    return _call("lora_base_gemm_expand", x, W0, B_pool, slot_ids, v_partial, ksplit, y, T, d_in,
+                 d_out, r, n_slots, dt, ws, ws_bytes, stream)
+
+
+def lora_get_error(ws, stream):
+    out = ctypes.c_int32(0)
+    st = _call("lora_get_error", ws, stream, ctypes.byref(out))
+    return st, out.value
+
+
+def lora_status_string(status):
+    return _call("lora_status_string", status).decode()
+
+
+# ----------------------------------------------------------- torch helpers
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream=None):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _dt(t):
+    import torch
+    if t.dtype == torch.bfloat16:
+        return DTYPE_BF16
+    if t.dtype == torch.float32:
+        return DTYPE_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def check(status, what):
+    if status != LORA_OK:
+        raise LoraError(status, what)
+
+
+def workspace(op, T, d_in, d_out, r, n_slots, device="cuda"):
+    """A zero-filled workspace tensor for `op` (uint8, 256-byte aligned)."""
+    import torch
+    n = lora_workspace_bytes(op, T, d_in, d_out, r, n_slots)
+    return torch.zeros(max(int(n), 16), dtype=torch.uint8, device=device)
+
+
+def build_segments_t(slot_ids, n_slots, ws, stream=None):
+    import torch
+    T = slot_ids.numel()
+    cap = max(1, min(T, n_slots))
+    dev = slot_ids.device
+    perm = torch.empty(max(T, 1), dtype=torch.int32, device=dev)
+    seg_slot = torch.empty(cap, dtype=torch.int32, device=dev)
+    seg_off = torch.empty(cap + 1, dtype=torch.int32, device=dev)
+    n_seg = torch.empty(1, dtype=torch.int32, device=dev)
+    check(lora_build_segments(_ptr(slot_ids), T, n_slots, _ptr(perm), _ptr(seg_slot),
+                              _ptr(seg_off), _ptr(n_seg), _ptr(ws), ws.numel(), _stream(stream)),
+          "lora_build_segments")
+    return perm[:T], seg_slot, seg_off, n_seg
+
+
+def bgmv_shrink_t(x, A_pool, slot_ids, scale, ksplit, ws, v_partial=None, stream=None):
+    import torch
+    T, d_in = x.shape
+    n_slots, _, r = A_pool.shape
+    if v_partial is None:
+        v_partial = torch.empty((ksplit, T, r), dtype=torch.float32, device=x.device)
+    check(lora_bgmv_shrink(_ptr(x), _ptr(A_pool), _ptr(slot_ids), _ptr(scale), _ptr(v_partial), T,
+                           d_in, r, n_slots, ksplit, _dt(x), _ptr(ws), ws.numel(), _stream(stream)),
+          "lora_bgmv_shrink")
+    return v_partial
+
+
+def bgmv_expand_t(v_partial, B_pool, slot_ids, y, ws, stream=None):
+    ksplit, T, r = v_partial.shape
+    n_slots, _, d_out = B_pool.shape
+    check(lora_bgmv_expand(_ptr(v_partial), ksplit, _ptr(B_pool), _ptr(slot_ids), _ptr(y), T, r,
+                           d_out, n_slots, _dt(y), _ptr(ws), ws.numel(), _stream(stream)),
+          "lora_bgmv_expand")
+    return y
+
+
+def sgmv_shrink_t(x, A_pool, segs, scale, ksplit, ws, v_partial=None, stream=None):
+    import torch
+    perm, seg_slot, seg_off, n_seg = segs
+    T, d_in = x.shape
+    n_slots, _, r = A_pool.shape
+    if v_partial is None:
+        v_partial = torch.empty((ksplit, T, r), dtype=torch.float32, device=x.device)
+    check(lora_sgmv_shrink(_ptr(x), _ptr(A_pool), _ptr(perm), _ptr(seg_slot), _ptr(seg_off),
+                           _ptr(n_seg), _ptr(scale), _ptr(v_partial), T, d_in, r, n_slots, ksplit,
+                           _dt(x), _ptr(ws), ws.numel(), _stream(stream)), "lora_sgmv_shrink")
+    return v_partial
+
+
+def sgmv_expand_t(v_partial, B_pool, segs, y, ws, stream=None):
+    perm, seg_slot, seg_off, n_seg = segs
+    ksplit, T, r = v_partial.shape
+    n_slots, _, d_out = B_pool.shape
+    check(lora_sgmv_expand(_ptr(v_partial), ksplit, _ptr(B_pool), _ptr(perm), _ptr(seg_slot),
+                           _ptr(seg_off), _ptr(n_seg), _ptr(y), T, r, d_out, n_slots, _dt(y),
+                           _ptr(ws), ws.numel(), _stream(stream)), "lora_sgmv_expand")
+    return y
+
+
+def linear_fused_t(x, W0, A_pool, B_pool, slot_ids, scale, ws, y=None, stream=None):
+    """y = x W0 + s (x A) B for the batch; allocates y if not given."""
+    import torch
+    T, d_in = x.shape
+    d_out = W0.shape[1]
+    n_slots, _, r = A_pool.shape
+    if y is None:
+        y = torch.empty((T, d_out), dtype=x.dtype, device=x.device)
+    check(lora_linear_fused(_ptr(x), _ptr(W0), _ptr(A_pool), _ptr(B_pool), _ptr(slot_ids),
+                            _ptr(scale), _ptr(y), T, d_in, d_out, r, n_slots, _dt(x), _ptr(ws),
+                            ws.numel(), _stream(stream)), "lora_linear_fused")
+    return y
+
+
+def base_gemm_expand_t(x, W0, B_pool, slot_ids, v_partial, ws, y=None, stream=None):
+    """y = x W0 + (sum of v_partial) B_a, overwriting y (allocated if None)."""
+    import torch
+    T, d_in = x.shape
+    d_out = W0.shape[1]
+    n_slots, r, _ = B_pool.shape
+    if y is None:
+        y = torch.empty((T, d_out), dtype=x.dtype, device=x.device)
+    check(lora_base_gemm_expand(_ptr(x), _ptr(W0), _ptr(B_pool), _ptr(slot_ids), _ptr(v_partial),
+                                v_partial.shape[0], _ptr(y), T, d_in, d_out, r, n_slots, _dt(x),
+                                _ptr(ws), ws.numel(), _stream(stream)), "lora_base_gemm_expand")
+    return y
+
+
+def get_error_t(ws, stream=None):
+    st, err = lora_get_error(_ptr(ws), _stream(stream))
+    check(st, "lora_get_error")
+    return err

@@ -1,0 +1,93 @@
+"""Host-side logic of bench.py, on CPU: argument contract, byte accounting,
+clock parsing, the library's shrink split, and the multi-rank timing
+reduction (gloo, world size 2)."""
+import os
+import socket
+
+import pytest
+
+import bench
+
+
+def test_args_contract():
+    a = bench.parse_args([])
+    assert a.gpus == 1 and a.steps >= 1 and a.warmup >= 3 and a.impl == "ours"
+    with pytest.raises(SystemExit):
+        bench.parse_args(["--warmup", "2"])
+    assert bench.parse_args(["--impl", "reference"]).impl == "reference"
+
+
+def test_layer_bytes_decode():
+    # W0 32 MiB + D (A+B) slices + x + y; ~40.6 MiB at the expected ~30.5
+    # distinct adapters of the decode workload
+    b = bench.layer_bytes(64, 4096, 4096, 16, 30.5)
+    assert abs(b / 2 ** 20 - 40.6) < 0.2
+    g = bench.gemm_bytes(64, 4096, 4096, 16, 30)
+    assert g < b and g > 32 * 2 ** 20
+
+
+def test_fused_ksplit_matches_library():
+    from lora_serving_device_gb300 import build, lora as L
+    build.build()
+    for T, d_in, n_slots, r in [(64, 4096, 256, 16), (8752, 4096, 64, 64), (256, 14336, 250, 64),
+                                (32, 4096, 1024, 16), (1, 64, 3, 8)]:
+        ks = bench.fused_ksplit(T, d_in, n_slots)
+        cap = min(T, n_slots)
+        head = 16 + T * 4 + cap * 4 + (cap + 1) * 4 + 4
+        head = -(-head // 256) * 256
+        want = -(-(head + ks * T * r * 4) // 256) * 256
+        assert L.lora_workspace_bytes(L.OP_LINEAR_FUSED, T, d_in, 0, r, n_slots) == want
+
+
+def test_parse_clocks():
+    lines = [
+        "2026/12/02 10:00:00.000, 0, 1965, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "2026/12/02 10:00:00.200, 0, 1980, 2070, 1100.0, 0x4, Not Active, Not Active, Not Active, Active",
+        "2026/12/02 10:00:00.400, 0, 345, 2070, 100.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+    ]
+    s = bench.parse_clocks(lines)
+    assert s["sm_max_mhz"] == 2070 and s["reasons"] == ["sw_power_cap"]
+    assert 1965 <= s["sm_mhz"] <= 1980        # idle sample excluded from "under load"
+    assert bench.parse_clocks([])["reasons"] == ["unsampled"]
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+def _worker(rank, world, port, q):
+    os.environ.update({"MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port), "RANK": str(rank),
+                       "WORLD_SIZE": str(world), "LOCAL_RANK": str(rank)})
+    import torch.distributed as dist
+    bench.dist_setup("gloo")
+    bench.barrier()
+    got = bench.reduce_max(10.0 * (rank + 1))
+    bench.barrier()
+    dist.destroy_process_group()
+    q.put((rank, got))
+
+
+def test_reduce_max_over_two_gloo_ranks():
+    import torch.multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = dict(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert res == {0: 20.0, 1: 20.0}
+
+
+def test_reference_arm_only_rank0_works(monkeypatch, capsys):
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    assert bench.run_reference(bench.parse_args(["--impl", "reference", "--steps", "1"])) == 0
+    assert capsys.readouterr().out == ""

@@ -1,0 +1,335 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU fp64 oracle.
+
+Integer outputs (segments) must match bit for bit; floating-point outputs
+must meet the bar in tests/tolerances.py, for y and for the adapter delta.
+Shapes span several tiles with ragged tails, every supported rank, empty and
+single-token batches, invalid ids, and the full-size workloads.
+"""
+import numpy as np
+import pytest
+
+from oracle import lora_ref as O
+from lora_serving_device_gb300 import workloads as W
+
+from tests.gpu_util import DeviceCase, dev, host, torch_mod
+from tests.tolerances import check_close
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def L():
+    torch = torch_mod()
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from lora_serving_device_gb300 import build, lora
+    build.build()
+    lora.load()
+    return lora
+
+
+def _ws(L, n=1 << 16):
+    torch = torch_mod()
+    return torch.zeros(n, dtype=torch.uint8, device="cuda")
+
+
+# ------------------------------------------------------------ segment builder
+SEG_CASES = [
+    ("toy", lambda: (W.toy_mixed_batch().slot_ids, 8)),
+    ("decode", lambda: (W.decode_ids(2), 256)),
+    ("prefill", lambda: (np.repeat(np.array(W.prefill_ids()[1], np.int32),
+                                   np.array(W.prefill_ids()[0])), 64)),
+    ("sweep", lambda: (W.sweep_ids(256, 64), 1024)),
+    ("empty", lambda: (np.zeros(0, np.int32), 5)),
+    ("one", lambda: (np.array([3], np.int32), 5)),
+    ("all_base", lambda: (np.full(100, -1, np.int32), 7)),
+    ("one_slot", lambda: (np.zeros(300, np.int32), 1)),
+    ("invalid", lambda: (W.random_case(3, 500, 8, 8, 8, 40, invalid=9).slot_ids, 40)),
+    ("max_tokens_16k", lambda: (np.random.default_rng(5).integers(-1, 64, 16432).astype(np.int32), 64)),
+    ("max_slots", lambda: (np.random.default_rng(6).integers(-1, 16384, 5000).astype(np.int32), 16384)),
+    ("many_tokens", lambda: (np.random.default_rng(7).integers(-1, 1024, 70000).astype(np.int32), 1024)),
+]
+
+
+@pytest.mark.parametrize("name,make", SEG_CASES, ids=[c[0] for c in SEG_CASES])
+def test_segments_bit_exact(L, name, make):
+    torch = torch_mod()
+    ids, n_slots = make()
+    ids = np.asarray(ids, np.int32)
+    ws = _ws(L)
+    perm, seg_slot, seg_off, n_seg = L.build_segments_t(dev(ids), n_slots, ws)
+    torch.cuda.synchronize()
+    ref = O.build_segments(ids, n_slots)
+    n = int(n_seg.item())
+    assert n == ref["n_seg"]
+    assert perm.cpu().numpy().tolist() == ref["perm"].tolist()
+    assert seg_slot.cpu().numpy()[:n].tolist() == ref["seg_slot"].tolist()
+    assert seg_off.cpu().numpy()[:n + 1].tolist() == ref["seg_off"].tolist()
+    err = L.get_error_t(ws)
+    bad = np.any((ids < -1) | (ids >= n_slots))
+    assert bool(err & L.DEVERR_BAD_SLOT) == bool(bad)
+
+
+# ------------------------------------------------------------ BGMV / SGMV
+GATHER_CASES = [
+    # T, d_in, d_out, r, n_slots, dtype
+    (1, 64, 64, 16, 3, "bf16"),
+    (37, 200, 136, 8, 5, "bf16"),
+    (64, 512, 264, 16, 9, "bf16"),
+    (130, 256, 520, 32, 4, "bf16"),
+    (70, 136, 200, 64, 6, "bf16"),
+    (45, 128, 1032, 128, 3, "bf16"),
+    (53, 256, 256, 16, 8, "f32"),
+    (90, 96, 72, 64, 4, "f32"),
+]
+
+
+def _v_input(T, r, ksplit, seed):
+    # a seeded synthetic v_partial (input of the expand tests)
+    rng = np.random.default_rng([7000, seed, T, r])
+    return (rng.standard_normal((ksplit, T, r)) * 0.5).astype(np.float32)
+
+
+@pytest.mark.parametrize("case", GATHER_CASES, ids=[str(c) for c in GATHER_CASES])
+@pytest.mark.parametrize("form", ["bgmv", "sgmv"])
+def test_shrink_matches_oracle(L, case, form):
+    torch = torch_mod()
+    T, d_in, d_out, r, n_slots, dt = case
+    w = W.random_case(11 + T, T, d_in, d_out, r, n_slots, runs=(form == "sgmv"),
+                      bf16=(dt == "bf16"))
+    d = DeviceCase(w)
+    ws = _ws(L)
+    ref = O.shrink(w.x, w.A_pool, w.scale, w.slot_ids)
+    for ksplit in (1, 3):
+        if form == "bgmv":
+            vp = L.bgmv_shrink_t(d.x, d.A, d.ids, d.scale, ksplit, ws)
+        else:
+            segs = L.build_segments_t(d.ids, n_slots, ws)
+            vp = L.sgmv_shrink_t(d.x, d.A, segs, d.scale, ksplit, ws)
+        torch.cuda.synchronize()
+        v = host(vp).sum(axis=0)
+        check_close(v, ref, f"{form} shrink ksplit={ksplit}")
+
+
+@pytest.mark.parametrize("case", GATHER_CASES, ids=[str(c) for c in GATHER_CASES])
+@pytest.mark.parametrize("form", ["bgmv", "sgmv"])
+def test_expand_matches_oracle(L, case, form):
+    torch = torch_mod()
+    T, d_in, d_out, r, n_slots, dt = case
+    w = W.random_case(23 + T, T, d_in, d_out, r, n_slots, runs=(form == "sgmv"),
+                      bf16=(dt == "bf16"))
+    d = DeviceCase(w)
+    ws = _ws(L)
+    ksplit = 2
+    vp = _v_input(T, r, ksplit, 1)
+    v = vp.astype(np.float64).sum(axis=0)
+    y0 = (np.random.default_rng([7001, T]).standard_normal((T, d_out)) * 0.1).astype(np.float32)
+    if dt == "bf16":
+        y0 = W.bf16_round(y0)
+    y = dev(y0, dt)
+    if form == "bgmv":
+        L.bgmv_expand_t(dev(vp, "f32"), d.B, d.ids, y, ws)
+    else:
+        segs = L.build_segments_t(d.ids, n_slots, ws)
+        L.sgmv_expand_t(dev(vp, "f32"), d.B, segs, y, ws)
+    torch.cuda.synchronize()
+    delta_ref = O.expand(v, w.B_pool, w.slot_ids)
+    got = host(y)
+    check_close(got, y0 + delta_ref, f"{form} expand y")
+    # base-only rows untouched, bit for bit
+    base_rows = ~((w.slot_ids >= 0) & (w.slot_ids < n_slots))
+    np.testing.assert_array_equal(got[base_rows], y0[base_rows].astype(np.float64))
+    # delta alone, measured where it is large enough to resolve
+    if dt == "f32":
+        check_close(got - y0, delta_ref, f"{form} expand delta")
+
+
+# ------------------------------------------------------------ fused layer
+FUSED_CASES = [
+    # T, d_in, d_out, r, n_slots : decode tiles (T <= 256) and prefill tiles
+    (1, 64, 128, 16, 3),
+    (5, 200, 136, 8, 7),
+    (32, 1000, 264, 16, 12),
+    (33, 256, 384, 32, 5),
+    (64, 512, 1024, 16, 40),
+    (100, 128, 520, 64, 9),
+    (128, 384, 256, 128, 4),
+    (200, 640, 136, 16, 30),
+    (256, 256, 512, 64, 70),
+    (257, 192, 264, 16, 11),
+    (300, 520, 512, 32, 6),
+    (517, 136, 776, 64, 13),
+    (1000, 256, 1288, 16, 50),
+]
+
+
+@pytest.mark.parametrize("case", FUSED_CASES, ids=[str(c) for c in FUSED_CASES])
+def test_fused_matches_oracle(L, case):
+    torch = torch_mod()
+    T, d_in, d_out, r, n_slots = case
+    for runs in (False, True):
+        w = W.random_case(100 + T + int(runs), T, d_in, d_out, r, n_slots, runs=runs)
+        d = DeviceCase(w)
+        y, ws = d.fused()
+        torch.cuda.synchronize()
+        ref = O.lora_linear(w.x, w.W0, w.A_pool, w.B_pool, w.scale, w.slot_ids)
+        check_close(host(y), ref, f"y runs={runs}")
+        assert L.get_error_t(ws) == 0
+        # the adapter path alone (W0 = 0), so bf16 rounding of the base term
+        # cannot hide an error in it
+        d0 = DeviceCase(w, W0_zero=True)
+        y0, _ = d0.fused()
+        torch.cuda.synchronize()
+        base = O.lora_linear(w.x, w.W0, w.A_pool, w.B_pool, w.scale, np.full(T, -1))
+        check_close(host(y0), ref - base, f"delta runs={runs}")
+
+
+def test_fused_invalid_ids_are_base_only_and_flagged(L):
+    torch = torch_mod()
+    w = W.random_case(501, 90, 256, 264, 16, 10, invalid=7)
+    d = DeviceCase(w)
+    y, ws = d.fused()
+    torch.cuda.synchronize()
+    ref = O.lora_linear(w.x, w.W0, w.A_pool, w.B_pool, w.scale, w.slot_ids)
+    check_close(host(y), ref, "y with invalid ids")
+    assert L.get_error_t(ws) & L.DEVERR_BAD_SLOT
+    assert L.get_error_t(ws) == 0          # cleared by the read
+
+
+def test_fused_all_base_and_zero_B(L):
+    torch = torch_mod()
+    w = W.random_case(502, 48, 256, 136, 16, 4)
+    w.slot_ids[:] = -1
+    d = DeviceCase(w)
+    y, _ = d.fused()
+    torch.cuda.synchronize()
+    check_close(host(y), O.lora_linear(w.x, w.W0, w.A_pool, w.B_pool, w.scale, w.slot_ids), "all base")
+    w2 = W.random_case(503, 48, 256, 136, 16, 4)
+    w2.B_pool[:] = 0
+    d2 = DeviceCase(w2)
+    y2, _ = d2.fused()
+    torch.cuda.synchronize()
+    base = O.lora_linear(w2.x, w2.W0, w2.A_pool, w2.B_pool, w2.scale, np.full(48, -1))
+    check_close(host(y2), base, "B = 0")
+
+
+def test_fused_deterministic_and_graph_capturable(L):
+    torch = torch_mod()
+    w = W.random_case(504, 64, 1024, 1024, 16, 20)
+    d = DeviceCase(w)
+    y1, ws = d.fused()
+    y2, _ = d.fused(ws=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)
+    y3 = torch.empty_like(y1)
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        d.fused(ws=ws, y=y3)     # warm-up on the capture stream
+        with torch.cuda.graph(g, stream=s):
+            d.fused(ws=ws, y=y3)
+    torch.cuda.current_stream().wait_stream(s)
+    y3.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y3)
+
+
+# ------------------------------------------------------------ the workloads
+def test_toy_mixed_batch_fp32(L):
+    torch = torch_mod()
+    w = W.toy_mixed_batch()
+    d = DeviceCase(w)
+    y, ws = d.fused()
+    torch.cuda.synchronize()
+    ref = O.lora_linear_per_request(w.x, w.W0, w.A_pool, w.B_pool, w.scale, w.req_lengths, w.req_slots)
+    check_close(host(y), ref, "toy y")
+    # fp32 storage: the toy page checks allclose at atol 1e-5
+    assert np.max(np.abs(host(y) - ref)) < 1e-4
+
+
+def test_decode_bgmv_full(L):
+    torch = torch_mod()
+    w = W.decode_bgmv()
+    d = DeviceCase(w)
+    y, ws = d.fused()
+    torch.cuda.synchronize()
+    ref = O.lora_linear(w.x, w.W0, w.A_pool, w.B_pool, w.scale, w.slot_ids)
+    check_close(host(y), ref, "decode y")
+    assert L.get_error_t(ws) == 0
+    # standalone BGMV shrink + expand on the same batch
+    wsb = _ws(L)
+    vp = L.bgmv_shrink_t(d.x, d.A, d.ids, d.scale, 16, wsb)
+    yb = dev(np.zeros((w.T, w.d_out), np.float32), "bf16")
+    L.bgmv_expand_t(vp, d.B, d.ids, yb, wsb)
+    torch.cuda.synchronize()
+    base = O.lora_linear(w.x, w.W0, w.A_pool, w.B_pool, w.scale, np.full(w.T, -1))
+    check_close(host(yb), ref - base, "decode BGMV delta")
+    d0 = DeviceCase(w, W0_zero=True)
+    y0, _ = d0.fused()
+    torch.cuda.synchronize()
+    check_close(host(y0), ref - base, "decode fused delta")
+
+
+def test_prefill_sgmv_full(L):
+    torch = torch_mod()
+    w = W.prefill_sgmv()
+    d = DeviceCase(w)
+    y, ws = d.fused()
+    torch.cuda.synchronize()
+    ref = O.lora_linear_per_request(w.x, w.W0, w.A_pool, w.B_pool, w.scale, w.req_lengths, w.req_slots)
+    check_close(host(y), ref, "prefill y")
+    assert L.get_error_t(ws) == 0
+    # standalone SGMV shrink + expand on the same batch (delta only)
+    wsb = _ws(L)
+    segs = L.build_segments_t(d.ids, w.n_slots, wsb)
+    vp = L.sgmv_shrink_t(d.x, d.A, segs, d.scale, 2, wsb)
+    yb = dev(np.zeros((w.T, w.d_out), np.float32), "bf16")
+    L.sgmv_expand_t(vp, d.B, segs, yb, wsb)
+    torch.cuda.synchronize()
+    base = O.lora_linear(w.x, w.W0, w.A_pool, w.B_pool, w.scale, np.full(w.T, -1))
+    delta = ref - base
+    check_close(host(yb), delta, "prefill SGMV delta")
+
+
+@pytest.mark.parametrize("T,k", W.SWEEP_POINTS)
+def test_diversity_sweep_point(L, T, k):
+    torch = torch_mod()
+    w = W.diversity_sweep(T, k, only_used_slots=True)
+    d = DeviceCase(w)
+    y, ws = d.fused()
+    torch.cuda.synchronize()
+    ref = O.lora_linear(w.x, w.W0, w.A_pool, w.B_pool, w.scale, w.slot_ids)
+    check_close(host(y), ref, f"sweep T={T} k={k}")
+    assert L.get_error_t(ws) == 0
+
+
+STACK_CHECK = [(0, p) for p in range(7)] + [(31, p) for p in range(7)] + [(13, 4), (22, 6)]
+
+
+@pytest.mark.parametrize("layer,proj", STACK_CHECK)
+def test_stack_8b_projection(L, layer, proj):
+    torch = torch_mod()
+    from lora_serving_device_gb300 import lora as Lm
+    ranks = W.stack_ranks()
+    ids = W.stack_ids()
+    t = W.stack_layer_device(layer, proj, ranks=ranks)
+    _, d_in, d_out = W.STACK_PROJECTIONS[proj]
+    n_slots, r = 250, 64
+    ws = Lm.workspace(Lm.OP_LINEAR_FUSED, 256, d_in, d_out, r, n_slots)
+    scale = torch.full((n_slots,), W.SCALE, dtype=torch.float32, device="cuda")
+    ids_d = torch.from_numpy(ids).cuda()
+    y = Lm.linear_fused_t(t["x"], t["W0"], t["A_pool"], t["B_pool"], ids_d, scale, ws)
+    torch.cuda.synchronize()
+    used = np.unique(ids[ids >= 0])
+    A = np.zeros((n_slots, d_in, r))
+    B = np.zeros((n_slots, r, d_out))
+    A[used] = host(t["A_pool"][torch.from_numpy(used).cuda()])
+    B[used] = host(t["B_pool"][torch.from_numpy(used).cuda()])
+    for j in used:   # rank padding really is zero
+        assert np.all(A[j][:, ranks[j]:] == 0) and np.all(B[j][ranks[j]:] == 0)
+    lengths, slots = W.stack_requests()
+    ref = O.lora_linear_per_request(host(t["x"]), host(t["W0"]), A, B,
+                                    np.full(n_slots, W.SCALE), lengths, slots)
+    check_close(host(y), ref, f"stack layer {layer} proj {proj}")
