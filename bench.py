@@ -585,7 +585,11 @@ def run_ours(args):
         raise SystemExit(f"device error word {err:#x}")
     value = world * T * args.steps / (ms_max / 1e3)
 
-    kt = per_kernel_times(sets, L, T, d_in, d_out, r, n_slots, 400, stream)
+    try:
+        kt = per_kernel_times(sets, L, T, d_in, d_out, r, n_slots, 400, stream)
+    except RuntimeError as e:   # timing events inside a captured graph unsupported
+        print(f"per-kernel timing unavailable: {e}", file=sys.stderr)
+        kt = None
     e2e_ms, h2d, d2h = e2e_steps(s0, L, T, d_in, d_out, r, n_slots, 2000, stream)
     e2e_ms = reduce_max(e2e_ms, device=dev)
     if rank != 0:

@@ -54,7 +54,7 @@ struct TcParams {
   int T, d_in, d_out, r, n_slots;
   int n_kblk;    // ceil(d_in / 64)
   int stages;
-  int box_rows;  // rows of one B_pool TMA box: min(r, 64)
+  int box_rows;  // rows of one B_pool TMA box: min(r, 32)
   int v_ksplit;
   const int32_t* ids;
   const float* vpart;
@@ -77,7 +77,7 @@ __host__ __device__ inline SmemLayout smem_layout(int stages, int r, int n_slots
   L.stages_total = static_cast<uint32_t>(stages) * L.stage_bytes;
   uint32_t o = L.stages_total;
   L.vt = o;
-  o += BT * r * 2;
+  o += BT * r * 4;
   o = (o + 15u) & ~15u;
   L.tok = o;
   o += BT * 4;
@@ -118,7 +118,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const SmemLayout L = smem_layout<BT, BN>(p.stages, p.r, p.n_slots);
-  bf16* vt = reinterpret_cast<bf16*>(smem + L.vt);
+  float* vt = reinterpret_cast<float*>(smem + L.vt);
   int* tok = reinterpret_cast<int*>(smem + L.tok);
   int* uniq = reinterpret_cast<int*>(smem + L.uniq);
   uint32_t* bitmap = reinterpret_cast<uint32_t*>(smem + L.bitmap);
@@ -202,8 +202,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const uint32_t tmem = *tmem_slot;
   const int n_uniq = *n_uniq_s;
-  const int upa = p.r / p.box_rows;   // TMA boxes per adapter (2 when r = 128)
-  const int G = kBK / p.box_rows;     // boxes per LoRA K-block
+  const int upa = p.r / p.box_rows;      // TMA boxes per adapter (r / min(r, 32))
+  const int G = (kBK / 2) / p.box_rows;  // boxes per LoRA K-block (each used twice)
   const int U = n_uniq * upa;
   const int n_groups = (U + G - 1) / G;
   const int my_groups = (z < n_groups) ? (n_groups - z + S - 1) / S : 0;
@@ -239,45 +239,63 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int g = z + (it - nbase) * S;
         const int u_first = g * G;
         const int n_units = min(G, U - u_first);
-        // masked V operand (K-major, 128-byte swizzle written by hand):
-        // row i, K index kk -> v[token i][q] if token i uses this K-block's
-        // adapter, else 0
+        // masked V operand (K-major, 128-byte swizzle written by hand).
+        // v is fp32; it enters the bf16 MMA as v = hi + lo with hi = bf16(v)
+        // and lo = bf16(v - hi), so the expand keeps ~16 mantissa bits.  K
+        // rows [0, 32) carry the hi parts of this block's adapters, rows
+        // [32, 64) the lo parts, each against its own copy of the B rows.
+        // Row i, K index kk -> part of v[token i][q] if token i uses the
+        // adapter of that K row, else 0.
         for (int e = lane; e < BT * 8; e += 32) {
           const int i = e >> 3, c = e & 7;
-          const int kk = c * 8;
-          const int wu = kk / p.box_rows;
+          const int kq = (c & 3) * 8;  // K offset inside the hi or lo half
+          const int wu = kq / p.box_rows;
           uint4 val = make_uint4(0u, 0u, 0u, 0u);
           if (wu < n_units) {
             const int w = u_first + wu;
             const int u = w / upa;
-            const int q0 = (w % upa) * p.box_rows + (kk % p.box_rows);
-            if (tok[i] == uniq[u]) val = *reinterpret_cast<const uint4*>(vt + i * p.r + q0);
+            const int q0 = (w % upa) * p.box_rows + (kq % p.box_rows);
+            if (tok[i] == uniq[u]) {
+              float f[8];
+              load8(vt + i * p.r + q0, f);
+              float h[8], l[8];
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                h[j] = __bfloat162float(__float2bfloat16_rn(f[j]));
+                l[j] = f[j] - h[j];
+              }
+              val = pack8_bf16(c < 4 ? h : l);
+            }
           }
           *reinterpret_cast<uint4*>(X + i * 128 + ((c ^ (i & 7)) << 4)) = val;
         }
         // K rows of the W side that no adapter fills this time are zeroed
         const int used = n_units * p.box_rows;
-        if (used < kBK) {
-          const int per_box = (kBK - used) * 8;
-          for (int e = lane; e < per_box * kWBoxes; e += 32) {
-            const int h = e / per_box, rem = e % per_box;
-            *reinterpret_cast<uint4*>(Wr + h * 8192 + (used + rem / 8) * 128 + (rem % 8) * 16) =
-                make_uint4(0u, 0u, 0u, 0u);
+        if (used < kBK / 2) {
+          const int per_half = (kBK / 2 - used) * 8;
+          for (int e = lane; e < 2 * per_half * kWBoxes; e += 32) {
+            const int h = e / (2 * per_half), rem = e % (2 * per_half);
+            const int half = rem / per_half, rr = rem % per_half;
+            *reinterpret_cast<uint4*>(Wr + h * 8192 + (half * (kBK / 2) + used + rr / 8) * 128 +
+                                      (rr % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
           }
         }
         ptx::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          ptx::mbar_arrive_expect_tx(&full[st],
-                                     static_cast<uint32_t>(n_units * p.box_rows * 128 * kWBoxes));
+          ptx::mbar_arrive_expect_tx(
+              &full[st], static_cast<uint32_t>(2 * n_units * p.box_rows * 128 * kWBoxes));
           for (int wu = 0; wu < n_units; ++wu) {
             const int w = u_first + wu;
             const int a = uniq[w / upa];
             const int qb = (w % upa) * p.box_rows;
 #pragma unroll
-            for (int h = 0; h < kWBoxes; ++h)
-              ptx::tma_load_2d(Wr + h * 8192 + wu * p.box_rows * 128, &tm_b, &full[st],
-                               n0 + 64 * h, a * p.r + qb);
+            for (int h = 0; h < kWBoxes; ++h) {
+#pragma unroll
+              for (int half = 0; half < 2; ++half)
+                ptx::tma_load_2d(Wr + h * 8192 + (half * (kBK / 2) + wu * p.box_rows) * 128,
+                                 &tm_b, &full[st], n0 + 64 * h, a * p.r + qb);
+            }
           }
         }
         __syncwarp();
@@ -327,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < 8; ++c) f[c] += g[c];
           }
         }
-        *reinterpret_cast<uint4*>(vt + i * p.r + qc * 8) = pack8_bf16(f);
+        store8(vt + i * p.r + qc * 8, f);
       }
     }
     ptx::mbar_arrive(vt_ready);
@@ -498,7 +516,7 @@ cudaError_t launch_fused_tc(const void* x, const void* W0, const void* B, const 
   prm.n_slots = n_slots;
   prm.n_kblk = (d_in + kBK - 1) / kBK;
   prm.stages = 0;
-  prm.box_rows = r < 64 ? r : 64;
+  prm.box_rows = r < 32 ? r : 32;
   prm.v_ksplit = v_ksplit;
   prm.ids = ids;
   prm.vpart = vpart;
@@ -514,11 +532,13 @@ cudaError_t launch_fused_tc(const void* x, const void* W0, const void* B, const 
   };
   if (T <= 256) {
     const int tiles_n = (d_out + 127) / 128;
-    const int S = pick_split(tiles_n);
-    if (T <= 32) return launch_variant<true, 32, 128>(x, W0, B, prm, tiles_n, 1, S, st, dev);
-    if (T <= 64) return launch_variant<true, 64, 128>(x, W0, B, prm, tiles_n, 1, S, st, dev);
-    if (T <= 128) return launch_variant<true, 128, 128>(x, W0, B, prm, tiles_n, 1, S, st, dev);
-    return launch_variant<true, 256, 128>(x, W0, B, prm, tiles_n, 1, S, st, dev);
+    if (T <= 32) return launch_variant<true, 32, 128>(x, W0, B, prm, tiles_n, 1, pick_split(tiles_n), st, dev);
+    if (T <= 64) return launch_variant<true, 64, 128>(x, W0, B, prm, tiles_n, 1, pick_split(tiles_n), st, dev);
+    if (T <= 128) return launch_variant<true, 128, 128>(x, W0, B, prm, tiles_n, 1, pick_split(tiles_n), st, dev);
+    if (r <= 64) return launch_variant<true, 256, 128>(x, W0, B, prm, tiles_n, 1, pick_split(tiles_n), st, dev);
+    // rank 128: the fp32 v tile of 256 tokens would crowd out the pipeline,
+    // so two 128-token tiles instead
+    return launch_variant<true, 128, 128>(x, W0, B, prm, tiles_n, 2, pick_split(2 * tiles_n), st, dev);
   }
   const int tiles_n = (d_out + 255) / 256;
   const int tiles_t = (T + 127) / 128;

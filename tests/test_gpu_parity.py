@@ -154,6 +154,8 @@ FUSED_CASES = [
     (64, 512, 1024, 16, 40),
     (100, 128, 520, 64, 9),
     (128, 384, 256, 128, 4),
+    (200, 256, 264, 128, 6),
+    (96, 320, 392, 8, 21),
     (200, 640, 136, 16, 30),
     (256, 256, 512, 64, 70),
     (257, 192, 264, 16, 11),
