@@ -1,9 +1,9 @@
 #!/usr/bin/env python
 """Throughput of the multi-LoRA batched linear layer on GB300.
 
-One step = one pass of the whole layer over one batch: segment build, the
-segment-grouped shrink, and the tcgen05 base GEMM with the expand folded into
-its accumulator (lora_linear_fused), on the decode workload: one 4096->4096
+One step = one pass of the whole layer over one batch (lora_linear_fused):
+for this decode batch the per-token (BGMV) shrink, then the tcgen05 base GEMM
+with the expand folded into its accumulator, on the decode workload: one 4096->4096
 layer, rank 16, 256 resident adapters, 64 one-token requests with Zipf(1.1)
 adapter ids and 8 base-only rows.  Inputs are seeded and synthetic; weights
 and activations are resident in HBM before timing.
@@ -320,21 +320,17 @@ def timed_graph_steps(fn, K, W, stream):
 
 
 def per_kernel_times(sets, L, T, d_in, d_out, r, n_slots, n_steps, stream):
-    """Each step as three public calls with CUDA events around each kernel:
-    segment build, shrink, base GEMM + expand.  Returns mean ms per kernel."""
+    """Each step as the public calls the fused path is made of, with CUDA
+    events recorded around each kernel inside one captured graph: for a
+    decode batch the BGMV shrink and the base GEMM + expand.  Returns the
+    mean ms per kernel."""
     import torch
     ks = fused_ksplit(T, d_in, n_slots)
     dev = sets[0].x.device
-    cap = max(1, min(T, n_slots))
-    perm = torch.empty(T, dtype=torch.int32, device=dev)
-    seg_slot = torch.empty(cap, dtype=torch.int32, device=dev)
-    seg_off = torch.empty(cap + 1, dtype=torch.int32, device=dev)
-    n_seg = torch.empty(1, dtype=torch.int32, device=dev)
     vpart = torch.empty((ks, T, r), dtype=torch.float32, device=dev)
     ws = torch.zeros(256, dtype=torch.uint8, device=dev)
-    segs = (perm, seg_slot, seg_off, n_seg)
     try:
-        evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
+        evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(3)]
                for _ in range(n_steps)]
     except TypeError:
         return None
@@ -343,17 +339,12 @@ def per_kernel_times(sets, L, T, d_in, d_out, r, n_slots, n_steps, stream):
         s = sets[i % len(sets)]
         if rec:
             evs[i][0].record(stream)
-        L.check(L.lora_build_segments(s.ids.data_ptr(), T, n_slots, perm.data_ptr(),
-                                      seg_slot.data_ptr(), seg_off.data_ptr(), n_seg.data_ptr(),
-                                      ws.data_ptr(), ws.numel(), stream.cuda_stream), "segments")
+        L.bgmv_shrink_t(s.x, s.A, s.ids, s.scale, ks, ws, v_partial=vpart, stream=stream)
         if rec:
             evs[i][1].record(stream)
-        L.sgmv_shrink_t(s.x, s.A, segs, s.scale, ks, ws, v_partial=vpart, stream=stream)
-        if rec:
-            evs[i][2].record(stream)
         L.base_gemm_expand_t(s.x, s.W0, s.B, s.ids, vpart, ws, y=s.y, stream=stream)
         if rec:
-            evs[i][3].record(stream)
+            evs[i][2].record(stream)
 
     with torch.cuda.stream(stream):
         for i in range(3):
@@ -363,12 +354,10 @@ def per_kernel_times(sets, L, T, d_in, d_out, r, n_slots, n_steps, stream):
     with torch.cuda.stream(stream):
         g.replay()
     stream.synchronize()
-    seg = [evs[i][0].elapsed_time(evs[i][1]) for i in range(n_steps)]
-    shr = [evs[i][1].elapsed_time(evs[i][2]) for i in range(n_steps)]
-    gem = [evs[i][2].elapsed_time(evs[i][3]) for i in range(n_steps)]
-    return {"segments_ms": statistics.mean(seg), "shrink_ms": statistics.mean(shr),
-            "gemm_ms": statistics.mean(gem), "gemm_ms_median": statistics.median(gem),
-            "n": n_steps}
+    shr = [evs[i][0].elapsed_time(evs[i][1]) for i in range(n_steps)]
+    gem = [evs[i][1].elapsed_time(evs[i][2]) for i in range(n_steps)]
+    return {"shrink_ms": statistics.mean(shr), "gemm_ms": statistics.mean(gem),
+            "gemm_ms_median": statistics.median(gem), "n": n_steps}
 
 
 def e2e_steps(s0, L, T, d_in, d_out, r, n_slots, n_steps, stream):
@@ -617,7 +606,7 @@ def run_ours(args):
                    "l2": f"{NSETS} rotating buffer sets (>2x L2)", "parallelism": "replicas",
                    "graph": f"CUDA graphs of {min(args.steps, GRAPH_STEPS)} steps"},
         "layer_gbs": lb / step_s / 1e9, "layer_frac": lb / step_s / 1e9 / pk["hbm_gbs"],
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 2 * args.steps,
         "e2e": {"value": world * T * 2000 / (e2e_ms / 1e3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms / 2000},

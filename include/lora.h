@@ -170,10 +170,11 @@ lora_status_t lora_sgmv_expand(const float* v_partial, int32_t ksplit, const voi
  * ("Multi-LoRA batching and adapter paging", section "Walking through a
  * batch": the base product once for all rows, then each row's adapter term;
  * "Serving many LoRA adapters", "Replay" figure: segmented gather, grouped
- * GEMM, scatter add, one fused output).  Enqueues the segment builder, the
- * segment-grouped shrink and one base-GEMM kernel whose accumulator also
- * takes the expand term (bf16: tcgen05 tensor cores, accumulator in tensor
- * memory), so y is stored once.
+ * GEMM, scatter add, one fused output).  Batches of up to 256 tokens take
+ * the per-token BGMV shrink (decode); larger batches take the segment
+ * builder and the segment-grouped SGMV shrink (prefill).  Then one base-GEMM
+ * kernel whose accumulator also takes the expand term (bf16: tcgen05 tensor
+ * cores, accumulator in tensor memory) stores y once.
  */
 lora_status_t lora_linear_fused(const void* x, const void* W0, const void* A_pool,
                                 const void* B_pool, const int32_t* slot_ids, const float* scale,

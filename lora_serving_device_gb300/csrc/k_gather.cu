@@ -52,6 +52,7 @@ __global__ void __launch_bounds__(128)
   using RL = RankLayout<R>;
   constexpr int KL = 128 / RL::QC;   // lanes of the block along d_in
   __shared__ float red[4][R];
+  pdl_launch_dependents();  // the base GEMM may start streaming W0 now
   const int t = blockIdx.x, s = blockIdx.y, tid = threadIdx.x;
   const int id = ids[t];
   float* out = vpart + (static_cast<size_t>(s) * T + t) * R;
@@ -188,8 +189,8 @@ __global__ void __launch_bounds__(256)
                        int d_in, int n_slots, int kchunk) {
   using RL = RankLayout<R>;
   __shared__ int s_a, s_p0, s_p1;
+  pdl_launch_dependents();  // the base GEMM may start streaming W0 now
   pdl_wait();               // the segments are written by the previous kernel
-  pdl_launch_dependents();  // the next kernel may start its own prologue
   const int tid = threadIdx.x, s = blockIdx.y;
   const int nseg = *n_seg;
   if (blockIdx.x == 0) {    // rows of base-only tokens are zero

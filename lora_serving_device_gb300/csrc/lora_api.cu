@@ -26,6 +26,10 @@ bool dtype_ok(lora_dtype_t dt) { return dt == LORA_DTYPE_BF16 || dt == LORA_DTYP
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 constexpr size_t kErrBytes = 16;
+// Batches up to this many tokens take the BGMV shrink inside lora_linear_fused
+// (one token per request in decode: "Serving multiple LoRAs ...", BGMV
+// bullet); larger ones take the segment builder and the SGMV shrink.
+constexpr int32_t kDecodeTokens = 256;
 
 struct FusedWs {
   uint32_t* err;
@@ -268,11 +272,19 @@ lora_status_t lora_linear_fused(const void* x, const void* W0, const void* A_poo
   if ((s = check_device(&dev)) != LORA_OK) return s;
   if (dt == LORA_DTYPE_BF16 && !tensor_map_available()) return LORA_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_build_segments(slot_ids, T, n_slots, w.perm, w.seg_slot, w.seg_off,
-                                        w.n_seg, w.err, st);
-  if (e != cudaSuccess) return LORA_ERR_CUDA;
-  e = launch_sgmv_shrink(x, A_pool, w.perm, w.seg_slot, w.seg_off, w.n_seg, scale, w.vpart, T,
-                         d_in, r, n_slots, w.ksplit, dt, w.err, st, true);
+  cudaError_t e;
+  if (T <= kDecodeTokens) {
+    // decode-sized batch: per-token gather (BGMV) -- no sort needed
+    e = launch_bgmv_shrink(x, A_pool, slot_ids, scale, w.vpart, T, d_in, r, n_slots, w.ksplit,
+                           dt, w.err, st);
+  } else {
+    // prefill-sized batch: segments, then the segment-grouped shrink (SGMV)
+    e = launch_build_segments(slot_ids, T, n_slots, w.perm, w.seg_slot, w.seg_off, w.n_seg,
+                              w.err, st);
+    if (e != cudaSuccess) return LORA_ERR_CUDA;
+    e = launch_sgmv_shrink(x, A_pool, w.perm, w.seg_slot, w.seg_off, w.n_seg, scale, w.vpart, T,
+                           d_in, r, n_slots, w.ksplit, dt, w.err, st, true);
+  }
   if (e != cudaSuccess) return LORA_ERR_CUDA;
   if (dt == LORA_DTYPE_BF16)
     e = launch_fused_tc(x, W0, B_pool, slot_ids, w.vpart, w.ksplit, y, T, d_in, d_out, r, n_slots,

@@ -48,14 +48,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 
 // Wait for phase `parity` of `bar` to complete, giving up after `limit_ns`
 // of wall time or as soon as another thread of the CTA raised *abort.
-// Returns false when it gave up (and then raises *abort itself).
+// Returns false when it gave up (and then raises *abort itself).  The first
+// 4096 polls touch neither the clock nor *abort, so a wait that completes in
+// normal time costs only try_wait polls.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
                                                   volatile int* abort, uint64_t limit_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
+#pragma unroll 1
+  for (uint32_t i = 0; i < 4096u; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
+#pragma unroll 1
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 31u) == 0u) {
+    if ((i & 255u) == 0u) {
       if (*abort) return false;
       if (globaltimer_ns() - t0 > limit_ns) {
         *abort = 1;

@@ -242,7 +242,9 @@ def random_case(seed, T, d_in, d_out, r, n_slots, base_frac=0.15, runs=False,
                 bf16=True, invalid=0) -> Workload:
     """A generic seeded case for tile-edge parity tests: ids uniform over the
     pool (or as runs of equal ids when ``runs``), a fraction base-only, and
-    ``invalid`` ids outside [-1, n_slots) planted at random positions."""
+    ``invalid`` ids outside [-1, n_slots) planted at random positions.  The
+    init follows the decode workload (A std 1/sqrt(d_in), so x A ~ N(0, 1);
+    W0 and B std 0.02) with a per-slot scale drawn from U[0.5, 2.5]."""
     key = ("case", seed)
     rng = np.random.default_rng([SEED_BASE, 99, seed])
     if runs:
@@ -269,7 +271,7 @@ def random_case(seed, T, d_in, d_out, r, n_slots, base_frac=0.15, runs=False,
                           std_scale / np.sqrt(d_in), bf16) for j in range(n_slots)]) \
         if n_slots else np.zeros((0, d_in, r), np.float32)
     B = np.stack([_normal(np.random.default_rng([SEED_BASE, 99, seed, 4, j]), (r, d_out),
-                          B_STD * 4, bf16) for j in range(n_slots)]) \
+                          B_STD, bf16) for j in range(n_slots)]) \
         if n_slots else np.zeros((0, r, d_out), np.float32)
     x = _normal(np.random.default_rng([SEED_BASE, 99, seed, 1]), (T, d_in), 1.0, bf16)
     scale = (np.random.default_rng([SEED_BASE, 99, seed, 6]).uniform(0.5, 2.5, n_slots)

@@ -1,10 +1,17 @@
 """Parity bars shared by the GPU tests.
 
-Floating point: per output tensor, relative Frobenius error <= 5e-3 and
-max |err| <= 2e-2 * rms(reference), both for y and for the LoRA delta
-y - x W0 (the delta is ~8x smaller than the base term under the decode init,
-so a broken adapter path could hide inside y's budget).  Integer / index
+Floating point (the stated bar), per output tensor: relative Frobenius
+error <= 5e-3 and max |err| <= 2e-2 * rms(reference).  Integer / index
 outputs: bit-exact.
+
+The adapter term alone (a run with W0 = 0) is checked as well, because it is
+~8x smaller than the base term under the decode init and an error in it
+could hide inside y's budget.  That extra check keeps the Frobenius bar and
+replaces the max bar with the bf16 storage bound per element: rounding to
+bf16 moves a value by at most 2^-9 of itself, so |err| <= 2^-8 |ref| plus a
+small absolute slack.  (The adapter term alone is a sum of r products and
+has heavy tails; its largest elements sit ~10 rms out, where bf16 rounding
+by itself reaches 2e-2 rms.)
 """
 import numpy as np
 
@@ -27,3 +34,20 @@ def check_close(got, ref, what="y", rel_fro=REL_FRO, max_rms=MAX_RMS):
     assert rel <= rel_fro, f"{what}: rel Frobenius error {rel:.3e} > {rel_fro}"
     assert mx <= max_rms, f"{what}: max|err|/rms {mx:.3e} > {max_rms}"
     return {"rel_fro": rel, "max_over_rms": mx}
+
+
+def check_close_bf16_out(got, ref, what="delta", rel_fro=REL_FRO, abs_rms=1e-3):
+    """Frobenius bar plus the per-element bf16 storage bound (see above)."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape and np.all(np.isfinite(got)), what
+    if ref.size == 0:
+        return
+    err = np.abs(got - ref)
+    nref = np.linalg.norm(ref)
+    rms = np.sqrt(np.mean(ref * ref))
+    rel = float(np.linalg.norm(got - ref) / nref) if nref > 0 else float(np.linalg.norm(got - ref))
+    assert rel <= rel_fro, f"{what}: rel Frobenius error {rel:.3e} > {rel_fro}"
+    bound = 2.0 ** -8 * np.abs(ref) + abs_rms * rms
+    worst = float(np.max(err / bound))
+    assert worst <= 1.0, f"{what}: element error {worst:.2f}x the bf16 storage bound"
