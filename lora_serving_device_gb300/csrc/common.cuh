@@ -54,6 +54,29 @@ __device__ __forceinline__ void store8(float* p, const float f[8]) {
   reinterpret_cast<float4*>(p)[1] = make_float4(f[4], f[5], f[6], f[7]);
 }
 
+// Loads of data written by the kernel this one depends on through a
+// programmatic (early) launch.  Such data is not read-only for this kernel's
+// lifetime, so it must not go through __restrict__ / non-coherent loads; an
+// asm volatile L2 load also cannot be hoisted above griddepcontrol.wait.
+__device__ __forceinline__ int ld_dep(const int32_t* p) {
+  int v;
+  asm volatile("ld.global.cg.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ float4 ld_dep_f4(const float* p) {
+  float4 v;
+  asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ void load8_dep(const float* p, float f[8]) {
+  const float4 a = ld_dep_f4(p), b = ld_dep_f4(p + 4);
+  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+  f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+
 __device__ __forceinline__ void flag_error(uint32_t* err, uint32_t bits) {
   if (err != nullptr) atomicOr(err, bits);
 }

@@ -14,7 +14,7 @@ constexpr int kBM = 32, kBN = 64, kBK = 32;
 __global__ void __launch_bounds__(256)
     fused_f32_kernel(const float* __restrict__ x, const float* __restrict__ W0,
                      const float* __restrict__ B, const int32_t* __restrict__ ids,
-                     const float* __restrict__ vpart, int v_ksplit, float* __restrict__ y, int T,
+                     const float* vpart, int v_ksplit, float* __restrict__ y, int T,
                      int d_in, int d_out, int r, int n_slots, uint32_t* err) {
   __shared__ float xs[kBM][kBK + 1];
   __shared__ float ws[kBK][kBN];
@@ -51,7 +51,12 @@ __global__ void __launch_bounds__(256)
     if (slot_valid(id, n_slots)) {
       for (int q = 0; q < r; ++q) {
         float vq = 0.f;
-        for (int s = 0; s < v_ksplit; ++s) vq += vpart[(static_cast<size_t>(s) * T + t) * r + q];
+        for (int s = 0; s < v_ksplit; ++s) {
+          const float* vp = vpart + (static_cast<size_t>(s) * T + t) * r + q;
+          float v;
+          asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(vp) : "memory");
+          vq += v;
+        }
         const float* Bq = B + (static_cast<size_t>(id) * r + q) * d_out;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {

@@ -340,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int t = t0 + i;
           for (int s = 0; s < p.v_ksplit; ++s) {
             float g[8];
-            load8(p.vpart + (static_cast<size_t>(s) * p.T + t) * p.r + qc * 8, g);
+            load8_dep(p.vpart + (static_cast<size_t>(s) * p.T + t) * p.r + qc * 8, g);
 #pragma unroll
             for (int c = 0; c < 8; ++c) f[c] += g[c];
           }

@@ -142,7 +142,8 @@ __device__ void sgmv_item(int item, const int32_t* seg_slot, const int32_t* seg_
   const int per = (nseg + nt - 1) / nt;
   const int j0 = min(nseg, tid * per), j1 = min(nseg, j0 + per);
   int c = 0;
-  for (int j = j0; j < j1; ++j) c += (seg_off[j + 1] - seg_off[j] + kSgTokens - 1) / kSgTokens;
+  for (int j = j0; j < j1; ++j)
+    c += (ld_dep(seg_off + j + 1) - ld_dep(seg_off + j) + kSgTokens - 1) / kSgTokens;
   int incl = c;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -166,10 +167,10 @@ __device__ void sgmv_item(int item, const int32_t* seg_slot, const int32_t* seg_
   if (item >= first && item < first + c) {
     int x = item - first;
     for (int j = j0; j < j1; ++j) {
-      const int o0 = seg_off[j], o1 = seg_off[j + 1];
+      const int o0 = ld_dep(seg_off + j), o1 = ld_dep(seg_off + j + 1);
       const int cj = (o1 - o0 + kSgTokens - 1) / kSgTokens;
       if (x < cj) {
-        *s_a = seg_slot[j];
+        *s_a = ld_dep(seg_slot + j);
         *s_p0 = o0 + x * kSgTokens;
         *s_p1 = min(o1, *s_p0 + kSgTokens);
         break;
@@ -182,9 +183,8 @@ __device__ void sgmv_item(int item, const int32_t* seg_slot, const int32_t* seg_
 
 template <typename E, int R>
 __global__ void __launch_bounds__(256)
-    sgmv_shrink_kernel(const E* __restrict__ x, const E* __restrict__ A,
-                       const int32_t* __restrict__ perm, const int32_t* __restrict__ seg_slot,
-                       const int32_t* __restrict__ seg_off, const int32_t* __restrict__ n_seg,
+    sgmv_shrink_kernel(const E* __restrict__ x, const E* __restrict__ A, const int32_t* perm,
+                       const int32_t* seg_slot, const int32_t* seg_off, const int32_t* n_seg,
                        const float* __restrict__ scale, float* __restrict__ vpart, int T,
                        int d_in, int n_slots, int kchunk) {
   using RL = RankLayout<R>;
@@ -192,11 +192,11 @@ __global__ void __launch_bounds__(256)
   pdl_launch_dependents();  // the base GEMM may start streaming W0 now
   pdl_wait();               // the segments are written by the previous kernel
   const int tid = threadIdx.x, s = blockIdx.y;
-  const int nseg = *n_seg;
+  const int nseg = ld_dep(n_seg);
   if (blockIdx.x == 0) {    // rows of base-only tokens are zero
-    const int nbase = seg_off[0];
+    const int nbase = ld_dep(seg_off);
     for (int e = tid; e < nbase * R; e += 256)
-      vpart[(static_cast<size_t>(s) * T + perm[e / R]) * R + (e % R)] = 0.f;
+      vpart[(static_cast<size_t>(s) * T + ld_dep(perm + e / R)) * R + (e % R)] = 0.f;
   }
   sgmv_item(blockIdx.x, seg_slot, seg_off, nseg, &s_a, &s_p0, &s_p1);
   const int a = s_a;
@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(256)
     const int nt = min(4, p1 - pb);
     int tok[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) tok[u] = (u < nt) ? perm[pb + u] : perm[pb];
+    for (int u = 0; u < 4; ++u) tok[u] = ld_dep(perm + pb + ((u < nt) ? u : 0));
     float acc[4][8];
 #pragma unroll
     for (int u = 0; u < 4; ++u)
@@ -251,20 +251,19 @@ __global__ void __launch_bounds__(256)
 template <typename E, int R>
 __global__ void __launch_bounds__(256)
     sgmv_expand_kernel(const float* __restrict__ vpart, int ksplit, const E* __restrict__ B,
-                       const int32_t* __restrict__ perm, const int32_t* __restrict__ seg_slot,
-                       const int32_t* __restrict__ seg_off, const int32_t* __restrict__ n_seg,
-                       E* __restrict__ y, int T, int d_out, int n_slots) {
+                       const int32_t* perm, const int32_t* seg_slot, const int32_t* seg_off,
+                       const int32_t* n_seg, E* __restrict__ y, int T, int d_out, int n_slots) {
   __shared__ float vs[kSgTokens][R];
   __shared__ int s_tok[kSgTokens];
   __shared__ int s_a, s_p0, s_p1;
   const int tid = threadIdx.x;
-  sgmv_item(blockIdx.x, seg_slot, seg_off, *n_seg, &s_a, &s_p0, &s_p1);
+  sgmv_item(blockIdx.x, seg_slot, seg_off, ld_dep(n_seg), &s_a, &s_p0, &s_p1);
   const int a = s_a;
   if (a < 0) return;
   const int p0 = s_p0, L = s_p1 - s_p0;
   for (int e = tid; e < L * R; e += 256) {
     const int i = e / R, q = e % R;
-    const int t = perm[p0 + i];
+    const int t = ld_dep(perm + p0 + i);
     float acc = 0.f;
     for (int s = 0; s < ksplit; ++s) acc += vpart[(static_cast<size_t>(s) * T + t) * R + q];
     vs[i][q] = acc;

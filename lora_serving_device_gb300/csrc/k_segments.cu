@@ -80,9 +80,6 @@ __global__ void __launch_bounds__(kThreads)
   int32_t* cnt = sm;              // [P][nb]: per-partition histogram -> offsets
   int32_t* start = sm + P * nb;   // [nb + 1]: per-bin totals -> first positions
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // a programmatic dependent (the SGMV shrink) may launch now; it waits for
-  // this grid to complete before it reads the segments
-  pdl_launch_dependents();
 
   for (int i = tid; i < P * nb + nb + 1; i += blockDim.x) sm[i] = 0;
   if (tid == 0) bad = 0;

@@ -175,7 +175,7 @@ def test_fused_matches_oracle(L, case):
         y, ws = d.fused()
         torch.cuda.synchronize()
         ref = O.lora_linear(w.x, w.W0, w.A_pool, w.B_pool, w.scale, w.slot_ids)
-        check_close(host(y), ref, f"y runs={runs}")
+        check_close_bf16_out(host(y), ref, f"y runs={runs}")
         assert L.get_error_t(ws) == 0
         # the adapter path alone (W0 = 0), so bf16 rounding of the base term
         # cannot hide an error in it

