@@ -55,6 +55,8 @@ struct TcParams {
   int n_kblk;    // ceil(d_in / 64)
   int stages;
   int box_rows;  // rows of one B_pool TMA box: min(r, 32)
+  int lg_box;    // log2(box_rows)
+  int lg_upa;    // log2(r / box_rows)
   int v_ksplit;
   const int32_t* ids;
   const float* vpart;
@@ -101,6 +103,11 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
+// Named barrier among the four epilogue warps only (barrier 0 is __syncthreads).
+__device__ __forceinline__ void epi_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+}
+
 template <bool SWAP, int BT, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     fused_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
@@ -133,9 +140,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n0 = blockIdx.x * BN, t0 = blockIdx.y * BT;
   const int S = static_cast<int>(gridDim.z), z = static_cast<int>(blockIdx.z);
-  const int n_words = (p.n_slots + 31) >> 5;
 
-  // ---- prologue: barriers, the tile's slot ids, TMEM --------------------
+  // ---- prologue: barriers and TMEM only; the TMA stream starts at once ----
   if (tid == 0) {
     for (int i = 0; i < p.stages; ++i) {
       ptx::mbar_init(&full[i], 1);
@@ -151,132 +157,100 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::prefetch_tmap(&tm_w);
     ptx::prefetch_tmap(&tm_b);
   }
-  bool bad = false;
-  for (int i = tid; i < BT; i += kThreads) {
-    const int t = t0 + i;
-    int s = -1;
-    if (t < p.T) {
-      const int id = p.ids[t];
-      if (slot_valid(id, p.n_slots)) s = id;
-      else if (id != -1) bad = true;
-    }
-    tok[i] = s;
-  }
-  for (int w = tid; w < n_words; w += kThreads) bitmap[w] = 0u;
-  if (bad && blockIdx.x == 0 && z == 0) flag_error(p.err, LORA_DEVERR_BAD_SLOT);
   if (warp == 1) {
     ptx::tmem_alloc(tmem_slot, kTmemCols);
     ptx::tmem_relinquish();
   }
-  __syncthreads();
-  for (int i = tid; i < BT; i += kThreads) {
-    const int s = tok[i];
-    if (s >= 0) atomicOr(&bitmap[s >> 5], 1u << (s & 31));
-  }
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
-  if (warp == 0) {  // distinct adapters of the tile, ascending slot order
-    const int per = (n_words + 31) / 32;
-    const int w0 = min(n_words, lane * per), w1 = min(n_words, w0 + per);
-    int c = 0;
-    for (int w = w0; w < w1; ++w) c += __popc(bitmap[w]);
-    int incl = c;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    int off = incl - c;
-    for (int w = w0; w < w1; ++w) {
-      uint32_t m = bitmap[w];
-      while (m) {
-        const int b = __ffs(m) - 1;
-        m &= m - 1;
-        uniq[off++] = w * 32 + b;
-      }
-    }
-    if (lane == 31) *n_uniq_s = incl;
-  }
-  __syncthreads();
 
   const uint32_t tmem = *tmem_slot;
-  const int n_uniq = *n_uniq_s;
-  const int upa = p.r / p.box_rows;      // TMA boxes per adapter (r / min(r, 32))
-  const int G = (kBK / 2) / p.box_rows;  // boxes per LoRA K-block (each used twice)
-  const int U = n_uniq * upa;
-  const int n_groups = (U + G - 1) / G;
-  const int my_groups = (z < n_groups) ? (n_groups - z + S - 1) / S : 0;
+  const int upa = p.r >> p.lg_box;       // TMA boxes per adapter (r / min(r, 32))
+  const int G = (kBK / 2) >> p.lg_box;   // boxes per LoRA K-block (each used twice)
   const int kb0 = static_cast<int>(static_cast<long long>(z) * p.n_kblk / S);
   const int kb1 = static_cast<int>(static_cast<long long>(z + 1) * p.n_kblk / S);
   const int nbase = kb1 - kb0;
-  const int n_iter = nbase + my_groups;
+  // LoRA K-blocks of this CTA; known once the epilogue warps published the
+  // tile's adapter list (vt_ready)
+  auto lora_groups = [&](int* U_out) {
+    const int U = *n_uniq_s * upa;
+    *U_out = U;
+    const int n_groups = (U + G - 1) / G;
+    return (z < n_groups) ? (n_groups - z + S - 1) / S : 0;
+  };
 
   if (warp == 0) {
     // ---------------- producer -------------------------------------------
-    bool vt_ok = false;
-    for (int it = 0; it < n_iter; ++it) {
+    int it = 0;
+    bool ok = true;
+    for (; it < nbase; ++it) {
       const int st = it % p.stages;
       const uint32_t ph = static_cast<uint32_t>(it / p.stages) & 1u;
-      if (!warp_wait(&empty[st], ph ^ 1u, abort_f)) break;
+      if (!warp_wait(&empty[st], ph ^ 1u, abort_f)) {
+        ok = false;
+        break;
+      }
       uint8_t* X = smem + static_cast<size_t>(st) * L.stage_bytes;
       uint8_t* Wr = X + L.x_bytes;
-      if (it < nbase) {
-        if (lane == 0) {
-          const int kb = kb0 + it;
-          ptx::mbar_arrive_expect_tx(&full[st], L.stage_bytes);
-          ptx::tma_load_2d(X, &tm_x, &full[st], kb * kBK, t0);
+      if (lane == 0) {
+        const int kb = kb0 + it;
+        ptx::mbar_arrive_expect_tx(&full[st], L.stage_bytes);
+        ptx::tma_load_2d(X, &tm_x, &full[st], kb * kBK, t0);
 #pragma unroll
-          for (int h = 0; h < kWBoxes; ++h)
-            ptx::tma_load_2d(Wr + h * 8192, &tm_w, &full[st], n0 + 64 * h, kb * kBK);
-        }
-        __syncwarp();
-      } else {
-        if (!vt_ok) {
-          if (!warp_wait(vt_ready, 0, abort_f)) break;
-          vt_ok = true;
-        }
-        const int g = z + (it - nbase) * S;
-        const int u_first = g * G;
+        for (int h = 0; h < kWBoxes; ++h)
+          ptx::tma_load_2d(Wr + h * 8192, &tm_w, &full[st], n0 + 64 * h, kb * kBK);
+      }
+      __syncwarp();
+    }
+    if (ok && warp_wait(vt_ready, 0, abort_f)) {
+      int U;
+      const int my_groups = lora_groups(&U);
+      // This lane always writes the same 16-byte chunk c of a row; which K
+      // rows that chunk holds is fixed per K-block.
+      const int c = lane & 7;
+      const bool lo_half = c >= 4;
+      const int kq = (c & 3) << 3;          // K offset inside the hi or lo half
+      const int wu = kq >> p.lg_box;        // box (unit) of this chunk
+      for (int gi = 0; gi < my_groups; ++gi, ++it) {
+        const int st = it % p.stages;
+        const uint32_t ph = static_cast<uint32_t>(it / p.stages) & 1u;
+        if (!warp_wait(&empty[st], ph ^ 1u, abort_f)) break;
+        uint8_t* X = smem + static_cast<size_t>(st) * L.stage_bytes;
+        uint8_t* Wr = X + L.x_bytes;
+        const int u_first = (z + gi * S) * G;
         const int n_units = min(G, U - u_first);
+        const int w = u_first + wu;
+        const int uw = (wu < n_units) ? (w >> p.lg_upa) : -2;     // adapter index
+        const int q0 = ((w & (upa - 1)) << p.lg_box) + (kq & (p.box_rows - 1));
         // masked V operand (K-major, 128-byte swizzle written by hand).
         // v is fp32; it enters the bf16 MMA as v = hi + lo with hi = bf16(v)
         // and lo = bf16(v - hi), so the expand keeps ~16 mantissa bits.  K
         // rows [0, 32) carry the hi parts of this block's adapters, rows
         // [32, 64) the lo parts, each against its own copy of the B rows.
-        // Row i, K index kk -> part of v[token i][q] if token i uses the
-        // adapter of that K row, else 0.
-        for (int e = lane; e < BT * 8; e += 32) {
-          const int i = e >> 3, c = e & 7;
-          const int kq = (c & 3) * 8;  // K offset inside the hi or lo half
-          const int wu = kq / p.box_rows;
+        // Row i holds the v of token i where token i uses that adapter, else 0.
+        for (int i = lane >> 3; i < BT; i += 4) {
           uint4 val = make_uint4(0u, 0u, 0u, 0u);
-          if (wu < n_units) {
-            const int w = u_first + wu;
-            const int u = w / upa;
-            const int q0 = (w % upa) * p.box_rows + (kq % p.box_rows);
-            if (tok[i] == uniq[u]) {
-              float f[8];
-              load8(vt + i * p.r + q0, f);
-              float h[8], l[8];
+          if (tok[i] == uw) {
+            float f[8], h[8], l[8];
+            load8(vt + i * p.r + q0, f);
 #pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                h[j] = __bfloat162float(__float2bfloat16_rn(f[j]));
-                l[j] = f[j] - h[j];
-              }
-              val = pack8_bf16(c < 4 ? h : l);
+            for (int j = 0; j < 8; ++j) {
+              h[j] = __bfloat162float(__float2bfloat16_rn(f[j]));
+              l[j] = f[j] - h[j];
             }
+            val = pack8_bf16(lo_half ? l : h);
           }
           *reinterpret_cast<uint4*>(X + i * 128 + ((c ^ (i & 7)) << 4)) = val;
         }
         // K rows of the W side that no adapter fills this time are zeroed
-        const int used = n_units * p.box_rows;
+        const int used = n_units << p.lg_box;
         if (used < kBK / 2) {
           const int per_half = (kBK / 2 - used) * 8;
           for (int e = lane; e < 2 * per_half * kWBoxes; e += 32) {
-            const int h = e / (2 * per_half), rem = e % (2 * per_half);
+            const int hb = e / (2 * per_half), rem = e % (2 * per_half);
             const int half = rem / per_half, rr = rem % per_half;
-            *reinterpret_cast<uint4*>(Wr + h * 8192 + (half * (kBK / 2) + used + rr / 8) * 128 +
+            *reinterpret_cast<uint4*>(Wr + hb * 8192 + (half * (kBK / 2) + used + rr / 8) * 128 +
                                       (rr % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
           }
         }
@@ -285,16 +259,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
           ptx::mbar_arrive_expect_tx(
               &full[st], static_cast<uint32_t>(2 * n_units * p.box_rows * 128 * kWBoxes));
-          for (int wu = 0; wu < n_units; ++wu) {
-            const int w = u_first + wu;
-            const int a = uniq[w / upa];
-            const int qb = (w % upa) * p.box_rows;
+          for (int u = 0; u < n_units; ++u) {
+            const int wv = u_first + u;
+            const int a = uniq[wv >> p.lg_upa];
+            const int qb = (wv & (upa - 1)) << p.lg_box;
 #pragma unroll
-            for (int h = 0; h < kWBoxes; ++h) {
+            for (int hb = 0; hb < kWBoxes; ++hb) {
 #pragma unroll
               for (int half = 0; half < 2; ++half)
-                ptx::tma_load_2d(Wr + h * 8192 + (half * (kBK / 2) + wu * p.box_rows) * 128,
-                                 &tm_b, &full[st], n0 + 64 * h, a * p.r + qb);
+                ptx::tma_load_2d(Wr + hb * 8192 + (half * (kBK / 2) + u * p.box_rows) * 128,
+                                 &tm_b, &full[st], n0 + 64 * hb, a * p.r + qb);
             }
           }
         }
@@ -304,10 +278,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ---------------- MMA issuer -----------------------------------------
     if (lane == 0) {
-      for (int it = 0; it < n_iter; ++it) {
+      auto consume = [&](int it) {
         const int st = it % p.stages;
         const uint32_t ph = static_cast<uint32_t>(it / p.stages) & 1u;
-        if (!ptx::mbar_wait_bounded(&full[st], ph, abort_f, kWaitLimitNs)) break;
+        if (!ptx::mbar_wait_bounded(&full[st], ph, abort_f, kWaitLimitNs)) return false;
         ptx::tc_fence_after();
         const uint32_t xa = ptx::smem_u32(smem + static_cast<size_t>(st) * L.stage_bytes);
         const uint32_t wa = xa + L.x_bytes;
@@ -323,6 +297,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           else ptx::mma_bf16(tmem, xd, wd, kIdesc, accum);
         }
         ptx::mma_commit(&empty[st]);
+        return true;
+      };
+      int it = 0;
+      bool ok = true;
+      for (; it < nbase && ok; ++it) ok = consume(it);
+      if (ok && ptx::mbar_wait_bounded(vt_ready, 0, abort_f, kWaitLimitNs)) {
+        int U;
+        const int my_groups = lora_groups(&U);
+        for (int gi = 0; gi < my_groups && ok; ++gi, ++it) ok = consume(it);
       }
       ptx::mma_commit(accum_full);
     }
@@ -330,13 +313,74 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ---------------- epilogue warps -------------------------------------
     const int etid = tid - 64;
+    const int n_words = (p.n_slots + 31) >> 5;
+    // the tile's slot ids and its distinct adapters (ascending slot order),
+    // built while the main loop streams W0
+    bool bad = false;
+    for (int i = etid; i < BT; i += kEpiThreads) {
+      const int t = t0 + i;
+      int sl = -1;
+      if (t < p.T) {
+        const int id = p.ids[t];
+        if (slot_valid(id, p.n_slots)) sl = id;
+        else if (id != -1) bad = true;
+      }
+      tok[i] = sl;
+    }
+    for (int wd = etid; wd < n_words; wd += kEpiThreads) bitmap[wd] = 0u;
+    if (bad && blockIdx.x == 0 && z == 0) flag_error(p.err, LORA_DEVERR_BAD_SLOT);
+    epi_sync();
+    for (int i = etid; i < BT; i += kEpiThreads) {
+      const int sl = tok[i];
+      if (sl >= 0) atomicOr(&bitmap[sl >> 5], 1u << (sl & 31));
+    }
+    epi_sync();
+    if (warp == 2) {
+      const int per = (n_words + 31) / 32;
+      const int w0 = min(n_words, lane * per), w1 = min(n_words, w0 + per);
+      int cnt = 0;
+      for (int wd = w0; wd < w1; ++wd) cnt += __popc(bitmap[wd]);
+      int incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      int off = incl - cnt;
+      for (int wd = w0; wd < w1; ++wd) {
+        uint32_t m = bitmap[wd];
+        while (m) {
+          const int b = __ffs(m) - 1;
+          m &= m - 1;
+          uniq[off++] = wd * 32 + b;
+        }
+      }
+      if (lane == 31) *n_uniq_s = incl;
+    }
+    epi_sync();
+    const int n_uniq = *n_uniq_s;
+    // tok[i] becomes the index of token i's adapter in uniq (-1: none)
+    for (int i = etid; i < BT; i += kEpiThreads) {
+      const int sl = tok[i];
+      int u = -1;
+      if (sl >= 0) {
+        int lo = 0, hi = n_uniq - 1;
+        while (lo < hi) {
+          const int mid = (lo + hi) >> 1;
+          if (uniq[mid] < sl) lo = mid + 1;
+          else hi = mid;
+        }
+        u = lo;
+      }
+      tok[i] = u;
+    }
     pdl_wait();  // v is written by the shrink kernel launched just before
     if (n_uniq > 0) {
       const int qcn = p.r / 8;
       for (int e = etid; e < BT * qcn; e += kEpiThreads) {
         const int i = e / qcn, qc = e % qcn;
         float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        if (tok[i] >= 0) {
+        if (t0 + i < p.T && tok[i] >= 0) {
           const int t = t0 + i;
           for (int s = 0; s < p.v_ksplit; ++s) {
             float g[8];
@@ -348,6 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         store8(vt + i * p.r + qc * 8, f);
       }
     }
+    epi_sync();
     ptx::mbar_arrive(vt_ready);
     if (warp_wait(accum_full, 0, abort_f)) {
       ptx::tc_fence_after();
@@ -389,19 +434,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n = n0 + c8;
       if (n >= p.d_out) continue;
       const uint32_t off = static_cast<uint32_t>((i * kRedLd + c8) * 4);
-      float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      for (int rk = 0; rk < S; ++rk) {
-        float4 a, b;
-        if (S > 1) {
-          const uint32_t ra = ptx::mapa_shared(red_s + off, static_cast<uint32_t>(rk));
-          a = ptx::ld_dsmem_f4(ra);
-          b = ptx::ld_dsmem_f4(ra + 16);
-        } else {
-          a = *reinterpret_cast<const float4*>(smem + off);
-          b = *reinterpret_cast<const float4*>(smem + off + 16);
+      // all S partial tiles' loads first, then the sum (fixed rank order)
+      float4 va[8], vb[8];
+#pragma unroll
+      for (int rk = 0; rk < 8; ++rk) {
+        if (rk < S) {
+          const uint32_t ra =
+              S > 1 ? ptx::mapa_shared(red_s + off, static_cast<uint32_t>(rk)) : red_s + off;
+          va[rk] = ptx::ld_dsmem_f4(ra);
+          vb[rk] = ptx::ld_dsmem_f4(ra + 16);
         }
-        f[0] += a.x; f[1] += a.y; f[2] += a.z; f[3] += a.w;
-        f[4] += b.x; f[5] += b.y; f[6] += b.z; f[7] += b.w;
+      }
+      float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int rk = 0; rk < 8; ++rk) {
+        if (rk < S) {
+          f[0] += va[rk].x; f[1] += va[rk].y; f[2] += va[rk].z; f[3] += va[rk].w;
+          f[4] += vb[rk].x; f[5] += vb[rk].y; f[6] += vb[rk].z; f[7] += vb[rk].w;
+        }
       }
       store8(p.y + static_cast<size_t>(t0 + i) * p.d_out + n, f);
     }
@@ -517,6 +567,8 @@ cudaError_t launch_fused_tc(const void* x, const void* W0, const void* B, const 
   prm.n_kblk = (d_in + kBK - 1) / kBK;
   prm.stages = 0;
   prm.box_rows = r < 32 ? r : 32;
+  prm.lg_box = 31 - __builtin_clz(static_cast<unsigned>(prm.box_rows));
+  prm.lg_upa = 31 - __builtin_clz(static_cast<unsigned>(r / prm.box_rows));
   prm.v_ksplit = v_ksplit;
   prm.ids = ids;
   prm.vpart = vpart;
