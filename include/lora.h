@@ -199,6 +199,33 @@ lora_status_t lora_base_gemm_expand(const void* x, const void* W0, const void* B
                                     void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * The whole layer (same contract and result as lora_linear_fused) for
+ * callers that cannot allocate device memory: code running under a
+ * framework whose allocator already owns the GPU's memory, plugins the host
+ * process does not let allocate, and paths that forbid allocation once they
+ * are running.  The pages have no counterpart; this is a library concern.
+ *
+ * Scratch: a fixed array of LORA_NOALLOC_SCRATCH_BYTES inside the library,
+ * present in every GPU's memory from load until process exit.  Batches whose
+ * scratch (lora_workspace_bytes(LORA_OP_LINEAR_FUSED, ...)) is larger are
+ * refused with LORA_ERR_WORKSPACE before anything is enqueued.  The call
+ * allocates nothing (no cudaMalloc, no allocating library routine).
+ *
+ * The first call on a device looks up the array's device address (with that
+ * device current) and caches it; make that first call before any stream
+ * capture.  Every call shares the one array: calls whose GPU work overlaps
+ * (other streams, other threads) race on it.  Each call clears the error
+ * word it keeps in the array; device error bits are not reported back (ids
+ * outside [-1, n_slots) are still read as base-only).
+ */
+#define LORA_NOALLOC_SCRATCH_BYTES (8u << 20)
+lora_status_t lora_linear_fused_noalloc(const void* x, const void* W0, const void* A_pool,
+                                        const void* B_pool, const int32_t* slot_ids,
+                                        const float* scale, void* y, int32_t T, int32_t d_in,
+                                        int32_t d_out, int32_t r, int32_t n_slots,
+                                        lora_dtype_t dt, void* stream);
+
+/*
  * Synchronises `stream`, copies the workspace error word to *device_err and
  * clears it.  Returns LORA_ERR_CUDA if the stream reports an error.
  */

@@ -22,11 +22,11 @@ OP_BUILD_SEGMENTS, OP_BGMV_SHRINK, OP_BGMV_EXPAND = 0, 1, 2
 OP_SGMV_SHRINK, OP_SGMV_EXPAND, OP_LINEAR_FUSED, OP_BASE_GEMM_EXPAND = 3, 4, 5, 6
 DEVERR_BAD_SLOT, DEVERR_TIMEOUT = 0x1, 0x2
 MAX_SLOTS, MAX_TOKENS, MAX_KSPLIT = 16384, 1 << 20, 64
+NOALLOC_SCRATCH_BYTES = 8 << 20
 
 EXPORTS = ("lora_workspace_bytes", "lora_build_segments", "lora_bgmv_shrink", "lora_bgmv_expand",
            "lora_sgmv_shrink", "lora_sgmv_expand", "lora_linear_fused", "lora_base_gemm_expand",
-           "lora_get_error",
-           "lora_status_string")
+           "lora_linear_fused_noalloc", "lora_get_error", "lora_status_string")
 
 
 class LoraError(RuntimeError):
@@ -49,6 +49,7 @@ _SIGS = {
     "lora_sgmv_expand": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _Z, _P]),
     "lora_linear_fused": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _Z, _P]),
     "lora_base_gemm_expand": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _Z, _P]),
+    "lora_linear_fused_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "lora_get_error": (_I, [_P, _P, ctypes.POINTER(ctypes.c_int32)]),
     "lora_status_string": (ctypes.c_char_p, [_I]),
 }
@@ -118,6 +119,12 @@ def lora_base_gemm_expand(x, W0, B_pool, slot_ids, v_partial, ksplit, y, T, d_in
                           n_slots, dt, ws, ws_bytes, stream):
     return _call("lora_base_gemm_expand", x, W0, B_pool, slot_ids, v_partial, ksplit, y, T, d_in,
                  d_out, r, n_slots, dt, ws, ws_bytes, stream)
+
+
+def lora_linear_fused_noalloc(x, W0, A_pool, B_pool, slot_ids, scale, y, T, d_in, d_out, r,
+                              n_slots, dt, stream):
+    return _call("lora_linear_fused_noalloc", x, W0, A_pool, B_pool, slot_ids, scale, y, T, d_in,
+                 d_out, r, n_slots, dt, stream)
 
 
 def lora_get_error(ws, stream):
