@@ -170,17 +170,45 @@ lora_status_t lora_sgmv_expand(const float* v_partial, int32_t ksplit, const voi
  * ("Multi-LoRA batching and adapter paging", section "Walking through a
  * batch": the base product once for all rows, then each row's adapter term;
  * "Serving many LoRA adapters", "Replay" figure: segmented gather, grouped
- * GEMM, scatter add, one fused output).  Batches of up to 256 tokens take
- * the per-token BGMV shrink (decode); larger batches take the segment
- * builder and the segment-grouped SGMV shrink (prefill).  Then one base-GEMM
- * kernel whose accumulator also takes the expand term (bf16: tcgen05 tensor
- * cores, accumulator in tensor memory) stores y once.
+ * GEMM, scatter add, one fused output).  Batches of up to 256 tokens
+ * (decode) take the per-token BGMV shrink and, for bf16, the BGMV expand
+ * into an fp32 term that the base-GEMM epilogue adds (lora_bgmv_shrink,
+ * lora_bgmv_delta, lora_base_gemm_delta).  Larger batches (prefill) take the
+ * segment builder, the segment-grouped SGMV shrink and a base GEMM whose
+ * tensor-memory accumulator also takes the expand as extra K-blocks
+ * (lora_base_gemm_expand).  Either way y is stored once.
  */
 lora_status_t lora_linear_fused(const void* x, const void* W0, const void* A_pool,
                                 const void* B_pool, const int32_t* slot_ids, const float* scale,
                                 void* y, int32_t T, int32_t d_in, int32_t d_out, int32_t r,
                                 int32_t n_slots, lora_dtype_t dt, void* ws, size_t ws_bytes,
                                 void* stream);
+
+/*
+ * BGMV expand into an fp32 adapter term (bf16 B only):
+ *   delta[t, :] = (sum_s v_partial[s, t, :]) B[a_t]      for tokens with a valid id
+ * delta [T, d_out] float32, rows of base-only tokens are not written.  This
+ * is the expand of lora_linear_fused for decode-sized batches (T <= 256): it
+ * runs while the base GEMM streams W0 and lora_base_gemm_delta adds it in
+ * its epilogue ("Serving multiple LoRAs ...": the expand is added directly
+ * to the base output; BGMV suits decode).  Workspace: the error word only.
+ */
+lora_status_t lora_bgmv_delta(const float* v_partial, int32_t ksplit, const void* B_pool,
+                              const int32_t* slot_ids, float* delta, int32_t T, int32_t r,
+                              int32_t d_out, int32_t n_slots, lora_dtype_t dt, void* ws,
+                              size_t ws_bytes, void* stream);
+
+/*
+ * The shared base product with a ready fp32 adapter term added in its
+ * epilogue (bf16, tcgen05 tensor cores):
+ *   y[t, :] = x[t, :] W0 + delta[t, :]     for tokens with a valid id
+ *   y[t, :] = x[t, :] W0                    otherwise (delta row not read)
+ * y is OVERWRITTEN and written once.  Workspace: the error word only.
+ */
+lora_status_t lora_base_gemm_delta(const void* x, const void* W0, const float* delta,
+                                   const int32_t* slot_ids, void* y, int32_t T, int32_t d_in,
+                                   int32_t d_out, int32_t n_slots, lora_dtype_t dt, void* ws,
+                                   size_t ws_bytes, void* stream);
 
 /*
  * The last kernel of lora_linear_fused on its own: the shared base product

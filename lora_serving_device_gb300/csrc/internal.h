@@ -50,10 +50,18 @@ int sgmv_max_items(int T, int n_slots);
 int fused_shrink_ksplit(int T, int d_in, int n_slots, int num_sms);
 
 // Base GEMM + expand-in-accumulator kernel, bf16 (tcgen05), see k_fused_tc.cu.
+// `delta` (may be null): a ready fp32 [T, d_out] adapter term written by the
+// kernel launched just before; then B / vpart are not read.
 cudaError_t launch_fused_tc(const void* x, const void* W0, const void* B, const int32_t* ids,
-                            const float* vpart, int v_ksplit, void* y, int T, int d_in, int d_out,
-                            int r, int n_slots, uint32_t* err, cudaStream_t st,
-                            const DeviceInfo& dev);
+                            const float* vpart, int v_ksplit, const float* delta, void* y, int T,
+                            int d_in, int d_out, int r, int n_slots, uint32_t* err,
+                            cudaStream_t st, const DeviceInfo& dev);
+// BGMV expand into an fp32 term: delta[t, :] = (sum_s vpart[s, t, :]) B[a_t]
+// for tokens with a valid id (other rows untouched); bf16 B.  `pdl`: launch
+// as a programmatic dependent of the shrink just before.
+cudaError_t launch_bgmv_delta(const float* vpart, int ksplit, const void* B, const int32_t* ids,
+                              float* delta, int T, int r, int d_out, int n_slots, uint32_t* err,
+                              cudaStream_t st, bool pdl);
 // Same contract for fp32 storage on CUDA cores, see k_fused_simt.cu.
 cudaError_t launch_fused_f32(const float* x, const float* W0, const float* B, const int32_t* ids,
                              const float* vpart, int v_ksplit, float* y, int T, int d_in,

@@ -60,6 +60,10 @@ struct TcParams {
   int v_ksplit;
   const int32_t* ids;
   const float* vpart;
+  // When set, the adapter term is given as a ready fp32 [T, d_out] tensor
+  // (written by the kernel launched just before) and added in the epilogue;
+  // no LoRA K-blocks are built.
+  const float* delta;
   bf16* y;
   uint32_t* err;
 };
@@ -182,19 +186,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ---------------- producer -------------------------------------------
+    // Base K-blocks stream W0 / x by TMA.  LoRA K-blocks (see the top of this
+    // file) are slotted in between them as soon as the epilogue warps have
+    // published the tile's adapters and v, so their B loads overlap the W0
+    // stream; the MMA issuer consumes stages in ring order whatever they hold.
     int it = 0;
     bool ok = true;
-    for (; it < nbase; ++it) {
-      const int st = it % p.stages;
-      const uint32_t ph = static_cast<uint32_t>(it / p.stages) & 1u;
-      if (!warp_wait(&empty[st], ph ^ 1u, abort_f)) {
-        ok = false;
-        break;
-      }
+    bool lora_known = false;
+    int U = 0, my_groups = 0, gi = 0;
+    auto issue_base = [&](int kb, int st) {
       uint8_t* X = smem + static_cast<size_t>(st) * L.stage_bytes;
       uint8_t* Wr = X + L.x_bytes;
       if (lane == 0) {
-        const int kb = kb0 + it;
         ptx::mbar_arrive_expect_tx(&full[st], L.stage_bytes);
         ptx::tma_load_2d(X, &tm_x, &full[st], kb * kBK, t0);
 #pragma unroll
@@ -202,78 +205,115 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tma_load_2d(Wr + h * 8192, &tm_w, &full[st], n0 + 64 * h, kb * kBK);
       }
       __syncwarp();
-    }
-    if (ok && warp_wait(vt_ready, 0, abort_f)) {
-      int U;
-      const int my_groups = lora_groups(&U);
-      // This lane always writes the same 16-byte chunk c of a row; which K
-      // rows that chunk holds is fixed per K-block.
+    };
+    auto issue_lora = [&](int g, int st) {
+      uint8_t* X = smem + static_cast<size_t>(st) * L.stage_bytes;
+      uint8_t* Wr = X + L.x_bytes;
+      const int u_first = (z + g * S) * G;
+      const int n_units = min(G, U - u_first);
+      const int ua = u_first >> p.lg_upa, ub = (u_first + n_units - 1) >> p.lg_upa;
+      // masked V operand (K-major, 128-byte swizzle written by hand): zeros,
+      // then the rows of the tokens that use this block's adapters.  v is
+      // fp32; it enters the bf16 MMA as v = hi + lo with hi = bf16(v) and
+      // lo = bf16(v - hi), so the expand keeps ~16 mantissa bits: K rows
+      // [0, 32) carry hi parts, rows [32, 64) lo parts, each against its
+      // own copy of the B rows.
+      for (int e = lane; e < BT * 8; e += 32)
+        reinterpret_cast<uint4*>(X)[e] = make_uint4(0u, 0u, 0u, 0u);
+      const int used = n_units << p.lg_box;   // K rows of W per half that B fills
+      if (used < kBK / 2) {
+        const int per_half = (kBK / 2 - used) * 8;
+        for (int e = lane; e < 2 * per_half * kWBoxes; e += 32) {
+          const int hb = e / (2 * per_half), rem = e % (2 * per_half);
+          const int half = rem / per_half, rr = rem % per_half;
+          *reinterpret_cast<uint4*>(Wr + hb * 8192 + (half * (kBK / 2) + used + rr / 8) * 128 +
+                                    (rr % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      __syncwarp();
       const int c = lane & 7;
-      const bool lo_half = c >= 4;
-      const int kq = (c & 3) << 3;          // K offset inside the hi or lo half
-      const int wu = kq >> p.lg_box;        // box (unit) of this chunk
-      for (int gi = 0; gi < my_groups; ++gi, ++it) {
-        const int st = it % p.stages;
-        const uint32_t ph = static_cast<uint32_t>(it / p.stages) & 1u;
-        if (!warp_wait(&empty[st], ph ^ 1u, abort_f)) break;
-        uint8_t* X = smem + static_cast<size_t>(st) * L.stage_bytes;
-        uint8_t* Wr = X + L.x_bytes;
-        const int u_first = (z + gi * S) * G;
-        const int n_units = min(G, U - u_first);
-        const int w = u_first + wu;
-        const int uw = (wu < n_units) ? (w >> p.lg_upa) : -2;     // adapter index
-        const int q0 = ((w & (upa - 1)) << p.lg_box) + (kq & (p.box_rows - 1));
-        // masked V operand (K-major, 128-byte swizzle written by hand).
-        // v is fp32; it enters the bf16 MMA as v = hi + lo with hi = bf16(v)
-        // and lo = bf16(v - hi), so the expand keeps ~16 mantissa bits.  K
-        // rows [0, 32) carry the hi parts of this block's adapters, rows
-        // [32, 64) the lo parts, each against its own copy of the B rows.
-        // Row i holds the v of token i where token i uses that adapter, else 0.
-        for (int i = lane >> 3; i < BT; i += 4) {
-          uint4 val = make_uint4(0u, 0u, 0u, 0u);
-          if (tok[i] == uw) {
+      const int kq = (c & 3) << 3;
+      const int wu = kq >> p.lg_box;
+      const int w = u_first + wu;
+      const int uw = (wu < n_units) ? (w >> p.lg_upa) : -2;
+      const int q0 = ((w & (upa - 1)) << p.lg_box) + (kq & (p.box_rows - 1));
+      // rows 4j + sub of every 32-row word; a quad of rows per iteration,
+      // skipped whole when none of the four uses this block's adapters
+      const int sub = lane >> 3;
+      for (int k = 0; k < BT / 32; ++k) {
+        const int tv = tok[k * 32 + lane];
+        const uint32_t m = __ballot_sync(0xffffffffu, tv >= ua && tv <= ub);
+        if (m == 0u) continue;
+#pragma unroll 1
+        for (int j = 0; j < 8; ++j) {
+          if (((m >> (4 * j)) & 0xFu) == 0u) continue;
+          const int b = 4 * j + sub;
+          const int ti = __shfl_sync(0xffffffffu, tv, b);
+          if (ti == uw) {
+            const int i = k * 32 + b;
             float f[8], h[8], l[8];
             load8(vt + i * p.r + q0, f);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              h[j] = __bfloat162float(__float2bfloat16_rn(f[j]));
-              l[j] = f[j] - h[j];
+            for (int q = 0; q < 8; ++q) {
+              h[q] = __bfloat162float(__float2bfloat16_rn(f[q]));
+              l[q] = f[q] - h[q];
             }
-            val = pack8_bf16(lo_half ? l : h);
-          }
-          *reinterpret_cast<uint4*>(X + i * 128 + ((c ^ (i & 7)) << 4)) = val;
-        }
-        // K rows of the W side that no adapter fills this time are zeroed
-        const int used = n_units << p.lg_box;
-        if (used < kBK / 2) {
-          const int per_half = (kBK / 2 - used) * 8;
-          for (int e = lane; e < 2 * per_half * kWBoxes; e += 32) {
-            const int hb = e / (2 * per_half), rem = e % (2 * per_half);
-            const int half = rem / per_half, rr = rem % per_half;
-            *reinterpret_cast<uint4*>(Wr + hb * 8192 + (half * (kBK / 2) + used + rr / 8) * 128 +
-                                      (rr % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(X + i * 128 + ((c ^ (i & 7)) << 4)) =
+                pack8_bf16(c >= 4 ? l : h);
           }
         }
-        ptx::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          ptx::mbar_arrive_expect_tx(
-              &full[st], static_cast<uint32_t>(2 * n_units * p.box_rows * 128 * kWBoxes));
-          for (int u = 0; u < n_units; ++u) {
-            const int wv = u_first + u;
-            const int a = uniq[wv >> p.lg_upa];
-            const int qb = (wv & (upa - 1)) << p.lg_box;
-#pragma unroll
-            for (int hb = 0; hb < kWBoxes; ++hb) {
-#pragma unroll
-              for (int half = 0; half < 2; ++half)
-                ptx::tma_load_2d(Wr + hb * 8192 + (half * (kBK / 2) + u * p.box_rows) * 128,
-                                 &tm_b, &full[st], n0 + 64 * hb, a * p.r + qb);
-            }
-          }
-        }
-        __syncwarp();
       }
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0)
+        ptx::mbar_arrive_expect_tx(
+            &full[st], static_cast<uint32_t>(2 * n_units * p.box_rows * 128 * kWBoxes));
+      __syncwarp();
+      // one B box per lane: (unit, 64-column box, hi/lo copy)
+      if (lane < 2 * n_units * kWBoxes) {
+        const int u = lane / (2 * kWBoxes), rem = lane % (2 * kWBoxes);
+        const int hb = rem >> 1, half = rem & 1;
+        const int wv = u_first + u;
+        const int a = uniq[wv >> p.lg_upa];
+        const int qb = (wv & (upa - 1)) << p.lg_box;
+        ptx::tma_load_2d(Wr + hb * 8192 + (half * (kBK / 2) + u * p.box_rows) * 128, &tm_b,
+                         &full[st], n0 + 64 * hb, a * p.r + qb);
+      }
+      __syncwarp();
+    };
+    auto next_slot = [&](int* st) {
+      *st = it % p.stages;
+      const uint32_t ph = static_cast<uint32_t>(it / p.stages) & 1u;
+      return warp_wait(&empty[*st], ph ^ 1u, abort_f);
+    };
+    for (int b = 0; b < nbase && ok; ++b) {
+      int st;
+      if (!(ok = next_slot(&st))) break;
+      issue_base(kb0 + b, st);
+      ++it;
+      if (!lora_known) {
+        int ready = 0;
+        if (lane == 0) ready = ptx::mbar_test_wait(vt_ready, 0) ? 1 : 0;
+        if (__shfl_sync(0xffffffffu, ready, 0)) {
+          lora_known = true;
+          my_groups = lora_groups(&U);
+        }
+      }
+      if (lora_known && gi < my_groups) {
+        if (!(ok = next_slot(&st))) break;
+        issue_lora(gi++, st);
+        ++it;
+      }
+    }
+    if (ok && !lora_known && warp_wait(vt_ready, 0, abort_f)) {
+      lora_known = true;
+      my_groups = lora_groups(&U);
+    }
+    while (ok && lora_known && gi < my_groups) {
+      int st;
+      if (!(ok = next_slot(&st))) break;
+      issue_lora(gi++, st);
+      ++it;
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer -----------------------------------------
@@ -314,6 +354,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- epilogue warps -------------------------------------
     const int etid = tid - 64;
     const int n_words = (p.n_slots + 31) >> 5;
+    if (p.delta != nullptr) {
+      // adapter term given in fp32: only which rows carry one is needed
+      bool bad_d = false;
+      for (int i = etid; i < BT; i += kEpiThreads) {
+        const int t = t0 + i;
+        int u = -1;
+        if (t < p.T) {
+          const int id = p.ids[t];
+          if (slot_valid(id, p.n_slots)) u = 0;
+          else if (id != -1) bad_d = true;
+        }
+        tok[i] = u;
+      }
+      if (bad_d && blockIdx.x == 0 && z == 0) flag_error(p.err, LORA_DEVERR_BAD_SLOT);
+      if (etid == 0) *n_uniq_s = 0;
+      epi_sync();
+    } else {
     // the tile's slot ids and its distinct adapters (ascending slot order),
     // built while the main loop streams W0
     bool bad = false;
@@ -393,6 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     epi_sync();
+    }
     ptx::mbar_arrive(vt_ready);
     if (warp_wait(accum_full, 0, abort_f)) {
       ptx::tc_fence_after();
@@ -423,6 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- split-K reduction through distributed shared memory, store y ------
   if (S > 1) ptx::cluster_sync();
   else __syncthreads();
+  if (p.delta != nullptr) pdl_wait();  // delta comes from the previous kernel
   if (!*abort_f) {
     const int rows = min(BT, p.T - t0);
     const int rb0 = static_cast<int>(static_cast<long long>(z) * rows / S);
@@ -452,6 +511,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           f[0] += va[rk].x; f[1] += va[rk].y; f[2] += va[rk].z; f[3] += va[rk].w;
           f[4] += vb[rk].x; f[5] += vb[rk].y; f[6] += vb[rk].z; f[7] += vb[rk].w;
         }
+      }
+      if (p.delta != nullptr && tok[i] >= 0) {
+        float d[8];
+        load8_dep(p.delta + static_cast<size_t>(t0 + i) * p.d_out + n, d);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) f[q] += d[q];
       }
       store8(p.y + static_cast<size_t>(t0 + i) * p.d_out + n, f);
     }
@@ -518,9 +583,13 @@ cudaError_t launch_variant(const void* x, const void* W0, const void* B, TcParam
   const size_t smem = L.total + 1024;
 
   CUtensorMap tm_x, tm_w, tm_b;
+  // with a ready adapter term (delta) no B rows are loaded; the B map then
+  // describes W0 only so that the parameter is a valid tensor map
+  const bool has_b = prm.delta == nullptr;
   if (!make_map(&tm_x, x, prm.d_in, prm.T, prm.d_in, kBK, BT) ||
       !make_map(&tm_w, W0, prm.d_out, prm.d_in, prm.d_out, 64, kBK) ||
-      !make_map(&tm_b, B, prm.d_out, static_cast<uint64_t>(prm.n_slots) * prm.r, prm.d_out, 64,
+      !make_map(&tm_b, has_b ? B : W0, prm.d_out,
+                has_b ? static_cast<uint64_t>(prm.n_slots) * prm.r : prm.d_in, prm.d_out, 64,
                 prm.box_rows))
     return cudaErrorInvalidValue;
 
@@ -553,9 +622,9 @@ bool tensor_map_available() {
 }
 
 cudaError_t launch_fused_tc(const void* x, const void* W0, const void* B, const int32_t* ids,
-                            const float* vpart, int v_ksplit, void* y, int T, int d_in, int d_out,
-                            int r, int n_slots, uint32_t* err, cudaStream_t st,
-                            const DeviceInfo& dev) {
+                            const float* vpart, int v_ksplit, const float* delta, void* y, int T,
+                            int d_in, int d_out, int r, int n_slots, uint32_t* err,
+                            cudaStream_t st, const DeviceInfo& dev) {
   resolve_encode();
   if (g_encode == nullptr) return cudaErrorNotSupported;
   TcParams prm;
@@ -566,12 +635,15 @@ cudaError_t launch_fused_tc(const void* x, const void* W0, const void* B, const 
   prm.n_slots = n_slots;
   prm.n_kblk = (d_in + kBK - 1) / kBK;
   prm.stages = 0;
+  if (delta != nullptr) r = 8;  // no v tile is staged; keep its footprint minimal
+  prm.r = r;
   prm.box_rows = r < 32 ? r : 32;
   prm.lg_box = 31 - __builtin_clz(static_cast<unsigned>(prm.box_rows));
   prm.lg_upa = 31 - __builtin_clz(static_cast<unsigned>(r / prm.box_rows));
   prm.v_ksplit = v_ksplit;
   prm.ids = ids;
   prm.vpart = vpart;
+  prm.delta = delta;
   prm.y = static_cast<bf16*>(y);
   prm.err = err;
 

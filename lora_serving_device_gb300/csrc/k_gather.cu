@@ -126,6 +126,52 @@ __global__ void __launch_bounds__(128)
   store8(yp, yv);
 }
 
+// BGMV expand into an fp32 adapter term, delta[t, :] = v[t, :] B[a_t], for
+// the fused decode path: it runs while the base GEMM streams W0 (launched as
+// a programmatic dependent of the shrink, and itself letting the GEMM start)
+// and the GEMM adds it in its epilogue.  Rows of base-only tokens are not
+// written.  One CTA per (token, 1024 columns).
+template <int R>
+__global__ void __launch_bounds__(128)
+    bgmv_delta_kernel(const float* vpart, int ksplit, const bf16* __restrict__ B,
+                      const int32_t* __restrict__ ids, float* __restrict__ delta, int T,
+                      int d_out, int n_slots, uint32_t* err) {
+  __shared__ float vs[R];
+  pdl_launch_dependents();
+  // every CTA waits, so that this grid completing implies the shrink completed
+  pdl_wait();  // v is written by the shrink kernel launched just before
+  const int t = blockIdx.x;
+  const int id = ids[t];
+  if (!slot_valid(id, n_slots)) {
+    if (threadIdx.x == 0 && blockIdx.y == 0 && id != -1) flag_error(err, LORA_DEVERR_BAD_SLOT);
+    return;
+  }
+  for (int q = threadIdx.x; q < R; q += 128) {
+    float a = 0.f;
+    for (int s = 0; s < ksplit; ++s) {
+      const float* vp = vpart + (static_cast<size_t>(s) * T + t) * R + q;
+      float v;
+      asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(vp) : "memory");
+      a += v;
+    }
+    vs[q] = a;
+  }
+  __syncthreads();
+  const int n = (blockIdx.y * 128 + threadIdx.x) * 8;
+  if (n >= d_out) return;
+  const bf16* Bp = B + static_cast<size_t>(id) * R * d_out + n;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+  for (int q = 0; q < R; ++q) {
+    float b[8];
+    load8(Bp + static_cast<size_t>(q) * d_out, b);
+    const float vq = vs[q];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) acc[c] = fmaf(vq, b[c], acc[c]);
+  }
+  store8(delta + static_cast<size_t>(t) * d_out + n, acc);
+}
+
 // ------------------------------------------------------------------- SGMV
 // Work item `item` -> (slot, first and one-past-last position in perm).
 // Items enumerate each segment's 64-token chunks in segment order.  The whole
@@ -440,6 +486,26 @@ cudaError_t launch_bgmv_expand(const float* vpart, int ksplit, const void* B, co
   return dt == LORA_DTYPE_BF16
              ? bgmv_expand_t<bf16>(vpart, ksplit, B, ids, y, T, r, d_out, n_slots, err, st)
              : bgmv_expand_t<float>(vpart, ksplit, B, ids, y, T, r, d_out, n_slots, err, st);
+}
+
+cudaError_t launch_bgmv_delta(const float* vpart, int ksplit, const void* B, const int32_t* ids,
+                              float* delta, int T, int r, int d_out, int n_slots, uint32_t* err,
+                              cudaStream_t st, bool pdl) {
+  const dim3 grid(T, (d_out + 1023) / 1024);
+  const bf16* Be = static_cast<const bf16*>(B);
+#define LORA_DELTA_CASE(RR)                                                                   \
+  case RR:                                                                                    \
+    return launch_maybe_pdl(bgmv_delta_kernel<RR>, grid, dim3(128), st, pdl, vpart, ksplit, Be, \
+                            ids, delta, T, d_out, n_slots, err);
+  switch (r) {
+    LORA_DELTA_CASE(8)
+    LORA_DELTA_CASE(16)
+    LORA_DELTA_CASE(32)
+    LORA_DELTA_CASE(64)
+    LORA_DELTA_CASE(128)
+    default: return cudaErrorInvalidValue;
+  }
+#undef LORA_DELTA_CASE
 }
 
 cudaError_t launch_sgmv_shrink(const void* x, const void* A, const int32_t* perm,

@@ -38,12 +38,15 @@ struct FusedWs {
   int32_t* seg_off;
   int32_t* n_seg;
   float* vpart;
+  float* delta;  // fp32 [T, d_out] adapter term (decode-sized batches only)
   int ksplit;
   size_t bytes;
 };
 
-// Workspace of lora_linear_fused: error word, segment arrays, shrink partials.
-FusedWs fused_ws_layout(void* ws, int32_t T, int32_t d_in, int32_t r, int32_t n_slots) {
+// Workspace of lora_linear_fused: error word, segment arrays, shrink
+// partials, and for decode-sized batches the fp32 adapter term.
+FusedWs fused_ws_layout(void* ws, int32_t T, int32_t d_in, int32_t d_out, int32_t r,
+                        int32_t n_slots) {
   FusedWs w;
   const size_t cap = static_cast<size_t>(T < n_slots ? T : n_slots);
   uint8_t* base = static_cast<uint8_t*>(ws);
@@ -60,6 +63,9 @@ FusedWs fused_ws_layout(void* ws, int32_t T, int32_t d_in, int32_t r, int32_t n_
   const size_t o_v = o;
   w.ksplit = fused_shrink_ksplit(T, d_in, n_slots, 152);
   o += static_cast<size_t>(w.ksplit) * T * r * 4;
+  o = round_up(o, 256);
+  const size_t o_d = o;
+  if (T <= kDecodeTokens) o += static_cast<size_t>(T) * d_out * 4;
   w.bytes = round_up(o, 256);
   w.err = reinterpret_cast<uint32_t*>(base);
   w.perm = reinterpret_cast<int32_t*>(base + o_perm);
@@ -67,6 +73,7 @@ FusedWs fused_ws_layout(void* ws, int32_t T, int32_t d_in, int32_t r, int32_t n_
   w.seg_off = reinterpret_cast<int32_t*>(base + o_off);
   w.n_seg = reinterpret_cast<int32_t*>(base + o_nseg);
   w.vpart = reinterpret_cast<float*>(base + o_v);
+  w.delta = T <= kDecodeTokens ? reinterpret_cast<float*>(base + o_d) : nullptr;
   return w;
 }
 
@@ -121,8 +128,8 @@ size_t lora_workspace_bytes(int32_t op, int32_t T, int32_t d_in, int32_t d_out, 
                             int32_t n_slots) {
   (void)d_out;
   if (op == LORA_OP_LINEAR_FUSED) {
-    if (T < 0 || !rank_ok(r) || !slots_ok(n_slots) || d_in < 8) return kErrBytes;
-    return fused_ws_layout(nullptr, T, d_in, r, n_slots).bytes;
+    if (T < 0 || !rank_ok(r) || !slots_ok(n_slots) || d_in < 8 || d_out < 0) return kErrBytes;
+    return fused_ws_layout(nullptr, T, d_in, d_out, r, n_slots).bytes;
   }
   return kErrBytes;
 }
@@ -264,7 +271,7 @@ lora_status_t lora_linear_fused(const void* x, const void* W0, const void* A_poo
       !aligned16(A_pool) || !aligned16(B_pool) || !aligned16(y))
     return LORA_ERR_INVALID_ARG;
   if (x == y) return LORA_ERR_INVALID_ARG;
-  const FusedWs w = fused_ws_layout(ws, T, d_in, r, n_slots);
+  const FusedWs w = fused_ws_layout(ws, T, d_in, d_out, r, n_slots);
   lora_status_t s = check_ws(ws, ws_bytes, w.bytes);
   if (s != LORA_OK) return s;
   if (T == 0) return LORA_OK;
@@ -273,10 +280,15 @@ lora_status_t lora_linear_fused(const void* x, const void* W0, const void* A_poo
   if (dt == LORA_DTYPE_BF16 && !tensor_map_available()) return LORA_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (T <= kDecodeTokens) {
-    // decode-sized batch: per-token gather (BGMV) -- no sort needed
+  const bool decode = T <= kDecodeTokens;
+  if (decode) {
+    // decode-sized batch: per-token gather (BGMV) -- no sort needed; for
+    // bf16 the expand runs into an fp32 term while the GEMM streams W0
     e = launch_bgmv_shrink(x, A_pool, slot_ids, scale, w.vpart, T, d_in, r, n_slots, w.ksplit,
                            dt, w.err, st);
+    if (e == cudaSuccess && dt == LORA_DTYPE_BF16)
+      e = launch_bgmv_delta(w.vpart, w.ksplit, B_pool, slot_ids, w.delta, T, r, d_out, n_slots,
+                            w.err, st, true);
   } else {
     // prefill-sized batch: segments, then the segment-grouped shrink (SGMV)
     e = launch_build_segments(slot_ids, T, n_slots, w.perm, w.seg_slot, w.seg_off, w.n_seg,
@@ -287,8 +299,8 @@ lora_status_t lora_linear_fused(const void* x, const void* W0, const void* A_poo
   }
   if (e != cudaSuccess) return LORA_ERR_CUDA;
   if (dt == LORA_DTYPE_BF16)
-    e = launch_fused_tc(x, W0, B_pool, slot_ids, w.vpart, w.ksplit, y, T, d_in, d_out, r, n_slots,
-                        w.err, st, dev);
+    e = launch_fused_tc(x, W0, B_pool, slot_ids, w.vpart, w.ksplit, decode ? w.delta : nullptr, y,
+                        T, d_in, d_out, r, n_slots, w.err, st, dev);
   else
     e = launch_fused_f32(static_cast<const float*>(x), static_cast<const float*>(W0),
                          static_cast<const float*>(B_pool), slot_ids, w.vpart, w.ksplit,
@@ -320,13 +332,57 @@ lora_status_t lora_base_gemm_expand(const void* x, const void* W0, const void* B
   uint32_t* err = static_cast<uint32_t*>(ws);
   cudaError_t e;
   if (dt == LORA_DTYPE_BF16)
-    e = launch_fused_tc(x, W0, B_pool, slot_ids, v_partial, ksplit, y, T, d_in, d_out, r, n_slots,
-                        err, st, dev);
+    e = launch_fused_tc(x, W0, B_pool, slot_ids, v_partial, ksplit, nullptr, y, T, d_in, d_out, r,
+                        n_slots, err, st, dev);
   else
     e = launch_fused_f32(static_cast<const float*>(x), static_cast<const float*>(W0),
                          static_cast<const float*>(B_pool), slot_ids, v_partial, ksplit,
                          static_cast<float*>(y), T, d_in, d_out, r, n_slots, err, st);
   return from_cuda(e);
+}
+
+lora_status_t lora_bgmv_delta(const float* v_partial, int32_t ksplit, const void* B_pool,
+                              const int32_t* slot_ids, float* delta, int32_t T, int32_t r,
+                              int32_t d_out, int32_t n_slots, lora_dtype_t dt, void* ws,
+                              size_t ws_bytes, void* stream) {
+  if (T < 0) return LORA_ERR_INVALID_ARG;
+  if (dt != LORA_DTYPE_BF16) return LORA_ERR_DTYPE;
+  if (!tokens_ok(T) || !dim_ok(d_out) || !rank_ok(r) || !slots_ok(n_slots) || ksplit < 1 ||
+      ksplit > LORA_MAX_KSPLIT)
+    return LORA_ERR_SHAPE;
+  if (v_partial == nullptr || B_pool == nullptr || slot_ids == nullptr || delta == nullptr ||
+      !aligned16(v_partial) || !aligned16(B_pool) || !aligned16(delta))
+    return LORA_ERR_INVALID_ARG;
+  lora_status_t s = check_ws(ws, ws_bytes, kErrBytes);
+  if (s != LORA_OK) return s;
+  if (T == 0) return LORA_OK;
+  DeviceInfo dev;
+  if ((s = check_device(&dev)) != LORA_OK) return s;
+  return from_cuda(launch_bgmv_delta(v_partial, ksplit, B_pool, slot_ids, delta, T, r, d_out,
+                                     n_slots, static_cast<uint32_t*>(ws),
+                                     static_cast<cudaStream_t>(stream), false));
+}
+
+lora_status_t lora_base_gemm_delta(const void* x, const void* W0, const float* delta,
+                                   const int32_t* slot_ids, void* y, int32_t T, int32_t d_in,
+                                   int32_t d_out, int32_t n_slots, lora_dtype_t dt, void* ws,
+                                   size_t ws_bytes, void* stream) {
+  if (T < 0) return LORA_ERR_INVALID_ARG;
+  if (dt != LORA_DTYPE_BF16) return LORA_ERR_DTYPE;
+  if (!tokens_ok(T) || !dim_ok(d_in) || !dim_ok(d_out) || !slots_ok(n_slots))
+    return LORA_ERR_SHAPE;
+  if (x == nullptr || W0 == nullptr || delta == nullptr || slot_ids == nullptr || y == nullptr ||
+      !aligned16(x) || !aligned16(W0) || !aligned16(delta) || !aligned16(y) || x == y)
+    return LORA_ERR_INVALID_ARG;
+  lora_status_t s = check_ws(ws, ws_bytes, kErrBytes);
+  if (s != LORA_OK) return s;
+  if (T == 0) return LORA_OK;
+  DeviceInfo dev;
+  if ((s = check_device(&dev)) != LORA_OK) return s;
+  if (!tensor_map_available()) return LORA_ERR_CUDA;
+  return from_cuda(launch_fused_tc(x, W0, nullptr, slot_ids, nullptr, 1, delta, y, T, d_in, d_out,
+                                   8, n_slots, static_cast<uint32_t*>(ws),
+                                   static_cast<cudaStream_t>(stream), dev));
 }
 
 lora_status_t lora_get_error(void* ws, void* stream, int32_t* device_err) {

@@ -26,7 +26,8 @@ NOALLOC_SCRATCH_BYTES = 8 << 20
 
 EXPORTS = ("lora_workspace_bytes", "lora_build_segments", "lora_bgmv_shrink", "lora_bgmv_expand",
            "lora_sgmv_shrink", "lora_sgmv_expand", "lora_linear_fused", "lora_base_gemm_expand",
-           "lora_linear_fused_noalloc", "lora_get_error", "lora_status_string")
+           "lora_linear_fused_noalloc", "lora_bgmv_delta", "lora_base_gemm_delta",
+           "lora_get_error", "lora_status_string")
 
 
 class LoraError(RuntimeError):
@@ -50,6 +51,8 @@ _SIGS = {
     "lora_linear_fused": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _Z, _P]),
     "lora_base_gemm_expand": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _Z, _P]),
     "lora_linear_fused_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
+    "lora_bgmv_delta": (_I, [_P, _I, _P, _P, _P, _I, _I, _I, _I, _I, _P, _Z, _P]),
+    "lora_base_gemm_delta": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _Z, _P]),
     "lora_get_error": (_I, [_P, _P, ctypes.POINTER(ctypes.c_int32)]),
     "lora_status_string": (ctypes.c_char_p, [_I]),
 }
@@ -125,6 +128,18 @@ def lora_linear_fused_noalloc(x, W0, A_pool, B_pool, slot_ids, scale, y, T, d_in
                               n_slots, dt, stream):
     return _call("lora_linear_fused_noalloc", x, W0, A_pool, B_pool, slot_ids, scale, y, T, d_in,
                  d_out, r, n_slots, dt, stream)
+
+
+def lora_bgmv_delta(v_partial, ksplit, B_pool, slot_ids, delta, T, r, d_out, n_slots, dt, ws,
+                    ws_bytes, stream):
+    return _call("lora_bgmv_delta", v_partial, ksplit, B_pool, slot_ids, delta, T, r, d_out,
+                 n_slots, dt, ws, ws_bytes, stream)
+
+
+def lora_base_gemm_delta(x, W0, delta, slot_ids, y, T, d_in, d_out, n_slots, dt, ws, ws_bytes,
+                         stream):
+    return _call("lora_base_gemm_delta", x, W0, delta, slot_ids, y, T, d_in, d_out, n_slots, dt,
+                 ws, ws_bytes, stream)
 
 
 def lora_get_error(ws, stream):
@@ -253,6 +268,32 @@ def base_gemm_expand_t(x, W0, B_pool, slot_ids, v_partial, ws, y=None, stream=No
     check(lora_base_gemm_expand(_ptr(x), _ptr(W0), _ptr(B_pool), _ptr(slot_ids), _ptr(v_partial),
                                 v_partial.shape[0], _ptr(y), T, d_in, d_out, r, n_slots, _dt(x),
                                 _ptr(ws), ws.numel(), _stream(stream)), "lora_base_gemm_expand")
+    return y
+
+
+def bgmv_delta_t(v_partial, B_pool, slot_ids, ws, delta=None, stream=None):
+    """fp32 adapter term delta[t] = v[t] B[a_t] (rows of base-only tokens untouched)."""
+    import torch
+    ksplit, T, r = v_partial.shape
+    n_slots, _, d_out = B_pool.shape
+    if delta is None:
+        delta = torch.zeros((T, d_out), dtype=torch.float32, device=v_partial.device)
+    check(lora_bgmv_delta(_ptr(v_partial), ksplit, _ptr(B_pool), _ptr(slot_ids), _ptr(delta), T, r,
+                          d_out, n_slots, _dt(B_pool), _ptr(ws), ws.numel(), _stream(stream)),
+          "lora_bgmv_delta")
+    return delta
+
+
+def base_gemm_delta_t(x, W0, delta, slot_ids, n_slots, ws, y=None, stream=None):
+    """y = x W0 + delta (rows of tokens with a valid id), overwriting y."""
+    import torch
+    T, d_in = x.shape
+    d_out = W0.shape[1]
+    if y is None:
+        y = torch.empty((T, d_out), dtype=x.dtype, device=x.device)
+    check(lora_base_gemm_delta(_ptr(x), _ptr(W0), _ptr(delta), _ptr(slot_ids), _ptr(y), T, d_in,
+                               d_out, n_slots, _dt(x), _ptr(ws), ws.numel(), _stream(stream)),
+          "lora_base_gemm_delta")
     return y
 
 

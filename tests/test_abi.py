@@ -28,6 +28,7 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ("lora_build_segments", "lora_bgmv_shrink", "lora_bgmv_expand", "lora_sgmv_shrink",
               "lora_sgmv_expand", "lora_linear_fused", "lora_base_gemm_expand",
+              "lora_bgmv_delta", "lora_base_gemm_delta",
               "lora_workspace_bytes", "lora_get_error",
               "lora_status_string"):
         assert n in names

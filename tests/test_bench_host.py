@@ -22,7 +22,7 @@ def test_layer_bytes_decode():
     # distinct adapters of the decode workload
     b = bench.layer_bytes(64, 4096, 4096, 16, 30.5)
     assert abs(b / 2 ** 20 - 40.6) < 0.2
-    g = bench.gemm_bytes(64, 4096, 4096, 16, 30)
+    g = bench.gemm_bytes(64, 4096, 4096, 56)
     assert g < b and g > 32 * 2 ** 20
 
 
@@ -35,8 +35,12 @@ def test_fused_ksplit_matches_library():
         cap = min(T, n_slots)
         head = 16 + T * 4 + cap * 4 + (cap + 1) * 4 + 4
         head = -(-head // 256) * 256
-        want = -(-(head + ks * T * r * 4) // 256) * 256
-        assert L.lora_workspace_bytes(L.OP_LINEAR_FUSED, T, d_in, 0, r, n_slots) == want
+        d_out = 1024
+        body = -(-(head + ks * T * r * 4) // 256) * 256
+        if T <= 256:                       # decode-sized: fp32 adapter term [T, d_out]
+            body += T * d_out * 4
+        want = -(-body // 256) * 256
+        assert L.lora_workspace_bytes(L.OP_LINEAR_FUSED, T, d_in, d_out, r, n_slots) == want
 
 
 def test_parse_clocks():

@@ -335,3 +335,64 @@ def test_stack_8b_projection(L, layer, proj):
     ref = O.lora_linear_per_request(host(t["x"]), host(t["W0"]), A, B,
                                     np.full(n_slots, W.SCALE), lengths, slots)
     check_close(host(y), ref, f"stack layer {layer} proj {proj}")
+
+
+# ------------------------------------------------- building-block entry points
+BLOCK_CASES = [(1, 64, 128, 16, 3), (40, 512, 264, 16, 20), (64, 1024, 1024, 64, 9),
+               (130, 256, 520, 8, 33), (256, 320, 392, 128, 5), (300, 256, 512, 32, 7)]
+
+
+@pytest.mark.parametrize("case", BLOCK_CASES, ids=[str(c) for c in BLOCK_CASES])
+def test_bgmv_delta_matches_oracle(L, case):
+    torch = torch_mod()
+    T, d_in, d_out, r, n_slots = case
+    w = W.random_case(700 + T, T, d_in, d_out, r, n_slots)
+    d = DeviceCase(w)
+    ws = _ws(L)
+    vp = _v_input(T, r, 3, 2)
+    delta = torch.full((T, d_out), 7.0, dtype=torch.float32, device="cuda")
+    L.bgmv_delta_t(dev(vp, "f32"), d.B, d.ids, ws, delta=delta)
+    torch.cuda.synchronize()
+    ref = O.expand(vp.astype(np.float64).sum(axis=0), w.B_pool, w.slot_ids)
+    got = host(delta)
+    valid = (w.slot_ids >= 0) & (w.slot_ids < n_slots)
+    check_close(got[valid], ref[valid], "bgmv delta (fp32 out)", rel_fro=1e-5, max_rms=1e-4)
+    assert np.all(got[~valid] == 7.0)          # base-only rows not written
+
+
+@pytest.mark.parametrize("case", BLOCK_CASES, ids=[str(c) for c in BLOCK_CASES])
+def test_base_gemm_delta_matches_oracle(L, case):
+    torch = torch_mod()
+    T, d_in, d_out, r, n_slots = case
+    w = W.random_case(710 + T, T, d_in, d_out, r, n_slots, invalid=1)
+    d = DeviceCase(w)
+    ws = _ws(L)
+    delta = (np.random.default_rng([7002, T]).standard_normal((T, d_out)) * 0.2).astype(np.float32)
+    y = L.base_gemm_delta_t(d.x, d.W0, dev(delta, "f32"), d.ids, n_slots, ws)
+    torch.cuda.synchronize()
+    base = O.lora_linear(w.x, w.W0, w.A_pool, w.B_pool, w.scale, np.full(T, -1))
+    valid = (w.slot_ids >= 0) & (w.slot_ids < n_slots)
+    ref = base + np.where(valid[:, None], delta.astype(np.float64), 0.0)
+    check_close_bf16_out(host(y), ref, "base GEMM + delta")
+    assert L.get_error_t(ws) & L.DEVERR_BAD_SLOT
+
+
+@pytest.mark.parametrize("case", BLOCK_CASES, ids=[str(c) for c in BLOCK_CASES])
+def test_base_gemm_expand_matches_oracle(L, case):
+    """The tensor-core fold of the expand (LoRA K-blocks), given a shrink
+    output, on decode and prefill tile shapes."""
+    torch = torch_mod()
+    T, d_in, d_out, r, n_slots = case
+    w = W.random_case(720 + T, T, d_in, d_out, r, n_slots, runs=True)
+    d = DeviceCase(w)
+    ws = _ws(L)
+    vp = _v_input(T, r, 2, 3)
+    y = L.base_gemm_expand_t(d.x, d.W0, d.B, d.ids, dev(vp, "f32"), ws)
+    torch.cuda.synchronize()
+    base = O.lora_linear(w.x, w.W0, w.A_pool, w.B_pool, w.scale, np.full(T, -1))
+    ref = base + O.expand(vp.astype(np.float64).sum(axis=0), w.B_pool, w.slot_ids)
+    check_close_bf16_out(host(y), ref, "base GEMM + folded expand")
+    d0 = DeviceCase(w, W0_zero=True)
+    y0 = L.base_gemm_expand_t(d0.x, d0.W0, d0.B, d0.ids, dev(vp, "f32"), ws)
+    torch.cuda.synchronize()
+    check_close_bf16_out(host(y0), ref - base, "folded expand alone")
