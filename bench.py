@@ -190,6 +190,8 @@ def parse_clocks(lines):
 def fused_ksplit(T, d_in, n_slots, num_sms=152):
     """The shrink split the fused path uses (mirrors the library's choice;
     tests/test_bench_host.py checks it against lora_workspace_bytes)."""
+    if T <= 256:      # decode-sized batch: per-token shrink, ~256 CTAs
+        return max(1, min(-(-256 // max(T, 1)), 16, max(d_in // 512, 1)))
     cap = min(T, n_slots)
     est = (T + 63) // 64 + (cap + 1) // 2
     ks = -(-2 * num_sms // max(est, 1))

@@ -2,6 +2,7 @@
 // and the kernel translation units.  Launchers assume validated arguments.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstddef>
 #include <cstdint>
@@ -46,8 +47,9 @@ cudaError_t launch_sgmv_expand(const float* vpart, int ksplit, const void* B, co
 
 // Upper bound on SGMV work items (segment x token-chunk pairs) for a batch.
 int sgmv_max_items(int T, int n_slots);
-// ksplit the fused path uses for its shrink.
+// ksplit the fused path uses for its shrink (SGMV / BGMV form).
 int fused_shrink_ksplit(int T, int d_in, int n_slots, int num_sms);
+int decode_shrink_ksplit(int T, int d_in);
 
 // Base GEMM + expand-in-accumulator kernel, bf16 (tcgen05), see k_fused_tc.cu.
 // `delta` (may be null): a ready fp32 [T, d_out] adapter term written by the
@@ -69,5 +71,15 @@ cudaError_t launch_fused_f32(const float* x, const float* W0, const float* B, co
 
 // Whether cuTensorMapEncodeTiled could be resolved (needed for bf16 fused).
 bool tensor_map_available();
+// 2-D bf16 tensor map with 128-byte swizzle: `inner` contiguous elements per
+// row, `outer` rows `row_elems` apart, box box_inner x box_outer; elements
+// outside the tensor read as zero.
+bool encode_tensor_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                            uint64_t row_elems, uint32_t box_inner, uint32_t box_outer);
+// Decode-sized base GEMM (T <= 256) adding a ready fp32 adapter term, see
+// k_decode_tc.cu.
+cudaError_t launch_decode_tc(const void* x, const void* W0, const int32_t* ids,
+                             const float* delta, void* y, int T, int d_in, int d_out, int n_slots,
+                             uint32_t* err, cudaStream_t st, const DeviceInfo& dev);
 
 }  // namespace lora

@@ -70,18 +70,28 @@ struct TcParams {
 
 struct SmemLayout {
   uint32_t x_bytes, stage_bytes, stages_total;
-  uint32_t vt, tok, uniq, bitmap, bars, misc, total;
+  uint32_t rb, vt, tok, uniq, bitmap, bars, misc, total;
 };
+
+// Decode tiles (swap, up to 128 tokens) reduce split-K partials by pushing
+// them into the owning CTA's receive buffer; larger tiles stage them in the
+// drained pipeline ring and pull.
+template <bool SWAP, int BT>
+__host__ __device__ constexpr bool push_reduce() {
+  return SWAP && BT <= 128;
+}
 
 // Offsets from a 1024-byte aligned base (the 128-byte swizzle repeats every
 // 8 rows = 1024 bytes, and TMA / MMA agree on it only from such a base).
-template <int BT, int BN>
+template <bool SWAP, int BT, int BN>
 __host__ __device__ inline SmemLayout smem_layout(int stages, int r, int n_slots) {
   SmemLayout L;
   L.x_bytes = BT * 128;
   L.stage_bytes = L.x_bytes + (BN / 64) * 8192;
   L.stages_total = static_cast<uint32_t>(stages) * L.stage_bytes;
   uint32_t o = L.stages_total;
+  L.rb = o;   // receive buffer of the push reduction: [src rank][d_out row][token] fp32
+  if (push_reduce<SWAP, BT>()) o += 128 * BT * 4;
   L.vt = o;
   o += BT * r * 4;
   o = (o + 15u) & ~15u;
@@ -107,9 +117,16 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
-// Named barrier among the four epilogue warps only (barrier 0 is __syncthreads).
+// Named barriers (barrier 0 is __syncthreads): 1 = the four epilogue warps,
+// 2 = barrier init done, 3 = TMEM address published.
 __device__ __forceinline__ void epi_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+}
+__device__ __forceinline__ void named_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ void named_arrive(int id, int n) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
 template <bool SWAP, int BT, int BN>
@@ -128,7 +145,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  const SmemLayout L = smem_layout<BT, BN>(p.stages, p.r, p.n_slots);
+  const SmemLayout L = smem_layout<SWAP, BT, BN>(p.stages, p.r, p.n_slots);
+  constexpr bool kPush = push_reduce<SWAP, BT>();
   float* vt = reinterpret_cast<float*>(smem + L.vt);
   int* tok = reinterpret_cast<int*>(smem + L.tok);
   int* uniq = reinterpret_cast<int*>(smem + L.uniq);
@@ -144,32 +162,42 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n0 = blockIdx.x * BN, t0 = blockIdx.y * BT;
   const int S = static_cast<int>(gridDim.z), z = static_cast<int>(blockIdx.z);
+  // push reduction: peers may write into this CTA's receive buffer once
+  // every CTA of the cluster is running (phase A of the cluster barrier)
+  if (kPush && S > 1) ptx::cluster_arrive_relaxed();
 
-  // ---- prologue: barriers and TMEM only; the TMA stream starts at once ----
-  if (tid == 0) {
-    for (int i = 0; i < p.stages; ++i) {
-      ptx::mbar_init(&full[i], 1);
-      ptx::mbar_init(&empty[i], 1);
+  // ---- prologue: warp 0 initialises the barriers and starts the TMA stream
+  // at once; the other warps wait for the barriers (named barrier 2), warp 1
+  // allocates TMEM and hands its address to the epilogue warps (barrier 3).
+  if (warp == 0) {
+    if (lane == 0) {
+      ptx::prefetch_tmap(&tm_x);
+      ptx::prefetch_tmap(&tm_w);
+      ptx::prefetch_tmap(&tm_b);
+      for (int i = 0; i < p.stages; ++i) {
+        ptx::mbar_init(&full[i], 1);
+        ptx::mbar_init(&empty[i], 1);
+      }
+      ptx::mbar_init(accum_full, 1);
+      ptx::mbar_init(vt_ready, kEpiThreads);
+      *abort_f = 0;
+      ptx::fence_mbar_init();
     }
-    ptx::mbar_init(accum_full, 1);
-    ptx::mbar_init(vt_ready, kEpiThreads);
-    *abort_f = 0;
-    ptx::fence_mbar_init();
+    __syncwarp();
+    named_arrive(2, kThreads);
+  } else {
+    named_sync(2, kThreads);
+    if (warp == 1) {
+      ptx::tmem_alloc(tmem_slot, kTmemCols);
+      ptx::tmem_relinquish();
+      ptx::tc_fence_before();
+      named_arrive(3, kThreads - 32);
+    } else {
+      named_sync(3, kThreads - 32);
+    }
+    ptx::tc_fence_after();
   }
-  if (tid == 32) {
-    ptx::prefetch_tmap(&tm_x);
-    ptx::prefetch_tmap(&tm_w);
-    ptx::prefetch_tmap(&tm_b);
-  }
-  if (warp == 1) {
-    ptx::tmem_alloc(tmem_slot, kTmemCols);
-    ptx::tmem_relinquish();
-  }
-  ptx::tc_fence_before();
-  __syncthreads();
-  ptx::tc_fence_after();
-
-  const uint32_t tmem = *tmem_slot;
+  const uint32_t tmem = warp == 0 ? 0u : *tmem_slot;
   const int upa = p.r >> p.lg_box;       // TMA boxes per adapter (r / min(r, 32))
   const int G = (kBK / 2) >> p.lg_box;   // boxes per LoRA K-block (each used twice)
   const int kb0 = static_cast<int>(static_cast<long long>(z) * p.n_kblk / S);
@@ -452,33 +480,96 @@ __global__ void __launch_bounds__(kThreads, 1)
     epi_sync();
     }
     ptx::mbar_arrive(vt_ready);
-    if (warp_wait(accum_full, 0, abort_f)) {
+    const bool acc_ok = warp_wait(accum_full, 0, abort_f);
+    if (kPush && S > 1) ptx::cluster_wait_acquire();   // phase A: peers are running
+    if (acc_ok) {
       ptx::tc_fence_after();
       const int q = warp & 3;  // TMEM lanes 32q..32q+31 belong to this warp
-      float* red = reinterpret_cast<float*>(smem);
       const uint32_t tq = tmem + (static_cast<uint32_t>(q * 32) << 16);
+      if (kPush) {
+        // TMEM lane = d_out row n of the tile, column = token.  Row n belongs
+        // to rank n / (128 / S); its partial goes to slot [z][n % (128/S)] of
+        // that rank's receive buffer, 16 tokens per vector store.
+        const int rows_own = 128 / S;
+        const int n = q * 32 + lane;
+        const int owner = n / rows_own, n_loc = n % rows_own;
+        const uint32_t local = ptx::smem_u32(smem + L.rb) +
+                               static_cast<uint32_t>(((z * rows_own + n_loc) * BT) * 4);
+        const uint32_t dst =
+            S > 1 ? ptx::mapa_shared(local, static_cast<uint32_t>(owner)) : local;
 #pragma unroll 1
-      for (int c0 = 0; c0 < kUmmaN; c0 += 16) {
-        uint32_t v[16];
-        ptx::tmem_ld16(tq + c0, v);
-        ptx::tmem_ld_wait();
-        if (SWAP) {
-          const int n = q * 32 + lane;  // TMEM lane = d_out column, column = token
-#pragma unroll
-          for (int j = 0; j < 16; ++j) red[(c0 + j) * kRedLd + n] = __uint_as_float(v[j]);
-        } else {
-          const int i = q * 32 + lane;  // TMEM lane = token, column = d_out column
-          float4* dst = reinterpret_cast<float4*>(red + i * kRedLd + c0);
+        for (int c0 = 0; c0 < kUmmaN; c0 += 16) {
+          uint32_t v[16];
+          ptx::tmem_ld16(tq + c0, v);
+          ptx::tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                 __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+            ptx::st_dsmem_f4(dst + static_cast<uint32_t>((c0 + 4 * j) * 4),
+                             make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                         __uint_as_float(v[4 * j + 2]),
+                                         __uint_as_float(v[4 * j + 3])));
+        }
+      } else {
+        float* red = reinterpret_cast<float*>(smem);
+#pragma unroll 1
+        for (int c0 = 0; c0 < kUmmaN; c0 += 16) {
+          uint32_t v[16];
+          ptx::tmem_ld16(tq + c0, v);
+          ptx::tmem_ld_wait();
+          if (SWAP) {
+            const int n = q * 32 + lane;  // TMEM lane = d_out column, column = token
+#pragma unroll
+            for (int j = 0; j < 16; ++j) red[(c0 + j) * kRedLd + n] = __uint_as_float(v[j]);
+          } else {
+            const int i = q * 32 + lane;  // TMEM lane = token, column = d_out column
+            float4* dst = reinterpret_cast<float4*>(red + i * kRedLd + c0);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                   __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+          }
         }
       }
     }
   }
 
-  // ---- split-K reduction through distributed shared memory, store y ------
+  // ---- split-K reduction, store y ------------------------------------------
+  if constexpr (kPush) {
+    if (S > 1) {
+      if (warp < 2) ptx::cluster_wait_acquire();   // phase A (epilogue warps did it)
+      ptx::cluster_arrive_release();               // phase B: every push has landed
+      ptx::cluster_wait_acquire();
+    } else {
+      __syncthreads();
+    }
+    if (p.delta != nullptr) pdl_wait();  // delta comes from the previous kernel
+    if (!*abort_f) {
+      // this rank owns d_out rows [z * 128/S, (z+1) * 128/S) of the tile for
+      // every token; the S partials sit in its own receive buffer
+      const int rows_own = 128 / S;
+      const int groups = rows_own / 8;
+      const int rows_tok = min(BT, p.T - t0);
+      const float* rb = reinterpret_cast<const float*>(smem + L.rb);
+      for (int e = tid; e < rows_tok * groups; e += kThreads) {
+        const int g = e / rows_tok, t = e % rows_tok;
+        const int n = n0 + z * rows_own + g * 8;
+        if (n >= p.d_out) continue;
+        float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int src = 0; src < S; ++src) {
+          const float* col = rb + (src * rows_own + g * 8) * BT + t;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) f[j] += col[j * BT];
+        }
+        if (p.delta != nullptr && tok[t] >= 0) {
+          float d[8];
+          load8_dep(p.delta + static_cast<size_t>(t0 + t) * p.d_out + n, d);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) f[j] += d[j];
+        }
+        store8(p.y + static_cast<size_t>(t0 + t) * p.d_out + n, f);
+      }
+    }
+  } else {
   if (S > 1) ptx::cluster_sync();
   else __syncthreads();
   if (p.delta != nullptr) pdl_wait();  // delta comes from the previous kernel
@@ -488,40 +579,55 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int rb1 = static_cast<int>(static_cast<long long>(z + 1) * rows / S);
     constexpr int kChunks = BN / 8;
     const uint32_t red_s = ptx::smem_u32(smem);
-    for (int e = tid; e < (rb1 - rb0) * kChunks; e += kThreads) {
-      const int i = rb0 + e / kChunks, c8 = (e % kChunks) * 8;
-      const int n = n0 + c8;
-      if (n >= p.d_out) continue;
-      const uint32_t off = static_cast<uint32_t>((i * kRedLd + c8) * 4);
-      // all S partial tiles' loads first, then the sum (fixed rank order)
-      float4 va[8], vb[8];
+    const int n_items = (rb1 - rb0) * kChunks;
+    // two output chunks per pass: every load of both is issued before any sum
+    for (int e0 = tid; e0 < n_items; e0 += 2 * kThreads) {
+      float4 va[2][8], vb[2][8];
+      float dl[2][8];
+      int ii[2], nn[2];
+      bool on[2], dd[2];
 #pragma unroll
-      for (int rk = 0; rk < 8; ++rk) {
-        if (rk < S) {
-          const uint32_t ra =
-              S > 1 ? ptx::mapa_shared(red_s + off, static_cast<uint32_t>(rk)) : red_s + off;
-          va[rk] = ptx::ld_dsmem_f4(ra);
-          vb[rk] = ptx::ld_dsmem_f4(ra + 16);
+      for (int u = 0; u < 2; ++u) {
+        const int e = e0 + u * kThreads;
+        ii[u] = rb0 + e / kChunks;
+        nn[u] = n0 + (e % kChunks) * 8;
+        on[u] = e < n_items && nn[u] < p.d_out;
+        dd[u] = on[u] && p.delta != nullptr && tok[ii[u]] >= 0;
+        if (on[u]) {
+          const uint32_t off = static_cast<uint32_t>((ii[u] * kRedLd + (nn[u] - n0)) * 4);
+#pragma unroll
+          for (int rk = 0; rk < 8; ++rk) {
+            if (rk < S) {
+              const uint32_t ra =
+                  S > 1 ? ptx::mapa_shared(red_s + off, static_cast<uint32_t>(rk)) : red_s + off;
+              va[u][rk] = ptx::ld_dsmem_f4(ra);
+              vb[u][rk] = ptx::ld_dsmem_f4(ra + 16);
+            }
+          }
         }
+        if (dd[u]) load8_dep(p.delta + static_cast<size_t>(t0 + ii[u]) * p.d_out + nn[u], dl[u]);
       }
-      float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int rk = 0; rk < 8; ++rk) {
-        if (rk < S) {
-          f[0] += va[rk].x; f[1] += va[rk].y; f[2] += va[rk].z; f[3] += va[rk].w;
-          f[4] += vb[rk].x; f[5] += vb[rk].y; f[6] += vb[rk].z; f[7] += vb[rk].w;
+      for (int u = 0; u < 2; ++u) {
+        if (!on[u]) continue;
+        float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int rk = 0; rk < 8; ++rk) {
+          if (rk < S) {
+            f[0] += va[u][rk].x; f[1] += va[u][rk].y; f[2] += va[u][rk].z; f[3] += va[u][rk].w;
+            f[4] += vb[u][rk].x; f[5] += vb[u][rk].y; f[6] += vb[u][rk].z; f[7] += vb[u][rk].w;
+          }
         }
-      }
-      if (p.delta != nullptr && tok[i] >= 0) {
-        float d[8];
-        load8_dep(p.delta + static_cast<size_t>(t0 + i) * p.d_out + n, d);
+        if (dd[u]) {
 #pragma unroll
-        for (int q = 0; q < 8; ++q) f[q] += d[q];
+          for (int q = 0; q < 8; ++q) f[q] += dl[u][q];
+        }
+        store8(p.y + static_cast<size_t>(t0 + ii[u]) * p.d_out + nn[u], f);
       }
-      store8(p.y + static_cast<size_t>(t0 + i) * p.d_out + n, f);
     }
   }
   if (S > 1) ptx::cluster_sync();
+  }
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -568,18 +674,19 @@ cudaError_t launch_variant(const void* x, const void* W0, const void* B, TcParam
   // deepest pipeline that fits next to the v tile and bookkeeping, and that
   // can hold the staged fp32 accumulator afterwards
   const size_t cap = dev.max_smem_optin;
-  const size_t red_bytes = static_cast<size_t>(BT) * (BN + kRedPad) * 4;
+  const size_t red_bytes =
+      push_reduce<SWAP, BT>() ? 0 : static_cast<size_t>(BT) * (BN + kRedPad) * 4;
   int stages = 0;
   for (int s = 8; s >= 2; --s) {
-    const SmemLayout L = smem_layout<BT, BN>(s, prm.r, prm.n_slots);
-    if (L.total + 1024 <= cap && L.stages_total >= red_bytes) {
+    const SmemLayout L = smem_layout<SWAP, BT, BN>(s, prm.r, prm.n_slots);
+    if (L.total + 1024 <= cap && (red_bytes == 0 || L.stages_total >= red_bytes)) {
       stages = s;
       break;
     }
   }
   if (stages == 0) return cudaErrorInvalidConfiguration;
   prm.stages = stages;
-  const SmemLayout L = smem_layout<BT, BN>(stages, prm.r, prm.n_slots);
+  const SmemLayout L = smem_layout<SWAP, BT, BN>(stages, prm.r, prm.n_slots);
   const size_t smem = L.total + 1024;
 
   CUtensorMap tm_x, tm_w, tm_b;
@@ -616,6 +723,12 @@ cudaError_t launch_variant(const void* x, const void* W0, const void* B, TcParam
 
 }  // namespace
 
+bool encode_tensor_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                            uint64_t row_elems, uint32_t box_inner, uint32_t box_outer) {
+  resolve_encode();
+  return g_encode != nullptr && make_map(m, base, inner, outer, row_elems, box_inner, box_outer);
+}
+
 bool tensor_map_available() {
   resolve_encode();
   return g_encode != nullptr;
@@ -647,23 +760,19 @@ cudaError_t launch_fused_tc(const void* x, const void* W0, const void* B, const 
   prm.y = static_cast<bf16*>(y);
   prm.err = err;
 
+  // split-K cluster size: as many CTAs per tile as fill the SMs, at most 8,
+  // a power of two (the push reduction splits the 128 rows of a tile evenly)
   auto pick_split = [&](int tiles) {
     int S = dev.num_sms / (tiles > 0 ? tiles : 1);
     if (S > 8) S = 8;
     if (S > prm.n_kblk) S = prm.n_kblk;
-    if (S < 1) S = 1;
-    return S;
+    int p2 = 1;
+    while (p2 * 2 <= S) p2 *= 2;
+    return p2;
   };
-  if (T <= 256) {
-    const int tiles_n = (d_out + 127) / 128;
-    if (T <= 32) return launch_variant<true, 32, 128>(x, W0, B, prm, tiles_n, 1, pick_split(tiles_n), st, dev);
-    if (T <= 64) return launch_variant<true, 64, 128>(x, W0, B, prm, tiles_n, 1, pick_split(tiles_n), st, dev);
-    if (T <= 128) return launch_variant<true, 128, 128>(x, W0, B, prm, tiles_n, 1, pick_split(tiles_n), st, dev);
-    if (r <= 64) return launch_variant<true, 256, 128>(x, W0, B, prm, tiles_n, 1, pick_split(tiles_n), st, dev);
-    // rank 128: the fp32 v tile of 256 tokens would crowd out the pipeline,
-    // so two 128-token tiles instead
-    return launch_variant<true, 128, 128>(x, W0, B, prm, tiles_n, 2, pick_split(2 * tiles_n), st, dev);
-  }
+  // a ready adapter term on a decode-sized batch: the swap-AB decode kernel
+  if (delta != nullptr && T <= 256)
+    return launch_decode_tc(x, W0, ids, delta, y, T, d_in, d_out, n_slots, err, st, dev);
   const int tiles_n = (d_out + 255) / 256;
   const int tiles_t = (T + 127) / 128;
   const int S = pick_split(tiles_n * tiles_t);

@@ -136,6 +136,8 @@ __global__ void __launch_bounds__(128)
     bgmv_delta_kernel(const float* vpart, int ksplit, const bf16* __restrict__ B,
                       const int32_t* __restrict__ ids, float* __restrict__ delta, int T,
                       int d_out, int n_slots, uint32_t* err) {
+  constexpr int kGroups = 128 / R;  // threads summing the partials of one column q
+  __shared__ float part[128];
   __shared__ float vs[R];
   pdl_launch_dependents();
   // every CTA waits, so that this grid completing implies the shrink completed
@@ -146,28 +148,56 @@ __global__ void __launch_bounds__(128)
     if (threadIdx.x == 0 && blockIdx.y == 0 && id != -1) flag_error(err, LORA_DEVERR_BAD_SLOT);
     return;
   }
-  for (int q = threadIdx.x; q < R; q += 128) {
+  const int n = (blockIdx.y * 128 + threadIdx.x) * 8;
+  const bool on = n < d_out;
+  const bf16* Bp = B + static_cast<size_t>(id) * R * d_out + (on ? n : 0);
+  // the first batch of B rows (independent of v) is loaded before the v sum
+  // so the two latencies overlap; B stays packed bf16 until the FMA
+  constexpr int kBatch = R < 32 ? R : 32;
+  uint4 braw[kBatch];
+  if (on) {
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j)
+      braw[j] = *reinterpret_cast<const uint4*>(Bp + static_cast<size_t>(j) * d_out);
+  }
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  {
+    const int q = threadIdx.x % R, g = threadIdx.x / R;
     float a = 0.f;
-    for (int s = 0; s < ksplit; ++s) {
+    for (int s = g; s < ksplit; s += kGroups) {
       const float* vp = vpart + (static_cast<size_t>(s) * T + t) * R + q;
       float v;
       asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(vp) : "memory");
       a += v;
     }
-    vs[q] = a;
+    part[threadIdx.x] = a;
   }
   __syncthreads();
-  const int n = (blockIdx.y * 128 + threadIdx.x) * 8;
-  if (n >= d_out) return;
-  const bf16* Bp = B + static_cast<size_t>(id) * R * d_out + n;
-  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll 8
-  for (int q = 0; q < R; ++q) {
-    float b[8];
-    load8(Bp + static_cast<size_t>(q) * d_out, b);
-    const float vq = vs[q];
+  if (threadIdx.x < R) {
+    float a = 0.f;
 #pragma unroll
-    for (int c = 0; c < 8; ++c) acc[c] = fmaf(vq, b[c], acc[c]);
+    for (int g = 0; g < kGroups; ++g) a += part[g * R + threadIdx.x];
+    vs[threadIdx.x] = a;
+  }
+  __syncthreads();
+  if (!on) return;
+#pragma unroll 1
+  for (int q0 = 0; q0 < R; q0 += kBatch) {
+    if (q0 > 0) {
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j)
+        braw[j] = *reinterpret_cast<const uint4*>(Bp + static_cast<size_t>(q0 + j) * d_out);
+    }
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const float vq = vs[q0 + j];
+      const uint32_t w4[4] = {braw[j].x, braw[j].y, braw[j].z, braw[j].w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        acc[2 * c] = fmaf(vq, bf16_lo(w4[c]), acc[2 * c]);
+        acc[2 * c + 1] = fmaf(vq, bf16_hi(w4[c]), acc[2 * c + 1]);
+      }
+    }
   }
   store8(delta + static_cast<size_t>(t) * d_out + n, acc);
 }
@@ -456,6 +486,15 @@ int sgmv_max_items(int T, int n_slots) {
   const int cap = T < n_slots ? T : n_slots;
   const int items = (T + kSgTokens - 1) / kSgTokens + cap;
   return items > 0 ? items : 1;
+}
+
+int decode_shrink_ksplit(int T, int d_in) {
+  // ~256 CTAs of the per-token shrink, each over at least 512 of d_in
+  int ks = (256 + T - 1) / (T > 0 ? T : 1);
+  const int kmax = d_in / 512 > 0 ? d_in / 512 : 1;
+  if (ks > 16) ks = 16;
+  if (ks > kmax) ks = kmax;
+  return ks < 1 ? 1 : ks;
 }
 
 int fused_shrink_ksplit(int T, int d_in, int n_slots, int num_sms) {
