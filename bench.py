@@ -2,9 +2,9 @@
 """Throughput of the multi-LoRA batched linear layer on GB300.
 
 One step = one pass of the whole layer over one batch (lora_linear_fused):
-for this decode batch the per-token (BGMV) shrink, the BGMV expand into an
-fp32 adapter term, and the tcgen05 base GEMM that adds it in its epilogue and
-stores y once -- on the decode workload: one 4096->4096
+for this decode batch one launch computes the per-token (BGMV) adapter term
+(shrink, cluster sum, expand into fp32) and the tcgen05 base GEMM adds it in
+its epilogue and stores y once -- on the decode workload: one 4096->4096
 layer, rank 16, 256 resident adapters, 64 one-token requests with Zipf(1.1)
 adapter ids and 8 base-only rows.  Inputs are seeded and synthetic; weights
 and activations are resident in HBM before timing.
@@ -15,7 +15,7 @@ Reported on one JSON line (rank 0):
   e2e       the same metric through the public call with host buffers: each
             step copies x and the ids from pinned memory, runs the layer and
             copies y back
-  roofline  the dominant kernel (base GEMM + expand), timed with CUDA events
+  roofline  the dominant kernel (the base GEMM), timed with CUDA events
             around each of its launches, against the measured HBM copy peak
   sweep     tokens/s and achieved GB/s over distinct adapters per batch
             (4096->4096, rank 16, 1024-slot pool; T = 32 and 256)
@@ -112,7 +112,7 @@ def peaks():
 
 def kernel_src_sha():
     h = hashlib.sha256()
-    for f in ("k_fused_tc.cu", "ptx.cuh", "common.cuh"):
+    for f in ("k_decode_tc.cu", "ptx.cuh", "common.cuh"):
         with open(os.path.join(ROOT, "lora_serving_device_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -121,7 +121,7 @@ def kernel_src_sha():
 def dram_traffic_per_launch():
     """DRAM bytes per launch of the dominant kernel from the committed ncu
     summary, or None when the kernel source changed since it was taken."""
-    p = os.path.join(ROOT, "profiles", "fused_tc_decode_traffic.json")
+    p = os.path.join(ROOT, "profiles", "decode_gemm_traffic.json")
     try:
         with open(p) as f:
             d = json.load(f)
@@ -325,16 +325,16 @@ def timed_graph_steps(fn, K, W, stream):
 def per_kernel_times(sets, L, T, d_in, d_out, r, n_slots, n_steps, stream):
     """Each step as the public calls the fused decode path is made of, with
     CUDA events recorded around each kernel inside one captured graph: the
-    BGMV shrink, the BGMV expand into the fp32 adapter term, and the base
-    GEMM that adds it (the dominant kernel).  Returns the mean ms per kernel."""
+    one-launch BGMV adapter term (shrink, cluster sum, expand into fp32) and
+    the base GEMM that adds it (the dominant kernel).  The events between the
+    two calls keep the GEMM from starting early, so its time here includes
+    the prologue that the fused chain hides.  Returns the mean ms per kernel."""
     import torch
-    ks = fused_ksplit(T, d_in, n_slots)
     dev = sets[0].x.device
-    vpart = torch.empty((ks, T, r), dtype=torch.float32, device=dev)
     delta = torch.zeros((T, d_out), dtype=torch.float32, device=dev)
     ws = torch.zeros(256, dtype=torch.uint8, device=dev)
     try:
-        evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
+        evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(3)]
                for _ in range(n_steps)]
     except TypeError:
         return None
@@ -343,15 +343,12 @@ def per_kernel_times(sets, L, T, d_in, d_out, r, n_slots, n_steps, stream):
         s = sets[i % len(sets)]
         if rec:
             evs[i][0].record(stream)
-        L.bgmv_shrink_t(s.x, s.A, s.ids, s.scale, ks, ws, v_partial=vpart, stream=stream)
+        L.bgmv_adapter_t(s.x, s.A, s.B, s.ids, s.scale, ws, delta=delta, stream=stream)
         if rec:
             evs[i][1].record(stream)
-        L.bgmv_delta_t(vpart, s.B, s.ids, ws, delta=delta, stream=stream)
-        if rec:
-            evs[i][2].record(stream)
         L.base_gemm_delta_t(s.x, s.W0, delta, s.ids, n_slots, ws, y=s.y, stream=stream)
         if rec:
-            evs[i][3].record(stream)
+            evs[i][2].record(stream)
 
     with torch.cuda.stream(stream):
         for i in range(3):
@@ -361,12 +358,10 @@ def per_kernel_times(sets, L, T, d_in, d_out, r, n_slots, n_steps, stream):
     with torch.cuda.stream(stream):
         g.replay()
     stream.synchronize()
-    shr = [evs[i][0].elapsed_time(evs[i][1]) for i in range(n_steps)]
-    dlt = [evs[i][1].elapsed_time(evs[i][2]) for i in range(n_steps)]
-    gem = [evs[i][2].elapsed_time(evs[i][3]) for i in range(n_steps)]
-    return {"shrink_ms": statistics.mean(shr), "expand_ms": statistics.mean(dlt),
-            "gemm_ms": statistics.mean(gem), "gemm_ms_median": statistics.median(gem),
-            "n": n_steps}
+    ada = [evs[i][0].elapsed_time(evs[i][1]) for i in range(n_steps)]
+    gem = [evs[i][1].elapsed_time(evs[i][2]) for i in range(n_steps)]
+    return {"adapter_ms": statistics.mean(ada), "gemm_ms": statistics.mean(gem),
+            "gemm_ms_median": statistics.median(gem), "n": n_steps}
 
 
 def e2e_steps(s0, L, T, d_in, d_out, r, n_slots, n_steps, stream):
@@ -603,7 +598,8 @@ def run_ours(args):
         traffic = dram_traffic_per_launch()
         roof = {"bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": ach / pk["hbm_gbs"], "traffic": traffic,
-                "kernel": "fused_tc_kernel (tcgen05 base GEMM, adapter term added in the epilogue)",
+                "kernel": "decode_gemm_kernel (tcgen05 swap-AB base GEMM, adapter term added "
+                          "in the epilogue)",
                 "algorithmic_bytes_per_launch": gb, "launch_us": kt["gemm_ms"] * 1e3,
                 "peak_source": pk["source"], "frac_vs_8tbs": ach / 8000.0}
     lb = layer_bytes(T, d_in, d_out, r, D)
@@ -616,7 +612,7 @@ def run_ours(args):
                    "l2": f"{NSETS} rotating buffer sets (>2x L2)", "parallelism": "replicas",
                    "graph": f"CUDA graphs of {min(args.steps, GRAPH_STEPS)} steps"},
         "layer_gbs": lb / step_s / 1e9, "layer_frac": lb / step_s / 1e9 / pk["hbm_gbs"],
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 2 * args.steps,
         "e2e": {"value": world * T * 2000 / (e2e_ms / 1e3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms / 2000},

@@ -171,9 +171,10 @@ lora_status_t lora_sgmv_expand(const float* v_partial, int32_t ksplit, const voi
  * batch": the base product once for all rows, then each row's adapter term;
  * "Serving many LoRA adapters", "Replay" figure: segmented gather, grouped
  * GEMM, scatter add, one fused output).  Batches of up to 256 tokens
- * (decode) take the per-token BGMV shrink and, for bf16, the BGMV expand
- * into an fp32 term that the base-GEMM epilogue adds (lora_bgmv_shrink,
- * lora_bgmv_delta, lora_base_gemm_delta).  Larger batches (prefill) take the
+ * (decode) take the per-token BGMV path: for bf16 one launch computes the
+ * whole adapter term in fp32 and the base-GEMM epilogue adds it
+ * (lora_bgmv_adapter, then lora_base_gemm_delta); fp32 takes the BGMV
+ * shrink and a CUDA-core layer kernel.  Larger batches (prefill) take the
  * segment builder, the segment-grouped SGMV shrink and a base GEMM whose
  * tensor-memory accumulator also takes the expand as extra K-blocks
  * (lora_base_gemm_expand).  Either way y is stored once.
@@ -197,6 +198,25 @@ lora_status_t lora_bgmv_delta(const float* v_partial, int32_t ksplit, const void
                               const int32_t* slot_ids, float* delta, int32_t T, int32_t r,
                               int32_t d_out, int32_t n_slots, lora_dtype_t dt, void* ws,
                               size_t ws_bytes, void* stream);
+
+/*
+ * The whole BGMV adapter term of every token in one launch (bf16 only):
+ *   delta[t, :] = scale[a_t] * (x[t, :] A[a_t]) B[a_t]    for tokens with a valid id
+ * fp32 delta [T, d_out]; rows of base-only tokens are not written
+ * ("Serving multiple LoRAs: segmented matrix multiplies and adapter
+ * scheduling", BGMV bullet and the paragraph after the toy script: shrink to
+ * rank r, then expand).  One thread-block cluster per token: its CTAs shrink
+ * slices of d_in, sum the rank-r partials through distributed shared memory
+ * in a fixed order (deterministic) and expand slices of d_out.  This is the
+ * first kernel of lora_linear_fused for bf16 batches of up to 256 tokens;
+ * lora_base_gemm_delta adds its output.  T <= 65535.  scale may be null
+ * (1.0).  Workspace: the error word only.
+ */
+lora_status_t lora_bgmv_adapter(const void* x, const void* A_pool, const void* B_pool,
+                                const int32_t* slot_ids, const float* scale, float* delta,
+                                int32_t T, int32_t d_in, int32_t d_out, int32_t r,
+                                int32_t n_slots, lora_dtype_t dt, void* ws, size_t ws_bytes,
+                                void* stream);
 
 /*
  * The shared base product with a ready fp32 adapter term added in its

@@ -61,6 +61,14 @@ cudaError_t launch_fused_tc(const void* x, const void* W0, const void* B, const 
 // BGMV expand into an fp32 term: delta[t, :] = (sum_s vpart[s, t, :]) B[a_t]
 // for tokens with a valid id (other rows untouched); bf16 B.  `pdl`: launch
 // as a programmatic dependent of the shrink just before.
+// The whole BGMV adapter term of a decode-sized bf16 batch in one launch
+// (shrink, cluster sum of the rank-r partials, expand), fp32 into delta
+// [T, d_out]; rows of base-only tokens are not written.  One cluster of
+// adapter_cluster_size(d_in, d_out) CTAs per token.
+int adapter_cluster_size(int d_in, int d_out);
+cudaError_t launch_bgmv_adapter(const void* x, const void* A, const void* B, const int32_t* ids,
+                                const float* scale, float* delta, int T, int d_in, int d_out,
+                                int r, int n_slots, uint32_t* err, cudaStream_t st);
 cudaError_t launch_bgmv_delta(const float* vpart, int ksplit, const void* B, const int32_t* ids,
                               float* delta, int T, int r, int d_out, int n_slots, uint32_t* err,
                               cudaStream_t st, bool pdl);

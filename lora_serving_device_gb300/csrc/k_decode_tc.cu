@@ -15,10 +15,13 @@
 // blocks and W0 arrives as two 64-column x (64*KSUB)-row boxes per stage.
 //
 // d_in is split over a thread-block cluster of S CTAs (S a power of two,
-// <= 8).  Each CTA's fp32 partial tile goes straight from tensor memory into
-// the receive buffer of the CTA that owns those 128/S rows (remote shared-
-// memory vector stores); one cluster barrier later every owner sums its S
-// partials, adds the adapter term and stores its rows of y.
+// <= 8); rank z owns d_out rows [z*128/S, (z+1)*128/S) of the tile.  Each
+// CTA moves its fp32 partial tile from tensor memory into shared memory
+// (its own rows straight into slot z of its receive buffer, the others into
+// a staging area that reuses the drained pipeline ring), then sends each
+// owner its rows with one bulk shared-memory copy per peer, counted in bytes
+// on the owner's receive mbarrier.  The owner sums the S slots, adds the
+// adapter term and stores its rows of y.
 //
 // Warp roles: warp 0 = TMA producer, warp 1 = MMA issuer (and TMEM
 // allocator), warps 2-5 = epilogue.  Every on-chip wait is bounded in time;
@@ -52,11 +55,14 @@ struct DecLayout {
   static constexpr uint32_t kXBytes = KSUB * kXSub;
   static constexpr uint32_t kWBox = 64 * KSUB * 128;         // 64 columns x 64*KSUB rows
   static constexpr uint32_t kStage = kXBytes + 2 * kWBox;
-  static constexpr uint32_t kRb = 128 * BT * 4;              // receive buffer
+  static constexpr uint32_t kRb = 128 * BT * 4;              // receive buffer: S slots
+  // the fp32 partial tile is staged in the (drained) ring before it is sent
+  static_assert(kRb <= kStage, "staging must fit in one pipeline stage");
   static __host__ __device__ uint32_t rb(int stages) { return stages * kStage; }
   static __host__ __device__ uint32_t tok(int stages) { return rb(stages) + kRb; }
   static __host__ __device__ uint32_t bars(int stages) { return tok(stages) + BT * 4; }
-  static __host__ __device__ uint32_t misc(int stages) { return bars(stages) + (2 * stages + 1) * 8; }
+  // full[stages], empty[stages], accum_full, rx_full
+  static __host__ __device__ uint32_t misc(int stages) { return bars(stages) + (2 * stages + 2) * 8; }
   static __host__ __device__ uint32_t total(int stages) { return misc(stages) + 16; }
 };
 
@@ -88,19 +94,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + Lay::bars(p.stages));
   uint64_t* empty = full + p.stages;
   uint64_t* accum_full = empty + p.stages;
+  uint64_t* rx_full = accum_full + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::misc(p.stages));
   volatile int* abort_f = reinterpret_cast<volatile int*>(smem + Lay::misc(p.stages) + 8);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n0 = blockIdx.x * 128, t0 = blockIdx.y * BT;
   const int S = static_cast<int>(gridDim.z), z = static_cast<int>(blockIdx.z);
-  // peers may write into this CTA's receive buffer only once every CTA of
-  // the cluster is running (phase A of the cluster barrier)
-  if (S > 1) ptx::cluster_arrive_relaxed();
+  const int rows_own = 128 / S;
+  const uint32_t slot_bytes = static_cast<uint32_t>(rows_own * BT * 4);
 
   // ---- prologue: warp 0 initialises the barriers and starts streaming;
   // the others wait for that (named barrier 2); warp 1 allocates TMEM and
-  // hands the address to the epilogue warps (named barrier 3)
+  // hands the address to the epilogue warps (named barrier 3).  Peers send
+  // into this CTA only after phase A of the cluster barrier, which every
+  // thread arrives at once the receive mbarrier is initialised.
   if (warp == 0) {
     if (lane == 0) {
       ptx::prefetch_tmap(&tm_w);
@@ -110,13 +118,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_init(&empty[i], 1);
       }
       ptx::mbar_init(accum_full, 1);
+      ptx::mbar_init(rx_full, 1);
       *abort_f = 0;
       ptx::fence_mbar_init();
+      // the S-1 peers' slots complete phase 0 of rx_full
+      if (S > 1) ptx::mbar_arrive_expect_tx(rx_full, static_cast<uint32_t>(S - 1) * slot_bytes);
     }
     __syncwarp();
+    if (S > 1) ptx::cluster_arrive_release();
     named_arrive(2, kThreads);
   } else {
     named_sync(2, kThreads);
+    if (S > 1) ptx::cluster_arrive_relaxed();
     if (warp == 1) {
       ptx::tmem_alloc(tmem_slot, kTmemCols);
       ptx::tmem_relinquish();
@@ -192,19 +205,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (bad && blockIdx.x == 0 && z == 0) flag_error(p.err, LORA_DEVERR_BAD_SLOT);
     const bool acc_ok = warp_wait(accum_full, 0, abort_f);
-    if (S > 1) ptx::cluster_wait_acquire();  // phase A: the peers are running
     if (acc_ok) {
       ptx::tc_fence_after();
-      // TMEM lane = d_out row n of the tile, column = token.  Row n belongs to
-      // rank n / (128/S); its partial goes to slot [z][n % (128/S)] of that
-      // rank's receive buffer, token-contiguous.
+      // TMEM lane = d_out row n of the tile, column = token.  Row n belongs
+      // to rank n / (128/S): this rank's own rows go to its receive slot z,
+      // the others to the staging area, rank-major so each peer's rows are
+      // one contiguous block.  Rows are BT fp32 (token-contiguous) and the
+      // 16-byte chunks of row n are XOR-swizzled by n & 7, so the 32 lanes'
+      // vector stores spread over all banks.
       const int q = warp & 3;
-      const int rows_own = 128 / S;
       const int n = q * 32 + lane;
-      const int owner = n / rows_own, n_loc = n % rows_own;
-      const uint32_t local = ptx::smem_u32(smem + Lay::rb(p.stages)) +
-                             static_cast<uint32_t>(((z * rows_own + n_loc) * BT) * 4);
-      const uint32_t dst = S > 1 ? ptx::mapa_shared(local, static_cast<uint32_t>(owner)) : local;
+      const int owner = n / rows_own, n_loc = n - owner * rows_own;
+      float* row = owner == z
+          ? reinterpret_cast<float*>(smem + Lay::rb(p.stages)) + (z * rows_own + n_loc) * BT
+          : reinterpret_cast<float*>(smem) + n * BT;
       const uint32_t tq = tmem + (static_cast<uint32_t>(q * 32) << 16);
 #pragma unroll 1
       for (int c0 = 0; c0 < BT; c0 += 32) {
@@ -213,26 +227,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tmem_ld16(tq + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
         ptx::tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          ptx::st_dsmem_f4(dst + static_cast<uint32_t>((c0 + 4 * j) * 4),
-                           make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                       __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3])));
+        for (int j = 0; j < 8; ++j) {
+          const int chunk = ((c0 >> 2) + j) ^ (n & 7);
+          *reinterpret_cast<float4*>(row + chunk * 4) =
+              make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                          __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+        }
+      }
+      ptx::fence_proxy_async_smem();  // the bulk copies read the staging area
+    }
+    named_sync(1, kEpiThreads);
+    if (S > 1) {
+      ptx::cluster_wait_acquire();  // phase A: every peer's rx_full is initialised
+      if (acc_ok && etid < S && etid != z) {
+        const uint32_t src = ptx::smem_u32(smem) + static_cast<uint32_t>(etid) * slot_bytes;
+        const uint32_t dst_local = ptx::smem_u32(smem + Lay::rb(p.stages)) +
+                                   static_cast<uint32_t>(z) * slot_bytes;
+        ptx::bulk_copy_to_cluster(ptx::mapa_shared(dst_local, static_cast<uint32_t>(etid)), src,
+                                  slot_bytes,
+                                  ptx::mapa_shared(ptx::smem_u32(rx_full), static_cast<uint32_t>(etid)));
       }
     }
   }
 
-  // ---- reduction of the S partials of this rank's rows, store y -----------
+  // ---- reduction of the S slots of this rank's rows, store y -------------
   if (S > 1 && warp < 2) ptx::cluster_wait_acquire();  // phase A (epilogue warps did it)
   // this rank owns d_out rows [z * 128/S, (z+1) * 128/S) of the tile; the
-  // adapter-term loads (L2) are issued before the barrier so they overlap it
-  const int rows_own = 128 / S;
+  // adapter-term loads (L2) are issued before the receive wait so they
+  // overlap it
   const int groups = rows_own / 8;
   const int rows_tok = min(BT, p.T - t0);
   const int n_items = rows_tok * groups;
   constexpr int kMaxItems = (BT * 16 + kThreads - 1) / kThreads;  // S = 1: 16 groups
   float dl[kMaxItems][8];
   // every CTA waits, so that this grid completing implies its predecessors
-  // completed; the adapter term is written by the kernel launched just before
+  // completed; the adapter term is written by the kernel launched just before.
+  // Rows of base-only tokens are loaded too (they are in bounds) and dropped
+  // in the sum, so this does not wait for the token table.
   pdl_wait();
   if (p.delta != nullptr) {
 #pragma unroll
@@ -240,17 +271,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int e = tid + u * kThreads;
       const int g = e / (rows_tok > 0 ? rows_tok : 1), t = e - g * rows_tok;
       const int n = n0 + z * rows_own + g * 8;
-      if (e < n_items && n < p.d_out && tok[t] >= 0)
+      if (e < n_items && n < p.d_out)
         load8_dep(p.delta + static_cast<size_t>(t0 + t) * p.d_out + n, dl[u]);
     }
   }
+  __syncthreads();  // the token table and slot z, written by the epilogue warps
+  bool rx_ok = true;
   if (S > 1) {
-    ptx::cluster_arrive_release();  // phase B: every push has landed
-    ptx::cluster_wait_acquire();
-  } else {
-    __syncthreads();
+    rx_ok = ptx::mbar_wait_bounded(rx_full, 0, abort_f, kWaitLimitNs);
+    __syncwarp();
+    // phase B: this CTA has received every peer's slot, so the peers'
+    // staging areas have been read; a CTA leaves only after phase B
+    ptx::cluster_arrive_relaxed();
   }
-  if (!*abort_f) {
+  if (rx_ok && !*abort_f) {
     const float* rb = reinterpret_cast<const float*>(smem + Lay::rb(p.stages));
 #pragma unroll
     for (int u = 0; u < kMaxItems; ++u) {
@@ -261,9 +295,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (n >= p.d_out) continue;
       float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       for (int src = 0; src < S; ++src) {
-        const float* col = rb + (src * rows_own + g * 8) * BT + t;
+        const float* blk = rb + (src * rows_own + g * 8) * BT;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) f[j] += col[j * BT];
+        for (int j = 0; j < 8; ++j) f[j] += blk[j * BT + ((((t >> 2) ^ j) << 2) | (t & 3))];
       }
       if (p.delta != nullptr && tok[t] >= 0) {
 #pragma unroll
@@ -279,6 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tmem_dealloc(tmem, kTmemCols);
   }
   if (tid == 0 && *abort_f) flag_error(p.err, LORA_DEVERR_TIMEOUT);
+  if (S > 1) ptx::cluster_wait_acquire();  // phase B
 }
 
 template <int BT, int KSUB>

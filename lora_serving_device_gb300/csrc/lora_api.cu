@@ -283,13 +283,15 @@ lora_status_t lora_linear_fused(const void* x, const void* W0, const void* A_poo
   cudaError_t e;
   const bool decode = T <= kDecodeTokens;
   if (decode) {
-    // decode-sized batch: per-token gather (BGMV) -- no sort needed; for
-    // bf16 the expand runs into an fp32 term while the GEMM streams W0
-    e = launch_bgmv_shrink(x, A_pool, slot_ids, scale, w.vpart, T, d_in, r, n_slots, w.ksplit,
-                           dt, w.err, st);
-    if (e == cudaSuccess && dt == LORA_DTYPE_BF16)
-      e = launch_bgmv_delta(w.vpart, w.ksplit, B_pool, slot_ids, w.delta, T, r, d_out, n_slots,
-                            w.err, st, true);
+    // decode-sized batch: per-token gather (BGMV) -- no sort needed.  For
+    // bf16 one launch computes the whole adapter term into fp32 while the
+    // GEMM (its programmatic dependent) streams W0
+    if (dt == LORA_DTYPE_BF16)
+      e = launch_bgmv_adapter(x, A_pool, B_pool, slot_ids, scale, w.delta, T, d_in, d_out, r,
+                              n_slots, w.err, st);
+    else
+      e = launch_bgmv_shrink(x, A_pool, slot_ids, scale, w.vpart, T, d_in, r, n_slots, w.ksplit,
+                             dt, w.err, st);
   } else {
     // prefill-sized batch: segments, then the segment-grouped shrink (SGMV)
     e = launch_build_segments(slot_ids, T, n_slots, w.perm, w.seg_slot, w.seg_off, w.n_seg,
@@ -362,6 +364,30 @@ lora_status_t lora_bgmv_delta(const float* v_partial, int32_t ksplit, const void
   return from_cuda(launch_bgmv_delta(v_partial, ksplit, B_pool, slot_ids, delta, T, r, d_out,
                                      n_slots, static_cast<uint32_t*>(ws),
                                      static_cast<cudaStream_t>(stream), false));
+}
+
+lora_status_t lora_bgmv_adapter(const void* x, const void* A_pool, const void* B_pool,
+                                const int32_t* slot_ids, const float* scale, float* delta,
+                                int32_t T, int32_t d_in, int32_t d_out, int32_t r,
+                                int32_t n_slots, lora_dtype_t dt, void* ws, size_t ws_bytes,
+                                void* stream) {
+  if (T < 0) return LORA_ERR_INVALID_ARG;
+  if (dt != LORA_DTYPE_BF16) return LORA_ERR_DTYPE;
+  if (!tokens_ok(T) || T > 65535 || !dim_ok(d_in) || !dim_ok(d_out) || !rank_ok(r) ||
+      !slots_ok(n_slots))
+    return LORA_ERR_SHAPE;
+  if (x == nullptr || A_pool == nullptr || B_pool == nullptr || slot_ids == nullptr ||
+      delta == nullptr || !aligned16(x) || !aligned16(A_pool) || !aligned16(B_pool) ||
+      !aligned16(delta))
+    return LORA_ERR_INVALID_ARG;
+  lora_status_t s = check_ws(ws, ws_bytes, kErrBytes);
+  if (s != LORA_OK) return s;
+  if (T == 0) return LORA_OK;
+  DeviceInfo dev;
+  if ((s = check_device(&dev)) != LORA_OK) return s;
+  return from_cuda(launch_bgmv_adapter(x, A_pool, B_pool, slot_ids, scale, delta, T, d_in, d_out,
+                                       r, n_slots, static_cast<uint32_t*>(ws),
+                                       static_cast<cudaStream_t>(stream)));
 }
 
 lora_status_t lora_base_gemm_delta(const void* x, const void* W0, const float* delta,

@@ -205,6 +205,19 @@ __device__ __forceinline__ void st_dsmem_f4(uint32_t addr, float4 v) {
                "f"(v.z), "f"(v.w)
                : "memory");
 }
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
+// from this CTA's shared memory into the shared memory of a CTA of the
+// cluster; completion is counted in bytes on `mbar_cluster`, an mbarrier of
+// the destination CTA.  Shared-memory writes feeding the copy must be made
+// visible to the async proxy first (fence_proxy_async_smem).
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst_cluster, uint32_t src_cta,
+                                                     uint32_t bytes, uint32_t mbar_cluster) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst_cluster),
+      "r"(src_cta), "r"(bytes), "r"(mbar_cluster)
+      : "memory");
+}
 // Address of the same shared-memory location in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
   uint32_t r;

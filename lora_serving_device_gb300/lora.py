@@ -26,7 +26,8 @@ NOALLOC_SCRATCH_BYTES = 8 << 20
 
 EXPORTS = ("lora_workspace_bytes", "lora_build_segments", "lora_bgmv_shrink", "lora_bgmv_expand",
            "lora_sgmv_shrink", "lora_sgmv_expand", "lora_linear_fused", "lora_base_gemm_expand",
-           "lora_linear_fused_noalloc", "lora_bgmv_delta", "lora_base_gemm_delta",
+           "lora_linear_fused_noalloc", "lora_bgmv_delta", "lora_bgmv_adapter",
+           "lora_base_gemm_delta",
            "lora_get_error", "lora_status_string")
 
 
@@ -52,6 +53,7 @@ _SIGS = {
     "lora_base_gemm_expand": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _Z, _P]),
     "lora_linear_fused_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "lora_bgmv_delta": (_I, [_P, _I, _P, _P, _P, _I, _I, _I, _I, _I, _P, _Z, _P]),
+    "lora_bgmv_adapter": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _Z, _P]),
     "lora_base_gemm_delta": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _Z, _P]),
     "lora_get_error": (_I, [_P, _P, ctypes.POINTER(ctypes.c_int32)]),
     "lora_status_string": (ctypes.c_char_p, [_I]),
@@ -133,6 +135,12 @@ def lora_linear_fused_noalloc(x, W0, A_pool, B_pool, slot_ids, scale, y, T, d_in
 def lora_bgmv_delta(v_partial, ksplit, B_pool, slot_ids, delta, T, r, d_out, n_slots, dt, ws,
                     ws_bytes, stream):
     return _call("lora_bgmv_delta", v_partial, ksplit, B_pool, slot_ids, delta, T, r, d_out,
+                 n_slots, dt, ws, ws_bytes, stream)
+
+
+def lora_bgmv_adapter(x, A_pool, B_pool, slot_ids, scale, delta, T, d_in, d_out, r, n_slots, dt,
+                      ws, ws_bytes, stream):
+    return _call("lora_bgmv_adapter", x, A_pool, B_pool, slot_ids, scale, delta, T, d_in, d_out, r,
                  n_slots, dt, ws, ws_bytes, stream)
 
 
@@ -281,6 +289,21 @@ def bgmv_delta_t(v_partial, B_pool, slot_ids, ws, delta=None, stream=None):
     check(lora_bgmv_delta(_ptr(v_partial), ksplit, _ptr(B_pool), _ptr(slot_ids), _ptr(delta), T, r,
                           d_out, n_slots, _dt(B_pool), _ptr(ws), ws.numel(), _stream(stream)),
           "lora_bgmv_delta")
+    return delta
+
+
+def bgmv_adapter_t(x, A_pool, B_pool, slot_ids, scale, ws, delta=None, stream=None):
+    """fp32 adapter term delta[t] = s_a (x[t] A_a) B_a in one launch (rows of base-only
+    tokens untouched)."""
+    import torch
+    T, d_in = x.shape
+    n_slots, r, d_out = B_pool.shape
+    if delta is None:
+        delta = torch.zeros((T, d_out), dtype=torch.float32, device=x.device)
+    check(lora_bgmv_adapter(_ptr(x), _ptr(A_pool), _ptr(B_pool), _ptr(slot_ids), _ptr(scale),
+                            _ptr(delta), T, d_in, d_out, r, n_slots, _dt(x), _ptr(ws), ws.numel(),
+                            _stream(stream)),
+          "lora_bgmv_adapter")
     return delta
 
 

@@ -156,6 +156,10 @@ FUSED_CASES = [
     (128, 384, 256, 128, 4),
     (200, 256, 264, 128, 6),
     (96, 320, 392, 8, 21),
+    # adapter clusters of 2 and 4 CTAs with ragged d_in / d_out slices
+    (7, 1032, 600, 32, 4),
+    (48, 2056, 2120, 16, 9),
+    (16, 2048, 2048, 128, 5),
     (200, 640, 136, 16, 30),
     (256, 256, 512, 64, 70),
     (257, 192, 264, 16, 11),
@@ -358,6 +362,38 @@ def test_bgmv_delta_matches_oracle(L, case):
     valid = (w.slot_ids >= 0) & (w.slot_ids < n_slots)
     check_close(got[valid], ref[valid], "bgmv delta (fp32 out)", rel_fro=1e-5, max_rms=1e-4)
     assert np.all(got[~valid] == 7.0)          # base-only rows not written
+
+
+ADAPTER_CASES = BLOCK_CASES + [(7, 1032, 600, 32, 4), (48, 2056, 2120, 16, 9),
+                               (16, 2048, 2048, 128, 5), (64, 4096, 4096, 16, 256)]
+
+
+@pytest.mark.parametrize("case", ADAPTER_CASES, ids=[str(c) for c in ADAPTER_CASES])
+def test_bgmv_adapter_matches_oracle(L, case):
+    """The one-launch adapter term (shrink, cluster sum, expand) against the
+    oracle's shrink then expand.  Nothing is rounded to bf16 on this path:
+    bf16 inputs, fp32 products and sums, fp32 out, so the bar is the fp32
+    accumulation error of a d_in-long and an r-long dot product."""
+    torch = torch_mod()
+    T, d_in, d_out, r, n_slots = case
+    w = W.random_case(730 + T, T, d_in, d_out, r, n_slots, invalid=1)
+    d = DeviceCase(w)
+    ws = _ws(L)
+    delta = torch.full((T, d_out), 7.0, dtype=torch.float32, device="cuda")
+    L.bgmv_adapter_t(d.x, d.A, d.B, d.ids, d.scale, ws, delta=delta)
+    torch.cuda.synchronize()
+    ref = O.expand(O.shrink(w.x, w.A_pool, w.scale, w.slot_ids), w.B_pool, w.slot_ids)
+    got = host(delta)
+    valid = (w.slot_ids >= 0) & (w.slot_ids < n_slots)
+    check_close(got[valid], ref[valid], "bgmv adapter term (fp32 out)", rel_fro=2e-5,
+                max_rms=2e-4)
+    assert np.all(got[~valid] == 7.0)          # base-only rows not written
+    assert L.get_error_t(ws) & L.DEVERR_BAD_SLOT
+    # deterministic: the cluster sums its partials in a fixed order
+    delta2 = torch.full((T, d_out), 7.0, dtype=torch.float32, device="cuda")
+    L.bgmv_adapter_t(d.x, d.A, d.B, d.ids, d.scale, ws, delta=delta2)
+    torch.cuda.synchronize()
+    assert torch.equal(delta, delta2)
 
 
 @pytest.mark.parametrize("case", BLOCK_CASES, ids=[str(c) for c in BLOCK_CASES])
