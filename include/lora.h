@@ -171,13 +171,24 @@ lora_status_t lora_sgmv_expand(const float* v_partial, int32_t ksplit, const voi
  * batch": the base product once for all rows, then each row's adapter term;
  * "Serving many LoRA adapters", "Replay" figure: segmented gather, grouped
  * GEMM, scatter add, one fused output).  Batches of up to 256 tokens
- * (decode) take the per-token BGMV path: for bf16 one launch computes the
- * whole adapter term in fp32 and the base-GEMM epilogue adds it
- * (lora_bgmv_adapter, then lora_base_gemm_delta); fp32 takes the BGMV
- * shrink and a CUDA-core layer kernel.  Larger batches (prefill) take the
- * segment builder, the segment-grouped SGMV shrink and a base GEMM whose
- * tensor-memory accumulator also takes the expand as extra K-blocks
+ * (decode) take the per-token BGMV path: for bf16 the base product split
+ * over d_in into fp32 partials (lora_base_gemm_splitk), then one kernel that
+ * computes each token's adapter term, adds the partials and stores y
+ * (lora_bgmv_adapter_merge).  fp32 takes the BGMV shrink and a CUDA-core
+ * layer kernel.  Larger batches (prefill) take the segment builder, the
+ * segment-grouped SGMV shrink and a base GEMM whose tensor-memory
+ * accumulator also takes the expand as extra K-blocks
  * (lora_base_gemm_expand).  Either way y is stored once.
+ *
+ * Overlap with the previous kernel (bf16 decode-sized batches): the first
+ * kernel is launched as a programmatic dependent of whatever precedes it
+ * in the stream.  If that kernel lets its dependents start early
+ * (griddepcontrol.launch_dependents), this layer's W0 starts streaming
+ * before it completes; everything else (x, the ids, the adapters, the
+ * scales) is read only after it completed.  So W0 must not be written by a
+ * kernel that lets its dependents start early and runs right before this
+ * call.  The last kernel of this call lets the next one start early in the
+ * same way, so consecutive layers overlap.
  */
 lora_status_t lora_linear_fused(const void* x, const void* W0, const void* A_pool,
                                 const void* B_pool, const int32_t* slot_ids, const float* scale,
@@ -207,10 +218,10 @@ lora_status_t lora_bgmv_delta(const float* v_partial, int32_t ksplit, const void
  * scheduling", BGMV bullet and the paragraph after the toy script: shrink to
  * rank r, then expand).  One thread-block cluster per token: its CTAs shrink
  * slices of d_in, sum the rank-r partials through distributed shared memory
- * in a fixed order (deterministic) and expand slices of d_out.  This is the
- * first kernel of lora_linear_fused for bf16 batches of up to 256 tokens;
- * lora_base_gemm_delta adds its output.  T <= 65535.  scale may be null
- * (1.0).  Workspace: the error word only.
+ * in a fixed order (deterministic) and expand slices of d_out.
+ * lora_bgmv_adapter_merge is the same kernel adding the base product, the
+ * last kernel of lora_linear_fused for bf16 batches of up to 256 tokens.
+ * T <= 65535.  scale may be null (1.0).  Workspace: the error word only.
  */
 lora_status_t lora_bgmv_adapter(const void* x, const void* A_pool, const void* B_pool,
                                 const int32_t* slot_ids, const float* scale, float* delta,
@@ -219,16 +230,46 @@ lora_status_t lora_bgmv_adapter(const void* x, const void* A_pool, const void* B
                                 void* stream);
 
 /*
- * The shared base product with a ready fp32 adapter term added in its
- * epilogue (bf16, tcgen05 tensor cores):
- *   y[t, :] = x[t, :] W0 + delta[t, :]     for tokens with a valid id
- *   y[t, :] = x[t, :] W0                    otherwise (delta row not read)
- * y is OVERWRITTEN and written once.  Workspace: the error word only.
+ * The merge form of lora_bgmv_adapter: the last kernel of lora_linear_fused
+ * for bf16 batches of up to 256 tokens (bf16 only):
+ *   y[t, :] = sum_s partial[s, t, :] + scale[a_t] (x[t, :] A[a_t]) B[a_t]   (a_t valid)
+ *   y[t, :] = sum_s partial[s, t, :]                                        (base only)
+ * partial [ksplit, T, d_out] fp32 is any split of the base product x W0
+ * over d_in (lora_base_gemm_splitk writes one).  y [T, d_out] bf16 is
+ * OVERWRITTEN, every row, rounded once ("Multi-LoRA batching and adapter
+ * paging", section "Walking through a batch": the base product once for
+ * all rows, each row then gets its own adapter term).  1 <= ksplit <=
+ * LORA_MAX_KSPLIT; T <= 65535; scale may be null (1.0).  Workspace: the
+ * error word only.
  */
-lora_status_t lora_base_gemm_delta(const void* x, const void* W0, const float* delta,
-                                   const int32_t* slot_ids, void* y, int32_t T, int32_t d_in,
-                                   int32_t d_out, int32_t n_slots, lora_dtype_t dt, void* ws,
-                                   size_t ws_bytes, void* stream);
+lora_status_t lora_bgmv_adapter_merge(const void* x, const void* A_pool, const void* B_pool,
+                                      const int32_t* slot_ids, const float* scale,
+                                      const float* partial, int32_t ksplit, void* y, int32_t T,
+                                      int32_t d_in, int32_t d_out, int32_t r, int32_t n_slots,
+                                      lora_dtype_t dt, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * The shared base product split over d_in, on tcgen05 tensor cores with
+ * the token dimension as the MMA's N (bf16 only):
+ *   partial[s, t, :] = x[t, K_s] W0[K_s, :]      s = 0 .. ksplit-1
+ * where K_0 .. K_{ksplit-1} are contiguous ranges of d_in that together
+ * cover it ("Multi-LoRA batching and adapter paging", section "Walking
+ * through a batch": one base product for the whole batch).  partial
+ * [ksplit, T, d_out] fp32, caller-owned, fully written.  1 <= ksplit <=
+ * the number of 192-row (T <= 64) or 128-row (T > 64) blocks of d_in, and
+ * <= LORA_MAX_KSPLIT; lora_decode_split gives the value lora_linear_fused
+ * uses.  Any T; it is built for T <= 256.  Workspace: the error word only.
+ */
+lora_status_t lora_base_gemm_splitk(const void* x, const void* W0, float* partial, int32_t T,
+                                    int32_t d_in, int32_t d_out, int32_t ksplit, lora_dtype_t dt,
+                                    void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * The ksplit lora_linear_fused uses for the base product of a bf16 batch of
+ * 1 <= T <= 256 tokens (a function of the shapes only, so results do not
+ * depend on the device); 0 for other T or invalid dimensions.
+ */
+int32_t lora_decode_split(int32_t T, int32_t d_in, int32_t d_out);
 
 /*
  * The last kernel of lora_linear_fused on its own: the shared base product

@@ -58,17 +58,27 @@ cudaError_t launch_fused_tc(const void* x, const void* W0, const void* B, const 
                             const float* vpart, int v_ksplit, const float* delta, void* y, int T,
                             int d_in, int d_out, int r, int n_slots, uint32_t* err,
                             cudaStream_t st, const DeviceInfo& dev);
-// BGMV expand into an fp32 term: delta[t, :] = (sum_s vpart[s, t, :]) B[a_t]
-// for tokens with a valid id (other rows untouched); bf16 B.  `pdl`: launch
-// as a programmatic dependent of the shrink just before.
 // The whole BGMV adapter term of a decode-sized bf16 batch in one launch
-// (shrink, cluster sum of the rank-r partials, expand), fp32 into delta
-// [T, d_out]; rows of base-only tokens are not written.  One cluster of
-// adapter_cluster_size(d_in, d_out) CTAs per token.
+// (shrink, cluster sum of the rank-r partials, expand), see k_adapter.cu.
+// One cluster of adapter_cluster_size(d_in, d_out) CTAs per token.
+//  - launch_bgmv_adapter: fp32 into delta [T, d_out]; rows of base-only
+//    tokens are not written.
+//  - launch_bgmv_adapter_merge: y = sum of the S fp32 partials [S, T, d_out]
+//    of the decode GEMM + the adapter term, bf16, every row written.  `pdl`:
+//    launch as a programmatic dependent of that GEMM (it waits for it before
+//    reading the partials).
 int adapter_cluster_size(int d_in, int d_out);
 cudaError_t launch_bgmv_adapter(const void* x, const void* A, const void* B, const int32_t* ids,
                                 const float* scale, float* delta, int T, int d_in, int d_out,
                                 int r, int n_slots, uint32_t* err, cudaStream_t st);
+cudaError_t launch_bgmv_adapter_merge(const void* x, const void* A, const void* B,
+                                      const int32_t* ids, const float* scale,
+                                      const float* partial, int S, void* y, int T, int d_in,
+                                      int d_out, int r, int n_slots, uint32_t* err, bool pdl,
+                                      cudaStream_t st);
+// BGMV expand into an fp32 term: delta[t, :] = (sum_s vpart[s, t, :]) B[a_t]
+// for tokens with a valid id (other rows untouched); bf16 B.  `pdl`: launch
+// as a programmatic dependent of the shrink just before.
 cudaError_t launch_bgmv_delta(const float* vpart, int ksplit, const void* B, const int32_t* ids,
                               float* delta, int T, int r, int d_out, int n_slots, uint32_t* err,
                               cudaStream_t st, bool pdl);
@@ -84,10 +94,15 @@ bool tensor_map_available();
 // outside the tensor read as zero.
 bool encode_tensor_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
                             uint64_t row_elems, uint32_t box_inner, uint32_t box_outer);
-// Decode-sized base GEMM (T <= 256) adding a ready fp32 adapter term, see
-// k_decode_tc.cu.
-cudaError_t launch_decode_tc(const void* x, const void* W0, const int32_t* ids,
-                             const float* delta, void* y, int T, int d_in, int d_out, int n_slots,
-                             uint32_t* err, cudaStream_t st, const DeviceInfo& dev);
+// Decode-sized base GEMM split over d_in into S fp32 partials
+// partial[z, t, :] = x[t, K_z] W0[K_z, :], see k_decode_tc.cu.  `pdl`: launch
+// as a programmatic dependent (W0 is prefetched before the wait, x after).
+// decode_gemm_split: the S the fused layer uses (a function of the shapes
+// only); decode_gemm_max_split: the largest S the kernel accepts.
+int decode_gemm_split(int T, int d_in, int d_out);
+int decode_gemm_max_split(int T, int d_in);
+cudaError_t launch_decode_gemm(const void* x, const void* W0, float* partial, int T, int d_in,
+                               int d_out, int S, uint32_t* err, bool pdl, cudaStream_t st,
+                               const DeviceInfo& dev);
 
 }  // namespace lora

@@ -1,20 +1,26 @@
-// The whole adapter term of a decode-sized batch in one launch:
-// delta[t, :] = s_a * (x[t, :] A_a) B_a for every token t with a valid
-// adapter a = ids[t] ("Serving multiple LoRAs: segmented matrix multiplies
-// and adapter scheduling", BGMV bullet: each token gathers its own adapter's
-// factors; the shrink to rank r comes first, then the expand).  The fp32
-// result is added by the decode base GEMM in its epilogue, so y is stored
-// once.
+// The BGMV adapter term of a decode-sized batch in one launch
+// ("Serving multiple LoRAs: segmented matrix multiplies and adapter
+// scheduling", BGMV bullet: each token gathers its own adapter's factors;
+// the shrink to rank r comes first, then the expand):
+//   delta[t, :] = s_a * (x[t, :] A_a) B_a          a = ids[t] valid
+// and, in its merge form, the last kernel of the decode layer:
+//   y[t, :] = sum_z partial[z, t, :] + delta[t, :]  (delta = 0 for base-only t)
+// where partial holds the split-K fp32 base product x W0 of the decode GEMM,
+// so y is stored once ("Multi-LoRA batching and adapter paging", section
+// "Walking through a batch": the base product once for all rows, then each
+// row's adapter term).
 //
 // One thread-block cluster of C CTAs per token.  CTA c shrinks the c-th
 // slice of d_in (x[t, K_c] A_a[K_c, :], the slice of A_a read once), the C
-// rank-r partials are summed through distributed shared memory in a fixed
-// order (deterministic, no atomics), and CTA c then expands the c-th slice
-// of the d_out columns.  B_a rows for the first columns are requested before
-// the shrink, so their latency overlaps it.  Launched first in the decode
-// chain, it lets the base GEMM start streaming W0 at once (programmatic
-// launch); it uses under 1 KiB of shared memory so its CTAs fit beside a
-// base-GEMM CTA on one SM.
+// rank-r partials are summed through distributed shared memory in rank
+// order (deterministic, no atomics), and CTA c expands the c-th slice of
+// the d_out columns into registers.  B_a rows of the first columns are
+// requested before the shrink, so their latency overlaps it.
+//
+// The merge form is launched as a programmatic dependent of the decode GEMM:
+// it starts while the GEMM still streams W0 (its CTAs need little shared
+// memory and fit beside a GEMM CTA), computes the adapter term, and only
+// then waits for the GEMM grid and reads its partials.
 #include "common.cuh"
 #include "internal.h"
 #include "ptx.cuh"
@@ -24,148 +30,219 @@ namespace {
 
 constexpr int kAdThreads = 256;
 constexpr int kAdWarps = kAdThreads / 32;
+constexpr int kPairs = kAdThreads / 2;     // thread pairs along the columns
+constexpr int kGroupCols = 8;              // columns of one thread pair
+constexpr int kStride = kPairs * kGroupCols;
+constexpr int kKeepGroups = 2;             // column groups held across the wait
 
 template <int R>
+struct AdapterShape {
+  static constexpr int QC = R / 8;             // 8-wide column chunks of an A row
+  static constexpr int KL = kAdThreads / QC;   // threads along d_in
+  static constexpr int RH = R / 2;             // B rows per thread of a pair
+  static constexpr int kPre = RH < 8 ? RH : 8; // B rows requested before the shrink
+  static_assert(R % 8 == 0 && QC <= 32, "rank");
+};
+
+// Adapter term of the 8 columns [g, g+8) for thread h of the pair: thread h
+// takes B rows [h*R/2, (h+1)*R/2), the halves are added with one shuffle, so
+// both threads of the pair end with all 8 values.  Every thread of the warp
+// must call it (the shuffle); `on` says whether g is inside the slice.  With
+// PRE the first rows come from `pre` (loaded earlier) instead of memory.
+template <int R, bool PRE>
+__device__ __forceinline__ void expand_group(const bf16* Ba, const float* vs, int d_out, int g,
+                                             int h, bool on,
+                                             const uint4 (&pre)[AdapterShape<R>::kPre],
+                                             float (&o)[8]) {
+  using SH = AdapterShape<R>;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) o[e] = 0.f;
+  if (on) {
+#pragma unroll
+    for (int j = 0; j < SH::RH; ++j) {
+      const uint4 w = (PRE && j < SH::kPre)
+                          ? pre[j < SH::kPre ? j : 0]
+                          : *reinterpret_cast<const uint4*>(
+                                Ba + static_cast<size_t>(h * SH::RH + j) * d_out + g);
+      const float vq = vs[h * SH::RH + j];
+      const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        o[2 * e] = fmaf(vq, bf16_lo(u[e]), o[2 * e]);
+        o[2 * e + 1] = fmaf(vq, bf16_hi(u[e]), o[2 * e + 1]);
+      }
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) o[e] += __shfl_xor_sync(0xffffffffu, o[e], 1);
+}
+
+// Output of one column group: thread h of the pair owns columns
+// [g + 4h, g + 4h + 4).  Delta form: the fp32 adapter term.  Merge form: the
+// S partials of the base product (written by the grid this one waited for)
+// plus the adapter term, rounded once to bf16.
+template <bool MERGE>
+__device__ __forceinline__ void store_group(const float (&o)[8], int g, int h, int t, int d_out,
+                                            const float* partial, int S, int T, void* out) {
+  const int n = g + 4 * h;
+  // (selects, not o[4 * h + k]: a runtime index would put o in local memory)
+  float f[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) f[k] = h ? o[4 + k] : o[k];
+  if (MERGE) {
+    for (int zz = 0; zz < S; ++zz) {
+      const float4 pz = ld_dep_f4(partial + (static_cast<size_t>(zz) * T + t) * d_out + n);
+      f[0] += pz.x;
+      f[1] += pz.y;
+      f[2] += pz.z;
+      f[3] += pz.w;
+    }
+    uint2 pk;
+    pk.x = pack_bf16x2(f[0], f[1]);
+    pk.y = pack_bf16x2(f[2], f[3]);
+    *reinterpret_cast<uint2*>(static_cast<bf16*>(out) + static_cast<size_t>(t) * d_out + n) = pk;
+  } else {
+    *reinterpret_cast<float4*>(static_cast<float*>(out) + static_cast<size_t>(t) * d_out + n) =
+        make_float4(f[0], f[1], f[2], f[3]);
+  }
+}
+
+template <int R, bool MERGE>
 __global__ void __launch_bounds__(kAdThreads)
     bgmv_adapter_kernel(const bf16* __restrict__ x, const bf16* __restrict__ A,
                         const bf16* __restrict__ B, const int32_t* __restrict__ ids,
-                        const float* __restrict__ scale, float* __restrict__ delta, int T,
-                        int d_in, int d_out, int n_slots, int kc, int nc, uint32_t* err) {
-  constexpr int QC = R / 8;             // 8-wide column chunks of an A row
-  constexpr int KL = kAdThreads / QC;   // threads along d_in
-  constexpr int H = 2;                  // threads sharing one 8-column group of the expand
-  constexpr int RH = R / H;             // B rows per thread
-  constexpr int kPre = RH < 8 ? RH : 8; // B rows requested before the shrink
-  static_assert(R % 8 == 0 && QC <= 32, "rank");
+                        const float* __restrict__ scale, const float* partial, int S,
+                        void* out, int T, int d_in, int d_out, int n_slots, int kc, int nc,
+                        uint32_t* err) {
+  using SH = AdapterShape<R>;
   __shared__ float red[kAdWarps][R];
   __shared__ float pv[R];  // this CTA's partial, read by the whole cluster
   __shared__ float vs[R];  // the token's full shrink output, scaled
 
-  pdl_launch_dependents();  // the base GEMM may start streaming W0 now
+  pdl_launch_dependents();
   const int c = static_cast<int>(ptx::cluster_ctarank());
   const int C = static_cast<int>(gridDim.x);
   const int t = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int id = ids[t];
-  if (!slot_valid(id, n_slots)) {
-    // every CTA of the cluster reads the same id and leaves here together
-    if (tid == 0 && c == 0 && id != -1) flag_error(err, LORA_DEVERR_BAD_SLOT);
-    return;
-  }
+  // every CTA of the cluster reads the same id, so `valid` and everything it
+  // guards (the cluster barriers included) is uniform over the cluster
+  const bool valid = slot_valid(id, n_slots);
+  if (!valid && id != -1 && tid == 0 && c == 0) flag_error(err, LORA_DEVERR_BAD_SLOT);
+  if (!MERGE && !valid) return;  // delta form: base-only rows are not written
 
-  // ---- first B rows of this thread's first column group (independent of v)
-  const int h = tid % H;
+  const int h = tid & 1, pair = tid >> 1;
   const int n_begin = c * nc, n_end = min(d_out, n_begin + nc);
-  const bf16* Ba = B + static_cast<size_t>(id) * R * d_out;
-  const int g0 = n_begin + (tid / H) * 8;
-  uint4 bpre[kPre];
-  if (g0 < n_end) {
+  const bf16* Ba = B + static_cast<size_t>(valid ? id : 0) * R * d_out;
+  float keep[kKeepGroups][8];
 #pragma unroll
-    for (int j = 0; j < kPre; ++j)
-      bpre[j] = *reinterpret_cast<const uint4*>(Ba + static_cast<size_t>(h * RH + j) * d_out + g0);
-  }
+  for (int i = 0; i < kKeepGroups; ++i)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) keep[i][e] = 0.f;
 
-  // ---- shrink of this CTA's d_in slice
-  const int qc = tid % QC, kl = tid / QC;
-  const int k_begin = c * kc, k_end = min(d_in, k_begin + kc);
-  const bf16* Aa = A + static_cast<size_t>(id) * d_in * R + qc * 8;
-  const bf16* xt = x + static_cast<size_t>(t) * d_in;
-  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  if (valid) {
+    // ---- first B rows of this thread's first column group (independent of v)
+    const int g0 = n_begin + pair * kGroupCols;
+    uint4 bpre[SH::kPre];
+    if (g0 < n_end) {
+#pragma unroll
+      for (int j = 0; j < SH::kPre; ++j)
+        bpre[j] = *reinterpret_cast<const uint4*>(Ba + static_cast<size_t>(h * SH::RH + j) * d_out + g0);
+    }
+
+    // ---- shrink of this CTA's d_in slice
+    const int qc = tid % SH::QC, kl = tid / SH::QC;
+    const int k_begin = c * kc, k_end = min(d_in, k_begin + kc);
+    const bf16* Aa = A + static_cast<size_t>(id) * d_in * R + qc * 8;
+    const bf16* xt = x + static_cast<size_t>(t) * d_in;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll 2
-  for (int k = k_begin + kl * 8; k < k_end; k += KL * 8) {
-    float xv[8];
-    load8(xt + k, xv);
+    for (int k = k_begin + kl * 8; k < k_end; k += SH::KL * 8) {
+      float xv[8];
+      load8(xt + k, xv);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      float a[8];
-      load8(Aa + static_cast<size_t>(k + j) * R, a);
+      for (int j = 0; j < 8; ++j) {
+        float a[8];
+        load8(Aa + static_cast<size_t>(k + j) * R, a);
 #pragma unroll
-      for (int q = 0; q < 8; ++q) acc[q] = fmaf(xv[j], a[q], acc[q]);
-    }
-  }
-  // lanes sharing a column chunk sit QC apart in the warp
-#pragma unroll
-  for (int o = QC; o < 32; o <<= 1) {
-#pragma unroll
-    for (int q = 0; q < 8; ++q) acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], o);
-  }
-  if (lane < QC) {
-#pragma unroll
-    for (int q = 0; q < 8; ++q) red[warp][lane * 8 + q] = acc[q];
-  }
-  __syncthreads();
-  if (tid < R) {
-    float a = 0.f;
-#pragma unroll
-    for (int w = 0; w < kAdWarps; ++w) a += red[w][tid];
-    pv[tid] = a;
-  }
-
-  // ---- sum the C partials in rank order; every CTA gets the same v
-  ptx::cluster_arrive_release();
-  ptx::cluster_wait_acquire();
-  if (tid < R) {
-    const uint32_t local = ptx::smem_u32(&pv[tid]);
-    float a = 0.f;
-    for (int src = 0; src < C; ++src) {
-      float v;
-      asm volatile("ld.shared::cluster.f32 %0, [%1];"
-                   : "=f"(v)
-                   : "r"(ptx::mapa_shared(local, static_cast<uint32_t>(src))));
-      a += v;
-    }
-    vs[tid] = a * (scale ? scale[id] : 1.f);
-  }
-  __syncthreads();
-  // done reading the peers' partials; a CTA leaves only after every peer is
-  ptx::cluster_arrive_relaxed();
-
-  // ---- expand this CTA's columns: thread pair (g, h) covers 8 columns, h
-  // takes half of the R rows, and the halves are added with one shuffle.
-  // The trip count is the same for every thread (the shuffle needs the
-  // whole warp).
-  constexpr int kStride = (kAdThreads / H) * 8;
-#pragma unroll 1
-  for (int base = n_begin; base < n_end; base += kStride) {
-    const int g = base + (tid / H) * 8;
-    const bool on = g < n_end;
-    float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    if (on) {
-#pragma unroll
-      for (int j = 0; j < RH; ++j) {
-        const uint4 w = (base == n_begin && j < kPre)
-                            ? bpre[j]
-                            : *reinterpret_cast<const uint4*>(
-                                  Ba + static_cast<size_t>(h * RH + j) * d_out + g);
-        const float vq = vs[h * RH + j];
-        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          o[2 * e] = fmaf(vq, bf16_lo(u[e]), o[2 * e]);
-          o[2 * e + 1] = fmaf(vq, bf16_hi(u[e]), o[2 * e + 1]);
-        }
+        for (int q = 0; q < 8; ++q) acc[q] = fmaf(xv[j], a[q], acc[q]);
       }
     }
-    if (H == 2) {
+    // lanes sharing a column chunk sit QC apart in the warp
 #pragma unroll
-      for (int e = 0; e < 8; ++e) o[e] += __shfl_xor_sync(0xffffffffu, o[e], 1);
+    for (int o = SH::QC; o < 32; o <<= 1) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], o);
     }
-    if (on && h == 0) store8(delta + static_cast<size_t>(t) * d_out + g, o);
+    if (lane < SH::QC) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) red[warp][lane * 8 + q] = acc[q];
+    }
+    __syncthreads();
+    if (tid < R) {
+      float a = 0.f;
+#pragma unroll
+      for (int w = 0; w < kAdWarps; ++w) a += red[w][tid];
+      pv[tid] = a;
+    }
+
+    // ---- sum the C partials in rank order; every CTA gets the same v
+    ptx::cluster_arrive_release();
+    ptx::cluster_wait_acquire();
+    if (tid < R) {
+      const uint32_t local = ptx::smem_u32(&pv[tid]);
+      float a = 0.f;
+      for (int src = 0; src < C; ++src) {
+        float v;
+        asm volatile("ld.shared::cluster.f32 %0, [%1];"
+                     : "=f"(v)
+                     : "r"(ptx::mapa_shared(local, static_cast<uint32_t>(src))));
+        a += v;
+      }
+      vs[tid] = a * (scale ? scale[id] : 1.f);
+    }
+    __syncthreads();
+    // done reading the peers' partials; a CTA leaves only after every peer is
+    ptx::cluster_arrive_relaxed();
+
+    // ---- expand the first column groups into registers
+    if (n_begin < n_end)  // uniform over the CTA
+      expand_group<R, true>(Ba, vs, d_out, g0, h, g0 < n_end, bpre, keep[0]);
+#pragma unroll
+    for (int i = 1; i < kKeepGroups; ++i) {
+      const int base = n_begin + i * kStride;
+      if (base < n_end) {  // uniform over the CTA
+        const int g = base + pair * kGroupCols;
+        expand_group<R, false>(Ba, vs, d_out, g, h, g < n_end, bpre, keep[i]);
+      }
+    }
   }
-  ptx::cluster_wait_acquire();
+
+  // ---- outputs.  Merge form: wait for the decode GEMM (its partials)
+  if (MERGE) pdl_wait();
+#pragma unroll
+  for (int i = 0; i < kKeepGroups; ++i) {
+    const int g = n_begin + i * kStride + pair * kGroupCols;
+    if (g < n_end) store_group<MERGE>(keep[i], g, h, t, d_out, partial, S, T, out);
+  }
+  // columns beyond the kept groups (slices wider than kKeepGroups * kStride)
+#pragma unroll 1
+  for (int base = n_begin + kKeepGroups * kStride; base < n_end; base += kStride) {
+    const int g = base + pair * kGroupCols;
+    float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (valid) {
+      uint4 none[AdapterShape<R>::kPre];  // not read: PRE is false
+      expand_group<R, false>(Ba, vs, d_out, g, h, g < n_end, none, o);
+    }
+    if (g < n_end) store_group<MERGE>(o, g, h, t, d_out, partial, S, T, out);
+  }
+  if (valid) ptx::cluster_wait_acquire();
 }
 
-}  // namespace
-
-int adapter_cluster_size(int d_in, int d_out) {
-  const int m = d_in < d_out ? d_in : d_out;
-  if (m >= 2048) return 4;
-  if (m >= 512) return 2;
-  return 1;
-}
-
-cudaError_t launch_bgmv_adapter(const void* x, const void* A, const void* B, const int32_t* ids,
-                                const float* scale, float* delta, int T, int d_in, int d_out,
-                                int r, int n_slots, uint32_t* err, cudaStream_t st) {
+template <bool MERGE>
+cudaError_t launch_adapter_form(const void* x, const void* A, const void* B, const int32_t* ids,
+                                const float* scale, const float* partial, int S, void* out,
+                                int T, int d_in, int d_out, int r, int n_slots, uint32_t* err,
+                                bool pdl, cudaStream_t st) {
   if (T <= 0) return cudaSuccess;
   if (T > 65535) return cudaErrorInvalidValue;
   const int C = adapter_cluster_size(d_in, d_out);
@@ -176,20 +253,22 @@ cudaError_t launch_bgmv_adapter(const void* x, const void* A, const void* B, con
   cfg.blockDim = dim3(kAdThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = C;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 2 : 1;
   const bf16* xe = static_cast<const bf16*>(x);
   const bf16* Ae = static_cast<const bf16*>(A);
   const bf16* Be = static_cast<const bf16*>(B);
-#define LORA_ADAPTER_CASE(RR)                                                                   \
-  case RR:                                                                                      \
-    return cudaLaunchKernelEx(&cfg, bgmv_adapter_kernel<RR>, xe, Ae, Be, ids, scale, delta, T, \
-                              d_in, d_out, n_slots, kc, nc, err);
+#define LORA_ADAPTER_CASE(RR)                                                                  \
+  case RR:                                                                                     \
+    return cudaLaunchKernelEx(&cfg, bgmv_adapter_kernel<RR, MERGE>, xe, Ae, Be, ids, scale,   \
+                              partial, S, out, T, d_in, d_out, n_slots, kc, nc, err);
   switch (r) {
     LORA_ADAPTER_CASE(8)
     LORA_ADAPTER_CASE(16)
@@ -199,6 +278,35 @@ cudaError_t launch_bgmv_adapter(const void* x, const void* A, const void* B, con
     default: return cudaErrorInvalidValue;
   }
 #undef LORA_ADAPTER_CASE
+}
+
+}  // namespace
+
+int adapter_cluster_size(int d_in, int d_out) {
+  // at least 4 CTAs per token on wide layers (the shrink's A slice and the
+  // expand's B slice per CTA stay small), enough that each CTA keeps its
+  // columns in registers, at most the portable cluster size of 8
+  const int m = d_in < d_out ? d_in : d_out;
+  int C = m >= 2048 ? 4 : (m >= 512 ? 2 : 1);
+  const int by_cols = (d_out + kKeepGroups * kStride - 1) / (kKeepGroups * kStride);
+  if (C < by_cols) C = by_cols;
+  return C > 8 ? 8 : C;
+}
+
+cudaError_t launch_bgmv_adapter(const void* x, const void* A, const void* B, const int32_t* ids,
+                                const float* scale, float* delta, int T, int d_in, int d_out,
+                                int r, int n_slots, uint32_t* err, cudaStream_t st) {
+  return launch_adapter_form<false>(x, A, B, ids, scale, nullptr, 0, delta, T, d_in, d_out, r,
+                                    n_slots, err, false, st);
+}
+
+cudaError_t launch_bgmv_adapter_merge(const void* x, const void* A, const void* B,
+                                      const int32_t* ids, const float* scale,
+                                      const float* partial, int S, void* y, int T, int d_in,
+                                      int d_out, int r, int n_slots, uint32_t* err, bool pdl,
+                                      cudaStream_t st) {
+  return launch_adapter_form<true>(x, A, B, ids, scale, partial, S, y, T, d_in, d_out, r,
+                                   n_slots, err, pdl, st);
 }
 
 }  // namespace lora

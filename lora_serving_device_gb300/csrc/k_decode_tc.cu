@@ -1,27 +1,26 @@
-// The decode-sized base product (T <= 256 tokens) on tcgen05 tensor cores,
-// with the adapter term -- a ready fp32 [T, d_out] tensor written by the
-// BGMV expand running concurrently -- added in the epilogue so y is stored
-// once ("Multi-LoRA batching and adapter paging", section "Walking through a
-// batch": the base matrix is read once for the whole batch and each row gets
-// its own adapter term; "Serving multiple LoRAs ...": the expand is added
-// directly to the base output).
+// The decode-sized base product on tcgen05 tensor cores, split over d_in:
+//   partial[z, t, :] = x[t, K_z] W0[K_z, :]        z = 0 .. S-1
+// where K_0 .. K_{S-1} are contiguous ranges of d_in.  The kernel that runs
+// next in the decode chain (the BGMV adapter kernel) sums the S fp32
+// partials, adds the adapter term and stores y once ("Multi-LoRA batching
+// and adapter paging", section "Walking through a batch": the base matrix is
+// read once for the whole batch and each row gets its own adapter term).
 //
 // Shape: "swap AB".  The MMA's M = 128 d_out columns of W0 (A operand,
 // MN-major, W0 stays [d_in, d_out] row-major), N = the token tile (B operand
 // = x, K-major), so the skinny token dimension is the MMA's N.  Decode is
-// bound by streaming W0 from HBM; what matters is how many bytes each SM
-// keeps in flight, and that depends on the size of each TMA box rather than
-// on the depth of the ring.  So each pipeline stage carries KSUB 64-row K
-// blocks and W0 arrives as two 64-column x (64*KSUB)-row boxes per stage.
+// bound by streaming W0 from HBM, and each SM's share of it arrives at the
+// rate its bytes in flight allow: each pipeline stage carries KSUB 64-row K
+// blocks, W0 arrives as two 64-column x (64*KSUB)-row TMA boxes per stage,
+// and the ring takes all the shared memory there is.
 //
-// d_in is split over a thread-block cluster of S CTAs (S a power of two,
-// <= 8); rank z owns d_out rows [z*128/S, (z+1)*128/S) of the tile.  Each
-// CTA moves its fp32 partial tile from tensor memory into shared memory
-// (its own rows straight into slot z of its receive buffer, the others into
-// a staging area that reuses the drained pipeline ring), then sends each
-// owner its rows with one bulk shared-memory copy per peer, counted in bytes
-// on the owner's receive mbarrier.  The owner sums the S slots, adds the
-// adapter term and stores its rows of y.
+// The split is over CTAs, not clusters: each CTA writes its partial tile
+// from tensor memory straight to global memory (L2) and exits, so nothing
+// in it waits on another CTA.  It is launched as a programmatic dependent:
+// the producer fills the ring with W0 (which no earlier kernel of the layer
+// writes) before it waits for the predecessor grid, then loads x, which the
+// predecessor may have written.  So the W0 stream of this layer overlaps the
+// tail of the previous kernel.
 //
 // Warp roles: warp 0 = TMA producer, warp 1 = MMA issuer (and TMEM
 // allocator), warps 2-5 = epilogue.  Every on-chip wait is bounded in time;
@@ -36,16 +35,13 @@ namespace lora {
 namespace {
 
 constexpr int kThreads = 192;
-constexpr int kEpiThreads = 128;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 struct DecParams {
-  int T, d_in, d_out, n_slots;
-  int n_stage;  // K stages over d_in: ceil(d_in / (64 * KSUB))
-  int stages;   // ring depth
-  const int32_t* ids;
-  const float* delta;  // fp32 [T, d_out] adapter term, or null (base only)
-  bf16* y;
+  int T, d_in, d_out;
+  int n_blk;   // K blocks of 64*KSUB rows over d_in
+  int stages;  // ring depth
+  float* partial;  // [S, T, d_out] fp32
   uint32_t* err;
 };
 
@@ -55,14 +51,9 @@ struct DecLayout {
   static constexpr uint32_t kXBytes = KSUB * kXSub;
   static constexpr uint32_t kWBox = 64 * KSUB * 128;         // 64 columns x 64*KSUB rows
   static constexpr uint32_t kStage = kXBytes + 2 * kWBox;
-  static constexpr uint32_t kRb = 128 * BT * 4;              // receive buffer: S slots
-  // the fp32 partial tile is staged in the (drained) ring before it is sent
-  static_assert(kRb <= kStage, "staging must fit in one pipeline stage");
-  static __host__ __device__ uint32_t rb(int stages) { return stages * kStage; }
-  static __host__ __device__ uint32_t tok(int stages) { return rb(stages) + kRb; }
-  static __host__ __device__ uint32_t bars(int stages) { return tok(stages) + BT * 4; }
-  // full[stages], empty[stages], accum_full, rx_full
-  static __host__ __device__ uint32_t misc(int stages) { return bars(stages) + (2 * stages + 2) * 8; }
+  static __host__ __device__ uint32_t bars(int stages) { return stages * kStage; }
+  // full[stages], empty[stages], accum_full
+  static __host__ __device__ uint32_t misc(int stages) { return bars(stages) + (2 * stages + 1) * 8; }
   static __host__ __device__ uint32_t total(int stages) { return misc(stages) + 16; }
 };
 
@@ -90,25 +81,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  int* tok = reinterpret_cast<int*>(smem + Lay::tok(p.stages));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + Lay::bars(p.stages));
   uint64_t* empty = full + p.stages;
   uint64_t* accum_full = empty + p.stages;
-  uint64_t* rx_full = accum_full + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::misc(p.stages));
   volatile int* abort_f = reinterpret_cast<volatile int*>(smem + Lay::misc(p.stages) + 8);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n0 = blockIdx.x * 128, t0 = blockIdx.y * BT;
   const int S = static_cast<int>(gridDim.z), z = static_cast<int>(blockIdx.z);
-  const int rows_own = 128 / S;
-  const uint32_t slot_bytes = static_cast<uint32_t>(rows_own * BT * 4);
 
   // ---- prologue: warp 0 initialises the barriers and starts streaming;
   // the others wait for that (named barrier 2); warp 1 allocates TMEM and
-  // hands the address to the epilogue warps (named barrier 3).  Peers send
-  // into this CTA only after phase A of the cluster barrier, which every
-  // thread arrives at once the receive mbarrier is initialised.
+  // hands the address to the epilogue warps (named barrier 3)
   if (warp == 0) {
     if (lane == 0) {
       ptx::prefetch_tmap(&tm_w);
@@ -118,18 +103,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_init(&empty[i], 1);
       }
       ptx::mbar_init(accum_full, 1);
-      ptx::mbar_init(rx_full, 1);
       *abort_f = 0;
       ptx::fence_mbar_init();
-      // the S-1 peers' slots complete phase 0 of rx_full
-      if (S > 1) ptx::mbar_arrive_expect_tx(rx_full, static_cast<uint32_t>(S - 1) * slot_bytes);
     }
     __syncwarp();
-    if (S > 1) ptx::cluster_arrive_release();
     named_arrive(2, kThreads);
   } else {
     named_sync(2, kThreads);
-    if (S > 1) ptx::cluster_arrive_relaxed();
     if (warp == 1) {
       ptx::tmem_alloc(tmem_slot, kTmemCols);
       ptx::tmem_relinquish();
@@ -141,12 +121,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
   }
   const uint32_t tmem = warp == 0 ? 0u : *tmem_slot;
-  const int kb0 = static_cast<int>(static_cast<long long>(z) * p.n_stage / S);
-  const int kb1 = static_cast<int>(static_cast<long long>(z + 1) * p.n_stage / S);
+  const int kb0 = z * p.n_blk / S;
+  const int kb1 = (z + 1) * p.n_blk / S;
+  const int n_it = kb1 - kb0;
 
   if (warp == 0) {
     // ---------------- producer -------------------------------------------
-    for (int it = 0; it < kb1 - kb0; ++it) {
+    // W0 of the first ring's worth of stages goes out before the wait for
+    // the predecessor grid; x of those stages right after it
+    const int pre = n_it < p.stages ? n_it : p.stages;
+    if (lane == 0) {
+      for (int it = 0; it < pre; ++it) {
+        uint8_t* Wr = smem + static_cast<size_t>(it) * Lay::kStage + Lay::kXBytes;
+        const int k0 = (kb0 + it) * 64 * KSUB;
+        ptx::mbar_arrive_expect_tx(&full[it], Lay::kStage);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) ptx::tma_load_2d(Wr + h * Lay::kWBox, &tm_w, &full[it], n0 + 64 * h, k0);
+      }
+    }
+    // every CTA waits, so this grid completing implies its predecessors did
+    pdl_wait();
+    pdl_launch_dependents();  // x is ready: the next kernel of the chain may start
+    if (lane == 0) {
+      for (int it = 0; it < pre; ++it) {
+        uint8_t* X = smem + static_cast<size_t>(it) * Lay::kStage;
+        const int k0 = (kb0 + it) * 64 * KSUB;
+#pragma unroll
+        for (int j = 0; j < KSUB; ++j) ptx::tma_load_2d(X + j * Lay::kXSub, &tm_x, &full[it], k0 + 64 * j, t0);
+      }
+    }
+    __syncwarp();
+    for (int it = pre; it < n_it; ++it) {
       const int st = it % p.stages;
       const uint32_t ph = static_cast<uint32_t>(it / p.stages) & 1u;
       if (!warp_wait(&empty[st], ph ^ 1u, abort_f)) break;
@@ -165,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ---------------- MMA issuer -----------------------------------------
     if (lane == 0) {
-      for (int it = 0; it < kb1 - kb0; ++it) {
+      for (int it = 0; it < n_it; ++it) {
         const int st = it % p.stages;
         const uint32_t ph = static_cast<uint32_t>(it / p.stages) & 1u;
         if (!ptx::mbar_wait_bounded(&full[st], ph, abort_f, kWaitLimitNs)) break;
@@ -190,122 +195,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else {
-    // ---------------- epilogue warps -------------------------------------
-    const int etid = tid - 64;
-    bool bad = false;
-    for (int i = etid; i < BT; i += kEpiThreads) {
-      const int t = t0 + i;
-      int u = -1;
-      if (t < p.T) {
-        const int id = p.ids[t];
-        if (slot_valid(id, p.n_slots)) u = 0;
-        else if (id != -1) bad = true;
-      }
-      tok[i] = u;
-    }
-    if (bad && blockIdx.x == 0 && z == 0) flag_error(p.err, LORA_DEVERR_BAD_SLOT);
-    const bool acc_ok = warp_wait(accum_full, 0, abort_f);
-    if (acc_ok) {
+    // ---------------- epilogue warps: TMEM -> fp32 partial tile ----------
+    // TMEM lane = d_out column n of the tile, TMEM column = token; a warp
+    // stores 32 consecutive columns of one token row at a time (128 bytes)
+    if (warp_wait(accum_full, 0, abort_f) && n_it > 0) {
       ptx::tc_fence_after();
-      // TMEM lane = d_out row n of the tile, column = token.  Row n belongs
-      // to rank n / (128/S): this rank's own rows go to its receive slot z,
-      // the others to the staging area, rank-major so each peer's rows are
-      // one contiguous block.  Rows are BT fp32 (token-contiguous) and the
-      // 16-byte chunks of row n are XOR-swizzled by n & 7, so the 32 lanes'
-      // vector stores spread over all banks.
       const int q = warp & 3;
-      const int n = q * 32 + lane;
-      const int owner = n / rows_own, n_loc = n - owner * rows_own;
-      float* row = owner == z
-          ? reinterpret_cast<float*>(smem + Lay::rb(p.stages)) + (z * rows_own + n_loc) * BT
-          : reinterpret_cast<float*>(smem) + n * BT;
+      const int n = n0 + q * 32 + lane;
+      const int rows_tok = min(BT, p.T - t0);
+      float* out = p.partial + (static_cast<size_t>(z) * p.T + t0) * p.d_out + n;
       const uint32_t tq = tmem + (static_cast<uint32_t>(q * 32) << 16);
+      constexpr int kCols = BT < 64 ? BT : 64;  // TMEM loads in flight before one wait
 #pragma unroll 1
-      for (int c0 = 0; c0 < BT; c0 += 32) {
-        uint32_t v[32];
-        ptx::tmem_ld16(tq + c0, *reinterpret_cast<uint32_t(*)[16]>(v));
-        ptx::tmem_ld16(tq + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
-        ptx::tmem_ld_wait();
+      for (int c0 = 0; c0 < BT; c0 += kCols) {
+        uint32_t v[kCols];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int chunk = ((c0 >> 2) + j) ^ (n & 7);
-          *reinterpret_cast<float4*>(row + chunk * 4) =
-              make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                          __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+        for (int j = 0; j < kCols / 16; ++j)
+          ptx::tmem_ld16(tq + c0 + 16 * j, *reinterpret_cast<uint32_t(*)[16]>(v + 16 * j));
+        ptx::tmem_ld_wait();
+        if (n < p.d_out) {
+#pragma unroll
+          for (int j = 0; j < kCols; ++j)
+            if (c0 + j < rows_tok) out[static_cast<size_t>(c0 + j) * p.d_out] = __uint_as_float(v[j]);
         }
-      }
-      ptx::fence_proxy_async_smem();  // the bulk copies read the staging area
-    }
-    named_sync(1, kEpiThreads);
-    if (S > 1) {
-      ptx::cluster_wait_acquire();  // phase A: every peer's rx_full is initialised
-      if (acc_ok && etid < S && etid != z) {
-        const uint32_t src = ptx::smem_u32(smem) + static_cast<uint32_t>(etid) * slot_bytes;
-        const uint32_t dst_local = ptx::smem_u32(smem + Lay::rb(p.stages)) +
-                                   static_cast<uint32_t>(z) * slot_bytes;
-        ptx::bulk_copy_to_cluster(ptx::mapa_shared(dst_local, static_cast<uint32_t>(etid)), src,
-                                  slot_bytes,
-                                  ptx::mapa_shared(ptx::smem_u32(rx_full), static_cast<uint32_t>(etid)));
       }
     }
   }
 
-  // ---- reduction of the S slots of this rank's rows, store y -------------
-  if (S > 1 && warp < 2) ptx::cluster_wait_acquire();  // phase A (epilogue warps did it)
-  // this rank owns d_out rows [z * 128/S, (z+1) * 128/S) of the tile; the
-  // adapter-term loads (L2) are issued before the receive wait so they
-  // overlap it
-  const int groups = rows_own / 8;
-  const int rows_tok = min(BT, p.T - t0);
-  const int n_items = rows_tok * groups;
-  constexpr int kMaxItems = (BT * 16 + kThreads - 1) / kThreads;  // S = 1: 16 groups
-  float dl[kMaxItems][8];
-  // every CTA waits, so that this grid completing implies its predecessors
-  // completed; the adapter term is written by the kernel launched just before.
-  // Rows of base-only tokens are loaded too (they are in bounds) and dropped
-  // in the sum, so this does not wait for the token table.
-  pdl_wait();
-  if (p.delta != nullptr) {
-#pragma unroll
-    for (int u = 0; u < kMaxItems; ++u) {
-      const int e = tid + u * kThreads;
-      const int g = e / (rows_tok > 0 ? rows_tok : 1), t = e - g * rows_tok;
-      const int n = n0 + z * rows_own + g * 8;
-      if (e < n_items && n < p.d_out)
-        load8_dep(p.delta + static_cast<size_t>(t0 + t) * p.d_out + n, dl[u]);
-    }
-  }
-  __syncthreads();  // the token table and slot z, written by the epilogue warps
-  bool rx_ok = true;
-  if (S > 1) {
-    rx_ok = ptx::mbar_wait_bounded(rx_full, 0, abort_f, kWaitLimitNs);
-    __syncwarp();
-    // phase B: this CTA has received every peer's slot, so the peers'
-    // staging areas have been read; a CTA leaves only after phase B
-    ptx::cluster_arrive_relaxed();
-  }
-  if (rx_ok && !*abort_f) {
-    const float* rb = reinterpret_cast<const float*>(smem + Lay::rb(p.stages));
-#pragma unroll
-    for (int u = 0; u < kMaxItems; ++u) {
-      const int e = tid + u * kThreads;
-      if (e >= n_items) break;
-      const int g = e / rows_tok, t = e - g * rows_tok;
-      const int n = n0 + z * rows_own + g * 8;
-      if (n >= p.d_out) continue;
-      float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      for (int src = 0; src < S; ++src) {
-        const float* blk = rb + (src * rows_own + g * 8) * BT;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) f[j] += blk[j * BT + ((((t >> 2) ^ j) << 2) | (t & 3))];
-      }
-      if (p.delta != nullptr && tok[t] >= 0) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) f[j] += dl[u][j];
-      }
-      store8(p.y + static_cast<size_t>(t0 + t) * p.d_out + n, f);
-    }
-  }
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -313,16 +229,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tmem_dealloc(tmem, kTmemCols);
   }
   if (tid == 0 && *abort_f) flag_error(p.err, LORA_DEVERR_TIMEOUT);
-  if (S > 1) ptx::cluster_wait_acquire();  // phase B
 }
 
 template <int BT, int KSUB>
 cudaError_t launch_decode_variant(const CUtensorMap& tm_x, const CUtensorMap& tm_w,
-                                  DecParams prm, int tiles_n, int tiles_t, int S,
+                                  DecParams prm, int tiles_n, int tiles_t, int S, bool pdl,
                                   cudaStream_t st, const DeviceInfo& dev) {
   using Lay = DecLayout<BT, KSUB>;
   int stages = 0;
-  for (int s = 4; s >= 2; --s) {
+  for (int s = 6; s >= 2; --s) {
     if (Lay::total(s) + 1024 <= dev.max_smem_optin) {
       stages = s;
       break;
@@ -340,34 +255,50 @@ cudaError_t launch_decode_variant(const CUtensorMap& tm_x, const CUtensorMap& tm
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 1;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = S;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
+  cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kern, tm_x, tm_w, prm);
+}
+
+// token tile and K-block depth per decode batch size
+int decode_bt(int T) { return T <= 32 ? 32 : (T <= 64 ? 64 : 128); }
+int decode_ksub(int BT) { return BT <= 64 ? 3 : 2; }
+int decode_blocks(int T, int d_in) {
+  const int rows = 64 * decode_ksub(decode_bt(T > 0 ? T : 1));
+  return (d_in + rows - 1) / rows;
 }
 
 }  // namespace
 
-cudaError_t launch_decode_tc(const void* x, const void* W0, const int32_t* ids,
-                             const float* delta, void* y, int T, int d_in, int d_out, int n_slots,
-                             uint32_t* err, cudaStream_t st, const DeviceInfo& dev) {
-  // token tile: 32 / 64 / 128 tokens; above 128, 128-token tiles
-  const int BT = T <= 32 ? 32 : (T <= 64 ? 64 : 128);
-  const int ksub = BT <= 64 ? 4 : 2;
+int decode_gemm_split(int T, int d_in, int d_out) {
+  // one CTA per SM of a 152-SM part: (d_out/128 column tiles) x (token
+  // tiles) x S; at most one split per K block and LORA_MAX_KSPLIT splits
+  const int BT = decode_bt(T > 0 ? T : 1);
+  const int tiles = ((d_out + 127) / 128) * ((T + BT - 1) / BT);
+  int S = 152 / (tiles > 0 ? tiles : 1);
+  const int smax = decode_gemm_max_split(T, d_in);
+  if (S > smax) S = smax;
+  return S < 1 ? 1 : S;
+}
+
+int decode_gemm_max_split(int T, int d_in) {
+  const int n_blk = decode_blocks(T, d_in);
+  return n_blk < LORA_MAX_KSPLIT ? n_blk : LORA_MAX_KSPLIT;
+}
+
+cudaError_t launch_decode_gemm(const void* x, const void* W0, float* partial, int T, int d_in,
+                               int d_out, int S, uint32_t* err, bool pdl, cudaStream_t st,
+                               const DeviceInfo& dev) {
+  if (T <= 0) return cudaSuccess;
+  const int BT = decode_bt(T);
+  const int ksub = decode_ksub(BT);
   const int tiles_n = (d_out + 127) / 128;
   const int tiles_t = (T + BT - 1) / BT;
-  const int n_stage = (d_in + 64 * ksub - 1) / (64 * ksub);
-  int S = dev.num_sms / (tiles_n * tiles_t);
-  if (S > 8) S = 8;
-  if (S > n_stage) S = n_stage;
-  int S2 = 1;
-  while (S2 * 2 <= S) S2 *= 2;
+  const int n_blk = decode_blocks(T, d_in);
+  if (S < 1 || S > n_blk || tiles_t > 65535) return cudaErrorInvalidValue;
 
   CUtensorMap tm_x, tm_w;
   if (!encode_tensor_map_bf16(&tm_x, x, d_in, T, d_in, 64, BT) ||
@@ -377,16 +308,13 @@ cudaError_t launch_decode_tc(const void* x, const void* W0, const int32_t* ids,
   prm.T = T;
   prm.d_in = d_in;
   prm.d_out = d_out;
-  prm.n_slots = n_slots;
-  prm.n_stage = n_stage;
+  prm.n_blk = n_blk;
   prm.stages = 0;
-  prm.ids = ids;
-  prm.delta = delta;
-  prm.y = static_cast<bf16*>(y);
+  prm.partial = partial;
   prm.err = err;
-  if (BT == 32) return launch_decode_variant<32, 4>(tm_x, tm_w, prm, tiles_n, tiles_t, S2, st, dev);
-  if (BT == 64) return launch_decode_variant<64, 4>(tm_x, tm_w, prm, tiles_n, tiles_t, S2, st, dev);
-  return launch_decode_variant<128, 2>(tm_x, tm_w, prm, tiles_n, tiles_t, S2, st, dev);
+  if (BT == 32) return launch_decode_variant<32, 3>(tm_x, tm_w, prm, tiles_n, tiles_t, S, pdl, st, dev);
+  if (BT == 64) return launch_decode_variant<64, 3>(tm_x, tm_w, prm, tiles_n, tiles_t, S, pdl, st, dev);
+  return launch_decode_variant<128, 2>(tm_x, tm_w, prm, tiles_n, tiles_t, S, pdl, st, dev);
 }
 
 }  // namespace lora

@@ -770,9 +770,6 @@ cudaError_t launch_fused_tc(const void* x, const void* W0, const void* B, const 
     while (p2 * 2 <= S) p2 *= 2;
     return p2;
   };
-  // a ready adapter term on a decode-sized batch: the swap-AB decode kernel
-  if (delta != nullptr && T <= 256)
-    return launch_decode_tc(x, W0, ids, delta, y, T, d_in, d_out, n_slots, err, st, dev);
   const int tiles_n = (d_out + 255) / 256;
   const int tiles_t = (T + 127) / 128;
   const int S = pick_split(tiles_n * tiles_t);

@@ -38,13 +38,14 @@ struct FusedWs {
   int32_t* seg_off;
   int32_t* n_seg;
   float* vpart;
-  float* delta;  // fp32 [T, d_out] adapter term (decode-sized batches only)
+  float* partial;  // fp32 [S, T, d_out] split-K base product (decode-sized batches only)
   int ksplit;
+  int split;       // S of the decode GEMM
   size_t bytes;
 };
 
 // Workspace of lora_linear_fused: error word, segment arrays, shrink
-// partials, and for decode-sized batches the fp32 adapter term.
+// partials, and for decode-sized batches the split-K fp32 base product.
 FusedWs fused_ws_layout(void* ws, int32_t T, int32_t d_in, int32_t d_out, int32_t r,
                         int32_t n_slots) {
   FusedWs w;
@@ -66,7 +67,8 @@ FusedWs fused_ws_layout(void* ws, int32_t T, int32_t d_in, int32_t d_out, int32_
   o += static_cast<size_t>(w.ksplit) * T * r * 4;
   o = round_up(o, 256);
   const size_t o_d = o;
-  if (T <= kDecodeTokens) o += static_cast<size_t>(T) * d_out * 4;
+  w.split = T <= kDecodeTokens ? decode_gemm_split(T, d_in, d_out) : 0;
+  o += static_cast<size_t>(w.split) * T * d_out * 4;
   w.bytes = round_up(o, 256);
   w.err = reinterpret_cast<uint32_t*>(base);
   w.perm = reinterpret_cast<int32_t*>(base + o_perm);
@@ -74,7 +76,7 @@ FusedWs fused_ws_layout(void* ws, int32_t T, int32_t d_in, int32_t d_out, int32_
   w.seg_off = reinterpret_cast<int32_t*>(base + o_off);
   w.n_seg = reinterpret_cast<int32_t*>(base + o_nseg);
   w.vpart = reinterpret_cast<float*>(base + o_v);
-  w.delta = T <= kDecodeTokens ? reinterpret_cast<float*>(base + o_d) : nullptr;
+  w.partial = T <= kDecodeTokens ? reinterpret_cast<float*>(base + o_d) : nullptr;
   return w;
 }
 
@@ -282,16 +284,23 @@ lora_status_t lora_linear_fused(const void* x, const void* W0, const void* A_poo
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   const bool decode = T <= kDecodeTokens;
+  if (decode && dt == LORA_DTYPE_BF16) {
+    // decode-sized bf16 batch: the split-K base GEMM, then one kernel that
+    // computes the per-token (BGMV, no sort) adapter term while the GEMM
+    // streams W0 and, once the GEMM is done, sums its partials, adds the
+    // term and stores y.  Both are programmatic dependents: the GEMM
+    // streams W0 while the previous kernel in the stream finishes and reads
+    // x only after it has.
+    e = launch_decode_gemm(x, W0, w.partial, T, d_in, d_out, w.split, w.err, true, st, dev);
+    if (e != cudaSuccess) return LORA_ERR_CUDA;
+    return from_cuda(launch_bgmv_adapter_merge(x, A_pool, B_pool, slot_ids, scale, w.partial,
+                                               w.split, y, T, d_in, d_out, r, n_slots, w.err,
+                                               true, st));
+  }
   if (decode) {
-    // decode-sized batch: per-token gather (BGMV) -- no sort needed.  For
-    // bf16 one launch computes the whole adapter term into fp32 while the
-    // GEMM (its programmatic dependent) streams W0
-    if (dt == LORA_DTYPE_BF16)
-      e = launch_bgmv_adapter(x, A_pool, B_pool, slot_ids, scale, w.delta, T, d_in, d_out, r,
-                              n_slots, w.err, st);
-    else
-      e = launch_bgmv_shrink(x, A_pool, slot_ids, scale, w.vpart, T, d_in, r, n_slots, w.ksplit,
-                             dt, w.err, st);
+    // decode-sized fp32 batch: per-token BGMV shrink, then the CUDA-core layer
+    e = launch_bgmv_shrink(x, A_pool, slot_ids, scale, w.vpart, T, d_in, r, n_slots, w.ksplit,
+                           dt, w.err, st);
   } else {
     // prefill-sized batch: segments, then the segment-grouped shrink (SGMV)
     e = launch_build_segments(slot_ids, T, n_slots, w.perm, w.seg_slot, w.seg_off, w.n_seg,
@@ -302,8 +311,8 @@ lora_status_t lora_linear_fused(const void* x, const void* W0, const void* A_poo
   }
   if (e != cudaSuccess) return LORA_ERR_CUDA;
   if (dt == LORA_DTYPE_BF16)
-    e = launch_fused_tc(x, W0, B_pool, slot_ids, w.vpart, w.ksplit, decode ? w.delta : nullptr, y,
-                        T, d_in, d_out, r, n_slots, w.err, st, dev);
+    e = launch_fused_tc(x, W0, B_pool, slot_ids, w.vpart, w.ksplit, nullptr, y, T, d_in, d_out, r,
+                        n_slots, w.err, st, dev);
   else
     e = launch_fused_f32(static_cast<const float*>(x), static_cast<const float*>(W0),
                          static_cast<const float*>(B_pool), slot_ids, w.vpart, w.ksplit,
@@ -390,16 +399,16 @@ lora_status_t lora_bgmv_adapter(const void* x, const void* A_pool, const void* B
                                        static_cast<cudaStream_t>(stream)));
 }
 
-lora_status_t lora_base_gemm_delta(const void* x, const void* W0, const float* delta,
-                                   const int32_t* slot_ids, void* y, int32_t T, int32_t d_in,
-                                   int32_t d_out, int32_t n_slots, lora_dtype_t dt, void* ws,
-                                   size_t ws_bytes, void* stream) {
+lora_status_t lora_base_gemm_splitk(const void* x, const void* W0, float* partial, int32_t T,
+                                    int32_t d_in, int32_t d_out, int32_t ksplit, lora_dtype_t dt,
+                                    void* ws, size_t ws_bytes, void* stream) {
   if (T < 0) return LORA_ERR_INVALID_ARG;
   if (dt != LORA_DTYPE_BF16) return LORA_ERR_DTYPE;
-  if (!tokens_ok(T) || !dim_ok(d_in) || !dim_ok(d_out) || !slots_ok(n_slots))
+  if (!tokens_ok(T) || !dim_ok(d_in) || !dim_ok(d_out) || ksplit < 1 ||
+      ksplit > decode_gemm_max_split(T, d_in))
     return LORA_ERR_SHAPE;
-  if (x == nullptr || W0 == nullptr || delta == nullptr || slot_ids == nullptr || y == nullptr ||
-      !aligned16(x) || !aligned16(W0) || !aligned16(delta) || !aligned16(y) || x == y)
+  if (x == nullptr || W0 == nullptr || partial == nullptr || !aligned16(x) || !aligned16(W0) ||
+      !aligned16(partial))
     return LORA_ERR_INVALID_ARG;
   lora_status_t s = check_ws(ws, ws_bytes, kErrBytes);
   if (s != LORA_OK) return s;
@@ -407,9 +416,39 @@ lora_status_t lora_base_gemm_delta(const void* x, const void* W0, const float* d
   DeviceInfo dev;
   if ((s = check_device(&dev)) != LORA_OK) return s;
   if (!tensor_map_available()) return LORA_ERR_CUDA;
-  return from_cuda(launch_fused_tc(x, W0, nullptr, slot_ids, nullptr, 1, delta, y, T, d_in, d_out,
-                                   8, n_slots, static_cast<uint32_t*>(ws),
-                                   static_cast<cudaStream_t>(stream), dev));
+  return from_cuda(launch_decode_gemm(x, W0, partial, T, d_in, d_out, ksplit,
+                                      static_cast<uint32_t*>(ws), false,
+                                      static_cast<cudaStream_t>(stream), dev));
+}
+
+lora_status_t lora_bgmv_adapter_merge(const void* x, const void* A_pool, const void* B_pool,
+                                      const int32_t* slot_ids, const float* scale,
+                                      const float* partial, int32_t ksplit, void* y, int32_t T,
+                                      int32_t d_in, int32_t d_out, int32_t r, int32_t n_slots,
+                                      lora_dtype_t dt, void* ws, size_t ws_bytes, void* stream) {
+  if (T < 0) return LORA_ERR_INVALID_ARG;
+  if (dt != LORA_DTYPE_BF16) return LORA_ERR_DTYPE;
+  if (!tokens_ok(T) || T > 65535 || !dim_ok(d_in) || !dim_ok(d_out) || !rank_ok(r) ||
+      !slots_ok(n_slots) || ksplit < 1 || ksplit > LORA_MAX_KSPLIT)
+    return LORA_ERR_SHAPE;
+  if (x == nullptr || A_pool == nullptr || B_pool == nullptr || slot_ids == nullptr ||
+      partial == nullptr || y == nullptr || !aligned16(x) || !aligned16(A_pool) ||
+      !aligned16(B_pool) || !aligned16(partial) || !aligned16(y) || x == y)
+    return LORA_ERR_INVALID_ARG;
+  lora_status_t s = check_ws(ws, ws_bytes, kErrBytes);
+  if (s != LORA_OK) return s;
+  if (T == 0) return LORA_OK;
+  DeviceInfo dev;
+  if ((s = check_device(&dev)) != LORA_OK) return s;
+  return from_cuda(launch_bgmv_adapter_merge(x, A_pool, B_pool, slot_ids, scale, partial, ksplit,
+                                             y, T, d_in, d_out, r, n_slots,
+                                             static_cast<uint32_t*>(ws), false,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
+int32_t lora_decode_split(int32_t T, int32_t d_in, int32_t d_out) {
+  if (T < 1 || T > kDecodeTokens || !dim_ok(d_in) || !dim_ok(d_out)) return 0;
+  return decode_gemm_split(T, d_in, d_out);
 }
 
 lora_status_t lora_get_error(void* ws, void* stream, int32_t* device_err) {

@@ -27,7 +27,7 @@ NOALLOC_SCRATCH_BYTES = 8 << 20
 EXPORTS = ("lora_workspace_bytes", "lora_build_segments", "lora_bgmv_shrink", "lora_bgmv_expand",
            "lora_sgmv_shrink", "lora_sgmv_expand", "lora_linear_fused", "lora_base_gemm_expand",
            "lora_linear_fused_noalloc", "lora_bgmv_delta", "lora_bgmv_adapter",
-           "lora_base_gemm_delta",
+           "lora_bgmv_adapter_merge", "lora_base_gemm_splitk", "lora_decode_split",
            "lora_get_error", "lora_status_string")
 
 
@@ -54,7 +54,10 @@ _SIGS = {
     "lora_linear_fused_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "lora_bgmv_delta": (_I, [_P, _I, _P, _P, _P, _I, _I, _I, _I, _I, _P, _Z, _P]),
     "lora_bgmv_adapter": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _Z, _P]),
-    "lora_base_gemm_delta": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _Z, _P]),
+    "lora_bgmv_adapter_merge": (_I, [_P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P,
+                                     _Z, _P]),
+    "lora_base_gemm_splitk": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _Z, _P]),
+    "lora_decode_split": (_I, [_I, _I, _I]),
     "lora_get_error": (_I, [_P, _P, ctypes.POINTER(ctypes.c_int32)]),
     "lora_status_string": (ctypes.c_char_p, [_I]),
 }
@@ -144,10 +147,19 @@ def lora_bgmv_adapter(x, A_pool, B_pool, slot_ids, scale, delta, T, d_in, d_out,
                  n_slots, dt, ws, ws_bytes, stream)
 
 
-def lora_base_gemm_delta(x, W0, delta, slot_ids, y, T, d_in, d_out, n_slots, dt, ws, ws_bytes,
-                         stream):
-    return _call("lora_base_gemm_delta", x, W0, delta, slot_ids, y, T, d_in, d_out, n_slots, dt,
-                 ws, ws_bytes, stream)
+def lora_bgmv_adapter_merge(x, A_pool, B_pool, slot_ids, scale, partial, ksplit, y, T, d_in,
+                            d_out, r, n_slots, dt, ws, ws_bytes, stream):
+    return _call("lora_bgmv_adapter_merge", x, A_pool, B_pool, slot_ids, scale, partial, ksplit, y,
+                 T, d_in, d_out, r, n_slots, dt, ws, ws_bytes, stream)
+
+
+def lora_base_gemm_splitk(x, W0, partial, T, d_in, d_out, ksplit, dt, ws, ws_bytes, stream):
+    return _call("lora_base_gemm_splitk", x, W0, partial, T, d_in, d_out, ksplit, dt, ws, ws_bytes,
+                 stream)
+
+
+def lora_decode_split(T, d_in, d_out):
+    return _call("lora_decode_split", T, d_in, d_out)
 
 
 def lora_get_error(ws, stream):
@@ -307,16 +319,34 @@ def bgmv_adapter_t(x, A_pool, B_pool, slot_ids, scale, ws, delta=None, stream=No
     return delta
 
 
-def base_gemm_delta_t(x, W0, delta, slot_ids, n_slots, ws, y=None, stream=None):
-    """y = x W0 + delta (rows of tokens with a valid id), overwriting y."""
+def base_gemm_splitk_t(x, W0, ws, ksplit=None, partial=None, stream=None):
+    """fp32 split-K base product partial[s] = x[:, K_s] W0[K_s, :]; ksplit defaults to the
+    one the fused layer uses."""
     import torch
     T, d_in = x.shape
     d_out = W0.shape[1]
+    if ksplit is None:
+        ksplit = lora_decode_split(T, d_in, d_out) or 1
+    if partial is None:
+        partial = torch.empty((ksplit, T, d_out), dtype=torch.float32, device=x.device)
+    check(lora_base_gemm_splitk(_ptr(x), _ptr(W0), _ptr(partial), T, d_in, d_out, ksplit, _dt(x),
+                                _ptr(ws), ws.numel(), _stream(stream)),
+          "lora_base_gemm_splitk")
+    return partial
+
+
+def bgmv_adapter_merge_t(x, A_pool, B_pool, slot_ids, scale, partial, ws, y=None, stream=None):
+    """y = sum_s partial[s] + s_a (x A_a) B_a, overwriting every row of y."""
+    import torch
+    T, d_in = x.shape
+    n_slots, r, d_out = B_pool.shape
     if y is None:
         y = torch.empty((T, d_out), dtype=x.dtype, device=x.device)
-    check(lora_base_gemm_delta(_ptr(x), _ptr(W0), _ptr(delta), _ptr(slot_ids), _ptr(y), T, d_in,
-                               d_out, n_slots, _dt(x), _ptr(ws), ws.numel(), _stream(stream)),
-          "lora_base_gemm_delta")
+    check(lora_bgmv_adapter_merge(_ptr(x), _ptr(A_pool), _ptr(B_pool), _ptr(slot_ids),
+                                  _ptr(scale), _ptr(partial), partial.shape[0], _ptr(y), T, d_in,
+                                  d_out, r, n_slots, _dt(x), _ptr(ws), ws.numel(),
+                                  _stream(stream)),
+          "lora_bgmv_adapter_merge")
     return y
 
 

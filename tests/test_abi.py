@@ -28,7 +28,8 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ("lora_build_segments", "lora_bgmv_shrink", "lora_bgmv_expand", "lora_sgmv_shrink",
               "lora_sgmv_expand", "lora_linear_fused", "lora_base_gemm_expand",
-              "lora_bgmv_delta", "lora_base_gemm_delta",
+              "lora_bgmv_delta", "lora_bgmv_adapter", "lora_bgmv_adapter_merge",
+              "lora_base_gemm_splitk", "lora_decode_split",
               "lora_workspace_bytes", "lora_get_error",
               "lora_status_string"):
         assert n in names
@@ -94,6 +95,27 @@ def test_validation_paths(L):
     assert L.lora_build_segments(FAKE, -2, 4, FAKE, FAKE, FAKE, FAKE, ws, 16, None) == 1
     st, _ = L.lora_get_error(None, None)
     assert st == 1
+    # decode building blocks: bf16 only, ksplit within the d_in blocks
+    assert L.lora_base_gemm_splitk(FAKE, FAKE, FAKE, 4, 4096, 4096, 1, L.DTYPE_F32, ws, 16,
+                                   None) == 3
+    assert L.lora_base_gemm_splitk(FAKE, FAKE, FAKE, 4, 4096, 4096, 0, 0, ws, 16, None) == 2
+    assert L.lora_base_gemm_splitk(FAKE, FAKE, FAKE, 4, 128, 4096, 2, 0, ws, 16, None) == 2
+    assert L.lora_base_gemm_splitk(FAKE, FAKE, None, 4, 4096, 4096, 2, 0, ws, 16, None) == 1
+    assert L.lora_bgmv_adapter(FAKE, FAKE, FAKE, FAKE, None, FAKE, 70000, 64, 64, 16, 4, 0, ws,
+                               16, None) == 2
+    assert L.lora_bgmv_adapter_merge(FAKE, FAKE, FAKE, FAKE, None, FAKE, 2, FAKE, 4, 64, 64, 16,
+                                     4, 0, ws, 16, None) == 1        # x and y alias
+    assert L.lora_bgmv_adapter_merge(FAKE, FAKE, FAKE, FAKE, None, FAKE, 65, FAKE + 4096, 4, 64,
+                                     64, 16, 4, 0, ws, 16, None) == 2
+
+
+def test_decode_split_is_a_function_of_the_shapes(L):
+    assert L.lora_decode_split(64, 4096, 4096) == 4       # 32 column tiles x 4 = 128 CTAs
+    assert L.lora_decode_split(256, 4096, 4096) == 2      # 2 token tiles
+    assert L.lora_decode_split(1, 64, 128) == 1           # one K block
+    assert L.lora_decode_split(0, 4096, 4096) == 0
+    assert L.lora_decode_split(257, 4096, 4096) == 0
+    assert L.lora_decode_split(64, 60, 4096) == 0
 
 
 def test_empty_batch_is_a_no_op(L):

@@ -22,7 +22,7 @@ def test_layer_bytes_decode():
     # distinct adapters of the decode workload
     b = bench.layer_bytes(64, 4096, 4096, 16, 30.5)
     assert abs(b / 2 ** 20 - 40.6) < 0.2
-    g = bench.gemm_bytes(64, 4096, 4096, 56)
+    g = bench.gemm_bytes(64, 4096, 4096)
     assert g < b and g > 32 * 2 ** 20
 
 
@@ -37,8 +37,10 @@ def test_fused_ksplit_matches_library():
         head = -(-head // 256) * 256
         d_out = 1024
         body = -(-(head + ks * T * r * 4) // 256) * 256
-        if T <= 256:                       # decode-sized: fp32 adapter term [T, d_out]
-            body += T * d_out * 4
+        if T <= 256:                       # decode-sized: split-K fp32 base product
+            S = L.lora_decode_split(T, d_in, d_out)
+            assert S >= 1
+            body += S * T * d_out * 4
         want = -(-body // 256) * 256
         assert L.lora_workspace_bytes(L.OP_LINEAR_FUSED, T, d_in, d_out, r, n_slots) == want
 

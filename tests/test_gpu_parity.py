@@ -396,20 +396,50 @@ def test_bgmv_adapter_matches_oracle(L, case):
     assert torch.equal(delta, delta2)
 
 
-@pytest.mark.parametrize("case", BLOCK_CASES, ids=[str(c) for c in BLOCK_CASES])
-def test_base_gemm_delta_matches_oracle(L, case):
+SPLITK_CASES = [(1, 64, 128, 1), (5, 200, 136, 2), (40, 1000, 264, 3), (64, 4096, 4096, 4),
+                (64, 4096, 4096, 21), (100, 512, 520, 4), (256, 4096, 4096, 2), (300, 256, 512, 2)]
+
+
+@pytest.mark.parametrize("case", SPLITK_CASES, ids=[str(c) for c in SPLITK_CASES])
+def test_base_gemm_splitk_matches_oracle(L, case):
+    """The split-K tensor-core base product: the S fp32 partials must add up
+    to x W0.  Nothing is rounded to bf16 on this path (bf16 inputs, fp32
+    products and sums), so the bar is the fp32 accumulation error of a
+    d_in-long dot product.  Every partial is written (no stale values)."""
     torch = torch_mod()
-    T, d_in, d_out, r, n_slots = case
-    w = W.random_case(710 + T, T, d_in, d_out, r, n_slots, invalid=1)
+    T, d_in, d_out, S = case
+    w = W.random_case(710 + T + S, T, d_in, d_out, 8, 2)
     d = DeviceCase(w)
     ws = _ws(L)
-    delta = (np.random.default_rng([7002, T]).standard_normal((T, d_out)) * 0.2).astype(np.float32)
-    y = L.base_gemm_delta_t(d.x, d.W0, dev(delta, "f32"), d.ids, n_slots, ws)
+    partial = torch.full((S, T, d_out), float("nan"), dtype=torch.float32, device="cuda")
+    L.base_gemm_splitk_t(d.x, d.W0, ws, ksplit=S, partial=partial)
     torch.cuda.synchronize()
-    base = O.lora_linear(w.x, w.W0, w.A_pool, w.B_pool, w.scale, np.full(T, -1))
-    valid = (w.slot_ids >= 0) & (w.slot_ids < n_slots)
-    ref = base + np.where(valid[:, None], delta.astype(np.float64), 0.0)
-    check_close_bf16_out(host(y), ref, "base GEMM + delta")
+    got = host(partial)
+    assert np.all(np.isfinite(got))
+    ref = O.lora_linear(w.x, w.W0, w.A_pool, w.B_pool, w.scale, np.full(T, -1))
+    check_close(got.astype(np.float64).sum(axis=0), ref, "sum of split-K partials",
+                rel_fro=2e-5, max_rms=2e-4)
+    if S > 1 and d_in >= 1024:      # the splits really are partial sums over d_in
+        assert not np.allclose(got[0], ref, rtol=1e-2, atol=1e-2)
+
+
+@pytest.mark.parametrize("case", BLOCK_CASES, ids=[str(c) for c in BLOCK_CASES])
+def test_bgmv_adapter_merge_matches_oracle(L, case):
+    """y = (sum of given fp32 partials) + adapter term, every row written,
+    one bf16 rounding; base-only and invalid ids get the partials only."""
+    torch = torch_mod()
+    T, d_in, d_out, r, n_slots = case
+    w = W.random_case(740 + T, T, d_in, d_out, r, n_slots, invalid=1)
+    d = DeviceCase(w)
+    ws = _ws(L)
+    S = 3
+    part = (np.random.default_rng([7003, T]).standard_normal((S, T, d_out)) * 0.3).astype(np.float32)
+    y = torch.full((T, d_out), float("nan"), dtype=torch.bfloat16, device="cuda")
+    L.bgmv_adapter_merge_t(d.x, d.A, d.B, d.ids, d.scale, dev(part, "f32"), ws, y=y)
+    torch.cuda.synchronize()
+    ref = part.astype(np.float64).sum(axis=0) + O.expand(
+        O.shrink(w.x, w.A_pool, w.scale, w.slot_ids), w.B_pool, w.slot_ids)
+    check_close_bf16_out(host(y), ref, "partials + adapter term")
     assert L.get_error_t(ws) & L.DEVERR_BAD_SLOT
 
 
