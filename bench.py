@@ -15,8 +15,9 @@ Reported on one JSON line (rank 0):
   e2e       the same metric through the public call with host buffers: each
             step copies x and the ids from pinned memory, runs the layer and
             copies y back
-  roofline  the dominant kernel (the base GEMM), timed with CUDA events
-            around each of its launches, against the measured HBM copy peak
+  roofline  the dominant kernel (the split-K base GEMM): its mean launch
+            duration over back-to-back launches timed with CUDA events,
+            against the measured HBM copy peak
   sweep     tokens/s and achieved GB/s over distinct adapters per batch
             (4096->4096, rank 16, 1024-slot pool; T = 32 and 256)
   configs   the prefill workload (and the 8B-shaped stack with --stack)
@@ -285,6 +286,39 @@ def capture(fn, n_steps, stream):
     return g
 
 
+def graph_mean_ms(fn, n_steps, stream):
+    """Mean ms per call of fn(i): n_steps calls replayed back to back from one
+    CUDA graph (after an eager warm-up and a warm replay), CUDA events on the
+    launching stream around the replay."""
+    import torch
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            fn(i)
+    stream.synchronize()
+    g = capture(fn, n_steps, stream)
+    with torch.cuda.stream(stream):
+        g.replay()
+    stream.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        g.replay()
+    e1.record(stream)
+    stream.synchronize()
+    return e0.elapsed_time(e1) / n_steps
+
+
+def block_row(ms, nbytes, pk):
+    """One standalone kernel against the HBM roofline of its algorithmic bytes;
+    points whose roofline time is under 5 us are launch/ramp floored."""
+    us = ms * 1e3
+    roof_us = nbytes / (pk["hbm_gbs"] * 1e9) * 1e6
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"us": us, "gbs": gbs, "frac": gbs / pk["hbm_gbs"], "algorithmic_bytes": nbytes,
+            "roofline_us": roof_us, "latency_floored": roof_us < 5.0}
+
+
 def timed_graph_steps(fn, K, W, stream):
     """Run W warm-up steps then time exactly K steps of `fn(i)` from CUDA
     graphs; returns (elapsed ms of the K steps, launches per replay)."""
@@ -325,47 +359,68 @@ def timed_graph_steps(fn, K, W, stream):
 
 
 def per_kernel_times(sets, L, T, d_in, d_out, r, n_slots, n_steps, stream):
-    """Each step as the two public calls the fused decode path is made of,
-    with CUDA events recorded around each kernel inside one captured graph:
-    the split-K base GEMM (the dominant kernel) and the kernel that computes
-    the BGMV adapter term, adds the GEMM's partials and stores y.  The events
-    between the calls keep each kernel from starting early, so these times
-    include the start-up that the fused chain overlaps.  Returns the mean ms
-    per kernel."""
+    """Mean launch duration of each kernel of the fused decode path, each
+    launched on its own through its public call: n_steps back-to-back
+    launches replayed from one CUDA graph, CUDA events on the launching
+    stream around the replay, rotating buffer sets.  The kernels are the
+    split-K base GEMM (the dominant one) and the kernel that computes the
+    BGMV adapter term, adds the GEMM's partials and stores y.  Launched on
+    their own they do not overlap, so each mean includes the start-up and
+    tail that the fused chain hides."""
     import torch
     dev = sets[0].x.device
     S = L.lora_decode_split(T, d_in, d_out)
-    partial = torch.empty((S, T, d_out), dtype=torch.float32, device=dev)
+    partial = torch.zeros((S, T, d_out), dtype=torch.float32, device=dev)
     ws = torch.zeros(256, dtype=torch.uint8, device=dev)
-    try:
-        evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(3)]
-               for _ in range(n_steps)]
-    except TypeError:
-        return None
 
-    def step(i, rec=True):
+    def gemm(i):
         s = sets[i % len(sets)]
-        if rec:
-            evs[i][0].record(stream)
         L.base_gemm_splitk_t(s.x, s.W0, ws, ksplit=S, partial=partial, stream=stream)
-        if rec:
-            evs[i][1].record(stream)
-        L.bgmv_adapter_merge_t(s.x, s.A, s.B, s.ids, s.scale, partial, ws, y=s.y, stream=stream)
-        if rec:
-            evs[i][2].record(stream)
 
-    with torch.cuda.stream(stream):
-        for i in range(3):
-            step(i, rec=False)
-    stream.synchronize()
-    g = capture(step, n_steps, stream)
-    with torch.cuda.stream(stream):
-        g.replay()
-    stream.synchronize()
-    gem = [evs[i][0].elapsed_time(evs[i][1]) for i in range(n_steps)]
-    mrg = [evs[i][1].elapsed_time(evs[i][2]) for i in range(n_steps)]
-    return {"gemm_ms": statistics.mean(gem), "gemm_ms_median": statistics.median(gem),
-            "adapter_merge_ms": statistics.mean(mrg), "split": S, "n": n_steps}
+    def merge(i):
+        s = sets[i % len(sets)]
+        L.bgmv_adapter_merge_t(s.x, s.A, s.B, s.ids, s.scale, partial, ws, y=s.y, stream=stream)
+
+    out = {"split": S, "n": n_steps}
+    for name, fn in (("gemm_ms", gemm), ("adapter_merge_ms", merge)):
+        out[name] = graph_mean_ms(fn, n_steps, stream)
+    return out
+
+
+def decode_blocks(sets, L, w, stream, pk, n_steps=400):
+    """The scope table's a2 / a3 rows on their own, on the decode workload
+    (rotating buffer sets): BGMV shrink, BGMV expand (accumulating into y),
+    and the one-launch adapter term (shrink + cluster sum + expand, fp32 out).
+    Algorithmic bytes: each distinct adapter's A or B once, x or v, y."""
+    import numpy as np
+    import torch
+    T, d_in, d_out, r, n_slots, D = w.T, w.d_in, w.d_out, w.r, w.n_slots, w.distinct
+    T_lora = int(((w.slot_ids >= 0) & (w.slot_ids < n_slots)).sum())
+    dev = sets[0].x.device
+    ks = fused_ksplit(T, d_in, n_slots)
+    vpart = torch.zeros((ks, T, r), dtype=torch.float32, device=dev)
+    delta = torch.zeros((T, d_out), dtype=torch.float32, device=dev)
+    ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+
+    def shrink(i):
+        s = sets[i % len(sets)]
+        L.bgmv_shrink_t(s.x, s.A, s.ids, s.scale, ks, ws, v_partial=vpart, stream=stream)
+
+    def expand(i):
+        s = sets[i % len(sets)]
+        L.bgmv_expand_t(vpart, s.B, s.ids, s.y, ws, stream=stream)
+
+    def adapter(i):
+        s = sets[i % len(sets)]
+        L.bgmv_adapter_t(s.x, s.A, s.B, s.ids, s.scale, ws, delta=delta, stream=stream)
+
+    b_shrink = D * d_in * r * 2 + T * d_in * 2 + ks * T * r * 4
+    b_expand = D * r * d_out * 2 + ks * T * r * 4 + 2 * T * d_out * 2
+    b_adapter = D * r * (d_in + d_out) * 2 + T * d_in * 2 + T_lora * d_out * 4
+    return {"workload": "decode_bgmv", "ksplit": ks,
+            "bgmv_shrink": block_row(graph_mean_ms(shrink, n_steps, stream), b_shrink, pk),
+            "bgmv_expand": block_row(graph_mean_ms(expand, n_steps, stream), b_expand, pk),
+            "bgmv_adapter": block_row(graph_mean_ms(adapter, n_steps, stream), b_adapter, pk)}
 
 
 def e2e_steps(s0, L, T, d_in, d_out, r, n_slots, n_steps, stream):
@@ -493,12 +548,31 @@ def prefill_point(L, stream, pk, dev, steps=30, warm=5):
     flops = 2.0 * T * d_in * d_out + 2.0 * T * r * (d_in + d_out)
     nbytes = layer_bytes(T, d_in, d_out, r, D)
     tf = flops / t / 1e12
+    # the scope table's a1 / a2 / a3 rows on their own on this workload
+    ks = fused_ksplit(T, d_in, n_slots)
+    wss = torch.zeros(256, dtype=torch.uint8, device=dev)
+    segs = L.build_segments_t(ids, n_slots, wss, stream=stream)
+    vpart = torch.zeros((ks, T, r), dtype=torch.float32, device=dev)
+    b_seg = 4 * T + 4 * T + 8 * D + 8
+    b_shrink = D * d_in * r * 2 + T * d_in * 2 + ks * T * r * 4
+    b_expand = D * r * d_out * 2 + ks * T * r * 4 + 2 * T * d_out * 2
+    blocks = {
+        "ksplit": ks,
+        "build_segments": block_row(graph_mean_ms(
+            lambda i: L.build_segments_t(ids, n_slots, wss, stream=stream), 50, stream), b_seg, pk),
+        "sgmv_shrink": block_row(graph_mean_ms(
+            lambda i: L.sgmv_shrink_t(x, A, segs, scale, ks, wss, v_partial=vpart, stream=stream),
+            30, stream), b_shrink, pk),
+        "sgmv_expand": block_row(graph_mean_ms(
+            lambda i: L.sgmv_expand_t(vpart, B, segs, y, wss, stream=stream), 30, stream),
+            b_expand, pk)}
     res = {"workload": "prefill_sgmv: 4096->14336, rank 64, 64 slots, 16 prefill requests "
                        "(U[64,1024] tokens) + 48 decode tokens",
            "T": T, "distinct": D, "ms_per_step": t * 1e3, "tokens_per_s": T / t,
            "tflops": tf, "gbs": nbytes / t / 1e9,
            "roofline": {"bound": "tensor", "achieved": tf, "peak": pk["bf16_tflops_sustained"],
-                        "unit": "TFLOP/s", "frac": tf / pk["bf16_tflops_sustained"]}}
+                        "unit": "TFLOP/s", "frac": tf / pk["bf16_tflops_sustained"]},
+           "blocks": blocks}
     del x, W0, A, B
     torch.cuda.empty_cache()
     return res
@@ -584,9 +658,10 @@ def run_ours(args):
 
     try:
         kt = per_kernel_times(sets, L, T, d_in, d_out, r, n_slots, 400, stream)
-    except RuntimeError as e:   # timing events inside a captured graph unsupported
+        blocks = decode_blocks(sets, L, w, stream, pk)
+    except RuntimeError as e:
         print(f"per-kernel timing unavailable: {e}", file=sys.stderr)
-        kt = None
+        kt, blocks = None, None
     e2e_ms, h2d, d2h = e2e_steps(s0, L, T, d_in, d_out, r, n_slots, 2000, stream)
     e2e_ms = reduce_max(e2e_ms, device=dev)
     if rank != 0:
@@ -619,7 +694,7 @@ def run_ours(args):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms / 2000},
         "roofline": roof,
-        "kernels_ms": kt,
+        "kernels_ms": kt, "blocks": blocks,
         "clocks": clk.summary(),
     }
     if not args.no_sweep:

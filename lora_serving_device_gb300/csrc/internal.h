@@ -52,22 +52,20 @@ int fused_shrink_ksplit(int T, int d_in, int n_slots, int num_sms);
 int decode_shrink_ksplit(int T, int d_in);
 
 // Base GEMM + expand-in-accumulator kernel, bf16 (tcgen05), see k_fused_tc.cu.
-// `delta` (may be null): a ready fp32 [T, d_out] adapter term written by the
-// kernel launched just before; then B / vpart are not read.
 cudaError_t launch_fused_tc(const void* x, const void* W0, const void* B, const int32_t* ids,
-                            const float* vpart, int v_ksplit, const float* delta, void* y, int T,
+                            const float* vpart, int v_ksplit, void* y, int T,
                             int d_in, int d_out, int r, int n_slots, uint32_t* err,
                             cudaStream_t st, const DeviceInfo& dev);
 // The whole BGMV adapter term of a decode-sized bf16 batch in one launch
 // (shrink, cluster sum of the rank-r partials, expand), see k_adapter.cu.
-// One cluster of adapter_cluster_size(d_in, d_out) CTAs per token.
+// One cluster of adapter_cluster_size(T, d_in, d_out) CTAs per token.
 //  - launch_bgmv_adapter: fp32 into delta [T, d_out]; rows of base-only
 //    tokens are not written.
 //  - launch_bgmv_adapter_merge: y = sum of the S fp32 partials [S, T, d_out]
 //    of the decode GEMM + the adapter term, bf16, every row written.  `pdl`:
 //    launch as a programmatic dependent of that GEMM (it waits for it before
 //    reading the partials).
-int adapter_cluster_size(int d_in, int d_out);
+int adapter_cluster_size(int T, int d_in, int d_out);
 cudaError_t launch_bgmv_adapter(const void* x, const void* A, const void* B, const int32_t* ids,
                                 const float* scale, float* delta, int T, int d_in, int d_out,
                                 int r, int n_slots, uint32_t* err, cudaStream_t st);
@@ -94,6 +92,10 @@ bool tensor_map_available();
 // outside the tensor read as zero.
 bool encode_tensor_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
                             uint64_t row_elems, uint32_t box_inner, uint32_t box_outer);
+// 3-D fp32 tensor map without swizzle: dims d0 (contiguous) x d1 x d2,
+// box box0 x box1 x 1; elements outside the tensor are not stored.
+bool encode_tensor_map_f32_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1,
+                              uint64_t d2, uint32_t box0, uint32_t box1);
 // Decode-sized base GEMM split over d_in into S fp32 partials
 // partial[z, t, :] = x[t, K_z] W0[K_z, :], see k_decode_tc.cu.  `pdl`: launch
 // as a programmatic dependent (W0 is prefetched before the wait, x after).

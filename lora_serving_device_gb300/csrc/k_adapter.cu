@@ -245,7 +245,7 @@ cudaError_t launch_adapter_form(const void* x, const void* A, const void* B, con
                                 bool pdl, cudaStream_t st) {
   if (T <= 0) return cudaSuccess;
   if (T > 65535) return cudaErrorInvalidValue;
-  const int C = adapter_cluster_size(d_in, d_out);
+  const int C = adapter_cluster_size(T, d_in, d_out);
   const int kc = ((d_in + 8 * C - 1) / (8 * C)) * 8;
   const int nc = ((d_out + 8 * C - 1) / (8 * C)) * 8;
   cudaLaunchConfig_t cfg = {};
@@ -282,12 +282,16 @@ cudaError_t launch_adapter_form(const void* x, const void* A, const void* B, con
 
 }  // namespace
 
-int adapter_cluster_size(int d_in, int d_out) {
-  // at least 4 CTAs per token on wide layers (the shrink's A slice and the
-  // expand's B slice per CTA stay small), enough that each CTA keeps its
-  // columns in registers, at most the portable cluster size of 8
+int adapter_cluster_size(int T, int d_in, int d_out) {
+  // up to 4 CTAs per token on wide layers (the shrink's A slice and the
+  // expand's B slice per CTA stay small) while the grid stays within ~256
+  // CTAs, so all of them fit on the GPU beside the decode GEMM; at least
+  // enough that each CTA keeps its columns in registers; at most the
+  // portable cluster size of 8
   const int m = d_in < d_out ? d_in : d_out;
   int C = m >= 2048 ? 4 : (m >= 512 ? 2 : 1);
+  const int cap = T > 0 && T < 256 ? 256 / T : 1;
+  if (C > cap) C = cap;
   const int by_cols = (d_out + kKeepGroups * kStride - 1) / (kKeepGroups * kStride);
   if (C < by_cols) C = by_cols;
   return C > 8 ? 8 : C;

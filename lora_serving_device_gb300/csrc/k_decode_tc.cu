@@ -14,13 +14,13 @@
 // blocks, W0 arrives as two 64-column x (64*KSUB)-row TMA boxes per stage,
 // and the ring takes all the shared memory there is.
 //
-// The split is over CTAs, not clusters: each CTA writes its partial tile
-// from tensor memory straight to global memory (L2) and exits, so nothing
-// in it waits on another CTA.  It is launched as a programmatic dependent:
-// the producer fills the ring with W0 (which no earlier kernel of the layer
-// writes) before it waits for the predecessor grid, then loads x, which the
-// predecessor may have written.  So the W0 stream of this layer overlaps the
-// tail of the previous kernel.
+// The split is over CTAs, not clusters: each CTA stages its partial tile
+// from tensor memory in the drained ring, stores it with one TMA tensor
+// store (into L2) and exits, so nothing in it waits on another CTA.  It is
+// launched as a programmatic dependent: the producer fills the ring with W0
+// (which no earlier kernel of the layer writes) before it waits for the
+// predecessor grid, then loads x, which the predecessor may have written.
+// So the W0 stream of this layer overlaps the tail of the previous kernel.
 //
 // Warp roles: warp 0 = TMA producer, warp 1 = MMA issuer (and TMEM
 // allocator), warps 2-5 = epilogue.  Every on-chip wait is bounded in time;
@@ -41,7 +41,6 @@ struct DecParams {
   int T, d_in, d_out;
   int n_blk;   // K blocks of 64*KSUB rows over d_in
   int stages;  // ring depth
-  float* partial;  // [S, T, d_out] fp32
   uint32_t* err;
 };
 
@@ -51,6 +50,8 @@ struct DecLayout {
   static constexpr uint32_t kXBytes = KSUB * kXSub;
   static constexpr uint32_t kWBox = 64 * KSUB * 128;         // 64 columns x 64*KSUB rows
   static constexpr uint32_t kStage = kXBytes + 2 * kWBox;
+  static constexpr uint32_t kOutBytes = BT * 128 * 4;       // fp32 partial tile, token-major
+  static_assert(kOutBytes <= kStage, "the partial tile is staged in one ring stage");
   static __host__ __device__ uint32_t bars(int stages) { return stages * kStage; }
   // full[stages], empty[stages], accum_full
   static __host__ __device__ uint32_t misc(int stages) { return bars(stages) + (2 * stages + 1) * 8; }
@@ -72,7 +73,8 @@ __device__ __forceinline__ void named_arrive(int id, int n) {
 template <int BT, int KSUB>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
-                       const __grid_constant__ CUtensorMap tm_w, const DecParams p) {
+                       const __grid_constant__ CUtensorMap tm_w,
+                       const __grid_constant__ CUtensorMap tm_p, const DecParams p) {
   using Lay = DecLayout<BT, KSUB>;
   constexpr int kTmemCols = BT < 32 ? 32 : BT;
   constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(128, BT, true, false);
@@ -98,6 +100,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       ptx::prefetch_tmap(&tm_w);
       ptx::prefetch_tmap(&tm_x);
+      ptx::prefetch_tmap(&tm_p);
       for (int i = 0; i < p.stages; ++i) {
         ptx::mbar_init(&full[i], 1);
         ptx::mbar_init(&empty[i], 1);
@@ -196,14 +199,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ---------------- epilogue warps: TMEM -> fp32 partial tile ----------
-    // TMEM lane = d_out column n of the tile, TMEM column = token; a warp
-    // stores 32 consecutive columns of one token row at a time (128 bytes)
-    if (warp_wait(accum_full, 0, abort_f) && n_it > 0) {
+    // TMEM lane = d_out column of the tile, TMEM column = token.  The tile is
+    // staged token-major ([BT][128] fp32) in ring stage 0, which the MMAs
+    // have finished reading: for each token a warp writes 32 consecutive
+    // floats (no bank conflicts).  One thread then stores it with a 3-D TMA
+    // store into partial [S][T][d_out]; rows past T and columns past d_out
+    // are clipped by the tensor bounds.
+    const int etid = tid - 64;
+    const bool acc_ok = warp_wait(accum_full, 0, abort_f) && n_it > 0 && !*abort_f;
+    float* stage_out = reinterpret_cast<float*>(smem);
+    if (acc_ok) {
       ptx::tc_fence_after();
       const int q = warp & 3;
-      const int n = n0 + q * 32 + lane;
-      const int rows_tok = min(BT, p.T - t0);
-      float* out = p.partial + (static_cast<size_t>(z) * p.T + t0) * p.d_out + n;
+      const int nl = q * 32 + lane;
       const uint32_t tq = tmem + (static_cast<uint32_t>(q * 32) << 16);
       constexpr int kCols = BT < 64 ? BT : 64;  // TMEM loads in flight before one wait
 #pragma unroll 1
@@ -213,12 +221,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < kCols / 16; ++j)
           ptx::tmem_ld16(tq + c0 + 16 * j, *reinterpret_cast<uint32_t(*)[16]>(v + 16 * j));
         ptx::tmem_ld_wait();
-        if (n < p.d_out) {
 #pragma unroll
-          for (int j = 0; j < kCols; ++j)
-            if (c0 + j < rows_tok) out[static_cast<size_t>(c0 + j) * p.d_out] = __uint_as_float(v[j]);
-        }
+        for (int j = 0; j < kCols; ++j) stage_out[(c0 + j) * 128 + nl] = __uint_as_float(v[j]);
       }
+      ptx::fence_proxy_async_smem();
+    }
+    named_sync(1, kThreads - 64);
+    if (etid == 0 && acc_ok) {
+      ptx::tma_store_3d(&tm_p, stage_out, n0, t0, z);
+      ptx::bulk_commit_group();
+      ptx::bulk_wait_group_read_all();  // the staging area must outlive the read
     }
   }
 
@@ -233,8 +245,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int BT, int KSUB>
 cudaError_t launch_decode_variant(const CUtensorMap& tm_x, const CUtensorMap& tm_w,
-                                  DecParams prm, int tiles_n, int tiles_t, int S, bool pdl,
-                                  cudaStream_t st, const DeviceInfo& dev) {
+                                  const CUtensorMap& tm_p, DecParams prm, int tiles_n,
+                                  int tiles_t, int S, bool pdl, cudaStream_t st,
+                                  const DeviceInfo& dev) {
   using Lay = DecLayout<BT, KSUB>;
   int stages = 0;
   for (int s = 6; s >= 2; --s) {
@@ -260,7 +273,7 @@ cudaError_t launch_decode_variant(const CUtensorMap& tm_x, const CUtensorMap& tm
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kern, tm_x, tm_w, prm);
+  return cudaLaunchKernelEx(&cfg, kern, tm_x, tm_w, tm_p, prm);
 }
 
 // token tile and K-block depth per decode batch size
@@ -300,9 +313,10 @@ cudaError_t launch_decode_gemm(const void* x, const void* W0, float* partial, in
   const int n_blk = decode_blocks(T, d_in);
   if (S < 1 || S > n_blk || tiles_t > 65535) return cudaErrorInvalidValue;
 
-  CUtensorMap tm_x, tm_w;
+  CUtensorMap tm_x, tm_w, tm_p;
   if (!encode_tensor_map_bf16(&tm_x, x, d_in, T, d_in, 64, BT) ||
-      !encode_tensor_map_bf16(&tm_w, W0, d_out, d_in, d_out, 64, 64 * ksub))
+      !encode_tensor_map_bf16(&tm_w, W0, d_out, d_in, d_out, 64, 64 * ksub) ||
+      !encode_tensor_map_f32_3d(&tm_p, partial, d_out, T, S, 128, BT))
     return cudaErrorInvalidValue;
   DecParams prm;
   prm.T = T;
@@ -310,11 +324,12 @@ cudaError_t launch_decode_gemm(const void* x, const void* W0, float* partial, in
   prm.d_out = d_out;
   prm.n_blk = n_blk;
   prm.stages = 0;
-  prm.partial = partial;
   prm.err = err;
-  if (BT == 32) return launch_decode_variant<32, 3>(tm_x, tm_w, prm, tiles_n, tiles_t, S, pdl, st, dev);
-  if (BT == 64) return launch_decode_variant<64, 3>(tm_x, tm_w, prm, tiles_n, tiles_t, S, pdl, st, dev);
-  return launch_decode_variant<128, 2>(tm_x, tm_w, prm, tiles_n, tiles_t, S, pdl, st, dev);
+  if (BT == 32)
+    return launch_decode_variant<32, 3>(tm_x, tm_w, tm_p, prm, tiles_n, tiles_t, S, pdl, st, dev);
+  if (BT == 64)
+    return launch_decode_variant<64, 3>(tm_x, tm_w, tm_p, prm, tiles_n, tiles_t, S, pdl, st, dev);
+  return launch_decode_variant<128, 2>(tm_x, tm_w, tm_p, prm, tiles_n, tiles_t, S, pdl, st, dev);
 }
 
 }  // namespace lora

@@ -20,14 +20,12 @@
 // B_a2 ...], turns the gathered expand into ordinary K-blocks of the same
 // MMA pipeline: one 64-row K-block holds 64 / r adapters (r <= 64).
 //
-// Two tile shapes:
-//  * decode (T <= 256), "swap": MMA M = 128 d_out columns (A operand = W0^T,
-//    MN-major), N = the token tile (B operand = x^T, K-major).  d_in is split
-//    over a cluster of S CTAs (split-K); the S fp32 partial tiles are summed
-//    through distributed shared memory, so W0 is streamed by ~all SMs.
-//  * prefill: MMA M = 128 tokens (A = x, K-major), N = 256 d_out columns
-//    (B = W0, MN-major).
-// Both operands arrive by TMA with 128-byte swizzle; the accumulator lives in
+// Tile: MMA M = 128 tokens (A = x, K-major), N = 256 d_out columns (B = W0,
+// MN-major); this is the prefill-sized path (more than 256 tokens).  d_in
+// is split over a cluster of S CTAs when there are fewer tiles than SMs; the
+// S fp32 partial tiles, staged in each CTA's drained ring, are summed
+// through distributed shared memory.  Both operands arrive by TMA with
+// 128-byte swizzle; the accumulator lives in
 // tensor memory; one thread issues the MMAs.  Warp roles: warp 0 = TMA
 // producer (also builds the masked V operand of the LoRA K-blocks), warp 1 =
 // MMA issuer (and TMEM allocator), warps 2-5 = epilogue (load v during the
@@ -60,38 +58,24 @@ struct TcParams {
   int v_ksplit;
   const int32_t* ids;
   const float* vpart;
-  // When set, the adapter term is given as a ready fp32 [T, d_out] tensor
-  // (written by the kernel launched just before) and added in the epilogue;
-  // no LoRA K-blocks are built.
-  const float* delta;
   bf16* y;
   uint32_t* err;
 };
 
 struct SmemLayout {
   uint32_t x_bytes, stage_bytes, stages_total;
-  uint32_t rb, vt, tok, uniq, bitmap, bars, misc, total;
+  uint32_t vt, tok, uniq, bitmap, bars, misc, total;
 };
-
-// Decode tiles (swap, up to 128 tokens) reduce split-K partials by pushing
-// them into the owning CTA's receive buffer; larger tiles stage them in the
-// drained pipeline ring and pull.
-template <bool SWAP, int BT>
-__host__ __device__ constexpr bool push_reduce() {
-  return SWAP && BT <= 128;
-}
 
 // Offsets from a 1024-byte aligned base (the 128-byte swizzle repeats every
 // 8 rows = 1024 bytes, and TMA / MMA agree on it only from such a base).
-template <bool SWAP, int BT, int BN>
+template <int BT, int BN>
 __host__ __device__ inline SmemLayout smem_layout(int stages, int r, int n_slots) {
   SmemLayout L;
   L.x_bytes = BT * 128;
   L.stage_bytes = L.x_bytes + (BN / 64) * 8192;
   L.stages_total = static_cast<uint32_t>(stages) * L.stage_bytes;
   uint32_t o = L.stages_total;
-  L.rb = o;   // receive buffer of the push reduction: [src rank][d_out row][token] fp32
-  if (push_reduce<SWAP, BT>()) o += 128 * BT * 4;
   L.vt = o;
   o += BT * r * 4;
   o = (o + 15u) & ~15u;
@@ -129,24 +113,22 @@ __device__ __forceinline__ void named_arrive(int id, int n) {
   asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
-template <bool SWAP, int BT, int BN>
+template <int BT, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     fused_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                     const __grid_constant__ CUtensorMap tm_b, const TcParams p) {
-  constexpr int kUmmaM = 128;
-  constexpr int kUmmaN = SWAP ? BT : BN;
+  constexpr int kUmmaN = BN;
   constexpr int kTmemCols = kUmmaN < 32 ? 32 : kUmmaN;
-  constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kUmmaM, kUmmaN, SWAP, !SWAP);
+  constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(128, kUmmaN, false, true);
   constexpr int kRedLd = BN + kRedPad;   // staged accumulator: [token][d_out column]
   constexpr int kWBoxes = BN / 64;
-  static_assert((SWAP ? BN : BT) == 128, "MMA M is 128");
+  static_assert(BT == 128, "MMA M is 128 tokens");
   static_assert(kUmmaN % 16 == 0 && kUmmaN >= 16 && kUmmaN <= 256, "MMA N");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  const SmemLayout L = smem_layout<SWAP, BT, BN>(p.stages, p.r, p.n_slots);
-  constexpr bool kPush = push_reduce<SWAP, BT>();
+  const SmemLayout L = smem_layout<BT, BN>(p.stages, p.r, p.n_slots);
   float* vt = reinterpret_cast<float*>(smem + L.vt);
   int* tok = reinterpret_cast<int*>(smem + L.tok);
   int* uniq = reinterpret_cast<int*>(smem + L.uniq);
@@ -162,9 +144,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n0 = blockIdx.x * BN, t0 = blockIdx.y * BT;
   const int S = static_cast<int>(gridDim.z), z = static_cast<int>(blockIdx.z);
-  // push reduction: peers may write into this CTA's receive buffer once
-  // every CTA of the cluster is running (phase A of the cluster barrier)
-  if (kPush && S > 1) ptx::cluster_arrive_relaxed();
 
   // ---- prologue: warp 0 initialises the barriers and starts the TMA stream
   // at once; the other warps wait for the barriers (named barrier 2), warp 1
@@ -361,8 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // are 8 KiB apart (LBO), 8-row groups 1 KiB apart (SBO)
           const uint64_t wd = ptx::sdesc_sw128(wa + kk * 2048, 8192, 1024);
           const uint32_t accum = (it > 0 || kk > 0) ? 1u : 0u;
-          if (SWAP) ptx::mma_bf16(tmem, wd, xd, kIdesc, accum);
-          else ptx::mma_bf16(tmem, xd, wd, kIdesc, accum);
+          ptx::mma_bf16(tmem, xd, wd, kIdesc, accum);
         }
         ptx::mma_commit(&empty[st]);
         return true;
@@ -382,23 +360,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- epilogue warps -------------------------------------
     const int etid = tid - 64;
     const int n_words = (p.n_slots + 31) >> 5;
-    if (p.delta != nullptr) {
-      // adapter term given in fp32: only which rows carry one is needed
-      bool bad_d = false;
-      for (int i = etid; i < BT; i += kEpiThreads) {
-        const int t = t0 + i;
-        int u = -1;
-        if (t < p.T) {
-          const int id = p.ids[t];
-          if (slot_valid(id, p.n_slots)) u = 0;
-          else if (id != -1) bad_d = true;
-        }
-        tok[i] = u;
-      }
-      if (bad_d && blockIdx.x == 0 && z == 0) flag_error(p.err, LORA_DEVERR_BAD_SLOT);
-      if (etid == 0) *n_uniq_s = 0;
-      epi_sync();
-    } else {
     // the tile's slot ids and its distinct adapters (ascending slot order),
     // built while the main loop streams W0
     bool bad = false;
@@ -478,101 +439,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     epi_sync();
-    }
     ptx::mbar_arrive(vt_ready);
     const bool acc_ok = warp_wait(accum_full, 0, abort_f);
-    if (kPush && S > 1) ptx::cluster_wait_acquire();   // phase A: peers are running
     if (acc_ok) {
       ptx::tc_fence_after();
       const int q = warp & 3;  // TMEM lanes 32q..32q+31 belong to this warp
       const uint32_t tq = tmem + (static_cast<uint32_t>(q * 32) << 16);
-      if (kPush) {
-        // TMEM lane = d_out row n of the tile, column = token.  Row n belongs
-        // to rank n / (128 / S); its partial goes to slot [z][n % (128/S)] of
-        // that rank's receive buffer, 16 tokens per vector store.
-        const int rows_own = 128 / S;
-        const int n = q * 32 + lane;
-        const int owner = n / rows_own, n_loc = n % rows_own;
-        const uint32_t local = ptx::smem_u32(smem + L.rb) +
-                               static_cast<uint32_t>(((z * rows_own + n_loc) * BT) * 4);
-        const uint32_t dst =
-            S > 1 ? ptx::mapa_shared(local, static_cast<uint32_t>(owner)) : local;
+      // the fp32 tile is staged token-major in the drained ring for the
+      // split-K reduction
+      float* red = reinterpret_cast<float*>(smem);
 #pragma unroll 1
-        for (int c0 = 0; c0 < kUmmaN; c0 += 16) {
-          uint32_t v[16];
-          ptx::tmem_ld16(tq + c0, v);
-          ptx::tmem_ld_wait();
+      for (int c0 = 0; c0 < kUmmaN; c0 += 16) {
+        uint32_t v[16];
+        ptx::tmem_ld16(tq + c0, v);
+        ptx::tmem_ld_wait();
+        const int i = q * 32 + lane;  // TMEM lane = token, column = d_out column
+        float4* dst = reinterpret_cast<float4*>(red + i * kRedLd + c0);
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            ptx::st_dsmem_f4(dst + static_cast<uint32_t>((c0 + 4 * j) * 4),
-                             make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                         __uint_as_float(v[4 * j + 2]),
-                                         __uint_as_float(v[4 * j + 3])));
-        }
-      } else {
-        float* red = reinterpret_cast<float*>(smem);
-#pragma unroll 1
-        for (int c0 = 0; c0 < kUmmaN; c0 += 16) {
-          uint32_t v[16];
-          ptx::tmem_ld16(tq + c0, v);
-          ptx::tmem_ld_wait();
-          if (SWAP) {
-            const int n = q * 32 + lane;  // TMEM lane = d_out column, column = token
-#pragma unroll
-            for (int j = 0; j < 16; ++j) red[(c0 + j) * kRedLd + n] = __uint_as_float(v[j]);
-          } else {
-            const int i = q * 32 + lane;  // TMEM lane = token, column = d_out column
-            float4* dst = reinterpret_cast<float4*>(red + i * kRedLd + c0);
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                   __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
-          }
-        }
+        for (int j = 0; j < 4; ++j)
+          dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                               __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
       }
     }
   }
 
   // ---- split-K reduction, store y ------------------------------------------
-  if constexpr (kPush) {
-    if (S > 1) {
-      if (warp < 2) ptx::cluster_wait_acquire();   // phase A (epilogue warps did it)
-      ptx::cluster_arrive_release();               // phase B: every push has landed
-      ptx::cluster_wait_acquire();
-    } else {
-      __syncthreads();
-    }
-    if (p.delta != nullptr) pdl_wait();  // delta comes from the previous kernel
-    if (!*abort_f) {
-      // this rank owns d_out rows [z * 128/S, (z+1) * 128/S) of the tile for
-      // every token; the S partials sit in its own receive buffer
-      const int rows_own = 128 / S;
-      const int groups = rows_own / 8;
-      const int rows_tok = min(BT, p.T - t0);
-      const float* rb = reinterpret_cast<const float*>(smem + L.rb);
-      for (int e = tid; e < rows_tok * groups; e += kThreads) {
-        const int g = e / rows_tok, t = e % rows_tok;
-        const int n = n0 + z * rows_own + g * 8;
-        if (n >= p.d_out) continue;
-        float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        for (int src = 0; src < S; ++src) {
-          const float* col = rb + (src * rows_own + g * 8) * BT + t;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) f[j] += col[j * BT];
-        }
-        if (p.delta != nullptr && tok[t] >= 0) {
-          float d[8];
-          load8_dep(p.delta + static_cast<size_t>(t0 + t) * p.d_out + n, d);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) f[j] += d[j];
-        }
-        store8(p.y + static_cast<size_t>(t0 + t) * p.d_out + n, f);
-      }
-    }
-  } else {
   if (S > 1) ptx::cluster_sync();
   else __syncthreads();
-  if (p.delta != nullptr) pdl_wait();  // delta comes from the previous kernel
   if (!*abort_f) {
     const int rows = min(BT, p.T - t0);
     const int rb0 = static_cast<int>(static_cast<long long>(z) * rows / S);
@@ -583,16 +476,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // two output chunks per pass: every load of both is issued before any sum
     for (int e0 = tid; e0 < n_items; e0 += 2 * kThreads) {
       float4 va[2][8], vb[2][8];
-      float dl[2][8];
       int ii[2], nn[2];
-      bool on[2], dd[2];
+      bool on[2];
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const int e = e0 + u * kThreads;
         ii[u] = rb0 + e / kChunks;
         nn[u] = n0 + (e % kChunks) * 8;
         on[u] = e < n_items && nn[u] < p.d_out;
-        dd[u] = on[u] && p.delta != nullptr && tok[ii[u]] >= 0;
         if (on[u]) {
           const uint32_t off = static_cast<uint32_t>((ii[u] * kRedLd + (nn[u] - n0)) * 4);
 #pragma unroll
@@ -605,7 +496,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (dd[u]) load8_dep(p.delta + static_cast<size_t>(t0 + ii[u]) * p.d_out + nn[u], dl[u]);
       }
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
@@ -618,16 +508,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             f[4] += vb[u][rk].x; f[5] += vb[u][rk].y; f[6] += vb[u][rk].z; f[7] += vb[u][rk].w;
           }
         }
-        if (dd[u]) {
-#pragma unroll
-          for (int q = 0; q < 8; ++q) f[q] += dl[u][q];
-        }
         store8(p.y + static_cast<size_t>(t0 + ii[u]) * p.d_out + nn[u], f);
       }
     }
   }
   if (S > 1) ptx::cluster_sync();
-  }
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -667,40 +552,35 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, 
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool SWAP, int BT, int BN>
+template <int BT, int BN>
 cudaError_t launch_variant(const void* x, const void* W0, const void* B, TcParams prm,
                            int tiles_n, int tiles_t, int S, cudaStream_t st,
                            const DeviceInfo& dev) {
   // deepest pipeline that fits next to the v tile and bookkeeping, and that
   // can hold the staged fp32 accumulator afterwards
   const size_t cap = dev.max_smem_optin;
-  const size_t red_bytes =
-      push_reduce<SWAP, BT>() ? 0 : static_cast<size_t>(BT) * (BN + kRedPad) * 4;
+  const size_t red_bytes = static_cast<size_t>(BT) * (BN + kRedPad) * 4;
   int stages = 0;
   for (int s = 8; s >= 2; --s) {
-    const SmemLayout L = smem_layout<SWAP, BT, BN>(s, prm.r, prm.n_slots);
-    if (L.total + 1024 <= cap && (red_bytes == 0 || L.stages_total >= red_bytes)) {
+    const SmemLayout L = smem_layout<BT, BN>(s, prm.r, prm.n_slots);
+    if (L.total + 1024 <= cap && L.stages_total >= red_bytes) {
       stages = s;
       break;
     }
   }
   if (stages == 0) return cudaErrorInvalidConfiguration;
   prm.stages = stages;
-  const SmemLayout L = smem_layout<SWAP, BT, BN>(stages, prm.r, prm.n_slots);
+  const SmemLayout L = smem_layout<BT, BN>(stages, prm.r, prm.n_slots);
   const size_t smem = L.total + 1024;
 
   CUtensorMap tm_x, tm_w, tm_b;
-  // with a ready adapter term (delta) no B rows are loaded; the B map then
-  // describes W0 only so that the parameter is a valid tensor map
-  const bool has_b = prm.delta == nullptr;
   if (!make_map(&tm_x, x, prm.d_in, prm.T, prm.d_in, kBK, BT) ||
       !make_map(&tm_w, W0, prm.d_out, prm.d_in, prm.d_out, 64, kBK) ||
-      !make_map(&tm_b, has_b ? B : W0, prm.d_out,
-                has_b ? static_cast<uint64_t>(prm.n_slots) * prm.r : prm.d_in, prm.d_out, 64,
+      !make_map(&tm_b, B, prm.d_out, static_cast<uint64_t>(prm.n_slots) * prm.r, prm.d_out, 64,
                 prm.box_rows))
     return cudaErrorInvalidValue;
 
-  auto kern = fused_tc_kernel<SWAP, BT, BN>;
+  auto kern = fused_tc_kernel<BT, BN>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
@@ -729,13 +609,26 @@ bool encode_tensor_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, ui
   return g_encode != nullptr && make_map(m, base, inner, outer, row_elems, box_inner, box_outer);
 }
 
+bool encode_tensor_map_f32_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1,
+                              uint64_t d2, uint32_t box0, uint32_t box1) {
+  resolve_encode();
+  if (g_encode == nullptr) return false;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {d0 * 4, d0 * d1 * 4};
+  cuuint32_t box[3] = {box0, box1, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool tensor_map_available() {
   resolve_encode();
   return g_encode != nullptr;
 }
 
 cudaError_t launch_fused_tc(const void* x, const void* W0, const void* B, const int32_t* ids,
-                            const float* vpart, int v_ksplit, const float* delta, void* y, int T,
+                            const float* vpart, int v_ksplit, void* y, int T,
                             int d_in, int d_out, int r, int n_slots, uint32_t* err,
                             cudaStream_t st, const DeviceInfo& dev) {
   resolve_encode();
@@ -748,20 +641,17 @@ cudaError_t launch_fused_tc(const void* x, const void* W0, const void* B, const 
   prm.n_slots = n_slots;
   prm.n_kblk = (d_in + kBK - 1) / kBK;
   prm.stages = 0;
-  if (delta != nullptr) r = 8;  // no v tile is staged; keep its footprint minimal
-  prm.r = r;
   prm.box_rows = r < 32 ? r : 32;
   prm.lg_box = 31 - __builtin_clz(static_cast<unsigned>(prm.box_rows));
   prm.lg_upa = 31 - __builtin_clz(static_cast<unsigned>(r / prm.box_rows));
   prm.v_ksplit = v_ksplit;
   prm.ids = ids;
   prm.vpart = vpart;
-  prm.delta = delta;
   prm.y = static_cast<bf16*>(y);
   prm.err = err;
 
   // split-K cluster size: as many CTAs per tile as fill the SMs, at most 8,
-  // a power of two (the push reduction splits the 128 rows of a tile evenly)
+  // a power of two
   auto pick_split = [&](int tiles) {
     int S = dev.num_sms / (tiles > 0 ? tiles : 1);
     if (S > 8) S = 8;
@@ -773,7 +663,7 @@ cudaError_t launch_fused_tc(const void* x, const void* W0, const void* B, const 
   const int tiles_n = (d_out + 255) / 256;
   const int tiles_t = (T + 127) / 128;
   const int S = pick_split(tiles_n * tiles_t);
-  return launch_variant<false, 128, 256>(x, W0, B, prm, tiles_n, tiles_t, S, st, dev);
+  return launch_variant<128, 256>(x, W0, B, prm, tiles_n, tiles_t, S, st, dev);
 }
 
 }  // namespace lora

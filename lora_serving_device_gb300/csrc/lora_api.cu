@@ -311,8 +311,8 @@ lora_status_t lora_linear_fused(const void* x, const void* W0, const void* A_poo
   }
   if (e != cudaSuccess) return LORA_ERR_CUDA;
   if (dt == LORA_DTYPE_BF16)
-    e = launch_fused_tc(x, W0, B_pool, slot_ids, w.vpart, w.ksplit, nullptr, y, T, d_in, d_out, r,
-                        n_slots, w.err, st, dev);
+    e = launch_fused_tc(x, W0, B_pool, slot_ids, w.vpart, w.ksplit, y, T, d_in, d_out, r, n_slots,
+                        w.err, st, dev);
   else
     e = launch_fused_f32(static_cast<const float*>(x), static_cast<const float*>(W0),
                          static_cast<const float*>(B_pool), slot_ids, w.vpart, w.ksplit,
@@ -344,7 +344,7 @@ lora_status_t lora_base_gemm_expand(const void* x, const void* W0, const void* B
   uint32_t* err = static_cast<uint32_t*>(ws);
   cudaError_t e;
   if (dt == LORA_DTYPE_BF16)
-    e = launch_fused_tc(x, W0, B_pool, slot_ids, v_partial, ksplit, nullptr, y, T, d_in, d_out, r,
+    e = launch_fused_tc(x, W0, B_pool, slot_ids, v_partial, ksplit, y, T, d_in, d_out, r,
                         n_slots, err, st, dev);
   else
     e = launch_fused_f32(static_cast<const float*>(x), static_cast<const float*>(W0),
