@@ -92,6 +92,18 @@ bool tensor_map_available();
 // outside the tensor read as zero.
 bool encode_tensor_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
                             uint64_t row_elems, uint32_t box_inner, uint32_t box_outer);
+// 3-D bf16 tensor map with 128-byte swizzle: dims d0 (contiguous) x d1 x
+// d2, box box0 x box1 x 1; elements outside the tensor read as zero.
+bool encode_tensor_map_bf16_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1,
+                               uint64_t d2, uint32_t box0, uint32_t box1);
+// SGMV shrink on tensor cores (bf16, r in {64, 128}), see k_sgmv_tc.cu; the
+// same contract as launch_sgmv_shrink.
+bool sgmv_shrink_tc_supported(int r);
+cudaError_t launch_sgmv_shrink_tc(const void* x, const void* A, const int32_t* perm,
+                                  const int32_t* seg_slot, const int32_t* seg_off,
+                                  const int32_t* n_seg, const float* scale, float* vpart, int T,
+                                  int d_in, int r, int n_slots, int ksplit, uint32_t* err,
+                                  cudaStream_t st, bool pdl, const DeviceInfo& dev);
 // 3-D fp32 tensor map without swizzle: dims d0 (contiguous) x d1 x d2,
 // box box0 x box1 x 1; elements outside the tensor are not stored.
 bool encode_tensor_map_f32_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1,

@@ -609,6 +609,20 @@ bool encode_tensor_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, ui
   return g_encode != nullptr && make_map(m, base, inner, outer, row_elems, box_inner, box_outer);
 }
 
+bool encode_tensor_map_bf16_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1,
+                               uint64_t d2, uint32_t box0, uint32_t box1) {
+  resolve_encode();
+  if (g_encode == nullptr) return false;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+  cuuint32_t box[3] = {box0, box1, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_tensor_map_f32_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1,
                               uint64_t d2, uint32_t box0, uint32_t box1) {
   resolve_encode();

@@ -1,0 +1,286 @@
+// SGMV shrink on tcgen05 tensor cores, for bf16 pools of rank 64 or 128
+// ("Serving multiple LoRAs: segmented matrix multiplies and adapter
+// scheduling", SGMV bullet: the tokens of one adapter's segment are
+// multiplied by that adapter's factor as one small matrix product):
+//
+//   v_partial[s, t, :] = scale[a] * x[t, K_s] A[a][K_s, :]
+//
+// for the tokens t of one segment (adapter a), in chunks of 128 tokens,
+// and the s-th 64-aligned range K_s of d_in.  At rank 64 and prefill sizes
+// this is 4.8 GFLOP against ~100 MB, so on CUDA cores it is bound by FMAs;
+// here it is a GEMM with M = 128 tokens (x rows gathered through perm,
+// K-major), N = r (A[a] rows, MN-major) and K = d_in.
+//
+// Warps 0-3 gather the chunk's x rows with 16-byte cp.async (the rows are
+// not contiguous in x) into the 128-byte-swizzled K-major layout, and one of
+// their threads brings A[a]'s K-block by TMA; then they run the epilogue
+// (TMEM -> registers -> v_partial rows, scaled).  Warp 4 allocates TMEM and
+// issues the MMAs.  Rows of base-only tokens are written as zeros by the
+// first item's CTA.  Every wait is bounded; on timeout the kernel raises
+// LORA_DEVERR_TIMEOUT and returns.
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+#include "sgmv_item.cuh"
+
+namespace lora {
+namespace {
+
+constexpr int kThreads = 160;  // warps 0-3: gather + epilogue, warp 4: MMA
+constexpr int kTok = 128;      // tokens per work item (the MMA's M)
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+template <int R>
+struct ShrinkLayout {
+  static constexpr uint32_t kX = kTok * 128;            // one 64-wide K block of x
+  static constexpr uint32_t kA = (R / 64) * 8192;       // R columns x 64 K rows of A[a]
+  static constexpr uint32_t kStage = kX + kA;
+  static constexpr int kStages = R == 64 ? 4 : 3;       // ~96 KiB: two CTAs per SM
+  static constexpr int kLag = kStages - 1;              // cp.async groups in flight
+  static constexpr uint32_t kBars = kStages * kStage;
+  static constexpr uint32_t kTotal = kBars + (2 * kStages + 1) * 8 + 16;
+};
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(ptx::smem_u32(dst)),
+               "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  int ok = 0;
+  if ((threadIdx.x & 31) == 0) ok = ptx::mbar_wait_bounded(bar, parity, abort, kWaitLimitNs) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+template <int R>
+__global__ void __launch_bounds__(kThreads, 2)
+    sgmv_shrink_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const bf16* x,
+                          const int32_t* perm, const int32_t* seg_slot, const int32_t* seg_off,
+                          const int32_t* n_seg, const float* scale, float* vpart, int T,
+                          int d_in, int kchunk, uint32_t* err) {
+  using Lay = ShrinkLayout<R>;
+  constexpr int S = Lay::kStages;
+  constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(128, R, false, true);
+  __shared__ int s_a, s_p0, s_p1;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Lay::kBars);
+  uint64_t* empty = full + S;
+  uint64_t* accum = empty + S;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
+  volatile int* abort_f = reinterpret_cast<volatile int*>(accum + 1) + 1;
+
+  pdl_launch_dependents();  // the base GEMM may start streaming W0 now
+  pdl_wait();               // the segments are written by the previous kernel
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, s = blockIdx.y;
+  const int nseg = ld_dep(n_seg);
+  if (blockIdx.x == 0) {  // rows of base-only tokens are zero
+    const int nbase = ld_dep(seg_off);
+    for (int e = tid; e < nbase * R; e += kThreads)
+      vpart[(static_cast<size_t>(s) * T + ld_dep(perm + e / R)) * R + (e % R)] = 0.f;
+  }
+  sgmv_item<kTok>(blockIdx.x, seg_slot, seg_off, nseg, &s_a, &s_p0, &s_p1);
+  const int a = s_a;
+  if (a < 0) return;  // no such item (uniform over the CTA)
+  const int p0 = s_p0, n_tok = s_p1 - s_p0;
+  const int k0 = s * kchunk, k1 = min(d_in, k0 + kchunk);
+  const int n_it = k1 > k0 ? (k1 - k0 + 63) / 64 : 0;
+  if (n_it == 0) {  // an empty split of d_in still writes its (zero) rows
+    for (int e = tid; e < n_tok * R; e += kThreads)
+      vpart[(static_cast<size_t>(s) * T + ld_dep(perm + p0 + e / R)) * R + (e % R)] = 0.f;
+    return;
+  }
+
+  if (warp == 4) {
+    if (lane == 0) {
+      ptx::prefetch_tmap(&tm_a);
+      for (int i = 0; i < S; ++i) {
+        ptx::mbar_init(&full[i], 4 * 32 + 1);  // every gathering thread + the TMA's arrival
+        ptx::mbar_init(&empty[i], 1);
+      }
+      ptx::mbar_init(accum, 1);
+      *abort_f = 0;
+      ptx::fence_mbar_init();
+    }
+    __syncwarp();
+    ptx::tmem_alloc(tmem_slot, R);
+    ptx::tmem_relinquish();
+    ptx::tc_fence_before();
+  }
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp < 4) {
+    // ---------------- gather producer ------------------------------------
+    // thread -> 16-byte chunk c of rows (tid >> 3) + 16 q, q = 0..7
+    const int c = tid & 7;
+    int rowtok[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int i = (tid >> 3) + 16 * q;
+      rowtok[q] = i < n_tok ? ld_dep(perm + p0 + i) : -1;
+    }
+    bool ok = true;
+    int it = 0;
+    for (; it < n_it; ++it) {
+      const int st = it % S;
+      const uint32_t ph = static_cast<uint32_t>(it / S) & 1u;
+      if (!warp_wait(&empty[st], ph ^ 1u, abort_f)) {
+        ok = false;
+        break;
+      }
+      uint8_t* X = smem + static_cast<size_t>(st) * Lay::kStage;
+      const int kb = k0 + it * 64;
+      if (tid == 0) {
+        ptx::mbar_arrive_expect_tx(&full[st], Lay::kA);
+#pragma unroll
+        for (int h = 0; h < R / 64; ++h)
+          ptx::tma_load_3d(X + Lay::kX + h * 8192, &tm_a, &full[st], 64 * h, kb, a);
+      }
+      const int col = kb + c * 8;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int i = (tid >> 3) + 16 * q;
+        if (rowtok[q] >= 0) {
+          const bool in = col < k1;
+          const bf16* src = x + (in ? static_cast<size_t>(rowtok[q]) * d_in + col : 0);
+          cp_async16(X + i * 128 + ((c ^ (i & 7)) << 4), src, in ? 16u : 0u);
+        }
+      }
+      cp_async_commit();
+      if (it >= Lay::kLag) {
+        cp_async_wait<Lay::kLag>();
+        ptx::fence_proxy_async_smem();
+        ptx::mbar_arrive(&full[(it - Lay::kLag) % S]);
+      }
+    }
+    cp_async_wait<0>();
+    ptx::fence_proxy_async_smem();
+    // the stages whose gather is complete but not yet signalled
+    for (int j = (it > Lay::kLag ? it - Lay::kLag : 0); j < it; ++j) ptx::mbar_arrive(&full[j % S]);
+    (void)ok;
+  } else if (lane == 0) {
+    // ---------------- MMA issuer -----------------------------------------
+    for (int it = 0; it < n_it; ++it) {
+      const int st = it % S;
+      const uint32_t ph = static_cast<uint32_t>(it / S) & 1u;
+      if (!ptx::mbar_wait_bounded(&full[st], ph, abort_f, kWaitLimitNs)) break;
+      ptx::tc_fence_after();
+      const uint32_t xa = ptx::smem_u32(smem + static_cast<size_t>(st) * Lay::kStage);
+      const uint32_t aa = xa + Lay::kX;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        // x: K-major, 16 elements = 32 bytes per step; A[a]: MN-major, 16
+        // K-rows = 2048 bytes per step, 64-column boxes 8 KiB apart
+        const uint64_t xd = ptx::sdesc_sw128(xa + kk * 32, 16, 1024);
+        const uint64_t ad = ptx::sdesc_sw128(aa + kk * 2048, 8192, 1024);
+        ptx::mma_bf16(tmem, xd, ad, kIdesc, (it > 0 || kk > 0) ? 1u : 0u);
+      }
+      ptx::mma_commit(&empty[st]);
+    }
+    ptx::mma_commit(accum);
+  }
+
+  if (warp < 4) {
+    // ---------------- epilogue: TMEM row i = token perm[p0 + i] ------------
+    const bool acc_ok = warp_wait(accum, 0, abort_f) && !*abort_f;
+    if (acc_ok) {
+      ptx::tc_fence_after();
+      const int i = warp * 32 + lane;
+      const float sc = scale ? scale[a] : 1.f;
+      float* out = i < n_tok ? vpart + (static_cast<size_t>(s) * T + ld_dep(perm + p0 + i)) * R
+                             : nullptr;
+      const uint32_t tq = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+#pragma unroll 1
+      for (int c0 = 0; c0 < R; c0 += 32) {
+        uint32_t v[32];
+        ptx::tmem_ld16(tq + c0, *reinterpret_cast<uint32_t(*)[16]>(v));
+        ptx::tmem_ld16(tq + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
+        ptx::tmem_ld_wait();
+        if (out != nullptr) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            reinterpret_cast<float4*>(out + c0)[j] =
+                make_float4(__uint_as_float(v[4 * j]) * sc, __uint_as_float(v[4 * j + 1]) * sc,
+                            __uint_as_float(v[4 * j + 2]) * sc, __uint_as_float(v[4 * j + 3]) * sc);
+        }
+      }
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 4) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, R);
+  }
+  if (tid == 0 && *abort_f) flag_error(err, LORA_DEVERR_TIMEOUT);
+}
+
+template <int R>
+cudaError_t launch_r(const CUtensorMap& tm, const bf16* x, const int32_t* perm,
+                     const int32_t* seg_slot, const int32_t* seg_off, const int32_t* n_seg,
+                     const float* scale, float* vpart, int T, int d_in, int n_slots, int ksplit,
+                     uint32_t* err, cudaStream_t st, bool pdl, const DeviceInfo& dev) {
+  using Lay = ShrinkLayout<R>;
+  const size_t smem = Lay::kTotal + 1024;
+  if (smem > dev.max_smem_optin) return cudaErrorInvalidConfiguration;
+  auto kern = sgmv_shrink_tc_kernel<R>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const int per = (d_in + ksplit - 1) / ksplit;
+  const int kchunk = (per + 63) / 64 * 64;
+  const int cap = T < n_slots ? T : n_slots;
+  const int items = (T + kTok - 1) / kTok + cap;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(items > 0 ? items : 1, ksplit);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, tm, x, perm, seg_slot, seg_off, n_seg, scale, vpart, T,
+                            d_in, kchunk, err);
+}
+
+}  // namespace
+
+bool sgmv_shrink_tc_supported(int r) { return r == 64 || r == 128; }
+
+cudaError_t launch_sgmv_shrink_tc(const void* x, const void* A, const int32_t* perm,
+                                  const int32_t* seg_slot, const int32_t* seg_off,
+                                  const int32_t* n_seg, const float* scale, float* vpart, int T,
+                                  int d_in, int r, int n_slots, int ksplit, uint32_t* err,
+                                  cudaStream_t st, bool pdl, const DeviceInfo& dev) {
+  if (T <= 0) return cudaSuccess;
+  CUtensorMap tm;
+  // A_pool as [n_slots][d_in][r]: 64 columns x 64 K rows per box; rows past
+  // d_in read as zero
+  if (!encode_tensor_map_bf16_3d(&tm, A, r, d_in, n_slots, 64, 64)) return cudaErrorInvalidValue;
+  const bf16* xe = static_cast<const bf16*>(x);
+  if (r == 64)
+    return launch_r<64>(tm, xe, perm, seg_slot, seg_off, n_seg, scale, vpart, T, d_in, n_slots,
+                        ksplit, err, st, pdl, dev);
+  if (r == 128)
+    return launch_r<128>(tm, xe, perm, seg_slot, seg_off, n_seg, scale, vpart, T, d_in, n_slots,
+                         ksplit, err, st, pdl, dev);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace lora

@@ -89,6 +89,20 @@ lora_status_t check_device(DeviceInfo* out) {
              : LORA_ERR_CUDA;
 }
 
+// SGMV shrink: tensor cores for bf16 pools of rank 64 / 128 (there it is a
+// GEMM the CUDA cores cannot feed), the CUDA-core kernel otherwise.
+cudaError_t sgmv_shrink_any(const void* x, const void* A, const int32_t* perm,
+                            const int32_t* seg_slot, const int32_t* seg_off, const int32_t* n_seg,
+                            const float* scale, float* vpart, int T, int d_in, int r, int n_slots,
+                            int ksplit, lora_dtype_t dt, uint32_t* err, cudaStream_t st, bool pdl,
+                            const DeviceInfo& dev) {
+  if (dt == LORA_DTYPE_BF16 && sgmv_shrink_tc_supported(r) && tensor_map_available())
+    return launch_sgmv_shrink_tc(x, A, perm, seg_slot, seg_off, n_seg, scale, vpart, T, d_in, r,
+                                 n_slots, ksplit, err, st, pdl, dev);
+  return launch_sgmv_shrink(x, A, perm, seg_slot, seg_off, n_seg, scale, vpart, T, d_in, r,
+                            n_slots, ksplit, dt, err, st, pdl);
+}
+
 lora_status_t check_ws(const void* ws, size_t ws_bytes, size_t need) {
   if (ws == nullptr || !aligned16(ws) || ws_bytes < need) return LORA_ERR_WORKSPACE;
   return LORA_OK;
@@ -231,9 +245,9 @@ lora_status_t lora_sgmv_shrink(const void* x, const void* A_pool, const int32_t*
   if (T == 0) return LORA_OK;
   DeviceInfo dev;
   if ((s = check_device(&dev)) != LORA_OK) return s;
-  return from_cuda(launch_sgmv_shrink(x, A_pool, perm, seg_slot, seg_off, n_seg, scale, v_partial,
-                                      T, d_in, r, n_slots, ksplit, dt, static_cast<uint32_t*>(ws),
-                                      static_cast<cudaStream_t>(stream), false));
+  return from_cuda(sgmv_shrink_any(x, A_pool, perm, seg_slot, seg_off, n_seg, scale, v_partial,
+                                   T, d_in, r, n_slots, ksplit, dt, static_cast<uint32_t*>(ws),
+                                   static_cast<cudaStream_t>(stream), false, dev));
 }
 
 lora_status_t lora_sgmv_expand(const float* v_partial, int32_t ksplit, const void* B_pool,
@@ -306,8 +320,8 @@ lora_status_t lora_linear_fused(const void* x, const void* W0, const void* A_poo
     e = launch_build_segments(slot_ids, T, n_slots, w.perm, w.seg_slot, w.seg_off, w.n_seg,
                               w.err, st);
     if (e != cudaSuccess) return LORA_ERR_CUDA;
-    e = launch_sgmv_shrink(x, A_pool, w.perm, w.seg_slot, w.seg_off, w.n_seg, scale, w.vpart, T,
-                           d_in, r, n_slots, w.ksplit, dt, w.err, st, true);
+    e = sgmv_shrink_any(x, A_pool, w.perm, w.seg_slot, w.seg_off, w.n_seg, scale, w.vpart, T,
+                        d_in, r, n_slots, w.ksplit, dt, w.err, st, true, dev);
   }
   if (e != cudaSuccess) return LORA_ERR_CUDA;
   if (dt == LORA_DTYPE_BF16)

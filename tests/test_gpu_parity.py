@@ -79,6 +79,9 @@ GATHER_CASES = [
     (130, 256, 520, 32, 4, "bf16"),
     (70, 136, 200, 64, 6, "bf16"),
     (45, 128, 1032, 128, 3, "bf16"),
+    # several 128-token SGMV items per segment, ragged d_in tail
+    (700, 4096, 72, 64, 9, "bf16"),
+    (300, 1000, 64, 128, 5, "bf16"),
     (53, 256, 256, 16, 8, "f32"),
     (90, 96, 72, 64, 4, "f32"),
 ]
