@@ -104,6 +104,14 @@ cudaError_t launch_sgmv_shrink_tc(const void* x, const void* A, const int32_t* p
                                   const int32_t* n_seg, const float* scale, float* vpart, int T,
                                   int d_in, int r, int n_slots, int ksplit, uint32_t* err,
                                   cudaStream_t st, bool pdl, const DeviceInfo& dev);
+// SGMV expand on tensor cores (bf16, r in {64, 128}), see k_sgmv_tc.cu; the
+// same contract as launch_sgmv_expand.
+bool sgmv_expand_tc_supported(int r);
+cudaError_t launch_sgmv_expand_tc(const float* vpart, int ksplit, const void* B,
+                                  const int32_t* perm, const int32_t* seg_slot,
+                                  const int32_t* seg_off, const int32_t* n_seg, void* y, int T,
+                                  int r, int d_out, int n_slots, uint32_t* err, cudaStream_t st,
+                                  const DeviceInfo& dev);
 // 3-D fp32 tensor map without swizzle: dims d0 (contiguous) x d1 x d2,
 // box box0 x box1 x 1; elements outside the tensor are not stored.
 bool encode_tensor_map_f32_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1,

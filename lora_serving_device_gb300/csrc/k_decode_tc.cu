@@ -51,7 +51,6 @@ struct DecLayout {
   static constexpr uint32_t kWBox = 64 * KSUB * 128;         // 64 columns x 64*KSUB rows
   static constexpr uint32_t kStage = kXBytes + 2 * kWBox;
   static constexpr uint32_t kOutBytes = BT * 128 * 4;       // fp32 partial tile, token-major
-  static_assert(kOutBytes <= kStage, "the partial tile is staged in one ring stage");
   static __host__ __device__ uint32_t bars(int stages) { return stages * kStage; }
   // full[stages], empty[stages], accum_full
   static __host__ __device__ uint32_t misc(int stages) { return bars(stages) + (2 * stages + 1) * 8; }
@@ -78,7 +77,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   using Lay = DecLayout<BT, KSUB>;
   constexpr int kTmemCols = BT < 32 ? 32 : BT;
   constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(128, BT, true, false);
-  static_assert(BT % 16 == 0 && BT >= 32 && BT <= 128, "token tile");
+  static_assert(BT % 16 == 0 && BT >= 32 && BT <= 256, "token tile");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -200,8 +199,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ---------------- epilogue warps: TMEM -> fp32 partial tile ----------
     // TMEM lane = d_out column of the tile, TMEM column = token.  The tile is
-    // staged token-major ([BT][128] fp32) in ring stage 0, which the MMAs
-    // have finished reading: for each token a warp writes 32 consecutive
+    // staged token-major ([BT][128] fp32) at the start of the ring, which the
+    // MMAs have finished reading: for each token a warp writes 32 consecutive
     // floats (no bank conflicts).  One thread then stores it with a 3-D TMA
     // store into partial [S][T][d_out]; rows past T and columns past d_out
     // are clipped by the tensor bounds.
@@ -256,7 +255,8 @@ cudaError_t launch_decode_variant(const CUtensorMap& tm_x, const CUtensorMap& tm
       break;
     }
   }
-  if (stages == 0) return cudaErrorInvalidConfiguration;
+  // the drained ring must hold the staged fp32 partial tile
+  if (stages == 0 || Lay::kOutBytes > stages * Lay::kStage) return cudaErrorInvalidConfiguration;
   prm.stages = stages;
   const size_t smem = Lay::total(stages) + 1024;
   auto kern = decode_gemm_kernel<BT, KSUB>;
@@ -277,8 +277,8 @@ cudaError_t launch_decode_variant(const CUtensorMap& tm_x, const CUtensorMap& tm
 }
 
 // token tile and K-block depth per decode batch size
-int decode_bt(int T) { return T <= 32 ? 32 : (T <= 64 ? 64 : 128); }
-int decode_ksub(int BT) { return BT <= 64 ? 3 : 2; }
+int decode_bt(int T) { return T <= 32 ? 32 : (T <= 64 ? 64 : (T <= 128 ? 128 : 256)); }
+int decode_ksub(int BT) { return BT <= 64 ? 3 : (BT == 128 ? 2 : 1); }
 int decode_blocks(int T, int d_in) {
   const int rows = 64 * decode_ksub(decode_bt(T > 0 ? T : 1));
   return (d_in + rows - 1) / rows;
@@ -329,7 +329,9 @@ cudaError_t launch_decode_gemm(const void* x, const void* W0, float* partial, in
     return launch_decode_variant<32, 3>(tm_x, tm_w, tm_p, prm, tiles_n, tiles_t, S, pdl, st, dev);
   if (BT == 64)
     return launch_decode_variant<64, 3>(tm_x, tm_w, tm_p, prm, tiles_n, tiles_t, S, pdl, st, dev);
-  return launch_decode_variant<128, 2>(tm_x, tm_w, tm_p, prm, tiles_n, tiles_t, S, pdl, st, dev);
+  if (BT == 128)
+    return launch_decode_variant<128, 2>(tm_x, tm_w, tm_p, prm, tiles_n, tiles_t, S, pdl, st, dev);
+  return launch_decode_variant<256, 1>(tm_x, tm_w, tm_p, prm, tiles_n, tiles_t, S, pdl, st, dev);
 }
 
 }  // namespace lora

@@ -46,6 +46,7 @@ constexpr int kBK = 64;           // K elements per stage: one 128-byte swizzle 
 constexpr int kThreads = 192;     // 6 warps
 constexpr int kEpiThreads = 128;  // warps 2..5
 constexpr int kRedPad = 4;        // fp32 padding per staged accumulator row
+constexpr int kPanel = 8;         // column tiles per L2 panel of the tile order
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s; the longest legitimate wait is ~ms
 
 struct TcParams {
@@ -142,7 +143,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_f = reinterpret_cast<volatile int*>(smem + L.misc + 8);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n0 = blockIdx.x * BN, t0 = blockIdx.y * BT;
+  // tile order: panels of kPanel column tiles; within a panel the column
+  // tile varies fastest, so the CTAs resident at one time share a W0 panel
+  // (16 MiB at d_in = 4096) and a band of x rows, and both stay in L2
+  const int tiles_n = (p.d_out + BN - 1) / BN, tiles_t = (p.T + BT - 1) / BT;
+  const int lin = static_cast<int>(blockIdx.x);
+  const int g = lin / (kPanel * tiles_t);
+  const int gn = min(kPanel, tiles_n - g * kPanel);
+  const int rem = lin - g * kPanel * tiles_t;
+  const int tile_n = g * kPanel + rem % gn, tile_t = rem / gn;
+  const int n0 = tile_n * BN, t0 = tile_t * BT;
   const int S = static_cast<int>(gridDim.z), z = static_cast<int>(blockIdx.z);
 
   // ---- prologue: warp 0 initialises the barriers and starts the TMA stream
@@ -374,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tok[i] = sl;
     }
     for (int wd = etid; wd < n_words; wd += kEpiThreads) bitmap[wd] = 0u;
-    if (bad && blockIdx.x == 0 && z == 0) flag_error(p.err, LORA_DEVERR_BAD_SLOT);
+    if (bad && tile_n == 0 && z == 0) flag_error(p.err, LORA_DEVERR_BAD_SLOT);
     epi_sync();
     for (int i = etid; i < BT; i += kEpiThreads) {
       const int sl = tok[i];
@@ -585,7 +595,7 @@ cudaError_t launch_variant(const void* x, const void* W0, const void* B, TcParam
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(tiles_n, tiles_t, S);
+  cfg.gridDim = dim3(tiles_n * tiles_t, 1, S);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;

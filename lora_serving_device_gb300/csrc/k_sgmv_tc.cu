@@ -11,13 +11,25 @@
 // here it is a GEMM with M = 128 tokens (x rows gathered through perm,
 // K-major), N = r (A[a] rows, MN-major) and K = d_in.
 //
-// Warps 0-3 gather the chunk's x rows with 16-byte cp.async (the rows are
-// not contiguous in x) into the 128-byte-swizzled K-major layout, and one of
-// their threads brings A[a]'s K-block by TMA; then they run the epilogue
-// (TMEM -> registers -> v_partial rows, scaled).  Warp 4 allocates TMEM and
+// When the item's tokens are consecutive rows of x (one prefill request),
+// one thread brings each K-block of x and of A[a] by TMA.  Otherwise warps
+// 0-3 gather the x rows with 16-byte cp.async into the 128-byte-swizzled
+// K-major layout and one of their threads brings A[a]'s K-block by TMA.
+// Warps 0-3 then run the epilogue (TMEM -> registers -> v_partial rows,
+// scaled).  Warp 4 allocates TMEM and
 // issues the MMAs.  Rows of base-only tokens are written as zeros by the
 // first item's CTA.  Every wait is bounded; on timeout the kernel raises
 // LORA_DEVERR_TIMEOUT and returns.
+//
+// SGMV expand on tensor cores (same page, same bullet; the expand is added
+// to the base output):  y[t, :] += (sum_s v_partial[s, t, :]) B[a]  for the
+// tokens of one segment, y bf16, read and written once.  At rank 64 over a
+// prefill batch this is 16.7 GFLOP against ~0.6 GB, again beyond the CUDA
+// cores.  A work item (128 tokens of one segment) builds its V tile once in
+// shared memory, as bf16 hi + lo halves (v = hi + lo keeps ~16 mantissa
+// bits), then runs 128-column tiles of d_out: B[a] by TMA, MMAs of both
+// halves into a double-buffered TMEM accumulator, and an epilogue that adds
+// it to the gathered y rows.
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
@@ -64,7 +76,8 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 
 template <int R>
 __global__ void __launch_bounds__(kThreads, 2)
-    sgmv_shrink_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const bf16* x,
+    sgmv_shrink_tc_kernel(const __grid_constant__ CUtensorMap tm_a,
+                          const __grid_constant__ CUtensorMap tm_x, const bf16* x,
                           const int32_t* perm, const int32_t* seg_slot, const int32_t* seg_off,
                           const int32_t* n_seg, const float* scale, float* vpart, int T,
                           int d_in, int kchunk, uint32_t* err) {
@@ -102,12 +115,18 @@ __global__ void __launch_bounds__(kThreads, 2)
       vpart[(static_cast<size_t>(s) * T + ld_dep(perm + p0 + e / R)) * R + (e % R)] = 0.f;
     return;
   }
+  // perm is ascending within a segment, so the item's rows are consecutive
+  // in x exactly when the first and last are n_tok - 1 apart
+  const int row0 = ld_dep(perm + p0);
+  const bool contig = ld_dep(perm + p0 + n_tok - 1) - row0 == n_tok - 1;
 
   if (warp == 4) {
     if (lane == 0) {
       ptx::prefetch_tmap(&tm_a);
+      ptx::prefetch_tmap(&tm_x);
       for (int i = 0; i < S; ++i) {
-        ptx::mbar_init(&full[i], 4 * 32 + 1);  // every gathering thread + the TMA's arrival
+        // TMA only: one arrival; gather: every gathering thread + the TMA's
+        ptx::mbar_init(&full[i], contig ? 1 : 4 * 32 + 1);
         ptx::mbar_init(&empty[i], 1);
       }
       ptx::mbar_init(accum, 1);
@@ -123,7 +142,24 @@ __global__ void __launch_bounds__(kThreads, 2)
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp < 4) {
+  if (warp < 4 && contig) {
+    // ---------------- TMA producer (consecutive rows) ---------------------
+    if (tid == 0) {
+      for (int it = 0; it < n_it; ++it) {
+        const int st = it % S;
+        const uint32_t ph = static_cast<uint32_t>(it / S) & 1u;
+        if (!ptx::mbar_wait_bounded(&empty[st], ph ^ 1u, abort_f, kWaitLimitNs)) break;
+        uint8_t* X = smem + static_cast<size_t>(st) * Lay::kStage;
+        const int kb = k0 + it * 64;
+        ptx::mbar_arrive_expect_tx(&full[st], Lay::kStage);
+        ptx::tma_load_2d(X, &tm_x, &full[st], kb, row0);
+#pragma unroll
+        for (int h = 0; h < R / 64; ++h)
+          ptx::tma_load_3d(X + Lay::kX + h * 8192, &tm_a, &full[st], 64 * h, kb, a);
+      }
+    }
+    __syncwarp();
+  } else if (warp < 4) {
     // ---------------- gather producer ------------------------------------
     // thread -> 16-byte chunk c of rows (tid >> 3) + 16 q, q = 0..7
     const int c = tid & 7;
@@ -230,7 +266,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 }
 
 template <int R>
-cudaError_t launch_r(const CUtensorMap& tm, const bf16* x, const int32_t* perm,
+cudaError_t launch_r(const CUtensorMap& tm, const CUtensorMap& tm_x, const bf16* x,
+                     const int32_t* perm,
                      const int32_t* seg_slot, const int32_t* seg_off, const int32_t* n_seg,
                      const float* scale, float* vpart, int T, int d_in, int n_slots, int ksplit,
                      uint32_t* err, cudaStream_t st, bool pdl, const DeviceInfo& dev) {
@@ -255,13 +292,245 @@ cudaError_t launch_r(const CUtensorMap& tm, const bf16* x, const int32_t* perm,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kern, tm, x, perm, seg_slot, seg_off, n_seg, scale, vpart, T,
-                            d_in, kchunk, err);
+  return cudaLaunchKernelEx(&cfg, kern, tm, tm_x, x, perm, seg_slot, seg_off, n_seg, scale, vpart,
+                            T, d_in, kchunk, err);
+}
+
+// ------------------------------------------------------------ expand
+constexpr int kXN = 128;      // d_out columns per tile (the MMA's N)
+constexpr int kXGroup = 8;    // d_out tiles per CTA
+
+template <int R>
+struct ExpandLayout {
+  static constexpr int KB = R / 64;                          // 64-wide K blocks of v
+  static constexpr uint32_t kVBlk = kTok * 128;              // one K block, K-major SW128
+  static constexpr uint32_t kV = 2 * KB * kVBlk;             // hi blocks, then lo blocks
+  static constexpr uint32_t kBBox = R * 128;                 // 64 columns x R rows
+  static constexpr uint32_t kB = (kXN / 64) * kBBox;
+  static constexpr uint32_t kBars = kV + 2 * kB;
+  static constexpr uint32_t kTotal = kBars + 8 * 8 + 16;
+};
+
+template <int R>
+__global__ void __launch_bounds__(kThreads)
+    sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap tm_b, const float* vpart, int ksplit,
+                          const int32_t* perm, const int32_t* seg_slot, const int32_t* seg_off,
+                          const int32_t* n_seg, bf16* y, int T, int d_out, uint32_t* err) {
+  using Lay = ExpandLayout<R>;
+  constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(128, kXN, false, true);
+  __shared__ int s_a, s_p0, s_p1;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* b_full = reinterpret_cast<uint64_t*>(smem + Lay::kBars);
+  uint64_t* b_empty = b_full + 2;
+  uint64_t* t_full = b_full + 4;
+  uint64_t* t_empty = b_full + 6;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(b_full + 8);
+  volatile int* abort_f = reinterpret_cast<volatile int*>(b_full + 8) + 1;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  sgmv_item<kTok>(blockIdx.x, seg_slot, seg_off, ld_dep(n_seg), &s_a, &s_p0, &s_p1);
+  const int a = s_a;
+  if (a < 0) return;  // no such item (uniform over the CTA)
+  const int p0 = s_p0, n_tok = s_p1 - s_p0;
+  const int n_tiles_all = (d_out + kXN - 1) / kXN;
+  const int j0 = blockIdx.y * kXGroup;
+  const int nt = min(kXGroup, n_tiles_all - j0);
+  if (nt <= 0) return;
+
+  auto issue_b = [&](int j) {  // B[a][:, tile j] into buffer j & 1
+    const int bs = j & 1;
+    ptx::mbar_arrive_expect_tx(&b_full[bs], Lay::kB);
+#pragma unroll
+    for (int h = 0; h < kXN / 64; ++h)
+      ptx::tma_load_3d(smem + Lay::kV + bs * Lay::kB + h * Lay::kBBox, &tm_b, &b_full[bs],
+                       (j0 + j) * kXN + 64 * h, 0, a);
+  };
+  if (warp == 4) {
+    if (lane == 0) {
+      ptx::prefetch_tmap(&tm_b);
+      for (int i = 0; i < 2; ++i) {
+        ptx::mbar_init(&b_full[i], 1);
+        ptx::mbar_init(&b_empty[i], 1);
+        ptx::mbar_init(&t_full[i], 1);
+        ptx::mbar_init(&t_empty[i], 4 * 32);
+      }
+      *abort_f = 0;
+      ptx::fence_mbar_init();
+      issue_b(0);
+      if (nt > 1) issue_b(1);
+    }
+    __syncwarp();
+    ptx::tmem_alloc(tmem_slot, 2 * kXN);
+    ptx::tmem_relinquish();
+    ptx::tc_fence_before();
+  } else {
+    // V tile: row i = token perm[p0 + i]; v summed over the d_in splits,
+    // split into bf16 hi + lo, written K-major with the 128-byte swizzle
+    const int i = tid;
+    if (i < n_tok) {
+      const int tok = ld_dep(perm + p0 + i);
+#pragma unroll 1
+      for (int q0 = 0; q0 < R; q0 += 8) {
+        float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int sp = 0; sp < ksplit; ++sp) {
+          const float* vp = vpart + (static_cast<size_t>(sp) * T + tok) * R + q0;
+          const float4 u0 = ld_dep_f4(vp), u1 = ld_dep_f4(vp + 4);
+          f[0] += u0.x; f[1] += u0.y; f[2] += u0.z; f[3] += u0.w;
+          f[4] += u1.x; f[5] += u1.y; f[6] += u1.z; f[7] += u1.w;
+        }
+        float hi[8], lo[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          hi[q] = __bfloat162float(__float2bfloat16_rn(f[q]));
+          lo[q] = f[q] - hi[q];
+        }
+        const int kb = q0 >> 6, ch = (q0 >> 3) & 7;
+        const uint32_t off = i * 128 + ((ch ^ (i & 7)) << 4);
+        *reinterpret_cast<uint4*>(smem + kb * Lay::kVBlk + off) = pack8_bf16(hi);
+        *reinterpret_cast<uint4*>(smem + (Lay::KB + kb) * Lay::kVBlk + off) = pack8_bf16(lo);
+      }
+    }
+    ptx::fence_proxy_async_smem();
+  }
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 4) {
+    // ---------------- MMA issuer (and B loads) ----------------------------
+    if (lane == 0) {
+      const uint32_t vbase = ptx::smem_u32(smem);
+      for (int j = 0; j < nt; ++j) {
+        const int bs = j & 1;
+        const uint32_t ph = static_cast<uint32_t>(j >> 1) & 1u;
+        if (!ptx::mbar_wait_bounded(&b_full[bs], ph, abort_f, kWaitLimitNs)) break;
+        if (!ptx::mbar_wait_bounded(&t_empty[bs], ph ^ 1u, abort_f, kWaitLimitNs)) break;
+        ptx::tc_fence_after();
+        const uint32_t bb = ptx::smem_u32(smem + Lay::kV + bs * Lay::kB);
+        const uint32_t acc = tmem + static_cast<uint32_t>(bs * kXN);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+#pragma unroll
+          for (int kk = 0; kk < R / 16; ++kk) {
+            const uint64_t vd = ptx::sdesc_sw128(
+                vbase + (half * Lay::KB + (kk >> 2)) * Lay::kVBlk + (kk & 3) * 32, 16, 1024);
+            const uint64_t bd = ptx::sdesc_sw128(bb + kk * 2048, Lay::kBBox, 1024);
+            ptx::mma_bf16(acc, vd, bd, kIdesc, (half > 0 || kk > 0) ? 1u : 0u);
+          }
+        }
+        ptx::mma_commit(&b_empty[bs]);
+        ptx::mma_commit(&t_full[bs]);
+        if (j + 2 < nt) {  // the buffer is free once these MMAs are done
+          if (!ptx::mbar_wait_bounded(&b_empty[bs], ph, abort_f, kWaitLimitNs)) break;
+          issue_b(j + 2);
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue: y rows += accumulator rows ----------------
+    const int i = warp * 32 + lane;
+    const bool row_on = i < n_tok;
+    bf16* yrow = row_on ? y + static_cast<size_t>(ld_dep(perm + p0 + i)) * d_out : nullptr;
+    const uint32_t tq = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    for (int j = 0; j < nt; ++j) {
+      const int bs = j & 1;
+      const uint32_t ph = static_cast<uint32_t>(j >> 1) & 1u;
+      const int n0 = (j0 + j) * kXN;
+      // this row's y for the tile, requested before the accumulator is ready
+      uint4 yv[kXN / 8];
+#pragma unroll
+      for (int c = 0; c < kXN / 8; ++c)
+        if (row_on && n0 + c * 8 < d_out) yv[c] = *reinterpret_cast<const uint4*>(yrow + n0 + c * 8);
+      if (!warp_wait(&t_full[bs], ph, abort_f)) break;
+      ptx::tc_fence_after();
+#pragma unroll
+      for (int c0 = 0; c0 < kXN; c0 += 32) {
+        uint32_t v[32];
+        ptx::tmem_ld16(tq + bs * kXN + c0, *reinterpret_cast<uint32_t(*)[16]>(v));
+        ptx::tmem_ld16(tq + bs * kXN + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int cc = c0 / 8 + c;
+          if (row_on && n0 + cc * 8 < d_out) {
+            const uint32_t w[4] = {yv[cc].x, yv[cc].y, yv[cc].z, yv[cc].w};
+            float f[8];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              f[2 * e] = bf16_lo(w[e]) + __uint_as_float(v[8 * c + 2 * e]);
+              f[2 * e + 1] = bf16_hi(w[e]) + __uint_as_float(v[8 * c + 2 * e + 1]);
+            }
+            *reinterpret_cast<uint4*>(yrow + n0 + cc * 8) = pack8_bf16(f);
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&t_empty[bs]);
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 4) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 2 * kXN);
+  }
+  if (tid == 0 && *abort_f) flag_error(err, LORA_DEVERR_TIMEOUT);
+}
+
+template <int R>
+cudaError_t launch_expand_r(const CUtensorMap& tm, const float* vpart, int ksplit,
+                            const int32_t* perm, const int32_t* seg_slot, const int32_t* seg_off,
+                            const int32_t* n_seg, bf16* y, int T, int d_out, int n_slots,
+                            uint32_t* err, cudaStream_t st, const DeviceInfo& dev) {
+  using Lay = ExpandLayout<R>;
+  // at most two CTAs per SM, so their 2 x 256 tensor-memory columns fit
+  size_t smem = Lay::kTotal + 1024;
+  if (smem < 100 * 1024) smem = 100 * 1024;
+  if (smem > dev.max_smem_optin) return cudaErrorInvalidConfiguration;
+  auto kern = sgmv_expand_tc_kernel<R>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const int cap = T < n_slots ? T : n_slots;
+  const int items = (T + kTok - 1) / kTok + cap;
+  const int groups = ((d_out + kXN - 1) / kXN + kXGroup - 1) / kXGroup;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(items > 0 ? items : 1, groups);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.numAttrs = 0;
+  return cudaLaunchKernelEx(&cfg, kern, tm, vpart, ksplit, perm, seg_slot, seg_off, n_seg, y, T,
+                            d_out, err);
 }
 
 }  // namespace
 
 bool sgmv_shrink_tc_supported(int r) { return r == 64 || r == 128; }
+bool sgmv_expand_tc_supported(int r) { return r == 64 || r == 128; }
+
+cudaError_t launch_sgmv_expand_tc(const float* vpart, int ksplit, const void* B,
+                                  const int32_t* perm, const int32_t* seg_slot,
+                                  const int32_t* seg_off, const int32_t* n_seg, void* y, int T,
+                                  int r, int d_out, int n_slots, uint32_t* err, cudaStream_t st,
+                                  const DeviceInfo& dev) {
+  if (T <= 0) return cudaSuccess;
+  CUtensorMap tm;
+  // B_pool as [n_slots][r][d_out]: 64 columns x r rows per box
+  if (!encode_tensor_map_bf16_3d(&tm, B, d_out, r, n_slots, 64, r)) return cudaErrorInvalidValue;
+  bf16* ye = static_cast<bf16*>(y);
+  if (r == 64)
+    return launch_expand_r<64>(tm, vpart, ksplit, perm, seg_slot, seg_off, n_seg, ye, T, d_out,
+                               n_slots, err, st, dev);
+  if (r == 128)
+    return launch_expand_r<128>(tm, vpart, ksplit, perm, seg_slot, seg_off, n_seg, ye, T, d_out,
+                                n_slots, err, st, dev);
+  return cudaErrorInvalidValue;
+}
 
 cudaError_t launch_sgmv_shrink_tc(const void* x, const void* A, const int32_t* perm,
                                   const int32_t* seg_slot, const int32_t* seg_off,
@@ -269,17 +538,19 @@ cudaError_t launch_sgmv_shrink_tc(const void* x, const void* A, const int32_t* p
                                   int d_in, int r, int n_slots, int ksplit, uint32_t* err,
                                   cudaStream_t st, bool pdl, const DeviceInfo& dev) {
   if (T <= 0) return cudaSuccess;
-  CUtensorMap tm;
+  CUtensorMap tm, tm_x;
   // A_pool as [n_slots][d_in][r]: 64 columns x 64 K rows per box; rows past
-  // d_in read as zero
-  if (!encode_tensor_map_bf16_3d(&tm, A, r, d_in, n_slots, 64, 64)) return cudaErrorInvalidValue;
+  // d_in read as zero.  x: 64 columns x 128 rows per box
+  if (!encode_tensor_map_bf16_3d(&tm, A, r, d_in, n_slots, 64, 64) ||
+      !encode_tensor_map_bf16(&tm_x, x, d_in, T, d_in, 64, kTok))
+    return cudaErrorInvalidValue;
   const bf16* xe = static_cast<const bf16*>(x);
   if (r == 64)
-    return launch_r<64>(tm, xe, perm, seg_slot, seg_off, n_seg, scale, vpart, T, d_in, n_slots,
-                        ksplit, err, st, pdl, dev);
+    return launch_r<64>(tm, tm_x, xe, perm, seg_slot, seg_off, n_seg, scale, vpart, T, d_in,
+                        n_slots, ksplit, err, st, pdl, dev);
   if (r == 128)
-    return launch_r<128>(tm, xe, perm, seg_slot, seg_off, n_seg, scale, vpart, T, d_in, n_slots,
-                         ksplit, err, st, pdl, dev);
+    return launch_r<128>(tm, tm_x, xe, perm, seg_slot, seg_off, n_seg, scale, vpart, T, d_in,
+                         n_slots, ksplit, err, st, pdl, dev);
   return cudaErrorInvalidValue;
 }
 

@@ -103,6 +103,19 @@ cudaError_t sgmv_shrink_any(const void* x, const void* A, const int32_t* perm,
                             n_slots, ksplit, dt, err, st, pdl);
 }
 
+// SGMV expand: tensor cores for bf16 pools of rank 64 / 128, the CUDA-core
+// kernel otherwise.
+cudaError_t sgmv_expand_any(const float* vpart, int ksplit, const void* B, const int32_t* perm,
+                            const int32_t* seg_slot, const int32_t* seg_off, const int32_t* n_seg,
+                            void* y, int T, int r, int d_out, int n_slots, lora_dtype_t dt,
+                            uint32_t* err, cudaStream_t st, const DeviceInfo& dev) {
+  if (dt == LORA_DTYPE_BF16 && sgmv_expand_tc_supported(r) && tensor_map_available())
+    return launch_sgmv_expand_tc(vpart, ksplit, B, perm, seg_slot, seg_off, n_seg, y, T, r, d_out,
+                                 n_slots, err, st, dev);
+  return launch_sgmv_expand(vpart, ksplit, B, perm, seg_slot, seg_off, n_seg, y, T, r, d_out,
+                            n_slots, dt, err, st);
+}
+
 lora_status_t check_ws(const void* ws, size_t ws_bytes, size_t need) {
   if (ws == nullptr || !aligned16(ws) || ws_bytes < need) return LORA_ERR_WORKSPACE;
   return LORA_OK;
@@ -269,9 +282,9 @@ lora_status_t lora_sgmv_expand(const float* v_partial, int32_t ksplit, const voi
   if (T == 0) return LORA_OK;
   DeviceInfo dev;
   if ((s = check_device(&dev)) != LORA_OK) return s;
-  return from_cuda(launch_sgmv_expand(v_partial, ksplit, B_pool, perm, seg_slot, seg_off, n_seg, y,
-                                      T, r, d_out, n_slots, dt, static_cast<uint32_t*>(ws),
-                                      static_cast<cudaStream_t>(stream)));
+  return from_cuda(sgmv_expand_any(v_partial, ksplit, B_pool, perm, seg_slot, seg_off, n_seg, y,
+                                   T, r, d_out, n_slots, dt, static_cast<uint32_t*>(ws),
+                                   static_cast<cudaStream_t>(stream), dev));
 }
 
 lora_status_t lora_linear_fused(const void* x, const void* W0, const void* A_pool,
