@@ -315,6 +315,31 @@ lora_status_t lora_linear_fused_noalloc(const void* x, const void* W0, const voi
                                         lora_dtype_t dt, void* stream);
 
 /*
+ * Uploads one adapter into pool slot `slot` (the data path of adapter
+ * paging: "Multi-LoRA batching and adapter paging", section "Adapter
+ * paging", and "Serving many LoRA adapters", section "Paging adapters": an
+ * adapter moves from host memory into a slot of the resident pool while the
+ * layer kernels keep running).  The adapter has rank r_a <= r; it is stored
+ * zero-padded to the pool rank, which leaves every layer result unchanged:
+ *   A_pool[slot][:, 0:r_a] = A_host [d_in, r_a]    A_pool[slot][:, r_a:r] = 0
+ *   B_pool[slot][0:r_a, :] = B_host [r_a, d_out]   B_pool[slot][r_a:r, :] = 0
+ *   scale[slot] = s                                 (skipped when scale is NULL)
+ * A_host / B_host are host pointers, row-major and contiguous; pin them
+ * (cudaHostAlloc) for the copies to be asynchronous and overlap kernels on
+ * other streams.  Only enqueues work on `stream` (two copies, the zero
+ * fills, and a one-thread kernel for the scale); the caller must not change
+ * the host buffers until the stream has passed this call, and must not run
+ * a layer that reads `slot` concurrently on another stream.  bf16 or fp32
+ * pools (dt).  Errors: LORA_ERR_SHAPE for slot outside [0, n_slots), r_a
+ * outside [1, r] or an invalid r / dims; LORA_ERR_INVALID_ARG for a null
+ * pointer or a pool not 16-byte aligned.  No workspace.
+ */
+lora_status_t lora_slot_upload(void* A_pool, void* B_pool, float* scale, int32_t slot,
+                               const void* A_host, const void* B_host, float s, int32_t d_in,
+                               int32_t d_out, int32_t r, int32_t r_a, int32_t n_slots,
+                               lora_dtype_t dt, void* stream);
+
+/*
  * Synchronises `stream`, copies the workspace error word to *device_err and
  * clears it.  Returns LORA_ERR_CUDA if the stream reports an error.
  */

@@ -45,6 +45,8 @@ cudaError_t launch_sgmv_expand(const float* vpart, int ksplit, const void* B, co
                                const int32_t* n_seg, void* y, int T, int r, int d_out,
                                int n_slots, lora_dtype_t dt, uint32_t* err, cudaStream_t st);
 
+// scale[slot] = s, one thread (the scale upload of lora_slot_upload).
+cudaError_t launch_set_scale(float* scale, int slot, float s, cudaStream_t st);
 // Upper bound on SGMV work items (segment x token-chunk pairs) for a batch.
 int sgmv_max_items(int T, int n_slots);
 // ksplit the fused path uses for its shrink (SGMV / BGMV form).

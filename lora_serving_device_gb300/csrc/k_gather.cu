@@ -430,6 +430,15 @@ cudaError_t sgmv_expand_t(const float* vpart, int ksplit, const void* B, const i
 
 }  // namespace
 
+namespace {
+__global__ void set_scale_kernel(float* scale, int slot, float s) { scale[slot] = s; }
+}  // namespace
+
+cudaError_t launch_set_scale(float* scale, int slot, float s, cudaStream_t st) {
+  set_scale_kernel<<<1, 1, 0, st>>>(scale, slot, s);
+  return cudaGetLastError();
+}
+
 int sgmv_max_items(int T, int n_slots) {
   const int cap = T < n_slots ? T : n_slots;
   const int items = (T + kSgTokens - 1) / kSgTokens + cap;

@@ -478,6 +478,38 @@ int32_t lora_decode_split(int32_t T, int32_t d_in, int32_t d_out) {
   return decode_gemm_split(T, d_in, d_out);
 }
 
+lora_status_t lora_slot_upload(void* A_pool, void* B_pool, float* scale, int32_t slot,
+                               const void* A_host, const void* B_host, float s, int32_t d_in,
+                               int32_t d_out, int32_t r, int32_t r_a, int32_t n_slots,
+                               lora_dtype_t dt, void* stream) {
+  if (!dtype_ok(dt)) return LORA_ERR_DTYPE;
+  if (!dim_ok(d_in) || !dim_ok(d_out) || !rank_ok(r) || !slots_ok(n_slots) || slot < 0 ||
+      slot >= n_slots || r_a < 1 || r_a > r)
+    return LORA_ERR_SHAPE;
+  if (A_pool == nullptr || B_pool == nullptr || A_host == nullptr || B_host == nullptr ||
+      !aligned16(A_pool) || !aligned16(B_pool))
+    return LORA_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t es = dt == LORA_DTYPE_BF16 ? 2 : 4;
+  uint8_t* A = static_cast<uint8_t*>(A_pool) + static_cast<size_t>(slot) * d_in * r * es;
+  uint8_t* B = static_cast<uint8_t*>(B_pool) + static_cast<size_t>(slot) * r * d_out * es;
+  // A: d_in rows of r_a values into rows of r values, then zero the padding
+  if (cudaMemcpy2DAsync(A, r * es, A_host, r_a * es, r_a * es, d_in, cudaMemcpyHostToDevice,
+                        st) != cudaSuccess)
+    return LORA_ERR_CUDA;
+  if (r_a < r && cudaMemset2DAsync(A + r_a * es, r * es, 0, (r - r_a) * es, d_in, st) != cudaSuccess)
+    return LORA_ERR_CUDA;
+  // B: r_a contiguous rows, then zero rows up to r
+  if (cudaMemcpyAsync(B, B_host, static_cast<size_t>(r_a) * d_out * es, cudaMemcpyHostToDevice,
+                      st) != cudaSuccess)
+    return LORA_ERR_CUDA;
+  if (r_a < r && cudaMemsetAsync(B + static_cast<size_t>(r_a) * d_out * es, 0,
+                                 static_cast<size_t>(r - r_a) * d_out * es, st) != cudaSuccess)
+    return LORA_ERR_CUDA;
+  if (scale != nullptr) return from_cuda(launch_set_scale(scale, slot, s, st));
+  return LORA_OK;
+}
+
 lora_status_t lora_get_error(void* ws, void* stream, int32_t* device_err) {
   if (ws == nullptr || device_err == nullptr || !aligned16(ws)) return LORA_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

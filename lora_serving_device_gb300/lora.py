@@ -28,6 +28,7 @@ EXPORTS = ("lora_workspace_bytes", "lora_build_segments", "lora_bgmv_shrink", "l
            "lora_sgmv_shrink", "lora_sgmv_expand", "lora_linear_fused", "lora_base_gemm_expand",
            "lora_linear_fused_noalloc", "lora_bgmv_delta", "lora_bgmv_adapter",
            "lora_bgmv_adapter_merge", "lora_base_gemm_splitk", "lora_decode_split",
+           "lora_slot_upload",
            "lora_get_error", "lora_status_string")
 
 
@@ -58,6 +59,8 @@ _SIGS = {
                                      _Z, _P]),
     "lora_base_gemm_splitk": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _Z, _P]),
     "lora_decode_split": (_I, [_I, _I, _I]),
+    "lora_slot_upload": (_I, [_P, _P, _P, _I, _P, _P, ctypes.c_float, _I, _I, _I, _I, _I, _I,
+                              _P]),
     "lora_get_error": (_I, [_P, _P, ctypes.POINTER(ctypes.c_int32)]),
     "lora_status_string": (ctypes.c_char_p, [_I]),
 }
@@ -160,6 +163,12 @@ def lora_base_gemm_splitk(x, W0, partial, T, d_in, d_out, ksplit, dt, ws, ws_byt
 
 def lora_decode_split(T, d_in, d_out):
     return _call("lora_decode_split", T, d_in, d_out)
+
+
+def lora_slot_upload(A_pool, B_pool, scale, slot, A_host, B_host, s, d_in, d_out, r, r_a, n_slots,
+                     dt, stream):
+    return _call("lora_slot_upload", A_pool, B_pool, scale, slot, A_host, B_host, s, d_in, d_out, r,
+                 r_a, n_slots, dt, stream)
 
 
 def lora_get_error(ws, stream):
@@ -317,6 +326,19 @@ def bgmv_adapter_t(x, A_pool, B_pool, slot_ids, scale, ws, delta=None, stream=No
                             _stream(stream)),
           "lora_bgmv_adapter")
     return delta
+
+
+def slot_upload_t(A_pool, B_pool, scale, slot, A_host, B_host, s, stream=None):
+    """Upload one adapter (host tensors A [d_in, r_a], B [r_a, d_out], pinned for overlap)
+    into pool slot `slot`, zero-padded to the pool rank; scale[slot] = s."""
+    n_slots, d_in, r = A_pool.shape
+    d_out = B_pool.shape[2]
+    r_a = A_host.shape[1]
+    assert A_host.is_contiguous() and B_host.is_contiguous() and B_host.shape == (r_a, d_out)
+    check(lora_slot_upload(_ptr(A_pool), _ptr(B_pool), _ptr(scale), slot, _ptr(A_host),
+                           _ptr(B_host), float(s), d_in, d_out, r, r_a, n_slots, _dt(A_pool),
+                           _stream(stream)),
+          "lora_slot_upload")
 
 
 def base_gemm_splitk_t(x, W0, ws, ksplit=None, partial=None, stream=None):

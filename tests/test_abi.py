@@ -29,7 +29,7 @@ def test_header_declares_the_boundary():
     for n in ("lora_build_segments", "lora_bgmv_shrink", "lora_bgmv_expand", "lora_sgmv_shrink",
               "lora_sgmv_expand", "lora_linear_fused", "lora_base_gemm_expand",
               "lora_bgmv_delta", "lora_bgmv_adapter", "lora_bgmv_adapter_merge",
-              "lora_base_gemm_splitk", "lora_decode_split",
+              "lora_base_gemm_splitk", "lora_decode_split", "lora_slot_upload",
               "lora_workspace_bytes", "lora_get_error",
               "lora_status_string"):
         assert n in names
@@ -109,9 +109,23 @@ def test_validation_paths(L):
                                      64, 16, 4, 0, ws, 16, None) == 2
 
 
+def test_slot_upload_validation(L):
+    up = L.lora_slot_upload
+    # (A_pool, B_pool, scale, slot, A_host, B_host, s, d_in, d_out, r, r_a, n_slots, dt, stream)
+    assert up(FAKE, FAKE, None, 4, FAKE, FAKE, 2.0, 64, 64, 16, 8, 4, 0, None) == 2    # slot
+    assert up(FAKE, FAKE, None, -1, FAKE, FAKE, 2.0, 64, 64, 16, 8, 4, 0, None) == 2
+    assert up(FAKE, FAKE, None, 0, FAKE, FAKE, 2.0, 64, 64, 16, 17, 4, 0, None) == 2   # r_a > r
+    assert up(FAKE, FAKE, None, 0, FAKE, FAKE, 2.0, 64, 64, 16, 0, 4, 0, None) == 2
+    assert up(FAKE, FAKE, None, 0, FAKE, FAKE, 2.0, 64, 64, 12, 8, 4, 0, None) == 2    # rank
+    assert up(FAKE, FAKE, None, 0, None, FAKE, 2.0, 64, 64, 16, 8, 4, 0, None) == 1    # null
+    assert up(FAKE + 2, FAKE, None, 0, FAKE, FAKE, 2.0, 64, 64, 16, 8, 4, 0, None) == 1
+    assert up(FAKE, FAKE, None, 0, FAKE, FAKE, 2.0, 64, 64, 16, 8, 4, 7, None) == 3    # dtype
+
+
 def test_decode_split_is_a_function_of_the_shapes(L):
     assert L.lora_decode_split(64, 4096, 4096) == 4       # 32 column tiles x 4 = 128 CTAs
-    assert L.lora_decode_split(256, 4096, 4096) == 2      # 2 token tiles
+    assert L.lora_decode_split(256, 4096, 4096) == 4      # one 256-token tile
+    assert L.lora_decode_split(100, 4096, 4096) == 4      # one 128-token tile
     assert L.lora_decode_split(1, 64, 128) == 1           # one K block
     assert L.lora_decode_split(0, 4096, 4096) == 0
     assert L.lora_decode_split(257, 4096, 4096) == 0

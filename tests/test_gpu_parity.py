@@ -465,3 +465,49 @@ def test_base_gemm_expand_matches_oracle(L, case):
     y0 = L.base_gemm_expand_t(d0.x, d0.W0, d0.B, d0.ids, dev(vp, "f32"), ws)
     torch.cuda.synchronize()
     check_close_bf16_out(host(y0), ref - base, "folded expand alone")
+
+
+# ------------------------------------------------------------- slot upload
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_slot_upload_then_layer_matches_oracle(L, dt):
+    """A rank-8 adapter uploaded from pinned host memory into slot 3 of a
+    rank-16 pool: the slot holds it zero-padded (bit-exact copy), the other
+    slots are untouched, and the layer over tokens that use the slot matches
+    the oracle (decode and prefill paths for bf16)."""
+    torch = torch_mod()
+    n_slots, d_in, d_out, r, r_a, slot, s = 6, 256, 264, 16, 8, 3, 1.75
+    w = W.random_case(760, 300, d_in, d_out, r, n_slots, runs=True, bf16=(dt == "bf16"))
+    d = DeviceCase(w)
+    rng = np.random.default_rng([7004])
+    A_a = (rng.standard_normal((d_in, r_a)) / 16).astype(np.float32)
+    B_a = (rng.standard_normal((r_a, d_out)) * 0.02).astype(np.float32)
+    if dt == "bf16":
+        A_a, B_a = W.bf16_round(A_a), W.bf16_round(B_a)
+    tdt = torch.bfloat16 if dt == "bf16" else torch.float32
+    A_h = torch.from_numpy(A_a).to(tdt).pin_memory()
+    B_h = torch.from_numpy(B_a).to(tdt).pin_memory()
+    A_before, B_before = host(d.A).copy(), host(d.B).copy()
+    L.slot_upload_t(d.A, d.B, d.scale, slot, A_h, B_h, s)
+    torch.cuda.synchronize()
+    A_after, B_after = host(d.A), host(d.B)
+    assert np.array_equal(A_after[slot, :, :r_a], A_a) and not A_after[slot, :, r_a:].any()
+    assert np.array_equal(B_after[slot, :r_a, :], B_a) and not B_after[slot, r_a:, :].any()
+    others = [i for i in range(n_slots) if i != slot]
+    assert np.array_equal(A_after[others], A_before[others])
+    assert np.array_equal(B_after[others], B_before[others])
+    assert float(d.scale[slot].item()) == s
+    A_pool, B_pool, scale = w.A_pool.copy(), w.B_pool.copy(), w.scale.copy()
+    A_pool[slot] = 0
+    B_pool[slot] = 0
+    A_pool[slot, :, :r_a] = A_a
+    B_pool[slot, :r_a, :] = B_a
+    scale[slot] = s
+    ids = w.slot_ids.copy()
+    ids[::3] = slot                                     # a third of the rows use the slot
+    for T in (64, 300) if dt == "bf16" else (53,):
+        ids_t = torch.from_numpy(ids[:T].astype(np.int32)).cuda()
+        ws = L.workspace(L.OP_LINEAR_FUSED, T, d_in, d_out, r, n_slots)
+        y = L.linear_fused_t(d.x[:T].contiguous(), d.W0, d.A, d.B, ids_t, d.scale, ws)
+        torch.cuda.synchronize()
+        ref = O.lora_linear(w.x[:T], w.W0, A_pool, B_pool, scale, ids[:T])
+        check_close(host(y), ref, f"layer after upload, T={T}")
