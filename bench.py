@@ -423,6 +423,68 @@ def decode_blocks(sets, L, w, stream, pk, n_steps=400):
             "bgmv_adapter": block_row(graph_mean_ms(adapter, n_steps, stream), b_adapter, pk)}
 
 
+def upload_point(L, sets, w, stream, n_steps=500, rounds=16):
+    """The slot-upload path (lora_slot_upload) from pinned host memory: its
+    H2D rate alone, and while the decode layer runs on another stream, with
+    the layer's time per step alone and with the uploads running (the
+    uploads go to slots the batch does not use)."""
+    import numpy as np
+    import torch
+    T, d_in, d_out, r, n_slots = w.T, w.d_in, w.d_out, w.r, w.n_slots
+    used = set(int(i) for i in w.slot_ids.tolist())
+    free = [sl for sl in range(n_slots) if sl not in used][:64]
+    g = torch.Generator().manual_seed(1002)
+    A_h = (torch.randn((d_in, r), generator=g) / 64).to(torch.bfloat16).pin_memory()
+    B_h = (torch.randn((r, d_out), generator=g) * 0.02).to(torch.bfloat16).pin_memory()
+    per = (d_in * r + r * d_out) * 2
+    side = torch.cuda.Stream(device=sets[0].x.device)
+    pool = sets[1]     # the other sets keep their own pools
+
+    def uploads():
+        for _ in range(rounds):
+            for sl in free:
+                L.slot_upload_t(pool.A, pool.B, None, sl, A_h, B_h, 2.0, stream=side)
+
+    nbytes = per * len(free) * rounds
+    uploads()                               # warm
+    side.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(side)
+    uploads()
+    e1.record(side)
+    side.synchronize()
+    alone_ms = e0.elapsed_time(e1)
+    ws = L.workspace(L.OP_LINEAR_FUSED, T, d_in, d_out, r, n_slots, device=sets[0].x.device)
+
+    def step(i):
+        s = sets[[0, 2, 3][i % 3]]
+        L.linear_fused_t(s.x, s.W0, s.A, s.B, s.ids, s.scale, ws, y=s.y, stream=stream)
+
+    layer_ms = graph_mean_ms(step, n_steps, stream)
+    gr = capture(step, n_steps, stream)
+    torch.cuda.synchronize()
+    f0 = torch.cuda.Event(enable_timing=True)
+    f1 = torch.cuda.Event(enable_timing=True)
+    u0 = torch.cuda.Event(enable_timing=True)
+    u1 = torch.cuda.Event(enable_timing=True)
+    u0.record(side)
+    uploads()
+    u1.record(side)
+    f0.record(stream)
+    with torch.cuda.stream(stream):
+        gr.replay()
+    f1.record(stream)
+    torch.cuda.synchronize()
+    both_ms = f0.elapsed_time(f1) / n_steps
+    up_ms = u0.elapsed_time(u1)
+    return {"adapter_bytes": per, "uploads": len(free) * rounds,
+            "upload_gbs": nbytes / (alone_ms * 1e-3) / 1e9,
+            "upload_gbs_during_layer": nbytes / (up_ms * 1e-3) / 1e9,
+            "layer_us": layer_ms * 1e3, "layer_us_during_upload": both_ms * 1e3,
+            "overlap_ms": min(up_ms, both_ms * n_steps)}
+
+
 def e2e_steps(s0, L, T, d_in, d_out, r, n_slots, n_steps, stream):
     """The public call with host buffers: H2D of x and ids from pinned memory,
     the layer, D2H of y -- every step inside the timed region."""
@@ -697,6 +759,7 @@ def run_ours(args):
         "kernels_ms": kt, "blocks": blocks,
         "clocks": clk.summary(),
     }
+    line["slot_upload"] = upload_point(L, sets, w, stream)
     if not args.no_sweep:
         line["sweep"] = sweep(L, stream, pk, dev)
     cfgs = {}
