@@ -90,12 +90,22 @@ __device__ __forceinline__ void store_group(const float (&o)[8], int g, int h, i
 #pragma unroll
   for (int k = 0; k < 4; ++k) f[k] = h ? o[4 + k] : o[k];
   if (MERGE) {
-    for (int zz = 0; zz < S; ++zz) {
-      const float4 pz = ld_dep_f4(partial + (static_cast<size_t>(zz) * T + t) * d_out + n);
-      f[0] += pz.x;
-      f[1] += pz.y;
-      f[2] += pz.z;
-      f[3] += pz.w;
+    // the partials' loads go out together, then they are added in split order
+    constexpr int kBatch = 8;
+    for (int z0 = 0; z0 < S; z0 += kBatch) {
+      float4 pz[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u)
+        if (z0 + u < S) pz[u] = ld_dep_f4(partial + (static_cast<size_t>(z0 + u) * T + t) * d_out + n);
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        if (z0 + u < S) {
+          f[0] += pz[u].x;
+          f[1] += pz[u].y;
+          f[2] += pz[u].z;
+          f[3] += pz[u].w;
+        }
+      }
     }
     uint2 pk;
     pk.x = pack_bf16x2(f[0], f[1]);
@@ -189,15 +199,20 @@ __global__ void __launch_bounds__(kAdThreads)
     ptx::cluster_arrive_release();
     ptx::cluster_wait_acquire();
     if (tid < R) {
+      // the C remote reads go out together, then they are added in rank order
       const uint32_t local = ptx::smem_u32(&pv[tid]);
-      float a = 0.f;
-      for (int src = 0; src < C; ++src) {
-        float v;
-        asm volatile("ld.shared::cluster.f32 %0, [%1];"
-                     : "=f"(v)
-                     : "r"(ptx::mapa_shared(local, static_cast<uint32_t>(src))));
-        a += v;
+      float pr[8];
+#pragma unroll
+      for (int src = 0; src < 8; ++src) {
+        if (src < C)
+          asm volatile("ld.shared::cluster.f32 %0, [%1];"
+                       : "=f"(pr[src])
+                       : "r"(ptx::mapa_shared(local, static_cast<uint32_t>(src))));
       }
+      float a = 0.f;
+#pragma unroll
+      for (int src = 0; src < 8; ++src)
+        if (src < C) a += pr[src];
       vs[tid] = a * (scale ? scale[id] : 1.f);
     }
     __syncthreads();

@@ -51,7 +51,7 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s; the longest legitimate
 
 struct TcParams {
   int T, d_in, d_out, r, n_slots;
-  int n_kblk;    // ceil(d_in / 64)
+  int n_kblk;    // base stages: ceil(d_in / (64 * KS))
   int stages;
   int box_rows;  // rows of one B_pool TMA box: min(r, 32)
   int lg_box;    // log2(box_rows)
@@ -64,17 +64,22 @@ struct TcParams {
 };
 
 struct SmemLayout {
-  uint32_t x_bytes, stage_bytes, stages_total;
+  uint32_t x_sub, x_bytes, w_box, stage_bytes, stages_total;
   uint32_t vt, tok, uniq, bitmap, bars, misc, total;
 };
 
 // Offsets from a 1024-byte aligned base (the 128-byte swizzle repeats every
 // 8 rows = 1024 bytes, and TMA / MMA agree on it only from such a base).
-template <int BT, int BN>
+// A base stage carries KS 64-deep K blocks: KS x boxes of 64 x BT and BN/64
+// W0 boxes of 64 columns x 64*KS rows (taller boxes move more bytes per TMA
+// operation).  A LoRA stage uses the first K block only.
+template <int BT, int BN, int KS>
 __host__ __device__ inline SmemLayout smem_layout(int stages, int r, int n_slots) {
   SmemLayout L;
-  L.x_bytes = BT * 128;
-  L.stage_bytes = L.x_bytes + (BN / 64) * 8192;
+  L.x_sub = BT * 128;
+  L.x_bytes = KS * L.x_sub;
+  L.w_box = KS * 8192;
+  L.stage_bytes = L.x_bytes + (BN / 64) * L.w_box;
   L.stages_total = static_cast<uint32_t>(stages) * L.stage_bytes;
   uint32_t o = L.stages_total;
   L.vt = o;
@@ -90,7 +95,7 @@ __host__ __device__ inline SmemLayout smem_layout(int stages, int r, int n_slots
   L.bars = o;
   o += (2 * stages + 2) * 8;
   L.misc = o;
-  o += 16;
+  o += 32;  // TMEM address, adapter count, abort flag, then one byte per stage: its K blocks
   L.total = o;
   return L;
 }
@@ -114,7 +119,7 @@ __device__ __forceinline__ void named_arrive(int id, int n) {
   asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
-template <int BT, int BN>
+template <int BT, int BN, int KS>
 __global__ void __launch_bounds__(kThreads, 1)
     fused_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                     const __grid_constant__ CUtensorMap tm_b, const TcParams p) {
@@ -129,7 +134,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  const SmemLayout L = smem_layout<BT, BN>(p.stages, p.r, p.n_slots);
+  const SmemLayout L = smem_layout<BT, BN, KS>(p.stages, p.r, p.n_slots);
   float* vt = reinterpret_cast<float*>(smem + L.vt);
   int* tok = reinterpret_cast<int*>(smem + L.tok);
   int* uniq = reinterpret_cast<int*>(smem + L.uniq);
@@ -141,6 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc);
   int* n_uniq_s = reinterpret_cast<int*>(smem + L.misc + 4);
   volatile int* abort_f = reinterpret_cast<volatile int*>(smem + L.misc + 8);
+  uint8_t* stage_kblocks = smem + L.misc + 16;  // K blocks the stage in each ring slot holds
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // tile order: panels of kPanel column tiles; within a panel the column
@@ -215,11 +221,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint8_t* X = smem + static_cast<size_t>(st) * L.stage_bytes;
       uint8_t* Wr = X + L.x_bytes;
       if (lane == 0) {
+        stage_kblocks[st] = KS;
         ptx::mbar_arrive_expect_tx(&full[st], L.stage_bytes);
-        ptx::tma_load_2d(X, &tm_x, &full[st], kb * kBK, t0);
+#pragma unroll
+        for (int j = 0; j < KS; ++j)
+          ptx::tma_load_2d(X + j * L.x_sub, &tm_x, &full[st], (kb * KS + j) * kBK, t0);
 #pragma unroll
         for (int h = 0; h < kWBoxes; ++h)
-          ptx::tma_load_2d(Wr + h * 8192, &tm_w, &full[st], n0 + 64 * h, kb * kBK);
+          ptx::tma_load_2d(Wr + h * L.w_box, &tm_w, &full[st], n0 + 64 * h, kb * KS * kBK);
       }
       __syncwarp();
     };
@@ -243,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = lane; e < 2 * per_half * kWBoxes; e += 32) {
           const int hb = e / (2 * per_half), rem = e % (2 * per_half);
           const int half = rem / per_half, rr = rem % per_half;
-          *reinterpret_cast<uint4*>(Wr + hb * 8192 + (half * (kBK / 2) + used + rr / 8) * 128 +
+          *reinterpret_cast<uint4*>(Wr + hb * L.w_box + (half * (kBK / 2) + used + rr / 8) * 128 +
                                     (rr % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
         }
       }
@@ -282,9 +291,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ptx::fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0)
+      if (lane == 0) {
+        stage_kblocks[st] = 1;
         ptx::mbar_arrive_expect_tx(
             &full[st], static_cast<uint32_t>(2 * n_units * p.box_rows * 128 * kWBoxes));
+      }
       __syncwarp();
       // one B box per lane: (unit, 64-column box, hi/lo copy)
       if (lane < 2 * n_units * kWBoxes) {
@@ -293,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int wv = u_first + u;
         const int a = uniq[wv >> p.lg_upa];
         const int qb = (wv & (upa - 1)) << p.lg_box;
-        ptx::tma_load_2d(Wr + hb * 8192 + (half * (kBK / 2) + u * p.box_rows) * 128, &tm_b,
+        ptx::tma_load_2d(Wr + hb * L.w_box + (half * (kBK / 2) + u * p.box_rows) * 128, &tm_b,
                          &full[st], n0 + 64 * hb, a * p.r + qb);
       }
       __syncwarp();
@@ -342,15 +353,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_after();
         const uint32_t xa = ptx::smem_u32(smem + static_cast<size_t>(st) * L.stage_bytes);
         const uint32_t wa = xa + L.x_bytes;
+        const int nkb = stage_kblocks[st];  // written by the producer before its arrive
 #pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk) {
-          // K-major x / V: advance 16 elements = 32 bytes inside the swizzle row
-          const uint64_t xd = ptx::sdesc_sw128(xa + kk * 32, 16, 1024);
-          // MN-major W0 / B: advance 16 K-rows = 2048 bytes; 64-column boxes
-          // are 8 KiB apart (LBO), 8-row groups 1 KiB apart (SBO)
-          const uint64_t wd = ptx::sdesc_sw128(wa + kk * 2048, 8192, 1024);
-          const uint32_t accum = (it > 0 || kk > 0) ? 1u : 0u;
-          ptx::mma_bf16(tmem, xd, wd, kIdesc, accum);
+        for (int j = 0; j < KS; ++j) {
+          if (j >= nkb) break;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            // K-major x / V: advance 16 elements = 32 bytes inside the swizzle row
+            const uint64_t xd = ptx::sdesc_sw128(xa + j * L.x_sub + kk * 32, 16, 1024);
+            // MN-major W0 / B: advance 16 K-rows = 2048 bytes; the 64-column
+            // boxes are w_box apart (LBO), 8-row groups 1 KiB apart (SBO)
+            const uint64_t wd = ptx::sdesc_sw128(wa + (j * kBK + kk * 16) * 128, L.w_box, 1024);
+            const uint32_t accum = (it > 0 || j > 0 || kk > 0) ? 1u : 0u;
+            ptx::mma_bf16(tmem, xd, wd, kIdesc, accum);
+          }
         }
         ptx::mma_commit(&empty[st]);
         return true;
@@ -562,35 +578,36 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, 
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BT, int BN>
+// Deepest pipeline that fits next to the v tile and bookkeeping, and that
+// can hold the staged fp32 accumulator afterwards (0: none fits).
+template <int BT, int BN, int KS>
+int pick_stages(const TcParams& prm, size_t cap) {
+  const size_t red_bytes = static_cast<size_t>(BT) * (BN + kRedPad) * 4;
+  for (int s = 8; s >= 2; --s) {
+    const SmemLayout L = smem_layout<BT, BN, KS>(s, prm.r, prm.n_slots);
+    if (L.total + 1024 <= cap && L.stages_total >= red_bytes) return s;
+  }
+  return 0;
+}
+
+template <int BT, int BN, int KS>
 cudaError_t launch_variant(const void* x, const void* W0, const void* B, TcParams prm,
                            int tiles_n, int tiles_t, int S, cudaStream_t st,
                            const DeviceInfo& dev) {
-  // deepest pipeline that fits next to the v tile and bookkeeping, and that
-  // can hold the staged fp32 accumulator afterwards
-  const size_t cap = dev.max_smem_optin;
-  const size_t red_bytes = static_cast<size_t>(BT) * (BN + kRedPad) * 4;
-  int stages = 0;
-  for (int s = 8; s >= 2; --s) {
-    const SmemLayout L = smem_layout<BT, BN>(s, prm.r, prm.n_slots);
-    if (L.total + 1024 <= cap && L.stages_total >= red_bytes) {
-      stages = s;
-      break;
-    }
-  }
+  const int stages = pick_stages<BT, BN, KS>(prm, dev.max_smem_optin);
   if (stages == 0) return cudaErrorInvalidConfiguration;
   prm.stages = stages;
-  const SmemLayout L = smem_layout<BT, BN>(stages, prm.r, prm.n_slots);
+  const SmemLayout L = smem_layout<BT, BN, KS>(stages, prm.r, prm.n_slots);
   const size_t smem = L.total + 1024;
 
   CUtensorMap tm_x, tm_w, tm_b;
   if (!make_map(&tm_x, x, prm.d_in, prm.T, prm.d_in, kBK, BT) ||
-      !make_map(&tm_w, W0, prm.d_out, prm.d_in, prm.d_out, 64, kBK) ||
+      !make_map(&tm_w, W0, prm.d_out, prm.d_in, prm.d_out, 64, KS * kBK) ||
       !make_map(&tm_b, B, prm.d_out, static_cast<uint64_t>(prm.n_slots) * prm.r, prm.d_out, 64,
                 prm.box_rows))
     return cudaErrorInvalidValue;
 
-  auto kern = fused_tc_kernel<BT, BN>;
+  auto kern = fused_tc_kernel<BT, BN, KS>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
@@ -663,7 +680,10 @@ cudaError_t launch_fused_tc(const void* x, const void* W0, const void* B, const 
   prm.d_out = d_out;
   prm.r = r;
   prm.n_slots = n_slots;
-  prm.n_kblk = (d_in + kBK - 1) / kBK;
+  // two 64-deep K blocks per base stage when the ring still holds two such
+  // stages next to the v tile (rank <= 64); one otherwise
+  const int KS = pick_stages<128, 256, 2>(prm, dev.max_smem_optin) > 0 ? 2 : 1;
+  prm.n_kblk = (d_in + KS * kBK - 1) / (KS * kBK);
   prm.stages = 0;
   prm.box_rows = r < 32 ? r : 32;
   prm.lg_box = 31 - __builtin_clz(static_cast<unsigned>(prm.box_rows));
@@ -687,7 +707,8 @@ cudaError_t launch_fused_tc(const void* x, const void* W0, const void* B, const 
   const int tiles_n = (d_out + 255) / 256;
   const int tiles_t = (T + 127) / 128;
   const int S = pick_split(tiles_n * tiles_t);
-  return launch_variant<128, 256>(x, W0, B, prm, tiles_n, tiles_t, S, st, dev);
+  if (KS == 2) return launch_variant<128, 256, 2>(x, W0, B, prm, tiles_n, tiles_t, S, st, dev);
+  return launch_variant<128, 256, 1>(x, W0, B, prm, tiles_n, tiles_t, S, st, dev);
 }
 
 }  // namespace lora

@@ -369,15 +369,18 @@ __global__ void __launch_bounds__(kThreads)
   } else {
     // V tile: row i = token perm[p0 + i]; v summed over the d_in splits,
     // split into bf16 hi + lo, written K-major with the 128-byte swizzle
+    // (plain loads: this kernel is not launched early, so stream order makes
+    // v visible, and the compiler may batch them)
     const int i = tid;
     if (i < n_tok) {
-      const int tok = ld_dep(perm + p0 + i);
-#pragma unroll 1
+      const int tok = perm[p0 + i];
+#pragma unroll 2
       for (int q0 = 0; q0 < R; q0 += 8) {
         float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         for (int sp = 0; sp < ksplit; ++sp) {
-          const float* vp = vpart + (static_cast<size_t>(sp) * T + tok) * R + q0;
-          const float4 u0 = ld_dep_f4(vp), u1 = ld_dep_f4(vp + 4);
+          const float4* vp =
+              reinterpret_cast<const float4*>(vpart + (static_cast<size_t>(sp) * T + tok) * R + q0);
+          const float4 u0 = vp[0], u1 = vp[1];
           f[0] += u0.x; f[1] += u0.y; f[2] += u0.z; f[3] += u0.w;
           f[4] += u1.x; f[5] += u1.y; f[6] += u1.z; f[7] += u1.w;
         }
