@@ -640,8 +640,10 @@ def prefill_point(L, stream, pk, dev, steps=30, warm=5):
     return res
 
 
-def stack_point(L, stream, pk, dev, steps=5, warm=3):
-    """The 8B-shaped stack: 32 layers x 7 projections, one fused call each."""
+def stack_point(L, stream, pk, dev, steps=5, warm=3, ragged=False):
+    """The 8B-shaped stack: 32 layers x 7 projections, one fused call each.
+    ragged: every adapter kept at its own rank (8, 16 or 64) in a ragged pool
+    instead of zero-padded to 64."""
     import numpy as np
     import torch
     from lora_serving_device_gb300 import workloads as W
@@ -654,22 +656,36 @@ def stack_point(L, stream, pk, dev, steps=5, warm=3):
         for p in range(7):
             t = W.stack_layer_device(layer, p, device=dev, ranks=ranks)
             _, d_in, d_out = W.STACK_PROJECTIONS[p]
+            pool = None
+            if ragged:
+                pool = L.RaggedPool.from_padded(t.pop("A_pool"), t.pop("B_pool"), ranks)
             ws = L.workspace(L.OP_LINEAR_FUSED, 256, d_in, d_out, 64, 250)
             y = torch.empty((256, d_out), dtype=torch.bfloat16, device=dev)
-            layers.append((t, ws, y))
+            layers.append((t, pool, ws, y))
 
     def fn(i):
-        for t, ws, y in layers:
-            L.linear_fused_t(t["x"], t["W0"], t["A_pool"], t["B_pool"], ids, scale, ws, y=y,
-                             stream=stream)
+        for t, pool, ws, y in layers:
+            if pool is None:
+                L.linear_fused_t(t["x"], t["W0"], t["A_pool"], t["B_pool"], ids, scale, ws, y=y,
+                                 stream=stream)
+            else:
+                L.linear_fused_ragged_t(t["x"], t["W0"], pool, ids, scale, ws, y=y,
+                                        stream=stream)
 
     ms, _ = timed_graph_steps(fn, steps, warm, stream)
     t = ms / 1e3 / steps
-    D = int(np.unique(ids_np[ids_np >= 0]).size)
-    nbytes = sum(layer_bytes(256, di, do, 64, D) for _, di, do in W.STACK_PROJECTIONS) * W.STACK_LAYERS
-    res = {"workload": "stack_8b: 32 layers x 7 projections, 250 slots (ranks 8/16/64 padded "
-                       "to 64), T=256", "distinct": D, "ms_per_step": t * 1e3,
-           "tokens_per_s": 256 / t, "gbs": nbytes / t / 1e9, "frac": nbytes / t / 1e9 / pk["hbm_gbs"]}
+    used = np.unique(ids_np[ids_np >= 0])
+    D = int(used.size)
+    # each distinct adapter's A and B once, at the rank the pool stores it
+    rank_sum = int(sum(int(ranks[a]) for a in used)) if ragged else 64 * D
+    nbytes = sum((di * do + rank_sum * (di + do) + 256 * (di + do)) * 2 + 256 * 4
+                 for _, di, do in W.STACK_PROJECTIONS) * W.STACK_LAYERS
+    form = "ranks 8/16/64 each at its own rank (ragged pool)" if ragged else \
+        "ranks 8/16/64 padded to 64"
+    res = {"workload": f"stack_8b: 32 layers x 7 projections, 250 slots ({form}), T=256",
+           "distinct": D, "adapter_rank_sum": rank_sum, "ms_per_step": t * 1e3,
+           "tokens_per_s": 256 / t, "gbs": nbytes / t / 1e9,
+           "frac": nbytes / t / 1e9 / pk["hbm_gbs"]}
     del layers
     torch.cuda.empty_cache()
     return res
@@ -767,6 +783,7 @@ def run_ours(args):
         cfgs["prefill_sgmv"] = prefill_point(L, stream, pk, dev)
     if args.stack:
         cfgs["stack_8b"] = stack_point(L, stream, pk, dev)
+        cfgs["stack_8b_ragged"] = stack_point(L, stream, pk, dev, ragged=True)
     if cfgs:
         line["configs"] = cfgs
     if world == 1 and not args.no_cpu:

@@ -89,6 +89,7 @@ typedef enum {
 /* device error word bits */
 #define LORA_DEVERR_BAD_SLOT 0x1u /* a slot id outside [-1, n_slots) was read   */
 #define LORA_DEVERR_TIMEOUT 0x2u  /* a bounded on-chip wait gave up (no hang)   */
+#define LORA_DEVERR_BAD_RANK 0x4u /* a ragged-pool entry (rank, offsets) read was out of range */
 
 #define LORA_MAX_SLOTS 16384
 #define LORA_MAX_TOKENS (1 << 20)
@@ -313,6 +314,54 @@ lora_status_t lora_linear_fused_noalloc(const void* x, const void* W0, const voi
                                         const float* scale, void* y, int32_t T, int32_t d_in,
                                         int32_t d_out, int32_t r, int32_t n_slots,
                                         lora_dtype_t dt, void* stream);
+
+/*
+ * Ragged-rank adapter pools: each adapter keeps its own rank instead of being
+ * zero-padded to the largest one ("Serving Many LoRA Adapters", section
+ * "When It Falls Down": padding a rank-4 adapter to rank 64 costs 16x on its
+ * term; "Serving multiple LoRAs ...", Exercise 2: kernels that take
+ * variable ranks; "Serving many LoRA adapters", section "Batching across
+ * different adapters": mixed ranks need ragged indexing or padding).
+ *   A_flat, B_flat  bf16, flat.  Slot a holds A_a [d_in, rank[a]] row-major at
+ *                   A_flat + a_off[a] and B_a [rank[a], d_out] row-major at
+ *                   B_flat + b_off[a] (offsets in elements).
+ *   a_off, b_off    [n_slots] int64, device; multiples of 8 (16-byte rows).
+ *   rank            [n_slots] int32, device; each one of 8, 16, 32, 64, 128
+ *                   and <= r_max.  An adapter of another rank is stored
+ *                   zero-padded to the next of these (at most 2x its own
+ *                   bytes, where padding to the largest rank costs up to 16x).
+ *   a_elems, b_elems  the lengths of A_flat and B_flat in elements.
+ *   r_max           one of 8, 16, 32, 64, 128: the largest rank allowed.
+ * Each token costs its own adapter's rank: the kernel runs the body compiled
+ * for that rank, so nothing of the larger ranks in the pool is read.  A slot entry
+ * outside these rules (or one that would read past a pool's end) is not read:
+ * LORA_DEVERR_BAD_RANK is set in the workspace error word and the token is
+ * treated as base-only.  The results equal those of the zero-padded pool.
+ *
+ * lora_bgmv_adapter_ragged: the adapter term only, as lora_bgmv_adapter
+ * (fp32 delta [T, d_out], base-only rows not written; T <= 65535; workspace:
+ * the error word).  lora_linear_fused_ragged: the whole layer for decode-sized batches
+ * (T <= 256), as lora_linear_fused's bf16 decode path (the split-K base
+ * GEMM, then the merge kernel over the ragged pool, with the same
+ * programmatic overlap rules); workspace: lora_workspace_bytes
+ * (LORA_OP_LINEAR_FUSED, T, d_in, d_out, r_max, n_slots); T > 256 gives
+ * LORA_ERR_SHAPE.  Both: bf16 only; LORA_ERR_INVALID_ARG for a null pointer,
+ * a pool, x or output not 16-byte aligned, or a negative pool length.
+ */
+lora_status_t lora_bgmv_adapter_ragged(const void* x, const void* A_flat, const void* B_flat,
+                                       const int64_t* a_off, const int64_t* b_off,
+                                       const int32_t* rank, int64_t a_elems, int64_t b_elems,
+                                       int32_t r_max, const int32_t* slot_ids,
+                                       const float* scale, float* delta, int32_t T,
+                                       int32_t d_in, int32_t d_out, int32_t n_slots,
+                                       lora_dtype_t dt, void* ws, size_t ws_bytes, void* stream);
+lora_status_t lora_linear_fused_ragged(const void* x, const void* W0, const void* A_flat,
+                                       const void* B_flat, const int64_t* a_off,
+                                       const int64_t* b_off, const int32_t* rank,
+                                       int64_t a_elems, int64_t b_elems, int32_t r_max,
+                                       const int32_t* slot_ids, const float* scale, void* y,
+                                       int32_t T, int32_t d_in, int32_t d_out, int32_t n_slots,
+                                       lora_dtype_t dt, void* ws, size_t ws_bytes, void* stream);
 
 /*
  * Uploads one adapter into pool slot `slot` (the data path of adapter

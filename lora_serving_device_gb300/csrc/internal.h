@@ -76,6 +76,27 @@ cudaError_t launch_bgmv_adapter_merge(const void* x, const void* A, const void* 
                                       const float* partial, int S, void* y, int T, int d_in,
                                       int d_out, int r, int n_slots, uint32_t* err, bool pdl,
                                       cudaStream_t st);
+// Ragged adapter pool: slot a holds A_a [d_in, rank[a]] at A + a_off[a] and
+// B_a [rank[a], d_out] at B + b_off[a] (bf16 elements, row-major); a_elems /
+// b_elems are the pools' lengths, r_max <= 128 the largest rank allowed.
+struct RaggedPool {
+  const int64_t* a_off;
+  const int64_t* b_off;
+  const int32_t* rank;
+  int64_t a_elems, b_elems;
+  int r_max;
+};
+// The two forms above over a ragged pool; a slot whose entry is out of range
+// sets LORA_DEVERR_BAD_RANK and its rows are treated as base-only.
+cudaError_t launch_bgmv_adapter_ragged(const void* x, const void* A, const void* B,
+                                       const RaggedPool& rp, const int32_t* ids,
+                                       const float* scale, float* delta, int T, int d_in,
+                                       int d_out, int n_slots, uint32_t* err, cudaStream_t st);
+cudaError_t launch_bgmv_adapter_ragged_merge(const void* x, const void* A, const void* B,
+                                             const RaggedPool& rp, const int32_t* ids,
+                                             const float* scale, const float* partial, int S,
+                                             void* y, int T, int d_in, int d_out, int n_slots,
+                                             uint32_t* err, bool pdl, cudaStream_t st);
 // BGMV expand into an fp32 term: delta[t, :] = (sum_s vpart[s, t, :]) B[a_t]
 // for tokens with a valid id (other rows untouched); bf16 B.  `pdl`: launch
 // as a programmatic dependent of the shrink just before.

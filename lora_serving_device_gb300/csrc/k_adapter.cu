@@ -60,11 +60,11 @@ __device__ __forceinline__ void expand_group(const bf16* Ba, const float* vs, in
   if (on) {
 #pragma unroll
     for (int j = 0; j < SH::RH; ++j) {
+      const int row = h * SH::RH + j;
       const uint4 w = (PRE && j < SH::kPre)
                           ? pre[j < SH::kPre ? j : 0]
-                          : *reinterpret_cast<const uint4*>(
-                                Ba + static_cast<size_t>(h * SH::RH + j) * d_out + g);
-      const float vq = vs[h * SH::RH + j];
+                          : *reinterpret_cast<const uint4*>(Ba + static_cast<size_t>(row) * d_out + g);
+      const float vq = vs[row];
       const uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -117,32 +117,31 @@ __device__ __forceinline__ void store_group(const float (&o)[8], int g, int h, i
   }
 }
 
-template <int R, bool MERGE>
-__global__ void __launch_bounds__(kAdThreads)
-    bgmv_adapter_kernel(const bf16* __restrict__ x, const bf16* __restrict__ A,
-                        const bf16* __restrict__ B, const int32_t* __restrict__ ids,
-                        const float* __restrict__ scale, const float* partial, int S,
-                        void* out, int T, int d_in, int d_out, int n_slots, int kc, int nc,
-                        uint32_t* err) {
-  using SH = AdapterShape<R>;
-  __shared__ float red[kAdWarps][R];
-  __shared__ float pv[R];  // this CTA's partial, read by the whole cluster
-  __shared__ float vs[R];  // the token's full shrink output, scaled
+// Shared-memory scratch of one CTA, sized for the largest rank it serves.
+template <int RM>
+struct AdapterSmem {
+  float red[kAdWarps * RM];  // per-warp column sums of the shrink
+  float pv[RM];              // this CTA's partial, read by the whole cluster
+  float vs[RM];              // the token's full shrink output, scaled
+};
 
-  pdl_launch_dependents();
+// One token's adapter term at rank R (the whole cluster runs the same R:
+// every CTA reads the same id).  Aa / Ba point at the token's A [d_in, R]
+// and B [R, d_out] (row-major), `s` is its scale.  `valid` false: base-only
+// row (merge form: partials only).  Every CTA of the cluster takes the same
+// branches.
+template <int R, bool MERGE, int RM>
+__device__ __forceinline__ void adapter_token(const bf16* __restrict__ x, const bf16* Aa,
+                                              const bf16* Ba, float s, bool valid,
+                                              const float* partial, int S, void* out, int T,
+                                              int d_in, int d_out, int kc, int nc,
+                                              AdapterSmem<RM>& sm) {
+  using SH = AdapterShape<R>;
   const int c = static_cast<int>(ptx::cluster_ctarank());
   const int C = static_cast<int>(gridDim.x);
   const int t = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int id = ids[t];
-  // every CTA of the cluster reads the same id, so `valid` and everything it
-  // guards (the cluster barriers included) is uniform over the cluster
-  const bool valid = slot_valid(id, n_slots);
-  if (!valid && id != -1 && tid == 0 && c == 0) flag_error(err, LORA_DEVERR_BAD_SLOT);
-  if (!MERGE && !valid) return;  // delta form: base-only rows are not written
-
   const int h = tid & 1, pair = tid >> 1;
   const int n_begin = c * nc, n_end = min(d_out, n_begin + nc);
-  const bf16* Ba = B + static_cast<size_t>(valid ? id : 0) * R * d_out;
   float keep[kKeepGroups][8];
 #pragma unroll
   for (int i = 0; i < kKeepGroups; ++i)
@@ -162,7 +161,7 @@ __global__ void __launch_bounds__(kAdThreads)
     // ---- shrink of this CTA's d_in slice
     const int qc = tid % SH::QC, kl = tid / SH::QC;
     const int k_begin = c * kc, k_end = min(d_in, k_begin + kc);
-    const bf16* Aa = A + static_cast<size_t>(id) * d_in * R + qc * 8;
+    const bf16* Ac = Aa + qc * 8;
     const bf16* xt = x + static_cast<size_t>(t) * d_in;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll 2
@@ -172,7 +171,7 @@ __global__ void __launch_bounds__(kAdThreads)
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         float a[8];
-        load8(Aa + static_cast<size_t>(k + j) * R, a);
+        load8(Ac + static_cast<size_t>(k + j) * R, a);
 #pragma unroll
         for (int q = 0; q < 8; ++q) acc[q] = fmaf(xv[j], a[q], acc[q]);
       }
@@ -185,14 +184,14 @@ __global__ void __launch_bounds__(kAdThreads)
     }
     if (lane < SH::QC) {
 #pragma unroll
-      for (int q = 0; q < 8; ++q) red[warp][lane * 8 + q] = acc[q];
+      for (int q = 0; q < 8; ++q) sm.red[warp * R + lane * 8 + q] = acc[q];
     }
     __syncthreads();
     if (tid < R) {
       float a = 0.f;
 #pragma unroll
-      for (int w = 0; w < kAdWarps; ++w) a += red[w][tid];
-      pv[tid] = a;
+      for (int w = 0; w < kAdWarps; ++w) a += sm.red[w * R + tid];
+      sm.pv[tid] = a;
     }
 
     // ---- sum the C partials in rank order; every CTA gets the same v
@@ -200,7 +199,7 @@ __global__ void __launch_bounds__(kAdThreads)
     ptx::cluster_wait_acquire();
     if (tid < R) {
       // the C remote reads go out together, then they are added in rank order
-      const uint32_t local = ptx::smem_u32(&pv[tid]);
+      const uint32_t local = ptx::smem_u32(&sm.pv[tid]);
       float pr[8];
 #pragma unroll
       for (int src = 0; src < 8; ++src) {
@@ -213,7 +212,7 @@ __global__ void __launch_bounds__(kAdThreads)
 #pragma unroll
       for (int src = 0; src < 8; ++src)
         if (src < C) a += pr[src];
-      vs[tid] = a * (scale ? scale[id] : 1.f);
+      sm.vs[tid] = a * s;
     }
     __syncthreads();
     // done reading the peers' partials; a CTA leaves only after every peer is
@@ -221,13 +220,13 @@ __global__ void __launch_bounds__(kAdThreads)
 
     // ---- expand the first column groups into registers
     if (n_begin < n_end)  // uniform over the CTA
-      expand_group<R, true>(Ba, vs, d_out, g0, h, g0 < n_end, bpre, keep[0]);
+      expand_group<R, true>(Ba, sm.vs, d_out, g0, h, g0 < n_end, bpre, keep[0]);
 #pragma unroll
     for (int i = 1; i < kKeepGroups; ++i) {
       const int base = n_begin + i * kStride;
       if (base < n_end) {  // uniform over the CTA
         const int g = base + pair * kGroupCols;
-        expand_group<R, false>(Ba, vs, d_out, g, h, g < n_end, bpre, keep[i]);
+        expand_group<R, false>(Ba, sm.vs, d_out, g, h, g < n_end, bpre, keep[i]);
       }
     }
   }
@@ -246,11 +245,118 @@ __global__ void __launch_bounds__(kAdThreads)
     float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     if (valid) {
       uint4 none[AdapterShape<R>::kPre];  // not read: PRE is false
-      expand_group<R, false>(Ba, vs, d_out, g, h, g < n_end, none, o);
+      expand_group<R, false>(Ba, sm.vs, d_out, g, h, g < n_end, none, o);
     }
     if (g < n_end) store_group<MERGE>(o, g, h, t, d_out, partial, S, T, out);
   }
   if (valid) ptx::cluster_wait_acquire();
+}
+
+// Padded pool: A [n_slots, d_in, R], B [n_slots, R, d_out].
+template <int R, bool MERGE>
+__global__ void __launch_bounds__(kAdThreads)
+    bgmv_adapter_kernel(const bf16* __restrict__ x, const bf16* __restrict__ A,
+                        const bf16* __restrict__ B, const int32_t* __restrict__ ids,
+                        const float* __restrict__ scale, const float* partial, int S,
+                        void* out, int T, int d_in, int d_out, int n_slots, int kc, int nc,
+                        uint32_t* err) {
+  __shared__ AdapterSmem<R> sm;
+  pdl_launch_dependents();
+  const int c = static_cast<int>(ptx::cluster_ctarank());
+  const int id = ids[blockIdx.y];
+  // every CTA of the cluster reads the same id, so `valid` and everything it
+  // guards (the cluster barriers included) is uniform over the cluster
+  const bool valid = slot_valid(id, n_slots);
+  if (!valid && id != -1 && threadIdx.x == 0 && c == 0) flag_error(err, LORA_DEVERR_BAD_SLOT);
+  if (!MERGE && !valid) return;  // delta form: base-only rows are not written
+  const int a = valid ? id : 0;
+  adapter_token<R, MERGE, R>(x, A + static_cast<size_t>(a) * d_in * R,
+                             B + static_cast<size_t>(a) * R * d_out,
+                             valid && scale ? scale[id] : 1.f, valid, partial, S, out, T, d_in,
+                             d_out, kc, nc, sm);
+}
+
+// Ragged pool: slot a holds A_a [d_in, rank[a]] at A + a_off[a] and B_a
+// [rank[a], d_out] at B + b_off[a] (elements), rank[a] in {8, 16, 32, 64,
+// 128}.  Each token runs the body of its own adapter's rank, so a rank-8
+// adapter costs a rank-8 pass, not one at the pool's largest rank.  (Ranks
+// between these are stored zero-padded to the next one: per-row rank checks
+// inside the body would cost registers and load batching.)
+template <bool MERGE>
+__global__ void __launch_bounds__(kAdThreads)
+    bgmv_adapter_ragged_kernel(const bf16* __restrict__ x, const bf16* __restrict__ A,
+                               const bf16* __restrict__ B, const int64_t* __restrict__ a_off,
+                               const int64_t* __restrict__ b_off,
+                               const int32_t* __restrict__ rank, int64_t a_elems,
+                               int64_t b_elems, int r_max, const int32_t* __restrict__ ids,
+                               const float* __restrict__ scale, const float* partial, int S,
+                               void* out, int T, int d_in, int d_out, int n_slots, int kc,
+                               int nc, uint32_t* err) {
+  __shared__ AdapterSmem<128> sm;
+  pdl_launch_dependents();
+  const int c = static_cast<int>(ptx::cluster_ctarank());
+  const int id = ids[blockIdx.y];
+  const bool first = threadIdx.x == 0 && c == 0;
+  bool valid = slot_valid(id, n_slots);
+  if (!valid && id != -1 && first) flag_error(err, LORA_DEVERR_BAD_SLOT);
+  int ra = 0;
+  int64_t ao = 0, bo = 0;
+  if (valid) {
+    // the slot's table entry; one that would read outside the pools or break
+    // the 16-byte alignment of the rows is flagged and the row is base-only
+    ra = rank[id];
+    ao = a_off[id];
+    bo = b_off[id];
+    const bool ok = (ra == 8 || ra == 16 || ra == 32 || ra == 64 || ra == 128) &&
+                    ra <= r_max && ao >= 0 && bo >= 0 &&
+                    ao % 8 == 0 && bo % 8 == 0 &&
+                    ao <= a_elems - static_cast<int64_t>(d_in) * ra &&
+                    bo <= b_elems - static_cast<int64_t>(ra) * d_out;
+    if (!ok) {
+      if (first) flag_error(err, LORA_DEVERR_BAD_RANK);
+      valid = false;
+    }
+  }
+  if (!MERGE && !valid) return;
+  const bf16* Aa = A + ao;
+  const bf16* Ba = B + bo;
+  const float s = valid && scale ? scale[id] : 1.f;
+#define LORA_RAGGED_CLASS(RR)                                                                  \
+  adapter_token<RR, MERGE, 128>(x, Aa, Ba, s, valid, partial, S, out, T, d_in, d_out, kc, nc, sm)
+  // uniform over the cluster: every CTA read the same table entry
+  if (!valid || ra == 8) LORA_RAGGED_CLASS(8);
+  else if (ra == 16) LORA_RAGGED_CLASS(16);
+  else if (ra == 32) LORA_RAGGED_CLASS(32);
+  else if (ra == 64) LORA_RAGGED_CLASS(64);
+  else LORA_RAGGED_CLASS(128);
+#undef LORA_RAGGED_CLASS
+}
+
+struct AdapterLaunch {
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[2];
+  int kc, nc;
+};
+
+// One cluster of C CTAs per token, C = adapter_cluster_size(T, d_in, d_out).
+void adapter_launch_config(AdapterLaunch& L, int T, int d_in, int d_out, bool pdl,
+                           cudaStream_t st) {
+  const int C = adapter_cluster_size(T, d_in, d_out);
+  L.kc = ((d_in + 8 * C - 1) / (8 * C)) * 8;
+  L.nc = ((d_out + 8 * C - 1) / (8 * C)) * 8;
+  L.cfg = cudaLaunchConfig_t{};
+  L.cfg.gridDim = dim3(C, T);
+  L.cfg.blockDim = dim3(kAdThreads);
+  L.cfg.dynamicSmemBytes = 0;
+  L.cfg.stream = st;
+  L.attr[0].id = cudaLaunchAttributeClusterDimension;
+  L.attr[0].val.clusterDim.x = C;
+  L.attr[0].val.clusterDim.y = 1;
+  L.attr[0].val.clusterDim.z = 1;
+  L.attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  L.attr[1].val.programmaticStreamSerializationAllowed = 1;
+  L.cfg.attrs = L.attr;
+  L.cfg.numAttrs = pdl ? 2 : 1;
 }
 
 template <bool MERGE>
@@ -260,30 +366,15 @@ cudaError_t launch_adapter_form(const void* x, const void* A, const void* B, con
                                 bool pdl, cudaStream_t st) {
   if (T <= 0) return cudaSuccess;
   if (T > 65535) return cudaErrorInvalidValue;
-  const int C = adapter_cluster_size(T, d_in, d_out);
-  const int kc = ((d_in + 8 * C - 1) / (8 * C)) * 8;
-  const int nc = ((d_out + 8 * C - 1) / (8 * C)) * 8;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(C, T);
-  cfg.blockDim = dim3(kAdThreads);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 2 : 1;
+  AdapterLaunch L;
+  adapter_launch_config(L, T, d_in, d_out, pdl, st);
   const bf16* xe = static_cast<const bf16*>(x);
   const bf16* Ae = static_cast<const bf16*>(A);
   const bf16* Be = static_cast<const bf16*>(B);
 #define LORA_ADAPTER_CASE(RR)                                                                  \
   case RR:                                                                                     \
-    return cudaLaunchKernelEx(&cfg, bgmv_adapter_kernel<RR, MERGE>, xe, Ae, Be, ids, scale,   \
-                              partial, S, out, T, d_in, d_out, n_slots, kc, nc, err);
+    return cudaLaunchKernelEx(&L.cfg, bgmv_adapter_kernel<RR, MERGE>, xe, Ae, Be, ids, scale, \
+                              partial, S, out, T, d_in, d_out, n_slots, L.kc, L.nc, err);
   switch (r) {
     LORA_ADAPTER_CASE(8)
     LORA_ADAPTER_CASE(16)
@@ -293,6 +384,22 @@ cudaError_t launch_adapter_form(const void* x, const void* A, const void* B, con
     default: return cudaErrorInvalidValue;
   }
 #undef LORA_ADAPTER_CASE
+}
+
+template <bool MERGE>
+cudaError_t launch_ragged_form(const void* x, const void* A, const void* B, const RaggedPool& rp,
+                               const int32_t* ids, const float* scale, const float* partial,
+                               int S, void* out, int T, int d_in, int d_out, int n_slots,
+                               uint32_t* err, bool pdl, cudaStream_t st) {
+  if (T <= 0) return cudaSuccess;
+  if (T > 65535 || rp.r_max < 8 || rp.r_max > 128) return cudaErrorInvalidValue;
+  AdapterLaunch L;
+  adapter_launch_config(L, T, d_in, d_out, pdl, st);
+  return cudaLaunchKernelEx(&L.cfg, bgmv_adapter_ragged_kernel<MERGE>,
+                            static_cast<const bf16*>(x), static_cast<const bf16*>(A),
+                            static_cast<const bf16*>(B), rp.a_off, rp.b_off, rp.rank,
+                            rp.a_elems, rp.b_elems, rp.r_max, ids, scale, partial, S, out, T,
+                            d_in, d_out, n_slots, L.kc, L.nc, err);
 }
 
 }  // namespace
@@ -326,6 +433,23 @@ cudaError_t launch_bgmv_adapter_merge(const void* x, const void* A, const void* 
                                       cudaStream_t st) {
   return launch_adapter_form<true>(x, A, B, ids, scale, partial, S, y, T, d_in, d_out, r,
                                    n_slots, err, pdl, st);
+}
+
+cudaError_t launch_bgmv_adapter_ragged(const void* x, const void* A, const void* B,
+                                       const RaggedPool& rp, const int32_t* ids,
+                                       const float* scale, float* delta, int T, int d_in,
+                                       int d_out, int n_slots, uint32_t* err, cudaStream_t st) {
+  return launch_ragged_form<false>(x, A, B, rp, ids, scale, nullptr, 0, delta, T, d_in, d_out,
+                                   n_slots, err, false, st);
+}
+
+cudaError_t launch_bgmv_adapter_ragged_merge(const void* x, const void* A, const void* B,
+                                             const RaggedPool& rp, const int32_t* ids,
+                                             const float* scale, const float* partial, int S,
+                                             void* y, int T, int d_in, int d_out, int n_slots,
+                                             uint32_t* err, bool pdl, cudaStream_t st) {
+  return launch_ragged_form<true>(x, A, B, rp, ids, scale, partial, S, y, T, d_in, d_out,
+                                  n_slots, err, pdl, st);
 }
 
 }  // namespace lora

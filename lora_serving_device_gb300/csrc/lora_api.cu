@@ -121,6 +121,24 @@ lora_status_t check_ws(const void* ws, size_t ws_bytes, size_t need) {
   return LORA_OK;
 }
 
+// Shared argument checks of the two ragged entry points.
+lora_status_t ragged_args(const void* x, const void* A_flat, const void* B_flat,
+                          const int64_t* a_off, const int64_t* b_off, const int32_t* rank,
+                          int64_t a_elems, int64_t b_elems, int32_t r_max,
+                          const int32_t* slot_ids, const void* out, int32_t T, int32_t T_max,
+                          int32_t d_in, int32_t d_out, int32_t n_slots, lora_dtype_t dt) {
+  if (T < 0 || a_elems < 0 || b_elems < 0) return LORA_ERR_INVALID_ARG;
+  if (dt != LORA_DTYPE_BF16) return LORA_ERR_DTYPE;
+  if (T > T_max || !dim_ok(d_in) || !dim_ok(d_out) || !rank_ok(r_max) ||
+      !slots_ok(n_slots))
+    return LORA_ERR_SHAPE;
+  if (x == nullptr || A_flat == nullptr || B_flat == nullptr || a_off == nullptr ||
+      b_off == nullptr || rank == nullptr || slot_ids == nullptr || out == nullptr ||
+      !aligned16(x) || !aligned16(A_flat) || !aligned16(B_flat) || !aligned16(out))
+    return LORA_ERR_INVALID_ARG;
+  return LORA_OK;
+}
+
 }  // namespace
 
 cudaError_t device_info(DeviceInfo* out) {
@@ -424,6 +442,54 @@ lora_status_t lora_bgmv_adapter(const void* x, const void* A_pool, const void* B
   return from_cuda(launch_bgmv_adapter(x, A_pool, B_pool, slot_ids, scale, delta, T, d_in, d_out,
                                        r, n_slots, static_cast<uint32_t*>(ws),
                                        static_cast<cudaStream_t>(stream)));
+}
+
+lora_status_t lora_bgmv_adapter_ragged(const void* x, const void* A_flat, const void* B_flat,
+                                       const int64_t* a_off, const int64_t* b_off,
+                                       const int32_t* rank, int64_t a_elems, int64_t b_elems,
+                                       int32_t r_max, const int32_t* slot_ids,
+                                       const float* scale, float* delta, int32_t T,
+                                       int32_t d_in, int32_t d_out, int32_t n_slots,
+                                       lora_dtype_t dt, void* ws, size_t ws_bytes, void* stream) {
+  lora_status_t s = ragged_args(x, A_flat, B_flat, a_off, b_off, rank, a_elems, b_elems, r_max,
+                                slot_ids, delta, T, 65535, d_in, d_out, n_slots, dt);
+  if (s != LORA_OK) return s;
+  if ((s = check_ws(ws, ws_bytes, kErrBytes)) != LORA_OK) return s;
+  if (T == 0) return LORA_OK;
+  DeviceInfo dev;
+  if ((s = check_device(&dev)) != LORA_OK) return s;
+  const RaggedPool rp{a_off, b_off, rank, a_elems, b_elems, r_max};
+  return from_cuda(launch_bgmv_adapter_ragged(x, A_flat, B_flat, rp, slot_ids, scale, delta, T,
+                                              d_in, d_out, n_slots, static_cast<uint32_t*>(ws),
+                                              static_cast<cudaStream_t>(stream)));
+}
+
+lora_status_t lora_linear_fused_ragged(const void* x, const void* W0, const void* A_flat,
+                                       const void* B_flat, const int64_t* a_off,
+                                       const int64_t* b_off, const int32_t* rank,
+                                       int64_t a_elems, int64_t b_elems, int32_t r_max,
+                                       const int32_t* slot_ids, const float* scale, void* y,
+                                       int32_t T, int32_t d_in, int32_t d_out, int32_t n_slots,
+                                       lora_dtype_t dt, void* ws, size_t ws_bytes, void* stream) {
+  lora_status_t s = ragged_args(x, A_flat, B_flat, a_off, b_off, rank, a_elems, b_elems, r_max,
+                                slot_ids, y, T, kDecodeTokens, d_in, d_out, n_slots, dt);
+  if (s != LORA_OK) return s;
+  if (W0 == nullptr || !aligned16(W0) || x == y) return LORA_ERR_INVALID_ARG;
+  const FusedWs w = fused_ws_layout(ws, T, d_in, d_out, r_max, n_slots);
+  if ((s = check_ws(ws, ws_bytes, w.bytes)) != LORA_OK) return s;
+  if (T == 0) return LORA_OK;
+  DeviceInfo dev;
+  if ((s = check_device(&dev)) != LORA_OK) return s;
+  if (!tensor_map_available()) return LORA_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // the decode chain of lora_linear_fused with the ragged merge kernel
+  cudaError_t e =
+      launch_decode_gemm(x, W0, w.partial, T, d_in, d_out, w.split, w.err, true, st, dev);
+  if (e != cudaSuccess) return LORA_ERR_CUDA;
+  const RaggedPool rp{a_off, b_off, rank, a_elems, b_elems, r_max};
+  return from_cuda(launch_bgmv_adapter_ragged_merge(x, A_flat, B_flat, rp, slot_ids, scale,
+                                                    w.partial, w.split, y, T, d_in, d_out,
+                                                    n_slots, w.err, true, st));
 }
 
 lora_status_t lora_base_gemm_splitk(const void* x, const void* W0, float* partial, int32_t T,

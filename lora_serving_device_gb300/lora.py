@@ -20,7 +20,8 @@ STATUS_NAMES = {0: "LORA_OK", 1: "LORA_ERR_INVALID_ARG", 2: "LORA_ERR_SHAPE", 3:
 DTYPE_BF16, DTYPE_F32 = 0, 1
 OP_BUILD_SEGMENTS, OP_BGMV_SHRINK, OP_BGMV_EXPAND = 0, 1, 2
 OP_SGMV_SHRINK, OP_SGMV_EXPAND, OP_LINEAR_FUSED, OP_BASE_GEMM_EXPAND = 3, 4, 5, 6
-DEVERR_BAD_SLOT, DEVERR_TIMEOUT = 0x1, 0x2
+DEVERR_BAD_SLOT, DEVERR_TIMEOUT, DEVERR_BAD_RANK = 0x1, 0x2, 0x4
+RAGGED_RANKS = (8, 16, 32, 64, 128)
 MAX_SLOTS, MAX_TOKENS, MAX_KSPLIT = 16384, 1 << 20, 64
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -28,7 +29,7 @@ EXPORTS = ("lora_workspace_bytes", "lora_build_segments", "lora_bgmv_shrink", "l
            "lora_sgmv_shrink", "lora_sgmv_expand", "lora_linear_fused", "lora_base_gemm_expand",
            "lora_linear_fused_noalloc", "lora_bgmv_delta", "lora_bgmv_adapter",
            "lora_bgmv_adapter_merge", "lora_base_gemm_splitk", "lora_decode_split",
-           "lora_slot_upload",
+           "lora_slot_upload", "lora_bgmv_adapter_ragged", "lora_linear_fused_ragged",
            "lora_get_error", "lora_status_string")
 
 
@@ -42,6 +43,7 @@ _lib = None
 _P = ctypes.c_void_p
 _I = ctypes.c_int32
 _Z = ctypes.c_size_t
+_L = ctypes.c_int64
 
 _SIGS = {
     "lora_workspace_bytes": (_Z, [_I, _I, _I, _I, _I, _I]),
@@ -61,6 +63,10 @@ _SIGS = {
     "lora_decode_split": (_I, [_I, _I, _I]),
     "lora_slot_upload": (_I, [_P, _P, _P, _I, _P, _P, ctypes.c_float, _I, _I, _I, _I, _I, _I,
                               _P]),
+    "lora_bgmv_adapter_ragged": (_I, [_P, _P, _P, _P, _P, _P, _L, _L, _I, _P, _P, _P, _I, _I, _I,
+                                      _I, _I, _P, _Z, _P]),
+    "lora_linear_fused_ragged": (_I, [_P, _P, _P, _P, _P, _P, _P, _L, _L, _I, _P, _P, _P, _I, _I,
+                                      _I, _I, _I, _P, _Z, _P]),
     "lora_get_error": (_I, [_P, _P, ctypes.POINTER(ctypes.c_int32)]),
     "lora_status_string": (ctypes.c_char_p, [_I]),
 }
@@ -169,6 +175,21 @@ def lora_slot_upload(A_pool, B_pool, scale, slot, A_host, B_host, s, d_in, d_out
                      dt, stream):
     return _call("lora_slot_upload", A_pool, B_pool, scale, slot, A_host, B_host, s, d_in, d_out, r,
                  r_a, n_slots, dt, stream)
+
+
+def lora_bgmv_adapter_ragged(x, A_flat, B_flat, a_off, b_off, rank, a_elems, b_elems, r_max,
+                             slot_ids, scale, delta, T, d_in, d_out, n_slots, dt, ws, ws_bytes,
+                             stream):
+    return _call("lora_bgmv_adapter_ragged", x, A_flat, B_flat, a_off, b_off, rank, a_elems,
+                 b_elems, r_max, slot_ids, scale, delta, T, d_in, d_out, n_slots, dt, ws, ws_bytes,
+                 stream)
+
+
+def lora_linear_fused_ragged(x, W0, A_flat, B_flat, a_off, b_off, rank, a_elems, b_elems, r_max,
+                             slot_ids, scale, y, T, d_in, d_out, n_slots, dt, ws, ws_bytes, stream):
+    return _call("lora_linear_fused_ragged", x, W0, A_flat, B_flat, a_off, b_off, rank, a_elems,
+                 b_elems, r_max, slot_ids, scale, y, T, d_in, d_out, n_slots, dt, ws, ws_bytes,
+                 stream)
 
 
 def lora_get_error(ws, stream):
@@ -369,6 +390,92 @@ def bgmv_adapter_merge_t(x, A_pool, B_pool, slot_ids, scale, partial, ws, y=None
                                   d_out, r, n_slots, _dt(x), _ptr(ws), ws.numel(),
                                   _stream(stream)),
           "lora_bgmv_adapter_merge")
+    return y
+
+
+def ragged_rank_class(r):
+    """The stored rank of a rank-r adapter in a ragged pool: the next of 8, 16, 32, 64, 128."""
+    for c in RAGGED_RANKS:
+        if r <= c:
+            return c
+    raise ValueError(f"rank {r} > {RAGGED_RANKS[-1]}")
+
+
+class RaggedPool:
+    """A ragged-rank adapter pool on the device: slot a keeps A_a [d_in, rank[a]] at
+    A_flat[a_off[a]:] and B_a [rank[a], d_out] at B_flat[b_off[a]:], each at its own
+    rank (zero-padded only up to the next of 8, 16, 32, 64, 128)."""
+
+    def __init__(self, A_list, B_list, device="cuda", dtype=None):
+        """A_list[a] [d_in, r_a], B_list[a] [r_a, d_out] (torch tensors, any device)."""
+        import torch
+        if len(A_list) != len(B_list) or not A_list:
+            raise ValueError("need one A and one B per slot")
+        self.n_slots = len(A_list)
+        self.d_in = int(A_list[0].shape[0])
+        self.d_out = int(B_list[0].shape[1])
+        dtype = dtype or A_list[0].dtype
+        ranks = [ragged_rank_class(int(a.shape[1])) for a in A_list]
+        a_off, b_off, a_n, b_n = [], [], 0, 0
+        for rc in ranks:
+            a_off.append(a_n)
+            b_off.append(b_n)
+            a_n += self.d_in * rc
+            b_n += rc * self.d_out
+        self.A_flat = torch.zeros(a_n, dtype=dtype, device=device)
+        self.B_flat = torch.zeros(b_n, dtype=dtype, device=device)
+        for a, (A, B, rc) in enumerate(zip(A_list, B_list, ranks)):
+            r_a = int(A.shape[1])
+            if A.shape[0] != self.d_in or tuple(B.shape) != (r_a, self.d_out):
+                raise ValueError(f"slot {a}: shapes {tuple(A.shape)} / {tuple(B.shape)}")
+            self.A_flat[a_off[a]:a_off[a] + self.d_in * rc].view(self.d_in, rc)[:, :r_a] = A
+            self.B_flat[b_off[a]:b_off[a] + rc * self.d_out].view(rc, self.d_out)[:r_a] = B
+        self.ranks = ranks
+        self.r_max = max(ranks)
+        self.a_off = torch.tensor(a_off, dtype=torch.int64, device=device)
+        self.b_off = torch.tensor(b_off, dtype=torch.int64, device=device)
+        self.rank = torch.tensor(ranks, dtype=torch.int32, device=device)
+
+    @classmethod
+    def from_padded(cls, A_pool, B_pool, ranks):
+        """The ragged pool of a zero-padded one: slot a keeps its first ranks[a] columns of A
+        and rows of B (the rest must be zero for the two to give the same layer)."""
+        return cls([A_pool[a, :, :int(r)] for a, r in enumerate(ranks)],
+                   [B_pool[a, :int(r), :] for a, r in enumerate(ranks)], device=A_pool.device)
+
+    @property
+    def nbytes(self):
+        return (self.A_flat.numel() + self.B_flat.numel()) * self.A_flat.element_size()
+
+
+def bgmv_adapter_ragged_t(x, pool, slot_ids, scale, ws, delta=None, stream=None):
+    """bgmv_adapter_t over a RaggedPool."""
+    import torch
+    T, d_in = x.shape
+    if delta is None:
+        delta = torch.zeros((T, pool.d_out), dtype=torch.float32, device=x.device)
+    check(lora_bgmv_adapter_ragged(_ptr(x), _ptr(pool.A_flat), _ptr(pool.B_flat),
+                                   _ptr(pool.a_off), _ptr(pool.b_off), _ptr(pool.rank),
+                                   pool.A_flat.numel(), pool.B_flat.numel(), pool.r_max,
+                                   _ptr(slot_ids), _ptr(scale), _ptr(delta), T, d_in, pool.d_out,
+                                   pool.n_slots, _dt(x), _ptr(ws), ws.numel(), _stream(stream)),
+          "lora_bgmv_adapter_ragged")
+    return delta
+
+
+def linear_fused_ragged_t(x, W0, pool, slot_ids, scale, ws, y=None, stream=None):
+    """linear_fused_t over a RaggedPool (decode-sized bf16 batches, T <= 256)."""
+    import torch
+    T, d_in = x.shape
+    d_out = W0.shape[1]
+    if y is None:
+        y = torch.empty((T, d_out), dtype=x.dtype, device=x.device)
+    check(lora_linear_fused_ragged(_ptr(x), _ptr(W0), _ptr(pool.A_flat), _ptr(pool.B_flat),
+                                   _ptr(pool.a_off), _ptr(pool.b_off), _ptr(pool.rank),
+                                   pool.A_flat.numel(), pool.B_flat.numel(), pool.r_max,
+                                   _ptr(slot_ids), _ptr(scale), _ptr(y), T, d_in, d_out,
+                                   pool.n_slots, _dt(x), _ptr(ws), ws.numel(), _stream(stream)),
+          "lora_linear_fused_ragged")
     return y
 
 

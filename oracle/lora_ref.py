@@ -116,6 +116,25 @@ def lora_linear_gathered(x, W0, A_pool, B_pool, scale, slot_ids):
     return y
 
 
+def lora_linear_ragged(x, W0, A_list, B_list, scale, slot_ids):
+    """The layer over adapters of different ranks, each kept at its own rank
+    (no padding to the largest): A_list[a] [d_in, r_a], B_list[a] [r_a, d_out].
+    [Blog, "Batching across different adapters"]: mixed ranks are served by
+    ragged indexing or by padding; [Concepts, "When It Falls Down"] and
+    [Handbook, Exercise 2]: padding changes the cost, not the result.  Per
+    token: y_t = x_t W0 + s_a (x_t A_a) B_a, base only for ids outside
+    [0, len(A_list))."""
+    x, W0 = _f64(x), _f64(W0)
+    ids = valid_ids(slot_ids, len(A_list))
+    y = x @ W0
+    for t in range(x.shape[0]):
+        a = ids[t]
+        if a >= 0:
+            v = float(scale[a]) * (x[t] @ _f64(A_list[a]))     # shrink to rank r_a
+            y[t] += v @ _f64(B_list[a])                        # expand, add
+    return y
+
+
 def build_segments(slot_ids, n_slots):
     """SGMV segments ([Handbook], SGMV bullet and its toy script): stable sort
     of the tokens by id, then runs of equal ids.

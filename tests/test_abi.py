@@ -122,6 +122,75 @@ def test_slot_upload_validation(L):
     assert up(FAKE, FAKE, None, 0, FAKE, FAKE, 2.0, 64, 64, 16, 8, 4, 7, None) == 3    # dtype
 
 
+def test_ragged_validation(L):
+    WS, NW = FAKE + 8192, 1 << 20
+
+    def fused(T=64, x=FAKE, y=FAKE + 4096, A=FAKE, a_elems=1 << 20, r_max=64, dt=0, d_in=64):
+        # (x, W0, A, B, a_off, b_off, rank, a_elems, b_elems, r_max, ids, scale, y,
+        #  T, d_in, d_out, n_slots, dt, ws, ws_bytes, stream)
+        return L.lora_linear_fused_ragged(x, FAKE, A, FAKE, FAKE, FAKE, FAKE, a_elems, 1 << 20,
+                                          r_max, FAKE, None, y, T, d_in, 64, 4, dt, WS, NW, None)
+
+    def delta(T=64, r_max=64):
+        return L.lora_bgmv_adapter_ragged(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 20, 1 << 20,
+                                          r_max, FAKE, None, FAKE + 4096, T, 64, 64, 4, 0, WS,
+                                          NW, None)
+
+    assert fused(T=257) == 2           # the fused layer takes decode-sized batches only
+    assert fused(r_max=48) == 2        # r_max is one of 8 .. 128
+    assert fused(r_max=256) == 2
+    assert fused(d_in=60) == 2
+    assert fused(dt=1) == 3            # bf16 only
+    assert fused(A=None) == 1
+    assert fused(A=FAKE + 2) == 1      # 16-byte aligned pools
+    assert fused(a_elems=-1) == 1
+    assert fused(x=FAKE + 4096) == 1   # x == y
+    assert fused(T=0) == 0             # empty batch: nothing launched
+    assert delta(T=65536) == 2
+    assert delta(r_max=12) == 2
+    assert delta(T=0) == 0
+
+
+def test_ragged_rank_class():
+    from lora_serving_device_gb300 import lora as Lb
+    assert [Lb.ragged_rank_class(r) for r in (1, 4, 8, 9, 16, 24, 33, 64, 65, 128)] == \
+        [8, 8, 8, 16, 16, 32, 64, 64, 128, 128]
+    with pytest.raises(ValueError):
+        Lb.ragged_rank_class(129)
+
+
+def test_ragged_pool_layout_on_cpu():
+    """The packed layout: each slot at its rank class, offsets contiguous and 16-byte
+    aligned, the padding zero, and the padded pool recovered exactly."""
+    import numpy as np
+    import torch
+    from lora_serving_device_gb300 import lora as Lb
+    rng = np.random.default_rng(5)
+    d_in, d_out, ranks = 24, 40, [8, 4, 64, 16, 24]
+    A = [torch.from_numpy(rng.standard_normal((d_in, r)).astype(np.float32)) for r in ranks]
+    B = [torch.from_numpy(rng.standard_normal((r, d_out)).astype(np.float32)) for r in ranks]
+    p = Lb.RaggedPool(A, B, device="cpu")
+    cls = [8, 8, 64, 16, 32]
+    assert p.ranks == cls and p.r_max == 64
+    assert p.a_off.tolist() == list(np.cumsum([0] + [d_in * c for c in cls[:-1]]))
+    assert p.b_off.tolist() == list(np.cumsum([0] + [c * d_out for c in cls[:-1]]))
+    assert all(o % 8 == 0 for o in p.a_off.tolist() + p.b_off.tolist())
+    assert p.A_flat.numel() == d_in * sum(cls) and p.B_flat.numel() == d_out * sum(cls)
+    for a, (r, c) in enumerate(zip(ranks, cls)):
+        Aa = p.A_flat[p.a_off[a]:p.a_off[a] + d_in * c].view(d_in, c)
+        Ba = p.B_flat[p.b_off[a]:p.b_off[a] + c * d_out].view(c, d_out)
+        assert torch.equal(Aa[:, :r], A[a]) and not Aa[:, r:].any()
+        assert torch.equal(Ba[:r], B[a]) and not Ba[r:].any()
+    # from_padded keeps the first ranks[a] columns / rows of a padded pool
+    Ap = torch.zeros(len(ranks), d_in, 64)
+    Bp = torch.zeros(len(ranks), 64, d_out)
+    for a, r in enumerate(ranks):
+        Ap[a, :, :r] = A[a]
+        Bp[a, :r] = B[a]
+    q = Lb.RaggedPool.from_padded(Ap, Bp, ranks)
+    assert torch.equal(q.A_flat, p.A_flat) and torch.equal(q.B_flat, p.B_flat)
+
+
 def test_decode_split_is_a_function_of_the_shapes(L):
     assert L.lora_decode_split(64, 4096, 4096) == 4       # 32 column tiles x 4 = 128 CTAs
     assert L.lora_decode_split(256, 4096, 4096) == 4      # one 256-token tile

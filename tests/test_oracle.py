@@ -178,6 +178,43 @@ def test_rank_padding_exact():
     assert f["r_max"] // f["r_small"] == f["penalty"]
 
 
+def test_ragged_brute_force_and_padding():
+    """Adapters at their own ranks: scalar loops over each adapter's own rank
+    give the same y, and so does the pool zero-padded to the largest rank
+    ([Concepts, "When It Falls Down"]; [Blog, "Batching across different
+    adapters"])."""
+    rng = np.random.default_rng(21)
+    T, d_in, d_out = 9, 11, 7
+    ranks = [1, 4, 2, 6, 3]
+    x = rng.standard_normal((T, d_in))
+    W0 = rng.standard_normal((d_in, d_out))
+    A = [rng.standard_normal((d_in, r)) for r in ranks]
+    B = [rng.standard_normal((r, d_out)) for r in ranks]
+    s = rng.uniform(0.5, 3.0, len(ranks))
+    ids = rng.integers(-1, len(ranks), T)
+    ids[0], ids[1] = len(ranks), -4           # read as base only
+    want = np.zeros((T, d_out))
+    for t in range(T):
+        a = int(ids[t])
+        for n in range(d_out):
+            acc = sum(x[t, k] * W0[k, n] for k in range(d_in))
+            if 0 <= a < len(ranks):
+                for q in range(ranks[a]):
+                    vq = s[a] * sum(x[t, k] * A[a][k, q] for k in range(d_in))
+                    acc += vq * B[a][q, n]
+            want[t, n] = acc
+    got = O.lora_linear_ragged(x, W0, A, B, s, ids)
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
+    r_pad = max(ranks)
+    Ap = np.stack([O.pad_rank(A[a], B[a], r_pad)[0] for a in range(len(ranks))])
+    Bp = np.stack([O.pad_rank(A[a], B[a], r_pad)[1] for a in range(len(ranks))])
+    np.testing.assert_allclose(O.lora_linear(x, W0, Ap, Bp, s, ids), want, rtol=1e-12,
+                               atol=1e-12)
+    # a plausible mistake: every adapter cut to the smallest rank
+    cut = O.lora_linear_ragged(x, W0, [a[:, :1] for a in A], [b[:1] for b in B], s, ids)
+    assert not np.allclose(cut, want, rtol=1e-6, atol=1e-6)
+
+
 # ----------------------------------------------------------------------------
 # the pages' printed figures
 # ----------------------------------------------------------------------------
