@@ -640,6 +640,45 @@ def prefill_point(L, stream, pk, dev, steps=30, warm=5):
     return res
 
 
+def q4_point(L, sets, w, stream, pk, steps=4000, warm=400):
+    """The decode layer with its base matrix in 4 bits (codebook + bf16
+    absmax per 64-row block, quantised by the library), bf16 adapters."""
+    import torch
+    from lora_serving_device_gb300 import workloads as W
+    T, d_in, d_out, r, n_slots = w.T, w.d_in, w.d_out, w.r, w.n_slots
+    cb = _up(W.nf4_like_codebook(), sets[0].x.device)
+    bases = [L.Base4bit.quantize(s.W0, cb, stream=stream) for s in sets]
+    stream.synchronize()
+    ws = L.workspace(L.OP_LINEAR_FUSED, T, d_in, d_out, r, n_slots, device=sets[0].x.device)
+    n = len(sets)
+
+    def step(i):
+        s = sets[i % n]
+        L.linear_fused_4bit_t(s.x, bases[i % n], s.A, s.B, s.ids, s.scale, ws, y=s.y,
+                              stream=stream)
+
+    ms, _ = timed_graph_steps(step, steps, warm, stream)
+    err = L.get_error_t(ws, stream=stream)
+    t = ms / 1e3 / steps
+    qbytes = d_in * d_out // 2 + (d_in // 64) * d_out * 2
+    D = w.distinct
+    lb = qbytes + (D * r * (d_in + d_out) + T * d_in + T * d_out) * 2 + T * 4
+    split = L.lora_decode_split(T, d_in, d_out)
+    part = torch.empty((split, T, d_out), dtype=torch.float32, device=sets[0].x.device)
+    gemm_ms = graph_mean_ms(lambda i: L.base_gemm_4bit_splitk_t(
+        sets[i % n].x, bases[i % n], ws, ksplit=split, partial=part, stream=stream), 400, stream)
+    gb = qbytes + T * d_in * 2 + T * d_out * 4
+    res = {"workload": "decode_4bit: " + DECODE_DESC + "; W0 as 4-bit codes + bf16 absmax per "
+                       "64-row block (0.53 B/weight)",
+           "us_per_step": t * 1e6, "tokens_per_s": T / t, "layer_bytes": lb,
+           "gbs": lb / t / 1e9, "frac": lb / t / 1e9 / pk["hbm_gbs"], "device_error": err,
+           "gemm": dict(block_row(gemm_ms, gb, pk),
+                        kernel="decode_q4_kernel (4-bit dequant in the mainloop, tcgen05)")}
+    del bases
+    torch.cuda.empty_cache()
+    return res
+
+
 def stack_point(L, stream, pk, dev, steps=5, warm=3, ragged=False):
     """The 8B-shaped stack: 32 layers x 7 projections, one fused call each.
     ragged: every adapter kept at its own rank (8, 16 or 64) in a ragged pool
@@ -776,9 +815,9 @@ def run_ours(args):
         "clocks": clk.summary(),
     }
     line["slot_upload"] = upload_point(L, sets, w, stream)
+    cfgs = {"decode_4bit": q4_point(L, sets, w, stream, pk)}
     if not args.no_sweep:
         line["sweep"] = sweep(L, stream, pk, dev)
-    cfgs = {}
     if not args.no_prefill:
         cfgs["prefill_sgmv"] = prefill_point(L, stream, pk, dev)
     if args.stack:

@@ -364,6 +364,56 @@ lora_status_t lora_linear_fused_ragged(const void* x, const void* W0, const void
                                        lora_dtype_t dt, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * 4-bit base matrix with bf16 adapters ("Serving Many LoRA Adapters", section
+ * "When It Falls Down": QLoRA-style 4-bit base models served next to bf16
+ * adapters, the base path passing through dequantisation).  Format (one
+ * reading of "QLoRA style": a 16-entry codebook scaled by the absolute
+ * maximum of each block of 64 weights):
+ *   W0q     [d_out, d_in / 2] uint8, k contiguous per output column (the
+ *           [out, in] orientation of a QLoRA weight): byte i of row n holds
+ *           the codes of rows 2i (low nibble) and 2i + 1 (high nibble) of
+ *           column n.
+ *   absmax  [d_in / 64, d_out] bf16; the scale of rows [64b, 64b + 64) of a
+ *           column.
+ *   codebook [16] bf16; code c stands for codebook[c] (for NF4-like codes,
+ *           values in [-1, 1]).
+ *   deq(W0)[k, n] = bf16(codebook[code[k, n]] * absmax[k / 64, n]), the
+ *           product rounded once to bf16.
+ * Shapes: d_in a multiple of 64, d_out a multiple of 32; all pointers device
+ * pointers, 16-byte aligned.
+ *
+ * lora_quantize_base_4bit: W0 [d_in, d_out] bf16 (finite) -> W0q, absmax:
+ * absmax = max |W0| over each block; code = the codebook entry nearest
+ * W0 / absmax (fp32 quotient and distances, ties to the lower code; an
+ * all-zero block takes the entry nearest 0).  Done once per weight matrix.
+ *
+ * lora_base_gemm_4bit_splitk: partial [ksplit, T, d_out] fp32 with
+ * partial[z] = x[:, K_z] deq(W0)[K_z, :] over ksplit contiguous ranges of
+ * d_in, 1 <= ksplit <= min(d_in / 64, 64); the dequantisation runs in the
+ * GEMM's mainloop on chip (into tensor memory, where the MMA reads it).
+ * Workspace: the error word.
+ *
+ * lora_linear_fused_4bit: the whole layer for decode-sized bf16 batches
+ * (T <= 256), y = x deq(W0) + s (x A) B: the 4-bit split-K GEMM, then the
+ * merge kernel of lora_linear_fused (bf16 adapters).  Same pools, ids,
+ * scale, workspace (lora_workspace_bytes(LORA_OP_LINEAR_FUSED, ...)) and
+ * programmatic-overlap rules as lora_linear_fused (W0q, absmax and the
+ * codebook play the part of W0 there).
+ */
+lora_status_t lora_quantize_base_4bit(const void* W0, const void* codebook, void* W0q,
+                                      void* absmax, int32_t d_in, int32_t d_out, void* stream);
+lora_status_t lora_base_gemm_4bit_splitk(const void* x, const void* W0q, const void* absmax,
+                                         const void* codebook, float* partial, int32_t T,
+                                         int32_t d_in, int32_t d_out, int32_t ksplit, void* ws,
+                                         size_t ws_bytes, void* stream);
+lora_status_t lora_linear_fused_4bit(const void* x, const void* W0q, const void* absmax,
+                                     const void* codebook, const void* A_pool,
+                                     const void* B_pool, const int32_t* slot_ids,
+                                     const float* scale, void* y, int32_t T, int32_t d_in,
+                                     int32_t d_out, int32_t r, int32_t n_slots, void* ws,
+                                     size_t ws_bytes, void* stream);
+
+/*
  * Uploads one adapter into pool slot `slot` (the data path of adapter
  * paging: "Multi-LoRA batching and adapter paging", section "Adapter
  * paging", and "Serving many LoRA adapters", section "Paging adapters": an

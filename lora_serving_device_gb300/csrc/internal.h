@@ -139,6 +139,27 @@ cudaError_t launch_sgmv_expand_tc(const float* vpart, int ksplit, const void* B,
 // box box0 x box1 x 1; elements outside the tensor are not stored.
 bool encode_tensor_map_f32_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1,
                               uint64_t d2, uint32_t box0, uint32_t box1);
+// 2-D tensor map without swizzle over 1-byte (uint8) or 2-byte (bf16)
+// elements: `inner` contiguous elements per row, `outer` rows `row_bytes`
+// apart, box box_inner x box_outer; elements outside read as zero.
+bool encode_tensor_map_plain_2d(CUtensorMap* m, const void* base, int elem_bytes, uint64_t inner,
+                                uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
+                                uint32_t box_outer);
+// 2-D uint8 tensor map with 128-byte swizzle (box_inner <= 128 bytes).
+bool encode_tensor_map_u8_sw128(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                                uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
+// Decode-sized base GEMM over a 4-bit base (codes [d_out, d_in / 2] bytes,
+// bf16 absmax [d_in / 64, d_out], bf16 codebook [16]), split over d_in into S
+// fp32 partials like launch_decode_gemm, see k_decode_q4.cu.  d_in % 64 == 0,
+// d_out % 32 == 0, 1 <= S <= decode_q4_max_split(d_in).
+int decode_q4_max_split(int d_in);
+cudaError_t launch_decode_q4(const void* x, const void* Wq, const void* absmax,
+                             const void* codebook, float* partial, int T, int d_in, int d_out,
+                             int S, uint32_t* err, bool pdl, cudaStream_t st,
+                             const DeviceInfo& dev);
+// bf16 W0 [d_in, d_out] -> 4-bit codes and bf16 absmax (see k_decode_q4.cu).
+cudaError_t launch_quantize_q4(const void* W0, const void* codebook, void* Wq, void* absmax,
+                               int d_in, int d_out, cudaStream_t st);
 // Decode-sized base GEMM split over d_in into S fp32 partials
 // partial[z, t, :] = x[t, K_z] W0[K_z, :], see k_decode_tc.cu.  `pdl`: launch
 // as a programmatic dependent (W0 is prefetched before the wait, x after).

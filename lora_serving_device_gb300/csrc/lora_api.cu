@@ -121,6 +121,11 @@ lora_status_t check_ws(const void* ws, size_t ws_bytes, size_t need) {
   return LORA_OK;
 }
 
+// 4-bit base shapes: whole 64-row scale blocks, 16-byte code rows.
+bool q4_dims_ok(int32_t d_in, int32_t d_out) {
+  return dim_ok(d_in) && dim_ok(d_out) && d_in % 64 == 0 && d_out % 32 == 0;
+}
+
 // Shared argument checks of the two ragged entry points.
 lora_status_t ragged_args(const void* x, const void* A_flat, const void* B_flat,
                           const int64_t* a_off, const int64_t* b_off, const int32_t* rank,
@@ -490,6 +495,74 @@ lora_status_t lora_linear_fused_ragged(const void* x, const void* W0, const void
   return from_cuda(launch_bgmv_adapter_ragged_merge(x, A_flat, B_flat, rp, slot_ids, scale,
                                                     w.partial, w.split, y, T, d_in, d_out,
                                                     n_slots, w.err, true, st));
+}
+
+lora_status_t lora_quantize_base_4bit(const void* W0, const void* codebook, void* W0q,
+                                      void* absmax, int32_t d_in, int32_t d_out, void* stream) {
+  if (!q4_dims_ok(d_in, d_out)) return LORA_ERR_SHAPE;
+  if (W0 == nullptr || codebook == nullptr || W0q == nullptr || absmax == nullptr ||
+      !aligned16(W0) || !aligned16(W0q) || !aligned16(absmax))
+    return LORA_ERR_INVALID_ARG;
+  DeviceInfo dev;
+  lora_status_t s = check_device(&dev);
+  if (s != LORA_OK) return s;
+  return from_cuda(launch_quantize_q4(W0, codebook, W0q, absmax, d_in, d_out,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+lora_status_t lora_base_gemm_4bit_splitk(const void* x, const void* W0q, const void* absmax,
+                                         const void* codebook, float* partial, int32_t T,
+                                         int32_t d_in, int32_t d_out, int32_t ksplit, void* ws,
+                                         size_t ws_bytes, void* stream) {
+  if (T < 0) return LORA_ERR_INVALID_ARG;
+  if (!tokens_ok(T) || !q4_dims_ok(d_in, d_out) || ksplit < 1 ||
+      ksplit > decode_q4_max_split(d_in))
+    return LORA_ERR_SHAPE;
+  if (x == nullptr || W0q == nullptr || absmax == nullptr || codebook == nullptr ||
+      partial == nullptr || !aligned16(x) || !aligned16(W0q) || !aligned16(absmax) ||
+      !aligned16(partial))
+    return LORA_ERR_INVALID_ARG;
+  lora_status_t s = check_ws(ws, ws_bytes, kErrBytes);
+  if (s != LORA_OK) return s;
+  if (T == 0) return LORA_OK;
+  DeviceInfo dev;
+  if ((s = check_device(&dev)) != LORA_OK) return s;
+  if (!tensor_map_available()) return LORA_ERR_CUDA;
+  return from_cuda(launch_decode_q4(x, W0q, absmax, codebook, partial, T, d_in, d_out, ksplit,
+                                    static_cast<uint32_t*>(ws), false,
+                                    static_cast<cudaStream_t>(stream), dev));
+}
+
+lora_status_t lora_linear_fused_4bit(const void* x, const void* W0q, const void* absmax,
+                                     const void* codebook, const void* A_pool,
+                                     const void* B_pool, const int32_t* slot_ids,
+                                     const float* scale, void* y, int32_t T, int32_t d_in,
+                                     int32_t d_out, int32_t r, int32_t n_slots, void* ws,
+                                     size_t ws_bytes, void* stream) {
+  if (T < 0) return LORA_ERR_INVALID_ARG;
+  if (T > kDecodeTokens || !q4_dims_ok(d_in, d_out) || !rank_ok(r) || !slots_ok(n_slots))
+    return LORA_ERR_SHAPE;
+  if (x == nullptr || W0q == nullptr || absmax == nullptr || codebook == nullptr ||
+      A_pool == nullptr || B_pool == nullptr || slot_ids == nullptr || y == nullptr ||
+      !aligned16(x) || !aligned16(W0q) || !aligned16(absmax) || !aligned16(A_pool) ||
+      !aligned16(B_pool) || !aligned16(y) || x == y)
+    return LORA_ERR_INVALID_ARG;
+  const FusedWs w = fused_ws_layout(ws, T, d_in, d_out, r, n_slots);
+  lora_status_t s = check_ws(ws, ws_bytes, w.bytes);
+  if (s != LORA_OK) return s;
+  if (T == 0) return LORA_OK;
+  DeviceInfo dev;
+  if ((s = check_device(&dev)) != LORA_OK) return s;
+  if (!tensor_map_available()) return LORA_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // the decode chain of lora_linear_fused with the 4-bit base GEMM (its
+  // split over 64-row blocks can always take the bf16 GEMM's split)
+  cudaError_t e = launch_decode_q4(x, W0q, absmax, codebook, w.partial, T, d_in, d_out, w.split,
+                                   w.err, true, st, dev);
+  if (e != cudaSuccess) return LORA_ERR_CUDA;
+  return from_cuda(launch_bgmv_adapter_merge(x, A_pool, B_pool, slot_ids, scale, w.partial,
+                                             w.split, y, T, d_in, d_out, r, n_slots, w.err,
+                                             true, st));
 }
 
 lora_status_t lora_base_gemm_splitk(const void* x, const void* W0, float* partial, int32_t T,

@@ -30,6 +30,7 @@ EXPORTS = ("lora_workspace_bytes", "lora_build_segments", "lora_bgmv_shrink", "l
            "lora_linear_fused_noalloc", "lora_bgmv_delta", "lora_bgmv_adapter",
            "lora_bgmv_adapter_merge", "lora_base_gemm_splitk", "lora_decode_split",
            "lora_slot_upload", "lora_bgmv_adapter_ragged", "lora_linear_fused_ragged",
+           "lora_quantize_base_4bit", "lora_base_gemm_4bit_splitk", "lora_linear_fused_4bit",
            "lora_get_error", "lora_status_string")
 
 
@@ -67,6 +68,10 @@ _SIGS = {
                                       _I, _I, _P, _Z, _P]),
     "lora_linear_fused_ragged": (_I, [_P, _P, _P, _P, _P, _P, _P, _L, _L, _I, _P, _P, _P, _I, _I,
                                       _I, _I, _I, _P, _Z, _P]),
+    "lora_quantize_base_4bit": (_I, [_P, _P, _P, _P, _I, _I, _P]),
+    "lora_base_gemm_4bit_splitk": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _Z, _P]),
+    "lora_linear_fused_4bit": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P,
+                                    _Z, _P]),
     "lora_get_error": (_I, [_P, _P, ctypes.POINTER(ctypes.c_int32)]),
     "lora_status_string": (ctypes.c_char_p, [_I]),
 }
@@ -190,6 +195,22 @@ def lora_linear_fused_ragged(x, W0, A_flat, B_flat, a_off, b_off, rank, a_elems,
     return _call("lora_linear_fused_ragged", x, W0, A_flat, B_flat, a_off, b_off, rank, a_elems,
                  b_elems, r_max, slot_ids, scale, y, T, d_in, d_out, n_slots, dt, ws, ws_bytes,
                  stream)
+
+
+def lora_quantize_base_4bit(W0, codebook, W0q, absmax, d_in, d_out, stream):
+    return _call("lora_quantize_base_4bit", W0, codebook, W0q, absmax, d_in, d_out, stream)
+
+
+def lora_base_gemm_4bit_splitk(x, W0q, absmax, codebook, partial, T, d_in, d_out, ksplit, ws,
+                               ws_bytes, stream):
+    return _call("lora_base_gemm_4bit_splitk", x, W0q, absmax, codebook, partial, T, d_in, d_out,
+                 ksplit, ws, ws_bytes, stream)
+
+
+def lora_linear_fused_4bit(x, W0q, absmax, codebook, A_pool, B_pool, slot_ids, scale, y, T, d_in,
+                           d_out, r, n_slots, ws, ws_bytes, stream):
+    return _call("lora_linear_fused_4bit", x, W0q, absmax, codebook, A_pool, B_pool, slot_ids,
+                 scale, y, T, d_in, d_out, r, n_slots, ws, ws_bytes, stream)
 
 
 def lora_get_error(ws, stream):
@@ -476,6 +497,62 @@ def linear_fused_ragged_t(x, W0, pool, slot_ids, scale, ws, y=None, stream=None)
                                    _ptr(slot_ids), _ptr(scale), _ptr(y), T, d_in, d_out,
                                    pool.n_slots, _dt(x), _ptr(ws), ws.numel(), _stream(stream)),
           "lora_linear_fused_ragged")
+    return y
+
+
+class Base4bit:
+    """A 4-bit base matrix on the device: codes W0q [d_out, d_in / 2] uint8 (k contiguous
+    per column, row 2i in the low nibble of byte i), absmax [d_in / 64, d_out] bf16,
+    codebook [16] bf16."""
+
+    def __init__(self, W0q, absmax, codebook):
+        self.W0q, self.absmax, self.codebook = W0q, absmax, codebook
+        self.d_out = int(W0q.shape[0])
+        self.d_in = int(W0q.shape[1]) * 2
+
+    @classmethod
+    def quantize(cls, W0, codebook, stream=None):
+        """Quantise a bf16 W0 [d_in, d_out] with the library's kernel."""
+        import torch
+        d_in, d_out = W0.shape
+        W0q = torch.empty((d_out, d_in // 2), dtype=torch.uint8, device=W0.device)
+        absmax = torch.empty((d_in // 64, d_out), dtype=torch.bfloat16, device=W0.device)
+        check(lora_quantize_base_4bit(_ptr(W0), _ptr(codebook), _ptr(W0q), _ptr(absmax), d_in,
+                                      d_out, _stream(stream)), "lora_quantize_base_4bit")
+        return cls(W0q, absmax, codebook)
+
+    @property
+    def nbytes(self):
+        return self.W0q.numel() + self.absmax.numel() * 2
+
+
+def base_gemm_4bit_splitk_t(x, base, ws, ksplit=None, partial=None, stream=None):
+    """fp32 split-K product partial[s] = x[:, K_s] deq(W0)[K_s, :] of a Base4bit."""
+    import torch
+    T, d_in = x.shape
+    if ksplit is None:
+        ksplit = lora_decode_split(T, d_in, base.d_out) or 1
+    if partial is None:
+        partial = torch.empty((ksplit, T, base.d_out), dtype=torch.float32, device=x.device)
+    check(lora_base_gemm_4bit_splitk(_ptr(x), _ptr(base.W0q), _ptr(base.absmax),
+                                     _ptr(base.codebook), _ptr(partial), T, d_in, base.d_out,
+                                     ksplit, _ptr(ws), ws.numel(), _stream(stream)),
+          "lora_base_gemm_4bit_splitk")
+    return partial
+
+
+def linear_fused_4bit_t(x, base, A_pool, B_pool, slot_ids, scale, ws, y=None, stream=None):
+    """y = x deq(W0) + s (x A) B over a Base4bit (decode-sized bf16 batches, T <= 256)."""
+    import torch
+    T, d_in = x.shape
+    n_slots, _, r = A_pool.shape
+    if y is None:
+        y = torch.empty((T, base.d_out), dtype=x.dtype, device=x.device)
+    check(lora_linear_fused_4bit(_ptr(x), _ptr(base.W0q), _ptr(base.absmax), _ptr(base.codebook),
+                                 _ptr(A_pool), _ptr(B_pool), _ptr(slot_ids), _ptr(scale), _ptr(y),
+                                 T, d_in, base.d_out, r, n_slots, _ptr(ws), ws.numel(),
+                                 _stream(stream)),
+          "lora_linear_fused_4bit")
     return y
 
 

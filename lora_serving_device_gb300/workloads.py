@@ -118,6 +118,40 @@ def _normal(rng, shape, std, dtype_bf16: bool) -> np.ndarray:
     return bf16_round(a) if dtype_bf16 else a
 
 
+def nf4_like_codebook():
+    """A 16-entry 4-bit codebook of normal-float kind: levels at quantiles of
+    N(0, 1) (8 above zero, 7 below, and an exact zero), scaled so the
+    extremes are -1 and +1, rounded to bf16 (returned as float32).  The
+    pages name QLoRA-style 4-bit bases without listing levels; this is one
+    codebook of that family, an input like the weights."""
+    from statistics import NormalDist
+    nd = NormalDist()
+    p_top = 0.97
+    pos = [nd.inv_cdf(0.5 + (p_top - 0.5) * i / 8) for i in range(1, 9)]
+    neg = [-nd.inv_cdf(0.5 + (p_top - 0.5) * i / 7) for i in range(1, 8)]
+    top = pos[-1]
+    vals = sorted([v / top for v in neg] + [0.0] + [v / top for v in pos])
+    vals[0], vals[-1] = -1.0, 1.0
+    return bf16_round(np.array(vals, np.float32))
+
+
+def pack_nibbles(codes):
+    """Byte layout of a 4-bit matrix [d_in, d_out] -> [d_out, d_in / 2] uint8,
+    k contiguous per column: byte i of row n holds rows 2i (low nibble) and
+    2i + 1 (high nibble) of column n."""
+    c = np.ascontiguousarray(np.asarray(codes, np.uint8).T)
+    return (c[:, 0::2] | (c[:, 1::2] << np.uint8(4))).astype(np.uint8)
+
+
+def random_4bit_base(seed, d_in, d_out):
+    """Seeded 4-bit base inputs: codes uniform over 0..15 and bf16 block
+    scales in [0.005, 0.05] (absmax [d_in / 64, d_out])."""
+    rng = np.random.default_rng([SEED_BASE, 41, seed])
+    codes = rng.integers(0, 16, (d_in, d_out)).astype(np.uint8)
+    absmax = bf16_round(rng.uniform(0.005, 0.05, (d_in // 64, d_out)).astype(np.float32))
+    return codes, absmax
+
+
 def make_pools(key, n_slots, d_in, d_out, r, slots=None, bf16=True,
                a_std=A_STD, b_std=B_STD, ranks=None):
     """Adapter pools, drawn slot by slot from per-slot streams.

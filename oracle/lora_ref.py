@@ -135,6 +135,63 @@ def lora_linear_ragged(x, W0, A_list, B_list, scale, slot_ids):
     return y
 
 
+# ----------------------------------------------------------------------------
+# 4-bit base matrix ([Concepts, "When It Falls Down"]: QLoRA-style 4-bit base
+# models next to bf16 adapters).  The pages name the style, not the format;
+# the reading taken: a 16-entry codebook scaled per block of 64 consecutive
+# d_in rows of a column by the block's absolute maximum; a weight's code is
+# the entry nearest weight / absmax; the dequantised weight is
+# codebook[code] * absmax rounded once to bf16, the type of the adapter path.
+# ----------------------------------------------------------------------------
+Q4_BLOCK = 64
+
+
+def bf16_round(a):
+    """Nearest bf16 value of each fp32 value (ties to even), as float64."""
+    f = np.ascontiguousarray(np.asarray(a, dtype=np.float32))
+    u = f.view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
+    return u.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def quantize_4bit(W, codebook):
+    """codes [d_in, d_out] (0..15) and absmax [d_in / 64, d_out] of W.
+
+    absmax: the largest |w| of each block; code: the entry of the codebook
+    nearest w / absmax, the quotient and the distances in fp32 (ties go to
+    the lower code); a block of zeros takes the entry nearest 0."""
+    W = np.asarray(W, dtype=np.float32)
+    cb = np.asarray(codebook, dtype=np.float32)
+    d_in, d_out = W.shape
+    blocks = W.reshape(d_in // Q4_BLOCK, Q4_BLOCK, d_out)
+    absmax = np.abs(blocks).max(axis=1)
+    safe = np.where(absmax > 0, absmax, np.float32(1.0)).astype(np.float32)
+    v = np.where(absmax[:, None, :] > 0, blocks / safe[:, None, :], np.float32(0.0))
+    v = v.astype(np.float32)
+    best = np.abs(v - cb[0])
+    codes = np.zeros(v.shape, np.uint8)
+    for c in range(1, cb.size):
+        d = np.abs(v - cb[c])
+        better = d < best
+        codes[better] = c
+        best = np.where(better, d, best)
+    return codes.reshape(d_in, d_out), absmax
+
+
+def dequantize_4bit(codes, absmax, codebook):
+    """deq[k, n] = bf16(codebook[codes[k, n]] * absmax[k // 64, n]) (fp32 product)."""
+    cb = np.asarray(codebook, dtype=np.float32)
+    s = np.repeat(np.asarray(absmax, dtype=np.float32), Q4_BLOCK, axis=0)
+    return bf16_round(cb[np.asarray(codes)] * s)
+
+
+def pack_4bit(codes):
+    """The stored code matrix [d_out, d_in / 2] of codes [d_in, d_out]: byte i
+    of row n holds rows 2i (low nibble) and 2i + 1 (high nibble) of column n."""
+    c = np.asarray(codes, dtype=np.uint8).T
+    return (c[:, 0::2] | (c[:, 1::2] << 4)).astype(np.uint8)
+
+
 def build_segments(slot_ids, n_slots):
     """SGMV segments ([Handbook], SGMV bullet and its toy script): stable sort
     of the tokens by id, then runs of equal ids.

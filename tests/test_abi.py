@@ -21,7 +21,7 @@ def L():
 def declared_functions():
     src = open(HEADER).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(lora_[a-z_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(lora_[a-z0-9_]+)\s*\(", src)))
 
 
 def test_header_declares_the_boundary():
@@ -149,6 +149,32 @@ def test_ragged_validation(L):
     assert delta(T=65536) == 2
     assert delta(r_max=12) == 2
     assert delta(T=0) == 0
+
+
+def test_4bit_validation(L):
+    WS, NW = FAKE + 8192, 1 << 20
+    q = L.lora_quantize_base_4bit
+    # (W0, codebook, W0q, absmax, d_in, d_out, stream)
+    assert q(FAKE, FAKE, FAKE, FAKE, 96, 64, None) == 2      # d_in not a multiple of 64
+    assert q(FAKE, FAKE, FAKE, FAKE, 128, 48, None) == 2     # d_out not a multiple of 32
+    assert q(None, FAKE, FAKE, FAKE, 128, 64, None) == 1
+    assert q(FAKE, FAKE, FAKE + 8, FAKE, 128, 64, None) == 1
+    g = L.lora_base_gemm_4bit_splitk
+    # (x, W0q, absmax, codebook, partial, T, d_in, d_out, ksplit, ws, ws_bytes, stream)
+    assert g(FAKE, FAKE, FAKE, FAKE, FAKE, 8, 128, 64, 3, WS, NW, None) == 2   # ksplit > blocks
+    assert g(FAKE, FAKE, FAKE, FAKE, FAKE, 8, 128, 64, 0, WS, NW, None) == 2
+    assert g(FAKE, FAKE, FAKE, None, FAKE, 8, 128, 64, 1, WS, NW, None) == 1
+    assert g(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 128, 64, 2, WS, NW, None) == 0   # empty batch
+    f = L.lora_linear_fused_4bit
+    # (x, W0q, absmax, codebook, A, B, ids, scale, y, T, d_in, d_out, r, n_slots, ws, ..)
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE + 4096, 257, 128, 64, 16, 4,
+             WS, NW, None) == 2                                          # decode-sized only
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE + 4096, 8, 128, 64, 12, 4,
+             WS, NW, None) == 2                                          # rank
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, 8, 128, 64, 16, 4,
+             WS, NW, None) == 1                                          # x == y
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE + 4096, 8, 128, 64, 16, 4,
+             WS, 16, None) == 4                                          # workspace
 
 
 def test_ragged_rank_class():

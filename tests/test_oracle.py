@@ -215,6 +215,94 @@ def test_ragged_brute_force_and_padding():
     assert not np.allclose(cut, want, rtol=1e-6, atol=1e-6)
 
 
+def test_bf16_round_closed_forms():
+    """Ties to even at the 8-bit significand, and agreement with rounding
+    x / ulp(x) half to even in float64 for normal numbers."""
+    one = 1.0
+    cases = {one: one, one + 2.0 ** -8: one, one + 3 * 2.0 ** -8: one + 2.0 ** -6,
+             one + 2.0 ** -8 + 2.0 ** -20: one + 2.0 ** -7, -(one + 2.0 ** -8): -one,
+             0.0: 0.0, 3.0: 3.0, 2.0 ** -100: 2.0 ** -100}
+    got = O.bf16_round(np.array(list(cases), np.float32))
+    assert got.tolist() == list(cases.values())
+    rng = np.random.default_rng(3)
+    x = (rng.standard_normal(4000) * 10.0 ** rng.uniform(-6, 6, 4000)).astype(np.float32)
+    xd = x.astype(np.float64)
+    ulp = 2.0 ** (np.floor(np.log2(np.abs(xd))) - 7)
+    want = np.round(xd / ulp) * ulp             # numpy rounds half to even
+    np.testing.assert_array_equal(O.bf16_round(x), want)
+
+
+def _codebook():
+    return O.bf16_round(np.array(W.nf4_like_codebook(), np.float32))
+
+
+def test_quantize_4bit_recovers_exact_codes():
+    """Weights built as absmax * codebook[code], each block holding a +-1
+    entry, quantise back to those codes and scales exactly; scales that vary
+    along both axes catch blocks taken along the wrong axis."""
+    cb = _codebook()
+    assert cb.size == 16 and np.unique(cb).size == 16 and cb.min() == -1 and cb.max() == 1
+    rng = np.random.default_rng(8)
+    d_in, d_out = 256, 40
+    codes = rng.integers(0, 16, (d_in, d_out)).astype(np.uint8)
+    codes[::64] = 15                                  # codebook[15] = +1 in every block
+    s = O.bf16_round(rng.uniform(0.01, 0.2, (d_in // 64, d_out)).astype(np.float32))
+    Wt = (cb[codes] * np.repeat(s, 64, axis=0)).astype(np.float32)
+    got_c, got_s = O.quantize_4bit(Wt, cb)
+    np.testing.assert_array_equal(got_c, codes)
+    np.testing.assert_array_equal(got_s, s)
+    np.testing.assert_array_equal(O.dequantize_4bit(got_c, got_s, cb), O.bf16_round(Wt))
+    # blocks along the other axis give other scales
+    wrong = np.abs(Wt.reshape(d_in, d_out // 8, 8)).max(axis=2)
+    assert wrong.shape != got_s.shape or not np.array_equal(wrong, got_s)
+
+
+def test_quantize_4bit_brute_force():
+    """Scalar loops over a tiny matrix with a zero block, in fp32 scalars."""
+    cb = _codebook().astype(np.float32)
+    rng = np.random.default_rng(12)
+    d_in, d_out = 128, 6
+    Wt = O.bf16_round(rng.standard_normal((d_in, d_out)).astype(np.float32) * 0.02)
+    Wt[64:, 2] = 0.0
+    Wt = Wt.astype(np.float32)
+    codes, absmax = O.quantize_4bit(Wt, cb)
+    for b in range(d_in // 64):
+        for n in range(d_out):
+            m = np.float32(0.0)
+            for k in range(64):
+                m = max(m, np.float32(abs(Wt[64 * b + k, n])))
+            assert absmax[b, n] == m
+            for k in range(64):
+                v = np.float32(Wt[64 * b + k, n]) / m if m > 0 else np.float32(0.0)
+                dists = [abs(np.float32(v) - cb[c]) for c in range(16)]
+                assert codes[64 * b + k, n] == int(np.argmin(dists))
+    assert np.all(codes[64:, 2] == int(np.argmin(np.abs(cb))))
+
+
+def test_dequantize_4bit_error_bound_and_packing():
+    """|w - deq(w)| is at most half the widest codebook gap times absmax plus
+    one bf16 rounding; the packing keeps k contiguous per column."""
+    cb = _codebook()
+    rng = np.random.default_rng(13)
+    Wt = O.bf16_round(rng.standard_normal((192, 64)).astype(np.float32) * 0.02)
+    codes, absmax = O.quantize_4bit(Wt, cb)
+    deq = O.dequantize_4bit(codes, absmax, cb)
+    gap = np.max(np.diff(np.sort(cb)))
+    s = np.repeat(absmax.astype(np.float64), 64, axis=0)
+    assert np.all(np.abs(Wt - deq) <= s * gap / 2 * (1 + 1e-6) + np.abs(deq) * 2.0 ** -8)
+    assert np.max(np.abs(Wt - deq)) > 0
+    packed = O.pack_4bit(codes)
+    assert packed.shape == (64, 96)
+    np.testing.assert_array_equal(packed & 15, codes[0::2, :].T)
+    np.testing.assert_array_equal(packed >> 4, codes[1::2, :].T)
+    assert packed[5, 7] == codes[14, 5] | (codes[15, 5] << 4)
+    # one value worked by hand: code 3 at scale 0.5
+    c3 = np.zeros((64, 2), np.uint8)
+    c3[0, 1] = 3
+    d = O.dequantize_4bit(c3, np.array([[1.0, 0.5]], np.float32), cb)
+    assert d[0, 1] == O.bf16_round(np.float32(cb[3]) * np.float32(0.5))[()]
+
+
 # ----------------------------------------------------------------------------
 # the pages' printed figures
 # ----------------------------------------------------------------------------
