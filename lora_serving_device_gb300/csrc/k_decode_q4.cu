@@ -44,7 +44,7 @@ namespace {
 constexpr int kQGroups = 4;                       // dequantising groups of 4 warps
 constexpr int kQDqWarps = 4 * kQGroups;
 constexpr int kQThreads = 64 + 32 * kQDqWarps;     // + the producer and MMA warps
-constexpr int kQND = 2 * kQGroups;                 // dequantised A tiles in TMEM (32 columns each)
+constexpr int kQSB = 2;   // TMEM buffers of dequantised A, one code stage (4 K blocks, 128 columns) each
 constexpr uint32_t kQLutBytes = 256 * 32 * 4;
 constexpr uint32_t kQStage = 128 * 128 + 1024;  // codes of 4 K blocks x 128 columns + scales
 constexpr uint64_t kQWaitNs = 2000000000ull;
@@ -63,16 +63,16 @@ template <int BT>
 struct Q4Layout {
   static constexpr uint32_t kX = BT * 128;             // x: BT tokens x 64 K, K-major, swizzled
   static constexpr uint32_t kOutBytes = BT * 128 * 4;  // fp32 partial tile, token-major
-  static constexpr int kTmemCols = BT + kQND * 32 <= 256 ? 256 : 512;
+  static constexpr int kTmemCols = 512;  // the accumulator, then the kQSB stage buffers
   static __host__ __device__ uint32_t qring(int xs) { return xs * kX; }
   static __host__ __device__ uint32_t lut(int xs, int qs) {
     const uint32_t rings = xs * kX + qs * kQStage;
     return rings > kOutBytes ? rings : ((kOutBytes + 1023u) & ~1023u);
   }
   static __host__ __device__ uint32_t bars(int xs, int qs) { return lut(xs, qs) + kQLutBytes; }
-  // x_full[xs], x_empty[xs], q_full[qs], q_empty[qs], dq_full[kQND], dq_empty[kQND], accum
+  // x_full[xs], q_full[qs], q_empty[qs], dq_full[kQSB], dq_empty[kQSB], accum
   static __host__ __device__ uint32_t misc(int xs, int qs) {
-    return bars(xs, qs) + (2 * xs + 2 * qs + 2 * kQND + 1) * 8;
+    return bars(xs, qs) + (xs + 2 * qs + 2 * kQSB + 1) * 8;
   }
   static __host__ __device__ uint32_t total(int xs, int qs) { return misc(xs, qs) + 16; }
 };
@@ -105,7 +105,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
   constexpr int kTmemCols = Lay::kTmemCols;
   constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(128, BT, false, false);
   static_assert(BT % 16 == 0 && BT >= 32 && BT <= 256, "token tile");
-  static_assert(BT + kQND * 32 <= kTmemCols && kQGroups == 4, "TMEM columns; one group per K block");
+  static_assert(BT + kQSB * 128 <= kTmemCols && kQGroups == 4, "TMEM columns; one group per K block");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -113,12 +113,11 @@ __global__ void __launch_bounds__(kQThreads, 1)
   uint8_t* qring = smem + Lay::qring(p.xs);
   uint32_t* lut = reinterpret_cast<uint32_t*>(smem + Lay::lut(p.xs, p.qs));
   uint64_t* x_full = reinterpret_cast<uint64_t*>(smem + Lay::bars(p.xs, p.qs));
-  uint64_t* x_empty = x_full + p.xs;
-  uint64_t* q_full = x_empty + p.xs;
+  uint64_t* q_full = x_full + p.xs;
   uint64_t* q_empty = q_full + p.qs;
   uint64_t* dq_full = q_empty + p.qs;
-  uint64_t* dq_empty = dq_full + kQND;
-  uint64_t* accum_full = dq_empty + kQND;
+  uint64_t* dq_empty = dq_full + kQSB;
+  uint64_t* accum_full = dq_empty + kQSB;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::misc(p.xs, p.qs));
   volatile int* abort_f = reinterpret_cast<volatile int*>(smem + Lay::misc(p.xs, p.qs) + 8);
 
@@ -137,16 +136,13 @@ __global__ void __launch_bounds__(kQThreads, 1)
       ptx::prefetch_tmap(&tm_s);
       ptx::prefetch_tmap(&tm_x);
       ptx::prefetch_tmap(&tm_p);
-      for (int i = 0; i < p.xs; ++i) {
-        ptx::mbar_init(&x_full[i], 1);
-        ptx::mbar_init(&x_empty[i], 1);
-      }
+      for (int i = 0; i < p.xs; ++i) ptx::mbar_init(&x_full[i], 1);
       for (int i = 0; i < p.qs; ++i) {
         ptx::mbar_init(&q_full[i], 1);
         ptx::mbar_init(&q_empty[i], kQDqWarps);  // every dequantising warp releases it
       }
-      for (int i = 0; i < kQND; ++i) {
-        ptx::mbar_init(&dq_full[i], 4);
+      for (int i = 0; i < kQSB; ++i) {
+        ptx::mbar_init(&dq_full[i], kQDqWarps);  // every dequantising warp fills its part
         ptx::mbar_init(&dq_empty[i], 1);
       }
       ptx::mbar_init(accum_full, 1);
@@ -168,7 +164,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
     ptx::tc_fence_after();
   }
   const uint32_t tmem = warp == 0 ? 0u : *tmem_slot;
-  const uint32_t a_tmem = tmem + BT;  // the kQND dequantised tiles follow the accumulator
+  const uint32_t a_tmem = tmem + BT;  // the kQSB stage buffers follow the accumulator
 
   if (warp == 0) {
     // ---------------- producer -------------------------------------------
@@ -189,9 +185,15 @@ __global__ void __launch_bounds__(kQThreads, 1)
     int iq_next = q_pre;
     for (int it = 0; it < n_it; ++it) {
       const int s = it % p.xs;
-      if (it >= p.xs &&
-          !q4_warp_wait(&x_empty[s], (static_cast<uint32_t>(it / p.xs) & 1u) ^ 1u, abort_f))
-        break;
+      // the slot's previous tile, x of block b = it - xs, is free once the MMAs
+      // of b's code stage completed: the commit that frees that stage's TMEM
+      // buffer (phase (b / 4) / kQSB of dq_empty[(b / 4) % kQSB]; with xs <= 8
+      // that barrier cannot have moved two phases past it)
+      if (it >= p.xs) {
+        const int sq = (it - p.xs) / 4;
+        if (!q4_warp_wait(&dq_empty[sq % kQSB], static_cast<uint32_t>(sq / kQSB) & 1u, abort_f))
+          break;
+      }
       if (lane == 0) {
         ptx::mbar_arrive_expect_tx(&x_full[s], Lay::kX);
         ptx::tma_load_2d(smem + static_cast<size_t>(s) * Lay::kX, &tm_x, &x_full[s],
@@ -220,22 +222,31 @@ __global__ void __launch_bounds__(kQThreads, 1)
   } else if (warp == 1) {
     // ---------------- MMA issuer -----------------------------------------
     if (lane == 0) {
-      for (int it = 0; it < n_it; ++it) {
-        const int s = it % p.xs, d = it % kQND;
-        const uint32_t ph = static_cast<uint32_t>(it / p.xs) & 1u;
-        const uint32_t dph = static_cast<uint32_t>(it / kQND) & 1u;
-        if (!ptx::mbar_wait_bounded(&x_full[s], ph, abort_f, kQWaitNs)) break;
-        if (!ptx::mbar_wait_bounded(&dq_full[d], dph, abort_f, kQWaitNs)) break;
+      bool live = true;
+      for (int iq = 0; iq < n_q && live; ++iq) {
+        const int sb = iq % kQSB;
+        if (!ptx::mbar_wait_bounded(&dq_full[sb], static_cast<uint32_t>(iq / kQSB) & 1u, abort_f,
+                                    kQWaitNs))
+          break;
         ptx::tc_fence_after();
-        const uint32_t xa = ptx::smem_u32(smem + static_cast<size_t>(s) * Lay::kX);
+        for (int j = 0; j < 4 && 4 * iq + j < n_it; ++j) {
+          const int it = 4 * iq + j, s = it % p.xs;
+          if (!ptx::mbar_wait_bounded(&x_full[s], static_cast<uint32_t>(it / p.xs) & 1u, abort_f,
+                                      kQWaitNs)) {
+            live = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t xa = ptx::smem_u32(smem + static_cast<size_t>(s) * Lay::kX);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          // A: 16 K elements = 8 TMEM columns per step; x: K-major, 32 bytes per step
-          const uint64_t xd = ptx::sdesc_sw128(xa + kk * 32, 16, 1024);
-          ptx::mma_bf16_ta(tmem, a_tmem + d * 32 + kk * 8, xd, kIdesc, (it > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < 4; ++kk) {
+            // A: 16 K elements = 8 TMEM columns per step; x: K-major, 32 bytes per step
+            const uint64_t xd = ptx::sdesc_sw128(xa + kk * 32, 16, 1024);
+            ptx::mma_bf16_ta(tmem, a_tmem + sb * 128 + j * 32 + kk * 8, xd, kIdesc,
+                             (it > 0 || kk > 0) ? 1u : 0u);
+          }
         }
-        ptx::mma_commit(&dq_empty[d]);
-        ptx::mma_commit(&x_empty[s]);
+        if (live) ptx::mma_commit(&dq_empty[sb]);  // frees stage buffer sb and its x slots
       }
       ptx::mma_commit(accum_full);
     }
@@ -280,30 +291,32 @@ __global__ void __launch_bounds__(kQThreads, 1)
       {
         const int j = grp;           // K block within the stage
         const int it = 4 * iq + j;   // K block of the CTA
-        if (it < n_it && ok) {       // warp-uniform
-          const int d = it % kQND;
+        const int sb = iq % kQSB;
+        uint32_t v[32];
+        if (it < n_it) {             // warp-uniform
           const uint4 lo = *reinterpret_cast<const uint4*>(st + m * 128 + (((2 * j) ^ sw) << 4));
           const uint4 hi = *reinterpret_cast<const uint4*>(st + m * 128 + (((2 * j + 1) ^ sw) << 4));
           const uint32_t s = *reinterpret_cast<const uint16_t*>(st + 128 * 128 + j * 256 + m * 2);
           const uint32_t s2 = s | (s << 16);
           const uint32_t w8[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-          uint32_t v[32];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
 #pragma unroll
             for (int bb = 0; bb < 4; ++bb)
               v[4 * e + bb] = bf16x2_mul(lut_l[((w8[e] >> (8 * bb)) & 0xffu) * 32], s2);
           }
-          ok = q4_warp_wait(&dq_empty[d], (static_cast<uint32_t>(it / kQND) & 1u) ^ 1u, abort_f);
-          if (ok) {
-            ptx::tc_fence_after();
-            ptx::tmem_st32(a_tmem + lane_base + d * 32, v);
-            ptx::tmem_st_wait();
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&dq_full[d]);
-          }
         }
+        // the buffer is free once the MMAs of the stage two back completed
+        ok = q4_warp_wait(&dq_empty[sb], (static_cast<uint32_t>(iq / kQSB) & 1u) ^ 1u, abort_f);
+        if (!ok) break;
+        if (it < n_it) {
+          ptx::tc_fence_after();
+          ptx::tmem_st32(a_tmem + lane_base + sb * 128 + j * 32, v);
+          ptx::tmem_st_wait();
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&dq_full[sb]);  // every warp, block or not
       }
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&q_empty[qsl]);  // this warp is done with the stage
@@ -357,8 +370,11 @@ cudaError_t launch_q4_variant(const CUtensorMap& tm_x, const CUtensorMap& tm_q,
                               const DeviceInfo& dev) {
   using Lay = Q4Layout<BT>;
   // x ring: about 64 KB of x; code ring: as deep as the rest allows (<= 8)
+  // x slots are recycled a code stage (4 K blocks) at a time through the
+  // dq_empty barriers, so the ring must hold a whole stage (4 <= xs <= 8; see
+  // the producer)
   int xs = static_cast<int>(65536 / Lay::kX);
-  if (xs < 2) xs = 2;
+  if (xs < 4) xs = 4;
   if (xs > 8) xs = 8;
   int qs = 0;
   for (int s = 8; s >= 2; --s) {
