@@ -2,12 +2,13 @@
 """Throughput of the multi-LoRA batched linear layer on GB300.
 
 One step = one pass of the whole layer over one batch (lora_linear_fused):
-for this decode batch one launch computes the per-token (BGMV) adapter term
-(shrink, cluster sum, expand into fp32) and the tcgen05 base GEMM adds it in
-its epilogue and stores y once -- on the decode workload: one 4096->4096
-layer, rank 16, 256 resident adapters, 64 one-token requests with Zipf(1.1)
-adapter ids and 8 base-only rows.  Inputs are seeded and synthetic; weights
-and activations are resident in HBM before timing.
+for this decode batch the tcgen05 base GEMM writes fp32 partials split over
+d_in, then one kernel computes each token's (BGMV) adapter term (shrink,
+cluster sum, expand), adds the summed partials and stores y once -- on the
+decode workload: one 4096->4096 layer, rank 16, 256 resident adapters, 64
+one-token requests with Zipf(1.1) adapter ids and 8 base-only rows.  Inputs
+are seeded and synthetic; weights and activations are resident in HBM before
+timing.
 
 Reported on one JSON line (rank 0):
   value     tokens/s over K steps (CUDA-graph replays; 4 rotating buffer sets
@@ -20,10 +21,13 @@ Reported on one JSON line (rank 0):
             against the measured HBM copy peak
   sweep     tokens/s and achieved GB/s over distinct adapters per batch
             (4096->4096, rank 16, 1024-slot pool; T = 32 and 256)
-  configs   the prefill workload (and the 8B-shaped stack with --stack)
+  configs   the decode layer over a 4-bit base, the prefill workload, and
+            with --stack the 8B-shaped stack, padded and with ragged ranks
   cpu_baseline  the fp64 CPU oracle on the host cores (a bounded sample)
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+    python bench.py --profile CASE    a few untimed launches of one workload's
+                                      kernels, for a profiler (no JSON line)
 """
 from __future__ import annotations
 
@@ -60,6 +64,8 @@ def parse_args(argv=None):
     p.add_argument("--no-prefill", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--stack", action="store_true", help="also time the 224-layer 8B-shaped stack")
+    p.add_argument("--profile", choices=["decode", "prefill", "decode4bit", "ragged"],
+                   help="run 3 untimed passes of one workload and exit (for ncu)")
     a = p.parse_args(argv)
     if a.warmup < 3:
         p.error("--warmup must be >= 3")
@@ -832,8 +838,72 @@ def run_ours(args):
     return 0
 
 
+def run_profile(case):
+    """Three untimed passes of one workload's kernels, nothing else: a short
+    command for a profiler's launch list or a single-kernel capture."""
+    import numpy as np
+    import torch
+    from lora_serving_device_gb300 import build as B
+    from lora_serving_device_gb300 import lora as L
+    from lora_serving_device_gb300 import workloads as W
+    if not os.path.exists(L.LIB_PATH):
+        B.build()
+    L.load()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(device=dev)
+    if case == "prefill":
+        lengths, slots = W.prefill_ids()
+        ids_np = np.repeat(np.array(slots, np.int32), np.array(lengths))
+        T, d_in, d_out, r, n_slots = int(ids_np.size), 4096, 14336, 64, 64
+        x = device_normal((T, d_in), 1.0, 30301, dev)
+        W0 = device_normal((d_in, d_out), W.W0_STD, 30302, dev)
+        A = device_normal((n_slots, d_in, r), W.A_STD, 30303, dev)
+        Bp = device_normal((n_slots, r, d_out), W.B_STD, 30304, dev)
+        ids = torch.from_numpy(ids_np).to(dev)
+        scale = torch.full((n_slots,), W.SCALE, dtype=torch.float32, device=dev)
+        y = torch.empty((T, d_out), dtype=torch.bfloat16, device=dev)
+        ws = L.workspace(L.OP_LINEAR_FUSED, T, d_in, d_out, r, n_slots)
+        ks = fused_ksplit(T, d_in, n_slots)
+        wss = torch.zeros(256, dtype=torch.uint8, device=dev)
+        vpart = torch.zeros((ks, T, r), dtype=torch.float32, device=dev)
+        for _ in range(3):
+            L.linear_fused_t(x, W0, A, Bp, ids, scale, ws, y=y, stream=stream)
+            segs = L.build_segments_t(ids, n_slots, wss, stream=stream)
+            L.sgmv_shrink_t(x, A, segs, scale, ks, wss, v_partial=vpart, stream=stream)
+            L.sgmv_expand_t(vpart, Bp, segs, y, wss, stream=stream)
+        err = L.get_error_t(ws, stream=stream)
+    else:
+        w = W.decode_bgmv()
+        s0 = LayerSet(_up(w.x, dev), _up(w.W0, dev), _up(w.A_pool, dev), _up(w.B_pool, dev),
+                      torch.from_numpy(w.slot_ids).to(dev), torch.from_numpy(w.scale).to(dev),
+                      torch.empty((w.T, w.d_out), dtype=torch.bfloat16, device=dev))
+        ws = L.workspace(L.OP_LINEAR_FUSED, w.T, w.d_in, w.d_out, w.r, w.n_slots, device=dev)
+        if case == "decode4bit":
+            base = L.Base4bit.quantize(s0.W0, _up(W.nf4_like_codebook(), dev), stream=stream)
+            run = lambda: L.linear_fused_4bit_t(s0.x, base, s0.A, s0.B, s0.ids, s0.scale, ws,
+                                                y=s0.y, stream=stream)
+        elif case == "ragged":
+            ranks = W.stack_ranks(w.n_slots) // 4          # 2, 4 or 16 -> classes 8, 8, 16
+            pool = L.RaggedPool.from_padded(s0.A, s0.B, np.minimum(ranks, w.r))
+            run = lambda: L.linear_fused_ragged_t(s0.x, s0.W0, pool, s0.ids, s0.scale, ws,
+                                                  y=s0.y, stream=stream)
+        else:
+            run = lambda: L.linear_fused_t(s0.x, s0.W0, s0.A, s0.B, s0.ids, s0.scale, ws,
+                                           y=s0.y, stream=stream)
+        for _ in range(3):
+            run()
+        err = L.get_error_t(ws, stream=stream)
+    stream.synchronize()
+    if err:
+        raise SystemExit(f"device error word {err:#x}")
+    print(f"profile case {case}: 3 passes done")
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
+    if args.profile:
+        return run_profile(args.profile)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)
