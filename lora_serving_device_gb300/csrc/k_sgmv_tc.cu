@@ -308,7 +308,12 @@ struct ExpandLayout {
   static constexpr uint32_t kBBox = R * 128;                 // 64 columns x R rows
   static constexpr uint32_t kB = (kXN / 64) * kBBox;
   static constexpr uint32_t kBars = kV + 2 * kB;
-  static constexpr uint32_t kTotal = kBars + 8 * 8 + 16;
+  // per epilogue warp: 32 rows x 64 accumulator columns (+4 floats of padding
+  // per row, so the 32 rows' float4 writes hit distinct banks)
+  static constexpr int kStLd = 64 + 4;
+  static constexpr uint32_t kStage = kBars + 8 * 8 + 16;
+  static constexpr uint32_t kStageWarp = 32 * kStLd * 4;
+  static constexpr uint32_t kTotal = kStage + 4 * kStageWarp;
 };
 
 template <int R>
@@ -435,41 +440,54 @@ __global__ void __launch_bounds__(kThreads)
     __syncwarp();
   } else {
     // ---------------- epilogue: y rows += accumulator rows ----------------
-    const int i = warp * 32 + lane;
-    const bool row_on = i < n_tok;
-    bf16* yrow = row_on ? y + static_cast<size_t>(ld_dep(perm + p0 + i)) * d_out : nullptr;
+    // TMEM lane = token row of the tile.  Each warp stages its 32 rows x 64
+    // columns of the accumulator in shared memory, then walks the rows: one
+    // warp instruction reads (and writes) 128 contiguous bytes of one y row,
+    // instead of 16 bytes of 32 different rows.
+    const int n_rows = min(32, n_tok - warp * 32);  // this warp's token rows
+    bf16* yrow = n_rows > lane ? y + static_cast<size_t>(ld_dep(perm + p0 + warp * 32 + lane)) * d_out
+                               : nullptr;
+    float* stg = reinterpret_cast<float*>(smem + Lay::kStage + warp * Lay::kStageWarp);
     const uint32_t tq = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     for (int j = 0; j < nt; ++j) {
       const int bs = j & 1;
       const uint32_t ph = static_cast<uint32_t>(j >> 1) & 1u;
-      const int n0 = (j0 + j) * kXN;
-      // this row's y for the tile, requested before the accumulator is ready
-      uint4 yv[kXN / 8];
-#pragma unroll
-      for (int c = 0; c < kXN / 8; ++c)
-        if (row_on && n0 + c * 8 < d_out) yv[c] = *reinterpret_cast<const uint4*>(yrow + n0 + c * 8);
       if (!warp_wait(&t_full[bs], ph, abort_f)) break;
       ptx::tc_fence_after();
+#pragma unroll 1
+      for (int h = 0; h < kXN / 64; ++h) {
+        const int nc = (j0 + j) * kXN + h * 64 + 2 * lane;  // this lane's column pair
+        // the accumulator's 64 columns of every row of the warp, to shared memory
 #pragma unroll
-      for (int c0 = 0; c0 < kXN; c0 += 32) {
-        uint32_t v[32];
-        ptx::tmem_ld16(tq + bs * kXN + c0, *reinterpret_cast<uint32_t(*)[16]>(v));
-        ptx::tmem_ld16(tq + bs * kXN + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
-        ptx::tmem_ld_wait();
+        for (int c0 = 0; c0 < 64; c0 += 32) {
+          uint32_t v[32];
+          ptx::tmem_ld16(tq + bs * kXN + h * 64 + c0, *reinterpret_cast<uint32_t(*)[16]>(v));
+          ptx::tmem_ld16(tq + bs * kXN + h * 64 + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
+          ptx::tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int cc = c0 / 8 + c;
-          if (row_on && n0 + cc * 8 < d_out) {
-            const uint32_t w[4] = {yv[cc].x, yv[cc].y, yv[cc].z, yv[cc].w};
-            float f[8];
+          for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<float4*>(stg + lane * Lay::kStLd + c0 + 4 * q) =
+                make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                            __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+        }
+        __syncwarp();
+        // row by row: every load first, then the sums and stores
+        uint32_t yv[32];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              f[2 * e] = bf16_lo(w[e]) + __uint_as_float(v[8 * c + 2 * e]);
-              f[2 * e + 1] = bf16_hi(w[e]) + __uint_as_float(v[8 * c + 2 * e + 1]);
-            }
-            *reinterpret_cast<uint4*>(yrow + n0 + cc * 8) = pack8_bf16(f);
+        for (int r = 0; r < 32; ++r) {
+          bf16* yr = reinterpret_cast<bf16*>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(yrow), r));
+          if (r < n_rows && nc < d_out) yv[r] = *reinterpret_cast<const uint32_t*>(yr + nc);
+        }
+#pragma unroll
+        for (int r = 0; r < 32; ++r) {
+          bf16* yr = reinterpret_cast<bf16*>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(yrow), r));
+          if (r < n_rows && nc < d_out) {
+            const float2 a = *reinterpret_cast<const float2*>(stg + r * Lay::kStLd + 2 * lane);
+            *reinterpret_cast<uint32_t*>(yr + nc) =
+                pack_bf16x2(bf16_lo(yv[r]) + a.x, bf16_hi(yv[r]) + a.y);
           }
         }
+        __syncwarp();
       }
       ptx::tc_fence_before();
       ptx::mbar_arrive(&t_empty[bs]);
