@@ -93,9 +93,12 @@ __host__ __device__ inline SmemLayout smem_layout(int stages, int r, int n_slots
   o += ((n_slots + 31) / 32) * 4;
   o = (o + 7u) & ~7u;
   L.bars = o;
-  o += (2 * stages + 2) * 8;
+  o += (3 * stages + 2) * 8;  // full, empty, accum_full, vt_ready, lora_built
   L.misc = o;
-  o += 32;  // TMEM address, adapter count, abort flag, then one byte per stage: its K blocks
+  // TMEM address, adapter count, abort flag, LoRA stages posted; per ring slot
+  // (16 at most) its K blocks and whether it is a LoRA stage; the ring slot of
+  // each posted LoRA stage (a 16-entry mailbox)
+  o += 112;
   L.total = o;
   return L;
 }
@@ -143,10 +146,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* empty = full + p.stages;
   uint64_t* accum_full = empty + p.stages;
   uint64_t* vt_ready = accum_full + 1;
+  uint64_t* lora_built = vt_ready + 1;  // [stages]: the epilogue warps built the V operand
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc);
   int* n_uniq_s = reinterpret_cast<int*>(smem + L.misc + 4);
   volatile int* abort_f = reinterpret_cast<volatile int*>(smem + L.misc + 8);
+  volatile int* lora_posted = reinterpret_cast<volatile int*>(smem + L.misc + 12);
   uint8_t* stage_kblocks = smem + L.misc + 16;  // K blocks the stage in each ring slot holds
+  uint8_t* stage_lora = smem + L.misc + 32;     // 1: the slot holds a LoRA stage
+  int* lora_mailbox = reinterpret_cast<int*>(smem + L.misc + 48);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // tile order: panels of kPanel column tiles; within a panel the column
@@ -175,7 +182,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ptx::mbar_init(accum_full, 1);
       ptx::mbar_init(vt_ready, kEpiThreads);
+      for (int i = 0; i < p.stages; ++i) ptx::mbar_init(&lora_built[i], kEpiThreads / 32);
       *abort_f = 0;
+      *lora_posted = 0;
       ptx::fence_mbar_init();
     }
     __syncwarp();
@@ -222,6 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint8_t* Wr = X + L.x_bytes;
       if (lane == 0) {
         stage_kblocks[st] = KS;
+        stage_lora[st] = 0;
         ptx::mbar_arrive_expect_tx(&full[st], L.stage_bytes);
 #pragma unroll
         for (int j = 0; j < KS; ++j)
@@ -233,66 +243,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
     };
     auto issue_lora = [&](int g, int st) {
+      // the epilogue warps build this stage's masked V operand (and zero the
+      // W rows B leaves empty); the producer only posts the slot and loads
+      // the B rows, so the base stream is not held up
       uint8_t* X = smem + static_cast<size_t>(st) * L.stage_bytes;
       uint8_t* Wr = X + L.x_bytes;
       const int u_first = (z + g * S) * G;
       const int n_units = min(G, U - u_first);
-      const int ua = u_first >> p.lg_upa, ub = (u_first + n_units - 1) >> p.lg_upa;
-      // masked V operand (K-major, 128-byte swizzle written by hand): zeros,
-      // then the rows of the tokens that use this block's adapters.  v is
-      // fp32; it enters the bf16 MMA as v = hi + lo with hi = bf16(v) and
-      // lo = bf16(v - hi), so the expand keeps ~16 mantissa bits: K rows
-      // [0, 32) carry hi parts, rows [32, 64) lo parts, each against its
-      // own copy of the B rows.
-      for (int e = lane; e < BT * 8; e += 32)
-        reinterpret_cast<uint4*>(X)[e] = make_uint4(0u, 0u, 0u, 0u);
-      const int used = n_units << p.lg_box;   // K rows of W per half that B fills
-      if (used < kBK / 2) {
-        const int per_half = (kBK / 2 - used) * 8;
-        for (int e = lane; e < 2 * per_half * kWBoxes; e += 32) {
-          const int hb = e / (2 * per_half), rem = e % (2 * per_half);
-          const int half = rem / per_half, rr = rem % per_half;
-          *reinterpret_cast<uint4*>(Wr + hb * L.w_box + (half * (kBK / 2) + used + rr / 8) * 128 +
-                                    (rr % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
-        }
-      }
-      __syncwarp();
-      const int c = lane & 7;
-      const int kq = (c & 3) << 3;
-      const int wu = kq >> p.lg_box;
-      const int w = u_first + wu;
-      const int uw = (wu < n_units) ? (w >> p.lg_upa) : -2;
-      const int q0 = ((w & (upa - 1)) << p.lg_box) + (kq & (p.box_rows - 1));
-      // rows 4j + sub of every 32-row word; a quad of rows per iteration,
-      // skipped whole when none of the four uses this block's adapters
-      const int sub = lane >> 3;
-      for (int k = 0; k < BT / 32; ++k) {
-        const int tv = tok[k * 32 + lane];
-        const uint32_t m = __ballot_sync(0xffffffffu, tv >= ua && tv <= ub);
-        if (m == 0u) continue;
-#pragma unroll 1
-        for (int j = 0; j < 8; ++j) {
-          if (((m >> (4 * j)) & 0xFu) == 0u) continue;
-          const int b = 4 * j + sub;
-          const int ti = __shfl_sync(0xffffffffu, tv, b);
-          if (ti == uw) {
-            const int i = k * 32 + b;
-            float f[8], h[8], l[8];
-            load8(vt + i * p.r + q0, f);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              h[q] = __bfloat162float(__float2bfloat16_rn(f[q]));
-              l[q] = f[q] - h[q];
-            }
-            *reinterpret_cast<uint4*>(X + i * 128 + ((c ^ (i & 7)) << 4)) =
-                pack8_bf16(c >= 4 ? l : h);
-          }
-        }
-      }
-      ptx::fence_proxy_async_smem();
-      __syncwarp();
       if (lane == 0) {
         stage_kblocks[st] = 1;
+        stage_lora[st] = 1;
+        lora_mailbox[g & 15] = st;
+        __threadfence_block();
+        *lora_posted = g + 1;
         ptx::mbar_arrive_expect_tx(
             &full[st], static_cast<uint32_t>(2 * n_units * p.box_rows * 128 * kWBoxes));
       }
@@ -346,10 +309,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ---------------- MMA issuer -----------------------------------------
     if (lane == 0) {
+      uint32_t lora_par = 0;  // bit s: phase parity of lora_built[s]
       auto consume = [&](int it) {
         const int st = it % p.stages;
         const uint32_t ph = static_cast<uint32_t>(it / p.stages) & 1u;
         if (!ptx::mbar_wait_bounded(&full[st], ph, abort_f, kWaitLimitNs)) return false;
+        if (stage_lora[st]) {  // written by the producer before its arrive
+          if (!ptx::mbar_wait_bounded(&lora_built[st], (lora_par >> st) & 1u, abort_f,
+                                      kWaitLimitNs))
+            return false;
+          lora_par ^= 1u << st;
+        }
         ptx::tc_fence_after();
         const uint32_t xa = ptx::smem_u32(smem + static_cast<size_t>(st) * L.stage_bytes);
         const uint32_t wa = xa + L.x_bytes;
@@ -466,6 +436,72 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     epi_sync();
     ptx::mbar_arrive(vt_ready);
+    {
+      // this CTA's LoRA stages, in the order the producer posts their ring
+      // slots: one token row per thread writes its 8 chunks of the masked V
+      // operand (K-major, 128-byte swizzle): v = hi + lo with hi = bf16(v),
+      // lo = bf16(v - hi); K rows [0, 32) carry hi parts, [32, 64) lo parts,
+      // each against its own copy of the B rows; rows of tokens on other
+      // adapters are zero
+      int U;
+      const int my_groups = lora_groups(&U);
+      const int i = etid;  // BT == kEpiThreads
+      for (int g2 = 0; g2 < my_groups; ++g2) {
+        if (etid == 0) {
+          const uint64_t tw = ptx::globaltimer_ns();
+          while (*lora_posted <= g2) {
+            if (*abort_f) break;
+            if (ptx::globaltimer_ns() - tw > kWaitLimitNs) {
+              *abort_f = 1;
+              break;
+            }
+          }
+          __threadfence_block();
+        }
+        epi_sync();
+        if (*abort_f) break;
+        const int st = lora_mailbox[g2 & 15];
+        uint8_t* X = smem + static_cast<size_t>(st) * L.stage_bytes;
+        uint8_t* Wr = X + L.x_bytes;
+        const int u_first = (z + g2 * S) * G;
+        const int n_units = min(G, U - u_first);
+        const int tv = tok[i];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const int kq = (c & 3) << 3;
+          const int wu = kq >> p.lg_box;
+          uint4 val = make_uint4(0u, 0u, 0u, 0u);
+          if (wu < n_units && tv >= 0) {
+            const int w = u_first + wu;
+            if ((w >> p.lg_upa) == tv) {
+              const int q0 = ((w & (upa - 1)) << p.lg_box) + (kq & (p.box_rows - 1));
+              float f[8], h[8], l[8];
+              load8(vt + i * p.r + q0, f);
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                h[q] = __bfloat162float(__float2bfloat16_rn(f[q]));
+                l[q] = f[q] - h[q];
+              }
+              val = pack8_bf16(c >= 4 ? l : h);
+            }
+          }
+          *reinterpret_cast<uint4*>(X + i * 128 + ((c ^ (i & 7)) << 4)) = val;
+        }
+        const int used = n_units << p.lg_box;  // K rows of W per half that B fills
+        if (used < kBK / 2) {
+          const int per_half = (kBK / 2 - used) * 8;
+          for (int e = etid; e < 2 * per_half * kWBoxes; e += kEpiThreads) {
+            const int hb = e / (2 * per_half), rem = e % (2 * per_half);
+            const int half = rem / per_half, rr = rem % per_half;
+            *reinterpret_cast<uint4*>(Wr + hb * L.w_box + (half * (kBK / 2) + used + rr / 8) * 128 +
+                                      (rr % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&lora_built[st]);
+      }
+    }
     const bool acc_ok = warp_wait(accum_full, 0, abort_f);
     if (acc_ok) {
       ptx::tc_fence_after();
@@ -496,9 +532,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int rows = min(BT, p.T - t0);
     const int rb0 = static_cast<int>(static_cast<long long>(z) * rows / S);
     const int rb1 = static_cast<int>(static_cast<long long>(z + 1) * rows / S);
+    if (S == 1) {
+      // no split: the staged tile is this CTA's own; consecutive threads take
+      // consecutive float4 of a row (conflict-free shared loads, coalesced
+      // 8-byte stores of y)
+      const float* red = reinterpret_cast<const float*>(smem);
+      constexpr int kQuads = BN / 4;
+      const int n_q = rows * kQuads;
+#pragma unroll 4
+      for (int e = tid; e < n_q; e += kThreads) {
+        const int ii = e / kQuads, n = n0 + (e % kQuads) * 4;
+        if (n < p.d_out) {
+          const float4 f = *reinterpret_cast<const float4*>(red + ii * kRedLd + (n - n0));
+          uint2 pk;
+          pk.x = pack_bf16x2(f.x, f.y);
+          pk.y = pack_bf16x2(f.z, f.w);
+          *reinterpret_cast<uint2*>(p.y + static_cast<size_t>(t0 + ii) * p.d_out + n) = pk;
+        }
+      }
+    }
     constexpr int kChunks = BN / 8;
     const uint32_t red_s = ptx::smem_u32(smem);
-    const int n_items = (rb1 - rb0) * kChunks;
+    const int n_items = S == 1 ? 0 : (rb1 - rb0) * kChunks;
     // two output chunks per pass: every load of both is issued before any sum
     for (int e0 = tid; e0 < n_items; e0 += 2 * kThreads) {
       float4 va[2][8], vb[2][8];
