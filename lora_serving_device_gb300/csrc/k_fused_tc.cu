@@ -125,7 +125,8 @@ __device__ __forceinline__ void named_arrive(int id, int n) {
 template <int BT, int BN, int KS>
 __global__ void __launch_bounds__(kThreads, 1)
     fused_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
-                    const __grid_constant__ CUtensorMap tm_b, const TcParams p) {
+                    const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_y,
+                    const TcParams p) {
   constexpr int kUmmaN = BN;
   constexpr int kTmemCols = kUmmaN < 32 ? 32 : kUmmaN;
   constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(128, kUmmaN, false, true);
@@ -503,7 +504,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     const bool acc_ok = warp_wait(accum_full, 0, abort_f);
-    if (acc_ok) {
+    if (acc_ok && S == 1) {
+      // no split: each thread rounds its token row to bf16 straight from
+      // TMEM into a 128-byte-swizzled tile in the drained ring (64-column
+      // boxes of 128 rows), and four TMA stores write y (clipped at T, d_out)
+      ptx::tc_fence_after();
+      const int q = warp & 3;
+      const uint32_t tq = tmem + (static_cast<uint32_t>(q * 32) << 16);
+      const int i = q * 32 + lane;
+#pragma unroll 1
+      for (int h = 0; h < kUmmaN / 64; ++h) {
+        uint8_t* box = smem + h * (BT * 128);
+#pragma unroll
+        for (int c0 = 0; c0 < 64; c0 += 16) {
+          uint32_t v[16];
+          ptx::tmem_ld16(tq + h * 64 + c0, v);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int ch = (c0 >> 3) + u;  // 16-byte chunk of the 128-byte row
+            uint4 pk;
+            pk.x = pack_bf16x2(__uint_as_float(v[8 * u + 0]), __uint_as_float(v[8 * u + 1]));
+            pk.y = pack_bf16x2(__uint_as_float(v[8 * u + 2]), __uint_as_float(v[8 * u + 3]));
+            pk.z = pack_bf16x2(__uint_as_float(v[8 * u + 4]), __uint_as_float(v[8 * u + 5]));
+            pk.w = pack_bf16x2(__uint_as_float(v[8 * u + 6]), __uint_as_float(v[8 * u + 7]));
+            *reinterpret_cast<uint4*>(box + i * 128 + ((ch ^ (i & 7)) << 4)) = pk;
+          }
+        }
+      }
+      ptx::fence_proxy_async_smem();
+      epi_sync();
+      if (etid == 0) {
+#pragma unroll
+        for (int h = 0; h < kUmmaN / 64; ++h)
+          if (n0 + 64 * h < p.d_out) ptx::tma_store_2d(&tm_y, smem + h * (BT * 128), n0 + 64 * h, t0);
+        ptx::bulk_commit_group();
+        ptx::bulk_wait_group_read_all();  // the tile must outlive the read
+      }
+    } else if (acc_ok) {
       ptx::tc_fence_after();
       const int q = warp & 3;  // TMEM lanes 32q..32q+31 belong to this warp
       const uint32_t tq = tmem + (static_cast<uint32_t>(q * 32) << 16);
@@ -532,25 +570,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int rows = min(BT, p.T - t0);
     const int rb0 = static_cast<int>(static_cast<long long>(z) * rows / S);
     const int rb1 = static_cast<int>(static_cast<long long>(z + 1) * rows / S);
-    if (S == 1) {
-      // no split: the staged tile is this CTA's own; consecutive threads take
-      // consecutive float4 of a row (conflict-free shared loads, coalesced
-      // 8-byte stores of y)
-      const float* red = reinterpret_cast<const float*>(smem);
-      constexpr int kQuads = BN / 4;
-      const int n_q = rows * kQuads;
-#pragma unroll 4
-      for (int e = tid; e < n_q; e += kThreads) {
-        const int ii = e / kQuads, n = n0 + (e % kQuads) * 4;
-        if (n < p.d_out) {
-          const float4 f = *reinterpret_cast<const float4*>(red + ii * kRedLd + (n - n0));
-          uint2 pk;
-          pk.x = pack_bf16x2(f.x, f.y);
-          pk.y = pack_bf16x2(f.z, f.w);
-          *reinterpret_cast<uint2*>(p.y + static_cast<size_t>(t0 + ii) * p.d_out + n) = pk;
-        }
-      }
-    }
     constexpr int kChunks = BN / 8;
     const uint32_t red_s = ptx::smem_u32(smem);
     const int n_items = S == 1 ? 0 : (rb1 - rb0) * kChunks;
@@ -655,11 +674,12 @@ cudaError_t launch_variant(const void* x, const void* W0, const void* B, TcParam
   const SmemLayout L = smem_layout<BT, BN, KS>(stages, prm.r, prm.n_slots);
   const size_t smem = L.total + 1024;
 
-  CUtensorMap tm_x, tm_w, tm_b;
+  CUtensorMap tm_x, tm_w, tm_b, tm_y;
   if (!make_map(&tm_x, x, prm.d_in, prm.T, prm.d_in, kBK, BT) ||
       !make_map(&tm_w, W0, prm.d_out, prm.d_in, prm.d_out, 64, KS * kBK) ||
       !make_map(&tm_b, B, prm.d_out, static_cast<uint64_t>(prm.n_slots) * prm.r, prm.d_out, 64,
-                prm.box_rows))
+                prm.box_rows) ||
+      !make_map(&tm_y, prm.y, prm.d_out, prm.T, prm.d_out, 64, BT))
     return cudaErrorInvalidValue;
 
   auto kern = fused_tc_kernel<BT, BN, KS>;
@@ -680,7 +700,7 @@ cudaError_t launch_variant(const void* x, const void* W0, const void* B, TcParam
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kern, tm_x, tm_w, tm_b, prm);
+  return cudaLaunchKernelEx(&cfg, kern, tm_x, tm_w, tm_b, tm_y, prm);
 }
 
 }  // namespace

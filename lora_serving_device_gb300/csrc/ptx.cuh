@@ -91,6 +91,12 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 // 3-D tiled store from this CTA's shared memory (bulk-group completion);
 // elements outside the tensor are not written.  Shared-memory writes feeding
 // it must be made visible to the async proxy first (fence_proxy_async_smem).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm, const void* src, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(tm),
+      "r"(smem_u32(src)), "r"(c0), "r"(c1)
+      : "memory");
+}
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* tm, const void* src, int c0, int c1,
                                              int c2) {
   asm volatile(
