@@ -340,13 +340,13 @@ lora_status_t lora_linear_fused_noalloc(const void* x, const void* W0, const voi
  *
  * lora_bgmv_adapter_ragged: the adapter term only, as lora_bgmv_adapter
  * (fp32 delta [T, d_out], base-only rows not written; T <= 65535; workspace:
- * the error word).  lora_linear_fused_ragged: the whole layer for decode-sized batches
- * (T <= 256), as lora_linear_fused's bf16 decode path (the split-K base
- * GEMM, then the merge kernel over the ragged pool, with the same
- * programmatic overlap rules); workspace: lora_workspace_bytes
- * (LORA_OP_LINEAR_FUSED, T, d_in, d_out, r_max, n_slots); T > 256 gives
- * LORA_ERR_SHAPE.  Both: bf16 only; LORA_ERR_INVALID_ARG for a null pointer,
- * a pool, x or output not 16-byte aligned, or a negative pool length.
+ * the error word).  lora_linear_fused_ragged: the whole layer, as
+ * lora_linear_fused's bf16 decode path (the split-K base GEMM, then the
+ * merge kernel over the ragged pool, with the same programmatic overlap
+ * rules), over consecutive chunks of at most 256 tokens; workspace:
+ * lora_workspace_bytes(LORA_OP_LINEAR_FUSED, min(T, 256), d_in, d_out, r_max,
+ * n_slots).  Both: bf16 only; LORA_ERR_INVALID_ARG for a null pointer, a
+ * pool, x or output not 16-byte aligned, or a negative pool length.
  */
 lora_status_t lora_bgmv_adapter_ragged(const void* x, const void* A_flat, const void* B_flat,
                                        const int64_t* a_off, const int64_t* b_off,
@@ -393,12 +393,13 @@ lora_status_t lora_linear_fused_ragged(const void* x, const void* W0, const void
  * GEMM's mainloop on chip (into tensor memory, where the MMA reads it).
  * Workspace: the error word.
  *
- * lora_linear_fused_4bit: the whole layer for decode-sized bf16 batches
- * (T <= 256), y = x deq(W0) + s (x A) B: the 4-bit split-K GEMM, then the
- * merge kernel of lora_linear_fused (bf16 adapters).  Same pools, ids,
- * scale, workspace (lora_workspace_bytes(LORA_OP_LINEAR_FUSED, ...)) and
- * programmatic-overlap rules as lora_linear_fused (W0q, absmax and the
- * codebook play the part of W0 there).
+ * lora_linear_fused_4bit: the whole layer, y = x deq(W0) + s (x A) B, for
+ * bf16 batches: the 4-bit split-K GEMM, then the merge kernel of
+ * lora_linear_fused's decode path (bf16 adapters), over consecutive chunks of
+ * at most 256 tokens.  Same pools, ids, scale and programmatic-overlap rules
+ * as lora_linear_fused (W0q, absmax and the codebook play the part of W0
+ * there); workspace: lora_workspace_bytes(LORA_OP_LINEAR_FUSED, min(T, 256),
+ * d_in, d_out, r, n_slots).
  */
 lora_status_t lora_quantize_base_4bit(const void* W0, const void* codebook, void* W0q,
                                       void* absmax, int32_t d_in, int32_t d_out, void* stream);

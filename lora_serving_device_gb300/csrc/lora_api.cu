@@ -477,24 +477,33 @@ lora_status_t lora_linear_fused_ragged(const void* x, const void* W0, const void
                                        int32_t T, int32_t d_in, int32_t d_out, int32_t n_slots,
                                        lora_dtype_t dt, void* ws, size_t ws_bytes, void* stream) {
   lora_status_t s = ragged_args(x, A_flat, B_flat, a_off, b_off, rank, a_elems, b_elems, r_max,
-                                slot_ids, y, T, kDecodeTokens, d_in, d_out, n_slots, dt);
+                                slot_ids, y, T, LORA_MAX_TOKENS, d_in, d_out, n_slots, dt);
   if (s != LORA_OK) return s;
   if (W0 == nullptr || !aligned16(W0) || x == y) return LORA_ERR_INVALID_ARG;
-  const FusedWs w = fused_ws_layout(ws, T, d_in, d_out, r_max, n_slots);
+  const FusedWs w = fused_ws_layout(ws, T < kDecodeTokens ? T : kDecodeTokens, d_in, d_out, r_max,
+                                    n_slots);
   if ((s = check_ws(ws, ws_bytes, w.bytes)) != LORA_OK) return s;
   if (T == 0) return LORA_OK;
   DeviceInfo dev;
   if ((s = check_device(&dev)) != LORA_OK) return s;
   if (!tensor_map_available()) return LORA_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // the decode chain of lora_linear_fused with the ragged merge kernel
-  cudaError_t e =
-      launch_decode_gemm(x, W0, w.partial, T, d_in, d_out, w.split, w.err, true, st, dev);
-  if (e != cudaSuccess) return LORA_ERR_CUDA;
   const RaggedPool rp{a_off, b_off, rank, a_elems, b_elems, r_max};
-  return from_cuda(launch_bgmv_adapter_ragged_merge(x, A_flat, B_flat, rp, slot_ids, scale,
-                                                    w.partial, w.split, y, T, d_in, d_out,
-                                                    n_slots, w.err, true, st));
+  // the decode chain of lora_linear_fused with the ragged merge kernel, over
+  // chunks of at most 256 tokens (the GEMM of each chunk starts while the
+  // previous chunk's merge runs)
+  for (int c0 = 0; c0 < T; c0 += kDecodeTokens) {
+    const int Tc = T - c0 < kDecodeTokens ? T - c0 : kDecodeTokens;
+    const int S = decode_gemm_split(Tc, d_in, d_out);
+    const uint16_t* xc = static_cast<const uint16_t*>(x) + static_cast<size_t>(c0) * d_in;  // bf16
+    uint16_t* yc = static_cast<uint16_t*>(y) + static_cast<size_t>(c0) * d_out;
+    cudaError_t e = launch_decode_gemm(xc, W0, w.partial, Tc, d_in, d_out, S, w.err, true, st, dev);
+    if (e != cudaSuccess) return LORA_ERR_CUDA;
+    e = launch_bgmv_adapter_ragged_merge(xc, A_flat, B_flat, rp, slot_ids + c0, scale, w.partial,
+                                         S, yc, Tc, d_in, d_out, n_slots, w.err, true, st);
+    if (e != cudaSuccess) return LORA_ERR_CUDA;
+  }
+  return LORA_OK;
 }
 
 lora_status_t lora_quantize_base_4bit(const void* W0, const void* codebook, void* W0q,
@@ -540,14 +549,15 @@ lora_status_t lora_linear_fused_4bit(const void* x, const void* W0q, const void*
                                      int32_t d_out, int32_t r, int32_t n_slots, void* ws,
                                      size_t ws_bytes, void* stream) {
   if (T < 0) return LORA_ERR_INVALID_ARG;
-  if (T > kDecodeTokens || !q4_dims_ok(d_in, d_out) || !rank_ok(r) || !slots_ok(n_slots))
+  if (!tokens_ok(T) || !q4_dims_ok(d_in, d_out) || !rank_ok(r) || !slots_ok(n_slots))
     return LORA_ERR_SHAPE;
   if (x == nullptr || W0q == nullptr || absmax == nullptr || codebook == nullptr ||
       A_pool == nullptr || B_pool == nullptr || slot_ids == nullptr || y == nullptr ||
       !aligned16(x) || !aligned16(W0q) || !aligned16(absmax) || !aligned16(A_pool) ||
       !aligned16(B_pool) || !aligned16(y) || x == y)
     return LORA_ERR_INVALID_ARG;
-  const FusedWs w = fused_ws_layout(ws, T, d_in, d_out, r, n_slots);
+  const FusedWs w =
+      fused_ws_layout(ws, T < kDecodeTokens ? T : kDecodeTokens, d_in, d_out, r, n_slots);
   lora_status_t s = check_ws(ws, ws_bytes, w.bytes);
   if (s != LORA_OK) return s;
   if (T == 0) return LORA_OK;
@@ -556,13 +566,21 @@ lora_status_t lora_linear_fused_4bit(const void* x, const void* W0q, const void*
   if (!tensor_map_available()) return LORA_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // the decode chain of lora_linear_fused with the 4-bit base GEMM (its
-  // split over 64-row blocks can always take the bf16 GEMM's split)
-  cudaError_t e = launch_decode_q4(x, W0q, absmax, codebook, w.partial, T, d_in, d_out, w.split,
-                                   w.err, true, st, dev);
-  if (e != cudaSuccess) return LORA_ERR_CUDA;
-  return from_cuda(launch_bgmv_adapter_merge(x, A_pool, B_pool, slot_ids, scale, w.partial,
-                                             w.split, y, T, d_in, d_out, r, n_slots, w.err,
-                                             true, st));
+  // split over 64-row blocks can always take the bf16 GEMM's split), over
+  // chunks of at most 256 tokens
+  for (int c0 = 0; c0 < T; c0 += kDecodeTokens) {
+    const int Tc = T - c0 < kDecodeTokens ? T - c0 : kDecodeTokens;
+    const int S = decode_gemm_split(Tc, d_in, d_out);
+    const uint16_t* xc = static_cast<const uint16_t*>(x) + static_cast<size_t>(c0) * d_in;  // bf16
+    uint16_t* yc = static_cast<uint16_t*>(y) + static_cast<size_t>(c0) * d_out;
+    cudaError_t e = launch_decode_q4(xc, W0q, absmax, codebook, w.partial, Tc, d_in, d_out, S,
+                                     w.err, true, st, dev);
+    if (e != cudaSuccess) return LORA_ERR_CUDA;
+    e = launch_bgmv_adapter_merge(xc, A_pool, B_pool, slot_ids + c0, scale, w.partial, S, yc, Tc,
+                                  d_in, d_out, r, n_slots, w.err, true, st);
+    if (e != cudaSuccess) return LORA_ERR_CUDA;
+  }
+  return LORA_OK;
 }
 
 lora_status_t lora_base_gemm_splitk(const void* x, const void* W0, float* partial, int32_t T,

@@ -485,7 +485,8 @@ def bgmv_adapter_ragged_t(x, pool, slot_ids, scale, ws, delta=None, stream=None)
 
 
 def linear_fused_ragged_t(x, W0, pool, slot_ids, scale, ws, y=None, stream=None):
-    """linear_fused_t over a RaggedPool (decode-sized bf16 batches, T <= 256)."""
+    """linear_fused_t over a RaggedPool (bf16; batches above 256 tokens run in 256-token
+    chunks, so ws is sized for min(T, 256) tokens)."""
     import torch
     T, d_in = x.shape
     d_out = W0.shape[1]
@@ -542,7 +543,8 @@ def base_gemm_4bit_splitk_t(x, base, ws, ksplit=None, partial=None, stream=None)
 
 
 def linear_fused_4bit_t(x, base, A_pool, B_pool, slot_ids, scale, ws, y=None, stream=None):
-    """y = x deq(W0) + s (x A) B over a Base4bit (decode-sized bf16 batches, T <= 256)."""
+    """y = x deq(W0) + s (x A) B over a Base4bit (bf16; batches above 256 tokens run in
+    256-token chunks, so ws is sized for min(T, 256) tokens)."""
     import torch
     T, d_in = x.shape
     n_slots, _, r = A_pool.shape

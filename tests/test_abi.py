@@ -136,7 +136,7 @@ def test_ragged_validation(L):
                                           r_max, FAKE, None, FAKE + 4096, T, 64, 64, 4, 0, WS,
                                           NW, None)
 
-    assert fused(T=257) == 2           # the fused layer takes decode-sized batches only
+    assert fused(T=(1 << 20) + 1) == 2  # more than LORA_MAX_TOKENS
     assert fused(r_max=48) == 2        # r_max is one of 8 .. 128
     assert fused(r_max=256) == 2
     assert fused(d_in=60) == 2
@@ -167,8 +167,8 @@ def test_4bit_validation(L):
     assert g(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 128, 64, 2, WS, NW, None) == 0   # empty batch
     f = L.lora_linear_fused_4bit
     # (x, W0q, absmax, codebook, A, B, ids, scale, y, T, d_in, d_out, r, n_slots, ws, ..)
-    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE + 4096, 257, 128, 64, 16, 4,
-             WS, NW, None) == 2                                          # decode-sized only
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE + 4096, (1 << 20) + 1, 128, 64,
+             16, 4, WS, NW, None) == 2                                   # > LORA_MAX_TOKENS
     assert f(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE + 4096, 8, 128, 64, 12, 4,
              WS, NW, None) == 2                                          # rank
     assert f(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, 8, 128, 64, 16, 4,

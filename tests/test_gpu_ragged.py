@@ -39,6 +39,9 @@ RAGGED_CASES = [
     (48, 2056, 2120, 9, (8, 16, 64, 128)),
     (200, 640, 136, 30, (8, 16, 32, 64, 128)),
     (256, 1024, 4096, 20, (8, 16, 64)),
+    # larger batches run as 256-token chunks
+    (300, 256, 384, 10, (8, 16, 64)),
+    (700, 520, 264, 25, (8, 32, 128)),
 ]
 
 
@@ -74,7 +77,7 @@ def test_fused_ragged_matches_oracle(L, case):
     T, d_in, d_out, n_slots, rank_set = case
     for W0_zero in (False, True):
         c = RaggedCase(L, 900 + T, T, d_in, d_out, n_slots, rank_set, W0_zero=W0_zero)
-        ws = L.workspace(L.OP_LINEAR_FUSED, T, d_in, d_out, c.pool.r_max, n_slots)
+        ws = L.workspace(L.OP_LINEAR_FUSED, min(T, 256), d_in, d_out, c.pool.r_max, n_slots)
         y = L.linear_fused_ragged_t(c.x, c.W0, c.pool, c.ids, c.scale, ws)
         torch.cuda.synchronize()
         ref = c.ref()
