@@ -622,6 +622,536 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0 && *abort_f) flag_error(p.err, LORA_DEVERR_TIMEOUT);
 }
 
+// ------------------------------------------------------------- persistent form
+// The same tile computation for unsplit tiles (S = 1), one CTA per SM looping
+// over tiles: two accumulators in tensor memory, so the epilogue warps drain
+// tile k (bf16 through a 16 KB swizzled box and TMA stores) while the MMA
+// issuer already accumulates tile k + 1, and the ring, the LoRA-stage mailbox
+// and every barrier phase run on across tiles.  The per-tile prologue (TMEM
+// allocation, barrier set-up, the first loads) and epilogue are paid once or
+// hidden behind the next tile's main loop.
+struct PersistLayout {
+  uint32_t x_sub, x_bytes, w_box, stage_bytes;
+  uint32_t tok, uniq, bitmap, ybox, bars, misc, total;
+};
+
+template <int BT, int BN, int KS>
+__host__ __device__ inline PersistLayout persist_layout(int stages, int r, int n_slots) {
+  PersistLayout L;
+  L.x_sub = BT * 128;
+  L.x_bytes = KS * L.x_sub;
+  L.w_box = KS * 8192;
+  L.stage_bytes = L.x_bytes + (BN / 64) * L.w_box;
+  uint32_t o = static_cast<uint32_t>(stages) * L.stage_bytes;
+  L.ybox = o;  // one 64-column bf16 box of the tile, 128-byte swizzle
+  o += BT * 128;
+  (void)r;  // v rows are read from the shrink's partials, not staged
+  L.tok = o;
+  o += BT * 4;
+  L.uniq = o;
+  o += BT * 4;
+  L.bitmap = o;
+  o += ((n_slots + 31) / 32) * 4;
+  o = (o + 7u) & ~7u;
+  L.bars = o;
+  // full, empty, lora_built per stage; one unused; acc_full[2]; acc_empty[2]
+  o += (3 * stages + 5) * 8;
+  L.misc = o;
+  o += 160;  // as the one-tile kernel, then per-tile LoRA group and unit counts (4 tiles), vt_seq
+  L.total = o;
+  return L;
+}
+
+struct PersistParams {
+  TcParams t;
+  int tiles_n, tiles_t, n_tiles;
+};
+
+template <int BT, int BN, int KS>
+__global__ void __launch_bounds__(kThreads, 1)
+    fused_tc_persistent_kernel(const __grid_constant__ CUtensorMap tm_x,
+                               const __grid_constant__ CUtensorMap tm_w,
+                               const __grid_constant__ CUtensorMap tm_b,
+                               const __grid_constant__ CUtensorMap tm_y, const PersistParams pp) {
+  const TcParams& p = pp.t;
+  constexpr int kUmmaN = BN;
+  constexpr int kTmemCols = 2 * BN;  // two accumulators
+  constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(128, kUmmaN, false, true);
+  constexpr int kWBoxes = BN / 64;
+  static_assert(BT == 128 && BN == 256, "persistent tile: 128 tokens x 256 columns");
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const PersistLayout L = persist_layout<BT, BN, KS>(p.stages, p.r, p.n_slots);
+  int* tok = reinterpret_cast<int*>(smem + L.tok);
+  int* uniq = reinterpret_cast<int*>(smem + L.uniq);
+  uint32_t* bitmap = reinterpret_cast<uint32_t*>(smem + L.bitmap);
+  uint8_t* ybox = smem + L.ybox;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
+  uint64_t* empty = full + p.stages;
+  uint64_t* lora_built = empty + p.stages;
+  uint64_t* acc_full = lora_built + p.stages + 1;
+  uint64_t* acc_empty = acc_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc);
+  int* n_uniq_s = reinterpret_cast<int*>(smem + L.misc + 4);
+  volatile int* abort_f = reinterpret_cast<volatile int*>(smem + L.misc + 8);
+  volatile int* lora_posted = reinterpret_cast<volatile int*>(smem + L.misc + 12);
+  uint8_t* stage_kblocks = smem + L.misc + 16;
+  uint8_t* stage_lora = smem + L.misc + 32;
+  int* lora_mailbox = reinterpret_cast<int*>(smem + L.misc + 48);
+  // per tile (k & 3): its LoRA groups and units, written by the epilogue warps
+  // before they publish tile k (vt_seq).  Entry k & 3 is rewritten for tile
+  // k + 4 only after tile k + 2's accumulator is full, so after the producer
+  // (which reads tile k's counts before it loads tile k + 1) and the MMA
+  // issuer have read it; two entries would not be enough when a tile without
+  // adapters lets the epilogue warps run ahead
+  int* tile_groups = reinterpret_cast<int*>(smem + L.misc + 112);
+  int* tile_units = tile_groups + 4;
+  // tiles whose adapter list, v and counts are published (monotonic: unlike
+  // a barrier's phase parity it cannot alias when the epilogue warps run a
+  // tile ahead of the producer or the MMA issuer)
+  volatile int* vt_seq = reinterpret_cast<volatile int*>(tile_groups + 8);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // tile lin -> (n0, t0) in the panel order of the one-tile kernel
+  auto tile_origin = [&](int lin, int* n0, int* t0) {
+    const int g = lin / (kPanel * pp.tiles_t);
+    const int gn = min(kPanel, pp.tiles_n - g * kPanel);
+    const int rem = lin - g * kPanel * pp.tiles_t;
+    *n0 = (g * kPanel + rem % gn) * BN;
+    *t0 = (rem / gn) * BT;
+  };
+  const int first_tile = static_cast<int>(blockIdx.x), tile_step = static_cast<int>(gridDim.x);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      ptx::prefetch_tmap(&tm_x);
+      ptx::prefetch_tmap(&tm_w);
+      ptx::prefetch_tmap(&tm_b);
+      ptx::prefetch_tmap(&tm_y);
+      for (int i = 0; i < p.stages; ++i) {
+        ptx::mbar_init(&full[i], 1);
+        ptx::mbar_init(&empty[i], 1);
+        ptx::mbar_init(&lora_built[i], kEpiThreads / 32);
+      }
+      for (int i = 0; i < 2; ++i) {
+        ptx::mbar_init(&acc_full[i], 1);
+        ptx::mbar_init(&acc_empty[i], kEpiThreads / 32);
+      }
+      *abort_f = 0;
+      *lora_posted = 0;
+      *vt_seq = 0;
+      ptx::fence_mbar_init();
+    }
+    __syncwarp();
+    named_arrive(2, kThreads);
+  } else {
+    named_sync(2, kThreads);
+    if (warp == 1) {
+      ptx::tmem_alloc(tmem_slot, kTmemCols);
+      ptx::tmem_relinquish();
+      ptx::tc_fence_before();
+      named_arrive(3, kThreads - 32);
+    } else {
+      named_sync(3, kThreads - 32);
+    }
+    ptx::tc_fence_after();
+  }
+  const uint32_t tmem = warp == 0 ? 0u : *tmem_slot;
+  const int upa = p.r >> p.lg_box;
+  const int G = (kBK / 2) >> p.lg_box;
+  const int nbase = p.n_kblk;
+  auto lora_groups = [&](int k, int* U_out) {
+    *U_out = tile_units[k & 3];
+    return tile_groups[k & 3];
+  };
+  // one thread waits (bounded) until tile k is published
+  auto seq_wait = [&](int k) {
+    const uint64_t tw = ptx::globaltimer_ns();
+    while (*vt_seq <= k) {
+      if (*abort_f) return false;
+      if (ptx::globaltimer_ns() - tw > kWaitLimitNs) {
+        *abort_f = 1;
+        return false;
+      }
+    }
+    __threadfence_block();
+    return true;
+  };
+
+  if (warp == 0) {
+    // ---------------- producer -------------------------------------------
+    int it = 0, g_run = 0;  // ring position; LoRA stages posted so far
+    bool ok = true;
+    for (int lin = first_tile, k = 0; lin < pp.n_tiles && ok; lin += tile_step, ++k) {
+      int n0, t0;
+      tile_origin(lin, &n0, &t0);
+      bool lora_known = false;
+      int U = 0, my_groups = 0, gi = 0;
+      auto next_slot = [&](int* st) {
+        *st = it % p.stages;
+        const uint32_t ph = static_cast<uint32_t>(it / p.stages) & 1u;
+        return warp_wait(&empty[*st], ph ^ 1u, abort_f);
+      };
+      auto issue_lora = [&](int st) {
+        uint8_t* Wr = smem + static_cast<size_t>(st) * L.stage_bytes + L.x_bytes;
+        const int u_first = gi * G;
+        const int n_units = min(G, U - u_first);
+        // the B rows' coordinates are read from the tile's adapter list before
+        // the stage is posted: once the epilogue warps have built the tile's
+        // last LoRA stage they may rewrite the list for the next tile
+        const bool loads = lane < 2 * n_units * kWBoxes;
+        int a = 0, hb = 0, half = 0, u = 0, qb = 0;
+        if (loads) {
+          u = lane / (2 * kWBoxes);
+          const int rem = lane % (2 * kWBoxes);
+          hb = rem >> 1;
+          half = rem & 1;
+          const int wv = u_first + u;
+          a = uniq[wv >> p.lg_upa];
+          qb = (wv & (upa - 1)) << p.lg_box;
+        }
+        __syncwarp();
+        if (lane == 0) {
+          stage_kblocks[st] = 1;
+          stage_lora[st] = 1;
+          lora_mailbox[g_run & 15] = st;
+          __threadfence_block();
+          *lora_posted = g_run + 1;
+          ptx::mbar_arrive_expect_tx(
+              &full[st], static_cast<uint32_t>(2 * n_units * p.box_rows * 128 * kWBoxes));
+        }
+        __syncwarp();
+        if (loads)
+          ptx::tma_load_2d(Wr + hb * L.w_box + (half * (kBK / 2) + u * p.box_rows) * 128, &tm_b,
+                           &full[st], n0 + 64 * hb, a * p.r + qb);
+        __syncwarp();
+        ++gi;
+        ++g_run;
+      };
+      for (int b = 0; b < nbase && ok; ++b) {
+        int st;
+        if (!(ok = next_slot(&st))) break;
+        uint8_t* X = smem + static_cast<size_t>(st) * L.stage_bytes;
+        if (lane == 0) {
+          stage_kblocks[st] = KS;
+          stage_lora[st] = 0;
+          ptx::mbar_arrive_expect_tx(&full[st], L.stage_bytes);
+#pragma unroll
+          for (int j = 0; j < KS; ++j)
+            ptx::tma_load_2d(X + j * L.x_sub, &tm_x, &full[st], (b * KS + j) * kBK, t0);
+#pragma unroll
+          for (int h = 0; h < kWBoxes; ++h)
+            ptx::tma_load_2d(X + L.x_bytes + h * L.w_box, &tm_w, &full[st], n0 + 64 * h,
+                             b * KS * kBK);
+        }
+        __syncwarp();
+        ++it;
+        if (!lora_known && __shfl_sync(0xffffffffu, *vt_seq > k ? 1 : 0, 0)) {
+          __threadfence_block();
+          lora_known = true;
+          my_groups = lora_groups(k, &U);
+        }
+        if (lora_known && gi < my_groups) {
+          if (!(ok = next_slot(&st))) break;
+          issue_lora(st);
+          ++it;
+        }
+      }
+      if (ok && !lora_known) {
+        int got = 0;
+        if (lane == 0) got = seq_wait(k) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, got, 0) != 0;
+        if (ok) {
+          lora_known = true;
+          my_groups = lora_groups(k, &U);
+        }
+      }
+      while (ok && lora_known && gi < my_groups) {
+        int st;
+        if (!(ok = next_slot(&st))) break;
+        issue_lora(st);
+        ++it;
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer -----------------------------------------
+    if (lane == 0) {
+      uint32_t lora_par = 0;
+      int it = 0;
+      bool ok = true;
+      for (int lin = first_tile, k = 0; lin < pp.n_tiles && ok; lin += tile_step, ++k) {
+        const int b = k & 1;
+        // the epilogue has drained this accumulator (tile k - 2)
+        if (!ptx::mbar_wait_bounded(&acc_empty[b], (static_cast<uint32_t>(k >> 1) & 1u) ^ 1u,
+                                    abort_f, kWaitLimitNs))
+          break;
+        ptx::tc_fence_after();
+        const uint32_t acc = tmem + static_cast<uint32_t>(b * BN);
+        int local = 0;  // stages of this tile consumed so far
+        auto consume = [&]() {
+          const int st = it % p.stages;
+          const uint32_t ph = static_cast<uint32_t>(it / p.stages) & 1u;
+          if (!ptx::mbar_wait_bounded(&full[st], ph, abort_f, kWaitLimitNs)) return false;
+          if (stage_lora[st]) {
+            if (!ptx::mbar_wait_bounded(&lora_built[st], (lora_par >> st) & 1u, abort_f,
+                                        kWaitLimitNs))
+              return false;
+            lora_par ^= 1u << st;
+          }
+          ptx::tc_fence_after();
+          const uint32_t xa = ptx::smem_u32(smem + static_cast<size_t>(st) * L.stage_bytes);
+          const uint32_t wa = xa + L.x_bytes;
+          const int nkb = stage_kblocks[st];
+#pragma unroll
+          for (int j = 0; j < KS; ++j) {
+            if (j >= nkb) break;
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk) {
+              const uint64_t xd = ptx::sdesc_sw128(xa + j * L.x_sub + kk * 32, 16, 1024);
+              const uint64_t wd =
+                  ptx::sdesc_sw128(wa + (j * kBK + kk * 16) * 128, L.w_box, 1024);
+              ptx::mma_bf16(acc, xd, wd, kIdesc, (local > 0 || j > 0 || kk > 0) ? 1u : 0u);
+            }
+          }
+          ptx::mma_commit(&empty[st]);
+          ++it;
+          ++local;
+          return true;
+        };
+        for (int s = 0; s < nbase && ok; ++s) ok = consume();
+        if (ok && seq_wait(k)) {
+          int U;
+          const int my_groups = lora_groups(k, &U);
+          for (int g = 0; g < my_groups && ok; ++g) ok = consume();
+        } else {
+          ok = false;
+        }
+        ptx::mma_commit(&acc_full[b]);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue warps -------------------------------------
+    const int etid = tid - 64;
+    const int n_words = (p.n_slots + 31) >> 5;
+    const int q = warp & 3;
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    const int i = q * 32 + lane;  // this thread's token row of the tile (== etid here)
+    int g_run = 0;                // LoRA stages built so far
+    // drain accumulator b of tile kk into y.  Every epilogue thread runs the
+    // same sequence of named barriers whatever happens: after an abort the
+    // work is skipped, never the barriers (waits then return at once)
+    auto drain = [&](int kk, int n0, int t0) {
+      const int b = kk & 1;
+      warp_wait(&acc_full[b], static_cast<uint32_t>(kk >> 1) & 1u, abort_f);
+      ptx::tc_fence_after();
+#pragma unroll 1
+      for (int h = 0; h < kUmmaN / 64; ++h) {
+        // the staging box is free once the previous TMA store has read it
+        if (etid == 0) ptx::bulk_wait_group_read_all();
+        epi_sync();
+        // warp-uniform: the TMEM loads are warp-collective
+        const bool live = __shfl_sync(0xffffffffu, *abort_f == 0 ? 1 : 0, 0) != 0;
+        if (live) {
+#pragma unroll
+          for (int c0 = 0; c0 < 64; c0 += 16) {
+            uint32_t v[16];
+            ptx::tmem_ld16(tmem + lane_base + b * BN + h * 64 + c0, v);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int ch = (c0 >> 3) + u;
+              uint4 pk;
+              pk.x = pack_bf16x2(__uint_as_float(v[8 * u + 0]), __uint_as_float(v[8 * u + 1]));
+              pk.y = pack_bf16x2(__uint_as_float(v[8 * u + 2]), __uint_as_float(v[8 * u + 3]));
+              pk.z = pack_bf16x2(__uint_as_float(v[8 * u + 4]), __uint_as_float(v[8 * u + 5]));
+              pk.w = pack_bf16x2(__uint_as_float(v[8 * u + 6]), __uint_as_float(v[8 * u + 7]));
+              *reinterpret_cast<uint4*>(ybox + i * 128 + ((ch ^ (i & 7)) << 4)) = pk;
+            }
+          }
+        }
+        ptx::fence_proxy_async_smem();
+        epi_sync();
+        if (etid == 0 && live) {
+          if (n0 + 64 * h < p.d_out) ptx::tma_store_2d(&tm_y, ybox, n0 + 64 * h, t0);
+          ptx::bulk_commit_group();
+        }
+      }
+      // every TMEM load of this accumulator has completed (tmem_ld_wait)
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&acc_empty[b]);
+    };
+    int k = 0;
+    int prev_n0 = 0, prev_t0 = 0;
+    for (int lin = first_tile; lin < pp.n_tiles; lin += tile_step, ++k) {
+      int n0, t0;
+      tile_origin(lin, &n0, &t0);
+      // ---- this tile's adapters and v (the main loop is already streaming)
+      bool bad = false;
+      {
+        const int t = t0 + i;
+        int sl = -1;
+        if (t < p.T) {
+          const int id = p.ids[t];
+          if (slot_valid(id, p.n_slots)) sl = id;
+          else if (id != -1) bad = true;
+        }
+        tok[i] = sl;
+      }
+      for (int wd = etid; wd < n_words; wd += kEpiThreads) bitmap[wd] = 0u;
+      if (bad && n0 == 0) flag_error(p.err, LORA_DEVERR_BAD_SLOT);
+      epi_sync();
+      if (tok[i] >= 0) atomicOr(&bitmap[tok[i] >> 5], 1u << (tok[i] & 31));
+      epi_sync();
+      if (warp == 2) {
+        const int per = (n_words + 31) / 32;
+        const int w0 = min(n_words, lane * per), w1 = min(n_words, w0 + per);
+        int cnt = 0;
+        for (int wd = w0; wd < w1; ++wd) cnt += __popc(bitmap[wd]);
+        int incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int vv = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += vv;
+        }
+        int off = incl - cnt;
+        for (int wd = w0; wd < w1; ++wd) {
+          uint32_t m = bitmap[wd];
+          while (m) {
+            const int bb = __ffs(m) - 1;
+            m &= m - 1;
+            uniq[off++] = wd * 32 + bb;
+          }
+        }
+        if (lane == 31) *n_uniq_s = incl;
+      }
+      epi_sync();
+      const int n_uniq = *n_uniq_s;
+      {
+        const int sl = tok[i];
+        int u = -1;
+        if (sl >= 0) {
+          int lo = 0, hi = n_uniq - 1;
+          while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (uniq[mid] < sl) lo = mid + 1;
+            else hi = mid;
+          }
+          u = lo;
+        }
+        tok[i] = u;
+      }
+      if (k == 0) pdl_wait();  // v is written by the shrink kernel launched just before
+      const int U = n_uniq * upa;
+      const int my_groups = (U + G - 1) / G;
+      if (etid == 0) {
+        tile_units[k & 3] = U;
+        tile_groups[k & 3] = my_groups;
+      }
+      epi_sync();
+      if (etid == 0) {
+        __threadfence_block();
+        *vt_seq = k + 1;  // tile k published
+      }
+      // ---- the previous tile's accumulator, while this tile streams
+      if (k > 0) drain(k - 1, prev_n0, prev_t0);
+      // ---- this tile's LoRA stages (as in the one-tile kernel)
+      for (int g2 = 0; g2 < my_groups; ++g2, ++g_run) {
+        if (etid == 0) {
+          const uint64_t tw = ptx::globaltimer_ns();
+          while (*lora_posted <= g_run) {
+            if (*abort_f) break;
+            if (ptx::globaltimer_ns() - tw > kWaitLimitNs) {
+              *abort_f = 1;
+              break;
+            }
+          }
+          __threadfence_block();
+        }
+        epi_sync();
+        if (__shfl_sync(0xffffffffu, *abort_f == 0 ? 1 : 0, 0)) {
+          const int st = lora_mailbox[g_run & 15];
+          uint8_t* X = smem + static_cast<size_t>(st) * L.stage_bytes;
+          uint8_t* Wr = X + L.x_bytes;
+          const int u_first = g2 * G;
+          const int n_units = min(G, U - u_first);
+          const int tv = tok[i];
+          // v[t, q0 .. q0+8) for each 8-column chunk of the stage's first half,
+          // summed over the shrink's d_in splits (this thread's row only: the
+          // values come from L2, with every load issued before any is used)
+          const size_t row = static_cast<size_t>(t0 + i) * p.r;
+          const size_t split = static_cast<size_t>(p.T) * p.r;
+          int q0[4];
+          float f[4][8];
+#pragma unroll
+          for (int cq = 0; cq < 4; ++cq) {
+            const int kq = cq << 3;
+            const int wu = kq >> p.lg_box;
+            const int w = u_first + wu;
+            q0[cq] = (wu < n_units && tv >= 0 && (w >> p.lg_upa) == tv)
+                         ? ((w & (upa - 1)) << p.lg_box) + (kq & (p.box_rows - 1))
+                         : -1;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) f[cq][c] = 0.f;
+          }
+          for (int s0 = 0; s0 < p.v_ksplit; ++s0) {
+            float g[4][8];
+#pragma unroll
+            for (int cq = 0; cq < 4; ++cq)
+              if (q0[cq] >= 0) load8_dep(p.vpart + s0 * split + row + q0[cq], g[cq]);
+#pragma unroll
+            for (int cq = 0; cq < 4; ++cq)
+              if (q0[cq] >= 0)
+#pragma unroll
+                for (int c = 0; c < 8; ++c) f[cq][c] += g[cq][c];
+          }
+#pragma unroll
+          for (int cq = 0; cq < 4; ++cq) {
+            float hh[8], ll[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              hh[c] = __bfloat162float(__float2bfloat16_rn(f[cq][c]));
+              ll[c] = f[cq][c] - hh[c];
+            }
+            // a chunk with no matching unit is all zeros (f stayed 0)
+            *reinterpret_cast<uint4*>(X + i * 128 + ((cq ^ (i & 7)) << 4)) = pack8_bf16(hh);
+            *reinterpret_cast<uint4*>(X + i * 128 + (((cq + 4) ^ (i & 7)) << 4)) = pack8_bf16(ll);
+          }
+          const int used = n_units << p.lg_box;
+          if (used < kBK / 2) {
+            const int per_half = (kBK / 2 - used) * 8;
+            for (int e = etid; e < 2 * per_half * kWBoxes; e += kEpiThreads) {
+              const int hb = e / (2 * per_half), rem = e % (2 * per_half);
+              const int half = rem / per_half, rr = rem % per_half;
+              *reinterpret_cast<uint4*>(Wr + hb * L.w_box + (half * (kBK / 2) + used + rr / 8) * 128 +
+                                        (rr % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
+            }
+          }
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&lora_built[st]);
+        }
+      }
+      prev_n0 = n0;
+      prev_t0 = t0;
+    }
+    // the last tile
+    if (k > 0) drain(k - 1, prev_n0, prev_t0);
+    if (etid == 0) ptx::bulk_wait_group_read_all();
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+  if (tid == 0 && *abort_f) flag_error(p.err, LORA_DEVERR_TIMEOUT);
+}
+
 // ------------------------------------------------------------- host side
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -701,6 +1231,51 @@ cudaError_t launch_variant(const void* x, const void* W0, const void* B, TcParam
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kern, tm_x, tm_w, tm_b, tm_y, prm);
+}
+
+template <int BT, int BN, int KS>
+cudaError_t launch_persistent(const void* x, const void* W0, const void* B, TcParams prm,
+                              int tiles_n, int tiles_t, cudaStream_t st, const DeviceInfo& dev) {
+  int stages = 0;
+  for (int s = 8; s >= (KS == 2 ? 2 : 3); --s) {
+    const PersistLayout L = persist_layout<BT, BN, KS>(s, prm.r, prm.n_slots);
+    if (L.total + 1024 <= dev.max_smem_optin) {
+      stages = s;
+      break;
+    }
+  }
+  if (stages == 0) return cudaErrorInvalidConfiguration;
+  prm.stages = stages;
+  const PersistLayout L = persist_layout<BT, BN, KS>(stages, prm.r, prm.n_slots);
+  const size_t smem = L.total + 1024;
+
+  CUtensorMap tm_x, tm_w, tm_b, tm_y;
+  if (!make_map(&tm_x, x, prm.d_in, prm.T, prm.d_in, kBK, BT) ||
+      !make_map(&tm_w, W0, prm.d_out, prm.d_in, prm.d_out, 64, KS * kBK) ||
+      !make_map(&tm_b, B, prm.d_out, static_cast<uint64_t>(prm.n_slots) * prm.r, prm.d_out, 64,
+                prm.box_rows) ||
+      !make_map(&tm_y, prm.y, prm.d_out, prm.T, prm.d_out, 64, BT))
+    return cudaErrorInvalidValue;
+  auto kern = fused_tc_persistent_kernel<BT, BN, KS>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  PersistParams pp;
+  pp.t = prm;
+  pp.tiles_n = tiles_n;
+  pp.tiles_t = tiles_t;
+  pp.n_tiles = tiles_n * tiles_t;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(pp.n_tiles < dev.num_sms ? pp.n_tiles : dev.num_sms);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tm_x, tm_w, tm_b, tm_y, pp);
 }
 
 }  // namespace
@@ -812,6 +1387,15 @@ cudaError_t launch_fused_tc(const void* x, const void* W0, const void* B, const 
   const int tiles_n = (d_out + 255) / 256;
   const int tiles_t = (T + 127) / 128;
   const int S = pick_split(tiles_n * tiles_t);
+  if (S == 1) {
+    // more tiles than SMs: the persistent form, one CTA per SM walking
+    // tiles with two accumulators in tensor memory (two 128-deep stages
+    // beside the y box; v rows come from L2 when a LoRA stage is built)
+    TcParams pp = prm;
+    pp.n_kblk = (d_in + 2 * kBK - 1) / (2 * kBK);
+    const cudaError_t e = launch_persistent<128, 256, 2>(x, W0, B, pp, tiles_n, tiles_t, st, dev);
+    if (e != cudaErrorInvalidConfiguration) return e;
+  }
   if (KS == 2) return launch_variant<128, 256, 2>(x, W0, B, prm, tiles_n, tiles_t, S, st, dev);
   return launch_variant<128, 256, 1>(x, W0, B, prm, tiles_n, tiles_t, S, st, dev);
 }

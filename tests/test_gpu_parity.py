@@ -302,6 +302,34 @@ def test_prefill_sgmv_full(L):
     check_close_bf16_out(host(yb), delta, "prefill SGMV delta")
 
 
+# more 128 x 256 output tiles than SMs: each CTA walks several tiles with two
+# accumulators in tensor memory (632 tiles: up to five per CTA)
+PERSIST_CASES = [(1000, 200, 20008, 16, True), (700, 1032, 12296, 64, False)]
+
+
+@pytest.mark.parametrize("T,d_in,d_out,r,runs", PERSIST_CASES, ids=[str(c) for c in PERSIST_CASES])
+def test_prefill_many_tiles(L, T, d_in, d_out, r, runs):
+    """Runs of adapters (or every token its own draw), whole tiles with no
+    adapter and ragged token, column and d_in tails, with and without the
+    base term."""
+    torch = torch_mod()
+    w = W.random_case(1200 + T, T, d_in, d_out, r, 24, runs=runs)
+    w.slot_ids[128:400] = -1
+    w.slot_ids[-40:] = -1
+    for W0_zero in (False, True):
+        d = DeviceCase(w, W0_zero=W0_zero)
+        y, ws = d.fused()
+        torch.cuda.synchronize()
+        W0 = np.zeros_like(w.W0) if W0_zero else w.W0
+        ref = O.lora_linear(w.x, W0, w.A_pool, w.B_pool, w.scale, w.slot_ids)
+        if W0_zero:
+            check_close_bf16_out(host(y), ref, "many-tile delta")
+        else:
+            check_close(host(y), ref, "many-tile y")
+        assert L.get_error_t(ws) == 0
+        del d, y, ws
+
+
 @pytest.mark.parametrize("T,k", W.SWEEP_POINTS)
 def test_diversity_sweep_point(L, T, k):
     torch = torch_mod()
