@@ -625,9 +625,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ------------------------------------------------------------- persistent form
 // The same tile computation for unsplit tiles (S = 1), one CTA per SM looping
 // over tiles: two accumulators in tensor memory, so the epilogue warps drain
-// tile k (bf16 through a 16 KB swizzled box and TMA stores) while the MMA
-// issuer already accumulates tile k + 1, and the ring, the LoRA-stage mailbox
-// and every barrier phase run on across tiles.  The per-tile prologue (TMEM
+// tile k - 1 (bf16 through a 16 KB swizzled box and TMA stores) while the MMA
+// issuer already accumulates tile k, and the ring, the LoRA-stage mailbox and
+// every barrier phase run on across tiles.  The per-tile prologue (TMEM
 // allocation, barrier set-up, the first loads) and epilogue are paid once or
 // hidden behind the next tile's main loop.
 struct PersistLayout {
@@ -636,7 +636,7 @@ struct PersistLayout {
 };
 
 template <int BT, int BN, int KS>
-__host__ __device__ inline PersistLayout persist_layout(int stages, int r, int n_slots) {
+__host__ __device__ inline PersistLayout persist_layout(int stages, int n_slots) {
   PersistLayout L;
   L.x_sub = BT * 128;
   L.x_bytes = KS * L.x_sub;
@@ -645,7 +645,7 @@ __host__ __device__ inline PersistLayout persist_layout(int stages, int r, int n
   uint32_t o = static_cast<uint32_t>(stages) * L.stage_bytes;
   L.ybox = o;  // one 64-column bf16 box of the tile, 128-byte swizzle
   o += BT * 128;
-  (void)r;  // v rows are read from the shrink's partials, not staged
+  // v rows are read from the shrink's partials when a LoRA stage is built
   L.tok = o;
   o += BT * 4;
   L.uniq = o;
@@ -664,7 +664,7 @@ __host__ __device__ inline PersistLayout persist_layout(int stages, int r, int n
 
 struct PersistParams {
   TcParams t;
-  int tiles_n, tiles_t, n_tiles;
+  int tiles_n, tiles_tp, n_tiles;  // tiles_tp: rows of tiles along the tokens
 };
 
 template <int BT, int BN, int KS>
@@ -683,7 +683,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  const PersistLayout L = persist_layout<BT, BN, KS>(p.stages, p.r, p.n_slots);
+  const PersistLayout L = persist_layout<BT, BN, KS>(p.stages, p.n_slots);
   int* tok = reinterpret_cast<int*>(smem + L.tok);
   int* uniq = reinterpret_cast<int*>(smem + L.uniq);
   uint32_t* bitmap = reinterpret_cast<uint32_t*>(smem + L.bitmap);
@@ -708,17 +708,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   // adapters lets the epilogue warps run ahead
   int* tile_groups = reinterpret_cast<int*>(smem + L.misc + 112);
   int* tile_units = tile_groups + 4;
-  // tiles whose adapter list, v and counts are published (monotonic: unlike
-  // a barrier's phase parity it cannot alias when the epilogue warps run a
-  // tile ahead of the producer or the MMA issuer)
+  // tiles whose adapter list and counts are published (monotonic: unlike a
+  // barrier's phase parity it cannot alias when the epilogue warps run a tile
+  // ahead of the producer or the MMA issuer)
   volatile int* vt_seq = reinterpret_cast<volatile int*>(tile_groups + 8);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // tile lin -> (n0, t0) in the panel order of the one-tile kernel
   auto tile_origin = [&](int lin, int* n0, int* t0) {
-    const int g = lin / (kPanel * pp.tiles_t);
+    const int g = lin / (kPanel * pp.tiles_tp);
     const int gn = min(kPanel, pp.tiles_n - g * kPanel);
-    const int rem = lin - g * kPanel * pp.tiles_t;
+    const int rem = lin - g * kPanel * pp.tiles_tp;
     *n0 = (g * kPanel + rem % gn) * BN;
     *t0 = (rem / gn) * BT;
   };
@@ -762,10 +762,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int upa = p.r >> p.lg_box;
   const int G = (kBK / 2) >> p.lg_box;
   const int nbase = p.n_kblk;
-  auto lora_groups = [&](int k, int* U_out) {
-    *U_out = tile_units[k & 3];
-    return tile_groups[k & 3];
-  };
   // one thread waits (bounded) until tile k is published
   auto seq_wait = [&](int k) {
     const uint64_t tw = ptx::globaltimer_ns();
@@ -784,10 +780,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- producer -------------------------------------------
     int it = 0, g_run = 0;  // ring position; LoRA stages posted so far
     bool ok = true;
+    // a tile's LoRA stages follow this base stage (the same place in every
+    // tile)
+    const int ins = nbase > 1 ? 1 : 0;
     for (int lin = first_tile, k = 0; lin < pp.n_tiles && ok; lin += tile_step, ++k) {
       int n0, t0;
       tile_origin(lin, &n0, &t0);
-      bool lora_known = false;
       int U = 0, my_groups = 0, gi = 0;
       auto next_slot = [&](int* st) {
         *st = it % p.stages;
@@ -848,31 +846,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         ++it;
-        if (!lora_known && __shfl_sync(0xffffffffu, *vt_seq > k ? 1 : 0, 0)) {
-          __threadfence_block();
-          lora_known = true;
-          my_groups = lora_groups(k, &U);
+        if (b == ins) {
+          int got = 0, cu = 0, cg = 0;
+          if (lane == 0 && seq_wait(k)) {
+            got = 1;
+            cu = tile_units[k & 3];
+            cg = tile_groups[k & 3];
+          }
+          ok = __shfl_sync(0xffffffffu, got, 0) != 0;
+          U = __shfl_sync(0xffffffffu, cu, 0);
+          my_groups = __shfl_sync(0xffffffffu, cg, 0);
+          while (ok && gi < my_groups) {
+            if (!(ok = next_slot(&st))) break;
+            issue_lora(st);
+            ++it;
+          }
         }
-        if (lora_known && gi < my_groups) {
-          if (!(ok = next_slot(&st))) break;
-          issue_lora(st);
-          ++it;
-        }
-      }
-      if (ok && !lora_known) {
-        int got = 0;
-        if (lane == 0) got = seq_wait(k) ? 1 : 0;
-        ok = __shfl_sync(0xffffffffu, got, 0) != 0;
-        if (ok) {
-          lora_known = true;
-          my_groups = lora_groups(k, &U);
-        }
-      }
-      while (ok && lora_known && gi < my_groups) {
-        int st;
-        if (!(ok = next_slot(&st))) break;
-        issue_lora(st);
-        ++it;
       }
     }
   } else if (warp == 1) {
@@ -920,10 +909,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++local;
           return true;
         };
+        // the tile's stages: nbase base stages with its LoRA stages among them
         for (int s = 0; s < nbase && ok; ++s) ok = consume();
         if (ok && seq_wait(k)) {
-          int U;
-          const int my_groups = lora_groups(k, &U);
+          const int my_groups = tile_groups[k & 3];
           for (int g = 0; g < my_groups && ok; ++g) ok = consume();
         } else {
           ok = false;
@@ -989,7 +978,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int lin = first_tile; lin < pp.n_tiles; lin += tile_step, ++k) {
       int n0, t0;
       tile_origin(lin, &n0, &t0);
-      // ---- this tile's adapters and v (the main loop is already streaming)
+      // ---- this tile's adapters (while the previous tile still streams)
       bool bad = false;
       {
         const int t = t0 + i;
@@ -1056,9 +1045,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         __threadfence_block();
         *vt_seq = k + 1;  // tile k published
       }
-      // ---- the previous tile's accumulator, while this tile streams
-      if (k > 0) drain(k - 1, prev_n0, prev_t0);
-      // ---- this tile's LoRA stages (as in the one-tile kernel)
+      // ---- this tile's LoRA stages, as the producer posts them early in the
+      // tile (the other accumulator, tile k - 1, waits meanwhile)
       for (int g2 = 0; g2 < my_groups; ++g2, ++g_run) {
         if (etid == 0) {
           const uint64_t tw = ptx::globaltimer_ns();
@@ -1122,6 +1110,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const int used = n_units << p.lg_box;
           if (used < kBK / 2) {
+            // B rows past the stage's units: no TMA writes them
             const int per_half = (kBK / 2 - used) * 8;
             for (int e = etid; e < 2 * per_half * kWBoxes; e += kEpiThreads) {
               const int hb = e / (2 * per_half), rem = e % (2 * per_half);
@@ -1135,6 +1124,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) ptx::mbar_arrive(&lora_built[st]);
         }
       }
+      // ---- the previous tile's accumulator, while this tile streams
+      if (k > 0) drain(k - 1, prev_n0, prev_t0);
       prev_n0 = n0;
       prev_t0 = t0;
     }
@@ -1148,6 +1139,497 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+  if (tid == 0 && *abort_f) flag_error(p.err, LORA_DEVERR_TIMEOUT);
+}
+
+// ------------------------------------------------------------- wide form
+// Persistent walk over tiles of 256 tokens x 256 columns.  Each 64-deep
+// stage brings x for the tile's two 128-token halves (32 KB) and one W0 slab
+// (32 KB), and the two M = 128 MMAs of a 16-deep step share the W0 operand.
+// An SM then takes in 64 KB of operands per 8.4 MFLOP instead of the 96 KB of
+// a 128 x 256 tile, and that intake, not the tensor pipe, is what bounds the
+// narrower tile's main loop (at the same L2 hit rate, multicasting W0 across
+// a CTA pair cut L2 reads without speeding it up).  The two accumulators fill
+// all 512 TMEM columns, so a tile is drained before the next one starts; eight
+// epilogue warps (two per TMEM lane quarter, one per 128-column half), each
+// with its own 4 KB store box, keep that drain short.
+constexpr int kWideThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue
+constexpr int kWideEpi = 256;
+
+__device__ __forceinline__ void wide_epi_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kWideEpi) : "memory");
+}
+
+struct WideLayout {
+  uint32_t x_sub, w_off, w_box, stage_bytes;
+  uint32_t ybox, tok, uniq, bitmap, bars, misc, total;
+};
+
+__host__ __device__ inline WideLayout wide_layout(int stages, int n_slots) {
+  WideLayout L;
+  L.x_sub = 128 * 128;  // 128 tokens x 64 K of bf16, 128-byte swizzle
+  L.w_off = 2 * L.x_sub;
+  L.w_box = kBK * 128;  // 64 K rows x 64 columns
+  L.stage_bytes = L.w_off + 4 * L.w_box;
+  uint32_t o = static_cast<uint32_t>(stages) * L.stage_bytes;
+  L.ybox = o;  // per epilogue warp: 32 rows x 64 columns of bf16
+  o += 8 * 4096;
+  L.tok = o;  // int16 per token of the tile
+  o += 256 * 2;
+  L.uniq = o;  // int16 per distinct adapter of the tile
+  o += 256 * 2;
+  L.bitmap = o;
+  o += ((n_slots + 31) / 32) * 4;
+  o = (o + 7u) & ~7u;
+  L.bars = o;  // full, empty, lora_built per stage; acc_full; acc_empty
+  o += (3 * stages + 2) * 8;
+  L.misc = o;
+  o += 160;
+  L.total = o;
+  return L;
+}
+
+__global__ void __launch_bounds__(kWideThreads, 1)
+    fused_tc_wide_kernel(const __grid_constant__ CUtensorMap tm_x,
+                         const __grid_constant__ CUtensorMap tm_w,
+                         const __grid_constant__ CUtensorMap tm_b,
+                         const __grid_constant__ CUtensorMap tm_y, const PersistParams pp) {
+  const TcParams& p = pp.t;
+  constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(128, 256, false, true);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const WideLayout L = wide_layout(p.stages, p.n_slots);
+  int16_t* tok = reinterpret_cast<int16_t*>(smem + L.tok);
+  int16_t* uniq = reinterpret_cast<int16_t*>(smem + L.uniq);
+  uint32_t* bitmap = reinterpret_cast<uint32_t*>(smem + L.bitmap);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
+  uint64_t* empty = full + p.stages;
+  uint64_t* lora_built = empty + p.stages;
+  uint64_t* acc_full = lora_built + p.stages;
+  uint64_t* acc_empty = acc_full + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc);
+  int* n_uniq_s = reinterpret_cast<int*>(smem + L.misc + 4);
+  volatile int* abort_f = reinterpret_cast<volatile int*>(smem + L.misc + 8);
+  volatile int* lora_posted = reinterpret_cast<volatile int*>(smem + L.misc + 12);
+  uint8_t* stage_lora = smem + L.misc + 32;
+  int* lora_mailbox = reinterpret_cast<int*>(smem + L.misc + 48);
+  // per tile (k & 3): LoRA groups and units; entry k & 3 is rewritten for
+  // tile k + 4 only after tile k + 3's LoRA stages were posted and tile
+  // k + 2's accumulators drained, so after the producer and the MMA issuer
+  // have read it
+  int* tile_groups = reinterpret_cast<int*>(smem + L.misc + 112);
+  int* tile_units = tile_groups + 4;
+  volatile int* vt_seq = reinterpret_cast<volatile int*>(tile_groups + 8);  // tiles published
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  auto tile_origin = [&](int lin, int* n0, int* t0) {
+    const int g = lin / (kPanel * pp.tiles_tp);
+    const int gn = min(kPanel, pp.tiles_n - g * kPanel);
+    const int rem = lin - g * kPanel * pp.tiles_tp;
+    *n0 = (g * kPanel + rem % gn) * 256;
+    *t0 = (rem / gn) * 256;
+  };
+  const int first_tile = static_cast<int>(blockIdx.x), tile_step = static_cast<int>(gridDim.x);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      ptx::prefetch_tmap(&tm_x);
+      ptx::prefetch_tmap(&tm_w);
+      ptx::prefetch_tmap(&tm_b);
+      ptx::prefetch_tmap(&tm_y);
+      for (int i = 0; i < p.stages; ++i) {
+        ptx::mbar_init(&full[i], 1);
+        ptx::mbar_init(&empty[i], 1);
+        ptx::mbar_init(&lora_built[i], kWideEpi / 32);
+      }
+      ptx::mbar_init(acc_full, 1);
+      ptx::mbar_init(acc_empty, kWideEpi / 32);
+      *abort_f = 0;
+      *lora_posted = 0;
+      *vt_seq = 0;
+      ptx::fence_mbar_init();
+    }
+    __syncwarp();
+    named_arrive(2, kWideThreads);
+  } else {
+    named_sync(2, kWideThreads);
+    if (warp == 1) {
+      ptx::tmem_alloc(tmem_slot, 512);
+      ptx::tmem_relinquish();
+      ptx::tc_fence_before();
+      named_arrive(3, kWideThreads - 32);
+    } else {
+      named_sync(3, kWideThreads - 32);
+    }
+    ptx::tc_fence_after();
+  }
+  const uint32_t tmem = warp == 0 ? 0u : *tmem_slot;
+  const int upa = p.r >> p.lg_box;
+  const int G = (kBK / 2) >> p.lg_box;
+  const int nbase = p.n_kblk;
+  auto seq_wait = [&](int k) {
+    const uint64_t tw = ptx::globaltimer_ns();
+    while (*vt_seq <= k) {
+      if (*abort_f) return false;
+      if (ptx::globaltimer_ns() - tw > kWaitLimitNs) {
+        *abort_f = 1;
+        return false;
+      }
+    }
+    __threadfence_block();
+    return true;
+  };
+
+  if (warp == 0) {
+    // ---------------- producer -------------------------------------------
+    int it = 0, g_run = 0;
+    bool ok = true;
+    // a tile's LoRA stages follow this base stage: late enough that the
+    // epilogue warps have drained the previous tile when they are posted
+    const int ins = nbase > 3 ? 3 : nbase - 1;
+    for (int lin = first_tile, k = 0; lin < pp.n_tiles && ok; lin += tile_step, ++k) {
+      int n0, t0;
+      tile_origin(lin, &n0, &t0);
+      int U = 0, my_groups = 0, gi = 0;
+      auto next_slot = [&](int* st) {
+        *st = it % p.stages;
+        const uint32_t ph = static_cast<uint32_t>(it / p.stages) & 1u;
+        return warp_wait(&empty[*st], ph ^ 1u, abort_f);
+      };
+      auto issue_lora = [&](int st) {
+        uint8_t* Wr = smem + static_cast<size_t>(st) * L.stage_bytes + L.w_off;
+        const int u_first = gi * G;
+        const int n_units = min(G, U - u_first);
+        const bool loads = lane < 2 * n_units * 4;
+        int a = 0, hb = 0, half = 0, u = 0, qb = 0;
+        if (loads) {
+          u = lane >> 3;
+          hb = (lane & 7) >> 1;
+          half = lane & 1;
+          const int wv = u_first + u;
+          a = uniq[wv >> p.lg_upa];
+          qb = (wv & (upa - 1)) << p.lg_box;
+        }
+        __syncwarp();
+        if (lane == 0) {
+          stage_lora[st] = 1;
+          lora_mailbox[g_run & 15] = st;
+          __threadfence_block();
+          *lora_posted = g_run + 1;
+          ptx::mbar_arrive_expect_tx(&full[st],
+                                     static_cast<uint32_t>(2 * n_units * p.box_rows * 128 * 4));
+        }
+        __syncwarp();
+        if (loads)
+          ptx::tma_load_2d(Wr + hb * L.w_box + (half * (kBK / 2) + u * p.box_rows) * 128, &tm_b,
+                           &full[st], n0 + 64 * hb, a * p.r + qb);
+        __syncwarp();
+        ++gi;
+        ++g_run;
+      };
+      for (int b = 0; b < nbase && ok; ++b) {
+        int st;
+        if (!(ok = next_slot(&st))) break;
+        uint8_t* X = smem + static_cast<size_t>(st) * L.stage_bytes;
+        if (lane == 0) {
+          stage_lora[st] = 0;
+          ptx::mbar_arrive_expect_tx(&full[st], L.stage_bytes);
+          ptx::tma_load_2d(X, &tm_x, &full[st], b * kBK, t0);
+          ptx::tma_load_2d(X + L.x_sub, &tm_x, &full[st], b * kBK, t0 + 128);
+#pragma unroll
+          for (int h = 0; h < 4; ++h)
+            ptx::tma_load_2d(X + L.w_off + h * L.w_box, &tm_w, &full[st], n0 + 64 * h, b * kBK);
+        }
+        __syncwarp();
+        ++it;
+        if (b == ins) {
+          int got = 0, cu = 0, cg = 0;
+          if (lane == 0 && seq_wait(k)) {
+            got = 1;
+            cu = tile_units[k & 3];
+            cg = tile_groups[k & 3];
+          }
+          ok = __shfl_sync(0xffffffffu, got, 0) != 0;
+          U = __shfl_sync(0xffffffffu, cu, 0);
+          my_groups = __shfl_sync(0xffffffffu, cg, 0);
+          while (ok && gi < my_groups) {
+            if (!(ok = next_slot(&st))) break;
+            issue_lora(st);
+            ++it;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer -----------------------------------------
+    if (lane == 0) {
+      uint32_t lora_par = 0;
+      int it = 0;
+      bool ok = true;
+      for (int lin = first_tile, k = 0; lin < pp.n_tiles && ok; lin += tile_step, ++k) {
+        // both accumulators drained (tile k - 1)
+        if (!ptx::mbar_wait_bounded(acc_empty, (static_cast<uint32_t>(k) & 1u) ^ 1u, abort_f,
+                                    kWaitLimitNs))
+          break;
+        ptx::tc_fence_after();
+        int local = 0;
+        auto consume = [&]() {
+          const int st = it % p.stages;
+          const uint32_t ph = static_cast<uint32_t>(it / p.stages) & 1u;
+          if (!ptx::mbar_wait_bounded(&full[st], ph, abort_f, kWaitLimitNs)) return false;
+          if (stage_lora[st]) {
+            if (!ptx::mbar_wait_bounded(&lora_built[st], (lora_par >> st) & 1u, abort_f,
+                                        kWaitLimitNs))
+              return false;
+            lora_par ^= 1u << st;
+          }
+          ptx::tc_fence_after();
+          const uint32_t xa = ptx::smem_u32(smem + static_cast<size_t>(st) * L.stage_bytes);
+          const uint32_t wa = xa + L.w_off;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint64_t wd = ptx::sdesc_sw128(wa + kk * 16 * 128, L.w_box, 1024);
+            const uint64_t x0 = ptx::sdesc_sw128(xa + kk * 32, 16, 1024);
+            const uint64_t x1 = ptx::sdesc_sw128(xa + L.x_sub + kk * 32, 16, 1024);
+            const uint32_t acc_in = (local > 0 || kk > 0) ? 1u : 0u;
+            ptx::mma_bf16(tmem, x0, wd, kIdesc, acc_in);
+            ptx::mma_bf16(tmem + 256u, x1, wd, kIdesc, acc_in);
+          }
+          ptx::mma_commit(&empty[st]);
+          ++it;
+          ++local;
+          return true;
+        };
+        for (int s = 0; s < nbase && ok; ++s) ok = consume();
+        if (ok && seq_wait(k)) {
+          const int my_groups = tile_groups[k & 3];
+          for (int g = 0; g < my_groups && ok; ++g) ok = consume();
+        } else {
+          ok = false;
+        }
+        ptx::mma_commit(acc_full);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue warps -------------------------------------
+    const int etid = tid - 64;
+    const int ew = warp - 2;
+    const int n_words = (p.n_slots + 31) >> 5;
+    const int q = warp & 3;   // TMEM lane quarter this warp may access
+    const int c = ew >> 2;    // column half it drains; V half it builds
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    const int i = q * 32 + lane;  // row within a 128-token half
+    const int rr = c * 128 + i;   // this thread's token row of the tile
+    uint8_t* mybox = smem + L.ybox + ew * 4096;
+    int g_run = 0;
+    // Both accumulators of tile kk: this warp's 32 rows of each, its 128
+    // columns, through its own box.  Every epilogue thread passes the same
+    // named barriers whatever happens (only work is skipped after an abort).
+    auto drain = [&](int kk, int n0, int t0) {
+      warp_wait(acc_full, static_cast<uint32_t>(kk) & 1u, abort_f);
+      ptx::tc_fence_after();
+      const bool live = __shfl_sync(0xffffffffu, *abort_f == 0 ? 1 : 0, 0) != 0;
+#pragma unroll 1
+      for (int a = 0; a < 2; ++a) {
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+          if (lane == 0) ptx::bulk_wait_group_read_all();  // the box is free again
+          __syncwarp();
+          if (live) {
+#pragma unroll
+            for (int c0 = 0; c0 < 64; c0 += 16) {
+              uint32_t v[16];
+              ptx::tmem_ld16(tmem + lane_base + a * 256 + c * 128 + h * 64 + c0, v);
+              ptx::tmem_ld_wait();
+#pragma unroll
+              for (int u = 0; u < 2; ++u) {
+                const int ch = (c0 >> 3) + u;
+                uint4 pk;
+                pk.x = pack_bf16x2(__uint_as_float(v[8 * u + 0]), __uint_as_float(v[8 * u + 1]));
+                pk.y = pack_bf16x2(__uint_as_float(v[8 * u + 2]), __uint_as_float(v[8 * u + 3]));
+                pk.z = pack_bf16x2(__uint_as_float(v[8 * u + 4]), __uint_as_float(v[8 * u + 5]));
+                pk.w = pack_bf16x2(__uint_as_float(v[8 * u + 6]), __uint_as_float(v[8 * u + 7]));
+                *reinterpret_cast<uint4*>(mybox + lane * 128 + ((ch ^ (lane & 7)) << 4)) = pk;
+              }
+            }
+          }
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && live) {
+            const int col = n0 + c * 128 + h * 64, row = t0 + a * 128 + q * 32;
+            if (col < p.d_out && row < p.T) ptx::tma_store_2d(&tm_y, mybox, col, row);
+            ptx::bulk_commit_group();
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(acc_empty);
+    };
+    int k = 0;
+    int prev_n0 = 0, prev_t0 = 0;
+    for (int lin = first_tile; lin < pp.n_tiles; lin += tile_step, ++k) {
+      int n0, t0;
+      tile_origin(lin, &n0, &t0);
+      // ---- this tile's adapters (while the previous tile still streams)
+      bool bad = false;
+      {
+        const int t = t0 + rr;
+        int sl = -1;
+        if (t < p.T) {
+          const int id = p.ids[t];
+          if (slot_valid(id, p.n_slots)) sl = id;
+          else if (id != -1) bad = true;
+        }
+        tok[rr] = static_cast<int16_t>(sl);
+      }
+      for (int wd = etid; wd < n_words; wd += kWideEpi) bitmap[wd] = 0u;
+      if (bad && n0 == 0) flag_error(p.err, LORA_DEVERR_BAD_SLOT);
+      wide_epi_sync();
+      if (tok[rr] >= 0) atomicOr(&bitmap[tok[rr] >> 5], 1u << (tok[rr] & 31));
+      wide_epi_sync();
+      if (warp == 2) {
+        const int per = (n_words + 31) / 32;
+        const int w0 = min(n_words, lane * per), w1 = min(n_words, w0 + per);
+        int cnt = 0;
+        for (int wd = w0; wd < w1; ++wd) cnt += __popc(bitmap[wd]);
+        int incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int vv = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += vv;
+        }
+        int off = incl - cnt;
+        for (int wd = w0; wd < w1; ++wd) {
+          uint32_t m = bitmap[wd];
+          while (m) {
+            const int bb = __ffs(m) - 1;
+            m &= m - 1;
+            uniq[off++] = static_cast<int16_t>(wd * 32 + bb);
+          }
+        }
+        if (lane == 31) *n_uniq_s = incl;
+      }
+      wide_epi_sync();
+      const int n_uniq = *n_uniq_s;
+      {
+        const int sl = tok[rr];
+        int u = -1;
+        if (sl >= 0) {
+          int lo = 0, hi = n_uniq - 1;
+          while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (uniq[mid] < sl) lo = mid + 1;
+            else hi = mid;
+          }
+          u = lo;
+        }
+        tok[rr] = static_cast<int16_t>(u);
+      }
+      if (k == 0) pdl_wait();  // v is written by the shrink kernel launched just before
+      const int U = n_uniq * upa;
+      const int my_groups = (U + G - 1) / G;
+      if (etid == 0) {
+        tile_units[k & 3] = U;
+        tile_groups[k & 3] = my_groups;
+      }
+      wide_epi_sync();
+      if (etid == 0) {
+        __threadfence_block();
+        *vt_seq = k + 1;
+      }
+      // ---- the previous tile's accumulators: the MMA issuer waits for them
+      if (k > 0) drain(k - 1, prev_n0, prev_t0);
+      // ---- this tile's LoRA stages
+      for (int g2 = 0; g2 < my_groups; ++g2, ++g_run) {
+        if (etid == 0) {
+          const uint64_t tw = ptx::globaltimer_ns();
+          while (*lora_posted <= g_run) {
+            if (*abort_f) break;
+            if (ptx::globaltimer_ns() - tw > kWaitLimitNs) {
+              *abort_f = 1;
+              break;
+            }
+          }
+          __threadfence_block();
+        }
+        wide_epi_sync();
+        if (__shfl_sync(0xffffffffu, *abort_f == 0 ? 1 : 0, 0)) {
+          const int st = lora_mailbox[g_run & 15];
+          uint8_t* X = smem + static_cast<size_t>(st) * L.stage_bytes;
+          uint8_t* Wr = X + L.w_off;
+          uint8_t* Xh = X + c * L.x_sub;  // this thread's V half
+          const int u_first = g2 * G;
+          const int n_units = min(G, U - u_first);
+          const int tv = tok[rr];
+          const size_t row = static_cast<size_t>(t0 + rr) * p.r;
+          const size_t split = static_cast<size_t>(p.T) * p.r;
+          int q0[4];
+          float f[4][8];
+#pragma unroll
+          for (int cq = 0; cq < 4; ++cq) {
+            const int kq = cq << 3;
+            const int wu = kq >> p.lg_box;
+            const int w = u_first + wu;
+            q0[cq] = (wu < n_units && tv >= 0 && (w >> p.lg_upa) == tv)
+                         ? ((w & (upa - 1)) << p.lg_box) + (kq & (p.box_rows - 1))
+                         : -1;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[cq][e] = 0.f;
+          }
+          for (int s0 = 0; s0 < p.v_ksplit; ++s0) {
+            float g[4][8];
+#pragma unroll
+            for (int cq = 0; cq < 4; ++cq)
+              if (q0[cq] >= 0) load8_dep(p.vpart + s0 * split + row + q0[cq], g[cq]);
+#pragma unroll
+            for (int cq = 0; cq < 4; ++cq)
+              if (q0[cq] >= 0)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) f[cq][e] += g[cq][e];
+          }
+#pragma unroll
+          for (int cq = 0; cq < 4; ++cq) {
+            float hh[8], ll[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              hh[e] = __bfloat162float(__float2bfloat16_rn(f[cq][e]));
+              ll[e] = f[cq][e] - hh[e];
+            }
+            *reinterpret_cast<uint4*>(Xh + i * 128 + ((cq ^ (i & 7)) << 4)) = pack8_bf16(hh);
+            *reinterpret_cast<uint4*>(Xh + i * 128 + (((cq + 4) ^ (i & 7)) << 4)) = pack8_bf16(ll);
+          }
+          const int used = n_units << p.lg_box;
+          if (used < kBK / 2) {
+            const int per_half = (kBK / 2 - used) * 8;
+            for (int e = etid; e < 2 * per_half * 4; e += kWideEpi) {
+              const int hb = e / (2 * per_half), rem = e % (2 * per_half);
+              const int half = rem / per_half, r2 = rem % per_half;
+              *reinterpret_cast<uint4*>(Wr + hb * L.w_box + (half * (kBK / 2) + used + r2 / 8) * 128 +
+                                        (r2 % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
+            }
+          }
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&lora_built[st]);
+        }
+      }
+      prev_n0 = n0;
+      prev_t0 = t0;
+    }
+    if (k > 0) drain(k - 1, prev_n0, prev_t0);
+    if (lane == 0) ptx::bulk_wait_group_read_all();  // this warp's own stores
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
   }
   if (tid == 0 && *abort_f) flag_error(p.err, LORA_DEVERR_TIMEOUT);
 }
@@ -1238,7 +1720,7 @@ cudaError_t launch_persistent(const void* x, const void* W0, const void* B, TcPa
                               int tiles_n, int tiles_t, cudaStream_t st, const DeviceInfo& dev) {
   int stages = 0;
   for (int s = 8; s >= (KS == 2 ? 2 : 3); --s) {
-    const PersistLayout L = persist_layout<BT, BN, KS>(s, prm.r, prm.n_slots);
+    const PersistLayout L = persist_layout<BT, BN, KS>(s, prm.n_slots);
     if (L.total + 1024 <= dev.max_smem_optin) {
       stages = s;
       break;
@@ -1246,7 +1728,7 @@ cudaError_t launch_persistent(const void* x, const void* W0, const void* B, TcPa
   }
   if (stages == 0) return cudaErrorInvalidConfiguration;
   prm.stages = stages;
-  const PersistLayout L = persist_layout<BT, BN, KS>(stages, prm.r, prm.n_slots);
+  const PersistLayout L = persist_layout<BT, BN, KS>(stages, prm.n_slots);
   const size_t smem = L.total + 1024;
 
   CUtensorMap tm_x, tm_w, tm_b, tm_y;
@@ -1263,7 +1745,7 @@ cudaError_t launch_persistent(const void* x, const void* W0, const void* B, TcPa
   PersistParams pp;
   pp.t = prm;
   pp.tiles_n = tiles_n;
-  pp.tiles_t = tiles_t;
+  pp.tiles_tp = tiles_t;
   pp.n_tiles = tiles_n * tiles_t;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(pp.n_tiles < dev.num_sms ? pp.n_tiles : dev.num_sms);
@@ -1276,6 +1758,49 @@ cudaError_t launch_persistent(const void* x, const void* W0, const void* B, TcPa
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, tm_x, tm_w, tm_b, tm_y, pp);
+}
+
+cudaError_t launch_wide(const void* x, const void* W0, const void* B, TcParams prm,
+                       int tiles_n, cudaStream_t st, const DeviceInfo& dev) {
+  if (prm.n_slots > 32767) return cudaErrorInvalidConfiguration;  // int16 slot lists
+  int stages = 0;
+  for (int s = 4; s >= 2; --s) {
+    if (wide_layout(s, prm.n_slots).total + 1024 <= dev.max_smem_optin) {
+      stages = s;
+      break;
+    }
+  }
+  if (stages == 0) return cudaErrorInvalidConfiguration;
+  prm.stages = stages;
+  prm.n_kblk = (prm.d_in + kBK - 1) / kBK;
+  const size_t smem = wide_layout(stages, prm.n_slots).total + 1024;
+  CUtensorMap tm_x, tm_w, tm_b, tm_y;
+  if (!make_map(&tm_x, x, prm.d_in, prm.T, prm.d_in, kBK, 128) ||
+      !make_map(&tm_w, W0, prm.d_out, prm.d_in, prm.d_out, 64, kBK) ||
+      !make_map(&tm_b, B, prm.d_out, static_cast<uint64_t>(prm.n_slots) * prm.r, prm.d_out, 64,
+                prm.box_rows) ||
+      !make_map(&tm_y, prm.y, prm.d_out, prm.T, prm.d_out, 64, 32))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(fused_tc_wide_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  PersistParams pp;
+  pp.t = prm;
+  pp.tiles_n = tiles_n;
+  pp.tiles_tp = (prm.T + 255) / 256;
+  pp.n_tiles = tiles_n * pp.tiles_tp;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(pp.n_tiles < dev.num_sms ? pp.n_tiles : dev.num_sms);
+  cfg.blockDim = dim3(kWideThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fused_tc_wide_kernel, tm_x, tm_w, tm_b, tm_y, pp);
 }
 
 }  // namespace
@@ -1390,10 +1915,18 @@ cudaError_t launch_fused_tc(const void* x, const void* W0, const void* B, const 
   if (S == 1) {
     // more tiles than SMs: the persistent form, one CTA per SM walking
     // tiles with two accumulators in tensor memory (two 128-deep stages
-    // beside the y box; v rows come from L2 when a LoRA stage is built)
+    // beside the y box; v rows come from L2 when a LoRA stage is built).
+    // Token-adjacent tiles run in pairs sharing each W0 box (multicast)
+    // when there are two tile rows to pair.
+    // With at least two waves of 256 x 256 tiles, the wide form (two M = 128
+    // MMAs per step sharing W0); otherwise 128 x 256 tiles.
+    cudaError_t e = cudaErrorInvalidConfiguration;
+    if (tiles_n * ((T + 255) / 256) >= 2 * dev.num_sms)
+      e = launch_wide(x, W0, B, prm, tiles_n, st, dev);
+    if (e != cudaErrorInvalidConfiguration) return e;
     TcParams pp = prm;
     pp.n_kblk = (d_in + 2 * kBK - 1) / (2 * kBK);
-    const cudaError_t e = launch_persistent<128, 256, 2>(x, W0, B, pp, tiles_n, tiles_t, st, dev);
+    e = launch_persistent<128, 256, 2>(x, W0, B, pp, tiles_n, tiles_t, st, dev);
     if (e != cudaErrorInvalidConfiguration) return e;
   }
   if (KS == 2) return launch_variant<128, 256, 2>(x, W0, B, prm, tiles_n, tiles_t, S, st, dev);
