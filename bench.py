@@ -194,11 +194,18 @@ def parse_clocks(lines):
             "samples": len(sm)}
 
 
-def fused_ksplit(T, d_in, n_slots, num_sms=152):
+# d_in split of the standalone SGMV shrink on the prefill workload (the
+# fastest of 1..8 there: 33 us against 38 us at 2 and 62 us at 1)
+SGMV_KSPLIT = 4
+
+
+def fused_ksplit(T, d_in, d_out, n_slots, num_sms=152):
     """The shrink split the fused path uses (mirrors the library's choice;
     tests/test_bench_host.py checks it against lora_workspace_bytes)."""
     if T <= 256:      # decode-sized batch: per-token shrink, ~256 CTAs
         return max(1, min(-(-256 // max(T, 1)), 16, max(d_in // 512, 1)))
+    if n_slots <= 32767 and -(-d_out // 256) * -(-T // 256) >= 2 * num_sms:
+        return 1      # 256 x 256 prefill tiles: v as one partial, copied ahead
     cap = min(T, n_slots)
     est = (T + 63) // 64 + (cap + 1) // 2
     ks = -(-2 * num_sms // max(est, 1))
@@ -403,7 +410,7 @@ def decode_blocks(sets, L, w, stream, pk, n_steps=400):
     T, d_in, d_out, r, n_slots, D = w.T, w.d_in, w.d_out, w.r, w.n_slots, w.distinct
     T_lora = int(((w.slot_ids >= 0) & (w.slot_ids < n_slots)).sum())
     dev = sets[0].x.device
-    ks = fused_ksplit(T, d_in, n_slots)
+    ks = fused_ksplit(T, d_in, d_out, n_slots)
     vpart = torch.zeros((ks, T, r), dtype=torch.float32, device=dev)
     delta = torch.zeros((T, d_out), dtype=torch.float32, device=dev)
     ws = torch.zeros(256, dtype=torch.uint8, device=dev)
@@ -617,7 +624,7 @@ def prefill_point(L, stream, pk, dev, steps=30, warm=5):
     nbytes = layer_bytes(T, d_in, d_out, r, D)
     tf = flops / t / 1e12
     # the scope table's a1 / a2 / a3 rows on their own on this workload
-    ks = fused_ksplit(T, d_in, n_slots)
+    ks = SGMV_KSPLIT
     wss = torch.zeros(256, dtype=torch.uint8, device=dev)
     segs = L.build_segments_t(ids, n_slots, wss, stream=stream)
     vpart = torch.zeros((ks, T, r), dtype=torch.float32, device=dev)
@@ -863,7 +870,7 @@ def run_profile(case):
         scale = torch.full((n_slots,), W.SCALE, dtype=torch.float32, device=dev)
         y = torch.empty((T, d_out), dtype=torch.bfloat16, device=dev)
         ws = L.workspace(L.OP_LINEAR_FUSED, T, d_in, d_out, r, n_slots)
-        ks = fused_ksplit(T, d_in, n_slots)
+        ks = SGMV_KSPLIT
         wss = torch.zeros(256, dtype=torch.uint8, device=dev)
         vpart = torch.zeros((ks, T, r), dtype=torch.float32, device=dev)
         for _ in range(3):

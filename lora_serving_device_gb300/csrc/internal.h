@@ -51,6 +51,10 @@ cudaError_t launch_set_scale(float* scale, int slot, float s, cudaStream_t st);
 int sgmv_max_items(int T, int n_slots);
 // ksplit the fused path uses for its shrink (SGMV / BGMV form).
 int fused_shrink_ksplit(int T, int d_in, int n_slots, int num_sms);
+// True when the fused prefill GEMM takes 256 x 256 tiles (k_fused_tc.cu);
+// its LoRA stages then copy v asynchronously, which wants a single shrink
+// partial (split 1).
+bool fused_wide_tiles(int T, int d_out, int n_slots, int num_sms);
 int decode_shrink_ksplit(int T, int d_in);
 
 // Base GEMM + expand-in-accumulator kernel, bf16 (tcgen05), see k_fused_tc.cu.

@@ -1287,9 +1287,14 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     // ---------------- producer -------------------------------------------
     int it = 0, g_run = 0;
     bool ok = true;
-    // a tile's LoRA stages follow this base stage: late enough that the
-    // epilogue warps have drained the previous tile when they are posted
+    // a tile's LoRA stages start after this base stage (late enough that the
+    // epilogue warps have drained the previous tile when the first is posted)
+    // and are spread over the next `span` base stages, so that their B loads
+    // and V builds overlap base-stage MMAs; the last is posted about eight
+    // stages before the tile ends, which leaves the epilogue warps time to
+    // publish the next tile's adapters
     const int ins = nbase > 3 ? 3 : nbase - 1;
+    const int span = nbase - ins - 8 > 1 ? nbase - ins - 8 : 1;
     for (int lin = first_tile, k = 0; lin < pp.n_tiles && ok; lin += tile_step, ++k) {
       int n0, t0;
       tile_origin(lin, &n0, &t0);
@@ -1355,12 +1360,22 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           ok = __shfl_sync(0xffffffffu, got, 0) != 0;
           U = __shfl_sync(0xffffffffu, cu, 0);
           my_groups = __shfl_sync(0xffffffffu, cg, 0);
-          while (ok && gi < my_groups) {
+        }
+        if (b >= ins) {
+          // groups due after base stage b: ceil((b - ins + 1) * groups / span)
+          const int due = min(my_groups, ((b - ins + 1) * my_groups + span - 1) / span);
+          while (ok && gi < due) {
             if (!(ok = next_slot(&st))) break;
             issue_lora(st);
             ++it;
           }
         }
+      }
+      while (ok && gi < my_groups) {
+        int st;
+        if (!(ok = next_slot(&st))) break;
+        issue_lora(st);
+        ++it;
       }
     }
   } else if (warp == 1) {
@@ -1868,6 +1883,12 @@ bool encode_tensor_map_u8_sw128(CUtensorMap* m, const void* base, uint64_t inner
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool fused_wide_tiles(int T, int d_out, int n_slots, int num_sms) {
+  // at least two waves of 256 x 256 tiles; int16 slot lists
+  return T > 256 && n_slots <= 32767 &&
+         static_cast<long long>((d_out + 255) / 256) * ((T + 255) / 256) >= 2LL * num_sms;
+}
+
 bool tensor_map_available() {
   resolve_encode();
   return g_encode != nullptr;
@@ -1921,7 +1942,7 @@ cudaError_t launch_fused_tc(const void* x, const void* W0, const void* B, const 
     // With at least two waves of 256 x 256 tiles, the wide form (two M = 128
     // MMAs per step sharing W0); otherwise 128 x 256 tiles.
     cudaError_t e = cudaErrorInvalidConfiguration;
-    if (tiles_n * ((T + 255) / 256) >= 2 * dev.num_sms)
+    if (fused_wide_tiles(T, d_out, n_slots, dev.num_sms))
       e = launch_wide(x, W0, B, prm, tiles_n, st, dev);
     if (e != cudaErrorInvalidConfiguration) return e;
     TcParams pp = prm;

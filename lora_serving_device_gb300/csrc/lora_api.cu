@@ -62,8 +62,9 @@ FusedWs fused_ws_layout(void* ws, int32_t T, int32_t d_in, int32_t d_out, int32_
   o += 4;
   o = round_up(o, 256);
   const size_t o_v = o;
-  w.ksplit = T <= kDecodeTokens ? decode_shrink_ksplit(T, d_in)
-                              : fused_shrink_ksplit(T, d_in, n_slots, 152);
+  w.ksplit = T <= kDecodeTokens                         ? decode_shrink_ksplit(T, d_in)
+              : fused_wide_tiles(T, d_out, n_slots, 152) ? 1
+                                                         : fused_shrink_ksplit(T, d_in, n_slots, 152);
   o += static_cast<size_t>(w.ksplit) * T * r * 4;
   o = round_up(o, 256);
   const size_t o_d = o;

@@ -29,13 +29,15 @@ def test_layer_bytes_decode():
 def test_fused_ksplit_matches_library():
     from lora_serving_device_gb300 import build, lora as L
     build.build()
-    for T, d_in, n_slots, r in [(64, 4096, 256, 16), (8752, 4096, 64, 64), (256, 14336, 250, 64),
-                                (32, 4096, 1024, 16), (1, 64, 3, 8)]:
-        ks = bench.fused_ksplit(T, d_in, n_slots)
+    for T, d_in, d_out, n_slots, r in [(64, 4096, 1024, 256, 16), (8752, 4096, 1024, 64, 64),
+                                       (8752, 4096, 14336, 64, 64), (9081, 4096, 14336, 64, 64),
+                                       (1000, 200, 20008, 24, 16), (700, 1032, 12296, 24, 64),
+                                       (256, 14336, 1024, 250, 64), (32, 4096, 1024, 1024, 16),
+                                       (1, 64, 1024, 3, 8)]:
+        ks = bench.fused_ksplit(T, d_in, d_out, n_slots)
         cap = min(T, n_slots)
         head = 16 + T * 4 + cap * 4 + (cap + 1) * 4 + 4
         head = -(-head // 256) * 256
-        d_out = 1024
         body = -(-(head + ks * T * r * 4) // 256) * 256
         if T <= 256:                       # decode-sized: split-K fp32 base product
             S = L.lora_decode_split(T, d_in, d_out)
