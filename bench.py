@@ -194,9 +194,12 @@ def parse_clocks(lines):
             "samples": len(sm)}
 
 
-# d_in split of the standalone SGMV shrink on the prefill workload (the
-# fastest of 1..8 there: 33 us against 38 us at 2 and 62 us at 1)
-SGMV_KSPLIT = 4
+# d_in splits for the standalone SGMV rows on the prefill workload: the shrink
+# is fastest at 4 of 1..8 (33 us against 38 us at 2 and 62 us at 1); the
+# expand, which sums the partials in its V build, at 2 (244 us against 266 us
+# at 4)
+SGMV_SHRINK_KSPLIT = 4
+SGMV_EXPAND_KSPLIT = 2
 
 
 def fused_ksplit(T, d_in, d_out, n_slots, num_sms=152):
@@ -624,22 +627,24 @@ def prefill_point(L, stream, pk, dev, steps=30, warm=5):
     nbytes = layer_bytes(T, d_in, d_out, r, D)
     tf = flops / t / 1e12
     # the scope table's a1 / a2 / a3 rows on their own on this workload
-    ks = SGMV_KSPLIT
+    ks, kx = SGMV_SHRINK_KSPLIT, SGMV_EXPAND_KSPLIT
     wss = torch.zeros(256, dtype=torch.uint8, device=dev)
     segs = L.build_segments_t(ids, n_slots, wss, stream=stream)
     vpart = torch.zeros((ks, T, r), dtype=torch.float32, device=dev)
+    vpart_x = torch.zeros((kx, T, r), dtype=torch.float32, device=dev)
+    L.sgmv_shrink_t(x, A, segs, scale, kx, wss, v_partial=vpart_x, stream=stream)
     b_seg = 4 * T + 4 * T + 8 * D + 8
     b_shrink = D * d_in * r * 2 + T * d_in * 2 + ks * T * r * 4
-    b_expand = D * r * d_out * 2 + ks * T * r * 4 + 2 * T * d_out * 2
+    b_expand = D * r * d_out * 2 + kx * T * r * 4 + 2 * T * d_out * 2
     blocks = {
-        "ksplit": ks,
+        "ksplit": {"sgmv_shrink": ks, "sgmv_expand": kx},
         "build_segments": block_row(graph_mean_ms(
             lambda i: L.build_segments_t(ids, n_slots, wss, stream=stream), 50, stream), b_seg, pk),
         "sgmv_shrink": block_row(graph_mean_ms(
             lambda i: L.sgmv_shrink_t(x, A, segs, scale, ks, wss, v_partial=vpart, stream=stream),
             30, stream), b_shrink, pk),
         "sgmv_expand": block_row(graph_mean_ms(
-            lambda i: L.sgmv_expand_t(vpart, B, segs, y, wss, stream=stream), 30, stream),
+            lambda i: L.sgmv_expand_t(vpart_x, B, segs, y, wss, stream=stream), 30, stream),
             b_expand, pk)}
     res = {"workload": "prefill_sgmv: 4096->14336, rank 64, 64 slots, 16 prefill requests "
                        "(U[64,1024] tokens) + 48 decode tokens",
@@ -870,14 +875,16 @@ def run_profile(case):
         scale = torch.full((n_slots,), W.SCALE, dtype=torch.float32, device=dev)
         y = torch.empty((T, d_out), dtype=torch.bfloat16, device=dev)
         ws = L.workspace(L.OP_LINEAR_FUSED, T, d_in, d_out, r, n_slots)
-        ks = SGMV_KSPLIT
+        ks, kx = SGMV_SHRINK_KSPLIT, SGMV_EXPAND_KSPLIT
         wss = torch.zeros(256, dtype=torch.uint8, device=dev)
         vpart = torch.zeros((ks, T, r), dtype=torch.float32, device=dev)
+        vpart_x = torch.zeros((kx, T, r), dtype=torch.float32, device=dev)
         for _ in range(3):
             L.linear_fused_t(x, W0, A, Bp, ids, scale, ws, y=y, stream=stream)
             segs = L.build_segments_t(ids, n_slots, wss, stream=stream)
             L.sgmv_shrink_t(x, A, segs, scale, ks, wss, v_partial=vpart, stream=stream)
-            L.sgmv_expand_t(vpart, Bp, segs, y, wss, stream=stream)
+            L.sgmv_shrink_t(x, A, segs, scale, kx, wss, v_partial=vpart_x, stream=stream)
+            L.sgmv_expand_t(vpart_x, Bp, segs, y, wss, stream=stream)
         err = L.get_error_t(ws, stream=stream)
     else:
         w = W.decode_bgmv()
