@@ -304,7 +304,10 @@ def test_prefill_sgmv_full(L):
 
 # more 128 x 256 output tiles than SMs: each CTA walks several tiles with two
 # accumulators in tensor memory (632 tiles: up to five per CTA)
-PERSIST_CASES = [(1000, 200, 20008, 16, True), (700, 1032, 12296, 64, False)]
+PERSIST_CASES = [(1000, 200, 20008, 16, True), (700, 1032, 12296, 64, False),
+                 # 256 x 256 tiles with four rank-8 units per LoRA stage (B rows
+                 # past the stage's units zero-filled) and with rank 128
+                 (1024, 136, 19456, 8, False), (600, 264, 30000, 128, True)]
 
 
 @pytest.mark.parametrize("T,d_in,d_out,r,runs", PERSIST_CASES, ids=[str(c) for c in PERSIST_CASES])
@@ -493,6 +496,34 @@ def test_base_gemm_expand_matches_oracle(L, case):
     y0 = L.base_gemm_expand_t(d0.x, d0.W0, d0.B, d0.ids, dev(vp, "f32"), ws)
     torch.cuda.synchronize()
     check_close_bf16_out(host(y0), ref - base, "folded expand alone")
+
+
+# more 256 x 256 tiles than two waves, v given as three partials: the wide
+# prefill GEMM's LoRA stages sum the partials while building V; and the 128 x
+# 256 persistent form
+GEMM_EXPAND_WIDE = [(1000, 200, 20008, 16, 24), (1024, 136, 19456, 8, 30),
+                    (700, 1032, 12296, 64, 24)]
+
+
+@pytest.mark.parametrize("case", GEMM_EXPAND_WIDE, ids=[str(c) for c in GEMM_EXPAND_WIDE])
+def test_base_gemm_expand_many_tiles(L, case):
+    torch = torch_mod()
+    T, d_in, d_out, r, n_slots = case
+    w = W.random_case(780 + T, T, d_in, d_out, r, n_slots, runs=True)
+    w.slot_ids[128:400] = -1
+    d = DeviceCase(w)
+    ws = _ws(L)
+    vp = _v_input(T, r, 3, 4)
+    y = L.base_gemm_expand_t(d.x, d.W0, d.B, d.ids, dev(vp, "f32"), ws)
+    torch.cuda.synchronize()
+    base = O.lora_linear(w.x, w.W0, w.A_pool, w.B_pool, w.scale, np.full(T, -1))
+    ref = base + O.expand(vp.astype(np.float64).sum(axis=0), w.B_pool, w.slot_ids)
+    check_close(host(y), ref, "many-tile base GEMM + folded expand")
+    assert L.get_error_t(ws) == 0
+    d0 = DeviceCase(w, W0_zero=True)
+    y0 = L.base_gemm_expand_t(d0.x, d0.W0, d0.B, d0.ids, dev(vp, "f32"), ws)
+    torch.cuda.synchronize()
+    check_close_bf16_out(host(y0), ref - base, "many-tile folded expand alone")
 
 
 # ------------------------------------------------------------- slot upload
