@@ -1287,13 +1287,12 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     // ---------------- producer -------------------------------------------
     int it = 0, g_run = 0;
     bool ok = true;
-    // a tile's LoRA stages start after this base stage (late enough that the
-    // epilogue warps have drained the previous tile when the first is posted)
-    // and are spread over the next `span` base stages, so that their B loads
-    // and V builds overlap base-stage MMAs; the last is posted about eight
-    // stages before the tile ends, which leaves the epilogue warps time to
-    // publish the next tile's adapters
-    const int ins = nbase > 3 ? 3 : nbase - 1;
+    // a tile's LoRA stages start after its second base stage and are spread
+    // over the next `span` base stages, so that their B loads and V builds
+    // overlap base-stage MMAs; the last is posted about eight stages before
+    // the tile ends, which leaves the epilogue warps time to publish the next
+    // tile's adapters
+    const int ins = nbase > 1 ? 1 : nbase - 1;
     const int span = nbase - ins - 8 > 1 ? nbase - ins - 8 : 1;
     for (int lin = first_tile, k = 0; lin < pp.n_tiles && ok; lin += tile_step, ++k) {
       int n0, t0;
