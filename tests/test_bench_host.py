@@ -4,6 +4,7 @@ reduction (gloo, world size 2)."""
 import os
 import socket
 
+import numpy as np
 import pytest
 
 import bench
@@ -26,14 +27,30 @@ def test_layer_bytes_decode():
     assert g < b and g > 32 * 2 ** 20
 
 
+def _ksplit_cases():
+    fixed = [(64, 4096, 1024, 256, 16), (8752, 4096, 1024, 64, 64),
+             (8752, 4096, 14336, 64, 64), (9081, 4096, 14336, 64, 64),
+             (1000, 200, 20008, 24, 16), (700, 1032, 12296, 24, 64),
+             (256, 14336, 1024, 250, 64), (32, 4096, 1024, 1024, 16), (1, 64, 1024, 3, 8),
+             # either side of two waves of 256 x 256 tiles (304 on 152 SMs)
+             (1024, 512, 256 * 76, 16, 16), (1024, 512, 256 * 76 - 8, 16, 16),
+             (257, 512, 256 * 152, 16, 16), (257, 512, 256 * 151, 16, 16),
+             (2048, 512, 256 * 38, 16384, 8)]
+    rng = np.random.default_rng(20261203)
+    drawn = [(int(rng.integers(1, 20000)), 8 * int(rng.integers(1, 2048)),
+              8 * int(rng.integers(1, 6000)), int(rng.integers(1, 3000)),
+              int(rng.choice([8, 16, 32, 64, 128]))) for _ in range(40)]
+    return fixed + drawn
+
+
 def test_fused_ksplit_matches_library():
+    """bench.py sizes its buffers with a mirror of the library's shrink-split
+    rule (including split 1 where the 256 x 256 prefill tiles run); the
+    workspace size the library reports pins the mirror on fixed and drawn
+    shapes."""
     from lora_serving_device_gb300 import build, lora as L
     build.build()
-    for T, d_in, d_out, n_slots, r in [(64, 4096, 1024, 256, 16), (8752, 4096, 1024, 64, 64),
-                                       (8752, 4096, 14336, 64, 64), (9081, 4096, 14336, 64, 64),
-                                       (1000, 200, 20008, 24, 16), (700, 1032, 12296, 24, 64),
-                                       (256, 14336, 1024, 250, 64), (32, 4096, 1024, 1024, 16),
-                                       (1, 64, 1024, 3, 8)]:
+    for T, d_in, d_out, n_slots, r in _ksplit_cases():
         ks = bench.fused_ksplit(T, d_in, d_out, n_slots)
         cap = min(T, n_slots)
         head = 16 + T * 4 + cap * 4 + (cap + 1) * 4 + 4
