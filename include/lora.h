@@ -131,9 +131,12 @@ lora_status_t lora_bgmv_shrink(const void* x, const void* A_pool, const int32_t*
                                void* ws, size_t ws_bytes, void* stream);
 
 /*
- * BGMV expand: y[t, :] += (sum_s v_partial[s, t, :]) B[a_t] for tokens with a
- * valid id (fp32 arithmetic, one rounding to dt per element).  Base-only rows
- * of y are not touched.  Accumulates into y.
+ * BGMV expand ("Serving multiple LoRAs ...", BGMV bullet: each token gathers
+ * its own adapter's factors by index; the paragraph after the toy script:
+ * the rank-r result is expanded with B and added into the base output):
+ * y[t, :] += (sum_s v_partial[s, t, :]) B[a_t] for tokens with a valid id
+ * (fp32 arithmetic, one rounding to dt per element).  Base-only rows of y
+ * are not touched.  Accumulates into y.
  */
 lora_status_t lora_bgmv_expand(const float* v_partial, int32_t ksplit, const void* B_pool,
                                const int32_t* slot_ids, void* y, int32_t T, int32_t r,
@@ -156,8 +159,11 @@ lora_status_t lora_sgmv_shrink(const void* x, const void* A_pool, const int32_t*
                                void* stream);
 
 /*
- * SGMV expand: per segment, y[t, :] += (sum_s v_partial[s, t, :]) B[a] for
- * the segment's tokens, reading B[a] once per segment.  Accumulates into y;
+ * SGMV expand ("Serving multiple LoRAs ...", SGMV bullet: one segment per
+ * adapter, so its factors are read once for the segment; the paragraph
+ * after the toy script: expand with B and add into the base output):
+ * per segment, y[t, :] += (sum_s v_partial[s, t, :]) B[a] for the
+ * segment's tokens, reading B[a] once per segment.  Accumulates into y;
  * base-only rows untouched.
  */
 lora_status_t lora_sgmv_expand(const float* v_partial, int32_t ksplit, const void* B_pool,
@@ -252,14 +258,16 @@ lora_status_t lora_bgmv_adapter_merge(const void* x, const void* A_pool, const v
 /*
  * The shared base product split over d_in, on tcgen05 tensor cores with
  * the token dimension as the MMA's N (bf16 only):
- *   partial[s, t, :] = x[t, K_s] W0[K_s, :]      s = 0 .. ksplit-1
- * where K_0 .. K_{ksplit-1} are contiguous ranges of d_in that together
- * cover it ("Multi-LoRA batching and adapter paging", section "Walking
- * through a batch": one base product for the whole batch).  partial
- * [ksplit, T, d_out] fp32, caller-owned, fully written.  1 <= ksplit <=
- * the number of 192-row (T <= 64) or 128-row (T > 64) blocks of d_in, and
- * <= LORA_MAX_KSPLIT; lora_decode_split gives the value lora_linear_fused
- * uses.  Any T; it is built for T <= 256.  Workspace: the error word only.
+ *   partial[s, t, :] = x[t, K_s] W0[K_s, :]      s = 0 .. S-1
+ * where K_0 .. K_{S-1} are contiguous ranges of d_in that together cover it
+ * ("Multi-LoRA batching and adapter paging", section "Walking through a
+ * batch": one base product for the whole batch), so sum_s partial[s] =
+ * x W0.  partial [S, T, d_out] (S = ksplit) fp32, caller-owned, fully
+ * written.  1 <= ksplit <= the number of 192-row (T <= 64) or 128-row
+ * (T > 64) blocks of d_in and <= LORA_MAX_KSPLIT, or ksplit == 0 for the
+ * split lora_linear_fused uses (S = lora_decode_split(T, d_in, d_out);
+ * 1 <= T <= 256 only).  Any T; it is built for T <= 256.  Workspace: the
+ * error word only.
  */
 lora_status_t lora_base_gemm_splitk(const void* x, const void* W0, float* partial, int32_t T,
                                     int32_t d_in, int32_t d_out, int32_t ksplit, lora_dtype_t dt,
@@ -267,10 +275,28 @@ lora_status_t lora_base_gemm_splitk(const void* x, const void* W0, float* partia
 
 /*
  * The ksplit lora_linear_fused uses for the base product of a bf16 batch of
- * 1 <= T <= 256 tokens (a function of the shapes only, so results do not
- * depend on the device); 0 for other T or invalid dimensions.
+ * 1 <= T <= 256 tokens: (d_out / 128 column tiles) x ksplit ~ 152 CTAs.  A
+ * function of the shapes only: it is laid out for a 152-SM GB300 whatever
+ * the current device, so results do not depend on the device.  0 for other
+ * T or invalid dimensions.
  */
 int32_t lora_decode_split(int32_t T, int32_t d_in, int32_t d_out);
+
+/*
+ * Diagnostic for tests of the failure path; the pages have no counterpart.
+ * Enqueues the kernel of lora_base_gemm_splitk (ksplit 1) with its TMA
+ * producer held back, so nothing ever arrives on the barrier its MMA issuer
+ * waits on.  Each bounded wait of the kernel gives up after wait_us
+ * microseconds (1 <= wait_us <= 2,000,000; the library's kernels otherwise
+ * use 2 s); the kernel then sets LORA_DEVERR_TIMEOUT in the workspace error
+ * word, writes nothing to partial, frees its tensor memory and returns, so
+ * the device stays usable.  partial is [1, T, d_out] fp32 (not written);
+ * 1 <= T <= 256.  Workspace: the error word only.
+ */
+lora_status_t lora_debug_gemm_wait_timeout(const void* x, const void* W0, float* partial,
+                                           int32_t T, int32_t d_in, int32_t d_out,
+                                           int32_t wait_us, void* ws, size_t ws_bytes,
+                                           void* stream);
 
 /*
  * The last kernel of lora_linear_fused on its own: the shared base product
@@ -295,11 +321,17 @@ lora_status_t lora_base_gemm_expand(const void* x, const void* W0, const void* B
  * process does not let allocate, and paths that forbid allocation once they
  * are running.  The pages have no counterpart; this is a library concern.
  *
- * Scratch: a fixed array of LORA_NOALLOC_SCRATCH_BYTES inside the library,
- * present in every GPU's memory from load until process exit.  Batches whose
+ * Scratch: a fixed array of LORA_NOALLOC_SCRATCH_BYTES inside the library.
+ * Its device memory is committed when the library's device code is loaded
+ * on a GPU: under CUDA's lazy module loading (the default) that happens in
+ * the first call on each device; with CUDA_MODULE_LOADING=EAGER, when the
+ * process first uses the GPU.  It is held until the process exits.  Make
+ * the first call on each device before an allocator reserves the rest of
+ * its memory, or that first call may fail (LORA_ERR_CUDA).  Batches whose
  * scratch (lora_workspace_bytes(LORA_OP_LINEAR_FUSED, ...)) is larger are
- * refused with LORA_ERR_WORKSPACE before anything is enqueued.  The call
- * allocates nothing (no cudaMalloc, no allocating library routine).
+ * refused with LORA_ERR_WORKSPACE, and every other invalid argument with
+ * its status, before anything is enqueued.  The call allocates nothing (no
+ * cudaMalloc, no allocating library routine).
  *
  * The first call on a device looks up the array's device address (with that
  * device current) and caches it; make that first call before any stream

@@ -164,15 +164,43 @@ cudaError_t launch_decode_q4(const void* x, const void* Wq, const void* absmax,
 // bf16 W0 [d_in, d_out] -> 4-bit codes and bf16 absmax (see k_decode_q4.cu).
 cudaError_t launch_quantize_q4(const void* W0, const void* codebook, void* Wq, void* absmax,
                                int d_in, int d_out, cudaStream_t st);
+// The fused layer's decode split is laid out for a 152-SM GB300
+// (kDecodeScheduleCtas CTAs at most), not for the current device, so that
+// the order of the fp32 additions (and so every result bit) and the
+// workspace size are the same on every device.
+constexpr int kDecodeScheduleCtas = 152;
+
 // Decode-sized base GEMM split over d_in into S fp32 partials
-// partial[z, t, :] = x[t, K_z] W0[K_z, :], see k_decode_tc.cu.  `pdl`: launch
-// as a programmatic dependent (W0 is prefetched before the wait, x after).
-// decode_gemm_split: the S the fused layer uses (a function of the shapes
-// only); decode_gemm_max_split: the largest S the kernel accepts.
+// partial[z, t, :] = x[t, K_z] W0[K_z, :] (K_z: contiguous ranges of whole
+// 64*KSUB-row blocks), see k_decode_tc.cu.  ksplit 0 takes
+// decode_gemm_split.  `pdl`: launch as a programmatic dependent (W0 is
+// prefetched before the wait, x after).  decode_gemm_split: the S the fused
+// layer uses, tiles x S ~ kDecodeScheduleCtas (a function of the shapes
+// only); decode_uniform_split: the 4-bit GEMM's split (the same rule);
+// decode_gemm_max_split: the largest S the kernel takes.
 int decode_gemm_split(int T, int d_in, int d_out);
 int decode_gemm_max_split(int T, int d_in);
+int decode_uniform_split(int T, int d_in, int d_out);
 cudaError_t launch_decode_gemm(const void* x, const void* W0, float* partial, int T, int d_in,
-                               int d_out, int S, uint32_t* err, bool pdl, cudaStream_t st,
+                               int d_out, int ksplit, uint32_t* err, bool pdl, cudaStream_t st,
                                const DeviceInfo& dev);
+// Diagnostic form for tests of the failure path: the same kernel (ksplit 1)
+// with its TMA producer held back, so nothing ever arrives on the barrier
+// the MMA issuer waits on, and every bounded wait gives up after wait_ns.
+// The kernel raises LORA_DEVERR_TIMEOUT, skips its output, frees its
+// tensor memory and returns.
+cudaError_t launch_decode_gemm_held(const void* x, const void* W0, float* partial, int T,
+                                    int d_in, int d_out, uint64_t wait_ns, uint32_t* err,
+                                    cudaStream_t st, const DeviceInfo& dev);
+
+// lora_linear_fused with one option: clear_error_word clears the
+// workspace's error word on the stream once every argument has passed
+// validation, right before the layer's kernels (lora_linear_fused_noalloc,
+// whose workspace is a shared array inside the library, uses it).
+lora_status_t linear_fused_impl(const void* x, const void* W0, const void* A_pool,
+                                const void* B_pool, const int32_t* slot_ids, const float* scale,
+                                void* y, int32_t T, int32_t d_in, int32_t d_out, int32_t r,
+                                int32_t n_slots, lora_dtype_t dt, void* ws, size_t ws_bytes,
+                                void* stream, bool clear_error_word);
 
 }  // namespace lora

@@ -39,8 +39,10 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 struct DecParams {
   int T, d_in, d_out;
-  int n_blk;   // K blocks of 64*KSUB rows over d_in
-  int stages;  // ring depth
+  int n_blk;          // K blocks of 64*KSUB rows over d_in
+  int stages;         // ring depth
+  uint64_t wait_ns;   // limit of every bounded wait
+  int hold_producer;  // diagnostic: the producer issues no load at all
   uint32_t* err;
 };
 
@@ -57,9 +59,10 @@ struct DecLayout {
   static __host__ __device__ uint32_t total(int stages) { return misc(stages) + 16; }
 };
 
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          uint64_t limit) {
   int ok = 0;
-  if ((threadIdx.x & 31) == 0) ok = ptx::mbar_wait_bounded(bar, parity, abort, kWaitLimitNs) ? 1 : 0;
+  if ((threadIdx.x & 31) == 0) ok = ptx::mbar_wait_bounded(bar, parity, abort, limit) ? 1 : 0;
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 __device__ __forceinline__ void named_sync(int id, int n) {
@@ -131,7 +134,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- producer -------------------------------------------
     // W0 of the first ring's worth of stages goes out before the wait for
     // the predecessor grid; x of those stages right after it
-    const int pre = n_it < p.stages ? n_it : p.stages;
+    // (held back: nothing is issued, so every consumer's bounded wait runs out)
+    const int pre = p.hold_producer ? 0 : (n_it < p.stages ? n_it : p.stages);
     if (lane == 0) {
       for (int it = 0; it < pre; ++it) {
         uint8_t* Wr = smem + static_cast<size_t>(it) * Lay::kStage + Lay::kXBytes;
@@ -153,10 +157,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-    for (int it = pre; it < n_it; ++it) {
+    for (int it = pre; !p.hold_producer && it < n_it; ++it) {
       const int st = it % p.stages;
       const uint32_t ph = static_cast<uint32_t>(it / p.stages) & 1u;
-      if (!warp_wait(&empty[st], ph ^ 1u, abort_f)) break;
+      if (!warp_wait(&empty[st], ph ^ 1u, abort_f, p.wait_ns)) break;
       if (lane == 0) {
         uint8_t* X = smem + static_cast<size_t>(st) * Lay::kStage;
         uint8_t* Wr = X + Lay::kXBytes;
@@ -175,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int it = 0; it < n_it; ++it) {
         const int st = it % p.stages;
         const uint32_t ph = static_cast<uint32_t>(it / p.stages) & 1u;
-        if (!ptx::mbar_wait_bounded(&full[st], ph, abort_f, kWaitLimitNs)) break;
+        if (!ptx::mbar_wait_bounded(&full[st], ph, abort_f, p.wait_ns)) break;
         ptx::tc_fence_after();
         const uint32_t xa = ptx::smem_u32(smem + static_cast<size_t>(st) * Lay::kStage);
         const uint32_t wa = xa + Lay::kXBytes;
@@ -205,7 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // store into partial [S][T][d_out]; rows past T and columns past d_out
     // are clipped by the tensor bounds.
     const int etid = tid - 64;
-    const bool acc_ok = warp_wait(accum_full, 0, abort_f) && n_it > 0 && !*abort_f;
+    const bool acc_ok = warp_wait(accum_full, 0, abort_f, p.wait_ns) && n_it > 0 && !*abort_f;
     float* stage_out = reinterpret_cast<float*>(smem);
     if (acc_ok) {
       ptx::tc_fence_after();
@@ -287,11 +291,11 @@ int decode_blocks(int T, int d_in) {
 }  // namespace
 
 int decode_gemm_split(int T, int d_in, int d_out) {
-  // one CTA per SM of a 152-SM part: (d_out/128 column tiles) x (token
+  // one CTA per SM of a 152-SM GB300: (d_out/128 column tiles) x (token
   // tiles) x S; at most one split per K block and LORA_MAX_KSPLIT splits
   const int BT = decode_bt(T > 0 ? T : 1);
   const int tiles = ((d_out + 127) / 128) * ((T + BT - 1) / BT);
-  int S = 152 / (tiles > 0 ? tiles : 1);
+  int S = kDecodeScheduleCtas / (tiles > 0 ? tiles : 1);
   const int smax = decode_gemm_max_split(T, d_in);
   if (S > smax) S = smax;
   return S < 1 ? 1 : S;
@@ -302,9 +306,11 @@ int decode_gemm_max_split(int T, int d_in) {
   return n_blk < LORA_MAX_KSPLIT ? n_blk : LORA_MAX_KSPLIT;
 }
 
-cudaError_t launch_decode_gemm(const void* x, const void* W0, float* partial, int T, int d_in,
-                               int d_out, int S, uint32_t* err, bool pdl, cudaStream_t st,
-                               const DeviceInfo& dev) {
+namespace {
+
+cudaError_t launch_decode_common(const void* x, const void* W0, float* partial, int T, int d_in,
+                                 int d_out, int S, uint64_t wait_ns, int hold, uint32_t* err,
+                                 bool pdl, cudaStream_t st, const DeviceInfo& dev) {
   if (T <= 0) return cudaSuccess;
   const int BT = decode_bt(T);
   const int ksub = decode_ksub(BT);
@@ -324,6 +330,8 @@ cudaError_t launch_decode_gemm(const void* x, const void* W0, float* partial, in
   prm.d_out = d_out;
   prm.n_blk = n_blk;
   prm.stages = 0;
+  prm.wait_ns = wait_ns;
+  prm.hold_producer = hold;
   prm.err = err;
   if (BT == 32)
     return launch_decode_variant<32, 3>(tm_x, tm_w, tm_p, prm, tiles_n, tiles_t, S, pdl, st, dev);
@@ -333,5 +341,23 @@ cudaError_t launch_decode_gemm(const void* x, const void* W0, float* partial, in
     return launch_decode_variant<128, 2>(tm_x, tm_w, tm_p, prm, tiles_n, tiles_t, S, pdl, st, dev);
   return launch_decode_variant<256, 1>(tm_x, tm_w, tm_p, prm, tiles_n, tiles_t, S, pdl, st, dev);
 }
+
+}  // namespace
+
+cudaError_t launch_decode_gemm(const void* x, const void* W0, float* partial, int T, int d_in,
+                               int d_out, int ksplit, uint32_t* err, bool pdl, cudaStream_t st,
+                               const DeviceInfo& dev) {
+  const int S = ksplit >= 1 ? ksplit : decode_gemm_split(T, d_in, d_out);
+  return launch_decode_common(x, W0, partial, T, d_in, d_out, S, kWaitLimitNs, 0, err, pdl, st,
+                              dev);
+}
+
+cudaError_t launch_decode_gemm_held(const void* x, const void* W0, float* partial, int T,
+                                    int d_in, int d_out, uint64_t wait_ns, uint32_t* err,
+                                    cudaStream_t st, const DeviceInfo& dev) {
+  return launch_decode_common(x, W0, partial, T, d_in, d_out, 1, wait_ns, 1, err, false, st, dev);
+}
+
+int decode_uniform_split(int T, int d_in, int d_out) { return decode_gemm_split(T, d_in, d_out); }
 
 }  // namespace lora

@@ -1149,8 +1149,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // (32 KB), and the two M = 128 MMAs of a 16-deep step share the W0 operand.
 // An SM then takes in 64 KB of operands per 8.4 MFLOP instead of the 96 KB of
 // a 128 x 256 tile, and that intake, not the tensor pipe, is what bounds the
-// narrower tile's main loop (at the same L2 hit rate, multicasting W0 across
-// a CTA pair cut L2 reads without speeding it up).  The two accumulators fill
+// narrower tile's main loop (at the same L2 hit rate; a CTA pair that shared
+// each W0 box, tried before, cut L2 reads without speeding it up).  The two accumulators fill
 // all 512 TMEM columns, so a tile is drained before the next one starts; eight
 // epilogue warps (two per TMEM lane quarter, one per 128-column half), each
 // with its own 4 KB store box, keep that drain short.
@@ -1933,13 +1933,12 @@ cudaError_t launch_fused_tc(const void* x, const void* W0, const void* B, const 
   const int tiles_t = (T + 127) / 128;
   const int S = pick_split(tiles_n * tiles_t);
   if (S == 1) {
-    // more tiles than SMs: the persistent form, one CTA per SM walking
-    // tiles with two accumulators in tensor memory (two 128-deep stages
-    // beside the y box; v rows come from L2 when a LoRA stage is built).
-    // Token-adjacent tiles run in pairs sharing each W0 box (multicast)
-    // when there are two tile rows to pair.
-    // With at least two waves of 256 x 256 tiles, the wide form (two M = 128
-    // MMAs per step sharing W0); otherwise 128 x 256 tiles.
+    // more tiles than SMs: a persistent form, one CTA per SM walking tiles
+    // (v rows come from L2 when a LoRA stage is built).  With at least two
+    // waves of 256 x 256 tiles, the wide form: two M = 128 MMAs per step
+    // share each W0 stage, and their two accumulators fill tensor memory.
+    // Otherwise 128 x 256 tiles with two accumulators, so the drain of one
+    // tile overlaps the next tile's main loop.
     cudaError_t e = cudaErrorInvalidConfiguration;
     if (fused_wide_tiles(T, d_out, n_slots, dev.num_sms))
       e = launch_wide(x, W0, B, prm, tiles_n, st, dev);

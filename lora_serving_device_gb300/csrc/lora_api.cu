@@ -62,14 +62,28 @@ FusedWs fused_ws_layout(void* ws, int32_t T, int32_t d_in, int32_t d_out, int32_
   o += 4;
   o = round_up(o, 256);
   const size_t o_v = o;
-  w.ksplit = T <= kDecodeTokens                         ? decode_shrink_ksplit(T, d_in)
-              : fused_wide_tiles(T, d_out, n_slots, 152) ? 1
-                                                         : fused_shrink_ksplit(T, d_in, n_slots, 152);
+  // The shrink split, the prefill tile form and the decode split are chosen
+  // for a 152-SM GB300 (kDecodeScheduleCtas), not the current device, so
+  // that the workspace size and every result bit are the same on every
+  // device; any split is correct with every form.
+  constexpr int kSms = kDecodeScheduleCtas;
+  w.ksplit = T <= kDecodeTokens                          ? decode_shrink_ksplit(T, d_in)
+              : fused_wide_tiles(T, d_out, n_slots, kSms) ? 1
+                                                          : fused_shrink_ksplit(T, d_in, n_slots, kSms);
   o += static_cast<size_t>(w.ksplit) * T * r * 4;
   o = round_up(o, 256);
   const size_t o_d = o;
-  w.split = T <= kDecodeTokens ? decode_gemm_split(T, d_in, d_out) : 0;
-  o += static_cast<size_t>(w.split) * T * d_out * 4;
+  // the split-K base product, S x T x d_out floats.  For T <= 256 there is
+  // one token tile, so S does not depend on T: the ragged and 4-bit layers,
+  // which run longer batches in chunks of at most 256 tokens, fit every
+  // chunk in the region laid out for min(T, 256)
+  size_t partial_rows = 0;
+  w.split = 0;
+  if (T <= kDecodeTokens) {
+    w.split = decode_gemm_split(T, d_in, d_out);
+    partial_rows = static_cast<size_t>(w.split) * T;
+  }
+  o += partial_rows * d_out * 4;
   w.bytes = round_up(o, 256);
   w.err = reinterpret_cast<uint32_t*>(base);
   w.perm = reinterpret_cast<int32_t*>(base + o_perm);
@@ -316,6 +330,19 @@ lora_status_t lora_linear_fused(const void* x, const void* W0, const void* A_poo
                                 void* y, int32_t T, int32_t d_in, int32_t d_out, int32_t r,
                                 int32_t n_slots, lora_dtype_t dt, void* ws, size_t ws_bytes,
                                 void* stream) {
+  return linear_fused_impl(x, W0, A_pool, B_pool, slot_ids, scale, y, T, d_in, d_out, r, n_slots,
+                           dt, ws, ws_bytes, stream, false);
+}
+
+}  // extern "C"
+
+namespace lora {
+
+lora_status_t linear_fused_impl(const void* x, const void* W0, const void* A_pool,
+                                const void* B_pool, const int32_t* slot_ids, const float* scale,
+                                void* y, int32_t T, int32_t d_in, int32_t d_out, int32_t r,
+                                int32_t n_slots, lora_dtype_t dt, void* ws, size_t ws_bytes,
+                                void* stream, bool clear_error_word) {
   if (T < 0) return LORA_ERR_INVALID_ARG;
   if (!dtype_ok(dt)) return LORA_ERR_DTYPE;
   if (!tokens_ok(T) || !dim_ok(d_in) || !dim_ok(d_out) || !rank_ok(r) || !slots_ok(n_slots))
@@ -334,6 +361,9 @@ lora_status_t lora_linear_fused(const void* x, const void* W0, const void* A_poo
   if (dt == LORA_DTYPE_BF16 && !tensor_map_available()) return LORA_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
+  // every argument has been checked: only now may the error word be cleared
+  if (clear_error_word && cudaMemsetAsync(w.err, 0, kErrBytes, st) != cudaSuccess)
+    return LORA_ERR_CUDA;
   const bool decode = T <= kDecodeTokens;
   if (decode && dt == LORA_DTYPE_BF16) {
     // decode-sized bf16 batch: the split-K base GEMM, then one kernel that
@@ -342,11 +372,11 @@ lora_status_t lora_linear_fused(const void* x, const void* W0, const void* A_poo
     // term and stores y.  Both are programmatic dependents: the GEMM
     // streams W0 while the previous kernel in the stream finishes and reads
     // x only after it has.
-    e = launch_decode_gemm(x, W0, w.partial, T, d_in, d_out, w.split, w.err, true, st, dev);
+    const int S = decode_gemm_split(T, d_in, d_out);
+    e = launch_decode_gemm(x, W0, w.partial, T, d_in, d_out, 0, w.err, true, st, dev);
     if (e != cudaSuccess) return LORA_ERR_CUDA;
-    return from_cuda(launch_bgmv_adapter_merge(x, A_pool, B_pool, slot_ids, scale, w.partial,
-                                               w.split, y, T, d_in, d_out, r, n_slots, w.err,
-                                               true, st));
+    return from_cuda(launch_bgmv_adapter_merge(x, A_pool, B_pool, slot_ids, scale, w.partial, S,
+                                               y, T, d_in, d_out, r, n_slots, w.err, true, st));
   }
   if (decode) {
     // decode-sized fp32 batch: per-token BGMV shrink, then the CUDA-core layer
@@ -370,6 +400,10 @@ lora_status_t lora_linear_fused(const void* x, const void* W0, const void* A_poo
                          static_cast<float*>(y), T, d_in, d_out, r, n_slots, w.err, st);
   return from_cuda(e);
 }
+
+}  // namespace lora
+
+extern "C" {
 
 lora_status_t lora_base_gemm_expand(const void* x, const void* W0, const void* B_pool,
                                     const int32_t* slot_ids, const float* v_partial,
@@ -498,7 +532,7 @@ lora_status_t lora_linear_fused_ragged(const void* x, const void* W0, const void
     const int S = decode_gemm_split(Tc, d_in, d_out);
     const uint16_t* xc = static_cast<const uint16_t*>(x) + static_cast<size_t>(c0) * d_in;  // bf16
     uint16_t* yc = static_cast<uint16_t*>(y) + static_cast<size_t>(c0) * d_out;
-    cudaError_t e = launch_decode_gemm(xc, W0, w.partial, Tc, d_in, d_out, S, w.err, true, st, dev);
+    cudaError_t e = launch_decode_gemm(xc, W0, w.partial, Tc, d_in, d_out, 0, w.err, true, st, dev);
     if (e != cudaSuccess) return LORA_ERR_CUDA;
     e = launch_bgmv_adapter_ragged_merge(xc, A_flat, B_flat, rp, slot_ids + c0, scale, w.partial,
                                          S, yc, Tc, d_in, d_out, n_slots, w.err, true, st);
@@ -566,12 +600,12 @@ lora_status_t lora_linear_fused_4bit(const void* x, const void* W0q, const void*
   if ((s = check_device(&dev)) != LORA_OK) return s;
   if (!tensor_map_available()) return LORA_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // the decode chain of lora_linear_fused with the 4-bit base GEMM (its
-  // split over 64-row blocks can always take the bf16 GEMM's split), over
-  // chunks of at most 256 tokens
+  // the decode chain of lora_linear_fused with the 4-bit base GEMM (split
+  // evenly over d_in, the same number of ranges for every column tile),
+  // over chunks of at most 256 tokens
   for (int c0 = 0; c0 < T; c0 += kDecodeTokens) {
     const int Tc = T - c0 < kDecodeTokens ? T - c0 : kDecodeTokens;
-    const int S = decode_gemm_split(Tc, d_in, d_out);
+    const int S = decode_uniform_split(Tc, d_in, d_out);
     const uint16_t* xc = static_cast<const uint16_t*>(x) + static_cast<size_t>(c0) * d_in;  // bf16
     uint16_t* yc = static_cast<uint16_t*>(y) + static_cast<size_t>(c0) * d_out;
     cudaError_t e = launch_decode_q4(xc, W0q, absmax, codebook, w.partial, Tc, d_in, d_out, S,
@@ -589,8 +623,8 @@ lora_status_t lora_base_gemm_splitk(const void* x, const void* W0, float* partia
                                     void* ws, size_t ws_bytes, void* stream) {
   if (T < 0) return LORA_ERR_INVALID_ARG;
   if (dt != LORA_DTYPE_BF16) return LORA_ERR_DTYPE;
-  if (!tokens_ok(T) || !dim_ok(d_in) || !dim_ok(d_out) || ksplit < 1 ||
-      ksplit > decode_gemm_max_split(T, d_in))
+  if (!tokens_ok(T) || !dim_ok(d_in) || !dim_ok(d_out) || ksplit < 0 ||
+      ksplit > decode_gemm_max_split(T, d_in) || (ksplit == 0 && T > kDecodeTokens))
     return LORA_ERR_SHAPE;
   if (x == nullptr || W0 == nullptr || partial == nullptr || !aligned16(x) || !aligned16(W0) ||
       !aligned16(partial))
@@ -604,6 +638,26 @@ lora_status_t lora_base_gemm_splitk(const void* x, const void* W0, float* partia
   return from_cuda(launch_decode_gemm(x, W0, partial, T, d_in, d_out, ksplit,
                                       static_cast<uint32_t*>(ws), false,
                                       static_cast<cudaStream_t>(stream), dev));
+}
+
+lora_status_t lora_debug_gemm_wait_timeout(const void* x, const void* W0, float* partial,
+                                           int32_t T, int32_t d_in, int32_t d_out,
+                                           int32_t wait_us, void* ws, size_t ws_bytes,
+                                           void* stream) {
+  if (T < 1 || T > kDecodeTokens || !dim_ok(d_in) || !dim_ok(d_out)) return LORA_ERR_SHAPE;
+  if (wait_us < 1 || wait_us > 2000000) return LORA_ERR_INVALID_ARG;
+  if (x == nullptr || W0 == nullptr || partial == nullptr || !aligned16(x) || !aligned16(W0) ||
+      !aligned16(partial))
+    return LORA_ERR_INVALID_ARG;
+  lora_status_t s = check_ws(ws, ws_bytes, kErrBytes);
+  if (s != LORA_OK) return s;
+  DeviceInfo dev;
+  if ((s = check_device(&dev)) != LORA_OK) return s;
+  if (!tensor_map_available()) return LORA_ERR_CUDA;
+  return from_cuda(launch_decode_gemm_held(x, W0, partial, T, d_in, d_out,
+                                           static_cast<uint64_t>(wait_us) * 1000ull,
+                                           static_cast<uint32_t*>(ws),
+                                           static_cast<cudaStream_t>(stream), dev));
 }
 
 lora_status_t lora_bgmv_adapter_merge(const void* x, const void* A_pool, const void* B_pool,

@@ -14,12 +14,16 @@
 #include <cstdint>
 #include <mutex>
 
+#include "internal.h"
 #include "lora.h"
 
 namespace {
 
-// The scratch lives here, in every GPU's memory, from the moment a process
-// loads the library until it exits.
+// The scratch lives here.  Its device memory is committed when the library's
+// device code is loaded on a GPU: with CUDA's lazy module loading (the
+// default) that is the first lookup of the address below, i.e. the first
+// call on that device; with CUDA_MODULE_LOADING=EAGER it is when the process
+// first uses that GPU.  It is held until the process exits.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[LORA_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
@@ -59,9 +63,9 @@ extern "C" lora_status_t lora_linear_fused_noalloc(const void* x, const void* W0
   void* scratch = nullptr;
   lora_status_t s = scratch_for_current_device(&scratch);
   if (s != LORA_OK) return s;
-  // the error word must start at zero; everything else is overwritten
-  if (T > 0 && cudaMemsetAsync(scratch, 0, 16, static_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return LORA_ERR_CUDA;
-  return lora_linear_fused(x, W0, A_pool, B_pool, slot_ids, scale, y, T, d_in, d_out, r, n_slots,
-                           dt, scratch, LORA_NOALLOC_SCRATCH_BYTES, stream);
+  // the error word must start at zero (everything else is overwritten); it
+  // is cleared only once every argument has been validated, so a refused
+  // call enqueues nothing at all
+  return lora::linear_fused_impl(x, W0, A_pool, B_pool, slot_ids, scale, y, T, d_in, d_out, r,
+                                 n_slots, dt, scratch, LORA_NOALLOC_SCRATCH_BYTES, stream, true);
 }

@@ -31,7 +31,7 @@ EXPORTS = ("lora_workspace_bytes", "lora_build_segments", "lora_bgmv_shrink", "l
            "lora_bgmv_adapter_merge", "lora_base_gemm_splitk", "lora_decode_split",
            "lora_slot_upload", "lora_bgmv_adapter_ragged", "lora_linear_fused_ragged",
            "lora_quantize_base_4bit", "lora_base_gemm_4bit_splitk", "lora_linear_fused_4bit",
-           "lora_get_error", "lora_status_string")
+           "lora_debug_gemm_wait_timeout", "lora_get_error", "lora_status_string")
 
 
 class LoraError(RuntimeError):
@@ -72,6 +72,7 @@ _SIGS = {
     "lora_base_gemm_4bit_splitk": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _Z, _P]),
     "lora_linear_fused_4bit": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P,
                                     _Z, _P]),
+    "lora_debug_gemm_wait_timeout": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _Z, _P]),
     "lora_get_error": (_I, [_P, _P, ctypes.POINTER(ctypes.c_int32)]),
     "lora_status_string": (ctypes.c_char_p, [_I]),
 }
@@ -174,6 +175,11 @@ def lora_base_gemm_splitk(x, W0, partial, T, d_in, d_out, ksplit, dt, ws, ws_byt
 
 def lora_decode_split(T, d_in, d_out):
     return _call("lora_decode_split", T, d_in, d_out)
+
+
+def lora_debug_gemm_wait_timeout(x, W0, partial, T, d_in, d_out, wait_us, ws, ws_bytes, stream):
+    return _call("lora_debug_gemm_wait_timeout", x, W0, partial, T, d_in, d_out, wait_us, ws,
+                 ws_bytes, stream)
 
 
 def lora_slot_upload(A_pool, B_pool, scale, slot, A_host, B_host, s, d_in, d_out, r, r_a, n_slots,
@@ -384,15 +390,17 @@ def slot_upload_t(A_pool, B_pool, scale, slot, A_host, B_host, s, stream=None):
 
 
 def base_gemm_splitk_t(x, W0, ws, ksplit=None, partial=None, stream=None):
-    """fp32 split-K base product partial[s] = x[:, K_s] W0[K_s, :]; ksplit defaults to the
-    one the fused layer uses."""
+    """fp32 split-K base product partial[s] = x[:, K_s] W0[K_s, :].  ksplit
+    None or 0: the split the fused layer uses (T <= 256; lora_decode_split
+    slots); >= 1: that many equal splits of d_in for every column tile."""
     import torch
     T, d_in = x.shape
     d_out = W0.shape[1]
     if ksplit is None:
-        ksplit = lora_decode_split(T, d_in, d_out) or 1
+        ksplit = 0 if 1 <= T <= 256 else 1
+    S = lora_decode_split(T, d_in, d_out) if ksplit == 0 else ksplit
     if partial is None:
-        partial = torch.empty((ksplit, T, d_out), dtype=torch.float32, device=x.device)
+        partial = torch.empty((max(S, 1), T, d_out), dtype=torch.float32, device=x.device)
     check(lora_base_gemm_splitk(_ptr(x), _ptr(W0), _ptr(partial), T, d_in, d_out, ksplit, _dt(x),
                                 _ptr(ws), ws.numel(), _stream(stream)),
           "lora_base_gemm_splitk")

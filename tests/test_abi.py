@@ -95,12 +95,20 @@ def test_validation_paths(L):
     assert L.lora_build_segments(FAKE, -2, 4, FAKE, FAKE, FAKE, FAKE, ws, 16, None) == 1
     st, _ = L.lora_get_error(None, None)
     assert st == 1
-    # decode building blocks: bf16 only, ksplit within the d_in blocks
+    # decode building blocks: bf16 only, ksplit within the 64-row blocks of
+    # d_in; ksplit 0 (the fused layer's split) only for T <= 256
     assert L.lora_base_gemm_splitk(FAKE, FAKE, FAKE, 4, 4096, 4096, 1, L.DTYPE_F32, ws, 16,
                                    None) == 3
-    assert L.lora_base_gemm_splitk(FAKE, FAKE, FAKE, 4, 4096, 4096, 0, 0, ws, 16, None) == 2
-    assert L.lora_base_gemm_splitk(FAKE, FAKE, FAKE, 4, 128, 4096, 2, 0, ws, 16, None) == 2
+    assert L.lora_base_gemm_splitk(FAKE, FAKE, FAKE, 4, 4096, 4096, -1, 0, ws, 16, None) == 2
+    assert L.lora_base_gemm_splitk(FAKE, FAKE, FAKE, 4, 128, 4096, 3, 0, ws, 16, None) == 2
+    assert L.lora_base_gemm_splitk(FAKE, FAKE, FAKE, 257, 128, 4096, 0, 0, ws, 16, None) == 2
     assert L.lora_base_gemm_splitk(FAKE, FAKE, None, 4, 4096, 4096, 2, 0, ws, 16, None) == 1
+    # the wait-timeout diagnostic: shapes and limit checked before anything runs
+    assert L.lora_debug_gemm_wait_timeout(FAKE, FAKE, FAKE, 0, 64, 128, 100, ws, 16, None) == 2
+    assert L.lora_debug_gemm_wait_timeout(FAKE, FAKE, FAKE, 4, 64, 128, 0, ws, 16, None) == 1
+    assert L.lora_debug_gemm_wait_timeout(FAKE, FAKE, FAKE, 4, 64, 128, 2000001, ws, 16,
+                                          None) == 1
+    assert L.lora_debug_gemm_wait_timeout(FAKE, FAKE, None, 4, 64, 128, 100, ws, 16, None) == 1
     assert L.lora_bgmv_adapter(FAKE, FAKE, FAKE, FAKE, None, FAKE, 70000, 64, 64, 16, 4, 0, ws,
                                16, None) == 2
     assert L.lora_bgmv_adapter_merge(FAKE, FAKE, FAKE, FAKE, None, FAKE, 2, FAKE, 4, 64, 64, 16,
@@ -221,7 +229,10 @@ def test_decode_split_is_a_function_of_the_shapes(L):
     assert L.lora_decode_split(64, 4096, 4096) == 4       # 32 column tiles x 4 = 128 CTAs
     assert L.lora_decode_split(256, 4096, 4096) == 4      # one 256-token tile
     assert L.lora_decode_split(100, 4096, 4096) == 4      # one 128-token tile
+    assert L.lora_decode_split(256, 4096, 1024) == 19     # 8 column tiles x 19
+    assert L.lora_decode_split(256, 14336, 4096) == 4
     assert L.lora_decode_split(1, 64, 128) == 1           # one K block
+    assert L.lora_decode_split(1, 16384, 128) == 64       # capped at LORA_MAX_KSPLIT
     assert L.lora_decode_split(0, 4096, 4096) == 0
     assert L.lora_decode_split(257, 4096, 4096) == 0
     assert L.lora_decode_split(64, 60, 4096) == 0

@@ -59,9 +59,28 @@ def test_fused_ksplit_matches_library():
         if T <= 256:                       # decode-sized: split-K fp32 base product
             S = L.lora_decode_split(T, d_in, d_out)
             assert S >= 1
+            # one token tile: the split does not depend on T
+            assert all(L.lora_decode_split(t, d_in, d_out) == S for t in (1, 33, 129, 256))
             body += S * T * d_out * 4
         want = -(-body // 256) * 256
         assert L.lora_workspace_bytes(L.OP_LINEAR_FUSED, T, d_in, d_out, r, n_slots) == want
+
+
+def test_graph_chunk_divides_steps_and_fits_warmup():
+    for K, W in [(20, 5), (20, 3), (100000, 5000), (7, 3), (1, 3), (13, 13), (600, 1000)]:
+        g = bench.graph_chunk(K, W)
+        assert K % g == 0 and 1 <= g <= max(1, min(W, K, bench.GRAPH_STEPS))
+    assert bench.graph_chunk(20, 5) == 5 and bench.graph_chunk(100000, 5000) == 500
+
+
+def test_parse_clocks_window():
+    lines = [
+        "2026/12/02 10:00:00.000, 0, 1965, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "2026/12/02 10:00:01.000, 0, 1500, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Active",
+    ]
+    t0 = bench._smi_time("2026/12/02 10:00:00.000")
+    s = bench.parse_clocks(lines, (t0 - 0.01, t0 + 0.5))
+    assert s["samples"] == 1 and s["sm_mhz"] == 1965 and s["reasons"] == []
 
 
 def test_parse_clocks():

@@ -165,6 +165,12 @@ FUSED_CASES = [
     (16, 2048, 2048, 128, 5),
     (200, 640, 136, 16, 30),
     (256, 256, 512, 64, 70),
+    # 65..256 tokens: the merge grouped by adapter (items of <= 8 tokens of
+    # one id): rank 32, one adapter for every token, ids nearly all distinct
+    (160, 1032, 600, 32, 11),
+    (200, 256, 264, 16, 1),
+    (220, 512, 1024, 8, 1000),
+    (65, 4096, 1032, 64, 3),
     (257, 192, 264, 16, 11),
     (300, 520, 512, 32, 6),
     (517, 136, 776, 64, 13),
@@ -431,7 +437,11 @@ def test_bgmv_adapter_matches_oracle(L, case):
 
 
 SPLITK_CASES = [(1, 64, 128, 1), (5, 200, 136, 2), (40, 1000, 264, 3), (64, 4096, 4096, 4),
-                (64, 4096, 4096, 21), (100, 512, 520, 4), (256, 4096, 4096, 2), (300, 256, 512, 2)]
+                (64, 4096, 4096, 21), (100, 512, 520, 4), (256, 4096, 4096, 2), (300, 256, 512, 2),
+                (64, 4096, 4096, 22), (40, 1000, 264, 6),
+                # split 0: the split the fused layer uses
+                (64, 4096, 4096, 0), (256, 4096, 4096, 0), (100, 4096, 4096, 0),
+                (48, 2056, 2120, 0), (7, 1032, 600, 0), (256, 4096, 1024, 0), (1, 16384, 128, 0)]
 
 
 @pytest.mark.parametrize("case", SPLITK_CASES, ids=[str(c) for c in SPLITK_CASES])
@@ -441,12 +451,13 @@ def test_base_gemm_splitk_matches_oracle(L, case):
     products and sums), so the bar is the fp32 accumulation error of a
     d_in-long dot product.  Every partial is written (no stale values)."""
     torch = torch_mod()
-    T, d_in, d_out, S = case
+    T, d_in, d_out, ks = case
+    S = ks if ks > 0 else L.lora_decode_split(T, d_in, d_out)
     w = W.random_case(710 + T + S, T, d_in, d_out, 8, 2)
     d = DeviceCase(w)
     ws = _ws(L)
     partial = torch.full((S, T, d_out), float("nan"), dtype=torch.float32, device="cuda")
-    L.base_gemm_splitk_t(d.x, d.W0, ws, ksplit=S, partial=partial)
+    L.base_gemm_splitk_t(d.x, d.W0, ws, ksplit=ks, partial=partial)
     torch.cuda.synchronize()
     got = host(partial)
     assert np.all(np.isfinite(got))

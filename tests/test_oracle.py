@@ -388,3 +388,22 @@ def test_adapter_size_figures():
         abs(f["adapter_size_r16"]["budget_gb"] * 1e9 / b16 - 100) < 5
     assert abs(f["adapter_size_hot"]["budget_gb"] * 1e9 / (f["adapter_size_hot"]["approx_mb"] * 1e6)
                - f["adapter_size_hot"]["resident_approx"]) < 1e-9
+
+
+def test_bf16_unit_roundoff_is_two_to_minus_eight():
+    """The per-element parity bound uses 2^-8 as bf16's unit roundoff: one
+    round-to-nearest-even to bf16 (8 significand bits) moves a value by at
+    most 2^-8 / (1 + 2^-8) of its magnitude, reached by the tie just above a
+    power of two.  A sweep of every fp32 significand pattern in one binade,
+    at two scales, never exceeds it, and the tie attains it."""
+    bound = 2.0 ** -8 / (1 + 2.0 ** -8)
+    for scale in (1.0, 2.0 ** -30):
+        # all 2^23 fp32 values in [1, 2), scaled (exact in fp32)
+        bits = np.arange(0x3F800000, 0x40000000, dtype=np.uint32)
+        x = bits.view(np.float32).astype(np.float64) * scale
+        rel = np.abs(O.bf16_round(x.astype(np.float32)) - x) / x
+        assert rel.max() <= bound * (1 + 1e-12)
+        assert rel.max() >= bound * (1 - 1e-6)
+    tie = np.float32(1 + 2.0 ** -8)
+    assert O.bf16_round(np.array([tie]))[0] == 1.0
+    assert abs((1.0 - float(tie)) / float(tie)) == pytest.approx(bound, rel=1e-12)

@@ -6,22 +6,41 @@ outputs: bit-exact.
 
 The five workloads are held to that bar.  The synthetic tile-edge cases
 (small d_in, large adapter terms) have heavier-tailed outputs than any
-workload; for them, and for the adapter-term checks below, the max bar is
-replaced by the bf16 storage bound per element.
+workload; for them, and for the adapter-term checks, the max bar is
+replaced by a per-element bound derived from how the library computes y:
 
-The adapter term alone (a run with W0 = 0) is checked as well, because it is
-~8x smaller than the base term under the decode init and an error in it
-could hide inside y's budget.  That extra check keeps the Frobenius bar and
-replaces the max bar with the bf16 storage bound per element: rounding to
-bf16 moves a value by at most 2^-9 of itself, so |err| <= 2^-8 |ref| plus a
-small absolute slack.  (The adapter term alone is a sum of r products and
-has heavy tails; its largest elements sit ~10 rms out, where bf16 rounding
-by itself reaches 2e-2 rms.)
+    y_gpu = bf16(y_acc),   y_acc = an fp32 accumulation of exact bf16 products
+
+so |y_gpu - y_ref| <= |bf16(y_acc) - y_acc| + |y_acc - y_ref|.
+
+* The first term is one round-to-nearest-even to bf16.  bf16 keeps 8
+  significand bits (7 stored, 1 implicit), so numbers in [2^e, 2^(e+1)) are
+  2^(e-7) apart and rounding moves a value by at most half that, 2^(e-8):
+  at most U_BF16 = 2^-8 of its magnitude (2^-8 / (1 + 2^-8) exactly; the
+  worst case is a tie just above a power of two, e.g. 1 + 2^-8 -> 1).
+  tests/test_oracle.py pins this against the oracle's bf16 rounding.
+* The second term is the fp32 accumulation error plus, in the prefill GEMM,
+  the rounding of v to a bf16 pair (hi + lo, ~2^-17 of the adapter term).
+  For a d_in-long fp32 dot product the usual probabilistic bound is about
+  sqrt(d_in) * 2^-24 * sum_k |x_k w_k|; with the decode init sum_k |x_k w_k|
+  is ~40 rms(y) at d_in = 4096, i.e. ~1.5e-4 rms.  ABS_RMS = 1e-3 rms leaves
+  ~6x room for the worst element.
+
+Bound per element: |err| <= U_BF16 * |ref| + ABS_RMS * rms(ref), with
+|y_acc| ~ |ref| up to the second term.  Every check records its worst
+err / bound ratio (and max|err| / rms against the stated 2e-2), and the
+session prints the largest ones at the end of the run.
 """
 import numpy as np
 
 REL_FRO = 5e-3
 MAX_RMS = 2e-2
+U_BF16 = 2.0 ** -8
+ABS_RMS = 1e-3
+
+# (what, kind, ratio): kind "max_rms" = (max|err| / rms) / MAX_RMS,
+# "element" = worst |err| / per-element bound.  A ratio <= 1 passes.
+RECORD = []
 
 
 def check_close(got, ref, what="y", rel_fro=REL_FRO, max_rms=MAX_RMS):
@@ -36,13 +55,15 @@ def check_close(got, ref, what="y", rel_fro=REL_FRO, max_rms=MAX_RMS):
     rms = np.sqrt(np.mean(ref * ref))
     rel = float(np.linalg.norm(err) / nref) if nref > 0 else float(np.linalg.norm(err))
     mx = float(np.max(np.abs(err)) / rms) if rms > 0 else float(np.max(np.abs(err)))
+    RECORD.append((what, "max_rms", mx / max_rms))
     assert rel <= rel_fro, f"{what}: rel Frobenius error {rel:.3e} > {rel_fro}"
     assert mx <= max_rms, f"{what}: max|err|/rms {mx:.3e} > {max_rms}"
     return {"rel_fro": rel, "max_over_rms": mx}
 
 
-def check_close_bf16_out(got, ref, what="delta", rel_fro=REL_FRO, abs_rms=1e-3):
-    """Frobenius bar plus the per-element bf16 storage bound (see above)."""
+def check_close_bf16_out(got, ref, what="delta", rel_fro=REL_FRO, abs_rms=ABS_RMS):
+    """Frobenius bar plus the per-element bound of a bf16-stored fp32 sum
+    (module docstring)."""
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
     assert got.shape == ref.shape and np.all(np.isfinite(got)), what
@@ -53,6 +74,9 @@ def check_close_bf16_out(got, ref, what="delta", rel_fro=REL_FRO, abs_rms=1e-3):
     rms = np.sqrt(np.mean(ref * ref))
     rel = float(np.linalg.norm(got - ref) / nref) if nref > 0 else float(np.linalg.norm(got - ref))
     assert rel <= rel_fro, f"{what}: rel Frobenius error {rel:.3e} > {rel_fro}"
-    bound = 2.0 ** -8 * np.abs(ref) + abs_rms * rms
+    bound = U_BF16 * np.abs(ref) + abs_rms * rms
     worst = float(np.max(err / bound))
+    RECORD.append((what, "element", worst))
+    if rms > 0:
+        RECORD.append((what, "max_rms", float(np.max(err)) / rms / MAX_RMS))
     assert worst <= 1.0, f"{what}: element error {worst:.2f}x the bf16 storage bound"
