@@ -311,14 +311,22 @@ struct ExpandLayout {
   // per epilogue warp: 32 rows x 64 accumulator columns (+4 floats of padding
   // per row, so the 32 rows' float4 writes hit distinct banks)
   static constexpr int kStLd = 64 + 4;
-  static constexpr uint32_t kStage = kBars + 8 * 8 + 16;
+  // b_full[2], b_empty[2], t_full[2], t_empty[2], y_full[2], TMEM slot, abort
+  static constexpr uint32_t kStage = kBars + 10 * 8 + 16;
   static constexpr uint32_t kStageWarp = 32 * kStLd * 4;
-  static constexpr uint32_t kTotal = kStage + 4 * kStageWarp;
+  // the staging area, or (full items whose rows are consecutive in y) two
+  // 16 KiB y half-tiles (128 rows x 64 columns, 128-byte swizzle) for TMA
+  static constexpr uint32_t kStageAll = 4 * kStageWarp;
+  static constexpr uint32_t kYHalf = kTok * 128;
+  static constexpr uint32_t kUnion = kStageAll > 2 * kYHalf ? kStageAll : 2 * kYHalf;
+  static constexpr uint32_t kStageOff = (kStage + 1023) / 1024 * 1024;
+  static constexpr uint32_t kTotal = kStageOff + kUnion;
 };
 
 template <int R>
 __global__ void __launch_bounds__(kThreads)
-    sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap tm_b, const float* vpart, int ksplit,
+    sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
+                          const __grid_constant__ CUtensorMap tm_y, const float* vpart, int ksplit,
                           const int32_t* perm, const int32_t* seg_slot, const int32_t* seg_off,
                           const int32_t* n_seg, bf16* y, int T, int d_out, uint32_t* err) {
   using Lay = ExpandLayout<R>;
@@ -332,8 +340,10 @@ __global__ void __launch_bounds__(kThreads)
   uint64_t* b_empty = b_full + 2;
   uint64_t* t_full = b_full + 4;
   uint64_t* t_empty = b_full + 6;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(b_full + 8);
-  volatile int* abort_f = reinterpret_cast<volatile int*>(b_full + 8) + 1;
+  uint64_t* y_full = b_full + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(b_full + 10);
+  volatile int* abort_f = reinterpret_cast<volatile int*>(b_full + 10) + 1;
+  uint8_t* uni = smem + Lay::kStageOff;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   sgmv_item<kTok>(blockIdx.x, seg_slot, seg_off, ld_dep(n_seg), &s_a, &s_p0, &s_p1);
@@ -344,6 +354,15 @@ __global__ void __launch_bounds__(kThreads)
   const int j0 = blockIdx.y * kXGroup;
   const int nt = min(kXGroup, n_tiles_all - j0);
   if (nt <= 0) return;
+  // a full item whose tokens are consecutive rows of y (a prefill request):
+  // y moves by TMA, 64-column half-tiles, two buffers
+  const int row0 = ld_dep(perm + p0);
+  const bool ytma = n_tok == kTok && ld_dep(perm + p0 + kTok - 1) - row0 == kTok - 1;
+  auto issue_y = [&](int hj) {  // half-tile hj = 2 j + h into buffer hj & 1
+    ptx::mbar_arrive_expect_tx(&y_full[hj & 1], Lay::kYHalf);
+    ptx::tma_load_2d(uni + (hj & 1) * Lay::kYHalf, &tm_y, &y_full[hj & 1],
+                     (j0 + (hj >> 1)) * kXN + 64 * (hj & 1), row0);
+  };
 
   auto issue_b = [&](int j) {  // B[a][:, tile j] into buffer j & 1
     const int bs = j & 1;
@@ -361,11 +380,17 @@ __global__ void __launch_bounds__(kThreads)
         ptx::mbar_init(&b_empty[i], 1);
         ptx::mbar_init(&t_full[i], 1);
         ptx::mbar_init(&t_empty[i], 4 * 32);
+        ptx::mbar_init(&y_full[i], 1);
       }
       *abort_f = 0;
       ptx::fence_mbar_init();
       issue_b(0);
       if (nt > 1) issue_b(1);
+      if (ytma) {
+        ptx::prefetch_tmap(&tm_y);
+        issue_y(0);
+        issue_y(1);
+      }
     }
     __syncwarp();
     ptx::tmem_alloc(tmem_slot, 2 * kXN);
@@ -438,6 +463,66 @@ __global__ void __launch_bounds__(kThreads)
       }
     }
     __syncwarp();
+  } else if (ytma) {
+    // ---------------- epilogue, y by TMA: y half-tile += accumulator ------
+    // TMEM lane = token row i of the tile = row row0 + i of y.  Half-tile hj
+    // (64 columns) sits in buffer hj & 1 as 128 rows of 128 bytes with the
+    // 128-byte swizzle: thread i adds its accumulator row in place (the 32
+    // rows of a warp spread over all banks), then one thread stores the
+    // half-tile with TMA, waits until the store has read it and loads half-
+    // tile hj + 2 into the same buffer.  The other buffer's load is in
+    // flight meanwhile.  Every epilogue thread passes the same named
+    // barriers, aborted or not.
+    const int i = warp * 32 + lane;
+    const uint32_t tq = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    bool ok = true;
+    for (int j = 0; j < nt; ++j) {
+      const int bs = j & 1;
+      const uint32_t ph = static_cast<uint32_t>(j >> 1) & 1u;
+      ok = ok && warp_wait(&t_full[bs], ph, abort_f);
+      if (ok) ptx::tc_fence_after();
+#pragma unroll 1
+      for (int h = 0; h < kXN / 64; ++h) {
+        const int hj = 2 * j + h;
+        ok = ok && warp_wait(&y_full[hj & 1], static_cast<uint32_t>(hj >> 1) & 1u, abort_f);
+        uint8_t* yb = uni + (hj & 1) * Lay::kYHalf + i * 128;
+        if (ok) {
+#pragma unroll
+          for (int c0 = 0; c0 < 64; c0 += 32) {
+            uint32_t v[32];
+            ptx::tmem_ld16(tq + bs * kXN + h * 64 + c0, *reinterpret_cast<uint32_t(*)[16]>(v));
+            ptx::tmem_ld16(tq + bs * kXN + h * 64 + c0 + 16,
+                           *reinterpret_cast<uint32_t(*)[16]>(v + 16));
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int ch = (c0 >> 3) + q;  // 16-byte chunk of the 128-byte row
+              uint4* p = reinterpret_cast<uint4*>(yb + ((ch ^ (i & 7)) << 4));
+              const uint4 w = *p;
+              const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+              float f[8];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                f[2 * e] = bf16_lo(u[e]) + __uint_as_float(v[8 * q + 2 * e]);
+                f[2 * e + 1] = bf16_hi(u[e]) + __uint_as_float(v[8 * q + 2 * e + 1]);
+              }
+              *p = pack8_bf16(f);
+            }
+          }
+          ptx::fence_proxy_async_smem();
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (i == 0 && ok && !*abort_f) {
+          ptx::tma_store_2d(&tm_y, uni + (hj & 1) * Lay::kYHalf,
+                            (j0 + j) * kXN + 64 * h, row0);
+          ptx::bulk_commit_group();
+          ptx::bulk_wait_group_read_all();  // the buffer is read: reload it
+          if (hj + 2 < 2 * nt) issue_y(hj + 2);
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&t_empty[bs]);
+    }
   } else {
     // ---------------- epilogue: y rows += accumulator rows ----------------
     // TMEM lane = token row of the tile.  Each warp stages its 32 rows x 64
@@ -447,7 +532,7 @@ __global__ void __launch_bounds__(kThreads)
     const int n_rows = min(32, n_tok - warp * 32);  // this warp's token rows
     bf16* yrow = n_rows > lane ? y + static_cast<size_t>(ld_dep(perm + p0 + warp * 32 + lane)) * d_out
                                : nullptr;
-    float* stg = reinterpret_cast<float*>(smem + Lay::kStage + warp * Lay::kStageWarp);
+    float* stg = reinterpret_cast<float*>(uni + warp * Lay::kStageWarp);
     const uint32_t tq = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     for (int j = 0; j < nt; ++j) {
       const int bs = j & 1;
@@ -503,7 +588,8 @@ __global__ void __launch_bounds__(kThreads)
 }
 
 template <int R>
-cudaError_t launch_expand_r(const CUtensorMap& tm, const float* vpart, int ksplit,
+cudaError_t launch_expand_r(const CUtensorMap& tm, const CUtensorMap& tm_y, const float* vpart,
+                            int ksplit,
                             const int32_t* perm, const int32_t* seg_slot, const int32_t* seg_off,
                             const int32_t* n_seg, bf16* y, int T, int d_out, int n_slots,
                             uint32_t* err, cudaStream_t st, const DeviceInfo& dev) {
@@ -525,8 +611,8 @@ cudaError_t launch_expand_r(const CUtensorMap& tm, const float* vpart, int kspli
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cfg.numAttrs = 0;
-  return cudaLaunchKernelEx(&cfg, kern, tm, vpart, ksplit, perm, seg_slot, seg_off, n_seg, y, T,
-                            d_out, err);
+  return cudaLaunchKernelEx(&cfg, kern, tm, tm_y, vpart, ksplit, perm, seg_slot, seg_off, n_seg,
+                            y, T, d_out, err);
 }
 
 }  // namespace
@@ -540,16 +626,19 @@ cudaError_t launch_sgmv_expand_tc(const float* vpart, int ksplit, const void* B,
                                   int r, int d_out, int n_slots, uint32_t* err, cudaStream_t st,
                                   const DeviceInfo& dev) {
   if (T <= 0) return cudaSuccess;
-  CUtensorMap tm;
-  // B_pool as [n_slots][r][d_out]: 64 columns x r rows per box
-  if (!encode_tensor_map_bf16_3d(&tm, B, d_out, r, n_slots, 64, r)) return cudaErrorInvalidValue;
+  CUtensorMap tm, tm_y;
+  // B_pool as [n_slots][r][d_out]: 64 columns x r rows per box; y [T][d_out]:
+  // 64 columns x 128 rows per box, 128-byte swizzle
+  if (!encode_tensor_map_bf16_3d(&tm, B, d_out, r, n_slots, 64, r) ||
+      !encode_tensor_map_bf16(&tm_y, y, d_out, T, d_out, 64, kTok))
+    return cudaErrorInvalidValue;
   bf16* ye = static_cast<bf16*>(y);
   if (r == 64)
-    return launch_expand_r<64>(tm, vpart, ksplit, perm, seg_slot, seg_off, n_seg, ye, T, d_out,
-                               n_slots, err, st, dev);
+    return launch_expand_r<64>(tm, tm_y, vpart, ksplit, perm, seg_slot, seg_off, n_seg, ye, T,
+                               d_out, n_slots, err, st, dev);
   if (r == 128)
-    return launch_expand_r<128>(tm, vpart, ksplit, perm, seg_slot, seg_off, n_seg, ye, T, d_out,
-                                n_slots, err, st, dev);
+    return launch_expand_r<128>(tm, tm_y, vpart, ksplit, perm, seg_slot, seg_off, n_seg, ye, T,
+                                d_out, n_slots, err, st, dev);
   return cudaErrorInvalidValue;
 }
 

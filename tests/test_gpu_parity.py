@@ -82,6 +82,10 @@ GATHER_CASES = [
     # several 128-token SGMV items per segment, ragged d_in tail
     (700, 4096, 72, 64, 9, "bf16"),
     (300, 1000, 64, 128, 5, "bf16"),
+    # many full 128-token items whose rows are consecutive (y moved by TMA in
+    # the SGMV expand), a ragged last column tile
+    (640, 256, 1032, 64, 4, "bf16"),
+    (384, 512, 264, 128, 3, "bf16"),
     (53, 256, 256, 16, 8, "f32"),
     (90, 96, 72, 64, 4, "f32"),
 ]
