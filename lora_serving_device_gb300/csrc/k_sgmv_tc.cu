@@ -44,12 +44,15 @@ constexpr int kThreads = 160;  // warps 0-3: gather + epilogue, warp 4: MMA
 constexpr int kTok = 128;      // tokens per work item (the MMA's M)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
-template <int R>
+// ST ring stages: ST = 4 at rank 64 (~96 KiB, two CTAs per SM) or 3 (~72 KiB,
+// three CTAs per SM, so more CTAs' start-up and drain overlap).  Grids of
+// more than one wave at two CTAs per SM take the shallower ring.
+template <int R, int ST>
 struct ShrinkLayout {
   static constexpr uint32_t kX = kTok * 128;            // one 64-wide K block of x
   static constexpr uint32_t kA = (R / 64) * 8192;       // R columns x 64 K rows of A[a]
   static constexpr uint32_t kStage = kX + kA;
-  static constexpr int kStages = R == 64 ? 4 : 3;       // ~96 KiB: two CTAs per SM
+  static constexpr int kStages = ST;
   static constexpr int kLag = kStages - 1;              // cp.async groups in flight
   static constexpr uint32_t kBars = kStages * kStage;
   static constexpr uint32_t kTotal = kBars + (2 * kStages + 1) * 8 + 16;
@@ -74,14 +77,14 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
-template <int R>
-__global__ void __launch_bounds__(kThreads, 2)
+template <int R, int ST>
+__global__ void __launch_bounds__(kThreads, ST == 3 && R == 64 ? 3 : 2)
     sgmv_shrink_tc_kernel(const __grid_constant__ CUtensorMap tm_a,
                           const __grid_constant__ CUtensorMap tm_x, const bf16* x,
                           const int32_t* perm, const int32_t* seg_slot, const int32_t* seg_off,
                           const int32_t* n_seg, const float* scale, float* vpart, int T,
                           int d_in, int kchunk, uint32_t* err) {
-  using Lay = ShrinkLayout<R>;
+  using Lay = ShrinkLayout<R, ST>;
   constexpr int S = Lay::kStages;
   constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(128, R, false, true);
   __shared__ int s_a, s_p0, s_p1;
@@ -265,16 +268,16 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (tid == 0 && *abort_f) flag_error(err, LORA_DEVERR_TIMEOUT);
 }
 
-template <int R>
+template <int R, int ST>
 cudaError_t launch_r(const CUtensorMap& tm, const CUtensorMap& tm_x, const bf16* x,
                      const int32_t* perm,
                      const int32_t* seg_slot, const int32_t* seg_off, const int32_t* n_seg,
                      const float* scale, float* vpart, int T, int d_in, int n_slots, int ksplit,
                      uint32_t* err, cudaStream_t st, bool pdl, const DeviceInfo& dev) {
-  using Lay = ShrinkLayout<R>;
+  using Lay = ShrinkLayout<R, ST>;
   const size_t smem = Lay::kTotal + 1024;
   if (smem > dev.max_smem_optin) return cudaErrorInvalidConfiguration;
-  auto kern = sgmv_shrink_tc_kernel<R>;
+  auto kern = sgmv_shrink_tc_kernel<R, ST>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
@@ -655,12 +658,21 @@ cudaError_t launch_sgmv_shrink_tc(const void* x, const void* A, const int32_t* p
       !encode_tensor_map_bf16(&tm_x, x, d_in, T, d_in, 64, kTok))
     return cudaErrorInvalidValue;
   const bf16* xe = static_cast<const bf16*>(x);
+  // more than one wave at two CTAs per SM: the shallower ring, three per SM
+  // (prefill workload: 33.3 -> 29.2 us at split 4, 35.7 -> 32.1 us at split
+  // 8; at split 2, one wave, the deeper ring stays ahead: 38.0 against 38.7)
+  const int cap = T < n_slots ? T : n_slots;
+  const long long ctas = static_cast<long long>((T + kTok - 1) / kTok + cap) * ksplit;
+  const bool wide = ctas > 2ll * dev.num_sms;
+  if (r == 64 && wide)
+    return launch_r<64, 3>(tm, tm_x, xe, perm, seg_slot, seg_off, n_seg, scale, vpart, T, d_in,
+                           n_slots, ksplit, err, st, pdl, dev);
   if (r == 64)
-    return launch_r<64>(tm, tm_x, xe, perm, seg_slot, seg_off, n_seg, scale, vpart, T, d_in,
-                        n_slots, ksplit, err, st, pdl, dev);
+    return launch_r<64, 4>(tm, tm_x, xe, perm, seg_slot, seg_off, n_seg, scale, vpart, T, d_in,
+                           n_slots, ksplit, err, st, pdl, dev);
   if (r == 128)
-    return launch_r<128>(tm, tm_x, xe, perm, seg_slot, seg_off, n_seg, scale, vpart, T, d_in,
-                         n_slots, ksplit, err, st, pdl, dev);
+    return launch_r<128, 3>(tm, tm_x, xe, perm, seg_slot, seg_off, n_seg, scale, vpart, T, d_in,
+                            n_slots, ksplit, err, st, pdl, dev);
   return cudaErrorInvalidValue;
 }
 
