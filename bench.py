@@ -970,7 +970,7 @@ def run_ours(args):
         traffic = dram_traffic_per_launch()
         roof = {"bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": ach / pk["hbm_gbs"], "traffic": traffic,
-                "kernel": "decode_gemm_kernel (tcgen05 swap-AB base GEMM; tile x 64-row work dealt over 152 CTAs)",
+                "kernel": "decode_gemm_kernel (tcgen05 swap-AB base GEMM, split over d_in)",
                 "algorithmic_bytes_per_launch": gb, "launch_us": kt["gemm_ms"] * 1e3,
                 "peak_source": pk["source"], "frac_vs_8tbs": ach / 8000.0}
     lb = layer_bytes(T, d_in, d_out, r, D)
