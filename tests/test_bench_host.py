@@ -135,3 +135,20 @@ def test_reference_arm_only_rank0_works(monkeypatch, capsys):
     monkeypatch.setenv("WORLD_SIZE", "2")
     assert bench.run_reference(bench.parse_args(["--impl", "reference", "--steps", "1"])) == 0
     assert capsys.readouterr().out == ""
+
+
+def test_gpus_n_relaunches_under_torch_distributed(monkeypatch):
+    """--gpus N > 1 without a launcher re-runs the script with N ranks on this
+    node (rendezvous on 127.0.0.1); with a launcher, a different world size is
+    refused."""
+    calls = []
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    monkeypatch.setattr(bench.subprocess, "call", lambda cmd: calls.append(cmd) or 0)
+    assert bench.main(["--gpus", "2", "--steps", "3", "--warmup", "3"]) == 0
+    cmd = calls[0]
+    assert cmd[1:3] == ["-m", "torch.distributed.run"]
+    assert "--nproc-per-node=2" in cmd and cmd[cmd.index("--master-addr") + 1] == "127.0.0.1"
+    assert cmd[-6:] == ["--gpus", "2", "--steps", "3", "--warmup", "3"]
+    monkeypatch.setenv("WORLD_SIZE", "1")
+    with pytest.raises(SystemExit):
+        bench.main(["--gpus", "2", "--steps", "3", "--warmup", "3"])
