@@ -799,6 +799,21 @@ def prefill_point(L, stream, pk, dev, steps=30, warm=5):
         "sgmv_expand": block_row(graph_mean_ms(
             lambda i: L.sgmv_expand_t(vpart_x, B, segs, y, wss, stream=stream), 30, stream),
             b_expand, pk)}
+    # the same layer over a 4-bit base: W0 dequantised once per call into the
+    # workspace, then the bf16 prefill path
+    cb = _up(W.nf4_like_codebook(), dev)
+    base4 = L.Base4bit.quantize(W0, cb, stream=stream)
+    ws4 = L.workspace(L.OP_LINEAR_FUSED_4BIT, T, d_in, d_out, r, n_slots)
+    ms4, _ = timed_graph_steps(
+        lambda i: L.linear_fused_4bit_t(x, base4, A, B, ids, scale, ws4, y=y, stream=stream),
+        steps, warm, stream)
+    t4 = ms4 / 1e3 / steps
+    prefill_4bit = {"workload": "prefill_sgmv with W0 as 4-bit codes + bf16 absmax per 64-row "
+                                "block, dequantised once per call into the workspace",
+                    "ms_per_step": t4 * 1e3, "tokens_per_s": T / t4,
+                    "tflops": flops / t4 / 1e12, "frac_burst_bf16": flops / t4 / 1e12 / pk["bf16_tflops"],
+                    "device_error": L.get_error_t(ws4, stream=stream)}
+    del base4, ws4
     res = {"workload": "prefill_sgmv: 4096->14336, rank 64, 64 slots, 16 prefill requests "
                        "(U[64,1024] tokens) + 48 decode tokens",
            "T": T, "distinct": D, "ms_per_step": t * 1e3, "tokens_per_s": T / t,
@@ -808,7 +823,7 @@ def prefill_point(L, stream, pk, dev, steps=30, warm=5):
                         "unit": "TFLOP/s", "frac": tf / pk["bf16_tflops"],
                         "peak_kind": "burst (cuBLAS bf16, measured)",
                         "frac_vs_sustained": tf / pk["bf16_tflops_sustained"]},
-           "blocks": blocks}
+           "blocks": blocks, "prefill_4bit": prefill_4bit}
     del x, W0, A, B
     torch.cuda.empty_cache()
     return res
@@ -823,7 +838,7 @@ def q4_point(L, sets, w, stream, pk, steps=4000, warm=400):
     cb = _up(W.nf4_like_codebook(), sets[0].x.device)
     bases = [L.Base4bit.quantize(s.W0, cb, stream=stream) for s in sets]
     stream.synchronize()
-    ws = L.workspace(L.OP_LINEAR_FUSED, T, d_in, d_out, r, n_slots, device=sets[0].x.device)
+    ws = L.workspace(L.OP_LINEAR_FUSED_4BIT, T, d_in, d_out, r, n_slots, device=sets[0].x.device)
     n = len(sets)
 
     def step(i):

@@ -83,7 +83,8 @@ typedef enum {
   LORA_OP_SGMV_SHRINK = 3,
   LORA_OP_SGMV_EXPAND = 4,
   LORA_OP_LINEAR_FUSED = 5,
-  LORA_OP_BASE_GEMM_EXPAND = 6
+  LORA_OP_BASE_GEMM_EXPAND = 6,
+  LORA_OP_LINEAR_FUSED_4BIT = 7
 } lora_op_t;
 
 /* device error word bits */
@@ -426,12 +427,17 @@ lora_status_t lora_linear_fused_ragged(const void* x, const void* W0, const void
  * Workspace: the error word.
  *
  * lora_linear_fused_4bit: the whole layer, y = x deq(W0) + s (x A) B, for
- * bf16 batches: the 4-bit split-K GEMM, then the merge kernel of
- * lora_linear_fused's decode path (bf16 adapters), over consecutive chunks of
- * at most 256 tokens.  Same pools, ids, scale and programmatic-overlap rules
- * as lora_linear_fused (W0q, absmax and the codebook play the part of W0
- * there); workspace: lora_workspace_bytes(LORA_OP_LINEAR_FUSED, min(T, 256),
- * d_in, d_out, r, n_slots).
+ * bf16 batches.  Up to 256 tokens: the 4-bit split-K GEMM, then the merge
+ * kernel of lora_linear_fused's decode path (bf16 adapters).  Larger
+ * batches: W0 dequantised once into the workspace (the same bf16 values the
+ * 4-bit GEMM feeds its MMAs), then lora_linear_fused's prefill path over it
+ * (segments, SGMV shrink, the GEMM with the expand in its accumulator), so
+ * the base is streamed once per call.  Same pools, ids, scale and
+ * programmatic-overlap rules as lora_linear_fused (W0q, absmax and the
+ * codebook play the part of W0 there); workspace:
+ * lora_workspace_bytes(LORA_OP_LINEAR_FUSED_4BIT, T, d_in, d_out, r,
+ * n_slots), which for T > 256 includes d_in x d_out x 2 bytes for the
+ * dequantised W0.
  */
 lora_status_t lora_quantize_base_4bit(const void* W0, const void* codebook, void* W0q,
                                       void* absmax, int32_t d_in, int32_t d_out, void* stream);

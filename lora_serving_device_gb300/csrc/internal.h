@@ -161,6 +161,10 @@ cudaError_t launch_decode_q4(const void* x, const void* Wq, const void* absmax,
                              const void* codebook, float* partial, int T, int d_in, int d_out,
                              int S, uint32_t* err, bool pdl, cudaStream_t st,
                              const DeviceInfo& dev);
+// 4-bit codes and absmax -> bf16 W [d_in, d_out], each weight rounded once
+// (see k_decode_q4.cu); d_in % 64 == 0, d_out % 32 == 0.
+cudaError_t launch_dequantize_q4(const void* Wq, const void* absmax, const void* codebook,
+                                 void* W, int d_in, int d_out, cudaStream_t st);
 // bf16 W0 [d_in, d_out] -> 4-bit codes and bf16 absmax (see k_decode_q4.cu).
 cudaError_t launch_quantize_q4(const void* W0, const void* codebook, void* Wq, void* absmax,
                                int d_in, int d_out, cudaStream_t st);

@@ -496,6 +496,69 @@ cudaError_t launch_decode_q4(const void* x, const void* Wq, const void* absmax,
   return launch_q4_variant<256>(tm_x, tm_q, tm_s, tm_p, prm, tiles_n, tiles_t, S, pdl, st, dev);
 }
 
+// ---------------------------------------------------------------- dequantiser
+// The inverse for batches above 256 tokens, which take the bf16 prefill path
+// over a dequantised copy of W0: W [d_in, d_out] bf16, W[k, n] =
+// bf16(codebook[code[n, k]] * absmax[k / 64, n]), the product of two bf16
+// values exact in fp32 and rounded once (the same values the 4-bit decode
+// GEMM feeds its MMAs).  One 64-row x 64-column block per CTA: each of 128
+// threads reads 32 codes of one column with one 16-byte load, the block is
+// transposed through shared memory and written as 64 rows of 128 bytes.
+__global__ void __launch_bounds__(256)
+    dequantize_q4_kernel(const uint8_t* __restrict__ Wq, const uint16_t* __restrict__ absmax,
+                         const uint16_t* __restrict__ cb, uint16_t* __restrict__ W, int d_in,
+                         int d_out) {
+  __shared__ __align__(16) uint16_t tile[64][64 + 8];  // [k][n], rows 144 bytes apart
+  __shared__ float cbf[16];
+  const int n0 = blockIdx.x * 64, k0 = blockIdx.y * 64;
+  if (threadIdx.x < 16) cbf[threadIdx.x] = __uint_as_float(static_cast<uint32_t>(cb[threadIdx.x]) << 16);
+  __syncthreads();
+  if (threadIdx.x < 128) {
+    const int c = threadIdx.x >> 1, hh = threadIdx.x & 1;
+    const int n = n0 + c;
+    if (n < d_out) {
+      const uint4 q = *reinterpret_cast<const uint4*>(Wq + static_cast<size_t>(n) * (d_in / 2) +
+                                                      k0 / 2 + 16 * hh);
+      const float sf =
+          __uint_as_float(static_cast<uint32_t>(absmax[static_cast<size_t>(k0 / 64) * d_out + n]) << 16);
+      const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+#pragma unroll
+        for (int bb = 0; bb < 4; ++bb) {
+          const uint32_t byte = (w4[e] >> (8 * bb)) & 0xffu;
+          const int k = 32 * hh + 2 * (4 * e + bb);  // low nibble: row k, high: row k + 1
+          const __nv_bfloat16 lo = __float2bfloat16_rn(cbf[byte & 15u] * sf);
+          const __nv_bfloat16 hi = __float2bfloat16_rn(cbf[byte >> 4] * sf);
+          tile[k][c] = *reinterpret_cast<const uint16_t*>(&lo);
+          tile[k + 1][c] = *reinterpret_cast<const uint16_t*>(&hi);
+        }
+      }
+    }
+  }
+  __syncthreads();
+  // 64 rows x 64 columns out: thread j writes 16 columns of row j / 4
+  const int row = threadIdx.x >> 2, qq = threadIdx.x & 3;
+  const int k = k0 + row, n = n0 + 16 * qq;
+  if (k < d_in && n < d_out) {
+    const uint4* src = reinterpret_cast<const uint4*>(&tile[row][16 * qq]);
+    uint4* dst = reinterpret_cast<uint4*>(W + static_cast<size_t>(k) * d_out + n);
+    dst[0] = src[0];
+    dst[1] = src[1];
+  }
+}
+
+cudaError_t launch_dequantize_q4(const void* Wq, const void* absmax, const void* codebook,
+                                 void* W, int d_in, int d_out, cudaStream_t st) {
+  if (d_in % 64 != 0 || d_out % 32 != 0) return cudaErrorInvalidValue;
+  const dim3 grid((d_out + 63) / 64, d_in / 64);
+  dequantize_q4_kernel<<<grid, 256, 0, st>>>(static_cast<const uint8_t*>(Wq),
+                                             static_cast<const uint16_t*>(absmax),
+                                             static_cast<const uint16_t*>(codebook),
+                                             static_cast<uint16_t*>(W), d_in, d_out);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_quantize_q4(const void* W0, const void* codebook, void* Wq, void* absmax,
                                int d_in, int d_out, cudaStream_t st) {
   if (d_in % 64 != 0 || d_out % 32 != 0) return cudaErrorInvalidValue;

@@ -95,6 +95,21 @@ FusedWs fused_ws_layout(void* ws, int32_t T, int32_t d_in, int32_t d_out, int32_
   return w;
 }
 
+// Workspace of lora_linear_fused_4bit: T <= 256, the decode chain's layout;
+// larger batches, the prefill layout followed by a bf16 copy of W0 [d_in,
+// d_out] (the dequantised base the prefill GEMM reads).  `wd` gets that copy.
+size_t q4_ws_bytes(void* ws, int32_t T, int32_t d_in, int32_t d_out, int32_t r, int32_t n_slots,
+                   FusedWs* w, void** wd) {
+  *w = fused_ws_layout(ws, T, d_in, d_out, r, n_slots);
+  if (T <= kDecodeTokens) {
+    *wd = nullptr;
+    return w->bytes;
+  }
+  const size_t o = round_up(w->bytes, 256);
+  *wd = static_cast<uint8_t*>(ws) + o;
+  return o + static_cast<size_t>(d_in) * d_out * 2;
+}
+
 lora_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? LORA_OK : LORA_ERR_CUDA; }
 
 // The library is built for sm_103a only.
@@ -198,6 +213,12 @@ size_t lora_workspace_bytes(int32_t op, int32_t T, int32_t d_in, int32_t d_out, 
   if (op == LORA_OP_LINEAR_FUSED) {
     if (T < 0 || !rank_ok(r) || !slots_ok(n_slots) || d_in < 8 || d_out < 0) return kErrBytes;
     return fused_ws_layout(nullptr, T, d_in, d_out, r, n_slots).bytes;
+  }
+  if (op == LORA_OP_LINEAR_FUSED_4BIT) {
+    if (T < 0 || !rank_ok(r) || !slots_ok(n_slots) || d_in < 8 || d_out < 0) return kErrBytes;
+    FusedWs w;
+    void* wd;
+    return q4_ws_bytes(nullptr, T, d_in, d_out, r, n_slots, &w, &wd);
   }
   return kErrBytes;
 }
@@ -338,6 +359,19 @@ lora_status_t lora_linear_fused(const void* x, const void* W0, const void* A_poo
 
 namespace lora {
 
+// Segments, then the segment-grouped shrink (SGMV) into w.vpart: the first
+// two kernels of the prefill path (the GEMM follows as their dependent).
+cudaError_t prefill_adapter_shrink(const void* x, const void* A_pool, const int32_t* slot_ids,
+                                   const float* scale, int32_t T, int32_t d_in, int32_t r,
+                                   int32_t n_slots, lora_dtype_t dt, const FusedWs& w,
+                                   cudaStream_t st, const DeviceInfo& dev) {
+  cudaError_t e = launch_build_segments(slot_ids, T, n_slots, w.perm, w.seg_slot, w.seg_off,
+                                        w.n_seg, w.err, st);
+  if (e != cudaSuccess) return e;
+  return sgmv_shrink_any(x, A_pool, w.perm, w.seg_slot, w.seg_off, w.n_seg, scale, w.vpart, T,
+                         d_in, r, n_slots, w.ksplit, dt, w.err, st, true, dev);
+}
+
 lora_status_t linear_fused_impl(const void* x, const void* W0, const void* A_pool,
                                 const void* B_pool, const int32_t* slot_ids, const float* scale,
                                 void* y, int32_t T, int32_t d_in, int32_t d_out, int32_t r,
@@ -384,11 +418,7 @@ lora_status_t linear_fused_impl(const void* x, const void* W0, const void* A_poo
                            dt, w.err, st);
   } else {
     // prefill-sized batch: segments, then the segment-grouped shrink (SGMV)
-    e = launch_build_segments(slot_ids, T, n_slots, w.perm, w.seg_slot, w.seg_off, w.n_seg,
-                              w.err, st);
-    if (e != cudaSuccess) return LORA_ERR_CUDA;
-    e = sgmv_shrink_any(x, A_pool, w.perm, w.seg_slot, w.seg_off, w.n_seg, scale, w.vpart, T,
-                        d_in, r, n_slots, w.ksplit, dt, w.err, st, true, dev);
+    e = prefill_adapter_shrink(x, A_pool, slot_ids, scale, T, d_in, r, n_slots, dt, w, st, dev);
   }
   if (e != cudaSuccess) return LORA_ERR_CUDA;
   if (dt == LORA_DTYPE_BF16)
@@ -591,31 +621,36 @@ lora_status_t lora_linear_fused_4bit(const void* x, const void* W0q, const void*
       !aligned16(x) || !aligned16(W0q) || !aligned16(absmax) || !aligned16(A_pool) ||
       !aligned16(B_pool) || !aligned16(y) || x == y)
     return LORA_ERR_INVALID_ARG;
-  const FusedWs w =
-      fused_ws_layout(ws, T < kDecodeTokens ? T : kDecodeTokens, d_in, d_out, r, n_slots);
-  lora_status_t s = check_ws(ws, ws_bytes, w.bytes);
+  FusedWs w;
+  void* wd = nullptr;
+  lora_status_t s = check_ws(ws, ws_bytes, q4_ws_bytes(ws, T, d_in, d_out, r, n_slots, &w, &wd));
   if (s != LORA_OK) return s;
   if (T == 0) return LORA_OK;
   DeviceInfo dev;
   if ((s = check_device(&dev)) != LORA_OK) return s;
   if (!tensor_map_available()) return LORA_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // the decode chain of lora_linear_fused with the 4-bit base GEMM (split
-  // evenly over d_in, the same number of ranges for every column tile),
-  // over chunks of at most 256 tokens
-  for (int c0 = 0; c0 < T; c0 += kDecodeTokens) {
-    const int Tc = T - c0 < kDecodeTokens ? T - c0 : kDecodeTokens;
-    const int S = decode_uniform_split(Tc, d_in, d_out);
-    const uint16_t* xc = static_cast<const uint16_t*>(x) + static_cast<size_t>(c0) * d_in;  // bf16
-    uint16_t* yc = static_cast<uint16_t*>(y) + static_cast<size_t>(c0) * d_out;
-    cudaError_t e = launch_decode_q4(xc, W0q, absmax, codebook, w.partial, Tc, d_in, d_out, S,
-                                     w.err, true, st, dev);
+  cudaError_t e;
+  if (T <= kDecodeTokens) {
+    // the decode chain of lora_linear_fused with the 4-bit base GEMM (split
+    // evenly over d_in, the same number of ranges for every column tile)
+    const int S = decode_uniform_split(T, d_in, d_out);
+    e = launch_decode_q4(x, W0q, absmax, codebook, w.partial, T, d_in, d_out, S, w.err, true, st,
+                         dev);
     if (e != cudaSuccess) return LORA_ERR_CUDA;
-    e = launch_bgmv_adapter_merge(xc, A_pool, B_pool, slot_ids + c0, scale, w.partial, S, yc, Tc,
-                                  d_in, d_out, r, n_slots, w.err, true, st);
-    if (e != cudaSuccess) return LORA_ERR_CUDA;
+    return from_cuda(launch_bgmv_adapter_merge(x, A_pool, B_pool, slot_ids, scale, w.partial, S,
+                                               y, T, d_in, d_out, r, n_slots, w.err, true, st));
   }
-  return LORA_OK;
+  // larger batches: W0 dequantised once into the workspace (each weight
+  // rounded to bf16 once, as the decode GEMM feeds its MMAs), then the bf16
+  // prefill path over it, so W0 is streamed once, not once per 256 tokens
+  e = launch_dequantize_q4(W0q, absmax, codebook, wd, d_in, d_out, st);
+  if (e != cudaSuccess) return LORA_ERR_CUDA;
+  e = prefill_adapter_shrink(x, A_pool, slot_ids, scale, T, d_in, r, n_slots, LORA_DTYPE_BF16, w,
+                             st, dev);
+  if (e != cudaSuccess) return LORA_ERR_CUDA;
+  return from_cuda(launch_fused_tc(x, wd, B_pool, slot_ids, w.vpart, w.ksplit, y, T, d_in, d_out,
+                                   r, n_slots, w.err, st, dev));
 }
 
 lora_status_t lora_base_gemm_splitk(const void* x, const void* W0, float* partial, int32_t T,

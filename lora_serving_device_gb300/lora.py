@@ -20,6 +20,7 @@ STATUS_NAMES = {0: "LORA_OK", 1: "LORA_ERR_INVALID_ARG", 2: "LORA_ERR_SHAPE", 3:
 DTYPE_BF16, DTYPE_F32 = 0, 1
 OP_BUILD_SEGMENTS, OP_BGMV_SHRINK, OP_BGMV_EXPAND = 0, 1, 2
 OP_SGMV_SHRINK, OP_SGMV_EXPAND, OP_LINEAR_FUSED, OP_BASE_GEMM_EXPAND = 3, 4, 5, 6
+OP_LINEAR_FUSED_4BIT = 7
 DEVERR_BAD_SLOT, DEVERR_TIMEOUT, DEVERR_BAD_RANK = 0x1, 0x2, 0x4
 RAGGED_RANKS = (8, 16, 32, 64, 128)
 MAX_SLOTS, MAX_TOKENS, MAX_KSPLIT = 16384, 1 << 20, 64
@@ -551,8 +552,8 @@ def base_gemm_4bit_splitk_t(x, base, ws, ksplit=None, partial=None, stream=None)
 
 
 def linear_fused_4bit_t(x, base, A_pool, B_pool, slot_ids, scale, ws, y=None, stream=None):
-    """y = x deq(W0) + s (x A) B over a Base4bit (bf16; batches above 256 tokens run in
-    256-token chunks, so ws is sized for min(T, 256) tokens)."""
+    """y = x deq(W0) + s (x A) B over a Base4bit (bf16).  ws: workspace(OP_LINEAR_FUSED_4BIT,
+    T, ...); above 256 tokens it holds a dequantised copy of W0 for the prefill path."""
     import torch
     T, d_in = x.shape
     n_slots, _, r = A_pool.shape

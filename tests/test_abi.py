@@ -250,3 +250,16 @@ def test_no_gpu_reports_cuda_error_without_crashing(L):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert _fused(L) in (5, 6)   # LORA_ERR_CUDA / LORA_ERR_DEVICE, nothing launched
+
+
+def test_4bit_workspace_holds_the_dequantised_base_above_256_tokens(L):
+    """Up to 256 tokens the 4-bit layer runs the decode chain (the fused
+    layer's workspace); above, its workspace also holds W0 in bf16."""
+    for T, d_in, d_out, r, n in [(64, 4096, 4096, 16, 256), (256, 512, 1024, 64, 9),
+                                 (300, 256, 512, 16, 8), (9081, 4096, 14336, 64, 64)]:
+        fused = L.lora_workspace_bytes(L.OP_LINEAR_FUSED, T, d_in, d_out, r, n)
+        q4 = L.lora_workspace_bytes(L.OP_LINEAR_FUSED_4BIT, T, d_in, d_out, r, n)
+        if T <= 256:
+            assert q4 == fused
+        else:
+            assert q4 == -(-fused // 256) * 256 + d_in * d_out * 2

@@ -89,8 +89,10 @@ def test_base_gemm_4bit_splitk_matches_oracle(L, case):
 Q4_FUSED_CASES = [(1, 64, 128, 16, 3), (5, 192, 160, 8, 7), (33, 256, 384, 32, 5),
                   (64, 512, 1024, 16, 40), (7, 1024, 608, 32, 4), (48, 2048, 2112, 16, 9),
                   (200, 640, 160, 16, 30), (256, 256, 512, 64, 70),
-                  # larger batches run as 256-token chunks
-                  (300, 256, 512, 16, 8), (700, 192, 160, 8, 7)]
+                  # larger batches: W0 dequantised into the workspace, then the
+                  # prefill path (many 256 x 256 tiles; a half 64-column block)
+                  (300, 256, 512, 16, 8), (700, 192, 160, 8, 7), (2000, 1024, 2048, 64, 12),
+                  (400, 256, 96, 16, 5)]
 
 
 @pytest.mark.parametrize("case", Q4_FUSED_CASES, ids=[str(c) for c in Q4_FUSED_CASES])
@@ -104,7 +106,7 @@ def test_fused_4bit_matches_oracle(L, case):
     for zero_base in (False, True):
         am = np.zeros_like(absmax) if zero_base else absmax
         base = _dev_base(L, codes, am, cb)
-        ws = L.workspace(L.OP_LINEAR_FUSED, min(T, 256), d_in, d_out, r, n_slots)
+        ws = L.workspace(L.OP_LINEAR_FUSED_4BIT, T, d_in, d_out, r, n_slots)
         y = L.linear_fused_4bit_t(d.x, base, d.A, d.B, d.ids, d.scale, ws)
         torch.cuda.synchronize()
         ref = O.lora_linear(w.x, O.dequantize_4bit(codes, am, cb), w.A_pool, w.B_pool, w.scale,
@@ -123,7 +125,7 @@ def test_fused_4bit_decode_layer_full_size(L):
     codes, absmax = O.quantize_4bit(w.W0, cb)
     d = DeviceCase(w)
     base = _dev_base(L, codes, absmax, cb)
-    ws = L.workspace(L.OP_LINEAR_FUSED, w.T, w.d_in, w.d_out, w.r, w.n_slots)
+    ws = L.workspace(L.OP_LINEAR_FUSED_4BIT, w.T, w.d_in, w.d_out, w.r, w.n_slots)
     y = L.linear_fused_4bit_t(d.x, base, d.A, d.B, d.ids, d.scale, ws)
     torch.cuda.synchronize()
     ref = O.lora_linear(w.x, O.dequantize_4bit(codes, absmax, cb), w.A_pool, w.B_pool, w.scale,
