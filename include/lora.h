@@ -91,6 +91,11 @@ typedef enum {
 #define LORA_DEVERR_BAD_SLOT 0x1u /* a slot id outside [-1, n_slots) was read   */
 #define LORA_DEVERR_TIMEOUT 0x2u  /* a bounded on-chip wait gave up (no hang)   */
 #define LORA_DEVERR_BAD_RANK 0x4u /* a ragged-pool entry (rank, offsets) read was out of range */
+/* debug builds of the library only (-DLORA_DEBUG, liblora_debug.so): an index
+ * handed from one kernel to another (segment offsets, perm rows, segment
+ * slots) fell outside its buffer; it was replaced by 0, so nothing was read or
+ * written outside a buffer.  Release builds never set it. */
+#define LORA_DEVERR_BOUNDS 0x8u
 
 #define LORA_MAX_SLOTS 16384
 #define LORA_MAX_TOKENS (1 << 20)

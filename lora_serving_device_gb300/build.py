@@ -5,7 +5,12 @@ under _build/, then linked into lora_serving_device_gb300/liblora.so.  The
 CUDA runtime is linked statically; the driver is reached through the
 runtime's entry-point query, so nothing else needs to be on the link line.
 
-    python -m lora_serving_device_gb300.build [--force] [--verbose]
+With debug=True the same sources are built with -DLORA_DEBUG into
+_build_debug/ and liblora_debug.so: indices handed from one kernel to
+another are checked on the device, and one outside its buffer sets
+LORA_DEVERR_BOUNDS instead of being used.
+
+    python -m lora_serving_device_gb300.build [--force] [--verbose] [--debug]
 """
 from __future__ import annotations
 
@@ -21,6 +26,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "liblora.so")
+BUILD_DEBUG = os.path.join(ROOT, "_build_debug")
+LIB_DEBUG = os.path.join(PKG, "liblora_debug.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
@@ -53,19 +60,23 @@ def _stale(target, deps):
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False) -> str:
-    """Compile (if stale) and return the path of liblora.so."""
+def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False,
+          debug: bool = False) -> str:
+    """Compile (if stale) and return the path of liblora.so (liblora_debug.so
+    with debug=True)."""
     nvcc = nvcc_path()
-    os.makedirs(BUILD, exist_ok=True)
+    build_dir, lib = (BUILD_DEBUG, LIB_DEBUG) if debug else (BUILD, LIB)
+    flags = CFLAGS + (["-DLORA_DEBUG"] if debug else [])
+    os.makedirs(build_dir, exist_ok=True)
     srcs = _sources()
     hdrs = _headers()
     procs = []
     objs = []
     for src in srcs:
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         if force or _stale(obj, [src] + hdrs):
-            cmd = [nvcc, *ARCH, *CFLAGS, "-c", src, "-o", obj]
+            cmd = [nvcc, *ARCH, *flags, "-c", src, "-o", obj]
             if ptxas_verbose:
                 cmd[1:1] = ["-Xptxas", "-v"]
             if verbose:
@@ -81,17 +92,16 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
             failed.append(src)
     if failed:
         raise RuntimeError("nvcc failed for: " + ", ".join(os.path.basename(f) for f in failed))
-    if force or procs or _stale(LIB, objs):
-        tmp = LIB + ".tmp"
+    if force or procs or _stale(lib, objs):
+        tmp = lib + ".tmp"
         cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
         if verbose:
             print(" ".join(cmd), flush=True)
         subprocess.run(cmd, check=True)
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    build(force="--force" in sys.argv, verbose="--verbose" in sys.argv,
-          ptxas_verbose="--ptxas" in sys.argv)
-    print(LIB)
+    print(build(force="--force" in sys.argv, verbose="--verbose" in sys.argv,
+                ptxas_verbose="--ptxas" in sys.argv, debug="--debug" in sys.argv))

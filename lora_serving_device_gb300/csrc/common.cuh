@@ -83,6 +83,29 @@ __device__ __forceinline__ void flag_error(uint32_t* err, uint32_t bits) {
 
 __device__ __forceinline__ bool slot_valid(int id, int n_slots) { return id >= 0 && id < n_slots; }
 
+// Indices that come from data one kernel hands to another (the segment
+// builder's perm and segment offsets and slots).  In a debug build
+// (-DLORA_DEBUG) an index outside [0, n) raises LORA_DEVERR_BOUNDS and is
+// replaced by 0, so no access leaves its buffer; the release build uses the
+// index as it is.
+#ifdef LORA_DEBUG
+__device__ __forceinline__ int checked_index(int i, int n, uint32_t* err) {
+  if (i >= 0 && i < n) return i;
+  flag_error(err, LORA_DEVERR_BOUNDS);
+  return 0;
+}
+#else
+__device__ __forceinline__ int checked_index(int i, int, uint32_t*) { return i; }
+#endif
+// perm[idx] of a batch of T tokens, written by the grid this one depends on
+// (ld_dep) or by an earlier kernel of the stream (plain load).
+__device__ __forceinline__ int perm_row(const int32_t* perm, int idx, int T, uint32_t* err) {
+  return checked_index(ld_dep(perm + checked_index(idx, T, err)), T, err);
+}
+__device__ __forceinline__ int perm_row_plain(const int32_t* perm, int idx, int T, uint32_t* err) {
+  return checked_index(perm[checked_index(idx, T, err)], T, err);
+}
+
 // Programmatic dependent launch: wait until the grids this one depends on
 // have completed and their writes are visible (no-op without the attribute);
 // allow the next dependent grid to start launching.

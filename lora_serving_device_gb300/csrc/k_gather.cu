@@ -210,7 +210,7 @@ __global__ void __launch_bounds__(256)
     sgmv_shrink_kernel(const E* __restrict__ x, const E* __restrict__ A, const int32_t* perm,
                        const int32_t* seg_slot, const int32_t* seg_off, const int32_t* n_seg,
                        const float* __restrict__ scale, float* __restrict__ vpart, int T,
-                       int d_in, int n_slots, int kchunk) {
+                       int d_in, int n_slots, int kchunk, uint32_t* err) {
   using RL = RankLayout<R>;
   __shared__ int s_a, s_p0, s_p1;
   pdl_launch_dependents();  // the base GEMM may start streaming W0 now
@@ -220,11 +220,11 @@ __global__ void __launch_bounds__(256)
   if (blockIdx.x == 0) {    // rows of base-only tokens are zero
     const int nbase = ld_dep(seg_off);
     for (int e = tid; e < nbase * R; e += 256)
-      vpart[(static_cast<size_t>(s) * T + ld_dep(perm + e / R)) * R + (e % R)] = 0.f;
+      vpart[(static_cast<size_t>(s) * T + perm_row(perm, e / R, T, err)) * R + (e % R)] = 0.f;
   }
   sgmv_item<kSgTokens>(blockIdx.x, seg_slot, seg_off, nseg, &s_a, &s_p0, &s_p1);
-  const int a = s_a;
-  if (a < 0) return;
+  if (s_a < 0) return;
+  const int a = checked_index(s_a, n_slots, err);
   const int p0 = s_p0, p1 = s_p1;
   const int warp = tid >> 5, lane = tid & 31;
   const int qc = lane % RL::QC, kl = lane / RL::QC;
@@ -235,7 +235,7 @@ __global__ void __launch_bounds__(256)
     const int nt = min(4, p1 - pb);
     int tok[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) tok[u] = ld_dep(perm + pb + ((u < nt) ? u : 0));
+    for (int u = 0; u < 4; ++u) tok[u] = perm_row(perm, pb + ((u < nt) ? u : 0), T, err);
     float acc[4][8];
 #pragma unroll
     for (int u = 0; u < 4; ++u)
@@ -276,18 +276,19 @@ template <typename E, int R>
 __global__ void __launch_bounds__(256)
     sgmv_expand_kernel(const float* __restrict__ vpart, int ksplit, const E* __restrict__ B,
                        const int32_t* perm, const int32_t* seg_slot, const int32_t* seg_off,
-                       const int32_t* n_seg, E* __restrict__ y, int T, int d_out, int n_slots) {
+                       const int32_t* n_seg, E* __restrict__ y, int T, int d_out, int n_slots,
+                       uint32_t* err) {
   __shared__ float vs[kSgTokens][R];
   __shared__ int s_tok[kSgTokens];
   __shared__ int s_a, s_p0, s_p1;
   const int tid = threadIdx.x;
   sgmv_item<kSgTokens>(blockIdx.x, seg_slot, seg_off, ld_dep(n_seg), &s_a, &s_p0, &s_p1);
-  const int a = s_a;
-  if (a < 0) return;
+  if (s_a < 0) return;
+  const int a = checked_index(s_a, n_slots, err);
   const int p0 = s_p0, L = s_p1 - s_p0;
   for (int e = tid; e < L * R; e += 256) {
     const int i = e / R, q = e % R;
-    const int t = ld_dep(perm + p0 + i);
+    const int t = perm_row(perm, p0 + i, T, err);
     float acc = 0.f;
     for (int s = 0; s < ksplit; ++s) acc += vpart[(static_cast<size_t>(s) * T + t) * R + q];
     vs[i][q] = acc;
@@ -390,7 +391,7 @@ template <typename E>
 cudaError_t sgmv_shrink_t(const void* x, const void* A, const int32_t* perm,
                           const int32_t* seg_slot, const int32_t* seg_off, const int32_t* n_seg,
                           const float* scale, float* vpart, int T, int d_in, int r, int n_slots,
-                          int ksplit, cudaStream_t st, bool pdl) {
+                          int ksplit, uint32_t* err, cudaStream_t st, bool pdl) {
   const dim3 grid(sgmv_max_items(T, n_slots), ksplit);
   const int kc = kchunk_for(d_in, ksplit);
   const E* xe = static_cast<const E*>(x);
@@ -398,7 +399,7 @@ cudaError_t sgmv_shrink_t(const void* x, const void* A, const int32_t* perm,
 #define LORA_SGMV_SHRINK_CASE(RR)                                                              \
   case RR:                                                                                     \
     return launch_maybe_pdl(sgmv_shrink_kernel<E, RR>, grid, dim3(256), st, pdl, xe, Ae, perm, \
-                            seg_slot, seg_off, n_seg, scale, vpart, T, d_in, n_slots, kc);
+                            seg_slot, seg_off, n_seg, scale, vpart, T, d_in, n_slots, kc, err);
   switch (r) {
     LORA_SGMV_SHRINK_CASE(8)
     LORA_SGMV_SHRINK_CASE(16)
@@ -413,16 +414,17 @@ cudaError_t sgmv_shrink_t(const void* x, const void* A, const int32_t* perm,
 template <typename E>
 cudaError_t sgmv_expand_t(const float* vpart, int ksplit, const void* B, const int32_t* perm,
                           const int32_t* seg_slot, const int32_t* seg_off, const int32_t* n_seg,
-                          void* y, int T, int r, int d_out, int n_slots, cudaStream_t st) {
+                          void* y, int T, int r, int d_out, int n_slots, uint32_t* err,
+                          cudaStream_t st) {
   const dim3 grid(sgmv_max_items(T, n_slots), (d_out + 2047) / 2048);
   const E* Be = static_cast<const E*>(B);
   E* ye = static_cast<E*>(y);
   switch (r) {
-    case 8: sgmv_expand_kernel<E, 8><<<grid, 256, 0, st>>>(vpart, ksplit, Be, perm, seg_slot, seg_off, n_seg, ye, T, d_out, n_slots); break;
-    case 16: sgmv_expand_kernel<E, 16><<<grid, 256, 0, st>>>(vpart, ksplit, Be, perm, seg_slot, seg_off, n_seg, ye, T, d_out, n_slots); break;
-    case 32: sgmv_expand_kernel<E, 32><<<grid, 256, 0, st>>>(vpart, ksplit, Be, perm, seg_slot, seg_off, n_seg, ye, T, d_out, n_slots); break;
-    case 64: sgmv_expand_kernel<E, 64><<<grid, 256, 0, st>>>(vpart, ksplit, Be, perm, seg_slot, seg_off, n_seg, ye, T, d_out, n_slots); break;
-    case 128: sgmv_expand_kernel<E, 128><<<grid, 256, 0, st>>>(vpart, ksplit, Be, perm, seg_slot, seg_off, n_seg, ye, T, d_out, n_slots); break;
+    case 8: sgmv_expand_kernel<E, 8><<<grid, 256, 0, st>>>(vpart, ksplit, Be, perm, seg_slot, seg_off, n_seg, ye, T, d_out, n_slots, err); break;
+    case 16: sgmv_expand_kernel<E, 16><<<grid, 256, 0, st>>>(vpart, ksplit, Be, perm, seg_slot, seg_off, n_seg, ye, T, d_out, n_slots, err); break;
+    case 32: sgmv_expand_kernel<E, 32><<<grid, 256, 0, st>>>(vpart, ksplit, Be, perm, seg_slot, seg_off, n_seg, ye, T, d_out, n_slots, err); break;
+    case 64: sgmv_expand_kernel<E, 64><<<grid, 256, 0, st>>>(vpart, ksplit, Be, perm, seg_slot, seg_off, n_seg, ye, T, d_out, n_slots, err); break;
+    case 128: sgmv_expand_kernel<E, 128><<<grid, 256, 0, st>>>(vpart, ksplit, Be, perm, seg_slot, seg_off, n_seg, ye, T, d_out, n_slots, err); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
@@ -509,24 +511,22 @@ cudaError_t launch_sgmv_shrink(const void* x, const void* A, const int32_t* perm
                                const int32_t* n_seg, const float* scale, float* vpart, int T,
                                int d_in, int r, int n_slots, int ksplit, lora_dtype_t dt,
                                uint32_t* err, cudaStream_t st, bool pdl) {
-  (void)err;
   return dt == LORA_DTYPE_BF16
              ? sgmv_shrink_t<bf16>(x, A, perm, seg_slot, seg_off, n_seg, scale, vpart, T, d_in,
-                                   r, n_slots, ksplit, st, pdl)
+                                   r, n_slots, ksplit, err, st, pdl)
              : sgmv_shrink_t<float>(x, A, perm, seg_slot, seg_off, n_seg, scale, vpart, T, d_in,
-                                    r, n_slots, ksplit, st, pdl);
+                                    r, n_slots, ksplit, err, st, pdl);
 }
 
 cudaError_t launch_sgmv_expand(const float* vpart, int ksplit, const void* B, const int32_t* perm,
                                const int32_t* seg_slot, const int32_t* seg_off,
                                const int32_t* n_seg, void* y, int T, int r, int d_out,
                                int n_slots, lora_dtype_t dt, uint32_t* err, cudaStream_t st) {
-  (void)err;
   return dt == LORA_DTYPE_BF16
              ? sgmv_expand_t<bf16>(vpart, ksplit, B, perm, seg_slot, seg_off, n_seg, y, T, r,
-                                   d_out, n_slots, st)
+                                   d_out, n_slots, err, st)
              : sgmv_expand_t<float>(vpart, ksplit, B, perm, seg_slot, seg_off, n_seg, y, T, r,
-                                    d_out, n_slots, st);
+                                    d_out, n_slots, err, st);
 }
 
 }  // namespace lora

@@ -122,7 +122,7 @@ __global__ void __launch_bounds__(kThreads)
       __syncwarp();
       if (b >= 0 && rank == 0) c[b] += __popc(peers);
       __syncwarp();
-      if (b >= 0) perm[pos] = t;
+      if (b >= 0) perm[checked_index(pos, T, err)] = t;
     }
   }
   __syncthreads();

@@ -83,7 +83,7 @@ __global__ void __launch_bounds__(kThreads, ST == 3 && R == 64 ? 3 : 2)
                           const __grid_constant__ CUtensorMap tm_x, const bf16* x,
                           const int32_t* perm, const int32_t* seg_slot, const int32_t* seg_off,
                           const int32_t* n_seg, const float* scale, float* vpart, int T,
-                          int d_in, int kchunk, uint32_t* err) {
+                          int d_in, int n_slots, int kchunk, uint32_t* err) {
   using Lay = ShrinkLayout<R, ST>;
   constexpr int S = Lay::kStages;
   constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(128, R, false, true);
@@ -105,23 +105,23 @@ __global__ void __launch_bounds__(kThreads, ST == 3 && R == 64 ? 3 : 2)
   if (blockIdx.x == 0) {  // rows of base-only tokens are zero
     const int nbase = ld_dep(seg_off);
     for (int e = tid; e < nbase * R; e += kThreads)
-      vpart[(static_cast<size_t>(s) * T + ld_dep(perm + e / R)) * R + (e % R)] = 0.f;
+      vpart[(static_cast<size_t>(s) * T + perm_row(perm, e / R, T, err)) * R + (e % R)] = 0.f;
   }
   sgmv_item<kTok>(blockIdx.x, seg_slot, seg_off, nseg, &s_a, &s_p0, &s_p1);
-  const int a = s_a;
-  if (a < 0) return;  // no such item (uniform over the CTA)
+  if (s_a < 0) return;  // no such item (uniform over the CTA)
+  const int a = checked_index(s_a, n_slots, err);
   const int p0 = s_p0, n_tok = s_p1 - s_p0;
   const int k0 = s * kchunk, k1 = min(d_in, k0 + kchunk);
   const int n_it = k1 > k0 ? (k1 - k0 + 63) / 64 : 0;
   if (n_it == 0) {  // an empty split of d_in still writes its (zero) rows
     for (int e = tid; e < n_tok * R; e += kThreads)
-      vpart[(static_cast<size_t>(s) * T + ld_dep(perm + p0 + e / R)) * R + (e % R)] = 0.f;
+      vpart[(static_cast<size_t>(s) * T + perm_row(perm, p0 + e / R, T, err)) * R + (e % R)] = 0.f;
     return;
   }
   // perm is ascending within a segment, so the item's rows are consecutive
   // in x exactly when the first and last are n_tok - 1 apart
-  const int row0 = ld_dep(perm + p0);
-  const bool contig = ld_dep(perm + p0 + n_tok - 1) - row0 == n_tok - 1;
+  const int row0 = perm_row(perm, p0, T, err);
+  const bool contig = perm_row(perm, p0 + n_tok - 1, T, err) - row0 == n_tok - 1;
 
   if (warp == 4) {
     if (lane == 0) {
@@ -170,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, ST == 3 && R == 64 ? 3 : 2)
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
       const int i = (tid >> 3) + 16 * q;
-      rowtok[q] = i < n_tok ? ld_dep(perm + p0 + i) : -1;
+      rowtok[q] = i < n_tok ? perm_row(perm, p0 + i, T, err) : -1;
     }
     bool ok = true;
     int it = 0;
@@ -240,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, ST == 3 && R == 64 ? 3 : 2)
       ptx::tc_fence_after();
       const int i = warp * 32 + lane;
       const float sc = scale ? scale[a] : 1.f;
-      float* out = i < n_tok ? vpart + (static_cast<size_t>(s) * T + ld_dep(perm + p0 + i)) * R
+      float* out = i < n_tok ? vpart + (static_cast<size_t>(s) * T + perm_row(perm, p0 + i, T, err)) * R
                              : nullptr;
       const uint32_t tq = tmem + (static_cast<uint32_t>(warp * 32) << 16);
 #pragma unroll 1
@@ -296,7 +296,7 @@ cudaError_t launch_r(const CUtensorMap& tm, const CUtensorMap& tm_x, const bf16*
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kern, tm, tm_x, x, perm, seg_slot, seg_off, n_seg, scale, vpart,
-                            T, d_in, kchunk, err);
+                            T, d_in, n_slots, kchunk, err);
 }
 
 // ------------------------------------------------------------ expand
@@ -350,8 +350,8 @@ __global__ void __launch_bounds__(kThreads)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   sgmv_item<kTok>(blockIdx.x, seg_slot, seg_off, ld_dep(n_seg), &s_a, &s_p0, &s_p1);
-  const int a = s_a;
-  if (a < 0) return;  // no such item (uniform over the CTA)
+  if (s_a < 0) return;  // no such item (uniform over the CTA)
+  const int a = s_a;    // B[a] arrives by TMA, which reads nothing outside the pool
   const int p0 = s_p0, n_tok = s_p1 - s_p0;
   const int n_tiles_all = (d_out + kXN - 1) / kXN;
   const int j0 = blockIdx.y * kXGroup;
@@ -359,8 +359,8 @@ __global__ void __launch_bounds__(kThreads)
   if (nt <= 0) return;
   // a full item whose tokens are consecutive rows of y (a prefill request):
   // y moves by TMA, 64-column half-tiles, two buffers
-  const int row0 = ld_dep(perm + p0);
-  const bool ytma = n_tok == kTok && ld_dep(perm + p0 + kTok - 1) - row0 == kTok - 1;
+  const int row0 = perm_row(perm, p0, T, err);
+  const bool ytma = n_tok == kTok && perm_row(perm, p0 + kTok - 1, T, err) - row0 == kTok - 1;
   auto issue_y = [&](int hj) {  // half-tile hj = 2 j + h into buffer hj & 1
     ptx::mbar_arrive_expect_tx(&y_full[hj & 1], Lay::kYHalf);
     ptx::tma_load_2d(uni + (hj & 1) * Lay::kYHalf, &tm_y, &y_full[hj & 1],
@@ -406,7 +406,7 @@ __global__ void __launch_bounds__(kThreads)
     // v visible, and the compiler may batch them)
     const int i = tid;
     if (i < n_tok) {
-      const int tok = perm[p0 + i];
+      const int tok = perm_row_plain(perm, p0 + i, T, err);
 #pragma unroll 2
       for (int q0 = 0; q0 < R; q0 += 8) {
         float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -533,7 +533,7 @@ __global__ void __launch_bounds__(kThreads)
     // warp instruction reads (and writes) 128 contiguous bytes of one y row,
     // instead of 16 bytes of 32 different rows.
     const int n_rows = min(32, n_tok - warp * 32);  // this warp's token rows
-    bf16* yrow = n_rows > lane ? y + static_cast<size_t>(ld_dep(perm + p0 + warp * 32 + lane)) * d_out
+    bf16* yrow = n_rows > lane ? y + static_cast<size_t>(perm_row(perm, p0 + warp * 32 + lane, T, err)) * d_out
                                : nullptr;
     float* stg = reinterpret_cast<float*>(uni + warp * Lay::kStageWarp);
     const uint32_t tq = tmem + (static_cast<uint32_t>(warp * 32) << 16);

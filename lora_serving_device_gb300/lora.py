@@ -12,6 +12,8 @@ import ctypes
 import os
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "liblora.so")
+# the same library built with -DLORA_DEBUG (bounds checks that set LORA_DEVERR_BOUNDS)
+LIB_DEBUG_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "liblora_debug.so")
 
 # status codes / enums mirrored from include/lora.h
 LORA_OK = 0
@@ -21,7 +23,7 @@ DTYPE_BF16, DTYPE_F32 = 0, 1
 OP_BUILD_SEGMENTS, OP_BGMV_SHRINK, OP_BGMV_EXPAND = 0, 1, 2
 OP_SGMV_SHRINK, OP_SGMV_EXPAND, OP_LINEAR_FUSED, OP_BASE_GEMM_EXPAND = 3, 4, 5, 6
 OP_LINEAR_FUSED_4BIT = 7
-DEVERR_BAD_SLOT, DEVERR_TIMEOUT, DEVERR_BAD_RANK = 0x1, 0x2, 0x4
+DEVERR_BAD_SLOT, DEVERR_TIMEOUT, DEVERR_BAD_RANK, DEVERR_BOUNDS = 0x1, 0x2, 0x4, 0x8
 RAGGED_RANKS = (8, 16, 32, 64, 128)
 MAX_SLOTS, MAX_TOKENS, MAX_KSPLIT = 16384, 1 << 20, 64
 NOALLOC_SCRATCH_BYTES = 8 << 20

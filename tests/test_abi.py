@@ -263,3 +263,16 @@ def test_4bit_workspace_holds_the_dequantised_base_above_256_tokens(L):
             assert q4 == fused
         else:
             assert q4 == -(-fused // 256) * 256 + d_in * d_out * 2
+
+
+def test_debug_build_exports_every_declared_symbol(L):
+    """liblora_debug.so (-DLORA_DEBUG) is the same boundary with device bounds
+    checks; its error bit is declared beside the others."""
+    from lora_serving_device_gb300 import build
+    path = build.build(debug=True)
+    lib = ctypes.CDLL(path)
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    with open(os.path.join(ROOT, "include", "lora.h")) as f:
+        assert "#define LORA_DEVERR_BOUNDS 0x8u" in f.read()
+    assert L.DEVERR_BOUNDS == 0x8
