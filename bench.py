@@ -220,10 +220,10 @@ def parse_clocks(lines, window=None):
             "samples": len(sm)}
 
 
-# d_in splits for the standalone SGMV rows on the prefill workload: the shrink
-# is fastest at 4 of 1..8 (33 us against 38 us at 2 and 62 us at 1); the
-# expand, which sums the partials in its V build, at 2 (244 us against 266 us
-# at 4)
+# d_in splits for the standalone SGMV rows on the prefill workload: the shrink,
+# with its three-CTA ring, is fastest at 4 (29.0 us; 38.0 at 2, 30.5 at 3, 30.7
+# at 5, 30.0 at 6, 32.0 at 8); the expand, which sums the partials in its V
+# build, at 2 (198 us; 244 us at 4 before y moved by TMA)
 SGMV_SHRINK_KSPLIT = 4
 SGMV_EXPAND_KSPLIT = 2
 
