@@ -64,14 +64,14 @@ cudaError_t launch_fused_tc(const void* x, const void* W0, const void* B, const 
                             cudaStream_t st, const DeviceInfo& dev);
 // The whole BGMV adapter term of a decode-sized bf16 batch in one launch
 // (shrink, cluster sum of the rank-r partials, expand), see k_adapter.cu.
-// One cluster of adapter_cluster_size(T, d_in, d_out) CTAs per token.
+// One cluster of adapter_cluster_size(T, d_in, d_out, ragged) CTAs per token.
 //  - launch_bgmv_adapter: fp32 into delta [T, d_out]; rows of base-only
 //    tokens are not written.
 //  - launch_bgmv_adapter_merge: y = sum of the S fp32 partials [S, T, d_out]
 //    of the decode GEMM + the adapter term, bf16, every row written.  `pdl`:
 //    launch as a programmatic dependent of that GEMM (it waits for it before
 //    reading the partials).
-int adapter_cluster_size(int T, int d_in, int d_out);
+int adapter_cluster_size(int T, int d_in, int d_out, bool ragged);
 cudaError_t launch_bgmv_adapter(const void* x, const void* A, const void* B, const int32_t* ids,
                                 const float* scale, float* delta, int T, int d_in, int d_out,
                                 int r, int n_slots, uint32_t* err, cudaStream_t st);

@@ -252,9 +252,12 @@ __device__ __forceinline__ void adapter_token(const bf16* __restrict__ x, const 
   if (valid) ptx::cluster_wait_acquire();
 }
 
-// Padded pool: A [n_slots, d_in, R], B [n_slots, R, d_out].
-template <int R, bool MERGE>
-__global__ void __launch_bounds__(kAdThreads)
+// Padded pool: A [n_slots, d_in, R], B [n_slots, R, d_out].  MINB is the
+// resident-CTA count the registers are budgeted for: 4 (64 registers, so
+// three CTAs fit beside a decode-GEMM CTA) or 3 (80 registers).  Ranks 64
+// and 128 always take 80: at 64 they spill and run slower.
+template <int R, bool MERGE, int MINB>
+__global__ void __launch_bounds__(kAdThreads, MINB)
     bgmv_adapter_kernel(const bf16* __restrict__ x, const bf16* __restrict__ A,
                         const bf16* __restrict__ B, const int32_t* __restrict__ ids,
                         const float* __restrict__ scale, const float* partial, int S,
@@ -281,9 +284,11 @@ __global__ void __launch_bounds__(kAdThreads)
 // 128}.  Each token runs the body of its own adapter's rank, so a rank-8
 // adapter costs a rank-8 pass, not one at the pool's largest rank.  (Ranks
 // between these are stored zero-padded to the next one: per-row rank checks
-// inside the body would cost registers and load batching.)
+// inside the body would cost registers and load batching.)  Compiled for 64
+// registers: the rank-64 and -128 bodies spill a little, but more resident
+// CTAs pay for it on the mixed-rank pools measured.
 template <bool MERGE>
-__global__ void __launch_bounds__(kAdThreads)
+__global__ void __launch_bounds__(kAdThreads, 4)
     bgmv_adapter_ragged_kernel(const bf16* __restrict__ x, const bf16* __restrict__ A,
                                const bf16* __restrict__ B, const int64_t* __restrict__ a_off,
                                const int64_t* __restrict__ b_off,
@@ -338,10 +343,10 @@ struct AdapterLaunch {
   int kc, nc;
 };
 
-// One cluster of C CTAs per token, C = adapter_cluster_size(T, d_in, d_out).
-void adapter_launch_config(AdapterLaunch& L, int T, int d_in, int d_out, bool pdl,
+// One cluster of C CTAs per token, C = adapter_cluster_size(T, d_in, d_out, ragged).
+void adapter_launch_config(AdapterLaunch& L, int T, int d_in, int d_out, bool ragged, bool pdl,
                            cudaStream_t st) {
-  const int C = adapter_cluster_size(T, d_in, d_out);
+  const int C = adapter_cluster_size(T, d_in, d_out, ragged);
   L.kc = ((d_in + 8 * C - 1) / (8 * C)) * 8;
   L.nc = ((d_out + 8 * C - 1) / (8 * C)) * 8;
   L.cfg = cudaLaunchConfig_t{};
@@ -367,20 +372,28 @@ cudaError_t launch_adapter_form(const void* x, const void* A, const void* B, con
   if (T <= 0) return cudaSuccess;
   if (T > 65535) return cudaErrorInvalidValue;
   AdapterLaunch L;
-  adapter_launch_config(L, T, d_in, d_out, pdl, st);
+  adapter_launch_config(L, T, d_in, d_out, false, pdl, st);
   const bf16* xe = static_cast<const bf16*>(x);
   const bf16* Ae = static_cast<const bf16*>(A);
   const bf16* Be = static_cast<const bf16*>(B);
-#define LORA_ADAPTER_CASE(RR)                                                                  \
-  case RR:                                                                                     \
-    return cudaLaunchKernelEx(&L.cfg, bgmv_adapter_kernel<RR, MERGE>, xe, Ae, Be, ids, scale, \
-                              partial, S, out, T, d_in, d_out, n_slots, L.kc, L.nc, err);
+  // ranks up to 32: 64 registers for up to 64 tokens and from 256 on, 80 in
+  // between (measured per batch size on 4096 x 4096 layers)
+  const bool lean = T <= 64 || T >= 256;
+#define LORA_ADAPTER_CASE(RR, MB)                                                              \
+  return cudaLaunchKernelEx(&L.cfg, bgmv_adapter_kernel<RR, MERGE, MB>, xe, Ae, Be, ids,      \
+                            scale, partial, S, out, T, d_in, d_out, n_slots, L.kc, L.nc, err)
   switch (r) {
-    LORA_ADAPTER_CASE(8)
-    LORA_ADAPTER_CASE(16)
-    LORA_ADAPTER_CASE(32)
-    LORA_ADAPTER_CASE(64)
-    LORA_ADAPTER_CASE(128)
+    case 8:
+      if (lean) LORA_ADAPTER_CASE(8, 4);
+      LORA_ADAPTER_CASE(8, 3);
+    case 16:
+      if (lean) LORA_ADAPTER_CASE(16, 4);
+      LORA_ADAPTER_CASE(16, 3);
+    case 32:
+      if (lean) LORA_ADAPTER_CASE(32, 4);
+      LORA_ADAPTER_CASE(32, 3);
+    case 64: LORA_ADAPTER_CASE(64, 3);
+    case 128: LORA_ADAPTER_CASE(128, 3);
     default: return cudaErrorInvalidValue;
   }
 #undef LORA_ADAPTER_CASE
@@ -394,7 +407,7 @@ cudaError_t launch_ragged_form(const void* x, const void* A, const void* B, cons
   if (T <= 0) return cudaSuccess;
   if (T > 65535 || rp.r_max < 8 || rp.r_max > 128) return cudaErrorInvalidValue;
   AdapterLaunch L;
-  adapter_launch_config(L, T, d_in, d_out, pdl, st);
+  adapter_launch_config(L, T, d_in, d_out, true, pdl, st);
   return cudaLaunchKernelEx(&L.cfg, bgmv_adapter_ragged_kernel<MERGE>,
                             static_cast<const bf16*>(x), static_cast<const bf16*>(A),
                             static_cast<const bf16*>(B), rp.a_off, rp.b_off, rp.rank,
@@ -404,15 +417,19 @@ cudaError_t launch_ragged_form(const void* x, const void* A, const void* B, cons
 
 }  // namespace
 
-int adapter_cluster_size(int T, int d_in, int d_out) {
+int adapter_cluster_size(int T, int d_in, int d_out, bool ragged) {
   // up to 4 CTAs per token on wide layers (the shrink's A slice and the
   // expand's B slice per CTA stay small) while the grid stays within ~256
   // CTAs, so all of them fit on the GPU beside the decode GEMM; at least
   // enough that each CTA keeps its columns in registers; at most the
-  // portable cluster size of 8
+  // portable cluster size of 8.  A ragged pool keeps up to 4 CTAs per token
+  // at any T: its high-rank tokens are the long ones, and shorter per-CTA
+  // slices measured faster there (for a padded rank-16 pool at 256 tokens,
+  // slower)
   const int m = d_in < d_out ? d_in : d_out;
   int C = m >= 2048 ? 4 : (m >= 512 ? 2 : 1);
-  const int cap = T > 0 && T < 256 ? 256 / T : 1;
+  int cap = T > 0 && T < 256 ? 256 / T : 1;
+  if (ragged && cap < 4) cap = 4;
   if (C > cap) C = cap;
   const int by_cols = (d_out + kKeepGroups * kStride - 1) / (kKeepGroups * kStride);
   if (C < by_cols) C = by_cols;
