@@ -302,6 +302,8 @@ cudaError_t launch_r(const CUtensorMap& tm, const CUtensorMap& tm_x, const bf16*
 // ------------------------------------------------------------ expand
 constexpr int kXN = 128;      // d_out columns per tile (the MMA's N)
 constexpr int kXGroup = 8;    // d_out tiles per CTA
+constexpr int kBBuf = 1;      // B[a] tile buffers
+constexpr int kYBuf = 3;      // y half-tile buffers (TMA path)
 
 template <int R>
 struct ExpandLayout {
@@ -310,18 +312,20 @@ struct ExpandLayout {
   static constexpr uint32_t kV = 2 * KB * kVBlk;             // hi blocks, then lo blocks
   static constexpr uint32_t kBBox = R * 128;                 // 64 columns x R rows
   static constexpr uint32_t kB = (kXN / 64) * kBBox;
-  static constexpr uint32_t kBars = kV + 2 * kB;
+  static constexpr uint32_t kBars = kV + kBBuf * kB;
   // per epilogue warp: 32 rows x 64 accumulator columns (+4 floats of padding
   // per row, so the 32 rows' float4 writes hit distinct banks)
   static constexpr int kStLd = 64 + 4;
-  // b_full[2], b_empty[2], t_full[2], t_empty[2], y_full[2], TMEM slot, abort
-  static constexpr uint32_t kStage = kBars + 10 * 8 + 16;
+  // b_full[kBBuf], b_empty[kBBuf], t_full[2], t_empty[2], y_full[kYBuf],
+  // TMEM slot, abort
+  static constexpr int kNBar = 2 * kBBuf + 4 + kYBuf;
+  static constexpr uint32_t kStage = kBars + kNBar * 8 + 16;
   static constexpr uint32_t kStageWarp = 32 * kStLd * 4;
-  // the staging area, or (full items whose rows are consecutive in y) two
+  // the staging area, or (full items whose rows are consecutive in y) kYBuf
   // 16 KiB y half-tiles (128 rows x 64 columns, 128-byte swizzle) for TMA
   static constexpr uint32_t kStageAll = 4 * kStageWarp;
   static constexpr uint32_t kYHalf = kTok * 128;
-  static constexpr uint32_t kUnion = kStageAll > 2 * kYHalf ? kStageAll : 2 * kYHalf;
+  static constexpr uint32_t kUnion = kStageAll > kYBuf * kYHalf ? kStageAll : kYBuf * kYHalf;
   static constexpr uint32_t kStageOff = (kStage + 1023) / 1024 * 1024;
   static constexpr uint32_t kTotal = kStageOff + kUnion;
 };
@@ -340,12 +344,12 @@ __global__ void __launch_bounds__(kThreads)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint64_t* b_full = reinterpret_cast<uint64_t*>(smem + Lay::kBars);
-  uint64_t* b_empty = b_full + 2;
-  uint64_t* t_full = b_full + 4;
-  uint64_t* t_empty = b_full + 6;
-  uint64_t* y_full = b_full + 8;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(b_full + 10);
-  volatile int* abort_f = reinterpret_cast<volatile int*>(b_full + 10) + 1;
+  uint64_t* b_empty = b_full + kBBuf;
+  uint64_t* t_full = b_empty + kBBuf;
+  uint64_t* t_empty = t_full + 2;
+  uint64_t* y_full = t_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(y_full + kYBuf);
+  volatile int* abort_f = reinterpret_cast<volatile int*>(y_full + kYBuf) + 1;
   uint8_t* uni = smem + Lay::kStageOff;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -358,17 +362,18 @@ __global__ void __launch_bounds__(kThreads)
   const int nt = min(kXGroup, n_tiles_all - j0);
   if (nt <= 0) return;
   // a full item whose tokens are consecutive rows of y (a prefill request):
-  // y moves by TMA, 64-column half-tiles, two buffers
+  // y moves by TMA, 64-column half-tiles, kYBuf buffers
   const int row0 = perm_row(perm, p0, T, err);
   const bool ytma = n_tok == kTok && perm_row(perm, p0 + kTok - 1, T, err) - row0 == kTok - 1;
-  auto issue_y = [&](int hj) {  // half-tile hj = 2 j + h into buffer hj & 1
-    ptx::mbar_arrive_expect_tx(&y_full[hj & 1], Lay::kYHalf);
-    ptx::tma_load_2d(uni + (hj & 1) * Lay::kYHalf, &tm_y, &y_full[hj & 1],
+  auto issue_y = [&](int hj) {  // half-tile hj = 2 j + h into buffer hj % kYBuf
+    const int yb = hj % kYBuf;
+    ptx::mbar_arrive_expect_tx(&y_full[yb], Lay::kYHalf);
+    ptx::tma_load_2d(uni + yb * Lay::kYHalf, &tm_y, &y_full[yb],
                      (j0 + (hj >> 1)) * kXN + 64 * (hj & 1), row0);
   };
 
-  auto issue_b = [&](int j) {  // B[a][:, tile j] into buffer j & 1
-    const int bs = j & 1;
+  auto issue_b = [&](int j) {  // B[a][:, tile j] into buffer j % kBBuf
+    const int bs = j % kBBuf;
     ptx::mbar_arrive_expect_tx(&b_full[bs], Lay::kB);
 #pragma unroll
     for (int h = 0; h < kXN / 64; ++h)
@@ -378,21 +383,21 @@ __global__ void __launch_bounds__(kThreads)
   if (warp == 4) {
     if (lane == 0) {
       ptx::prefetch_tmap(&tm_b);
-      for (int i = 0; i < 2; ++i) {
+      for (int i = 0; i < kBBuf; ++i) {
         ptx::mbar_init(&b_full[i], 1);
         ptx::mbar_init(&b_empty[i], 1);
+      }
+      for (int i = 0; i < 2; ++i) {
         ptx::mbar_init(&t_full[i], 1);
         ptx::mbar_init(&t_empty[i], 4 * 32);
-        ptx::mbar_init(&y_full[i], 1);
       }
+      for (int i = 0; i < kYBuf; ++i) ptx::mbar_init(&y_full[i], 1);
       *abort_f = 0;
       ptx::fence_mbar_init();
-      issue_b(0);
-      if (nt > 1) issue_b(1);
+      for (int j = 0; j < kBBuf && j < nt; ++j) issue_b(j);
       if (ytma) {
         ptx::prefetch_tmap(&tm_y);
-        issue_y(0);
-        issue_y(1);
+        for (int hj = 0; hj < kYBuf && hj < 2 * nt; ++hj) issue_y(hj);
       }
     }
     __syncwarp();
@@ -440,13 +445,14 @@ __global__ void __launch_bounds__(kThreads)
     if (lane == 0) {
       const uint32_t vbase = ptx::smem_u32(smem);
       for (int j = 0; j < nt; ++j) {
-        const int bs = j & 1;
-        const uint32_t ph = static_cast<uint32_t>(j >> 1) & 1u;
-        if (!ptx::mbar_wait_bounded(&b_full[bs], ph, abort_f, kWaitLimitNs)) break;
-        if (!ptx::mbar_wait_bounded(&t_empty[bs], ph ^ 1u, abort_f, kWaitLimitNs)) break;
+        const int bs = j % kBBuf, ts = j & 1;  // B buffer, TMEM accumulator
+        const uint32_t bph = static_cast<uint32_t>(j / kBBuf) & 1u;
+        const uint32_t tph = static_cast<uint32_t>(j >> 1) & 1u;
+        if (!ptx::mbar_wait_bounded(&b_full[bs], bph, abort_f, kWaitLimitNs)) break;
+        if (!ptx::mbar_wait_bounded(&t_empty[ts], tph ^ 1u, abort_f, kWaitLimitNs)) break;
         ptx::tc_fence_after();
         const uint32_t bb = ptx::smem_u32(smem + Lay::kV + bs * Lay::kB);
-        const uint32_t acc = tmem + static_cast<uint32_t>(bs * kXN);
+        const uint32_t acc = tmem + static_cast<uint32_t>(ts * kXN);
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
 #pragma unroll
@@ -458,10 +464,10 @@ __global__ void __launch_bounds__(kThreads)
           }
         }
         ptx::mma_commit(&b_empty[bs]);
-        ptx::mma_commit(&t_full[bs]);
-        if (j + 2 < nt) {  // the buffer is free once these MMAs are done
-          if (!ptx::mbar_wait_bounded(&b_empty[bs], ph, abort_f, kWaitLimitNs)) break;
-          issue_b(j + 2);
+        ptx::mma_commit(&t_full[ts]);
+        if (j + kBBuf < nt) {  // the buffer is free once these MMAs are done
+          if (!ptx::mbar_wait_bounded(&b_empty[bs], bph, abort_f, kWaitLimitNs)) break;
+          issue_b(j + kBBuf);
         }
       }
     }
@@ -469,12 +475,13 @@ __global__ void __launch_bounds__(kThreads)
   } else if (ytma) {
     // ---------------- epilogue, y by TMA: y half-tile += accumulator ------
     // TMEM lane = token row i of the tile = row row0 + i of y.  Half-tile hj
-    // (64 columns) sits in buffer hj & 1 as 128 rows of 128 bytes with the
-    // 128-byte swizzle: thread i adds its accumulator row in place (the 32
-    // rows of a warp spread over all banks), then one thread stores the
-    // half-tile with TMA, waits until the store has read it and loads half-
-    // tile hj + 2 into the same buffer.  The other buffer's load is in
-    // flight meanwhile.  Every epilogue thread passes the same named
+    // (64 columns) sits in buffer hj % kYBuf as 128 rows of 128 bytes with
+    // the 128-byte swizzle: thread i adds its accumulator row in place (the
+    // 32 rows of a warp spread over all banks), then one thread stores the
+    // half-tile with TMA.  It does not wait for that store: once the store
+    // before it has read its buffer (at most kYBuf - 2 stores still reading),
+    // that buffer takes the load of half-tile hj + 2, so every load is issued
+    // two half-tiles ahead.  Every epilogue thread passes the same named
     // barriers, aborted or not.
     const int i = warp * 32 + lane;
     const uint32_t tq = tmem + (static_cast<uint32_t>(warp * 32) << 16);
@@ -487,8 +494,8 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll 1
       for (int h = 0; h < kXN / 64; ++h) {
         const int hj = 2 * j + h;
-        ok = ok && warp_wait(&y_full[hj & 1], static_cast<uint32_t>(hj >> 1) & 1u, abort_f);
-        uint8_t* yb = uni + (hj & 1) * Lay::kYHalf + i * 128;
+        ok = ok && warp_wait(&y_full[hj % kYBuf], static_cast<uint32_t>(hj / kYBuf) & 1u, abort_f);
+        uint8_t* yb = uni + (hj % kYBuf) * Lay::kYHalf + i * 128;
         if (ok) {
 #pragma unroll
           for (int c0 = 0; c0 < 64; c0 += 32) {
@@ -516,16 +523,18 @@ __global__ void __launch_bounds__(kThreads)
         }
         asm volatile("bar.sync 1, 128;" ::: "memory");
         if (i == 0 && ok && !*abort_f) {
-          ptx::tma_store_2d(&tm_y, uni + (hj & 1) * Lay::kYHalf,
+          ptx::tma_store_2d(&tm_y, uni + (hj % kYBuf) * Lay::kYHalf,
                             (j0 + j) * kXN + 64 * h, row0);
           ptx::bulk_commit_group();
-          ptx::bulk_wait_group_read_all();  // the buffer is read: reload it
-          if (hj + 2 < 2 * nt) issue_y(hj + 2);
+          // the store of half-tile hj + 2 - kYBuf has read its buffer
+          ptx::bulk_wait_group_read<kYBuf - 2>();
+          if (hj + 2 >= kYBuf && hj + 2 < 2 * nt) issue_y(hj + 2);
         }
       }
       ptx::tc_fence_before();
       ptx::mbar_arrive(&t_empty[bs]);
     }
+    if (i == 0) ptx::bulk_wait_group_read_all();  // the buffers outlive every store
   } else {
     // ---------------- epilogue: y rows += accumulator rows ----------------
     // TMEM lane = token row of the tile.  Each warp stages its 32 rows x 64
