@@ -814,6 +814,32 @@ def prefill_point(L, stream, pk, dev, steps=30, warm=5):
                     "tflops": flops / t4 / 1e12, "frac_burst_bf16": flops / t4 / 1e12 / pk["bf16_tflops"],
                     "device_error": L.get_error_t(ws4, stream=stream)}
     del base4, ws4
+    # the same layer over a ragged-rank pool (ranks drawn from 8 / 16 / 64 per
+    # slot, as in workload 5): with its own workspace it takes the prefill
+    # route over a compact padded copy of the batch's adapters; with a
+    # workspace for 256 tokens, 256-token chunks of the decode path
+    ranks = W.stack_ranks(n_slots)
+    pool = L.RaggedPool.from_padded(A, B, ranks)
+    wsr = L.workspace(L.OP_LINEAR_FUSED_RAGGED, T, d_in, d_out, pool.r_max, n_slots)
+    msr, _ = timed_graph_steps(
+        lambda i: L.linear_fused_ragged_t(x, W0, pool, ids, scale, wsr, y=y, stream=stream),
+        steps, warm, stream)
+    err_r = L.get_error_t(wsr, stream=stream)
+    del wsr
+    wsc = L.workspace(L.OP_LINEAR_FUSED, 256, d_in, d_out, pool.r_max, n_slots)
+    msc, _ = timed_graph_steps(
+        lambda i: L.linear_fused_ragged_t(x, W0, pool, ids, scale, wsc, y=y, stream=stream),
+        max(3, steps // 10), 2, stream)
+    tr = msr / 1e3 / steps
+    tc = msc / 1e3 / max(3, steps // 10)
+    prefill_ragged = {"workload": "prefill_sgmv over a ragged-rank pool (ranks 8 / 16 / 64 per "
+                                  "slot), the prefill route (the batch's adapters padded to the "
+                                  "pool's rank 64 in the workspace)",
+                      "ms_per_step": tr * 1e3, "tokens_per_s": T / tr,
+                      "tflops": flops / tr / 1e12, "frac_burst_bf16": flops / tr / 1e12 / pk["bf16_tflops"],
+                      "device_error": err_r,
+                      "chunked_decode_path_ms": tc * 1e3}
+    del pool, wsc
     res = {"workload": "prefill_sgmv: 4096->14336, rank 64, 64 slots, 16 prefill requests "
                        "(U[64,1024] tokens) + 48 decode tokens",
            "T": T, "distinct": D, "ms_per_step": t * 1e3, "tokens_per_s": T / t,
@@ -823,7 +849,7 @@ def prefill_point(L, stream, pk, dev, steps=30, warm=5):
                         "unit": "TFLOP/s", "frac": tf / pk["bf16_tflops"],
                         "peak_kind": "burst (cuBLAS bf16, measured)",
                         "frac_vs_sustained": tf / pk["bf16_tflops_sustained"]},
-           "blocks": blocks, "prefill_4bit": prefill_4bit}
+           "blocks": blocks, "prefill_4bit": prefill_4bit, "prefill_ragged": prefill_ragged}
     del x, W0, A, B
     torch.cuda.empty_cache()
     return res

@@ -84,7 +84,8 @@ typedef enum {
   LORA_OP_SGMV_EXPAND = 4,
   LORA_OP_LINEAR_FUSED = 5,
   LORA_OP_BASE_GEMM_EXPAND = 6,
-  LORA_OP_LINEAR_FUSED_4BIT = 7
+  LORA_OP_LINEAR_FUSED_4BIT = 7,
+  LORA_OP_LINEAR_FUSED_RAGGED = 8
 } lora_op_t;
 
 /* device error word bits */
@@ -378,13 +379,29 @@ lora_status_t lora_linear_fused_noalloc(const void* x, const void* W0, const voi
  *
  * lora_bgmv_adapter_ragged: the adapter term only, as lora_bgmv_adapter
  * (fp32 delta [T, d_out], base-only rows not written; T <= 65535; workspace:
- * the error word).  lora_linear_fused_ragged: the whole layer, as
- * lora_linear_fused's bf16 decode path (the split-K base GEMM, then the
- * merge kernel over the ragged pool, with the same programmatic overlap
- * rules), over consecutive chunks of at most 256 tokens; workspace:
- * lora_workspace_bytes(LORA_OP_LINEAR_FUSED, min(T, 256), d_in, d_out, r_max,
- * n_slots).  Both: bf16 only; LORA_ERR_INVALID_ARG for a null pointer, a
- * pool, x or output not 16-byte aligned, or a negative pool length.
+ * the error word).  lora_linear_fused_ragged: the whole layer.
+ *   - Up to 256 tokens: lora_linear_fused's bf16 decode path (the split-K
+ *     base GEMM, then the merge kernel over the ragged pool, with the same
+ *     programmatic overlap rules).
+ *   - More tokens, with a workspace of lora_workspace_bytes(
+ *     LORA_OP_LINEAR_FUSED_RAGGED, T, d_in, d_out, r_max, n_slots) bytes: the
+ *     prefill route.  The adapters the batch uses are copied into the
+ *     workspace as a dense pool at rank r_max (zero-padded), their tokens'
+ *     ids remapped to it, and lora_linear_fused's prefill path runs over it
+ *     (segments, SGMV shrink, the base GEMM with the expand in its
+ *     accumulator): W0 is read once.  The result equals that of the
+ *     zero-padded pool, as on the decode path.
+ *   - More tokens with a workspace too small for that but of at least
+ *     lora_workspace_bytes(LORA_OP_LINEAR_FUSED, 256, ...) bytes: the decode
+ *     path over consecutive chunks of at most 256 tokens, which reads W0
+ *     once per chunk.  (The prefill route's workspace can be the smaller of
+ *     the two: the chunked route's holds the split-K partials.)
+ *   LORA_OP_LINEAR_FUSED_RAGGED gives, for T <= 256, the decode path's
+ *   workspace; for T > 256 the prefill route's (with n_c = min(T, n_slots):
+ *   the prefill layout of lora_linear_fused for T tokens over n_c slots at
+ *   rank r_max, plus n_c x (d_in + d_out) x r_max x 2 bytes of pool).
+ * Both: bf16 only; LORA_ERR_INVALID_ARG for a null pointer, a pool, x or
+ * output not 16-byte aligned, or a negative pool length.
  */
 lora_status_t lora_bgmv_adapter_ragged(const void* x, const void* A_flat, const void* B_flat,
                                        const int64_t* a_off, const int64_t* b_off,

@@ -101,6 +101,20 @@ cudaError_t launch_bgmv_adapter_ragged_merge(const void* x, const void* A, const
                                              const float* scale, const float* partial, int S,
                                              void* y, int T, int d_in, int d_out, int n_slots,
                                              uint32_t* err, bool pdl, cudaStream_t st);
+// The prefill route of the ragged layer, see k_ragged_compact.cu.  Given the
+// segments of the batch's ids (seg_slot / n_seg from the segment builder):
+//  - launch_ragged_compact: segment j's adapter into compact slot j of a
+//    dense bf16 pool at rank rp.r_max (A_c [n_c, d_in, r_max], B_c [n_c,
+//    r_max, d_out], zero-padded; scale_c [n_c]); n_c >= the segment count;
+//  - launch_ragged_remap: ids_c[t] = the compact slot of token t, or -1.
+cudaError_t launch_ragged_compact(const void* A, const void* B, const RaggedPool& rp,
+                                  const float* scale, const int32_t* seg_slot,
+                                  const int32_t* n_seg, int n_c, int n_slots, void* A_c,
+                                  void* B_c, float* scale_c, int d_in, int d_out, uint32_t* err,
+                                  cudaStream_t st);
+cudaError_t launch_ragged_remap(const int32_t* ids, const int32_t* seg_slot, const int32_t* n_seg,
+                                int32_t* ids_c, int T, int n_slots, uint32_t* err,
+                                cudaStream_t st);
 // BGMV expand into an fp32 term: delta[t, :] = (sum_s vpart[s, t, :]) B[a_t]
 // for tokens with a valid id (other rows untouched); bf16 B.  `pdl`: launch
 // as a programmatic dependent of the shrink just before.

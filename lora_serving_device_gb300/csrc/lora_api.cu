@@ -110,6 +110,41 @@ size_t q4_ws_bytes(void* ws, int32_t T, int32_t d_in, int32_t d_out, int32_t r, 
   return o + static_cast<size_t>(d_in) * d_out * 2;
 }
 
+// Workspace of lora_linear_fused_ragged's prefill route (T > 256): the
+// prefill layout of lora_linear_fused over a compact pool of n_c = min(T,
+// n_slots) slots at rank r_max, then the compact ids [T], scales [n_c] and
+// pool, A_c [n_c, d_in, r_max] and B_c [n_c, r_max, d_out] bf16.  The
+// layout's segment arrays first hold the segments of the batch's own ids
+// (at most n_c of them), which the compact pool is built from.
+struct RaggedWs {
+  FusedWs w;
+  int32_t n_c;
+  int32_t* ids_c;
+  float* scale_c;
+  void* A_c;
+  void* B_c;
+  size_t bytes;
+};
+
+RaggedWs ragged_ws_layout(void* ws, int32_t T, int32_t d_in, int32_t d_out, int32_t r_max,
+                          int32_t n_slots) {
+  RaggedWs rw;
+  rw.n_c = T < n_slots ? T : n_slots;
+  rw.w = fused_ws_layout(ws, T, d_in, d_out, r_max, rw.n_c);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  size_t o = round_up(rw.w.bytes, 256);
+  rw.ids_c = reinterpret_cast<int32_t*>(base + o);
+  o += static_cast<size_t>(T) * 4;
+  rw.scale_c = reinterpret_cast<float*>(base + o);
+  o = round_up(o + static_cast<size_t>(rw.n_c) * 4, 256);
+  rw.A_c = base + o;
+  o = round_up(o + static_cast<size_t>(rw.n_c) * d_in * r_max * 2, 256);
+  rw.B_c = base + o;
+  o += static_cast<size_t>(rw.n_c) * r_max * d_out * 2;
+  rw.bytes = round_up(o, 256);
+  return rw;
+}
+
 lora_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? LORA_OK : LORA_ERR_CUDA; }
 
 // The library is built for sm_103a only.
@@ -219,6 +254,11 @@ size_t lora_workspace_bytes(int32_t op, int32_t T, int32_t d_in, int32_t d_out, 
     FusedWs w;
     void* wd;
     return q4_ws_bytes(nullptr, T, d_in, d_out, r, n_slots, &w, &wd);
+  }
+  if (op == LORA_OP_LINEAR_FUSED_RAGGED) {
+    if (T < 0 || !rank_ok(r) || !slots_ok(n_slots) || d_in < 8 || d_out < 0) return kErrBytes;
+    if (T <= kDecodeTokens) return fused_ws_layout(nullptr, T, d_in, d_out, r, n_slots).bytes;
+    return ragged_ws_layout(nullptr, T, d_in, d_out, r, n_slots).bytes;
   }
   return kErrBytes;
 }
@@ -545,15 +585,40 @@ lora_status_t lora_linear_fused_ragged(const void* x, const void* W0, const void
                                 slot_ids, y, T, LORA_MAX_TOKENS, d_in, d_out, n_slots, dt);
   if (s != LORA_OK) return s;
   if (W0 == nullptr || !aligned16(W0) || x == y) return LORA_ERR_INVALID_ARG;
+  // above 256 tokens a workspace that holds the prefill route's layout takes
+  // that route (it can be smaller than the chunked route's, which holds the
+  // split-K partials); any other workspace must hold the chunked route's
+  const RaggedWs rw = ragged_ws_layout(ws, T, d_in, d_out, r_max, n_slots);
+  const bool prefill = T > kDecodeTokens && check_ws(ws, ws_bytes, rw.bytes) == LORA_OK;
   const FusedWs w = fused_ws_layout(ws, T < kDecodeTokens ? T : kDecodeTokens, d_in, d_out, r_max,
                                     n_slots);
-  if ((s = check_ws(ws, ws_bytes, w.bytes)) != LORA_OK) return s;
+  if (!prefill && (s = check_ws(ws, ws_bytes, w.bytes)) != LORA_OK) return s;
   if (T == 0) return LORA_OK;
   DeviceInfo dev;
   if ((s = check_device(&dev)) != LORA_OK) return s;
   if (!tensor_map_available()) return LORA_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const RaggedPool rp{a_off, b_off, rank, a_elems, b_elems, r_max};
+  if (prefill) {
+    // prefill route: the batch's adapters into a dense pool at rank r_max in
+    // the workspace, then lora_linear_fused's prefill path over it (segments,
+    // SGMV shrink, the base GEMM with the expand in its accumulator)
+    const FusedWs& wp = rw.w;
+    cudaError_t e = launch_build_segments(slot_ids, T, n_slots, wp.perm, wp.seg_slot, wp.seg_off,
+                                          wp.n_seg, wp.err, st);
+    if (e == cudaSuccess)
+      e = launch_ragged_compact(A_flat, B_flat, rp, scale, wp.seg_slot, wp.n_seg, rw.n_c, n_slots,
+                                rw.A_c, rw.B_c, rw.scale_c, d_in, d_out, wp.err, st);
+    if (e == cudaSuccess)
+      e = launch_ragged_remap(slot_ids, wp.seg_slot, wp.n_seg, rw.ids_c, T, n_slots, wp.err, st);
+    if (e == cudaSuccess)
+      e = prefill_adapter_shrink(x, rw.A_c, rw.ids_c, rw.scale_c, T, d_in, r_max, rw.n_c,
+                                 LORA_DTYPE_BF16, wp, st, dev);
+    if (e == cudaSuccess)
+      e = launch_fused_tc(x, W0, rw.B_c, rw.ids_c, wp.vpart, wp.ksplit, y, T, d_in, d_out, r_max,
+                          rw.n_c, wp.err, st, dev);
+    return from_cuda(e);
+  }
   // the decode chain of lora_linear_fused with the ragged merge kernel, over
   // chunks of at most 256 tokens (the GEMM of each chunk starts while the
   // previous chunk's merge runs)

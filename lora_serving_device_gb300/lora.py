@@ -23,6 +23,7 @@ DTYPE_BF16, DTYPE_F32 = 0, 1
 OP_BUILD_SEGMENTS, OP_BGMV_SHRINK, OP_BGMV_EXPAND = 0, 1, 2
 OP_SGMV_SHRINK, OP_SGMV_EXPAND, OP_LINEAR_FUSED, OP_BASE_GEMM_EXPAND = 3, 4, 5, 6
 OP_LINEAR_FUSED_4BIT = 7
+OP_LINEAR_FUSED_RAGGED = 8
 DEVERR_BAD_SLOT, DEVERR_TIMEOUT, DEVERR_BAD_RANK, DEVERR_BOUNDS = 0x1, 0x2, 0x4, 0x8
 RAGGED_RANKS = (8, 16, 32, 64, 128)
 MAX_SLOTS, MAX_TOKENS, MAX_KSPLIT = 16384, 1 << 20, 64
@@ -496,8 +497,10 @@ def bgmv_adapter_ragged_t(x, pool, slot_ids, scale, ws, delta=None, stream=None)
 
 
 def linear_fused_ragged_t(x, W0, pool, slot_ids, scale, ws, y=None, stream=None):
-    """linear_fused_t over a RaggedPool (bf16; batches above 256 tokens run in 256-token
-    chunks, so ws is sized for min(T, 256) tokens)."""
+    """linear_fused_t over a RaggedPool (bf16).  With ws = workspace(OP_LINEAR_FUSED_RAGGED,
+    T, ...) batches above 256 tokens take the prefill route (the batch's adapters copied
+    into a dense pool at rank r_max in ws, then the prefill path); with a workspace for
+    256 tokens (OP_LINEAR_FUSED) they run as 256-token chunks of the decode path."""
     import torch
     T, d_in = x.shape
     d_out = W0.shape[1]

@@ -265,6 +265,27 @@ def test_4bit_workspace_holds_the_dequantised_base_above_256_tokens(L):
             assert q4 == -(-fused // 256) * 256 + d_in * d_out * 2
 
 
+def test_ragged_workspace_holds_a_compact_pool_above_256_tokens(L):
+    """Up to 256 tokens the ragged layer runs the decode chain (the fused
+    layer's workspace); above, its prefill route lays out lora_linear_fused's
+    prefill workspace over n_c = min(T, n_slots) compact slots, then the
+    compact ids, scales and the padded pool A_c / B_c."""
+    rup = lambda v: -(-v // 256) * 256
+    for T, d_in, d_out, r, n in [(64, 4096, 4096, 16, 256), (256, 512, 1024, 64, 9),
+                                 (300, 256, 512, 16, 8), (9081, 4096, 14336, 64, 64),
+                                 (700, 520, 264, 128, 2000)]:
+        rag = L.lora_workspace_bytes(L.OP_LINEAR_FUSED_RAGGED, T, d_in, d_out, r, n)
+        if T <= 256:
+            assert rag == L.lora_workspace_bytes(L.OP_LINEAR_FUSED, T, d_in, d_out, r, n)
+            continue
+        n_c = min(T, n)
+        o = rup(L.lora_workspace_bytes(L.OP_LINEAR_FUSED, T, d_in, d_out, r, n_c))
+        o = rup(o + T * 4 + n_c * 4)
+        o = rup(o + n_c * d_in * r * 2)
+        assert rag == rup(o + n_c * r * d_out * 2)
+    assert L.lora_workspace_bytes(L.OP_LINEAR_FUSED_RAGGED, 300, 256, 512, 24, 8) == 16  # bad rank
+
+
 def test_debug_build_exports_every_declared_symbol(L):
     """liblora_debug.so (-DLORA_DEBUG) is the same boundary with device bounds
     checks; its error bit is declared beside the others."""

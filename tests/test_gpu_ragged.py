@@ -163,3 +163,55 @@ def test_ragged_stack_projection(L):
         assert L.get_error_t(ws) == 0
         del t, pool
         torch.cuda.empty_cache()
+
+
+# prefill route (T > 256 with a workspace for it): the batch's adapters copied
+# into a dense pool at r_max, then the prefill path; T, d_in, d_out, n_slots, ranks
+RAGGED_PREFILL_CASES = [
+    (300, 256, 384, 10, (8, 16, 64)),
+    (700, 520, 264, 25, (8, 32, 128)),
+    (1000, 1024, 4104, 40, (8, 16, 64)),
+    (513, 264, 520, 600, (16, 64)),             # more slots than tokens: n_c = T
+    (4096, 512, 5120, 12, (8, 16, 64)),         # enough 256 x 256 tiles for the wide form
+]
+
+
+@pytest.mark.parametrize("case", RAGGED_PREFILL_CASES, ids=[str(c) for c in RAGGED_PREFILL_CASES])
+def test_fused_ragged_prefill_route_matches_oracle(L, case):
+    """With the ragged layer's own workspace, batches above 256 tokens read W0
+    once through the prefill path over a compact padded copy of their
+    adapters; the result must still be the per-rank oracle's."""
+    torch = torch_mod()
+    T, d_in, d_out, n_slots, rank_set = case
+    for W0_zero in (False, True):
+        c = RaggedCase(L, 1600 + T, T, d_in, d_out, n_slots, rank_set, W0_zero=W0_zero)
+        ws = L.workspace(L.OP_LINEAR_FUSED_RAGGED, T, d_in, d_out, c.pool.r_max, n_slots)
+        y = L.linear_fused_ragged_t(c.x, c.W0, c.pool, c.ids, c.scale, ws)
+        torch.cuda.synchronize()
+        what = "ragged prefill route delta" if W0_zero else "ragged prefill route y"
+        check_close_bf16_out(host(y), c.ref(), what)
+        assert L.get_error_t(ws) == 0
+
+
+def test_ragged_prefill_route_bad_entries_and_ids(L):
+    """On the prefill route, slots with bad table entries are copied as zeros
+    (their tokens get the base term, BAD_RANK raised) and ids outside
+    [-1, n_slots) are base-only (BAD_SLOT raised)."""
+    torch = torch_mod()
+    T, d_in, d_out, n_slots = 600, 256, 264, 8
+    c = RaggedCase(L, 1701, T, d_in, d_out, n_slots, (8, 16, 64))
+    ids = (np.arange(T, dtype=np.int32) * 7) % n_slots
+    ids[::50] = -1
+    ids[3::97] = n_slots + 3                              # invalid ids
+    c.ids = torch.from_numpy(ids).cuda()
+    saved = (c.pool.rank.clone(), c.pool.a_off.clone())
+    c.pool.rank[1] = 12                                   # not a stored rank class
+    c.pool.a_off[2] = c.pool.A_flat.numel() - 8           # runs past the pool's end
+    ws = L.workspace(L.OP_LINEAR_FUSED_RAGGED, T, d_in, d_out, c.pool.r_max, n_slots)
+    y = L.linear_fused_ragged_t(c.x, c.W0, c.pool, c.ids, c.scale, ws)
+    torch.cuda.synchronize()
+    ref_ids = np.where(np.isin(ids, [1, 2]) | (ids >= n_slots), -1, ids)
+    check_close_bf16_out(host(y), c.ref(ref_ids), "ragged prefill route, bad entries and ids")
+    assert L.get_error_t(ws) == L.DEVERR_BAD_RANK | L.DEVERR_BAD_SLOT
+    c.pool.rank.copy_(saved[0])
+    c.pool.a_off.copy_(saved[1])
