@@ -21,6 +21,8 @@
 // (which no earlier kernel of the layer writes) before it waits for the
 // predecessor grid, then loads x, which the predecessor may have written.
 // So the W0 stream of this layer overlaps the tail of the previous kernel.
+// The x blocks of those first stages are prefetched into L2 before the wait
+// as well, so that their loads after it are L2 hits.
 //
 // Warp roles: warp 0 = TMA producer, warp 1 = MMA issuer (and TMEM
 // allocator), warps 2-5 = epilogue.  Every on-chip wait is bounded in time;
@@ -143,6 +145,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_arrive_expect_tx(&full[it], Lay::kStage);
 #pragma unroll
         for (int h = 0; h < 2; ++h) ptx::tma_load_2d(Wr + h * Lay::kWBox, &tm_w, &full[it], n0 + 64 * h, k0);
+      }
+    }
+    // x of the ring's first stages into L2 before the wait (the blocks the
+    // loads right after it fetch): a prefetch moves no data into this SM,
+    // and those loads read what the predecessor wrote.  One CTA in eight
+    // column tiles of a split issues it.
+    if (lane == 0 && !p.hold_producer && blockIdx.x % 8 == 0) {
+      for (int it = 0; it < pre; ++it) {
+        const int k0 = (kb0 + it) * 64 * KSUB;
+#pragma unroll
+        for (int j = 0; j < KSUB; ++j)
+          if (k0 + 64 * j < p.d_in) ptx::tma_prefetch_l2_2d(&tm_x, k0 + 64 * j, t0);
       }
     }
     // every CTA waits, so this grid completing implies its predecessors did

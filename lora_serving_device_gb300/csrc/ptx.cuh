@@ -130,6 +130,14 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, ui
       : "memory");
 }
 
+// 2-D tiled prefetch of one box into L2 (no shared memory, no completion:
+// a later load of the same box finds it in L2, or merges with it in flight)
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* tm, int c0, int c1) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(tm),
+               "r"(c0), "r"(c1)
+               : "memory");
+}
+
 // 3-D tiled load into this CTA's shared memory (c0 innermost), completion
 // counted in bytes on `bar`; elements outside the tensor read as zero.
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* tm, uint64_t* bar, int c0,
