@@ -215,3 +215,26 @@ def test_ragged_prefill_route_bad_entries_and_ids(L):
     assert L.get_error_t(ws) == L.DEVERR_BAD_RANK | L.DEVERR_BAD_SLOT
     c.pool.rank.copy_(saved[0])
     c.pool.a_off.copy_(saved[1])
+
+
+@pytest.mark.parametrize("ids_kind", ["all_base", "one_slot", "257_mixed"])
+def test_ragged_prefill_route_edges(L, ids_kind):
+    """The prefill route's edges: every token base-only (no segment, nothing
+    copied), every token on one slot, and the smallest batch that takes the
+    route (257 tokens), each against the oracle."""
+    torch = torch_mod()
+    d_in, d_out, n_slots = 264, 520, 6
+    T = 257 if ids_kind == "257_mixed" else 300
+    c = RaggedCase(L, 1750 + len(ids_kind), T, d_in, d_out, n_slots, (8, 16, 32, 64, 128))
+    if ids_kind == "all_base":
+        ids = np.full(T, -1, np.int32)
+    elif ids_kind == "one_slot":
+        ids = np.full(T, 3, np.int32)
+    else:
+        ids = c.w.slot_ids.copy()
+    c.ids = torch.from_numpy(ids).cuda()
+    ws = L.workspace(L.OP_LINEAR_FUSED_RAGGED, T, d_in, d_out, c.pool.r_max, n_slots)
+    y = L.linear_fused_ragged_t(c.x, c.W0, c.pool, c.ids, c.scale, ws)
+    torch.cuda.synchronize()
+    check_close_bf16_out(host(y), c.ref(ids), f"ragged prefill route, {ids_kind}")
+    assert L.get_error_t(ws) == 0
