@@ -71,7 +71,7 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--no-stack", action="store_true",
                    help="skip the 224-layer 8B-shaped stack (timed by default)")
-    p.add_argument("--profile", choices=["decode", "prefill", "decode4bit", "ragged"],
+    p.add_argument("--profile", choices=["decode", "prefill", "decode4bit", "ragged", "sweep256"],
                    help="run 3 untimed passes of one workload and exit (for ncu)")
     p.add_argument("--oracle-child", type=int, default=0, help=argparse.SUPPRESS)
     p.add_argument("--oracle-budget", type=float, default=12.0, help=argparse.SUPPRESS)
@@ -1121,6 +1121,21 @@ def run_profile(case):
             L.sgmv_shrink_t(x, A, segs, scale, ks, wss, v_partial=vpart, stream=stream)
             L.sgmv_shrink_t(x, A, segs, scale, kx, wss, v_partial=vpart_x, stream=stream)
             L.sgmv_expand_t(vpart_x, Bp, segs, y, wss, stream=stream)
+        err = L.get_error_t(ws, stream=stream)
+    elif case == "sweep256":
+        # the T = 256 sweep point with 16 distinct adapters (weights drawn on
+        # the device as in the sweep)
+        T, d_in, d_out, r, n_slots = 256, 4096, 4096, 16, 1024
+        W0 = device_normal((d_in, d_out), W.W0_STD, 40400, dev)
+        A = device_normal((n_slots, d_in, r), W.A_STD, 40410, dev)
+        Bp = device_normal((n_slots, r, d_out), W.B_STD, 40420, dev)
+        x = device_normal((T, d_in), 1.0, 40430 + T, dev)
+        ids = torch.from_numpy(W.sweep_ids(T, 16)).to(dev)
+        scale = torch.full((n_slots,), W.SCALE, dtype=torch.float32, device=dev)
+        y = torch.empty((T, d_out), dtype=torch.bfloat16, device=dev)
+        ws = L.workspace(L.OP_LINEAR_FUSED, T, d_in, d_out, r, n_slots)
+        for _ in range(3):
+            L.linear_fused_t(x, W0, A, Bp, ids, scale, ws, y=y, stream=stream)
         err = L.get_error_t(ws, stream=stream)
     else:
         w = W.decode_bgmv()
