@@ -303,7 +303,10 @@ cudaError_t launch_r(const CUtensorMap& tm, const CUtensorMap& tm_x, const bf16*
 constexpr int kXN = 128;      // d_out columns per tile (the MMA's N)
 constexpr int kXGroup = 8;    // d_out tiles per CTA
 constexpr int kBBuf = 1;      // B[a] tile buffers
-constexpr int kYBuf = 3;      // y half-tile buffers (TMA path)
+constexpr int kYBuf = 3;      // y half-tile buffers
+constexpr int kYPitch = 144;  // bytes per token row moved by its own bulk copy
+constexpr int kMinRun = 16;   // shortest run of consecutive rows moved by TMA
+constexpr int kMaxTail = 16;  // most rows after such a run
 
 template <int R>
 struct ExpandLayout {
@@ -313,25 +316,27 @@ struct ExpandLayout {
   static constexpr uint32_t kBBox = R * 128;                 // 64 columns x R rows
   static constexpr uint32_t kB = (kXN / 64) * kBBox;
   static constexpr uint32_t kBars = kV + kBBuf * kB;
-  // per epilogue warp: 32 rows x 64 accumulator columns (+4 floats of padding
-  // per row, so the 32 rows' float4 writes hit distinct banks)
-  static constexpr int kStLd = 64 + 4;
   // b_full[kBBuf], b_empty[kBBuf], t_full[2], t_empty[2], y_full[kYBuf],
   // TMEM slot, abort
   static constexpr int kNBar = 2 * kBBuf + 4 + kYBuf;
   static constexpr uint32_t kStage = kBars + kNBar * 8 + 16;
-  static constexpr uint32_t kStageWarp = 32 * kStLd * 4;
-  // the staging area, or (full items whose rows are consecutive in y) kYBuf
-  // 16 KiB y half-tiles (128 rows x 64 columns, 128-byte swizzle) for TMA
-  static constexpr uint32_t kStageAll = 4 * kStageWarp;
+  // kYBuf buffers of one y half-tile (128 token rows x 64 columns).  Rows of
+  // a run of consecutive y rows arrive by TMA with the 128-byte swizzle, row i
+  // at i * 128 (the whole buffer head for a full item); the rows after a
+  // ragged run (its tail) follow at kTail, kYPitch apart; an item moved row
+  // by row has row i at i * kYPitch.
   static constexpr uint32_t kYHalf = kTok * 128;
-  static constexpr uint32_t kUnion = kStageAll > kYBuf * kYHalf ? kStageAll : kYBuf * kYHalf;
+  static constexpr uint32_t kTail = kYHalf;
+  static constexpr uint32_t kYBufBytes =
+      ((kTail + kMaxTail * kYPitch > kTok * kYPitch ? kTail + kMaxTail * kYPitch : kTok * kYPitch) +
+       1023) / 1024 * 1024;
+  static constexpr uint32_t kUnion = kYBuf * kYBufBytes;
   static constexpr uint32_t kStageOff = (kStage + 1023) / 1024 * 1024;
   static constexpr uint32_t kTotal = kStageOff + kUnion;
 };
 
 template <int R>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 2)
     sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
                           const __grid_constant__ CUtensorMap tm_y, const float* vpart, int ksplit,
                           const int32_t* perm, const int32_t* seg_slot, const int32_t* seg_off,
@@ -361,15 +366,77 @@ __global__ void __launch_bounds__(kThreads)
   const int j0 = blockIdx.y * kXGroup;
   const int nt = min(kXGroup, n_tiles_all - j0);
   if (nt <= 0) return;
-  // a full item whose tokens are consecutive rows of y (a prefill request):
-  // y moves by TMA, 64-column half-tiles, kYBuf buffers
-  const int row0 = perm_row(perm, p0, T, err);
-  const bool ytma = n_tok == kTok && perm_row(perm, p0 + kTok - 1, T, err) - row0 == kTok - 1;
-  auto issue_y = [&](int hj) {  // half-tile hj = 2 j + h into buffer hj % kYBuf
-    const int yb = hj % kYBuf;
-    ptx::mbar_arrive_expect_tx(&y_full[yb], Lay::kYHalf);
-    ptx::tma_load_2d(uni + yb * Lay::kYHalf, &tm_y, &y_full[yb],
-                     (j0 + (hj >> 1)) * kXN + 64 * (hj & 1), row0);
+  // y moves in 64-column half-tiles through kYBuf buffers, in one of three
+  // ways.  The tokens of an item sit in increasing row order, so the rows
+  // that are consecutive in y from its first one (a prefill request, or its
+  // last item) are a prefix of n_run rows.
+  //  - kFull (n_run = 128): each half-tile is one 128-row TMA box, loaded,
+  //    updated in place and stored back.
+  //  - kRun (n_run >= kMinRun, at most kMaxTail rows after it): the run
+  //    arrives as the same 128-row box (rows past it are read, never
+  //    written), every tail row by its own bulk copy.
+  //  - kRows (any other item): every row arrives by its own bulk copy,
+  //    issued by the epilogue thread that owns the row.
+  // In kRun and kRows each thread stores its own row from registers, so a
+  // buffer is free once it has been read and loads run three half-tiles
+  // ahead; in kFull the buffer is free once the TMA store has read it, and
+  // loads run two ahead.
+  enum { kFull, kRun, kRows };
+  const int row0 = perm_row_plain(perm, p0, T, err);
+  const int my_row = tid < n_tok ? perm_row_plain(perm, p0 + tid, T, err) : -1;
+  if (tid == 4 * 32) {
+    ptx::prefetch_tmap(&tm_b);
+    ptx::prefetch_tmap(&tm_y);
+    for (int i = 0; i < kBBuf; ++i) {
+      ptx::mbar_init(&b_full[i], 1);
+      ptx::mbar_init(&b_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&t_full[i], 1);
+      ptx::mbar_init(&t_empty[i], 4 * 32);
+    }
+    for (int i = 0; i < kYBuf; ++i) ptx::mbar_init(&y_full[i], 1);
+    *abort_f = 0;
+    ptx::fence_mbar_init();
+  }
+  // (also: the barriers are initialised before any copy counts on them)
+  const int n_run = __syncthreads_count(tid < n_tok && my_row - row0 == tid);
+  const int n_tail = n_tok - n_run;
+  const int mode = n_run == kTok ? kFull : (n_run >= kMinRun && n_tail <= kMaxTail ? kRun : kRows);
+  const bool tail_row = mode == kRun && tid >= n_run && tid < n_tok;
+
+  auto hcol = [&](int hj) { return (j0 + (hj >> 1)) * kXN + 64 * (hj & 1); };
+  auto ybuf = [&](int hj) { return uni + (hj % kYBuf) * Lay::kYBufBytes; };
+  // the bytes of one row inside half-tile hj moved by a bulk copy (columns
+  // past d_out are not moved; d_out is a multiple of 8, so this is a
+  // multiple of 16)
+  auto row_bytes = [&](int hj) {
+    const int c = d_out - hcol(hj);
+    return static_cast<uint32_t>(c <= 0 ? 0 : (c < 64 ? c : 64) * 2);
+  };
+  // one thread: the TMA part of half-tile hj and the byte count of its phase
+  // (bulk-copied rows may land before the count is set)
+  auto issue_y = [&](int hj) {
+    uint64_t* bar = &y_full[hj % kYBuf];
+    if (mode == kFull) {
+      ptx::mbar_arrive_expect_tx(bar, Lay::kYHalf);
+      ptx::tma_load_2d(ybuf(hj), &tm_y, bar, hcol(hj), row0);
+    } else if (mode == kRun) {
+      ptx::mbar_arrive_expect_tx(bar, Lay::kYHalf + static_cast<uint32_t>(n_tail) * row_bytes(hj));
+      ptx::tma_load_2d(ybuf(hj), &tm_y, bar, hcol(hj), row0);
+    } else {
+      ptx::mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n_tok) * row_bytes(hj));
+    }
+  };
+  // the epilogue thread of row tid: its own bulk copy of half-tile hj
+  auto issue_y_own = [&](int hj) {
+    const uint32_t nb = row_bytes(hj);
+    if (nb == 0) return;
+    uint8_t* dst = nullptr;
+    if (mode == kRows && tid < n_tok) dst = ybuf(hj) + tid * kYPitch;
+    if (tail_row) dst = ybuf(hj) + Lay::kTail + (tid - n_run) * kYPitch;
+    if (dst)
+      ptx::bulk_load(dst, y + static_cast<size_t>(my_row) * d_out + hcol(hj), nb, &y_full[hj % kYBuf]);
   };
 
   auto issue_b = [&](int j) {  // B[a][:, tile j] into buffer j % kBBuf
@@ -382,36 +449,26 @@ __global__ void __launch_bounds__(kThreads)
   };
   if (warp == 4) {
     if (lane == 0) {
-      ptx::prefetch_tmap(&tm_b);
-      for (int i = 0; i < kBBuf; ++i) {
-        ptx::mbar_init(&b_full[i], 1);
-        ptx::mbar_init(&b_empty[i], 1);
-      }
-      for (int i = 0; i < 2; ++i) {
-        ptx::mbar_init(&t_full[i], 1);
-        ptx::mbar_init(&t_empty[i], 4 * 32);
-      }
-      for (int i = 0; i < kYBuf; ++i) ptx::mbar_init(&y_full[i], 1);
-      *abort_f = 0;
-      ptx::fence_mbar_init();
       for (int j = 0; j < kBBuf && j < nt; ++j) issue_b(j);
-      if (ytma) {
-        ptx::prefetch_tmap(&tm_y);
+      if (mode != kRows)
         for (int hj = 0; hj < kYBuf && hj < 2 * nt; ++hj) issue_y(hj);
-      }
     }
     __syncwarp();
     ptx::tmem_alloc(tmem_slot, 2 * kXN);
     ptx::tmem_relinquish();
     ptx::tc_fence_before();
   } else {
+    for (int hj = 0; hj < kYBuf && hj < 2 * nt; ++hj) {
+      if (mode == kRows && tid == 0) issue_y(hj);
+      issue_y_own(hj);
+    }
     // V tile: row i = token perm[p0 + i]; v summed over the d_in splits,
     // split into bf16 hi + lo, written K-major with the 128-byte swizzle
     // (plain loads: this kernel is not launched early, so stream order makes
     // v visible, and the compiler may batch them)
     const int i = tid;
     if (i < n_tok) {
-      const int tok = perm_row_plain(perm, p0 + i, T, err);
+      const int tok = my_row;
 #pragma unroll 2
       for (int q0 = 0; q0 < R; q0 += 8) {
         float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -472,19 +529,27 @@ __global__ void __launch_bounds__(kThreads)
       }
     }
     __syncwarp();
-  } else if (ytma) {
-    // ---------------- epilogue, y by TMA: y half-tile += accumulator ------
-    // TMEM lane = token row i of the tile = row row0 + i of y.  Half-tile hj
-    // (64 columns) sits in buffer hj % kYBuf as 128 rows of 128 bytes with
-    // the 128-byte swizzle: thread i adds its accumulator row in place (the
-    // 32 rows of a warp spread over all banks), then one thread stores the
-    // half-tile with TMA.  It does not wait for that store: once the store
-    // before it has read its buffer (at most kYBuf - 2 stores still reading),
-    // that buffer takes the load of half-tile hj + 2, so every load is issued
-    // two half-tiles ahead.  Every epilogue thread passes the same named
-    // barriers, aborted or not.
+  } else {
+    // ---------------- epilogue: y half-tiles += accumulator rows -----------
+    // TMEM lane = token row i of the tile; thread i reads its row of each
+    // half-tile from the buffer and adds its accumulator row.  kFull writes
+    // the sum back in place for one TMA store of the half-tile; the other
+    // modes store the row straight from registers (16 bytes per store), so
+    // their buffer is free once every thread has read its row.  Every
+    // epilogue thread passes the same waits and named barriers, aborted or
+    // not; the barrier that ends a half-tile keeps the four warps within one
+    // half-tile of each other, so no buffer's phase can complete twice before
+    // every thread has waited on it.
     const int i = warp * 32 + lane;
+    const bool own = i < n_tok;
     const uint32_t tq = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    bf16* const yrow = own ? y + static_cast<size_t>(my_row) * d_out : nullptr;
+    // this thread's row of a buffer: swizzled rows of a TMA box, else
+    // kYPitch-apart rows of bulk copies
+    const bool swz = mode == kFull || (mode == kRun && i < n_run);
+    const uint32_t row_off = swz ? static_cast<uint32_t>(i) * 128
+                           : (mode == kRun ? Lay::kTail + static_cast<uint32_t>(i - n_run) * kYPitch
+                                           : static_cast<uint32_t>(i) * kYPitch);
     bool ok = true;
     for (int j = 0; j < nt; ++j) {
       const int bs = j & 1;
@@ -495,8 +560,10 @@ __global__ void __launch_bounds__(kThreads)
       for (int h = 0; h < kXN / 64; ++h) {
         const int hj = 2 * j + h;
         ok = ok && warp_wait(&y_full[hj % kYBuf], static_cast<uint32_t>(hj / kYBuf) & 1u, abort_f);
-        uint8_t* yb = uni + (hj % kYBuf) * Lay::kYHalf + i * 128;
-        if (ok) {
+        uint8_t* const buf = ybuf(hj);
+        uint8_t* const yb = buf + row_off;
+        if (ok && mode == kFull) {
+          // in place, 32 columns at a time, for the TMA store
 #pragma unroll
           for (int c0 = 0; c0 < 64; c0 += 32) {
             uint32_t v[32];
@@ -506,8 +573,7 @@ __global__ void __launch_bounds__(kThreads)
             ptx::tmem_ld_wait();
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              const int ch = (c0 >> 3) + q;  // 16-byte chunk of the 128-byte row
-              uint4* p = reinterpret_cast<uint4*>(yb + ((ch ^ (i & 7)) << 4));
+              uint4* p = reinterpret_cast<uint4*>(yb + ((((c0 >> 3) + q) ^ (i & 7)) << 4));
               const uint4 w = *p;
               const uint32_t u[4] = {w.x, w.y, w.z, w.w};
               float f[8];
@@ -519,76 +585,65 @@ __global__ void __launch_bounds__(kThreads)
               *p = pack8_bf16(f);
             }
           }
-          ptx::fence_proxy_async_smem();
-        }
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        if (i == 0 && ok && !*abort_f) {
-          ptx::tma_store_2d(&tm_y, uni + (hj % kYBuf) * Lay::kYHalf,
-                            (j0 + j) * kXN + 64 * h, row0);
-          ptx::bulk_commit_group();
-          // the store of half-tile hj + 2 - kYBuf has read its buffer
-          ptx::bulk_wait_group_read<kYBuf - 2>();
-          if (hj + 2 >= kYBuf && hj + 2 < 2 * nt) issue_y(hj + 2);
-        }
-      }
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(&t_empty[bs]);
-    }
-    if (i == 0) ptx::bulk_wait_group_read_all();  // the buffers outlive every store
-  } else {
-    // ---------------- epilogue: y rows += accumulator rows ----------------
-    // TMEM lane = token row of the tile.  Each warp stages its 32 rows x 64
-    // columns of the accumulator in shared memory, then walks the rows: one
-    // warp instruction reads (and writes) 128 contiguous bytes of one y row,
-    // instead of 16 bytes of 32 different rows.
-    const int n_rows = min(32, n_tok - warp * 32);  // this warp's token rows
-    bf16* yrow = n_rows > lane ? y + static_cast<size_t>(perm_row(perm, p0 + warp * 32 + lane, T, err)) * d_out
-                               : nullptr;
-    float* stg = reinterpret_cast<float*>(uni + warp * Lay::kStageWarp);
-    const uint32_t tq = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    for (int j = 0; j < nt; ++j) {
-      const int bs = j & 1;
-      const uint32_t ph = static_cast<uint32_t>(j >> 1) & 1u;
-      if (!warp_wait(&t_full[bs], ph, abort_f)) break;
-      ptx::tc_fence_after();
-#pragma unroll 1
-      for (int h = 0; h < kXN / 64; ++h) {
-        const int nc = (j0 + j) * kXN + h * 64 + 2 * lane;  // this lane's column pair
-        // the accumulator's 64 columns of every row of the warp, to shared memory
+        } else if (ok && warp * 32 < n_tok) {  // uniform over the warp
+          // 32 columns at a time: the row's chunks read, then the sums
+          // stored from registers
+          const int col = hcol(hj);
 #pragma unroll
-        for (int c0 = 0; c0 < 64; c0 += 32) {
-          uint32_t v[32];
-          ptx::tmem_ld16(tq + bs * kXN + h * 64 + c0, *reinterpret_cast<uint32_t(*)[16]>(v));
-          ptx::tmem_ld16(tq + bs * kXN + h * 64 + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
-          ptx::tmem_ld_wait();
+          for (int c0 = 0; c0 < 64; c0 += 32) {
+            uint4 yv[4];
+            if (own) {
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            *reinterpret_cast<float4*>(stg + lane * Lay::kStLd + c0 + 4 * q) =
-                make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                            __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
-        }
-        __syncwarp();
-        // row by row: every load first, then the sums and stores
-        uint32_t yv[32];
+              for (int q = 0; q < 4; ++q) {
+                const int ch = (c0 >> 3) + q;
+                yv[q] = *reinterpret_cast<const uint4*>(yb + ((swz ? ch ^ (i & 7) : ch) << 4));
+              }
+            }
+            uint32_t v[32];
+            ptx::tmem_ld16(tq + bs * kXN + h * 64 + c0, *reinterpret_cast<uint32_t(*)[16]>(v));
+            ptx::tmem_ld16(tq + bs * kXN + h * 64 + c0 + 16,
+                           *reinterpret_cast<uint32_t(*)[16]>(v + 16));
+            ptx::tmem_ld_wait();
+            if (own) {
 #pragma unroll
-        for (int r = 0; r < 32; ++r) {
-          bf16* yr = reinterpret_cast<bf16*>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(yrow), r));
-          if (r < n_rows && nc < d_out) yv[r] = *reinterpret_cast<const uint32_t*>(yr + nc);
-        }
+              for (int q = 0; q < 4; ++q) {
+                const uint32_t u[4] = {yv[q].x, yv[q].y, yv[q].z, yv[q].w};
+                float f[8];
 #pragma unroll
-        for (int r = 0; r < 32; ++r) {
-          bf16* yr = reinterpret_cast<bf16*>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(yrow), r));
-          if (r < n_rows && nc < d_out) {
-            const float2 a = *reinterpret_cast<const float2*>(stg + r * Lay::kStLd + 2 * lane);
-            *reinterpret_cast<uint32_t*>(yr + nc) =
-                pack_bf16x2(bf16_lo(yv[r]) + a.x, bf16_hi(yv[r]) + a.y);
+                for (int e = 0; e < 4; ++e) {
+                  f[2 * e] = bf16_lo(u[e]) + __uint_as_float(v[8 * q + 2 * e]);
+                  f[2 * e + 1] = bf16_hi(u[e]) + __uint_as_float(v[8 * q + 2 * e + 1]);
+                }
+                if (col + c0 + 8 * q < d_out)  // d_out is a multiple of 8
+                  *reinterpret_cast<uint4*>(yrow + col + c0 + 8 * q) = pack8_bf16(f);
+              }
+            }
           }
         }
-        __syncwarp();
+        if (mode == kFull) {
+          // one thread stores the half-tile; once the store before it has
+          // read its buffer, that buffer takes the load of half-tile hj + 2
+          if (ok) ptx::fence_proxy_async_smem();
+          asm volatile("bar.sync 1, 128;" ::: "memory");
+          if (i == 0 && ok && !*abort_f) {
+            ptx::tma_store_2d(&tm_y, buf, hcol(hj), row0);
+            ptx::bulk_commit_group();
+            ptx::bulk_wait_group_read<kYBuf - 2>();
+            if (hj + 2 >= kYBuf && hj + 2 < 2 * nt) issue_y(hj + 2);
+          }
+        } else {
+          // every row of the buffer has been read: it takes half-tile hj + kYBuf
+          asm volatile("bar.sync 1, 128;" ::: "memory");
+          if (ok && hj + kYBuf < 2 * nt) {
+            if (i == 0) issue_y(hj + kYBuf);
+            issue_y_own(hj + kYBuf);
+          }
+        }
       }
       ptx::tc_fence_before();
       ptx::mbar_arrive(&t_empty[bs]);
     }
+    if (mode == kFull && i == 0) ptx::bulk_wait_group_read_all();  // buffers outlive stores
   }
   ptx::tc_fence_before();
   __syncthreads();

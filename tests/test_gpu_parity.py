@@ -151,6 +151,76 @@ def test_expand_matches_oracle(L, case, form):
         check_close(got - y0, delta_ref, f"{form} expand delta")
 
 
+# SGMV expand items whose token rows are not consecutive in y (every token its
+# own adapter draw): full 128-token items and ragged ones move y row by row
+SCATTERED_EXPAND_CASES = [(600, 264, 64, 3), (1000, 1032, 64, 5), (300, 520, 128, 2),
+                          (160, 136, 64, 1)]
+
+
+@pytest.mark.parametrize("T,d_out,r,n_slots", SCATTERED_EXPAND_CASES,
+                         ids=[str(c) for c in SCATTERED_EXPAND_CASES])
+def test_sgmv_expand_scattered_rows(L, T, d_out, r, n_slots):
+    torch = torch_mod()
+    w = W.random_case(31 + T, T, 64, d_out, r, n_slots, runs=False)
+    d = DeviceCase(w)
+    ws = _ws(L)
+    vp = _v_input(T, r, 2, 3)
+    y0 = W.bf16_round((np.random.default_rng([7002, T]).standard_normal((T, d_out)) * 0.1)
+                      .astype(np.float32))
+    y = dev(y0, "bf16")
+    segs = L.build_segments_t(d.ids, n_slots, ws)
+    L.sgmv_expand_t(dev(vp, "f32"), d.B, segs, y, ws)
+    torch.cuda.synchronize()
+    got = host(y)
+    check_close(got, y0 + O.expand(vp.astype(np.float64).sum(axis=0), w.B_pool, w.slot_ids),
+                "scattered SGMV expand y")
+    base_rows = ~((w.slot_ids >= 0) & (w.slot_ids < n_slots))
+    np.testing.assert_array_equal(got[base_rows], y0[base_rows].astype(np.float64))
+    assert L.get_error_t(ws) == 0
+
+
+def _run_tail_ids(T, layout, seed):
+    """Slot ids with, per slot, a run of consecutive rows and a number of
+    scattered rows after it: layout = [(slot, run start, run length, n
+    scattered)]; every other row is base-only."""
+    rng = np.random.default_rng([7003, seed])
+    ids = np.full(T, -1, np.int32)
+    for slot, start, n_run, _ in layout:
+        ids[start:start + n_run] = slot
+    for slot, start, n_run, n_sc in layout:
+        free = np.flatnonzero(ids[start + n_run:] == -1) + start + n_run
+        ids[rng.choice(free, size=n_sc, replace=False)] = slot
+    return ids
+
+
+# SGMV expand items that start with a run of consecutive rows and end with
+# scattered ones (a prefill request's last item joined by decode tokens of
+# the same adapter): runs of 22 / 100 rows with 16 / 1 later rows move the
+# run by TMA; 17 later rows, or a run shorter than 16, move row by row
+RUN_TAIL_LAYOUT = [(0, 0, 150, 16), (1, 160, 40, 17), (2, 210, 15, 3), (3, 240, 100, 1)]
+
+
+@pytest.mark.parametrize("d_out,r", [(264, 64), (1032, 128)])
+def test_sgmv_expand_run_and_tail_items(L, d_out, r):
+    torch = torch_mod()
+    T, n_slots = 700, 4
+    ids = _run_tail_ids(T, RUN_TAIL_LAYOUT, d_out)
+    rng = np.random.default_rng([7004, d_out])
+    B = W.bf16_round((rng.standard_normal((n_slots, r, d_out)) * 0.02).astype(np.float32))
+    vp = _v_input(T, r, 2, 4)
+    y0 = W.bf16_round((rng.standard_normal((T, d_out)) * 0.1).astype(np.float32))
+    y = dev(y0, "bf16")
+    ws = _ws(L)
+    segs = L.build_segments_t(dev(ids), n_slots, ws)
+    L.sgmv_expand_t(dev(vp, "f32"), dev(B, "bf16"), segs, y, ws)
+    torch.cuda.synchronize()
+    got = host(y)
+    check_close(got, y0 + O.expand(vp.astype(np.float64).sum(axis=0), B, ids),
+                "run + tail SGMV expand y")
+    np.testing.assert_array_equal(got[ids < 0], y0[ids < 0].astype(np.float64))
+    assert L.get_error_t(ws) == 0
+
+
 # ------------------------------------------------------------ fused layer
 FUSED_CASES = [
     # T, d_in, d_out, r, n_slots : decode tiles (T <= 256) and prefill tiles
