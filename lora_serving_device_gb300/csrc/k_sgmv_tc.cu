@@ -465,30 +465,54 @@ __global__ void __launch_bounds__(kThreads, 2)
     // V tile: row i = token perm[p0 + i]; v summed over the d_in splits,
     // split into bf16 hi + lo, written K-major with the 128-byte swizzle
     // (plain loads: this kernel is not launched early, so stream order makes
-    // v visible, and the compiler may batch them)
+    // v visible).
+    // Each thread reads 32 values of its row from two splits at once (16
+    // loads in flight), adding the splits in order.
     const int i = tid;
     if (i < n_tok) {
-      const int tok = my_row;
-#pragma unroll 2
-      for (int q0 = 0; q0 < R; q0 += 8) {
-        float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        for (int sp = 0; sp < ksplit; ++sp) {
-          const float4* vp =
-              reinterpret_cast<const float4*>(vpart + (static_cast<size_t>(sp) * T + tok) * R + q0);
-          const float4 u0 = vp[0], u1 = vp[1];
-          f[0] += u0.x; f[1] += u0.y; f[2] += u0.z; f[3] += u0.w;
-          f[4] += u1.x; f[5] += u1.y; f[6] += u1.z; f[7] += u1.w;
-        }
-        float hi[8], lo[8];
+      const float* vrow = vpart + static_cast<size_t>(my_row) * R;
+      const size_t split = static_cast<size_t>(T) * R;
+#pragma unroll 1
+      for (int q0 = 0; q0 < R; q0 += 32) {
+        float f[32];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          hi[q] = __bfloat162float(__float2bfloat16_rn(f[q]));
-          lo[q] = f[q] - hi[q];
+        for (int k = 0; k < 32; ++k) f[k] = 0.f;
+        for (int sp = 0; sp < ksplit; sp += 2) {
+          const bool two = sp + 1 < ksplit;
+          const float4* a = reinterpret_cast<const float4*>(vrow + sp * split + q0);
+          float4 u[8], w[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) u[k] = a[k];
+          if (two) {
+            const float4* b = reinterpret_cast<const float4*>(vrow + (sp + 1) * split + q0);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) w[k] = b[k];
+          }
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            f[4 * k] += u[k].x; f[4 * k + 1] += u[k].y; f[4 * k + 2] += u[k].z; f[4 * k + 3] += u[k].w;
+          }
+          if (two) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              f[4 * k] += w[k].x; f[4 * k + 1] += w[k].y; f[4 * k + 2] += w[k].z; f[4 * k + 3] += w[k].w;
+            }
+          }
         }
-        const int kb = q0 >> 6, ch = (q0 >> 3) & 7;
-        const uint32_t off = i * 128 + ((ch ^ (i & 7)) << 4);
-        *reinterpret_cast<uint4*>(smem + kb * Lay::kVBlk + off) = pack8_bf16(hi);
-        *reinterpret_cast<uint4*>(smem + (Lay::KB + kb) * Lay::kVBlk + off) = pack8_bf16(lo);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float hi[8], lo[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            hi[q] = __bfloat162float(__float2bfloat16_rn(f[8 * c + q]));
+            lo[q] = f[8 * c + q] - hi[q];
+          }
+          const int q8 = q0 + 8 * c;
+          const int kb = q8 >> 6, ch = (q8 >> 3) & 7;
+          const uint32_t off = i * 128 + ((ch ^ (i & 7)) << 4);
+          *reinterpret_cast<uint4*>(smem + kb * Lay::kVBlk + off) = pack8_bf16(hi);
+          *reinterpret_cast<uint4*>(smem + (Lay::KB + kb) * Lay::kVBlk + off) = pack8_bf16(lo);
+        }
       }
     }
     ptx::fence_proxy_async_smem();
