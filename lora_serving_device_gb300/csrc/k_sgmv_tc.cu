@@ -300,39 +300,48 @@ cudaError_t launch_r(const CUtensorMap& tm, const CUtensorMap& tm_x, const bf16*
 }
 
 // ------------------------------------------------------------ expand
-constexpr int kXN = 128;      // d_out columns per tile (the MMA's N)
-constexpr int kXGroup = 8;    // d_out tiles per CTA
-constexpr int kBBuf = 1;      // B[a] tile buffers
-constexpr int kYBuf = 3;      // y half-tile buffers
+// y[rows of an item, the CTA's columns] += V B[a], V = the item's v rows
+// summed over the d_in splits.  V sits in tensor memory as the MMAs' A
+// operand, as bf16 hi + lo halves (hi = v rounded to bf16, lo = the rest
+// rounded), so the product keeps v's fp32 precision.  The CTA walks its
+// column tiles in 64-column half-tiles: one group of MMAs (N = 64) per
+// half-tile into one of two 64-column accumulators, B[a] through a ring of
+// half-tile boxes, y through kYBuf half-tile buffers.
+constexpr int kXN = 128;      // d_out columns per tile
+constexpr int kXGroup = 8;    // d_out tiles per CTA (16 half-tiles)
+constexpr int kYBuf = 4;      // y half-tile buffers
 constexpr int kYPitch = 144;  // bytes per token row moved by its own bulk copy
 constexpr int kMinRun = 16;   // shortest run of consecutive rows moved by TMA
 constexpr int kMaxTail = 16;  // most rows after such a run
+constexpr uint32_t kAccCols = 64;  // one accumulator: 64 fp32 columns
 
 template <int R>
 struct ExpandLayout {
-  static constexpr int KB = R / 64;                          // 64-wide K blocks of v
-  static constexpr uint32_t kVBlk = kTok * 128;              // one K block, K-major SW128
-  static constexpr uint32_t kV = 2 * KB * kVBlk;             // hi blocks, then lo blocks
-  static constexpr uint32_t kBBox = R * 128;                 // 64 columns x R rows
-  static constexpr uint32_t kB = (kXN / 64) * kBBox;
-  static constexpr uint32_t kBars = kV + kBBuf * kB;
-  // b_full[kBBuf], b_empty[kBBuf], t_full[2], t_empty[2], y_full[kYBuf],
-  // TMEM slot, abort
-  static constexpr int kNBar = 2 * kBBuf + 4 + kYBuf;
-  static constexpr uint32_t kStage = kBars + kNBar * 8 + 16;
-  // kYBuf buffers of one y half-tile (128 token rows x 64 columns).  Rows of
-  // a run of consecutive y rows arrive by TMA with the 128-byte swizzle, row i
-  // at i * 128 (the whole buffer head for a full item); the rows after a
-  // ragged run (its tail) follow at kTail, kYPitch apart; an item moved row
-  // by row has row i at i * kYPitch.
+  // B[a] ring: half-tile boxes of 64 columns x R rows (128-byte swizzle);
+  // two CTAs per SM fit with three rank-64 boxes or two rank-128 ones
+  static constexpr int kBRing = R == 64 ? 3 : 2;
+  static constexpr uint32_t kBBox = R * 128;
+  // y buffers of one half-tile (128 token rows x 64 columns).  Rows of a run
+  // of consecutive y rows arrive by TMA with the 128-byte swizzle, row i at
+  // i * 128 (the whole buffer head for a full item); the rows after a ragged
+  // run (its tail) follow at kTail, kYPitch apart; an item moved row by row
+  // has row i at i * kYPitch.
   static constexpr uint32_t kYHalf = kTok * 128;
   static constexpr uint32_t kTail = kYHalf;
   static constexpr uint32_t kYBufBytes =
       ((kTail + kMaxTail * kYPitch > kTok * kYPitch ? kTail + kMaxTail * kYPitch : kTok * kYPitch) +
        1023) / 1024 * 1024;
-  static constexpr uint32_t kUnion = kYBuf * kYBufBytes;
-  static constexpr uint32_t kStageOff = (kStage + 1023) / 1024 * 1024;
-  static constexpr uint32_t kTotal = kStageOff + kUnion;
+  static constexpr uint32_t kYOff = kBRing * kBBox;  // a multiple of 1024
+  static constexpr uint32_t kBars = kYOff + kYBuf * kYBufBytes;
+  // b_full[kBRing], b_empty[kBRing], t_full[2], t_empty[2], y_full[kYBuf],
+  // TMEM slot, abort
+  static constexpr int kNBar = 2 * kBRing + 4 + kYBuf;
+  static constexpr uint32_t kTotal = kBars + kNBar * 8 + 16;
+  // tensor memory: the two accumulators, then V hi (R / 2 columns of bf16
+  // pairs) and V lo
+  static constexpr uint32_t kVCol = 2 * kAccCols;
+  static constexpr uint32_t kTmemCols = 256;
+  static_assert(kVCol + R <= kTmemCols, "tensor memory");
 };
 
 template <int R>
@@ -342,20 +351,21 @@ __global__ void __launch_bounds__(kThreads, 2)
                           const int32_t* perm, const int32_t* seg_slot, const int32_t* seg_off,
                           const int32_t* n_seg, bf16* y, int T, int d_out, uint32_t* err) {
   using Lay = ExpandLayout<R>;
-  constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(128, kXN, false, true);
+  constexpr int kBRing = Lay::kBRing;
+  constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(128, 64, false, true);
   __shared__ int s_a, s_p0, s_p1;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint64_t* b_full = reinterpret_cast<uint64_t*>(smem + Lay::kBars);
-  uint64_t* b_empty = b_full + kBBuf;
-  uint64_t* t_full = b_empty + kBBuf;
+  uint64_t* b_empty = b_full + kBRing;
+  uint64_t* t_full = b_empty + kBRing;
   uint64_t* t_empty = t_full + 2;
   uint64_t* y_full = t_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(y_full + kYBuf);
   volatile int* abort_f = reinterpret_cast<volatile int*>(y_full + kYBuf) + 1;
-  uint8_t* uni = smem + Lay::kStageOff;
+  uint8_t* ybase = smem + Lay::kYOff;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   sgmv_item<kTok>(blockIdx.x, seg_slot, seg_off, ld_dep(n_seg), &s_a, &s_p0, &s_p1);
@@ -366,10 +376,12 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int j0 = blockIdx.y * kXGroup;
   const int nt = min(kXGroup, n_tiles_all - j0);
   if (nt <= 0) return;
-  // y moves in 64-column half-tiles through kYBuf buffers, in one of three
-  // ways.  The tokens of an item sit in increasing row order, so the rows
-  // that are consecutive in y from its first one (a prefill request, or its
-  // last item) are a prefix of n_run rows.
+  const int n_half = 2 * nt;  // half-tiles of this CTA
+
+  // y moves in half-tiles in one of three ways.  The tokens of an item sit in
+  // increasing row order, so the rows that are consecutive in y from its
+  // first one (a prefill request, or its last item) are a prefix of n_run
+  // rows.
   //  - kFull (n_run = 128): each half-tile is one 128-row TMA box, loaded,
   //    updated in place and stored back.
   //  - kRun (n_run >= kMinRun, at most kMaxTail rows after it): the run
@@ -378,16 +390,16 @@ __global__ void __launch_bounds__(kThreads, 2)
   //  - kRows (any other item): every row arrives by its own bulk copy,
   //    issued by the epilogue thread that owns the row.
   // In kRun and kRows each thread stores its own row from registers, so a
-  // buffer is free once it has been read and loads run three half-tiles
-  // ahead; in kFull the buffer is free once the TMA store has read it, and
-  // loads run two ahead.
+  // buffer is free once it has been read and loads run kYBuf half-tiles
+  // ahead; in kFull a buffer is free once the TMA store has read it, and
+  // loads run kYBuf - 1 ahead.
   enum { kFull, kRun, kRows };
   const int row0 = perm_row_plain(perm, p0, T, err);
   const int my_row = tid < n_tok ? perm_row_plain(perm, p0 + tid, T, err) : -1;
   if (tid == 4 * 32) {
     ptx::prefetch_tmap(&tm_b);
     ptx::prefetch_tmap(&tm_y);
-    for (int i = 0; i < kBBuf; ++i) {
+    for (int i = 0; i < kBRing; ++i) {
       ptx::mbar_init(&b_full[i], 1);
       ptx::mbar_init(&b_empty[i], 1);
     }
@@ -399,14 +411,22 @@ __global__ void __launch_bounds__(kThreads, 2)
     *abort_f = 0;
     ptx::fence_mbar_init();
   }
-  // (also: the barriers are initialised before any copy counts on them)
+  if (warp == 4) {
+    __syncwarp();
+    ptx::tmem_alloc(tmem_slot, Lay::kTmemCols);
+    ptx::tmem_relinquish();
+    ptx::tc_fence_before();
+  }
+  // (also: the barriers are initialised and tensor memory is allocated)
   const int n_run = __syncthreads_count(tid < n_tok && my_row - row0 == tid);
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
   const int n_tail = n_tok - n_run;
   const int mode = n_run == kTok ? kFull : (n_run >= kMinRun && n_tail <= kMaxTail ? kRun : kRows);
   const bool tail_row = mode == kRun && tid >= n_run && tid < n_tok;
 
-  auto hcol = [&](int hj) { return (j0 + (hj >> 1)) * kXN + 64 * (hj & 1); };
-  auto ybuf = [&](int hj) { return uni + (hj % kYBuf) * Lay::kYBufBytes; };
+  auto hcol = [&](int hj) { return j0 * kXN + 64 * hj; };
+  auto ybuf = [&](int hj) { return ybase + (hj % kYBuf) * Lay::kYBufBytes; };
   // the bytes of one row inside half-tile hj moved by a bulk copy (columns
   // past d_out are not moved; d_out is a multiple of 8, so this is a
   // multiple of 16)
@@ -438,55 +458,52 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (dst)
       ptx::bulk_load(dst, y + static_cast<size_t>(my_row) * d_out + hcol(hj), nb, &y_full[hj % kYBuf]);
   };
-
-  auto issue_b = [&](int j) {  // B[a][:, tile j] into buffer j % kBBuf
-    const int bs = j % kBBuf;
-    ptx::mbar_arrive_expect_tx(&b_full[bs], Lay::kB);
-#pragma unroll
-    for (int h = 0; h < kXN / 64; ++h)
-      ptx::tma_load_3d(smem + Lay::kV + bs * Lay::kB + h * Lay::kBBox, &tm_b, &b_full[bs],
-                       (j0 + j) * kXN + 64 * h, 0, a);
+  // B[a][:, half-tile hj] into ring slot hj % kBRing
+  auto issue_b = [&](int hj) {
+    const int bs = hj % kBRing;
+    ptx::mbar_arrive_expect_tx(&b_full[bs], Lay::kBBox);
+    ptx::tma_load_3d(smem + bs * Lay::kBBox, &tm_b, &b_full[bs], hcol(hj), 0, a);
   };
+
   if (warp == 4) {
     if (lane == 0) {
-      for (int j = 0; j < kBBuf && j < nt; ++j) issue_b(j);
+      for (int hj = 0; hj < kBRing && hj < n_half; ++hj) issue_b(hj);
       if (mode != kRows)
-        for (int hj = 0; hj < kYBuf && hj < 2 * nt; ++hj) issue_y(hj);
+        for (int hj = 0; hj < kYBuf && hj < n_half; ++hj) issue_y(hj);
     }
     __syncwarp();
-    ptx::tmem_alloc(tmem_slot, 2 * kXN);
-    ptx::tmem_relinquish();
-    ptx::tc_fence_before();
   } else {
-    for (int hj = 0; hj < kYBuf && hj < 2 * nt; ++hj) {
+    for (int hj = 0; hj < kYBuf && hj < n_half; ++hj) {
       if (mode == kRows && tid == 0) issue_y(hj);
       issue_y_own(hj);
     }
-    // V tile: row i = token perm[p0 + i]; v summed over the d_in splits,
-    // split into bf16 hi + lo, written K-major with the 128-byte swizzle
-    // (plain loads: this kernel is not launched early, so stream order makes
-    // v visible).
-    // Each thread reads 32 values of its row from two splits at once (16
-    // loads in flight), adding the splits in order.
-    const int i = tid;
-    if (i < n_tok) {
-      const float* vrow = vpart + static_cast<size_t>(my_row) * R;
+    // V rows into tensor memory: row i = token perm[p0 + i], summed over the
+    // d_in splits in order (32 values of two splits per round of loads),
+    // split into bf16 hi + lo, two K elements per 32-bit column.  The store
+    // is collective over the warp: a warp with any row stores all 32 lanes
+    // (rows past the item hold zeros; their accumulator rows are never read).
+    // Plain loads: this kernel is not launched early, so stream order makes
+    // v visible.
+    if (warp * 32 < n_tok) {  // uniform over the warp
+      const bool own = tid < n_tok;
+      const float* vrow = vpart + static_cast<size_t>(own ? my_row : 0) * R;
       const size_t split = static_cast<size_t>(T) * R;
+      const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16) + Lay::kVCol;
 #pragma unroll 1
       for (int q0 = 0; q0 < R; q0 += 32) {
         float f[32];
 #pragma unroll
         for (int k = 0; k < 32; ++k) f[k] = 0.f;
-        for (int sp = 0; sp < ksplit; sp += 2) {
+        for (int sp = 0; own && sp < ksplit; sp += 2) {
           const bool two = sp + 1 < ksplit;
-          const float4* a = reinterpret_cast<const float4*>(vrow + sp * split + q0);
+          const float4* pa = reinterpret_cast<const float4*>(vrow + sp * split + q0);
           float4 u[8], w[8];
 #pragma unroll
-          for (int k = 0; k < 8; ++k) u[k] = a[k];
+          for (int k = 0; k < 8; ++k) u[k] = pa[k];
           if (two) {
-            const float4* b = reinterpret_cast<const float4*>(vrow + (sp + 1) * split + q0);
+            const float4* pb = reinterpret_cast<const float4*>(vrow + (sp + 1) * split + q0);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) w[k] = b[k];
+            for (int k = 0; k < 8; ++k) w[k] = pb[k];
           }
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
@@ -499,56 +516,52 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
           }
         }
+        uint32_t hp[16], lp[16];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float hi[8], lo[8];
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            hi[q] = __bfloat162float(__float2bfloat16_rn(f[8 * c + q]));
-            lo[q] = f[8 * c + q] - hi[q];
-          }
-          const int q8 = q0 + 8 * c;
-          const int kb = q8 >> 6, ch = (q8 >> 3) & 7;
-          const uint32_t off = i * 128 + ((ch ^ (i & 7)) << 4);
-          *reinterpret_cast<uint4*>(smem + kb * Lay::kVBlk + off) = pack8_bf16(hi);
-          *reinterpret_cast<uint4*>(smem + (Lay::KB + kb) * Lay::kVBlk + off) = pack8_bf16(lo);
+        for (int m = 0; m < 16; ++m) {
+          const float h0 = __bfloat162float(__float2bfloat16_rn(f[2 * m]));
+          const float h1 = __bfloat162float(__float2bfloat16_rn(f[2 * m + 1]));
+          hp[m] = pack_bf16x2(h0, h1);
+          lp[m] = pack_bf16x2(f[2 * m] - h0, f[2 * m + 1] - h1);
         }
+        ptx::tmem_st16(lane_base + q0 / 2, hp);
+        ptx::tmem_st16(lane_base + R / 2 + q0 / 2, lp);
       }
+      ptx::tmem_st_wait();
     }
-    ptx::fence_proxy_async_smem();
+    ptx::tc_fence_before();
   }
   __syncthreads();
   ptx::tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
 
   if (warp == 4) {
     // ---------------- MMA issuer (and B loads) ----------------------------
     if (lane == 0) {
-      const uint32_t vbase = ptx::smem_u32(smem);
-      for (int j = 0; j < nt; ++j) {
-        const int bs = j % kBBuf, ts = j & 1;  // B buffer, TMEM accumulator
-        const uint32_t bph = static_cast<uint32_t>(j / kBBuf) & 1u;
-        const uint32_t tph = static_cast<uint32_t>(j >> 1) & 1u;
+      for (int hj = 0; hj < n_half; ++hj) {
+        const int bs = hj % kBRing, ts = hj & 1;  // B slot, accumulator
+        const uint32_t bph = static_cast<uint32_t>(hj / kBRing) & 1u;
+        const uint32_t tph = static_cast<uint32_t>(hj >> 1) & 1u;
         if (!ptx::mbar_wait_bounded(&b_full[bs], bph, abort_f, kWaitLimitNs)) break;
         if (!ptx::mbar_wait_bounded(&t_empty[ts], tph ^ 1u, abort_f, kWaitLimitNs)) break;
         ptx::tc_fence_after();
-        const uint32_t bb = ptx::smem_u32(smem + Lay::kV + bs * Lay::kB);
-        const uint32_t acc = tmem + static_cast<uint32_t>(ts * kXN);
+        const uint32_t bb = ptx::smem_u32(smem + bs * Lay::kBBox);
+        const uint32_t acc = tmem + static_cast<uint32_t>(ts) * kAccCols;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
 #pragma unroll
           for (int kk = 0; kk < R / 16; ++kk) {
-            const uint64_t vd = ptx::sdesc_sw128(
-                vbase + (half * Lay::KB + (kk >> 2)) * Lay::kVBlk + (kk & 3) * 32, 16, 1024);
+            // A: V hi or lo, 16 K elements = 8 columns per step; B: MN-major,
+            // 16 K rows = 2048 bytes per step
+            const uint32_t va = tmem + Lay::kVCol + half * (R / 2) + kk * 8;
             const uint64_t bd = ptx::sdesc_sw128(bb + kk * 2048, Lay::kBBox, 1024);
-            ptx::mma_bf16(acc, vd, bd, kIdesc, (half > 0 || kk > 0) ? 1u : 0u);
+            ptx::mma_bf16_ta(acc, va, bd, kIdesc, (half > 0 || kk > 0) ? 1u : 0u);
           }
         }
         ptx::mma_commit(&b_empty[bs]);
         ptx::mma_commit(&t_full[ts]);
-        if (j + kBBuf < nt) {  // the buffer is free once these MMAs are done
+        if (hj + kBRing < n_half) {  // the slot is free once these MMAs are done
           if (!ptx::mbar_wait_bounded(&b_empty[bs], bph, abort_f, kWaitLimitNs)) break;
-          issue_b(j + kBBuf);
+          issue_b(hj + kBRing);
         }
       }
     }
@@ -558,12 +571,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     // TMEM lane = token row i of the tile; thread i reads its row of each
     // half-tile from the buffer and adds its accumulator row.  kFull writes
     // the sum back in place for one TMA store of the half-tile; the other
-    // modes store the row straight from registers (16 bytes per store), so
-    // their buffer is free once every thread has read its row.  Every
-    // epilogue thread passes the same waits and named barriers, aborted or
-    // not; the barrier that ends a half-tile keeps the four warps within one
-    // half-tile of each other, so no buffer's phase can complete twice before
-    // every thread has waited on it.
+    // modes store the row straight from registers (16 bytes per store).
+    // Every epilogue thread passes the same waits and named barriers, aborted
+    // or not; the barrier that ends a half-tile keeps the four warps within
+    // one half-tile of each other, so no buffer's phase can complete twice
+    // before every thread has waited on it.
     const int i = warp * 32 + lane;
     const bool own = i < n_tok;
     const uint32_t tq = tmem + (static_cast<uint32_t>(warp * 32) << 16);
@@ -575,97 +587,93 @@ __global__ void __launch_bounds__(kThreads, 2)
                            : (mode == kRun ? Lay::kTail + static_cast<uint32_t>(i - n_run) * kYPitch
                                            : static_cast<uint32_t>(i) * kYPitch);
     bool ok = true;
-    for (int j = 0; j < nt; ++j) {
-      const int bs = j & 1;
-      const uint32_t ph = static_cast<uint32_t>(j >> 1) & 1u;
-      ok = ok && warp_wait(&t_full[bs], ph, abort_f);
-      if (ok) ptx::tc_fence_after();
 #pragma unroll 1
-      for (int h = 0; h < kXN / 64; ++h) {
-        const int hj = 2 * j + h;
-        ok = ok && warp_wait(&y_full[hj % kYBuf], static_cast<uint32_t>(hj / kYBuf) & 1u, abort_f);
-        uint8_t* const buf = ybuf(hj);
-        uint8_t* const yb = buf + row_off;
-        if (ok && mode == kFull) {
-          // in place, 32 columns at a time, for the TMA store
+    for (int hj = 0; hj < n_half; ++hj) {
+      const int ts = hj & 1;
+      ok = ok && warp_wait(&t_full[ts], static_cast<uint32_t>(hj >> 1) & 1u, abort_f);
+      if (ok) ptx::tc_fence_after();
+      ok = ok && warp_wait(&y_full[hj % kYBuf], static_cast<uint32_t>(hj / kYBuf) & 1u, abort_f);
+      uint8_t* const buf = ybuf(hj);
+      uint8_t* const yb = buf + row_off;
+      const uint32_t acc = tq + static_cast<uint32_t>(ts) * kAccCols;
+      if (ok && mode == kFull) {
+        // in place, 32 columns at a time, for the TMA store
 #pragma unroll
-          for (int c0 = 0; c0 < 64; c0 += 32) {
-            uint32_t v[32];
-            ptx::tmem_ld16(tq + bs * kXN + h * 64 + c0, *reinterpret_cast<uint32_t(*)[16]>(v));
-            ptx::tmem_ld16(tq + bs * kXN + h * 64 + c0 + 16,
-                           *reinterpret_cast<uint32_t(*)[16]>(v + 16));
-            ptx::tmem_ld_wait();
+        for (int c0 = 0; c0 < 64; c0 += 32) {
+          uint32_t v[32];
+          ptx::tmem_ld16(acc + c0, *reinterpret_cast<uint32_t(*)[16]>(v));
+          ptx::tmem_ld16(acc + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4* p = reinterpret_cast<uint4*>(yb + ((((c0 >> 3) + q) ^ (i & 7)) << 4));
+            const uint4 w = *p;
+            const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+            float f[8];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              f[2 * e] = bf16_lo(u[e]) + __uint_as_float(v[8 * q + 2 * e]);
+              f[2 * e + 1] = bf16_hi(u[e]) + __uint_as_float(v[8 * q + 2 * e + 1]);
+            }
+            *p = pack8_bf16(f);
+          }
+        }
+      } else if (ok && warp * 32 < n_tok) {  // uniform over the warp
+        // 32 columns at a time: the row's chunks read, then the sums stored
+        // from registers
+        const int col = hcol(hj);
+#pragma unroll
+        for (int c0 = 0; c0 < 64; c0 += 32) {
+          uint4 yv[4];
+          if (own) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              uint4* p = reinterpret_cast<uint4*>(yb + ((((c0 >> 3) + q) ^ (i & 7)) << 4));
-              const uint4 w = *p;
-              const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+              const int ch = (c0 >> 3) + q;
+              yv[q] = *reinterpret_cast<const uint4*>(yb + ((swz ? ch ^ (i & 7) : ch) << 4));
+            }
+          }
+          uint32_t v[32];
+          ptx::tmem_ld16(acc + c0, *reinterpret_cast<uint32_t(*)[16]>(v));
+          ptx::tmem_ld16(acc + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
+          ptx::tmem_ld_wait();
+          if (own) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const uint32_t u[4] = {yv[q].x, yv[q].y, yv[q].z, yv[q].w};
               float f[8];
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
                 f[2 * e] = bf16_lo(u[e]) + __uint_as_float(v[8 * q + 2 * e]);
                 f[2 * e + 1] = bf16_hi(u[e]) + __uint_as_float(v[8 * q + 2 * e + 1]);
               }
-              *p = pack8_bf16(f);
+              if (col + c0 + 8 * q < d_out)  // d_out is a multiple of 8
+                *reinterpret_cast<uint4*>(yrow + col + c0 + 8 * q) = pack8_bf16(f);
             }
-          }
-        } else if (ok && warp * 32 < n_tok) {  // uniform over the warp
-          // 32 columns at a time: the row's chunks read, then the sums
-          // stored from registers
-          const int col = hcol(hj);
-#pragma unroll
-          for (int c0 = 0; c0 < 64; c0 += 32) {
-            uint4 yv[4];
-            if (own) {
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const int ch = (c0 >> 3) + q;
-                yv[q] = *reinterpret_cast<const uint4*>(yb + ((swz ? ch ^ (i & 7) : ch) << 4));
-              }
-            }
-            uint32_t v[32];
-            ptx::tmem_ld16(tq + bs * kXN + h * 64 + c0, *reinterpret_cast<uint32_t(*)[16]>(v));
-            ptx::tmem_ld16(tq + bs * kXN + h * 64 + c0 + 16,
-                           *reinterpret_cast<uint32_t(*)[16]>(v + 16));
-            ptx::tmem_ld_wait();
-            if (own) {
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const uint32_t u[4] = {yv[q].x, yv[q].y, yv[q].z, yv[q].w};
-                float f[8];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  f[2 * e] = bf16_lo(u[e]) + __uint_as_float(v[8 * q + 2 * e]);
-                  f[2 * e + 1] = bf16_hi(u[e]) + __uint_as_float(v[8 * q + 2 * e + 1]);
-                }
-                if (col + c0 + 8 * q < d_out)  // d_out is a multiple of 8
-                  *reinterpret_cast<uint4*>(yrow + col + c0 + 8 * q) = pack8_bf16(f);
-              }
-            }
-          }
-        }
-        if (mode == kFull) {
-          // one thread stores the half-tile; once the store before it has
-          // read its buffer, that buffer takes the load of half-tile hj + 2
-          if (ok) ptx::fence_proxy_async_smem();
-          asm volatile("bar.sync 1, 128;" ::: "memory");
-          if (i == 0 && ok && !*abort_f) {
-            ptx::tma_store_2d(&tm_y, buf, hcol(hj), row0);
-            ptx::bulk_commit_group();
-            ptx::bulk_wait_group_read<kYBuf - 2>();
-            if (hj + 2 >= kYBuf && hj + 2 < 2 * nt) issue_y(hj + 2);
-          }
-        } else {
-          // every row of the buffer has been read: it takes half-tile hj + kYBuf
-          asm volatile("bar.sync 1, 128;" ::: "memory");
-          if (ok && hj + kYBuf < 2 * nt) {
-            if (i == 0) issue_y(hj + kYBuf);
-            issue_y_own(hj + kYBuf);
           }
         }
       }
+      // the accumulator is read: the MMAs of half-tile hj + 2 may start
       ptx::tc_fence_before();
-      ptx::mbar_arrive(&t_empty[bs]);
+      ptx::mbar_arrive(&t_empty[ts]);
+      if (mode == kFull) {
+        // one thread stores the half-tile; once the store before it has read
+        // its buffer, that buffer takes the load of half-tile hj + kYBuf - 1
+        if (ok) ptx::fence_proxy_async_smem();
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (i == 0 && ok && !*abort_f) {
+          ptx::tma_store_2d(&tm_y, buf, hcol(hj), row0);
+          ptx::bulk_commit_group();
+          ptx::bulk_wait_group_read<1>();
+          if (hj >= 1 && hj + kYBuf - 1 < n_half) issue_y(hj + kYBuf - 1);
+        }
+      } else {
+        // every row of the buffer has been read: it takes half-tile hj + kYBuf
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (ok && hj + kYBuf < n_half) {
+          if (i == 0) issue_y(hj + kYBuf);
+          issue_y_own(hj + kYBuf);
+        }
+      }
     }
     if (mode == kFull && i == 0) ptx::bulk_wait_group_read_all();  // buffers outlive stores
   }
@@ -673,21 +681,22 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
   if (warp == 4) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, 2 * kXN);
+    ptx::tmem_dealloc(tmem, Lay::kTmemCols);
   }
   if (tid == 0 && *abort_f) flag_error(err, LORA_DEVERR_TIMEOUT);
 }
 
 template <int R>
 cudaError_t launch_expand_r(const CUtensorMap& tm, const CUtensorMap& tm_y, const float* vpart,
-                            int ksplit,
-                            const int32_t* perm, const int32_t* seg_slot, const int32_t* seg_off,
-                            const int32_t* n_seg, bf16* y, int T, int d_out, int n_slots,
-                            uint32_t* err, cudaStream_t st, const DeviceInfo& dev) {
+                            int ksplit, const int32_t* perm, const int32_t* seg_slot,
+                            const int32_t* seg_off, const int32_t* n_seg, bf16* y, int T,
+                            int d_out, int n_slots, uint32_t* err, cudaStream_t st,
+                            const DeviceInfo& dev) {
   using Lay = ExpandLayout<R>;
-  // at most two CTAs per SM, so their 2 x 256 tensor-memory columns fit
+  // at least 80 KB, so that at most two CTAs share an SM and their 2 x 256
+  // tensor-memory columns fit
   size_t smem = Lay::kTotal + 1024;
-  if (smem < 100 * 1024) smem = 100 * 1024;
+  if (smem < 80 * 1024) smem = 80 * 1024;
   if (smem > dev.max_smem_optin) return cudaErrorInvalidConfiguration;
   auto kern = sgmv_expand_tc_kernel<R>;
   cudaError_t e =
