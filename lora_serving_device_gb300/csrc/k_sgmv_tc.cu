@@ -305,7 +305,8 @@ cudaError_t launch_r(const CUtensorMap& tm, const CUtensorMap& tm_x, const bf16*
 // operand, as bf16 hi + lo halves (hi = v rounded to bf16, lo = the rest
 // rounded), so the product keeps v's fp32 precision.  The CTA walks its
 // column tiles in 64-column half-tiles: one group of MMAs (N = 64) per
-// half-tile into one of two 64-column accumulators, B[a] through a ring of
+// half-tile into one of kNAcc 64-column accumulators (three at rank 64, so
+// the MMAs run two half-tiles ahead of the epilogue), B[a] through a ring of
 // half-tile boxes, y through kYBuf half-tile buffers.
 constexpr int kXN = 128;      // d_out columns per tile
 constexpr int kXGroup = 8;    // d_out tiles per CTA (16 half-tiles)
@@ -314,12 +315,13 @@ constexpr int kYPitch = 144;  // bytes per token row moved by its own bulk copy
 constexpr int kMinRun = 16;   // shortest run of consecutive rows moved by TMA
 constexpr int kMaxTail = 16;  // most rows after such a run
 constexpr uint32_t kAccCols = 64;  // one accumulator: 64 fp32 columns
+constexpr uint32_t kYWarp = 32 * 128;  // one warp's 32 rows of a TMA box buffer
 
 template <int R>
 struct ExpandLayout {
   // B[a] ring: half-tile boxes of 64 columns x R rows (128-byte swizzle);
-  // two CTAs per SM fit with three rank-64 boxes or two rank-128 ones
-  static constexpr int kBRing = R == 64 ? 3 : 2;
+  // two CTAs per SM fit with four rank-64 boxes or two rank-128 ones
+  static constexpr int kBRing = R == 64 ? 4 : 2;
   static constexpr uint32_t kBBox = R * 128;
   // y buffers of one half-tile (128 token rows x 64 columns).  Rows of a run
   // of consecutive y rows arrive by TMA with the 128-byte swizzle, row i at
@@ -333,13 +335,14 @@ struct ExpandLayout {
        1023) / 1024 * 1024;
   static constexpr uint32_t kYOff = kBRing * kBBox;  // a multiple of 1024
   static constexpr uint32_t kBars = kYOff + kYBuf * kYBufBytes;
-  // b_full[kBRing], b_empty[kBRing], t_full[2], t_empty[2], y_full[kYBuf],
-  // TMEM slot, abort
-  static constexpr int kNBar = 2 * kBRing + 4 + kYBuf;
+  // tensor memory: kNAcc accumulators, then V hi (R / 2 columns of bf16
+  // pairs) and V lo, in 256 columns
+  static constexpr int kNAcc = R == 64 ? 3 : 2;
+  static constexpr uint32_t kVCol = kNAcc * kAccCols;
+  // b_full[kBRing], b_empty[kBRing], t_full[kNAcc], t_empty[kNAcc],
+  // y_full[4 warps][kYBuf], TMEM slot, abort
+  static constexpr int kNBar = 2 * kBRing + 2 * kNAcc + 4 * kYBuf;
   static constexpr uint32_t kTotal = kBars + kNBar * 8 + 16;
-  // tensor memory: the two accumulators, then V hi (R / 2 columns of bf16
-  // pairs) and V lo
-  static constexpr uint32_t kVCol = 2 * kAccCols;
   static constexpr uint32_t kTmemCols = 256;
   static_assert(kVCol + R <= kTmemCols, "tensor memory");
 };
@@ -352,6 +355,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                           const int32_t* n_seg, bf16* y, int T, int d_out, uint32_t* err) {
   using Lay = ExpandLayout<R>;
   constexpr int kBRing = Lay::kBRing;
+  constexpr int kNAcc = Lay::kNAcc;
   constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(128, 64, false, true);
   __shared__ int s_a, s_p0, s_p1;
 
@@ -361,10 +365,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint64_t* b_full = reinterpret_cast<uint64_t*>(smem + Lay::kBars);
   uint64_t* b_empty = b_full + kBRing;
   uint64_t* t_full = b_empty + kBRing;
-  uint64_t* t_empty = t_full + 2;
-  uint64_t* y_full = t_empty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(y_full + kYBuf);
-  volatile int* abort_f = reinterpret_cast<volatile int*>(y_full + kYBuf) + 1;
+  uint64_t* t_empty = t_full + kNAcc;
+  uint64_t* y_full = t_empty + kNAcc;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(y_full + 4 * kYBuf);
+  volatile int* abort_f = reinterpret_cast<volatile int*>(y_full + 4 * kYBuf) + 1;
   uint8_t* ybase = smem + Lay::kYOff;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -403,11 +407,11 @@ __global__ void __launch_bounds__(kThreads, 2)
       ptx::mbar_init(&b_full[i], 1);
       ptx::mbar_init(&b_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kNAcc; ++i) {
       ptx::mbar_init(&t_full[i], 1);
       ptx::mbar_init(&t_empty[i], 4 * 32);
     }
-    for (int i = 0; i < kYBuf; ++i) ptx::mbar_init(&y_full[i], 1);
+    for (int i = 0; i < 4 * kYBuf; ++i) ptx::mbar_init(&y_full[i], 1);
     *abort_f = 0;
     ptx::fence_mbar_init();
   }
@@ -434,19 +438,21 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int c = d_out - hcol(hj);
     return static_cast<uint32_t>(c <= 0 ? 0 : (c < 64 ? c : 64) * 2);
   };
-  // one thread: the TMA part of half-tile hj and the byte count of its phase
-  // (bulk-copied rows may land before the count is set)
-  auto issue_y = [&](int hj) {
-    uint64_t* bar = &y_full[hj % kYBuf];
-    if (mode == kFull) {
-      ptx::mbar_arrive_expect_tx(bar, Lay::kYHalf);
-      ptx::tma_load_2d(ybuf(hj), &tm_y, bar, hcol(hj), row0);
-    } else if (mode == kRun) {
-      ptx::mbar_arrive_expect_tx(bar, Lay::kYHalf + static_cast<uint32_t>(n_tail) * row_bytes(hj));
-      ptx::tma_load_2d(ybuf(hj), &tm_y, bar, hcol(hj), row0);
-    } else {
-      ptx::mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n_tok) * row_bytes(hj));
-    }
+  // Each epilogue warp moves its own 32 rows of every half-tile (rows 32 w ..
+  // 32 w + 31 of the item, 4 KiB at 4096 w of a TMA box buffer) and waits on
+  // its own barrier per buffer, so the four warps never wait for each other.
+  auto ybar = [&](int w, int hj) { return &y_full[w * kYBuf + hj % kYBuf]; };
+  // lane 0 of warp w: the TMA part of the warp's rows of half-tile hj and the
+  // byte count of its phase (bulk-copied rows may land before it is set)
+  auto issue_y = [&](int w, int hj) {
+    uint64_t* bar = ybar(w, hj);
+    const int nr = min(32, n_tok - 32 * w);                   // the warp's rows
+    const int nrun = mode == kRows ? 0 : max(0, min(32, n_run - 32 * w));  // of them by TMA
+    uint32_t bytes = static_cast<uint32_t>(nr - nrun) * row_bytes(hj);
+    if (nrun > 0) bytes += kYWarp;
+    ptx::mbar_arrive_expect_tx(bar, bytes);
+    if (nrun > 0)
+      ptx::tma_load_2d(ybuf(hj) + w * kYWarp, &tm_y, bar, hcol(hj), row0 + 32 * w);
   };
   // the epilogue thread of row tid: its own bulk copy of half-tile hj
   auto issue_y_own = [&](int hj) {
@@ -456,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (mode == kRows && tid < n_tok) dst = ybuf(hj) + tid * kYPitch;
     if (tail_row) dst = ybuf(hj) + Lay::kTail + (tid - n_run) * kYPitch;
     if (dst)
-      ptx::bulk_load(dst, y + static_cast<size_t>(my_row) * d_out + hcol(hj), nb, &y_full[hj % kYBuf]);
+      ptx::bulk_load(dst, y + static_cast<size_t>(my_row) * d_out + hcol(hj), nb, ybar(tid >> 5, hj));
   };
   // B[a][:, half-tile hj] into ring slot hj % kBRing
   auto issue_b = [&](int hj) {
@@ -468,14 +474,14 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (warp == 4) {
     if (lane == 0) {
       for (int hj = 0; hj < kBRing && hj < n_half; ++hj) issue_b(hj);
-      if (mode != kRows)
-        for (int hj = 0; hj < kYBuf && hj < n_half; ++hj) issue_y(hj);
     }
     __syncwarp();
   } else {
-    for (int hj = 0; hj < kYBuf && hj < n_half; ++hj) {
-      if (mode == kRows && tid == 0) issue_y(hj);
-      issue_y_own(hj);
+    if (warp * 32 < n_tok) {  // uniform over the warp
+      for (int hj = 0; hj < kYBuf && hj < n_half; ++hj) {
+        if (lane == 0) issue_y(warp, hj);
+        issue_y_own(hj);
+      }
     }
     // V rows into tensor memory: row i = token perm[p0 + i], summed over the
     // d_in splits in order (32 values of two splits per round of loads),
@@ -538,9 +544,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     // ---------------- MMA issuer (and B loads) ----------------------------
     if (lane == 0) {
       for (int hj = 0; hj < n_half; ++hj) {
-        const int bs = hj % kBRing, ts = hj & 1;  // B slot, accumulator
+        const int bs = hj % kBRing, ts = hj % kNAcc;  // B slot, accumulator
         const uint32_t bph = static_cast<uint32_t>(hj / kBRing) & 1u;
-        const uint32_t tph = static_cast<uint32_t>(hj >> 1) & 1u;
+        const uint32_t tph = static_cast<uint32_t>(hj / kNAcc) & 1u;
         if (!ptx::mbar_wait_bounded(&b_full[bs], bph, abort_f, kWaitLimitNs)) break;
         if (!ptx::mbar_wait_bounded(&t_empty[ts], tph ^ 1u, abort_f, kWaitLimitNs)) break;
         ptx::tc_fence_after();
@@ -559,9 +565,16 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         ptx::mma_commit(&b_empty[bs]);
         ptx::mma_commit(&t_full[ts]);
-        if (hj + kBRing < n_half) {  // the slot is free once these MMAs are done
-          if (!ptx::mbar_wait_bounded(&b_empty[bs], bph, abort_f, kWaitLimitNs)) break;
-          issue_b(hj + kBRing);
+        // the previous half-tile's slot is free once its MMAs are done (they
+        // ran ahead of the ones just issued): it takes B of half-tile
+        // hj - 1 + kBRing, so these MMAs never wait on their own completion
+        const int hr = hj - 1 + kBRing;
+        if (hj >= 1 && hr < n_half) {
+          const int rs = (hj - 1) % kBRing;
+          if (!ptx::mbar_wait_bounded(&b_empty[rs], static_cast<uint32_t>((hj - 1) / kBRing) & 1u,
+                                      abort_f, kWaitLimitNs))
+            break;
+          issue_b(hr);
         }
       }
     }
@@ -573,11 +586,12 @@ __global__ void __launch_bounds__(kThreads, 2)
     // the sum back in place for one TMA store of the half-tile; the other
     // modes store the row straight from registers (16 bytes per store).
     // Every epilogue thread passes the same waits and named barriers, aborted
-    // or not; the barrier that ends a half-tile keeps the four warps within
-    // one half-tile of each other, so no buffer's phase can complete twice
-    // before every thread has waited on it.
+    // or not.  A warp waits only on its own y barriers, and the accumulator
+    // barriers keep every warp within kNAcc half-tiles of the slowest, so no
+    // phase can complete twice before a thread has waited on it.
     const int i = warp * 32 + lane;
     const bool own = i < n_tok;
+    const bool rows = warp * 32 < n_tok;  // this warp has rows (uniform)
     const uint32_t tq = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     bf16* const yrow = own ? y + static_cast<size_t>(my_row) * d_out : nullptr;
     // this thread's row of a buffer: swizzled rows of a TMA box, else
@@ -589,13 +603,22 @@ __global__ void __launch_bounds__(kThreads, 2)
     bool ok = true;
 #pragma unroll 1
     for (int hj = 0; hj < n_half; ++hj) {
-      const int ts = hj & 1;
-      ok = ok && warp_wait(&t_full[ts], static_cast<uint32_t>(hj >> 1) & 1u, abort_f);
+      const int ts = hj % kNAcc;
+      ok = ok && warp_wait(&t_full[ts], static_cast<uint32_t>(hj / kNAcc) & 1u, abort_f);
       if (ok) ptx::tc_fence_after();
-      ok = ok && warp_wait(&y_full[hj % kYBuf], static_cast<uint32_t>(hj / kYBuf) & 1u, abort_f);
+      if (rows)
+        ok = ok && warp_wait(ybar(warp, hj), static_cast<uint32_t>(hj / kYBuf) & 1u, abort_f);
       uint8_t* const buf = ybuf(hj);
       uint8_t* const yb = buf + row_off;
       const uint32_t acc = tq + static_cast<uint32_t>(ts) * kAccCols;
+      // the accumulator is free once its last columns are in registers: the
+      // MMAs of half-tile hj + kNAcc may start while these are added
+      bool freed = false;
+      auto free_acc = [&]() {
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&t_empty[ts]);
+        freed = true;
+      };
       if (ok && mode == kFull) {
         // in place, 32 columns at a time, for the TMA store
 #pragma unroll
@@ -604,6 +627,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           ptx::tmem_ld16(acc + c0, *reinterpret_cast<uint32_t(*)[16]>(v));
           ptx::tmem_ld16(acc + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
           ptx::tmem_ld_wait();
+          if (c0 == 32) free_acc();
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             uint4* p = reinterpret_cast<uint4*>(yb + ((((c0 >> 3) + q) ^ (i & 7)) << 4));
@@ -618,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             *p = pack8_bf16(f);
           }
         }
-      } else if (ok && warp * 32 < n_tok) {  // uniform over the warp
+      } else if (ok && rows) {
         // 32 columns at a time: the row's chunks read, then the sums stored
         // from registers
         const int col = hcol(hj);
@@ -636,6 +660,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           ptx::tmem_ld16(acc + c0, *reinterpret_cast<uint32_t(*)[16]>(v));
           ptx::tmem_ld16(acc + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
           ptx::tmem_ld_wait();
+          if (c0 == 32) free_acc();
           if (own) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -652,30 +677,31 @@ __global__ void __launch_bounds__(kThreads, 2)
           }
         }
       }
-      // the accumulator is read: the MMAs of half-tile hj + 2 may start
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(&t_empty[ts]);
-      if (mode == kFull) {
-        // one thread stores the half-tile; once the store before it has read
-        // its buffer, that buffer takes the load of half-tile hj + kYBuf - 1
-        if (ok) ptx::fence_proxy_async_smem();
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        if (i == 0 && ok && !*abort_f) {
-          ptx::tma_store_2d(&tm_y, buf, hcol(hj), row0);
-          ptx::bulk_commit_group();
-          ptx::bulk_wait_group_read<1>();
-          if (hj >= 1 && hj + kYBuf - 1 < n_half) issue_y(hj + kYBuf - 1);
-        }
-      } else {
-        // every row of the buffer has been read: it takes half-tile hj + kYBuf
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        if (ok && hj + kYBuf < n_half) {
-          if (i == 0) issue_y(hj + kYBuf);
+      if (!freed) free_acc();  // (a warp without rows, or aborted)
+      if (rows && ok) {
+        if (mode == kFull) {
+          // lane 0 stores the warp's 32 rows; once its store before that has
+          // read the buffer, that buffer takes the load of half-tile
+          // hj + kYBuf - 1
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && !*abort_f) {
+            ptx::tma_store_2d(&tm_y, buf + warp * kYWarp, hcol(hj), row0 + 32 * warp);
+            ptx::bulk_commit_group();
+            ptx::bulk_wait_group_read<1>();
+            if (hj >= 1 && hj + kYBuf - 1 < n_half) issue_y(warp, hj + kYBuf - 1);
+          }
+        } else if (hj + kYBuf < n_half) {
+          // every row of the warp has been read: its part of the buffer
+          // takes half-tile hj + kYBuf
+          __syncwarp();
+          if (lane == 0) issue_y(warp, hj + kYBuf);
           issue_y_own(hj + kYBuf);
         }
       }
+      __syncwarp();
     }
-    if (mode == kFull && i == 0) ptx::bulk_wait_group_read_all();  // buffers outlive stores
+    if (mode == kFull && lane == 0 && rows) ptx::bulk_wait_group_read_all();  // buffers outlive stores
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -728,9 +754,9 @@ cudaError_t launch_sgmv_expand_tc(const float* vpart, int ksplit, const void* B,
   if (T <= 0) return cudaSuccess;
   CUtensorMap tm, tm_y;
   // B_pool as [n_slots][r][d_out]: 64 columns x r rows per box; y [T][d_out]:
-  // 64 columns x 128 rows per box, 128-byte swizzle
+  // 64 columns x 32 rows (one epilogue warp's rows) per box, 128-byte swizzle
   if (!encode_tensor_map_bf16_3d(&tm, B, d_out, r, n_slots, 64, r) ||
-      !encode_tensor_map_bf16(&tm_y, y, d_out, T, d_out, 64, kTok))
+      !encode_tensor_map_bf16(&tm_y, y, d_out, T, d_out, 64, 32))
     return cudaErrorInvalidValue;
   bf16* ye = static_cast<bf16*>(y);
   if (r == 64)
