@@ -223,9 +223,9 @@ def parse_clocks(lines, window=None):
 # d_in splits for the standalone SGMV rows on the prefill workload: the shrink,
 # with its three-CTA ring, is fastest at 4 (29.0 us; 38.0 at 2, 30.5 at 3, 30.7
 # at 5, 30.0 at 6, 32.0 at 8); the expand, which sums the partials in its V
-# build, at 2 (198 us; 244 us at 4 before y moved by TMA)
+# build at the start of every CTA, on one (131.4 us; 136.9 on two)
 SGMV_SHRINK_KSPLIT = 4
-SGMV_EXPAND_KSPLIT = 2
+SGMV_EXPAND_KSPLIT = 1
 
 
 def fused_ksplit(T, d_in, d_out, n_slots, num_sms=152):

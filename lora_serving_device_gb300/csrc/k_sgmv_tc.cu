@@ -347,8 +347,10 @@ struct ExpandLayout {
   static_assert(kVCol + R <= kTmemCols, "tensor memory");
 };
 
+// At most 128 registers a thread: measured, the kernel ran 6-20% slower on
+// the prefill workload's full items in every build that used 155-168.
 template <int R>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __maxnreg__(128)
     sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
                           const __grid_constant__ CUtensorMap tm_y, const float* vpart, int ksplit,
                           const int32_t* perm, const int32_t* seg_slot, const int32_t* seg_off,
@@ -495,33 +497,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       const float* vrow = vpart + static_cast<size_t>(own ? my_row : 0) * R;
       const size_t split = static_cast<size_t>(T) * R;
       const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16) + Lay::kVCol;
-#pragma unroll 1
-      for (int q0 = 0; q0 < R; q0 += 32) {
-        float f[32];
-#pragma unroll
-        for (int k = 0; k < 32; ++k) f[k] = 0.f;
-        for (int sp = 0; own && sp < ksplit; sp += 2) {
-          const bool two = sp + 1 < ksplit;
-          const float4* pa = reinterpret_cast<const float4*>(vrow + sp * split + q0);
-          float4 u[8], w[8];
-#pragma unroll
-          for (int k = 0; k < 8; ++k) u[k] = pa[k];
-          if (two) {
-            const float4* pb = reinterpret_cast<const float4*>(vrow + (sp + 1) * split + q0);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) w[k] = pb[k];
-          }
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            f[4 * k] += u[k].x; f[4 * k + 1] += u[k].y; f[4 * k + 2] += u[k].z; f[4 * k + 3] += u[k].w;
-          }
-          if (two) {
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              f[4 * k] += w[k].x; f[4 * k + 1] += w[k].y; f[4 * k + 2] += w[k].z; f[4 * k + 3] += w[k].w;
-            }
-          }
-        }
+      // f (32 values of the row, summed over the splits) -> V hi and lo
+      auto store_v = [&](int q0, const float (&f)[32]) {
         uint32_t hp[16], lp[16];
 #pragma unroll
         for (int m = 0; m < 16; ++m) {
@@ -532,6 +509,40 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         ptx::tmem_st16(lane_base + q0 / 2, hp);
         ptx::tmem_st16(lane_base + R / 2 + q0 / 2, lp);
+      };
+      {
+        // 32 values of the row from two splits per round of loads (a whole
+        // row per round needs ~168 registers, and the kernel runs slower
+        // above 128)
+#pragma unroll 1
+        for (int q0 = 0; q0 < R; q0 += 32) {
+          float f[32];
+#pragma unroll
+          for (int k = 0; k < 32; ++k) f[k] = 0.f;
+          for (int sp = 0; own && sp < ksplit; sp += 2) {
+            const bool two = sp + 1 < ksplit;
+            const float4* pa = reinterpret_cast<const float4*>(vrow + sp * split + q0);
+            float4 u[8], w[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) u[k] = pa[k];
+            if (two) {
+              const float4* pb = reinterpret_cast<const float4*>(vrow + (sp + 1) * split + q0);
+#pragma unroll
+              for (int k = 0; k < 8; ++k) w[k] = pb[k];
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              f[4 * k] += u[k].x; f[4 * k + 1] += u[k].y; f[4 * k + 2] += u[k].z; f[4 * k + 3] += u[k].w;
+            }
+            if (two) {
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                f[4 * k] += w[k].x; f[4 * k + 1] += w[k].y; f[4 * k + 2] += w[k].z; f[4 * k + 3] += w[k].w;
+              }
+            }
+          }
+          store_v(q0, f);
+        }
       }
       ptx::tmem_st_wait();
     }
