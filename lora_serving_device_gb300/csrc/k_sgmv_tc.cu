@@ -510,10 +510,31 @@ __global__ void __maxnreg__(128)
         ptx::tmem_st16(lane_base + q0 / 2, hp);
         ptx::tmem_st16(lane_base + R / 2 + q0 / 2, lp);
       };
-      {
+      if (R == 64 && ksplit == 1) {
+        // rank 64, one split: the whole row in one round of loads, nothing to add
+        float4 u[R / 4];
+        if (own) {
+          const float4* pa = reinterpret_cast<const float4*>(vrow);
+#pragma unroll
+          for (int k = 0; k < R / 4; ++k) u[k] = pa[k];
+        } else {
+#pragma unroll
+          for (int k = 0; k < R / 4; ++k) u[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int q0 = 0; q0 < R; q0 += 32) {
+          float f[32];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const float4 w = u[q0 / 4 + k];
+            f[4 * k] = w.x; f[4 * k + 1] = w.y; f[4 * k + 2] = w.z; f[4 * k + 3] = w.w;
+          }
+          store_v(q0, f);
+        }
+      } else {
         // 32 values of the row from two splits per round of loads (a whole
-        // row per round needs ~168 registers, and the kernel runs slower
-        // above 128)
+        // row of two splits per round needs ~168 registers, and the kernel
+        // runs slower above 128)
 #pragma unroll 1
         for (int q0 = 0; q0 < R; q0 += 32) {
           float f[32];
