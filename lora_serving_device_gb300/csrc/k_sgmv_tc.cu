@@ -314,8 +314,96 @@ constexpr int kYBuf = 4;      // y half-tile buffers
 constexpr int kYPitch = 144;  // bytes per token row moved by its own bulk copy
 constexpr int kMinRun = 16;   // shortest run of consecutive rows moved by TMA
 constexpr int kMaxTail = 16;  // most rows after such a run
+constexpr int kPairTok = 16;  // segments this short share an item, two by two
 constexpr uint32_t kAccCols = 64;  // one accumulator: 64 fp32 columns
 constexpr uint32_t kYWarp = 32 * 128;  // one warp's 32 rows of a TMA box buffer
+
+// Work items of the expand.  Segments of more than kPairTok tokens give one
+// item per 128-token chunk, in segment order; after them, every two
+// consecutive segments of at most kPairTok tokens (decode tokens of adapters
+// no prefill request uses) share one item, so that a CTA's sweep over its
+// columns serves both.  With pairs off, every segment is chunked.  The whole
+// block cooperates (each thread counts a run of segments, two block-wide
+// scans place the runs); every thread must call it, and the result is valid
+// after it returns.  it[0..2] = slot, first and one-past-last position in
+// perm of the first part; it[3..5] the same for the second part (slot -1:
+// none); it[0] = -1: no such item.
+__device__ __forceinline__ void expand_item(int item, bool pairs, const int32_t* seg_slot,
+                                            const int32_t* seg_off, int nseg, int* it) {
+  __shared__ int ws_big[33], ws_small[33], tot[2];
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const int lane = tid & 31, warp = tid >> 5, nwarps = nt >> 5;
+  if (tid < 6) it[tid] = -1;
+  const int per = (nseg + nt - 1) / nt;
+  const int j0 = min(nseg, tid * per), j1 = min(nseg, j0 + per);
+  int cb = 0, cs = 0;  // this run's big chunks and small segments
+  for (int j = j0; j < j1; ++j) {
+    const int n = ld_dep(seg_off + j + 1) - ld_dep(seg_off + j);
+    if (pairs && n <= kPairTok) ++cs;
+    else cb += (n + kTok - 1) / kTok;
+  }
+  int ib = cb, is = cs;  // inclusive scans within the warp
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int vb = __shfl_up_sync(0xffffffffu, ib, o), vs = __shfl_up_sync(0xffffffffu, is, o);
+    if (lane >= o) { ib += vb; is += vs; }
+  }
+  if (lane == 31) { ws_big[warp] = ib; ws_small[warp] = is; }
+  __syncthreads();
+  if (warp == 0) {
+    const int wb = lane < nwarps ? ws_big[lane] : 0, wsm = lane < nwarps ? ws_small[lane] : 0;
+    int xb = wb, xs = wsm;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int vb = __shfl_up_sync(0xffffffffu, xb, o), vs = __shfl_up_sync(0xffffffffu, xs, o);
+      if (lane >= o) { xb += vb; xs += vs; }
+    }
+    ws_big[lane] = xb - wb;
+    ws_small[lane] = xs - wsm;
+    if (lane == 31) { tot[0] = xb; tot[1] = xs; }
+  }
+  __syncthreads();
+  const int fb = ws_big[warp] + ib - cb;    // this run's first big chunk
+  const int fs = ws_small[warp] + is - cs;  // and first small segment
+  const int n_big = tot[0];
+  if (item < n_big) {
+    if (item >= fb && item < fb + cb) {
+      int x = item - fb;
+      for (int j = j0; j < j1; ++j) {
+        const int o0 = ld_dep(seg_off + j), o1 = ld_dep(seg_off + j + 1);
+        if (pairs && o1 - o0 <= kPairTok) continue;
+        const int cj = (o1 - o0 + kTok - 1) / kTok;
+        if (x < cj) {
+          it[0] = ld_dep(seg_slot + j);
+          it[1] = o0 + x * kTok;
+          it[2] = min(o1, it[1] + kTok);
+          break;
+        }
+        x -= cj;
+      }
+    }
+  } else {
+    // small segments 2 q and 2 q + 1; the thread holding each writes its part
+    const int q = item - n_big;
+    for (int part = 0; part < 2; ++part) {
+      const int k = 2 * q + part;
+      if (k < fs || k >= fs + cs) continue;
+      int x = k - fs;
+      for (int j = j0; j < j1; ++j) {
+        const int o0 = ld_dep(seg_off + j), o1 = ld_dep(seg_off + j + 1);
+        if (o1 - o0 > kPairTok) continue;
+        if (x == 0) {
+          it[3 * part] = ld_dep(seg_slot + j);
+          it[3 * part + 1] = o0;
+          it[3 * part + 2] = o1;
+          break;
+        }
+        --x;
+      }
+    }
+  }
+  __syncthreads();
+}
 
 template <int R>
 struct ExpandLayout {
@@ -335,6 +423,12 @@ struct ExpandLayout {
        1023) / 1024 * 1024;
   static constexpr uint32_t kYOff = kBRing * kBBox;  // a multiple of 1024
   static constexpr uint32_t kBars = kYOff + kYBuf * kYBufBytes;
+  // a pair's second B box sits in y buffer bs past its at most 2 kPairTok
+  // rows (pairs are formed at rank 64 only)
+  static constexpr uint32_t kPairB = 8192;
+  static_assert(R != 64 || (2 * kPairTok * kYPitch <= kPairB && kPairB + kBBox <= kYBufBytes &&
+                            kPairB % 1024 == 0 && kYBuf == kBRing),
+                "pair B boxes in the y buffers");
   // tensor memory: kNAcc accumulators, then V hi (R / 2 columns of bf16
   // pairs) and V lo, in 256 columns
   static constexpr int kNAcc = R == 64 ? 3 : 2;
@@ -359,7 +453,7 @@ __global__ void __maxnreg__(128)
   constexpr int kBRing = Lay::kBRing;
   constexpr int kNAcc = Lay::kNAcc;
   constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(128, 64, false, true);
-  __shared__ int s_a, s_p0, s_p1;
+  __shared__ int s_it[6];
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -374,10 +468,20 @@ __global__ void __maxnreg__(128)
   uint8_t* ybase = smem + Lay::kYOff;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  sgmv_item<kTok>(blockIdx.x, seg_slot, seg_off, ld_dep(n_seg), &s_a, &s_p0, &s_p1);
-  if (s_a < 0) return;  // no such item (uniform over the CTA)
-  const int a = s_a;    // B[a] arrives by TMA, which reads nothing outside the pool
-  const int p0 = s_p0, n_tok = s_p1 - s_p0;
+  // rank 64 pairs short segments (two copies of V and two accumulators fit
+  // in tensor memory; at rank 128 they do not)
+  expand_item(blockIdx.x, R == 64, seg_slot, seg_off, ld_dep(n_seg), s_it);
+  if (s_it[0] < 0) return;  // no such item (uniform over the CTA)
+  // B[a] and B[a2] arrive by TMA, which reads nothing outside the pool
+  const int a = s_it[0], p0 = s_it[1], n1 = s_it[2] - s_it[1];
+  const bool pair = s_it[3] >= 0;
+  const int a2 = pair ? s_it[3] : a, p0b = s_it[4], n2 = pair ? s_it[5] - s_it[4] : 0;
+  const int n_tok = n1 + n2;  // rows 0 .. n1 - 1 are the first part's tokens
+  // accumulators, B ring depth (a pair takes two slots per half-tile) and
+  // V's columns for this CTA
+  const int nacc = pair ? 2 : kNAcc;
+  const int bdepth = kBRing;
+  const uint32_t vcol = pair ? 2 * kAccCols : Lay::kVCol, vcol2 = 2 * kAccCols + R;
   const int n_tiles_all = (d_out + kXN - 1) / kXN;
   const int j0 = blockIdx.y * kXGroup;
   const int nt = min(kXGroup, n_tiles_all - j0);
@@ -401,7 +505,9 @@ __global__ void __maxnreg__(128)
   // loads run kYBuf - 1 ahead.
   enum { kFull, kRun, kRows };
   const int row0 = perm_row_plain(perm, p0, T, err);
-  const int my_row = tid < n_tok ? perm_row_plain(perm, p0 + tid, T, err) : -1;
+  const int my_row = tid < n1      ? perm_row_plain(perm, p0 + tid, T, err)
+                     : tid < n_tok ? perm_row_plain(perm, p0b + tid - n1, T, err)
+                                   : -1;
   if (tid == 4 * 32) {
     ptx::prefetch_tmap(&tm_b);
     ptx::prefetch_tmap(&tm_y);
@@ -428,7 +534,9 @@ __global__ void __maxnreg__(128)
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int n_tail = n_tok - n_run;
-  const int mode = n_run == kTok ? kFull : (n_run >= kMinRun && n_tail <= kMaxTail ? kRun : kRows);
+  const int mode = pair ? kRows
+                   : n_run == kTok ? kFull
+                   : (n_run >= kMinRun && n_tail <= kMaxTail ? kRun : kRows);
   const bool tail_row = mode == kRun && tid >= n_run && tid < n_tok;
 
   auto hcol = [&](int hj) { return j0 * kXN + 64 * hj; };
@@ -466,16 +574,29 @@ __global__ void __maxnreg__(128)
     if (dst)
       ptx::bulk_load(dst, y + static_cast<size_t>(my_row) * d_out + hcol(hj), nb, ybar(tid >> 5, hj));
   };
-  // B[a][:, half-tile hj] into ring slot hj % kBRing
-  auto issue_b = [&](int hj) {
-    const int bs = hj % kBRing;
-    ptx::mbar_arrive_expect_tx(&b_full[bs], Lay::kBBox);
-    ptx::tma_load_3d(smem + bs * Lay::kBBox, &tm_b, &b_full[bs], hcol(hj), 0, a);
+  // B[a][:, half-tile hj] into ring slot bs = hj % bdepth; a pair's B[a2] box
+  // goes to the part of y buffer bs that its 32 rows leave free (slots and
+  // phases are stepped as counters in the loops: the accumulator count is
+  // not a compile-time constant)
+  auto bslot = [&](int bs, int part) {
+    return part == 0 ? smem + bs * Lay::kBBox : ybase + bs * Lay::kYBufBytes + Lay::kPairB;
+  };
+  auto issue_b = [&](int hj, int bs) {
+    ptx::mbar_arrive_expect_tx(&b_full[bs], (pair ? 2u : 1u) * Lay::kBBox);
+    ptx::tma_load_3d(bslot(bs, 0), &tm_b, &b_full[bs], hcol(hj), 0, a);
+    if (pair) ptx::tma_load_3d(bslot(bs, 1), &tm_b, &b_full[bs], hcol(hj), 0, a2);
+  };
+  // step a ring slot and its phase bit
+  auto step = [](int& slot, uint32_t& phase, int n) {
+    if (++slot == n) {
+      slot = 0;
+      phase ^= 1u;
+    }
   };
 
   if (warp == 4) {
     if (lane == 0) {
-      for (int hj = 0; hj < kBRing && hj < n_half; ++hj) issue_b(hj);
+      for (int hj = 0; hj < bdepth && hj < n_half; ++hj) issue_b(hj, hj);
     }
     __syncwarp();
   } else {
@@ -496,8 +617,10 @@ __global__ void __maxnreg__(128)
       const bool own = tid < n_tok;
       const float* vrow = vpart + static_cast<size_t>(own ? my_row : 0) * R;
       const size_t split = static_cast<size_t>(T) * R;
-      const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16) + Lay::kVCol;
-      // f (32 values of the row, summed over the splits) -> V hi and lo
+      const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+      // f (32 values of the row, summed over the splits) -> V hi and lo.  A
+      // pair keeps two copies of V, each with only its own part's rows (zeros
+      // elsewhere), so one accumulator sums V1 B[a] + V2 B[a2] row by row.
       auto store_v = [&](int q0, const float (&f)[32]) {
         uint32_t hp[16], lp[16];
 #pragma unroll
@@ -507,8 +630,24 @@ __global__ void __maxnreg__(128)
           hp[m] = pack_bf16x2(h0, h1);
           lp[m] = pack_bf16x2(f[2 * m] - h0, f[2 * m + 1] - h1);
         }
-        ptx::tmem_st16(lane_base + q0 / 2, hp);
-        ptx::tmem_st16(lane_base + R / 2 + q0 / 2, lp);
+        const uint32_t keep = !pair || tid < n1 ? ~0u : 0u;
+#pragma unroll
+        for (int m = 0; m < 16; ++m) { hp[m] &= keep; lp[m] &= keep; }
+        ptx::tmem_st16(lane_base + vcol + q0 / 2, hp);
+        ptx::tmem_st16(lane_base + vcol + R / 2 + q0 / 2, lp);
+        if (pair) {
+          // the rows of the first part are zero here, the others kept
+          ptx::tmem_st_wait();
+#pragma unroll
+          for (int m = 0; m < 16; ++m) {
+            const float h0 = __bfloat162float(__float2bfloat16_rn(f[2 * m]));
+            const float h1 = __bfloat162float(__float2bfloat16_rn(f[2 * m + 1]));
+            hp[m] = tid >= n1 ? pack_bf16x2(h0, h1) : 0u;
+            lp[m] = tid >= n1 ? pack_bf16x2(f[2 * m] - h0, f[2 * m + 1] - h1) : 0u;
+          }
+          ptx::tmem_st16(lane_base + vcol2 + q0 / 2, hp);
+          ptx::tmem_st16(lane_base + vcol2 + R / 2 + q0 / 2, lp);
+        }
       };
       if (R == 64 && ksplit == 1) {
         // rank 64, one split: the whole row in one round of loads, nothing to add
@@ -575,39 +714,43 @@ __global__ void __maxnreg__(128)
   if (warp == 4) {
     // ---------------- MMA issuer (and B loads) ----------------------------
     if (lane == 0) {
+      int bs = 0, ts = 0, rs = 0;  // B slot, accumulator, previous half-tile's slot
+      uint32_t bph = 0, tph = 0, rph = 0;
       for (int hj = 0; hj < n_half; ++hj) {
-        const int bs = hj % kBRing, ts = hj % kNAcc;  // B slot, accumulator
-        const uint32_t bph = static_cast<uint32_t>(hj / kBRing) & 1u;
-        const uint32_t tph = static_cast<uint32_t>(hj / kNAcc) & 1u;
         if (!ptx::mbar_wait_bounded(&b_full[bs], bph, abort_f, kWaitLimitNs)) break;
         if (!ptx::mbar_wait_bounded(&t_empty[ts], tph ^ 1u, abort_f, kWaitLimitNs)) break;
         ptx::tc_fence_after();
-        const uint32_t bb = ptx::smem_u32(smem + bs * Lay::kBBox);
         const uint32_t acc = tmem + static_cast<uint32_t>(ts) * kAccCols;
+        for (int part = 0; part < (pair ? 2 : 1); ++part) {
+          const uint32_t bb = ptx::smem_u32(bslot(bs, part));
+          const uint32_t vc = part ? vcol2 : vcol;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
+          for (int half = 0; half < 2; ++half) {
 #pragma unroll
-          for (int kk = 0; kk < R / 16; ++kk) {
-            // A: V hi or lo, 16 K elements = 8 columns per step; B: MN-major,
-            // 16 K rows = 2048 bytes per step
-            const uint32_t va = tmem + Lay::kVCol + half * (R / 2) + kk * 8;
-            const uint64_t bd = ptx::sdesc_sw128(bb + kk * 2048, Lay::kBBox, 1024);
-            ptx::mma_bf16_ta(acc, va, bd, kIdesc, (half > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < R / 16; ++kk) {
+              // A: V hi or lo, 16 K elements = 8 columns per step; B:
+              // MN-major, 16 K rows = 2048 bytes per step
+              const uint32_t va = tmem + vc + half * (R / 2) + kk * 8;
+              const uint64_t bd = ptx::sdesc_sw128(bb + kk * 2048, Lay::kBBox, 1024);
+              ptx::mma_bf16_ta(acc, va, bd, kIdesc, (part > 0 || half > 0 || kk > 0) ? 1u : 0u);
+            }
           }
         }
         ptx::mma_commit(&b_empty[bs]);
         ptx::mma_commit(&t_full[ts]);
         // the previous half-tile's slot is free once its MMAs are done (they
         // ran ahead of the ones just issued): it takes B of half-tile
-        // hj - 1 + kBRing, so these MMAs never wait on their own completion
-        const int hr = hj - 1 + kBRing;
-        if (hj >= 1 && hr < n_half) {
-          const int rs = (hj - 1) % kBRing;
-          if (!ptx::mbar_wait_bounded(&b_empty[rs], static_cast<uint32_t>((hj - 1) / kBRing) & 1u,
-                                      abort_f, kWaitLimitNs))
-            break;
-          issue_b(hr);
+        // hj - 1 + bdepth, so these MMAs never wait on their own completion
+        const int hr = hj - 1 + bdepth;
+        if (hj >= 1) {
+          if (hr < n_half) {
+            if (!ptx::mbar_wait_bounded(&b_empty[rs], rph, abort_f, kWaitLimitNs)) break;
+            issue_b(hr, rs);
+          }
+          step(rs, rph, bdepth);
         }
+        step(bs, bph, bdepth);
+        step(ts, tph, nacc);
       }
     }
     __syncwarp();
@@ -633,10 +776,11 @@ __global__ void __maxnreg__(128)
                            : (mode == kRun ? Lay::kTail + static_cast<uint32_t>(i - n_run) * kYPitch
                                            : static_cast<uint32_t>(i) * kYPitch);
     bool ok = true;
+    int ts = 0;  // accumulator of half-tile hj, and its phase
+    uint32_t tph = 0;
 #pragma unroll 1
-    for (int hj = 0; hj < n_half; ++hj) {
-      const int ts = hj % kNAcc;
-      ok = ok && warp_wait(&t_full[ts], static_cast<uint32_t>(hj / kNAcc) & 1u, abort_f);
+    for (int hj = 0; hj < n_half; ++hj, step(ts, tph, nacc)) {
+      ok = ok && warp_wait(&t_full[ts], tph, abort_f);
       if (ok) ptx::tc_fence_after();
       if (rows)
         ok = ok && warp_wait(ybar(warp, hj), static_cast<uint32_t>(hj / kYBuf) & 1u, abort_f);

@@ -221,6 +221,45 @@ def test_sgmv_expand_run_and_tail_items(L, d_out, r):
     assert L.get_error_t(ws) == 0
 
 
+def _short_segment_ids(T, n_single, seed):
+    """Slot ids for segments of at most 16 tokens (which the rank-64 SGMV
+    expand serves two to a CTA): n_single one-token segments, one segment of 5
+    tokens and one of 17 (not paired), the rest base-only, shuffled."""
+    rng = np.random.default_rng([7005, seed])
+    ids = np.full(T, -1, np.int32)
+    pos = rng.permutation(T)
+    k = 0
+    for slot in range(n_single):
+        ids[pos[k]] = slot
+        k += 1
+    for slot, n in ((n_single, 5), (n_single + 1, 17)):
+        ids[pos[k:k + n]] = slot
+        k += n
+    return ids
+
+
+# an odd and an even number of short segments; a ragged last column tile
+@pytest.mark.parametrize("n_single,d_out", [(30, 1032), (21, 264)])
+def test_sgmv_expand_short_segments_in_pairs(L, n_single, d_out):
+    torch = torch_mod()
+    T, r, n_slots = 80, 64, n_single + 2
+    ids = _short_segment_ids(T, n_single, n_single)
+    rng = np.random.default_rng([7006, n_single])
+    B = W.bf16_round((rng.standard_normal((n_slots, r, d_out)) * 0.02).astype(np.float32))
+    vp = _v_input(T, r, 1, 5)
+    y0 = W.bf16_round((rng.standard_normal((T, d_out)) * 0.1).astype(np.float32))
+    y = dev(y0, "bf16")
+    ws = _ws(L)
+    segs = L.build_segments_t(dev(ids), n_slots, ws)
+    L.sgmv_expand_t(dev(vp, "f32"), dev(B, "bf16"), segs, y, ws)
+    torch.cuda.synchronize()
+    got = host(y)
+    check_close(got, y0 + O.expand(vp.astype(np.float64).sum(axis=0), B, ids),
+                "short-segment SGMV expand y")
+    np.testing.assert_array_equal(got[ids < 0], y0[ids < 0].astype(np.float64))
+    assert L.get_error_t(ws) == 0
+
+
 # ------------------------------------------------------------ fused layer
 FUSED_CASES = [
     # T, d_in, d_out, r, n_slots : decode tiles (T <= 256) and prefill tiles
