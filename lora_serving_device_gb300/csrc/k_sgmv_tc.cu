@@ -325,7 +325,9 @@ constexpr uint32_t kYWarp = 32 * 128;  // one warp's 32 rows of a TMA box buffer
 // columns serves both.  With pairs off, every segment is chunked.  The whole
 // block cooperates (each thread counts a run of segments, two block-wide
 // scans place the runs); every thread must call it, and the result is valid
-// after it returns.  it[0..2] = slot, first and one-past-last position in
+// after it returns.  The expand is not launched early, so the segments,
+// written by an earlier kernel of the stream, are read through the cached
+// read-only path.  it[0..2] = slot, first and one-past-last position in
 // perm of the first part; it[3..5] the same for the second part (slot -1:
 // none); it[0] = -1: no such item.
 __device__ __forceinline__ void expand_item(int item, bool pairs, const int32_t* seg_slot,
@@ -338,7 +340,7 @@ __device__ __forceinline__ void expand_item(int item, bool pairs, const int32_t*
   const int j0 = min(nseg, tid * per), j1 = min(nseg, j0 + per);
   int cb = 0, cs = 0;  // this run's big chunks and small segments
   for (int j = j0; j < j1; ++j) {
-    const int n = ld_dep(seg_off + j + 1) - ld_dep(seg_off + j);
+    const int n = __ldg(seg_off + j + 1) - __ldg(seg_off + j);
     if (pairs && n <= kPairTok) ++cs;
     else cb += (n + kTok - 1) / kTok;
   }
@@ -370,11 +372,11 @@ __device__ __forceinline__ void expand_item(int item, bool pairs, const int32_t*
     if (item >= fb && item < fb + cb) {
       int x = item - fb;
       for (int j = j0; j < j1; ++j) {
-        const int o0 = ld_dep(seg_off + j), o1 = ld_dep(seg_off + j + 1);
+        const int o0 = __ldg(seg_off + j), o1 = __ldg(seg_off + j + 1);
         if (pairs && o1 - o0 <= kPairTok) continue;
         const int cj = (o1 - o0 + kTok - 1) / kTok;
         if (x < cj) {
-          it[0] = ld_dep(seg_slot + j);
+          it[0] = __ldg(seg_slot + j);
           it[1] = o0 + x * kTok;
           it[2] = min(o1, it[1] + kTok);
           break;
@@ -390,10 +392,10 @@ __device__ __forceinline__ void expand_item(int item, bool pairs, const int32_t*
       if (k < fs || k >= fs + cs) continue;
       int x = k - fs;
       for (int j = j0; j < j1; ++j) {
-        const int o0 = ld_dep(seg_off + j), o1 = ld_dep(seg_off + j + 1);
+        const int o0 = __ldg(seg_off + j), o1 = __ldg(seg_off + j + 1);
         if (o1 - o0 > kPairTok) continue;
         if (x == 0) {
-          it[3 * part] = ld_dep(seg_slot + j);
+          it[3 * part] = __ldg(seg_slot + j);
           it[3 * part + 1] = o0;
           it[3 * part + 2] = o1;
           break;
