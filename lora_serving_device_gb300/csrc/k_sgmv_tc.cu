@@ -315,6 +315,7 @@ constexpr int kYPitch = 144;  // bytes per token row moved by its own bulk copy
 constexpr int kMinRun = 16;   // shortest run of consecutive rows moved by TMA
 constexpr int kMaxTail = 16;  // most rows after such a run
 constexpr int kPairTok = 16;  // segments this short share an item, two by two
+constexpr int kXThreads = 192;  // warps 0-3: epilogue, warp 4: MMA, warp 5: B[a] loads
 constexpr uint32_t kAccCols = 64;  // one accumulator: 64 fp32 columns
 constexpr uint32_t kYWarp = 32 * 128;  // one warp's 32 rows of a TMA box buffer
 
@@ -472,7 +473,11 @@ __global__ void __maxnreg__(128)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // rank 64 pairs short segments (two copies of V and two accumulators fit
   // in tensor memory; at rank 128 they do not)
-  expand_item(blockIdx.x, R == 64, seg_slot, seg_off, ld_dep(n_seg), s_it);
+  const int nseg = ld_dep(n_seg);
+  // every segment adds at most one chunk beyond T / 128 (pairs only merge
+  // items), so CTAs past that bound hold no item and leave before the lookup
+  if (static_cast<int>(blockIdx.x) >= (T + kTok - 1) / kTok + nseg) return;
+  expand_item(blockIdx.x, R == 64, seg_slot, seg_off, nseg, s_it);
   if (s_it[0] < 0) return;  // no such item (uniform over the CTA)
   // B[a] and B[a2] arrive by TMA, which reads nothing outside the pool
   const int a = s_it[0], p0 = s_it[1], n1 = s_it[2] - s_it[1];
@@ -596,12 +601,12 @@ __global__ void __maxnreg__(128)
     }
   };
 
-  if (warp == 4) {
+  if (warp == 5) {
     if (lane == 0) {
       for (int hj = 0; hj < bdepth && hj < n_half; ++hj) issue_b(hj, hj);
     }
     __syncwarp();
-  } else {
+  } else if (warp < 4) {
     if (warp * 32 < n_tok) {  // uniform over the warp
       for (int hj = 0; hj < kYBuf && hj < n_half; ++hj) {
         if (lane == 0) issue_y(warp, hj);
@@ -714,11 +719,11 @@ __global__ void __maxnreg__(128)
   ptx::tc_fence_after();
 
   if (warp == 4) {
-    // ---------------- MMA issuer (and B loads) ----------------------------
+    // ---------------- MMA issuer -----------------------------------------
     if (lane == 0) {
-      int bs = 0, ts = 0, rs = 0;  // B slot, accumulator, previous half-tile's slot
-      uint32_t bph = 0, tph = 0, rph = 0;
-      for (int hj = 0; hj < n_half; ++hj) {
+      int bs = 0, ts = 0;  // B slot and accumulator of half-tile hj
+      uint32_t bph = 0, tph = 0;
+      for (int hj = 0; hj < n_half; ++hj, step(bs, bph, bdepth), step(ts, tph, nacc)) {
         if (!ptx::mbar_wait_bounded(&b_full[bs], bph, abort_f, kWaitLimitNs)) break;
         if (!ptx::mbar_wait_bounded(&t_empty[ts], tph ^ 1u, abort_f, kWaitLimitNs)) break;
         ptx::tc_fence_after();
@@ -740,19 +745,18 @@ __global__ void __maxnreg__(128)
         }
         ptx::mma_commit(&b_empty[bs]);
         ptx::mma_commit(&t_full[ts]);
-        // the previous half-tile's slot is free once its MMAs are done (they
-        // ran ahead of the ones just issued): it takes B of half-tile
-        // hj - 1 + bdepth, so these MMAs never wait on their own completion
-        const int hr = hj - 1 + bdepth;
-        if (hj >= 1) {
-          if (hr < n_half) {
-            if (!ptx::mbar_wait_bounded(&b_empty[rs], rph, abort_f, kWaitLimitNs)) break;
-            issue_b(hr, rs);
-          }
-          step(rs, rph, bdepth);
-        }
-        step(bs, bph, bdepth);
-        step(ts, tph, nacc);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ---------------- B[a] loads: a slot takes half-tile hj + bdepth once
+    // the MMAs of half-tile hj are done ------------------------------------
+    if (lane == 0) {
+      int bs = 0;
+      uint32_t bph = 0;
+      for (int hj = 0; hj + bdepth < n_half; ++hj, step(bs, bph, bdepth)) {
+        if (!ptx::mbar_wait_bounded(&b_empty[bs], bph, abort_f, kWaitLimitNs)) break;
+        issue_b(hj + bdepth, bs);
       }
     }
     __syncwarp();
@@ -911,7 +915,7 @@ cudaError_t launch_expand_r(const CUtensorMap& tm, const CUtensorMap& tm_y, cons
   const int groups = ((d_out + kXN - 1) / kXN + kXGroup - 1) / kXGroup;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(items > 0 ? items : 1, groups);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(kXThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cfg.numAttrs = 0;
