@@ -310,6 +310,7 @@ cudaError_t launch_r(const CUtensorMap& tm, const CUtensorMap& tm_x, const bf16*
 // half-tile boxes, y through kYBuf half-tile buffers.
 constexpr int kXN = 128;      // d_out columns per tile
 constexpr int kXGroup = 8;    // d_out tiles per CTA (16 half-tiles)
+constexpr int kXGroupFull = 14;  // per CTA of a full item (28 half-tiles)
 constexpr int kYBuf = 4;      // y half-tile buffers
 constexpr int kYPitch = 144;  // bytes per token row moved by its own bulk copy
 constexpr int kMinRun = 16;   // shortest run of consecutive rows moved by TMA
@@ -490,10 +491,7 @@ __global__ void __maxnreg__(128)
   const int bdepth = kBRing;
   const uint32_t vcol = pair ? 2 * kAccCols : Lay::kVCol, vcol2 = 2 * kAccCols + R;
   const int n_tiles_all = (d_out + kXN - 1) / kXN;
-  const int j0 = blockIdx.y * kXGroup;
-  const int nt = min(kXGroup, n_tiles_all - j0);
-  if (nt <= 0) return;
-  const int n_half = 2 * nt;  // half-tiles of this CTA
+  if (static_cast<int>(blockIdx.y) * kXGroup >= n_tiles_all) return;
 
   // y moves in half-tiles in one of three ways.  The tokens of an item sit in
   // increasing row order, so the rows that are consecutive in y from its
@@ -515,6 +513,20 @@ __global__ void __maxnreg__(128)
   const int my_row = tid < n1      ? perm_row_plain(perm, p0 + tid, T, err)
                      : tid < n_tok ? perm_row_plain(perm, p0b + tid - n1, T, err)
                                    : -1;
+  // the rows consecutive in y from the first (barrier: the rows are known)
+  const int n_run = __syncthreads_count(tid < n_tok && my_row - row0 == tid);
+  const int n_tail = n_tok - n_run;
+  const int mode = pair ? kRows
+                   : n_run == kTok ? kFull
+                   : (n_run >= kMinRun && n_tail <= kMaxTail ? kRun : kRows);
+  // column tiles of this CTA: a full item's CTA sweeps kXGroupFull of them
+  // (fewer start-ups for the items that stream the most y; blockIdx.y past
+  // its groups leaves), any other item's kXGroup
+  const int grp = mode == kFull ? kXGroupFull : kXGroup;
+  const int j0 = blockIdx.y * grp;
+  const int nt = min(grp, n_tiles_all - j0);
+  if (nt <= 0) return;  // uniform over the CTA; nothing is allocated yet
+  const int n_half = 2 * nt;  // half-tiles of this CTA
   if (tid == 4 * 32) {
     ptx::prefetch_tmap(&tm_b);
     ptx::prefetch_tmap(&tm_y);
@@ -536,14 +548,9 @@ __global__ void __maxnreg__(128)
     ptx::tmem_relinquish();
     ptx::tc_fence_before();
   }
-  // (also: the barriers are initialised and tensor memory is allocated)
-  const int n_run = __syncthreads_count(tid < n_tok && my_row - row0 == tid);
+  __syncthreads();  // the barriers are initialised and tensor memory is allocated
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int n_tail = n_tok - n_run;
-  const int mode = pair ? kRows
-                   : n_run == kTok ? kFull
-                   : (n_run >= kMinRun && n_tail <= kMaxTail ? kRun : kRows);
   const bool tail_row = mode == kRun && tid >= n_run && tid < n_tok;
 
   auto hcol = [&](int hj) { return j0 * kXN + 64 * hj; };
