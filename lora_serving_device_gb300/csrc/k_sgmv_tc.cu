@@ -25,11 +25,13 @@
 // to the base output):  y[t, :] += (sum_s v_partial[s, t, :]) B[a]  for the
 // tokens of one segment, y bf16, read and written once.  At rank 64 over a
 // prefill batch this is 16.7 GFLOP against ~0.6 GB, again beyond the CUDA
-// cores.  A work item (128 tokens of one segment) builds its V tile once in
-// shared memory, as bf16 hi + lo halves (v = hi + lo keeps ~16 mantissa
-// bits), then runs 128-column tiles of d_out: B[a] by TMA, MMAs of both
-// halves into a double-buffered TMEM accumulator, and an epilogue that adds
-// it to the gathered y rows.
+// cores.  A work item (128 tokens of one segment; at rank 64 also two short
+// segments together) writes its V rows once into tensor memory, as bf16
+// hi + lo halves (v = hi + lo keeps ~16 mantissa bits), then sweeps a group
+// of 64-column half-tiles of d_out: B[a] by TMA through a ring fed by its own
+// warp, MMAs of both halves into one of several TMEM accumulators, and an
+// epilogue in which every warp moves its own rows of y (details at the
+// expand's code below).
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
@@ -493,21 +495,21 @@ __global__ void __maxnreg__(128)
   const int n_tiles_all = (d_out + kXN - 1) / kXN;
   if (static_cast<int>(blockIdx.y) * kXGroup >= n_tiles_all) return;
 
-  // y moves in half-tiles in one of three ways.  The tokens of an item sit in
-  // increasing row order, so the rows that are consecutive in y from its
-  // first one (a prefill request, or its last item) are a prefix of n_run
-  // rows.
-  //  - kFull (n_run = 128): each half-tile is one 128-row TMA box, loaded,
-  //    updated in place and stored back.
+  // y moves in half-tiles in one of three ways, each epilogue warp moving
+  // its own 32 rows.  The tokens of an item sit in increasing row order, so
+  // the rows that are consecutive in y from its first one (a prefill request,
+  // or its last item) are a prefix of n_run rows.
+  //  - kFull (n_run = 128): a warp's rows of each half-tile are one 32-row
+  //    TMA box, loaded, updated in place and stored back.
   //  - kRun (n_run >= kMinRun, at most kMaxTail rows after it): the run
-  //    arrives as the same 128-row box (rows past it are read, never
-  //    written), every tail row by its own bulk copy.
-  //  - kRows (any other item): every row arrives by its own bulk copy,
-  //    issued by the epilogue thread that owns the row.
+  //    arrives as 32-row boxes (rows past it are read, never written), every
+  //    tail row by its own bulk copy.
+  //  - kRows (any other item, and every pair): every row arrives by its own
+  //    bulk copy, issued by the epilogue thread that owns the row.
   // In kRun and kRows each thread stores its own row from registers, so a
   // buffer is free once it has been read and loads run kYBuf half-tiles
-  // ahead; in kFull a buffer is free once the TMA store has read it, and
-  // loads run kYBuf - 1 ahead.
+  // ahead; in kFull a buffer is free once the warp's TMA store has read it,
+  // and loads run kYBuf - 1 ahead.
   enum { kFull, kRun, kRows };
   const int row0 = perm_row_plain(perm, p0, T, err);
   const int my_row = tid < n1      ? perm_row_plain(perm, p0 + tid, T, err)
