@@ -79,6 +79,74 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
+// Work items of the shrink: every segment's last 128-token chunk first, in
+// segment order, then the other chunks.  A segment's last chunk is where
+// decode tokens of the same adapter join a prefill request's rows, the
+// items whose rows are gathered and take longest; numbering them first
+// starts them first.  Every thread must call it; the result is valid after
+// it returns (slot -1: no such item).
+__device__ __forceinline__ void shrink_item(int item, const int32_t* seg_slot,
+                                            const int32_t* seg_off, int nseg, int* s_a, int* s_p0,
+                                            int* s_p1) {
+  __shared__ int warp_sum[33];
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const int lane = tid & 31, warp = tid >> 5, nwarps = nt >> 5;
+  if (tid == 0) *s_a = -1;
+  if (item < nseg) {  // segment `item`'s last chunk: one thread looks it up
+    if (tid == 0) {
+      const int o0 = ld_dep(seg_off + item), o1 = ld_dep(seg_off + item + 1);
+      *s_a = ld_dep(seg_slot + item);
+      *s_p0 = o0 + (o1 - o0 - 1) / kTok * kTok;
+      *s_p1 = o1;
+    }
+    __syncthreads();
+    return;
+  }
+  // the other chunks: every thread counts a run of segments, a block-wide
+  // exclusive scan places the runs
+  const int x0 = item - nseg;
+  const int per = (nseg + nt - 1) / nt;
+  const int j0 = min(nseg, tid * per), j1 = min(nseg, j0 + per);
+  int c = 0;
+  for (int j = j0; j < j1; ++j)
+    c += (ld_dep(seg_off + j + 1) - ld_dep(seg_off + j) + kTok - 1) / kTok - 1;
+  int incl = c;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_sum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int w = lane < nwarps ? warp_sum[lane] : 0;
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += v;
+    }
+    warp_sum[lane] = wi - w;
+  }
+  __syncthreads();
+  const int first = warp_sum[warp] + incl - c;
+  if (x0 >= first && x0 < first + c) {
+    int x = x0 - first;
+    for (int j = j0; j < j1; ++j) {
+      const int o0 = ld_dep(seg_off + j), o1 = ld_dep(seg_off + j + 1);
+      const int cj = (o1 - o0 + kTok - 1) / kTok - 1;
+      if (x < cj) {
+        *s_a = ld_dep(seg_slot + j);
+        *s_p0 = o0 + x * kTok;
+        *s_p1 = *s_p0 + kTok;
+        break;
+      }
+      x -= cj;
+    }
+  }
+  __syncthreads();
+}
+
 template <int R, int ST>
 __global__ void __launch_bounds__(kThreads, ST == 3 && R == 64 ? 3 : 2)
     sgmv_shrink_tc_kernel(const __grid_constant__ CUtensorMap tm_a,
@@ -109,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, ST == 3 && R == 64 ? 3 : 2)
     for (int e = tid; e < nbase * R; e += kThreads)
       vpart[(static_cast<size_t>(s) * T + perm_row(perm, e / R, T, err)) * R + (e % R)] = 0.f;
   }
-  sgmv_item<kTok>(blockIdx.x, seg_slot, seg_off, nseg, &s_a, &s_p0, &s_p1);
+  shrink_item(blockIdx.x, seg_slot, seg_off, nseg, &s_a, &s_p0, &s_p1);
   if (s_a < 0) return;  // no such item (uniform over the CTA)
   const int a = checked_index(s_a, n_slots, err);
   const int p0 = s_p0, n_tok = s_p1 - s_p0;
