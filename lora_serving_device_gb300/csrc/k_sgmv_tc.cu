@@ -37,7 +37,6 @@
 #include "common.cuh"
 #include "internal.h"
 #include "ptx.cuh"
-#include "sgmv_item.cuh"
 
 namespace lora {
 namespace {
