@@ -221,6 +221,28 @@ def test_sgmv_expand_run_and_tail_items(L, d_out, r):
     assert L.get_error_t(ws) == 0
 
 
+# SGMV shrink on the same layouts: a segment's last chunk mixes a run with
+# scattered rows (gathered), its other chunks are consecutive rows (TMA); the
+# shrink numbers every last chunk first
+@pytest.mark.parametrize("d_in,r", [(520, 64), (1032, 128)])
+def test_sgmv_shrink_run_and_tail_items(L, d_in, r):
+    torch = torch_mod()
+    T, n_slots = 700, 4
+    ids = _run_tail_ids(T, RUN_TAIL_LAYOUT, d_in)
+    rng = np.random.default_rng([7007, d_in])
+    A = W.bf16_round((rng.standard_normal((n_slots, d_in, r)) / np.sqrt(d_in)).astype(np.float32))
+    x = W.bf16_round(rng.standard_normal((T, d_in)).astype(np.float32))
+    scale = rng.uniform(0.5, 2.5, n_slots).astype(np.float32)
+    ws = _ws(L)
+    segs = L.build_segments_t(dev(ids), n_slots, ws)
+    ref = O.shrink(x, A, scale, ids)
+    for ksplit in (1, 4):
+        vp = L.sgmv_shrink_t(dev(x, "bf16"), dev(A, "bf16"), segs, dev(scale, "f32"), ksplit, ws)
+        torch.cuda.synchronize()
+        check_close(host(vp).sum(axis=0), ref, f"run + tail SGMV shrink ksplit={ksplit}")
+    assert L.get_error_t(ws) == 0
+
+
 def _short_segment_ids(T, n_single, seed):
     """Slot ids for segments of at most 16 tokens (which the rank-64 SGMV
     expand serves two to a CTA): n_single one-token segments, one segment of 5
