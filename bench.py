@@ -228,14 +228,17 @@ SGMV_SHRINK_KSPLIT = 4
 SGMV_EXPAND_KSPLIT = 1
 
 
-def fused_ksplit(T, d_in, d_out, n_slots, num_sms=152):
+def fused_ksplit(T, d_in, d_out, n_slots, r, num_sms=152):
     """The shrink split the fused path uses (mirrors the library's choice;
     tests/test_bench_host.py checks it against lora_workspace_bytes)."""
     if T <= 256:      # decode-sized batch: per-token shrink, ~256 CTAs
         return max(1, min(-(-256 // max(T, 1)), 16, max(d_in // 512, 1)))
-    if n_slots <= 32767 and -(-d_out // 256) * -(-T // 256) >= 2 * num_sms:
-        return 1      # 256 x 256 prefill tiles: v as one partial, copied ahead
     cap = min(T, n_slots)
+    if r in (64, 128):  # tensor-core shrink, splits folded into one partial
+        est = -(-T // 128) + (cap + 1) // 2
+        return max(1, min(-(-3 * num_sms // max(est, 1)), 4, max(d_in // 128, 1)))
+    if n_slots <= 32767 and -(-d_out // 256) * -(-T // 256) >= 2 * num_sms:
+        return 1      # 256 x 256 prefill tiles: v as one partial
     est = (T + 63) // 64 + (cap + 1) // 2
     ks = -(-2 * num_sms // max(est, 1))
     return max(1, min(ks, 16, max(d_in // 128, 1)))
@@ -596,7 +599,7 @@ def decode_blocks(sets, L, w, stream, pk, n_steps=400):
     T, d_in, d_out, r, n_slots, D = w.T, w.d_in, w.d_out, w.r, w.n_slots, w.distinct
     T_lora = int(((w.slot_ids >= 0) & (w.slot_ids < n_slots)).sum())
     dev = sets[0].x.device
-    ks = fused_ksplit(T, d_in, d_out, n_slots)
+    ks = fused_ksplit(T, d_in, d_out, n_slots, r)
     vpart = torch.zeros((ks, T, r), dtype=torch.float32, device=dev)
     delta = torch.zeros((T, d_out), dtype=torch.float32, device=dev)
     ws = torch.zeros(256, dtype=torch.uint8, device=dev)

@@ -20,10 +20,12 @@ struct DeviceInfo {
 };
 cudaError_t device_info(DeviceInfo* out);
 
-// Segment builder: one CTA, see k_segments.cu.
+// Segment builder: one CTA, see k_segments.cu.  It also zeroes the n_zero
+// words at `zero` (the counters of the shrink's split fold), if given.
 cudaError_t launch_build_segments(const int32_t* ids, int T, int n_slots, int32_t* perm,
                                   int32_t* seg_slot, int32_t* seg_off, int32_t* n_seg,
-                                  uint32_t* err, cudaStream_t st);
+                                  uint32_t* err, cudaStream_t st, int32_t* zero = nullptr,
+                                  int n_zero = 0);
 
 // Gather kernels (CUDA cores), see k_gather.cu.
 cudaError_t launch_bgmv_shrink(const void* x, const void* A, const int32_t* ids,
@@ -51,10 +53,11 @@ cudaError_t launch_set_scale(float* scale, int slot, float s, cudaStream_t st);
 int sgmv_max_items(int T, int n_slots);
 // ksplit the fused path uses for its shrink (SGMV / BGMV form).
 int fused_shrink_ksplit(int T, int d_in, int n_slots, int num_sms);
-// True when the fused prefill GEMM takes 256 x 256 tiles (k_fused_tc.cu);
-// its LoRA stages then copy v asynchronously, which wants a single shrink
-// partial (split 1).
+// True when the fused prefill GEMM takes 256 x 256 tiles (k_fused_tc.cu).
 bool fused_wide_tiles(int T, int d_out, int n_slots, int num_sms);
+// ksplit of the tensor-core shrink when it folds its splits into one
+// partial (the prefill path at rank 64 / 128), see k_sgmv_tc.cu.
+int fold_shrink_ksplit(int T, int d_in, int n_slots, int num_sms);
 int decode_shrink_ksplit(int T, int d_in);
 
 // Base GEMM + expand-in-accumulator kernel, bf16 (tcgen05), see k_fused_tc.cu.
@@ -138,13 +141,17 @@ bool encode_tensor_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, ui
 bool encode_tensor_map_bf16_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1,
                                uint64_t d2, uint32_t box0, uint32_t box1);
 // SGMV shrink on tensor cores (bf16, r in {64, 128}), see k_sgmv_tc.cu; the
-// same contract as launch_sgmv_shrink.
+// same contract as launch_sgmv_shrink.  With `fold` (sgmv_shrink_tc_items
+// zeroed words) and ksplit > 1, split 0 of vpart ends as the sum of all
+// splits (in split order); the other splits hold their own partials.
 bool sgmv_shrink_tc_supported(int r);
+int sgmv_shrink_tc_items(int T, int n_slots);
 cudaError_t launch_sgmv_shrink_tc(const void* x, const void* A, const int32_t* perm,
                                   const int32_t* seg_slot, const int32_t* seg_off,
                                   const int32_t* n_seg, const float* scale, float* vpart, int T,
-                                  int d_in, int r, int n_slots, int ksplit, uint32_t* err,
-                                  cudaStream_t st, bool pdl, const DeviceInfo& dev);
+                                  int d_in, int r, int n_slots, int ksplit, int32_t* fold,
+                                  uint32_t* err, cudaStream_t st, bool pdl,
+                                  const DeviceInfo& dev);
 // SGMV expand on tensor cores (bf16, r in {64, 128}), see k_sgmv_tc.cu; the
 // same contract as launch_sgmv_expand.
 bool sgmv_expand_tc_supported(int r);

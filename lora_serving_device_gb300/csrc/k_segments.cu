@@ -72,7 +72,7 @@ __global__ void __launch_bounds__(kThreads)
     build_segments_kernel(const int32_t* __restrict__ ids, int T, int n_slots, int P,
                           int32_t* __restrict__ perm, int32_t* __restrict__ seg_slot,
                           int32_t* __restrict__ seg_off, int32_t* __restrict__ n_seg_out,
-                          uint32_t* err) {
+                          uint32_t* err, int32_t* __restrict__ zero, int n_zero) {
   extern __shared__ int32_t sm[];
   __shared__ int warp_tmp[33];
   __shared__ int bad;
@@ -82,6 +82,7 @@ __global__ void __launch_bounds__(kThreads)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
   for (int i = tid; i < P * nb + nb + 1; i += blockDim.x) sm[i] = 0;
+  for (int i = tid; i < n_zero; i += blockDim.x) zero[i] = 0;
   if (tid == 0) bad = 0;
   __syncthreads();
 
@@ -151,7 +152,7 @@ __global__ void __launch_bounds__(kThreads)
 
 cudaError_t launch_build_segments(const int32_t* ids, int T, int n_slots, int32_t* perm,
                                   int32_t* seg_slot, int32_t* seg_off, int32_t* n_seg,
-                                  uint32_t* err, cudaStream_t st) {
+                                  uint32_t* err, cudaStream_t st, int32_t* zero, int n_zero) {
   const size_t nb = static_cast<size_t>(n_slots) + 1;
   // partitions: as many warps as the shared-memory budget allows, but no
   // more than one per 32 tokens
@@ -167,7 +168,7 @@ cudaError_t launch_build_segments(const int32_t* ids, int T, int n_slots, int32_
                                        static_cast<int>(kSmemBudget + 4 * 1024));
   if (e != cudaSuccess) return e;
   build_segments_kernel<<<1, kThreads, smem, st>>>(ids, T, n_slots, P, perm, seg_slot, seg_off,
-                                                   n_seg, err);
+                                                   n_seg, err, zero, zero != nullptr ? n_zero : 0);
   return cudaGetLastError();
 }
 

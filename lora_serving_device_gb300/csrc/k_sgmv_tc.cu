@@ -146,13 +146,73 @@ __device__ __forceinline__ void shrink_item(int item, const int32_t* seg_slot,
   __syncthreads();
 }
 
+// Folds the d_in splits of one shrink item into split 0.  Every CTA of the
+// item (one per split, blockIdx.y) counts itself on fold[item] after its
+// partial rows are written; the CTA that counts last adds the other splits'
+// rows to split 0's, in split order, so the sum does not depend on which
+// CTA finishes last.  No CTA waits for another.  Every thread of the CTA
+// calls it.
+template <int R>
+__device__ __forceinline__ void fold_splits(int32_t* fold, float* vpart, const int32_t* perm,
+                                            int p0, int n_tok, int T, uint32_t* err) {
+  __shared__ int s_rows[kTok];
+  __shared__ int s_last;
+  __threadfence();  // this CTA's rows before its count
+  __syncthreads();
+  if (threadIdx.x == 0)
+    s_last = atomicAdd(fold + blockIdx.x, 1) == static_cast<int>(gridDim.y) - 1 ? 1 : 0;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  for (int i = threadIdx.x; i < n_tok; i += blockDim.x) s_rows[i] = perm_row(perm, p0 + i, T, err);
+  __syncthreads();
+  constexpr int kQ = R / 4;  // float4 per row
+  constexpr int kU = 4;      // float4 per thread per pass
+  constexpr int kS = 4;      // splits loaded per round trip
+  const int ks = gridDim.y, n = n_tok * kQ, nt = blockDim.x;
+  const size_t plane = static_cast<size_t>(T) * R;
+  for (int e0 = threadIdx.x; e0 < n; e0 += kU * nt) {
+    float* p[kU];
+    float4 acc[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int e = e0 + u * nt;
+      p[u] = e < n ? vpart + static_cast<size_t>(s_rows[e / kQ]) * R + (e % kQ) * 4 : nullptr;
+      acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    for (int s0 = 0; s0 < ks; s0 += kS) {
+      float4 v[kS][kU];
+#pragma unroll
+      for (int j = 0; j < kS; ++j)
+#pragma unroll
+        for (int u = 0; u < kU; ++u)
+          v[j][u] = p[u] != nullptr && s0 + j < ks
+                        ? __ldcg(reinterpret_cast<const float4*>(p[u] + (s0 + j) * plane))
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < kS; ++j)
+#pragma unroll
+        for (int u = 0; u < kU; ++u)
+          if (s0 + j < ks) {
+            acc[u].x += v[j][u].x;
+            acc[u].y += v[j][u].y;
+            acc[u].z += v[j][u].z;
+            acc[u].w += v[j][u].w;
+          }
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u)
+      if (p[u] != nullptr) *reinterpret_cast<float4*>(p[u]) = acc[u];
+  }
+}
+
 template <int R, int ST>
 __global__ void __launch_bounds__(kThreads, ST == 3 && R == 64 ? 3 : 2)
     sgmv_shrink_tc_kernel(const __grid_constant__ CUtensorMap tm_a,
                           const __grid_constant__ CUtensorMap tm_x, const bf16* x,
                           const int32_t* perm, const int32_t* seg_slot, const int32_t* seg_off,
                           const int32_t* n_seg, const float* scale, float* vpart, int T,
-                          int d_in, int n_slots, int kchunk, uint32_t* err) {
+                          int d_in, int n_slots, int kchunk, int32_t* fold, uint32_t* err) {
   using Lay = ShrinkLayout<R, ST>;
   constexpr int S = Lay::kStages;
   constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(128, R, false, true);
@@ -182,9 +242,11 @@ __global__ void __launch_bounds__(kThreads, ST == 3 && R == 64 ? 3 : 2)
   const int p0 = s_p0, n_tok = s_p1 - s_p0;
   const int k0 = s * kchunk, k1 = min(d_in, k0 + kchunk);
   const int n_it = k1 > k0 ? (k1 - k0 + 63) / 64 : 0;
+  const bool folds = fold != nullptr && gridDim.y > 1;
   if (n_it == 0) {  // an empty split of d_in still writes its (zero) rows
     for (int e = tid; e < n_tok * R; e += kThreads)
       vpart[(static_cast<size_t>(s) * T + perm_row(perm, p0 + e / R, T, err)) * R + (e % R)] = 0.f;
+    if (folds) fold_splits<R>(fold, vpart, perm, p0, n_tok, T, err);
     return;
   }
   // perm is ascending within a segment, so the item's rows are consecutive
@@ -335,6 +397,7 @@ __global__ void __launch_bounds__(kThreads, ST == 3 && R == 64 ? 3 : 2)
     ptx::tmem_dealloc(tmem, R);
   }
   if (tid == 0 && *abort_f) flag_error(err, LORA_DEVERR_TIMEOUT);
+  if (folds) fold_splits<R>(fold, vpart, perm, p0, n_tok, T, err);
 }
 
 template <int R, int ST>
@@ -342,7 +405,8 @@ cudaError_t launch_r(const CUtensorMap& tm, const CUtensorMap& tm_x, const bf16*
                      const int32_t* perm,
                      const int32_t* seg_slot, const int32_t* seg_off, const int32_t* n_seg,
                      const float* scale, float* vpart, int T, int d_in, int n_slots, int ksplit,
-                     uint32_t* err, cudaStream_t st, bool pdl, const DeviceInfo& dev) {
+                     int32_t* fold, uint32_t* err, cudaStream_t st, bool pdl,
+                     const DeviceInfo& dev) {
   using Lay = ShrinkLayout<R, ST>;
   const size_t smem = Lay::kTotal + 1024;
   if (smem > dev.max_smem_optin) return cudaErrorInvalidConfiguration;
@@ -352,8 +416,7 @@ cudaError_t launch_r(const CUtensorMap& tm, const CUtensorMap& tm_x, const bf16*
   if (e != cudaSuccess) return e;
   const int per = (d_in + ksplit - 1) / ksplit;
   const int kchunk = (per + 63) / 64 * 64;
-  const int cap = T < n_slots ? T : n_slots;
-  const int items = (T + kTok - 1) / kTok + cap;
+  const int items = sgmv_shrink_tc_items(T, n_slots);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(items > 0 ? items : 1, ksplit);
   cfg.blockDim = dim3(kThreads);
@@ -365,7 +428,7 @@ cudaError_t launch_r(const CUtensorMap& tm, const CUtensorMap& tm_x, const bf16*
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kern, tm, tm_x, x, perm, seg_slot, seg_off, n_seg, scale, vpart,
-                            T, d_in, n_slots, kchunk, err);
+                            T, d_in, n_slots, kchunk, fold, err);
 }
 
 // ------------------------------------------------------------ expand
@@ -1003,6 +1066,26 @@ cudaError_t launch_expand_r(const CUtensorMap& tm, const CUtensorMap& tm_y, cons
 }  // namespace
 
 bool sgmv_shrink_tc_supported(int r) { return r == 64 || r == 128; }
+
+int sgmv_shrink_tc_items(int T, int n_slots) {
+  // the chunks of 128 tokens, plus at most one more per segment
+  const int cap = T < n_slots ? T : n_slots;
+  return (T + kTok - 1) / kTok + cap;
+}
+
+int fold_shrink_ksplit(int T, int d_in, int n_slots, int num_sms) {
+  // about three CTAs per SM (the ring the shrink takes above two per SM),
+  // expected real items ~ chunks + half the segment bound; at most four
+  // splits, which the fold loads in one round trip
+  const int cap = T < n_slots ? T : n_slots;
+  const int est = (T + kTok - 1) / kTok + (cap + 1) / 2;
+  int ks = (3 * num_sms + est - 1) / (est > 0 ? est : 1);
+  const int kmax = d_in / 128 > 0 ? d_in / 128 : 1;
+  if (ks > 4) ks = 4;
+  if (ks > kmax) ks = kmax;
+  if (ks < 1) ks = 1;
+  return ks;
+}
 bool sgmv_expand_tc_supported(int r) { return r == 64 || r == 128; }
 
 cudaError_t launch_sgmv_expand_tc(const float* vpart, int ksplit, const void* B,
@@ -1030,8 +1113,9 @@ cudaError_t launch_sgmv_expand_tc(const float* vpart, int ksplit, const void* B,
 cudaError_t launch_sgmv_shrink_tc(const void* x, const void* A, const int32_t* perm,
                                   const int32_t* seg_slot, const int32_t* seg_off,
                                   const int32_t* n_seg, const float* scale, float* vpart, int T,
-                                  int d_in, int r, int n_slots, int ksplit, uint32_t* err,
-                                  cudaStream_t st, bool pdl, const DeviceInfo& dev) {
+                                  int d_in, int r, int n_slots, int ksplit, int32_t* fold,
+                                  uint32_t* err, cudaStream_t st, bool pdl,
+                                  const DeviceInfo& dev) {
   if (T <= 0) return cudaSuccess;
   CUtensorMap tm, tm_x;
   // A_pool as [n_slots][d_in][r]: 64 columns x 64 K rows per box; rows past
@@ -1048,13 +1132,13 @@ cudaError_t launch_sgmv_shrink_tc(const void* x, const void* A, const int32_t* p
   const bool wide = ctas > 2ll * dev.num_sms;
   if (r == 64 && wide)
     return launch_r<64, 3>(tm, tm_x, xe, perm, seg_slot, seg_off, n_seg, scale, vpart, T, d_in,
-                           n_slots, ksplit, err, st, pdl, dev);
+                           n_slots, ksplit, fold, err, st, pdl, dev);
   if (r == 64)
     return launch_r<64, 4>(tm, tm_x, xe, perm, seg_slot, seg_off, n_seg, scale, vpart, T, d_in,
-                           n_slots, ksplit, err, st, pdl, dev);
+                           n_slots, ksplit, fold, err, st, pdl, dev);
   if (r == 128)
     return launch_r<128, 3>(tm, tm_x, xe, perm, seg_slot, seg_off, n_seg, scale, vpart, T, d_in,
-                            n_slots, ksplit, err, st, pdl, dev);
+                            n_slots, ksplit, fold, err, st, pdl, dev);
   return cudaErrorInvalidValue;
 }
 

@@ -37,6 +37,8 @@ struct FusedWs {
   int32_t* seg_slot;
   int32_t* seg_off;
   int32_t* n_seg;
+  int32_t* fold;   // counters of the shrink's split fold (prefill-sized batches only)
+  int n_fold;
   float* vpart;
   float* partial;  // fp32 [S, T, d_out] split-K base product (decode-sized batches only)
   int ksplit;
@@ -60,14 +62,20 @@ FusedWs fused_ws_layout(void* ws, int32_t T, int32_t d_in, int32_t d_out, int32_
   o += (cap + 1) * 4;
   const size_t o_nseg = o;
   o += 4;
+  const size_t o_fold = o;
+  w.n_fold = T > kDecodeTokens ? sgmv_shrink_tc_items(T, n_slots) : 0;
+  o += static_cast<size_t>(w.n_fold) * 4;
   o = round_up(o, 256);
   const size_t o_v = o;
   // The shrink split, the prefill tile form and the decode split are chosen
   // for a 152-SM GB300 (kDecodeScheduleCtas), not the current device, so
   // that the workspace size and every result bit are the same on every
   // device; any split is correct with every form.
+  // At rank 64 / 128 the tensor-core shrink folds its splits into one
+  // partial (bf16), so the GEMM's LoRA stages read v once.
   constexpr int kSms = kDecodeScheduleCtas;
   w.ksplit = T <= kDecodeTokens                          ? decode_shrink_ksplit(T, d_in)
+              : sgmv_shrink_tc_supported(r)               ? fold_shrink_ksplit(T, d_in, n_slots, kSms)
               : fused_wide_tiles(T, d_out, n_slots, kSms) ? 1
                                                           : fused_shrink_ksplit(T, d_in, n_slots, kSms);
   o += static_cast<size_t>(w.ksplit) * T * r * 4;
@@ -90,6 +98,7 @@ FusedWs fused_ws_layout(void* ws, int32_t T, int32_t d_in, int32_t d_out, int32_
   w.seg_slot = reinterpret_cast<int32_t*>(base + o_slot);
   w.seg_off = reinterpret_cast<int32_t*>(base + o_off);
   w.n_seg = reinterpret_cast<int32_t*>(base + o_nseg);
+  w.fold = w.n_fold > 0 ? reinterpret_cast<int32_t*>(base + o_fold) : nullptr;
   w.vpart = reinterpret_cast<float*>(base + o_v);
   w.partial = T <= kDecodeTokens ? reinterpret_cast<float*>(base + o_d) : nullptr;
   return w;
@@ -160,10 +169,14 @@ cudaError_t sgmv_shrink_any(const void* x, const void* A, const int32_t* perm,
                             const int32_t* seg_slot, const int32_t* seg_off, const int32_t* n_seg,
                             const float* scale, float* vpart, int T, int d_in, int r, int n_slots,
                             int ksplit, lora_dtype_t dt, uint32_t* err, cudaStream_t st, bool pdl,
-                            const DeviceInfo& dev) {
-  if (dt == LORA_DTYPE_BF16 && sgmv_shrink_tc_supported(r) && tensor_map_available())
+                            const DeviceInfo& dev, int32_t* fold = nullptr,
+                            int* v_parts = nullptr) {
+  if (dt == LORA_DTYPE_BF16 && sgmv_shrink_tc_supported(r) && tensor_map_available()) {
+    if (v_parts != nullptr) *v_parts = fold != nullptr ? 1 : ksplit;
     return launch_sgmv_shrink_tc(x, A, perm, seg_slot, seg_off, n_seg, scale, vpart, T, d_in, r,
-                                 n_slots, ksplit, err, st, pdl, dev);
+                                 n_slots, ksplit, fold, err, st, pdl, dev);
+  }
+  if (v_parts != nullptr) *v_parts = ksplit;
   return launch_sgmv_shrink(x, A, perm, seg_slot, seg_off, n_seg, scale, vpart, T, d_in, r,
                             n_slots, ksplit, dt, err, st, pdl);
 }
@@ -401,15 +414,19 @@ namespace lora {
 
 // Segments, then the segment-grouped shrink (SGMV) into w.vpart: the first
 // two kernels of the prefill path (the GEMM follows as their dependent).
+// *v_parts gets the number of partials the GEMM sums: 1 where the
+// tensor-core shrink folds its splits (the segment build zeroes its
+// counters), w.ksplit otherwise.
 cudaError_t prefill_adapter_shrink(const void* x, const void* A_pool, const int32_t* slot_ids,
                                    const float* scale, int32_t T, int32_t d_in, int32_t r,
                                    int32_t n_slots, lora_dtype_t dt, const FusedWs& w,
-                                   cudaStream_t st, const DeviceInfo& dev) {
+                                   cudaStream_t st, const DeviceInfo& dev, int* v_parts) {
+  int32_t* fold = w.ksplit > 1 ? w.fold : nullptr;
   cudaError_t e = launch_build_segments(slot_ids, T, n_slots, w.perm, w.seg_slot, w.seg_off,
-                                        w.n_seg, w.err, st);
+                                        w.n_seg, w.err, st, fold, w.n_fold);
   if (e != cudaSuccess) return e;
   return sgmv_shrink_any(x, A_pool, w.perm, w.seg_slot, w.seg_off, w.n_seg, scale, w.vpart, T,
-                         d_in, r, n_slots, w.ksplit, dt, w.err, st, true, dev);
+                         d_in, r, n_slots, w.ksplit, dt, w.err, st, true, dev, fold, v_parts);
 }
 
 lora_status_t linear_fused_impl(const void* x, const void* W0, const void* A_pool,
@@ -452,21 +469,23 @@ lora_status_t linear_fused_impl(const void* x, const void* W0, const void* A_poo
     return from_cuda(launch_bgmv_adapter_merge(x, A_pool, B_pool, slot_ids, scale, w.partial, S,
                                                y, T, d_in, d_out, r, n_slots, w.err, true, st));
   }
+  int v_parts = w.ksplit;
   if (decode) {
     // decode-sized fp32 batch: per-token BGMV shrink, then the CUDA-core layer
     e = launch_bgmv_shrink(x, A_pool, slot_ids, scale, w.vpart, T, d_in, r, n_slots, w.ksplit,
                            dt, w.err, st);
   } else {
     // prefill-sized batch: segments, then the segment-grouped shrink (SGMV)
-    e = prefill_adapter_shrink(x, A_pool, slot_ids, scale, T, d_in, r, n_slots, dt, w, st, dev);
+    e = prefill_adapter_shrink(x, A_pool, slot_ids, scale, T, d_in, r, n_slots, dt, w, st, dev,
+                               &v_parts);
   }
   if (e != cudaSuccess) return LORA_ERR_CUDA;
   if (dt == LORA_DTYPE_BF16)
-    e = launch_fused_tc(x, W0, B_pool, slot_ids, w.vpart, w.ksplit, y, T, d_in, d_out, r, n_slots,
+    e = launch_fused_tc(x, W0, B_pool, slot_ids, w.vpart, v_parts, y, T, d_in, d_out, r, n_slots,
                         w.err, st, dev);
   else
     e = launch_fused_f32(static_cast<const float*>(x), static_cast<const float*>(W0),
-                         static_cast<const float*>(B_pool), slot_ids, w.vpart, w.ksplit,
+                         static_cast<const float*>(B_pool), slot_ids, w.vpart, v_parts,
                          static_cast<float*>(y), T, d_in, d_out, r, n_slots, w.err, st);
   return from_cuda(e);
 }
@@ -611,11 +630,12 @@ lora_status_t lora_linear_fused_ragged(const void* x, const void* W0, const void
                                 rw.A_c, rw.B_c, rw.scale_c, d_in, d_out, wp.err, st);
     if (e == cudaSuccess)
       e = launch_ragged_remap(slot_ids, wp.seg_slot, wp.n_seg, rw.ids_c, T, n_slots, wp.err, st);
+    int v_parts = wp.ksplit;
     if (e == cudaSuccess)
       e = prefill_adapter_shrink(x, rw.A_c, rw.ids_c, rw.scale_c, T, d_in, r_max, rw.n_c,
-                                 LORA_DTYPE_BF16, wp, st, dev);
+                                 LORA_DTYPE_BF16, wp, st, dev, &v_parts);
     if (e == cudaSuccess)
-      e = launch_fused_tc(x, W0, rw.B_c, rw.ids_c, wp.vpart, wp.ksplit, y, T, d_in, d_out, r_max,
+      e = launch_fused_tc(x, W0, rw.B_c, rw.ids_c, wp.vpart, v_parts, y, T, d_in, d_out, r_max,
                           rw.n_c, wp.err, st, dev);
     return from_cuda(e);
   }
@@ -711,10 +731,11 @@ lora_status_t lora_linear_fused_4bit(const void* x, const void* W0q, const void*
   // prefill path over it, so W0 is streamed once, not once per 256 tokens
   e = launch_dequantize_q4(W0q, absmax, codebook, wd, d_in, d_out, st);
   if (e != cudaSuccess) return LORA_ERR_CUDA;
+  int v_parts = w.ksplit;
   e = prefill_adapter_shrink(x, A_pool, slot_ids, scale, T, d_in, r, n_slots, LORA_DTYPE_BF16, w,
-                             st, dev);
+                             st, dev, &v_parts);
   if (e != cudaSuccess) return LORA_ERR_CUDA;
-  return from_cuda(launch_fused_tc(x, wd, B_pool, slot_ids, w.vpart, w.ksplit, y, T, d_in, d_out,
+  return from_cuda(launch_fused_tc(x, wd, B_pool, slot_ids, w.vpart, v_parts, y, T, d_in, d_out,
                                    r, n_slots, w.err, st, dev));
 }
 

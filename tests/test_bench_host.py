@@ -45,15 +45,17 @@ def _ksplit_cases():
 
 def test_fused_ksplit_matches_library():
     """bench.py sizes its buffers with a mirror of the library's shrink-split
-    rule (including split 1 where the 256 x 256 prefill tiles run); the
-    workspace size the library reports pins the mirror on fixed and drawn
-    shapes."""
+    rule (the folded tensor-core split at rank 64 / 128, split 1 where the
+    256 x 256 prefill tiles run); the workspace size the library reports pins
+    the mirror on fixed and drawn shapes."""
     from lora_serving_device_gb300 import build, lora as L
     build.build()
     for T, d_in, d_out, n_slots, r in _ksplit_cases():
-        ks = bench.fused_ksplit(T, d_in, d_out, n_slots)
+        ks = bench.fused_ksplit(T, d_in, d_out, n_slots, r)
         cap = min(T, n_slots)
         head = 16 + T * 4 + cap * 4 + (cap + 1) * 4 + 4
+        if T > 256:                        # the shrink's fold counters
+            head += (-(-T // 128) + cap) * 4
         head = -(-head // 256) * 256
         body = -(-(head + ks * T * r * 4) // 256) * 256
         if T <= 256:                       # decode-sized: split-K fp32 base product

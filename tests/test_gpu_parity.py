@@ -479,6 +479,37 @@ def test_prefill_many_tiles(L, T, d_in, d_out, r, runs):
         del d, y, ws
 
 
+# prefill batches at rank 64 / 128: the tensor-core shrink folds its d_in
+# splits into one partial; d_in 520 at split 4 leaves the last split empty,
+# d_in 264 runs at split 2
+FOLD_CASES = [(300, 520, 264, 64), (1100, 1032, 1032, 128), (700, 264, 520, 64)]
+
+
+@pytest.mark.parametrize("T,d_in,d_out,r", FOLD_CASES, ids=[str(c) for c in FOLD_CASES])
+def test_prefill_shrink_fold(L, T, d_in, d_out, r):
+    """The CTA of each shrink item that finishes last sums the splits in
+    split order, counted on words of the workspace that the segment build
+    zeroes: a workspace that starts as 0xFF bytes (error word aside) must
+    give the oracle's result, and a second call the same bits."""
+    torch = torch_mod()
+    w = W.random_case(1300 + T, T, d_in, d_out, r, 24, runs=True)
+    w.slot_ids[40:90] = -1
+    ws = L.workspace(L.OP_LINEAR_FUSED, T, d_in, d_out, r, w.n_slots)
+    ws.fill_(255)
+    ws[:16] = 0
+    for W0_zero in (False, True):
+        d = DeviceCase(w, W0_zero=W0_zero)
+        y1, _ = d.fused(ws=ws)
+        y2, _ = d.fused(ws=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(y1, y2)
+        W0 = np.zeros_like(w.W0) if W0_zero else w.W0
+        ref = O.lora_linear(w.x, W0, w.A_pool, w.B_pool, w.scale, w.slot_ids)
+        check_close_bf16_out(host(y1), ref, f"folded shrink, W0 zero={W0_zero}")
+        assert L.get_error_t(ws) == 0
+        del d, y1, y2
+
+
 @pytest.mark.parametrize("T,k", W.SWEEP_POINTS)
 def test_diversity_sweep_point(L, T, k):
     torch = torch_mod()
