@@ -221,14 +221,23 @@ def test_sgmv_expand_run_and_tail_items(L, d_out, r):
     assert L.get_error_t(ws) == 0
 
 
-# SGMV shrink on the same layouts: a segment's last chunk mixes a run with
-# scattered rows (gathered), its other chunks are consecutive rows (TMA); the
-# shrink numbers every last chunk first
-@pytest.mark.parametrize("d_in,r", [(520, 64), (1032, 128)])
-def test_sgmv_shrink_run_and_tail_items(L, d_in, r):
+# SGMV shrink on the same layouts and on more runs with a few scattered rows
+# after them (a segment's last chunk mixes a run with scattered rows and is
+# gathered; its other chunks are consecutive rows, moved by TMA); the shrink
+# numbers every last chunk first; d_in with and without a ragged last K-block
+SHRINK_RUN_TAIL_LAYOUTS = [RUN_TAIL_LAYOUT,
+                           [(0, 0, 100, 20), (1, 130, 16, 112), (2, 300, 127, 1),
+                            (3, 450, 60, 0)],
+                           [(0, 0, 150, 3), (1, 200, 16, 14), (2, 300, 112, 2),
+                            (3, 450, 50, 5)]]
+
+
+@pytest.mark.parametrize("layout", [0, 1, 2])
+@pytest.mark.parametrize("d_in,r", [(520, 64), (1032, 128), (1024, 64), (512, 128)])
+def test_sgmv_shrink_run_and_tail_items(L, d_in, r, layout):
     torch = torch_mod()
     T, n_slots = 700, 4
-    ids = _run_tail_ids(T, RUN_TAIL_LAYOUT, d_in)
+    ids = _run_tail_ids(T, SHRINK_RUN_TAIL_LAYOUTS[layout], d_in)
     rng = np.random.default_rng([7007, d_in])
     A = W.bf16_round((rng.standard_normal((n_slots, d_in, r)) / np.sqrt(d_in)).astype(np.float32))
     x = W.bf16_round(rng.standard_normal((T, d_in)).astype(np.float32))
