@@ -221,13 +221,12 @@ def test_sgmv_expand_run_and_tail_items(L, d_out, r):
     assert L.get_error_t(ws) == 0
 
 
-# SGMV shrink on the same layouts and on more runs with a few scattered rows
-# after them: a segment's last chunk that mixes a run of 32 rows or more with
-# later rows is split into the run (TMA) and the rest (gathered): 40 + 17,
-# 100 + 1, 100 + 20, 127 + 1, 62 + 3 (a 193-token segment), 112 + 2, 50 + 5;
-# shorter runs are gathered whole (22 + 16, 15 + 3, 17 + 111, 16 + 14); the
-# other chunks are consecutive rows (TMA); d_in with and without a ragged
-# last K-block
+# SGMV shrink on the same layouts and on more runs with scattered rows after
+# them (a segment's last chunk mixes a run with later rows and is gathered:
+# 22 + 16, 40 + 17, 15 + 3, 100 + 1, 100 + 20, 17 + 111, 127 + 1, 62 + 3 in a
+# 193-token segment, 16 + 14, 112 + 2, 50 + 5; the other chunks are
+# consecutive rows, moved by TMA); the shrink numbers every last chunk first;
+# d_in with and without a ragged last K-block
 SHRINK_RUN_TAIL_LAYOUTS = [RUN_TAIL_LAYOUT,
                            [(0, 0, 100, 20), (1, 130, 16, 112), (2, 300, 127, 1),
                             (3, 450, 60, 0)],
