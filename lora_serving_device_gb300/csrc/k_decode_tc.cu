@@ -150,9 +150,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // x of the ring's first stages into L2 before the wait (the blocks the
     // loads right after it fetch): a prefetch moves no data into this SM,
     // and those loads read what the predecessor wrote.  One CTA in eight
-    // column tiles of a split issues it.
+    // column tiles of a split issues it.  A short K range (at most two
+    // rings' worth) has the x of all its stages prefetched; on longer ones
+    // the prefetches would queue ahead of the ring's own loads.
     if (lane == 0 && !p.hold_producer && blockIdx.x % 8 == 0) {
-      for (int it = 0; it < pre; ++it) {
+      const int n_pf = n_it <= 2 * p.stages ? n_it : pre;
+      for (int it = 0; it < n_pf; ++it) {
         const int k0 = (kb0 + it) * 64 * KSUB;
 #pragma unroll
         for (int j = 0; j < KSUB; ++j)
