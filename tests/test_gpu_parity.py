@@ -518,6 +518,25 @@ def test_prefill_shrink_fold(L, T, d_in, d_out, r):
         ref = O.lora_linear(w.x, W0, w.A_pool, w.B_pool, w.scale, w.slot_ids)
         check_close_bf16_out(host(y1), ref, f"folded shrink, W0 zero={W0_zero}")
         assert L.get_error_t(ws) == 0
+        if not W0_zero:
+            # replays of a captured call: the counters are zeroed by the
+            # captured segment build on every replay
+            y3 = torch.empty_like(y1)
+            g = torch.cuda.CUDAGraph()
+            st = torch.cuda.Stream()
+            st.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(st):
+                d.fused(ws=ws, y=y3)
+                with torch.cuda.graph(g, stream=st):
+                    d.fused(ws=ws, y=y3)
+            torch.cuda.current_stream().wait_stream(st)
+            for _ in range(2):
+                y3.zero_()
+                g.replay()
+                torch.cuda.synchronize()
+                assert torch.equal(y1, y3)
+            assert L.get_error_t(ws) == 0
+            del g, y3
         del d, y1, y2
 
 
