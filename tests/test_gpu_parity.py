@@ -540,6 +540,41 @@ def test_prefill_shrink_fold(L, T, d_in, d_out, r):
         del d, y1, y2
 
 
+# the folded shrink at the edges of the prefill path: one token above the
+# decode sizes, one adapter for every token (16 chunks of one segment, split
+# 4), ids outside the pool (flagged, base-only), and a batch with no adapter
+# at all (no work item; the GEMM alone)
+FOLD_EDGE_CASES = [("T=257", 257, 512, 264, 64, 3, 0, False),
+                   ("one adapter", 2000, 1024, 520, 128, 1, 0, False),
+                   ("invalid ids", 600, 512, 1032, 64, 12, 9, False),
+                   ("all base-only", 300, 512, 264, 64, 4, 0, True)]
+
+
+@pytest.mark.parametrize("name,T,d_in,d_out,r,n_slots,invalid,all_base", FOLD_EDGE_CASES,
+                         ids=[c[0] for c in FOLD_EDGE_CASES])
+def test_prefill_fold_edge_cases(L, name, T, d_in, d_out, r, n_slots, invalid, all_base):
+    torch = torch_mod()
+    w = W.random_case(1400 + T, T, d_in, d_out, r, n_slots, base_frac=0.0 if n_slots == 1 else 0.15,
+                      runs=n_slots > 1, invalid=invalid)
+    if all_base:
+        w.slot_ids[:] = -1
+    for W0_zero in (False, True):
+        d = DeviceCase(w, W0_zero=W0_zero)
+        y, ws = d.fused()
+        torch.cuda.synchronize()
+        W0 = np.zeros_like(w.W0) if W0_zero else w.W0
+        ref = O.lora_linear(w.x, W0, w.A_pool, w.B_pool, w.scale, w.slot_ids)
+        if all_base and W0_zero:
+            np.testing.assert_array_equal(host(y), 0.0)
+        elif W0_zero:
+            check_close_bf16_out(host(y), ref, f"{name} delta")
+        else:
+            check_close(host(y), ref, f"{name} y")
+        err = L.get_error_t(ws)
+        assert (err & L.DEVERR_BAD_SLOT) if invalid else err == 0
+        del d, y, ws
+
+
 @pytest.mark.parametrize("T,k", W.SWEEP_POINTS)
 def test_diversity_sweep_point(L, T, k):
     torch = torch_mod()
