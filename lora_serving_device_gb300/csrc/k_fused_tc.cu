@@ -1558,7 +1558,36 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       }
       // ---- the previous tile's accumulators: the MMA issuer waits for them
       if (k > 0) drain(k - 1, prev_n0, prev_t0);
-      // ---- this tile's LoRA stages
+      // ---- this tile's LoRA stages.  This thread's units are those of its
+      // token's adapter tv (units tv * upa .. tv * upa + upa - 1).  Its v
+      // values for the next stage that holds one of them are loaded ahead
+      // (f): the first at the tile's start, each next one as soon as the
+      // last is written.
+      const int tv = tok[rr];
+      const float* vrow = p.vpart + static_cast<size_t>(t0 + rr) * p.r;
+      // chunk cq of stage g: this thread's rank offset in v, or -1
+      auto chunk_q0 = [&](int g, int cq) {
+        const int kq = cq << 3;
+        const int wu = kq >> p.lg_box;
+        const int w = g * G + wu;
+        return (tv >= 0 && wu < min(G, U - g * G) && (w >> p.lg_upa) == tv)
+                   ? ((w & (upa - 1)) << p.lg_box) + (kq & (p.box_rows - 1))
+                   : -1;
+      };
+      float f[4][8];
+      int next_part = 0, next_g = -1;  // the stage f is loaded for
+      auto load_next = [&]() {
+        next_g = -1;
+        if (tv < 0 || next_part >= upa) return;
+        next_g = (tv * upa + next_part) / G;
+        ++next_part;
+#pragma unroll
+        for (int cq = 0; cq < 4; ++cq) {
+          const int q0 = chunk_q0(next_g, cq);
+          if (q0 >= 0) load8_dep(vrow + q0, f[cq]);
+        }
+      };
+      load_next();
       for (int g2 = 0; g2 < my_groups; ++g2, ++g_run) {
         if (etid == 0) {
           const uint64_t tw = ptx::globaltimer_ns();
@@ -1577,46 +1606,22 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           uint8_t* X = smem + static_cast<size_t>(st) * L.stage_bytes;
           uint8_t* Wr = X + L.w_off;
           uint8_t* Xh = X + c * L.x_sub;  // this thread's V half
-          const int u_first = g2 * G;
-          const int n_units = min(G, U - u_first);
-          const int tv = tok[rr];
-          const size_t row = static_cast<size_t>(t0 + rr) * p.r;
-          const size_t split = static_cast<size_t>(p.T) * p.r;
-          int q0[4];
-          float f[4][8];
+          const int n_units = min(G, U - g2 * G);
+          const bool mine = g2 == next_g;
 #pragma unroll
           for (int cq = 0; cq < 4; ++cq) {
-            const int kq = cq << 3;
-            const int wu = kq >> p.lg_box;
-            const int w = u_first + wu;
-            q0[cq] = (wu < n_units && tv >= 0 && (w >> p.lg_upa) == tv)
-                         ? ((w & (upa - 1)) << p.lg_box) + (kq & (p.box_rows - 1))
-                         : -1;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) f[cq][e] = 0.f;
-          }
-          for (int s0 = 0; s0 < p.v_ksplit; ++s0) {
-            float g[4][8];
-#pragma unroll
-            for (int cq = 0; cq < 4; ++cq)
-              if (q0[cq] >= 0) load8_dep(p.vpart + s0 * split + row + q0[cq], g[cq]);
-#pragma unroll
-            for (int cq = 0; cq < 4; ++cq)
-              if (q0[cq] >= 0)
-#pragma unroll
-                for (int e = 0; e < 8; ++e) f[cq][e] += g[cq][e];
-          }
-#pragma unroll
-          for (int cq = 0; cq < 4; ++cq) {
+            const bool use = mine && chunk_q0(g2, cq) >= 0;
             float hh[8], ll[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-              hh[e] = __bfloat162float(__float2bfloat16_rn(f[cq][e]));
-              ll[e] = f[cq][e] - hh[e];
+              const float v = use ? f[cq][e] : 0.f;
+              hh[e] = __bfloat162float(__float2bfloat16_rn(v));
+              ll[e] = v - hh[e];
             }
             *reinterpret_cast<uint4*>(Xh + i * 128 + ((cq ^ (i & 7)) << 4)) = pack8_bf16(hh);
             *reinterpret_cast<uint4*>(Xh + i * 128 + (((cq + 4) ^ (i & 7)) << 4)) = pack8_bf16(ll);
           }
+          if (mine) load_next();
           const int used = n_units << p.lg_box;
           if (used < kBK / 2) {
             const int per_half = (kBK / 2 - used) * 8;
@@ -1777,6 +1782,7 @@ cudaError_t launch_persistent(const void* x, const void* W0, const void* B, TcPa
 cudaError_t launch_wide(const void* x, const void* W0, const void* B, TcParams prm,
                        int tiles_n, cudaStream_t st, const DeviceInfo& dev) {
   if (prm.n_slots > 32767) return cudaErrorInvalidConfiguration;  // int16 slot lists
+  if (prm.v_ksplit != 1) return cudaErrorInvalidConfiguration;    // one v partial
   int stages = 0;
   for (int s = 4; s >= 2; --s) {
     if (wide_layout(s, prm.n_slots).total + 1024 <= dev.max_smem_optin) {
