@@ -1225,14 +1225,38 @@ __global__ void __launch_bounds__(kWideThreads, 1)
   volatile int* vt_seq = reinterpret_cast<volatile int*>(tile_groups + 8);  // tiles published
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int first_tile = static_cast<int>(blockIdx.x), tile_step = static_cast<int>(gridDim.x);
+  // Tile order.  CTA b takes positions b, b + gridDim.x, ...; the first
+  // `extra` CTAs also take one of the last, partial round.  A tile row far
+  // heavier in LoRA stages than the others (many adapter runs, as where a
+  // mixed batch's decode tokens sit) is placed at positions [extra, extra +
+  // tiles_n), on CTAs without a tile in that last round; every other tile
+  // keeps the panel order (kPanel column tiles per panel).
+  int heavy = -1;
   auto tile_origin = [&](int lin, int* n0, int* t0) {
+    if (heavy >= 0) {
+      const int extra = pp.n_tiles % tile_step;
+      if (lin >= extra && lin < extra + pp.tiles_n) {
+        *n0 = (lin - extra) * 256;
+        *t0 = heavy * 256;
+        return;
+      }
+      const int j = lin < extra ? lin : lin - pp.tiles_n;  // among the other rows' tiles
+      const int rows = pp.tiles_tp - 1;
+      const int g = j / (kPanel * rows);
+      const int gn = min(kPanel, pp.tiles_n - g * kPanel);
+      const int rem = j - g * kPanel * rows;
+      const int row = rem / gn;
+      *n0 = (g * kPanel + rem % gn) * 256;
+      *t0 = (row < heavy ? row : row + 1) * 256;
+      return;
+    }
     const int g = lin / (kPanel * pp.tiles_tp);
     const int gn = min(kPanel, pp.tiles_n - g * kPanel);
     const int rem = lin - g * kPanel * pp.tiles_tp;
     *n0 = (g * kPanel + rem % gn) * 256;
     *t0 = (rem / gn) * 256;
   };
-  const int first_tile = static_cast<int>(blockIdx.x), tile_step = static_cast<int>(gridDim.x);
 
   if (warp == 0) {
     if (lane == 0) {
@@ -1265,6 +1289,41 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       named_sync(3, kWideThreads - 32);
     }
     ptx::tc_fence_after();
+  }
+  {
+    // adapter runs per tile row, counted by the whole CTA in the store boxes
+    // (unused until the first drain); ids were written before the kernel
+    // ahead of this one started, so they are read before its wait
+    int* row_runs = reinterpret_cast<int*>(smem + L.ybox);
+    volatile int* heavy_s = reinterpret_cast<volatile int*>(smem + L.misc + 152);
+    for (int i = tid; i < pp.tiles_tp; i += kWideThreads) row_runs[i] = 0;
+    __syncthreads();
+#pragma unroll 8
+    for (int t = tid; t < p.T; t += kWideThreads) {
+      const int id = p.ids[t];
+      const int prev = (t & 255) ? p.ids[t - 1] : -1;
+      if (slot_valid(id, p.n_slots) && id != prev) atomicAdd(&row_runs[t >> 8], 1);
+    }
+    __syncthreads();
+    if (tid == 0) {
+      int best = -1, most = 0, total = 0;
+      for (int i = 0; i < pp.tiles_tp; ++i) {
+        total += row_runs[i];
+        if (row_runs[i] > most) {
+          most = row_runs[i];
+          best = i;
+        }
+      }
+      // at least 8 runs and four times the other rows' average, and room
+      // for its tiles beside the CTAs of the last round
+      const int extra = pp.n_tiles % tile_step;
+      const bool move = best >= 0 && pp.tiles_tp > 1 && pp.n_tiles > tile_step &&
+                        extra + pp.tiles_n <= tile_step && most >= 8 &&
+                        most * (pp.tiles_tp - 1) >= 4 * (total - most);
+      *heavy_s = move ? best : -1;
+    }
+    __syncthreads();
+    heavy = *heavy_s;
   }
   const uint32_t tmem = warp == 0 ? 0u : *tmem_slot;
   const int upa = p.r >> p.lg_box;

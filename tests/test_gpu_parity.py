@@ -575,6 +575,29 @@ def test_prefill_fold_edge_cases(L, name, T, d_in, d_out, r, n_slots, invalid, a
         del d, y, ws
 
 
+# the prefill GEMM's 256 x 256 tiles with one tile row far heavier in LoRA
+# stages (40 one-token adapters at the batch's end, after long runs): the
+# kernel moves that row's tiles to CTAs without a tile in the walk's last,
+# partial round.  T 1100 over 76 column tiles: 380 tiles, 76 in the last
+# round; T 1024: 304 tiles, none
+@pytest.mark.parametrize("T", [1100, 1024])
+def test_prefill_heavy_tile_row(L, T):
+    torch = torch_mod()
+    d_in, d_out, r, n_slots = 136, 256 * 76, 64, 48
+    w = W.random_case(1500 + T, T, d_in, d_out, r, n_slots, base_frac=0.0)
+    ids = np.repeat(np.arange(5, dtype=np.int32), -(-(T - 40) // 5))[:T - 40]
+    w.slot_ids[:] = np.concatenate([ids, np.arange(8, 48, dtype=np.int32)])
+    for W0_zero in (False, True):
+        d = DeviceCase(w, W0_zero=W0_zero)
+        y, ws = d.fused()
+        torch.cuda.synchronize()
+        W0 = np.zeros_like(w.W0) if W0_zero else w.W0
+        ref = O.lora_linear(w.x, W0, w.A_pool, w.B_pool, w.scale, w.slot_ids)
+        check_close_bf16_out(host(y), ref, f"heavy row {'delta' if W0_zero else 'y'} T={T}")
+        assert L.get_error_t(ws) == 0
+        del d, y, ws
+
+
 @pytest.mark.parametrize("T,k", W.SWEEP_POINTS)
 def test_diversity_sweep_point(L, T, k):
     torch = torch_mod()
